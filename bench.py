@@ -1,0 +1,481 @@
+#!/usr/bin/env python3
+"""Throughput of the multi-tenant LoRA delta on one GB300 (per GPU replica).
+
+One step = one pass of the hot path over one batch: device metadata build
+(stable sort of tokens by adapter) + the fused shrink/expand of every packed
+slice (dense workloads), or metadata + MoE w13 + MoE w2 (MoE workloads).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl gb300|reference]
+
+Prints one JSON line.  Under torchrun every rank runs its own replica on its
+own GPU (the path shards by token with no exchange step: "replicas only"),
+the timed region is bracketed by a barrier and a device synchronise, and the
+time is the maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from heterogeneous_adapters_lora_gb300 import inputs as gen  # noqa: E402
+
+WORKLOADS = {
+    "decode_qkv": "decode BGMV, Llama-3-8B packed QKV: T=256 (1 token/request), H=4096 -> 4096/1024/1024, "
+                  "32 adapters rank 16, idx uniform over 32 + 10% -1, scale 2",
+    "tiny": "single 512 -> 512 projection, T=64, 4 adapters rank 8, idx over {-1,0..3}, scale 2",
+    "prefill_gate_up": "prefill SGMV gate_up: 8 requests, lengths U[128,2048] contiguous, H=4096 -> 2x14336, "
+                       "8 adapters rank 64, request i -> adapter i",
+    "many_adapter_down": "many-adapter decode down_proj 14336 -> 4096, T=2048, 1024 adapters ranks {8,16,32,64} "
+                         "padded to 64, Zipf(1.2) popularity",
+    "moe": "MoE-LoRA: E=64, top-8 of softmax(N(0,1)), D=2048, F=1408, 8 adapters rank 16, T=1024, "
+           "w13 (gate+up) and w2",
+    "moe_shared": "MoE-LoRA as 'moe' in the shared-outer layout (w13-A and w2-B expert dim 1)",
+}
+
+
+def make_case(name):
+    if name == "decode_qkv":
+        return gen.decode_qkv()
+    if name == "tiny":
+        return gen.tiny()
+    if name == "prefill_gate_up":
+        return gen.prefill_gate_up()
+    if name == "many_adapter_down":
+        return gen.many_adapter_down()
+    if name == "moe":
+        return gen.moe()
+    if name == "moe_shared":
+        return gen.moe(shared_outer=True)
+    raise ValueError(name)
+
+
+def is_moe(name):
+    return name.startswith("moe")
+
+
+# ----------------------------------------------------------------- algorithmic bytes
+
+def dense_algorithmic_bytes(c):
+    """Bytes of x, A, B and y the delta must touch: x rows and y rows (read +
+    write) of active tokens, A and B of each distinct active slot at its true
+    rank, plus the idx vector the metadata reads."""
+    act = np.array([0 <= a < c.L and c.enabled[a] and c.ranks[a] > 0 for a in c.idx], bool)
+    n = int(act.sum())
+    slots = np.unique(c.idx[act])
+    r = c.ranks[slots].astype(np.int64)
+    A = int(r.sum()) * c.H * 2 * c.n_slices
+    B = int(r.sum()) * c.out_total * 2
+    return dict(x=n * c.H * 2, A=A, B=B, y=2 * n * c.out_total * 2, idx=c.T * 4,
+                total=n * c.H * 2 + A + B + 2 * n * c.out_total * 2 + c.T * 4, active=n)
+
+
+def moe_algorithmic_bytes(c):
+    t = np.repeat(np.arange(c.T), c.K)
+    a = c.idx[t]
+    e = c.topk_ids.reshape(-1)
+    act = (a >= 0) & (a < c.L)
+    act[act] &= (c.enabled[a[act]] != 0) & (c.ranks[a[act]] > 0)
+    n_pairs = int(act.sum())
+    tokens = np.unique(t[act])
+    keys = np.unique(a[act] * c.E + e[act])
+    slots = np.unique(a[act])
+    r_key = c.ranks[keys // c.E].astype(np.int64)
+    r_slot = c.ranks[slots].astype(np.int64)
+    ea = r_slot.sum() if c.shared_outer else r_key.sum()
+    w13 = (len(tokens) * c.D * 2 + c.n13 * ea * c.D * 2 + c.n13 * r_key.sum() * c.F13 * 2
+           + 2 * n_pairs * c.n13 * c.F13 * 2)
+    eb = r_slot.sum() if c.shared_outer else r_key.sum()
+    w2 = (n_pairs * c.F * 2 + r_key.sum() * c.F * 2 + eb * c.D * 2 + 2 * n_pairs * c.D * 2 + n_pairs * 4)
+    meta = c.T * 4 + c.T * c.K * 4
+    return dict(w13=int(w13), w2=int(w2), meta=meta, total=int(w13 + w2 + meta), active=len(tokens),
+                pairs=n_pairs)
+
+
+# ----------------------------------------------------------------- clocks
+
+CLOCK_Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+           "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+           "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={CLOCK_Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- reference arm (oracle on CPU)
+
+def oracle_step_fn(name, c):
+    import oracle
+    if is_moe(name):
+        def step():
+            oracle.moe_meta(c.topk_ids, c.idx, c.L, c.E, c.enabled, c.ranks)
+            oracle.moe_w13(c)
+            oracle.moe_w2(c)
+        return step, c.T
+    if name == "many_adapter_down":
+        # bounded sample: the first 256 tokens (the oracle is per-token)
+        n = 256
+        sub = dict(x=c.x[:n], idx=c.idx[:n], y_in=c.y0[:n])
+
+        def step():
+            oracle.dense_meta(sub["idx"], c.L, c.enabled, c.ranks)
+            oracle.dense_delta(c, **sub)
+        return step, n
+    if name == "prefill_gate_up":
+        n = 512
+        sub = dict(x=c.x[:n], idx=c.idx[:n], y_in=c.y0[:n])
+
+        def step():
+            oracle.dense_meta(sub["idx"], c.L, c.enabled, c.ranks)
+            oracle.dense_delta(c, **sub)
+        return step, n
+
+    def step():
+        oracle.dense_meta(c.idx, c.L, c.enabled, c.ranks)
+        oracle.dense_delta(c)
+    return step, c.T
+
+
+def cpu_sample_desc(name, c, tokens):
+    if tokens == c.T:
+        return f"the full batch ({c.T} tokens) per call"
+    return f"the first {tokens} of {c.T} tokens per call (the oracle is per-token)"
+
+
+def time_oracle(name, c, min_seconds=2.0, max_calls=1000):
+    import oracle
+    step, tokens = oracle_step_fn(name, c)
+    step()  # build + warm
+    n, t0 = 0, time.perf_counter()
+    while True:
+        step()
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds or n >= max_calls:
+            break
+    return dict(value=tokens * n / el, unit="tokens/s", cores=oracle.max_threads(), kind="oracle",
+                sample=f"{n} oracle calls on {cpu_sample_desc(name, c, tokens)} of {name}")
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    c = make_case(args.workload)
+    import oracle
+    step, tokens = oracle_step_fn(args.workload, c)
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    value = tokens * args.steps / el
+    line = {"impl": "reference", "metric": "LoRA-delta tokens/s", "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": f"{args.workload}: {WORKLOADS[args.workload]}",
+                       "sample": cpu_sample_desc(args.workload, c, tokens)},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.max_threads(),
+                             "kind": "oracle", "sample": cpu_sample_desc(args.workload, c, tokens)},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------- GPU arm
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "heterogeneous_adapters_lora_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        if fn.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, fn), "rb") as f:
+                h.update(fn.encode())
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload, kernel):
+    """dram bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = rec.get(workload, {}).get(kernel)
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except (OSError, ValueError, KeyError):
+        return 6800.0, "fallback"
+
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    from heterogeneous_adapters_lora_gb300 import harness as Hn
+    from heterogeneous_adapters_lora_gb300 import lora as L
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    L.lib()
+    name = args.workload
+    c = make_case(name)
+    moe = is_moe(name)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    ab = moe_algorithmic_bytes(c) if moe else dense_algorithmic_bytes(c)
+    foot = ab["total"]
+    n_rot = max(1, math.ceil(2 * l2 / max(foot, 1)))
+    n_rot = min(n_rot, args.max_copies)
+
+    runs = []
+    for _ in range(n_rot):
+        runs.append(Hn.MoERun(c, device=dev) if moe else Hn.DenseRun(c, device=dev))
+    torch.cuda.synchronize(dev)
+
+    def step(r):
+        r.step()
+
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for r in runs:           # warm-up outside the graph (also resets state)
+            for _ in range(max(1, args.warmup)):
+                step(r)
+        stream.synchronize()
+        graphs = []
+        for r in runs:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step(r)
+            graphs.append(g)
+        for i in range(args.warmup):
+            graphs[i % n_rot].replay()
+        stream.synchronize()
+
+        # clocks: ~1 s of the same work right before the timed region, and during it
+        with ClockSampler(local_rank) as cs:
+            t_end = time.perf_counter() + args.clock_seconds
+            i = 0
+            while time.perf_counter() < t_end:
+                for _ in range(200):
+                    graphs[i % n_rot].replay()
+                    i += 1
+                stream.synchronize()
+            if world > 1:
+                dist.barrier()
+            torch.cuda.synchronize(dev)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for k in range(args.steps):
+                graphs[k % n_rot].replay()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            if world > 1:
+                dist.barrier()
+        ms = e0.elapsed_time(e1)
+
+        # the dominant kernel alone: one launch at a time between events, same rotation
+        kname = "moe" if moe else "apply"
+        kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.kernel_launches)]
+        for k, (a0, a1) in enumerate(kev):
+            r = runs[k % n_rot]
+            r.build_meta()
+            a0.record(stream)
+            if moe:
+                r.w13()
+                r.w2()
+            else:
+                r.apply()
+            a1.record(stream)
+        stream.synchronize()
+        kms = statistics.mean(a0.elapsed_time(a1) for a0, a1 in kev)
+
+        # end to end through the public API with host buffers: H2D of the
+        # step's inputs from pinned memory, the calls, D2H of the result
+        r = runs[0]
+        if moe:
+            h_in = [torch.from_numpy(np.ascontiguousarray(c.x).view(np.int16)).pin_memory(),
+                    torch.from_numpy(np.ascontiguousarray(c.ic2).view(np.int16)).pin_memory(),
+                    torch.from_numpy(c.idx).pin_memory(),
+                    torch.from_numpy(np.ascontiguousarray(c.topk_ids)).pin_memory(),
+                    torch.from_numpy(np.ascontiguousarray(c.topk_w).reshape(-1)).pin_memory(),
+                    torch.from_numpy(c.ic1_0.view(np.int16)).pin_memory(),
+                    torch.from_numpy(c.ic3_0.view(np.int16)).pin_memory()]
+            d_in = [r.x, r.ic2, r.idx, r.topk, r.topk_w, r.ic1, r.ic3]
+            h_out = [torch.empty_like(r.ic1, device="cpu").pin_memory(),
+                     torch.empty_like(r.ic3, device="cpu").pin_memory()]
+            d_out = [r.ic1, r.ic3]
+        else:
+            h_in = [torch.from_numpy(np.ascontiguousarray(c.x).view(np.int16)).pin_memory(),
+                    torch.from_numpy(c.idx).pin_memory(),
+                    torch.from_numpy(c.y0.view(np.int16)).pin_memory()]
+            d_in = [r.x, r.idx, r.y]
+            h_out = [torch.empty_like(r.y, device="cpu").pin_memory()]
+            d_out = [r.y]
+        bi = sum(t.numel() * t.element_size() for t in h_in)
+        bo = sum(t.numel() * t.element_size() for t in h_out)
+
+        def e2e_step():
+            for h, d in zip(h_in, d_in):
+                d.copy_(h, non_blocking=True)
+            step(r)
+            for h, d in zip(h_out, d_out):
+                h.copy_(d, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        stream.synchronize()
+        if world > 1:
+            dist.barrier()
+        f0 = torch.cuda.Event(enable_timing=True)
+        f1 = torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        f1.record(stream)
+        stream.synchronize()
+        e2e_ms = f0.elapsed_time(f1)
+
+    if world > 1:
+        t = torch.tensor([ms, e2e_ms, kms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, e2e_ms, kms = t.tolist()
+    for r in runs:
+        r.close()
+    if rank != 0:
+        return 0
+
+    tokens = c.T
+    value = tokens * args.steps * world / (ms * 1e-3)
+    e2e = tokens * args.steps * world / (e2e_ms * 1e-3)
+    peak, peak_kind = load_peaks()
+    kbytes = (ab["w13"] + ab["w2"]) if moe else (ab["total"] - ab["idx"])
+    achieved = kbytes / (kms * 1e-3) / 1e9
+    launches_per_step = 3 if moe else 2
+    line = {
+        "metric": "LoRA-delta tokens/s", "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"{name}: {WORKLOADS[name]}", "tokens_per_step": tokens,
+                   "active_rows": ab["active"],
+                   "algorithmic_bytes_per_step": ab["total"],
+                   "hbm_gbs_per_step": ab["total"] / (ms / args.steps * 1e-3) / 1e9,
+                   "l2": f"inputs rotate over {n_rot} resident copies "
+                         f"({n_rot * foot / 1e6:.0f} MB of algorithmic bytes, L2 {l2 / 1e6:.0f} MB)",
+                   "timing": "CUDA graph per step (metadata + apply), K replays between CUDA events",
+                   "parallelism": f"replicas{world}"},
+        "roofline": {"bound": "hbm", "kernel": "grouped_lora_kernel (fused shrink+expand)" if not moe
+                     else "grouped_lora_kernel (w13 + w2)", "achieved": achieved, "peak": peak,
+                     "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": ncu_traffic(name, kname),
+                     "algorithmic_bytes_per_launch": kbytes, "avg_launch_us": kms * 1e3},
+        "clocks": cs.summary(),
+        "e2e": {"value": e2e, "unit": "tokens/s", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo},
+        "gpu_launches": launches_per_step * args.steps,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = time_oracle(name, c, min_seconds=args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="decode_qkv", choices=sorted(WORKLOADS))
+    ap.add_argument("--max-copies", type=int, default=16)
+    ap.add_argument("--kernel-launches", type=int, default=200)
+    ap.add_argument("--clock-seconds", type=float, default=1.0)
+    ap.add_argument("--cpu-seconds", type=float, default=2.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        return run_gpu(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,683 @@
+// Grouped shrink/expand on CUDA cores (BGMV-style decode path, and the
+// fallback for every group size): the multi-tenant LoRA delta of the vLLM
+// LoRA layer pages (add_shrink into an fp32 buffer, then add_expand with
+// add_input=True at the slice offsets; add_lora_fused_moe per (adapter,
+// expert) group after top-k routing).
+//
+// Work is cut into items over the tile list built by lora_build_meta (tiles
+// of up to 16 rows of one group, i.e. one slot or one (slot, expert)):
+//   shrink item (tile, slice j, hidden chunk c):
+//       partial[c][j][k][row] = sum_{h in chunk c} x[row][h] * A_j[a][k][h]
+//       (x tile staged in shared memory with cp.async, A rows streamed with
+//       16-byte non-allocating loads, 4 ranks x 16 rows of fp32 accumulators
+//       per lane, one butterfly reduce-scatter across the warp)
+//   expand item (tile, slice j, 512-column chunk):
+//       v[row][k] = scale[a] * w[row] * sum_c partial[c][j][k][row]
+//       y[row][off_j + o] += sum_k v[row][k] * B_j[a][o][k]   (bf16x2 RMW)
+// In the fused kernel one persistent grid takes items from a ticket counter
+// (all shrink items precede all expand items), and an expand item waits with
+// a bounded spin for its tile's shrink chunks.  Waits only ever point to
+// lower tickets, which are held by running CTAs, so the schedule cannot
+// deadlock whatever the residency.  The last CTA to finish zeroes the
+// control words so the workspace is ready for the next call.
+#include <stdlib.h>
+#include <string.h>
+
+#include "lora_internal.cuh"
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kTile = LORA_TILE_ROWS;  // 16 rows per tile
+constexpr int kOC = 2 * kThreads;      // output columns per expand item
+constexpr int kMaxHC = 1024;           // hidden chunk cap (shared-memory x tile)
+constexpr int kXPad = 8;               // bf16 padding per staged x row
+constexpr int kRedUnits = 16;
+
+enum Mode { kFused = 0, kShrinkAtomic = 1, kExpandOnly = 2 };
+
+struct GArgs {
+    int n_slices, in_dim, E, row_div, R, T, NC, HC;
+    int out_w[LORA_MAX_SLICES], out_off[LORA_MAX_SLICES], och_start[LORA_MAX_SLICES + 1];
+    const uint16_t *A[LORA_MAX_SLICES];
+    long long A_ss[LORA_MAX_SLICES], A_es[LORA_MAX_SLICES];
+    const uint16_t *B[LORA_MAX_SLICES];
+    long long B_ss[LORA_MAX_SLICES];
+    int B_shared[LORA_MAX_SLICES];
+    const int32_t *rank;
+    const float *scale;
+    const int32_t *sorted, *group_key, *group_start, *tile_group, *tile_row0, *counters;
+    const uint16_t *in;
+    long long ld_in;
+    uint16_t *out;
+    long long ld_out;
+    const float *row_w;
+    float *part;  // fused: [NC][n_slices][R][rows]; shrink: v [n_slices][T][R]; expand: v
+    int rows;     // row capacity of the partial buffer (T * top_k)
+    int *ctrl;    // [0] ticket, [1] finished CTAs
+    int *tile_cnt;
+    int *status;
+    int spin_limit;
+};
+
+struct TileInfo {
+    int row0, n, a, e, r;
+};
+
+__device__ __forceinline__ TileInfo tile_info(const GArgs &p, int tile) {
+    TileInfo ti;
+    const int g = p.tile_group[tile];
+    ti.row0 = p.tile_row0[tile];
+    ti.n = min(kTile, p.group_start[g + 1] - ti.row0);
+    const int key = p.group_key[g];
+    ti.a = key / p.E;
+    ti.e = key - ti.a * p.E;
+    ti.r = p.rank[ti.a];
+    return ti;
+}
+
+__device__ __forceinline__ void cvt8(const uint4 &u, float f[8]) {
+    f[0] = bf16lo(u.x); f[1] = bf16hi(u.x);
+    f[2] = bf16lo(u.y); f[3] = bf16hi(u.y);
+    f[4] = bf16lo(u.z); f[5] = bf16hi(u.z);
+    f[6] = bf16lo(u.w); f[7] = bf16hi(u.w);
+}
+
+// Reduce-scatter of 64 per-lane values across the warp: afterwards lane l
+// holds the warp sums of entries 2l and 2l+1 in v[0], v[1].
+__device__ __forceinline__ void warp_reduce_scatter64(float v[64], int lane) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const bool up = lane & 16;
+        const float send = up ? v[i] : v[i + 32];
+        const float keep = up ? v[i + 32] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const bool up = lane & 8;
+        const float send = up ? v[i] : v[i + 16];
+        const float keep = up ? v[i + 16] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const bool up = lane & 4;
+        const float send = up ? v[i] : v[i + 8];
+        const float keep = up ? v[i + 8] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const bool up = lane & 2;
+        const float send = up ? v[i] : v[i + 4];
+        const float keep = up ? v[i + 4] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const bool up = lane & 1;
+        const float send = up ? v[i] : v[i + 2];
+        const float keep = up ? v[i + 2] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+    }
+}
+
+template <int MODE>
+__device__ __forceinline__ void store_partial(const GArgs &p, const TileInfo &ti, int j, int c,
+                                              int k, int t, float s) {
+    if (MODE == kFused) {
+        p.part[(((long long)c * p.n_slices + j) * p.R + k) * p.rows + ti.row0 + t] = s;
+    } else {
+        const int tok = p.sorted[ti.row0 + t];
+        atomicAdd(p.part + ((long long)j * p.T + tok) * p.R + k, s);
+    }
+}
+
+template <int MODE>
+__device__ void shrink_item(const GArgs &p, int tile, int j, int c, char *smem) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const TileInfo ti = tile_info(p, tile);
+    const int XS = p.HC + kXPad;
+    uint16_t *xs = (uint16_t *)smem;
+    float *red = (float *)(smem + (size_t)kTile * XS * 2);
+    const int h0 = c * p.HC;
+    const int hc = min(p.in_dim - h0, p.HC);
+    const int nvec = hc >> 3;
+    const uint16_t *Ab = p.A[j] + (long long)ti.a * p.A_ss[j] + (long long)ti.e * p.A_es[j] + h0;
+
+    for (int i = tid; i < ti.n * nvec; i += kThreads) {
+        const int t = i / nvec, q = i - t * nvec;
+        const int row = p.sorted[ti.row0 + t];
+        cp_async16(xs + t * XS + q * 8, p.in + (long long)(row / p.row_div) * p.ld_in + h0 + q * 8);
+    }
+    cp_async_wait_all();
+    __syncthreads();
+
+    const int nkg = (ti.r + 3) >> 2;
+    const int nhs = nkg >= 8 ? 1 : nkg >= 4 ? 2 : nkg >= 2 ? 4 : 8;
+    const int units = nkg * nhs;
+    const int hs_len = ((nvec + nhs - 1) / nhs) * 8;
+    for (int u = warp; u < units; u += kThreads / 32) {
+        const int kg = u / nhs, hs = u - kg * nhs;
+        const int hb = hs * hs_len, he = min(hc, hb + hs_len);
+        float v[64];
+#pragma unroll
+        for (int i = 0; i < 64; ++i) v[i] = 0.f;
+        for (int hh = hb + lane * 8; hh < he; hh += 256) {
+            float af[4][8];
+#pragma unroll
+            for (int kb = 0; kb < 4; ++kb) {
+                const int k = kg * 4 + kb;
+                uint4 q = make_uint4(0, 0, 0, 0);
+                if (k < ti.r) q = ldg_stream(Ab + (long long)k * p.in_dim + hh);
+                cvt8(q, af[kb]);
+            }
+#pragma unroll
+            for (int t = 0; t < kTile; ++t) {
+                if (t < ti.n) {
+                    float xf[8];
+                    cvt8(*(const uint4 *)(xs + t * XS + hh), xf);
+#pragma unroll
+                    for (int kb = 0; kb < 4; ++kb) {
+                        float s = v[kb * kTile + t];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) s = fmaf(af[kb][i], xf[i], s);
+                        v[kb * kTile + t] = s;
+                    }
+                }
+            }
+        }
+        warp_reduce_scatter64(v, lane);
+        // lane holds f = 2*lane + m: rank kg*4 + (f >> 4), row f & 15
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+            const int f = 2 * lane + m;
+            const int k = kg * 4 + (f >> 4), t = f & 15;
+            if (nhs == 1) {
+                if (k < ti.r && t < ti.n) store_partial<MODE>(p, ti, j, c, k, t, v[m]);
+            } else {
+                red[u * 64 + f] = v[m];
+            }
+        }
+    }
+    if (nhs > 1) {
+        __syncthreads();
+        for (int i = tid; i < nkg * 64; i += kThreads) {
+            const int kg = i >> 6, f = i & 63;
+            const int k = kg * 4 + (f >> 4), t = f & 15;
+            if (k < ti.r && t < ti.n) {
+                float s = 0.f;
+                for (int hs = 0; hs < nhs; ++hs) s += red[(kg * nhs + hs) * 64 + f];
+                store_partial<MODE>(p, ti, j, c, k, t, s);
+            }
+        }
+    }
+}
+
+template <int MODE>
+__device__ void expand_item(const GArgs &p, int tile, int j, int oc, char *smem, int *s_flag) {
+    const int tid = threadIdx.x;
+    const TileInfo ti = tile_info(p, tile);
+    if (MODE == kFused) {
+        if (tid == 0) {
+            const int *cnt = p.tile_cnt + tile * p.n_slices + j;
+            int ok = 1, polls = 0;
+            while (ld_acquire_gpu(cnt) < p.NC) {
+                if (p.spin_limit < 0 || ++polls > p.spin_limit) {
+                    ok = 0;
+                    break;
+                }
+                __nanosleep(64);
+            }
+            if (!ok) atomicExch(p.status, (int)LORA_ERR_TIMEOUT);
+            *s_flag = ok;
+        }
+        __syncthreads();
+        if (!*s_flag) return;
+    }
+    const int rs = (ti.r + 7) & ~7;
+    const int VS = ((p.R + 7) & ~7) + 4;  // row stride of v in shared memory (multiple of 4)
+    float *vs = (float *)smem;
+    const float sc = p.scale[ti.a];
+    for (int i = tid; i < ti.n * rs; i += kThreads) {
+        const int t = i / rs, k = i - t * rs;
+        float s = 0.f;
+        if (k < ti.r) {
+            if (MODE == kFused) {
+                const float *src = p.part + ((long long)j * p.R + k) * p.rows + ti.row0 + t;
+                const long long cstride = (long long)p.n_slices * p.R * p.rows;
+                for (int c = 0; c < p.NC; ++c) s += __ldcg(src + c * cstride);
+            } else {
+                const int tok = p.sorted[ti.row0 + t];
+                s = p.part[((long long)j * p.T + tok) * p.R + k];
+            }
+            float w = sc;
+            if (p.row_w) w *= p.row_w[p.sorted[ti.row0 + t]];
+            s *= w;
+        }
+        vs[t * VS + k] = s;
+    }
+    __syncthreads();
+    const int Ow = p.out_w[j];
+    const int o = oc * kOC + tid * 2;
+    if (o < Ow) {
+        const uint16_t *Bb = p.B[j] + (long long)ti.a * p.B_ss[j] +
+                             (p.B_shared[j] ? 0ll : (long long)ti.e * Ow * rs);
+        const uint16_t *b0p = Bb + (long long)o * rs;
+        const uint16_t *b1p = b0p + rs;
+        float acc0[kTile], acc1[kTile];
+#pragma unroll
+        for (int t = 0; t < kTile; ++t) acc0[t] = acc1[t] = 0.f;
+        for (int kk = 0; kk < rs; kk += 8) {
+            float f0[8], f1[8];
+            cvt8(ldg_stream(b0p + kk), f0);
+            cvt8(ldg_stream(b1p + kk), f1);
+#pragma unroll
+            for (int t = 0; t < kTile; ++t) {
+                if (t < ti.n) {
+                    const float4 va = *(const float4 *)(vs + t * VS + kk);
+                    const float4 vb = *(const float4 *)(vs + t * VS + kk + 4);
+                    const float vv[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+                    float s0 = acc0[t], s1 = acc1[t];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        s0 = fmaf(vv[i], f0[i], s0);
+                        s1 = fmaf(vv[i], f1[i], s1);
+                    }
+                    acc0[t] = s0;
+                    acc1[t] = s1;
+                }
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < kTile; ++t) {
+            if (t < ti.n) {
+                const int row = p.sorted[ti.row0 + t];
+                uint32_t *yp = (uint32_t *)(p.out + (long long)row * p.ld_out + p.out_off[j] + o);
+                const uint32_t u = *yp;
+                const __nv_bfloat162 r2 = __floats2bfloat162_rn(bf16lo(u) + acc0[t], bf16hi(u) + acc1[t]);
+                *yp = *(const uint32_t *)&r2;
+            }
+        }
+    }
+}
+
+template <int MODE>
+__device__ __forceinline__ void run_item(const GArgs &p, int item, int n_sh, char *smem, int *s_flag) {
+    if (item < n_sh) {
+        const int per_tile = p.n_slices * p.NC;
+        const int tile = item / per_tile;
+        const int rem = item - tile * per_tile;
+        const int j = rem / p.NC, c = rem - j * p.NC;
+        shrink_item<MODE>(p, tile, j, c, smem);
+        if (MODE == kFused) {
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                __threadfence();
+                atomicAdd(p.tile_cnt + tile * p.n_slices + j, 1);
+            }
+        }
+    } else {
+        const int it = item - n_sh;
+        const int och = p.och_start[p.n_slices];
+        const int tile = it / och;
+        const int q = it - tile * och;
+        int j = 0;
+        while (q >= p.och_start[j + 1]) ++j;
+        expand_item<MODE>(p, tile, j, q - p.och_start[j], smem, s_flag);
+    }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads) grouped_lora_kernel(const __grid_constant__ GArgs p) {
+    extern __shared__ __align__(16) char smem[];
+    __shared__ int s_item, s_flag, s_last;
+    const int n_tiles = p.counters[3];
+    const int n_sh = (MODE == kExpandOnly) ? 0 : n_tiles * p.n_slices * p.NC;
+    const int n_ex = (MODE == kShrinkAtomic) ? 0 : n_tiles * p.och_start[p.n_slices];
+    const int total = n_sh + n_ex;
+    if (MODE == kFused) {
+        int nxt = 0;
+        if (threadIdx.x == 0) nxt = atomicAdd(p.ctrl, 1);
+        for (;;) {
+            if (threadIdx.x == 0) {
+                s_item = nxt;
+                nxt = atomicAdd(p.ctrl, 1);
+            }
+            __syncthreads();
+            const int item = s_item;
+            if (item >= total) break;
+            run_item<MODE>(p, item, n_sh, smem, &s_flag);
+            __syncthreads();
+        }
+        if (threadIdx.x == 0) {
+            __threadfence();
+            s_last = (atomicAdd(p.ctrl + 1, 1) == (int)gridDim.x - 1);
+        }
+        __syncthreads();
+        if (s_last) {
+            __threadfence();
+            for (int i = threadIdx.x; i < n_tiles * p.n_slices; i += kThreads) p.tile_cnt[i] = 0;
+            if (threadIdx.x == 0) {
+                p.ctrl[0] = 0;
+                p.ctrl[1] = 0;
+            }
+        }
+    } else {
+        for (int item = blockIdx.x; item < total; item += gridDim.x) {
+            run_item<MODE>(p, item, n_sh, smem, &s_flag);
+            __syncthreads();
+        }
+    }
+}
+
+int g_spin_limit = 1 << 20;
+
+struct Plan {
+    int NC, HC;
+    size_t part_floats, cnt_ints;
+};
+
+// Split the hidden dimension so that every shrink item stays small
+// (<= ~0.5M FMAs) and the grid has several items per SM.
+Plan make_plan(int num_sms, int in_dim, int n_slices, int R, int rows, int n_keys) {
+    Plan pl;
+    const long long tiles_est = (rows + kTile - 1) / kTile + (rows < n_keys ? rows : n_keys);
+    const long long units = tiles_est * n_slices > 0 ? tiles_est * n_slices : 1;
+    int nc_par = (int)((6LL * num_sms + units - 1) / units);
+    int nc_work = (int)(((long long)in_dim * kTile * R + (1 << 19) - 1) >> 19);
+    int nc = nc_par > nc_work ? nc_par : nc_work;
+    if (nc < 1) nc = 1;
+    int hc = lora_round8(lora_ceil_div(in_dim, nc));
+    if (hc > kMaxHC) hc = kMaxHC;
+    if (hc < 8) hc = 8;
+    pl.HC = hc;
+    pl.NC = lora_ceil_div(in_dim, hc);
+    pl.part_floats = (size_t)pl.NC * n_slices * R * (size_t)rows;
+    const size_t max_tiles = (size_t)rows / kTile + n_keys + 1;
+    pl.cnt_ints = max_tiles * n_slices;
+    return pl;
+}
+
+constexpr size_t kCtrlBytes = 256;
+
+size_t ws_bytes_for(const Plan &pl) {
+    size_t b = kCtrlBytes + ((pl.cnt_ints * 4 + 255) & ~(size_t)255);
+    return b + pl.part_floats * 4;
+}
+
+size_t smem_bytes(const GArgs &g) {
+    const size_t shrink = (size_t)kTile * (g.HC + kXPad) * 2 + (size_t)kRedUnits * 64 * 4;
+    const size_t expand = (size_t)kTile * (((g.R + 7) & ~7) + 4) * 4;
+    return shrink > expand ? shrink : expand;
+}
+
+constexpr size_t kMaxSmem = (size_t)kTile * (kMaxHC + kXPad) * 2 + (size_t)kRedUnits * 64 * 4;
+static_assert(kMaxSmem <= 48 * 1024, "grouped kernel must fit the default shared-memory limit");
+static_assert((size_t)kTile * (((LORA_MAX_RANK + 7) & ~7) + 4) * 4 <= kMaxSmem, "v tile");
+
+// Occupancy per (device, mode), queried once outside any stream capture.
+int g_occ[64][3];
+
+template <int MODE>
+lora_status_t launch(const lora_pool_t *pool, GArgs &g, long long est_items, cudaStream_t s) {
+    const size_t smem = smem_bytes(g);
+    int dev = pool->device < 64 ? pool->device : 63;
+    int &occ = g_occ[dev][MODE];
+    if (occ == 0) {
+        int o = 0;
+        LORA_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, grouped_lora_kernel<MODE>,
+                                                                    kThreads, kMaxSmem));
+        occ = o < 1 ? 1 : o;
+    }
+    long long grid = (long long)pool->num_sms * occ;
+    if (est_items < grid) grid = est_items;
+    if (grid < 1) grid = 1;
+    g.spin_limit = g_spin_limit;
+    grouped_lora_kernel<MODE><<<(unsigned)grid, kThreads, smem, s>>>(g);
+    LORA_CUDA_TRY(cudaGetLastError());
+    return LORA_OK;
+}
+
+// Fill the fields shared by every mode for a dense pool.
+lora_status_t dense_args(const lora_pool_t *pool, const lora_meta_t *meta, GArgs &g) {
+    if (pool->is_moe) return LORA_ERR_UNSUPPORTED;
+    if (!meta || meta->mode != 0 || meta->n_keys != pool->desc.max_loras) return LORA_ERR_INVALID_ARG;
+    memset(&g, 0, sizeof(g));
+    const lora_pool_desc_t &d = pool->desc;
+    g.n_slices = d.n_slices;
+    g.in_dim = d.in_dim;
+    g.E = 1;
+    g.row_div = 1;
+    g.R = d.max_rank;
+    g.T = meta->T;
+    int off = 0, och = 0;
+    for (int j = 0; j < d.n_slices; ++j) {
+        g.out_w[j] = d.out_dims[j];
+        g.out_off[j] = off;
+        off += d.out_dims[j];
+        g.och_start[j] = och;
+        och += lora_ceil_div(d.out_dims[j], kOC);
+        g.A[j] = pool->A[j];
+        g.A_ss[j] = pool->a_slot_elems[j];
+        g.A_es[j] = 0;
+        g.B[j] = pool->B[j];
+        g.B_ss[j] = pool->b_slot_elems[j];
+        g.B_shared[j] = 1;
+    }
+    g.och_start[d.n_slices] = och;
+    g.rank = pool->d_rank;
+    g.scale = pool->d_scale;
+    g.sorted = meta->sorted;
+    g.group_key = meta->group_key;
+    g.group_start = meta->group_start;
+    g.tile_group = meta->tile_group;
+    g.tile_row0 = meta->tile_row0;
+    g.counters = meta->counters;
+    g.status = pool->d_status;
+    g.rows = meta->T;
+    return LORA_OK;
+}
+
+int out_total(const lora_pool_t *pool) {
+    int s = 0;
+    for (int j = 0; j < pool->desc.n_slices; ++j) s += pool->desc.out_dims[j];
+    return s;
+}
+
+// A workspace sized for T tokens always fits a smaller batch once the hidden
+// chunks are widened (fewer chunks, fewer partials).
+Plan fit_plan(Plan pl, int in_dim, int n_slices, int R, int rows, size_t ws_bytes) {
+    while (ws_bytes_for(pl) > ws_bytes && pl.HC < kMaxHC) {
+        pl.HC = pl.HC * 2 > kMaxHC ? kMaxHC : pl.HC * 2;
+        pl.NC = lora_ceil_div(in_dim, pl.HC);
+        pl.part_floats = (size_t)pl.NC * n_slices * R * (size_t)rows;
+    }
+    return pl;
+}
+
+lora_status_t bind_workspace(GArgs &g, const Plan &pl, void *ws, size_t ws_bytes) {
+    if (!ws || !lora_aligned16(ws)) return LORA_ERR_INVALID_ARG;
+    if (ws_bytes < ws_bytes_for(pl)) return LORA_ERR_CAPACITY;
+    char *b = (char *)ws;
+    g.ctrl = (int *)b;
+    g.tile_cnt = (int *)(b + kCtrlBytes);
+    g.part = (float *)(b + kCtrlBytes + ((pl.cnt_ints * 4 + 255) & ~(size_t)255));
+    g.NC = pl.NC;
+    g.HC = pl.HC;
+    return LORA_OK;
+}
+
+long long est_items(const GArgs &g, int rows, int n_keys, int mode) {
+    const long long tiles = (rows + kTile - 1) / kTile + (rows < n_keys ? rows : n_keys);
+    long long n = 0;
+    if (mode != kExpandOnly) n += tiles * g.n_slices * g.NC;
+    if (mode != kShrinkAtomic) n += tiles * g.och_start[g.n_slices];
+    return n;
+}
+
+}  // namespace
+
+extern "C" void lora_set_spin_limit(int32_t max_polls) { g_spin_limit = max_polls; }
+
+extern "C" size_t lora_workspace_bytes(const lora_pool_t *pool, int32_t T, int32_t top_k) {
+    if (!pool || T < 0) return 0;
+    const lora_pool_desc_t &d = pool->desc;
+    if (!pool->is_moe) {
+        const Plan pl = make_plan(pool->num_sms, d.in_dim, d.n_slices, d.max_rank, T, d.max_loras);
+        return ws_bytes_for(pl);
+    }
+    if (top_k < 1) return 0;
+    const int rows = T * top_k, keys = d.max_loras * d.num_experts;
+    const Plan p13 = make_plan(pool->num_sms, d.d_model, d.n_w13_slices, d.max_rank, rows, keys);
+    const Plan p2 = make_plan(pool->num_sms, d.d_mlp, 1, d.max_rank, rows, keys);
+    const size_t a = ws_bytes_for(p13), b = ws_bytes_for(p2);
+    return a > b ? a : b;
+}
+
+extern "C" lora_status_t lora_workspace_init(void *workspace, size_t bytes, void *stream) {
+    if (!workspace) return LORA_ERR_INVALID_ARG;
+    LORA_CUDA_TRY(cudaMemsetAsync(workspace, 0, bytes, (cudaStream_t)stream));
+    return LORA_OK;
+}
+
+extern "C" lora_status_t lora_apply_slices(const lora_pool_t *pool, const lora_meta_t *meta,
+                                           const void *x, int64_t ldx, void *y, int64_t ldy,
+                                           void *workspace, size_t ws_bytes, void *stream) {
+    if (!pool) return LORA_ERR_INVALID_ARG;
+    GArgs g;
+    lora_status_t st = dense_args(pool, meta, g);
+    if (st != LORA_OK) return st;
+    if (meta->T == 0) return LORA_OK;
+    if (!x || !y || !lora_aligned16(x) || !lora_aligned16(y) || ldx % 8 || ldy % 8 ||
+        ldx < pool->desc.in_dim || ldy < out_total(pool))
+        return LORA_ERR_INVALID_ARG;
+    const Plan pl = fit_plan(make_plan(pool->num_sms, g.in_dim, g.n_slices, g.R, meta->T,
+                                       pool->desc.max_loras),
+                             g.in_dim, g.n_slices, g.R, meta->T, ws_bytes);
+    st = bind_workspace(g, pl, workspace, ws_bytes);
+    if (st != LORA_OK) return st;
+    g.in = (const uint16_t *)x;
+    g.ld_in = ldx;
+    g.out = (uint16_t *)y;
+    g.ld_out = ldy;
+    return launch<kFused>(pool, g, est_items(g, meta->T, pool->desc.max_loras, kFused),
+                          (cudaStream_t)stream);
+}
+
+extern "C" lora_status_t lora_shrink(const lora_pool_t *pool, const lora_meta_t *meta,
+                                     const void *x, int64_t ldx, float *v, void *stream) {
+    if (!pool) return LORA_ERR_INVALID_ARG;
+    GArgs g;
+    lora_status_t st = dense_args(pool, meta, g);
+    if (st != LORA_OK) return st;
+    if (meta->T == 0) return LORA_OK;
+    if (!x || !v || !lora_aligned16(x) || ldx % 8 || ldx < pool->desc.in_dim)
+        return LORA_ERR_INVALID_ARG;
+    const Plan pl = make_plan(pool->num_sms, g.in_dim, g.n_slices, g.R, meta->T, pool->desc.max_loras);
+    g.NC = pl.NC;
+    g.HC = pl.HC;
+    g.in = (const uint16_t *)x;
+    g.ld_in = ldx;
+    g.part = v;
+    cudaStream_t s = (cudaStream_t)stream;
+    LORA_CUDA_TRY(cudaMemsetAsync(v, 0, (size_t)g.n_slices * meta->T * g.R * 4, s));
+    return launch<kShrinkAtomic>(pool, g, est_items(g, meta->T, pool->desc.max_loras, kShrinkAtomic), s);
+}
+
+extern "C" lora_status_t lora_expand(const lora_pool_t *pool, const lora_meta_t *meta,
+                                     const float *v, void *y, int64_t ldy, void *stream) {
+    if (!pool) return LORA_ERR_INVALID_ARG;
+    GArgs g;
+    lora_status_t st = dense_args(pool, meta, g);
+    if (st != LORA_OK) return st;
+    if (meta->T == 0) return LORA_OK;
+    if (!v || !y || !lora_aligned16(y) || ldy % 8 || ldy < out_total(pool)) return LORA_ERR_INVALID_ARG;
+    g.NC = 1;
+    g.HC = 8;
+    g.part = (float *)v;
+    g.out = (uint16_t *)y;
+    g.ld_out = ldy;
+    return launch<kExpandOnly>(pool, g, est_items(g, meta->T, pool->desc.max_loras, kExpandOnly),
+                               (cudaStream_t)stream);
+}
+
+extern "C" lora_status_t lora_moe_apply(const lora_pool_t *pool, const lora_meta_t *meta,
+                                        int32_t which, const void *in, int64_t ld_in,
+                                        const float *topk_w, void *out, int64_t ld_out,
+                                        void *workspace, size_t ws_bytes, void *stream) {
+    if (!pool || !meta) return LORA_ERR_INVALID_ARG;
+    if (!pool->is_moe) return LORA_ERR_UNSUPPORTED;
+    const lora_pool_desc_t &d = pool->desc;
+    const int E = d.num_experts;
+    if (meta->mode != 1 || meta->n_keys != d.max_loras * E) return LORA_ERR_INVALID_ARG;
+    if (which != LORA_MOE_W13 && which != LORA_MOE_W2) return LORA_ERR_INVALID_ARG;
+    if (meta->T == 0) return LORA_OK;
+    GArgs g;
+    memset(&g, 0, sizeof(g));
+    const int rows = meta->T * meta->top_k;
+    const int n13 = d.n_w13_slices;
+    g.E = E;
+    g.R = d.max_rank;
+    g.T = meta->T;
+    g.rows = rows;
+    int och = 0;
+    if (which == LORA_MOE_W13) {
+        g.n_slices = n13;
+        g.in_dim = d.d_model;
+        g.row_div = meta->top_k;
+        for (int s = 0; s < n13; ++s) {
+            g.out_w[s] = d.w13_slice_width;
+            g.out_off[s] = s * d.w13_slice_width;
+            g.och_start[s] = och;
+            och += lora_ceil_div(d.w13_slice_width, kOC);
+            g.A[s] = pool->A[s];
+            g.A_ss[s] = pool->a_slot_elems[s];
+            g.A_es[s] = pool->a_experts[s] == 1 ? 0 : (long long)d.max_rank * d.d_model;
+            g.B[s] = pool->B[s];
+            g.B_ss[s] = pool->b_slot_elems[s];
+            g.B_shared[s] = pool->b_experts[s] == 1;
+        }
+        if (topk_w) return LORA_ERR_INVALID_ARG;
+        if (ld_out < (long long)n13 * d.w13_slice_width || ld_in < d.d_model) return LORA_ERR_INVALID_ARG;
+    } else {
+        g.n_slices = 1;
+        g.in_dim = d.d_mlp;
+        g.row_div = 1;
+        g.out_w[0] = d.d_model;
+        g.out_off[0] = 0;
+        g.och_start[0] = 0;
+        och = lora_ceil_div(d.d_model, kOC);
+        g.A[0] = pool->A[n13];
+        g.A_ss[0] = pool->a_slot_elems[n13];
+        g.A_es[0] = pool->a_experts[n13] == 1 ? 0 : (long long)d.max_rank * d.d_mlp;
+        g.B[0] = pool->B[n13];
+        g.B_ss[0] = pool->b_slot_elems[n13];
+        g.B_shared[0] = pool->b_experts[n13] == 1;
+        g.row_w = topk_w;
+        if (ld_out < d.d_model || ld_in < d.d_mlp) return LORA_ERR_INVALID_ARG;
+    }
+    g.och_start[g.n_slices] = och;
+    if (!in || !out || !lora_aligned16(in) || !lora_aligned16(out) || ld_in % 8 || ld_out % 8)
+        return LORA_ERR_INVALID_ARG;
+    g.rank = pool->d_rank;
+    g.scale = pool->d_scale;
+    g.sorted = meta->sorted;
+    g.group_key = meta->group_key;
+    g.group_start = meta->group_start;
+    g.tile_group = meta->tile_group;
+    g.tile_row0 = meta->tile_row0;
+    g.counters = meta->counters;
+    g.status = pool->d_status;
+    g.in = (const uint16_t *)in;
+    g.ld_in = ld_in;
+    g.out = (uint16_t *)out;
+    g.ld_out = ld_out;
+    const int keys = d.max_loras * E;
+    const Plan pl = fit_plan(make_plan(pool->num_sms, g.in_dim, g.n_slices, g.R, rows, keys), g.in_dim,
+                             g.n_slices, g.R, rows, ws_bytes);
+    lora_status_t st = bind_workspace(g, pl, workspace, ws_bytes);
+    if (st != LORA_OK) return st;
+    return launch<kFused>(pool, g, est_items(g, rows, keys, kFused), (cudaStream_t)stream);
+}

@@ -1,0 +1,248 @@
+// Adapter-batch metadata on the device: a stable counting sort of rows by
+// key in one CTA (the grouping the Punica/S-LoRA kernels consume; SGLang's
+// LoRAManager.prepare_lora_batch builds the per-row slot table on the host,
+// vLLM's moe_lora_align_block_size the per-(adapter, expert) grouping).
+//
+// Rows are tokens (dense) or pairs p = t*K + k (MoE).  key(row) = a
+// (dense) or a*E + e (MoE) for active rows, n_keys for inactive ones, so the
+// inactive rows land last in original order.  The rows are cut into up to 32
+// contiguous chunks, one per warp; each warp keeps its own histogram in
+// shared memory, which makes the scatter stable without atomics:
+//   1. per-warp histograms (warp match-any: one leader per key per step)
+//   2. per-key prefix over the chunks, block scan over keys -> key offsets
+//   3. scatter: position = key offset + earlier chunks + earlier lanes
+//   4. groups = non-empty keys, tiles of LORA_TILE_ROWS rows per group
+#include "lora_internal.cuh"
+
+namespace {
+
+constexpr int kThreads = 1024;
+constexpr int kSmemBudgetInts = 56 * 1024;  // 224 KB
+
+struct MetaArgs {
+    const int32_t *idx;
+    const int32_t *topk;
+    const int32_t *rank;
+    const int32_t *enabled;
+    int32_t *status;
+    int T, K, E, L, n_keys, n_chunks;
+    lora_meta_t m;
+};
+
+// Exclusive scan of data[0..n) in shared memory; returns the total.
+__device__ int block_exclusive_scan(int *data, int n, int *warp_tot) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int per = (n + kThreads - 1) / kThreads;
+    const int b = min(n, tid * per), e = min(n, b + per);
+    int local = 0;
+    for (int i = b; i < e; ++i) local += data[i];
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int w = warp_tot[lane];
+        int wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int v = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o) wi += v;
+        }
+        warp_tot[lane] = wi - w;     // exclusive warp base
+        if (lane == 31) warp_tot[32] = wi;
+    }
+    __syncthreads();
+    int run = warp_tot[warp] + incl - local;
+    for (int i = b; i < e; ++i) {
+        int v = data[i];
+        data[i] = run;
+        run += v;
+    }
+    const int total = warp_tot[32];
+    __syncthreads();
+    return total;
+}
+
+__device__ __forceinline__ int row_key(const MetaArgs &a, int row, int *bad) {
+    const int t = row / a.K;
+    const int s = a.idx[t];
+    const bool valid = s >= 0 && s < a.L;
+    int b = (s != -1 && !valid && (row % a.K) == 0) ? 1 : 0;
+    bool act = valid && a.enabled[s] != 0 && a.rank[s] > 0;
+    int key = a.n_keys;
+    if (a.topk) {
+        const int e = a.topk[row];
+        const bool ev = e >= 0 && e < a.E;
+        b += ev ? 0 : 1;
+        if (act && ev) key = s * a.E + e;
+    } else if (act) {
+        key = s;
+    }
+    *bad += b;
+    return key;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) build_meta_kernel(MetaArgs a) {
+    extern __shared__ int sm[];
+    const int NK = a.n_keys, NK1 = NK + 1, W = a.n_chunks;
+    int *hist = sm;                 // [W][NK1]
+    int *cnt = hist + W * NK1;      // [NK1]
+    int *off = cnt + NK1;           // [NK1]
+    int *misc = off + NK1;          // [40]: warp totals(33), n_bad
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int rows = a.T * a.K;
+
+    for (int i = tid; i < W * NK1; i += kThreads) hist[i] = 0;
+    if (tid == 0) misc[36] = 0;
+    __syncthreads();
+
+    const int chunk = (rows + W - 1) / W;
+    if (warp < W) {
+        const int r0 = warp * chunk, r1 = min(rows, r0 + chunk);
+        int bad = 0;
+        for (int base = r0; base < r1; base += 32) {
+            const int row = base + lane;
+            const bool v = row < r1;
+            const int key = v ? row_key(a, row, &bad) : -1;
+            const unsigned peers = __match_any_sync(0xffffffffu, key);
+            if (v && lane == __ffs(peers) - 1) hist[warp * NK1 + key] += __popc(peers);
+            __syncwarp();
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) bad += __shfl_xor_sync(0xffffffffu, bad, o);
+        if (lane == 0 && bad) atomicAdd(&misc[36], bad);
+    }
+    __syncthreads();
+
+    for (int b = tid; b < NK1; b += kThreads) {
+        int run = 0;
+        for (int w = 0; w < W; ++w) {
+            const int c = hist[w * NK1 + b];
+            hist[w * NK1 + b] = run;
+            run += c;
+        }
+        cnt[b] = run;
+        off[b] = run;
+    }
+    __syncthreads();
+    block_exclusive_scan(off, NK1, misc);
+    for (int b = tid; b < NK1; b += kThreads) {
+        const int o = off[b];
+        for (int w = 0; w < W; ++w) hist[w * NK1 + b] += o;
+        if (b < NK) {
+            a.m.key_count[b] = cnt[b];
+        }
+        a.m.key_offset[b] = o;
+    }
+    __syncthreads();
+
+    if (warp < W) {
+        const int r0 = warp * chunk, r1 = min(rows, r0 + chunk);
+        const unsigned lt = (1u << lane) - 1u;
+        for (int base = r0; base < r1; base += 32) {
+            const int row = base + lane;
+            const bool v = row < r1;
+            int dummy = 0;
+            const int key = v ? row_key(a, row, &dummy) : -1;
+            const unsigned peers = __match_any_sync(0xffffffffu, key);
+            int pos = 0;
+            if (v) pos = hist[warp * NK1 + key] + __popc(peers & lt);
+            __syncwarp();
+            if (v) {
+                a.m.sorted[pos] = row;
+                if (lane == __ffs(peers) - 1) hist[warp * NK1 + key] += __popc(peers);
+            }
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+
+    // groups: non-empty keys in ascending order
+    int *gidx = hist;             // [NK1] reuse
+    int *tiles = hist + NK1;      // [NK1]
+    for (int b = tid; b < NK1; b += kThreads) {
+        const bool ne = b < NK && cnt[b] > 0;
+        gidx[b] = ne ? 1 : 0;
+        tiles[b] = ne ? (cnt[b] + LORA_TILE_ROWS - 1) / LORA_TILE_ROWS : 0;
+    }
+    __syncthreads();
+    const int G = block_exclusive_scan(gidx, NK1, misc);
+    const int NT = block_exclusive_scan(tiles, NK1, misc);
+    for (int b = tid; b < NK; b += kThreads) {
+        const int c = cnt[b];
+        if (c > 0) {
+            const int g = gidx[b];
+            a.m.key_group[b] = g;
+            a.m.group_key[g] = b;
+            a.m.group_start[g] = off[b];
+            const int nt = (c + LORA_TILE_ROWS - 1) / LORA_TILE_ROWS;
+            for (int i = 0; i < nt; ++i) {
+                a.m.tile_group[tiles[b] + i] = g;
+                a.m.tile_row0[tiles[b] + i] = off[b] + i * LORA_TILE_ROWS;
+            }
+        } else {
+            a.m.key_group[b] = -1;
+        }
+    }
+    if (tid == 0) {
+        const int n_active = off[NK];
+        const int n_bad = misc[36];
+        a.m.group_start[G] = n_active;
+        a.m.counters[0] = n_active;
+        a.m.counters[1] = G;
+        a.m.counters[2] = n_bad;
+        a.m.counters[3] = NT;
+        if (n_bad) atomicExch(a.status, (int)LORA_ERR_DEVICE_INDEX);
+    }
+}
+
+}  // namespace
+
+lora_status_t lora_launch_build_meta(const lora_pool_t *pool, const int32_t *d_idx, int32_t T,
+                                     const int32_t *d_topk, int32_t top_k, lora_meta_t *meta,
+                                     cudaStream_t stream) {
+    const int L = pool->desc.max_loras;
+    const int E = pool->is_moe ? pool->desc.num_experts : 1;
+    const int64_t rows = (int64_t)T * top_k;
+    const int n_keys = L * E;
+    if (rows > meta->max_rows || n_keys > meta->max_keys || n_keys > LORA_MAX_KEYS)
+        return LORA_ERR_CAPACITY;
+    if (!meta->sorted || !meta->counters) return LORA_ERR_INVALID_ARG;
+    const int NK1 = n_keys + 1;
+    int W = (kSmemBudgetInts - 2 * NK1 - 40) / NK1;
+    if (W > 32) W = 32;
+    if (W < 2) return LORA_ERR_CAPACITY;  // the group/tile pass reuses two histogram rows
+    MetaArgs a;
+    a.idx = d_idx;
+    a.topk = d_topk;
+    a.rank = pool->d_rank;
+    a.enabled = pool->d_enabled;
+    a.status = pool->d_status;
+    a.T = T;
+    a.K = top_k;
+    a.E = E;
+    a.L = L;
+    a.n_keys = n_keys;
+    a.n_chunks = W;
+    a.m = *meta;
+    const size_t smem = (size_t)(W * NK1 + 2 * NK1 + 40) * 4;
+    // raise the kernel's shared-memory limit once per device (outside any capture)
+    static int configured[64];
+    const int dev = pool->device < 64 ? pool->device : 63;
+    if (!configured[dev]) {
+        LORA_CUDA_TRY(cudaFuncSetAttribute(build_meta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           kSmemBudgetInts * 4));
+        configured[dev] = 1;
+    }
+    build_meta_kernel<<<1, kThreads, smem, stream>>>(a);
+    LORA_CUDA_TRY(cudaGetLastError());
+    meta->T = T;
+    meta->top_k = top_k;
+    meta->n_keys = n_keys;
+    meta->mode = pool->is_moe ? 1 : 0;
+    return LORA_OK;
+}

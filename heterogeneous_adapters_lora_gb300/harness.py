@@ -1,0 +1,194 @@
+"""Device-side plumbing around the C ABI: upload a seeded case into a pool,
+allocate metadata/workspace buffers with PyTorch, and call the library.
+
+Nothing here computes any part of the LoRA delta; it only moves the inputs
+of ``inputs.DenseCase`` / ``inputs.MoECase`` to the GPU and forwards to the
+same-name wrappers of ``lora``.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import lora as L
+
+
+def to_dev_u16(a: np.ndarray, device="cuda") -> torch.Tensor:
+    """bf16 bit patterns (uint16) -> int16 device tensor with the same bits."""
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device)
+
+
+def from_dev_u16(t: torch.Tensor) -> np.ndarray:
+    return t.cpu().numpy().view(np.uint16)
+
+
+class MetaBuffer:
+    """Caller-owned metadata buffer bound to a ``lora_meta_t``."""
+
+    def __init__(self, max_rows: int, max_keys: int, device="cuda"):
+        self.nbytes = L.lora_meta_bytes(max_rows, max_keys)
+        self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device)
+        self.meta = L.Meta()
+        L.lora_meta_bind(self.meta, self.buf, self.nbytes, max_rows, max_keys)
+
+    def _arr(self, name, n):
+        addr = getattr(self.meta, name)
+        off = addr - self.buf.data_ptr()
+        return self.buf[off:off + 4 * n].view(torch.int32)
+
+    def read(self):
+        """Copy the metadata arrays to host numpy (synchronises)."""
+        m = self.meta
+        cnt = self._arr("counters", 4).cpu().numpy()
+        n_active, G, n_bad, NT = (int(v) for v in cnt)
+        rows = m.T * m.top_k
+        K = m.n_keys
+        out = dict(n_active=n_active, n_groups=G, n_bad=n_bad, n_tiles=NT,
+                   sorted=self._arr("sorted", rows).cpu().numpy(),
+                   key_count=self._arr("key_count", K).cpu().numpy(),
+                   key_offset=self._arr("key_offset", K + 1).cpu().numpy(),
+                   group_key=self._arr("group_key", G).cpu().numpy(),
+                   group_start=self._arr("group_start", G + 1).cpu().numpy(),
+                   key_group=self._arr("key_group", K).cpu().numpy(),
+                   tile_group=self._arr("tile_group", NT).cpu().numpy(),
+                   tile_row0=self._arr("tile_row0", NT).cpu().numpy())
+        return out
+
+
+def dense_desc(case, lm_head: bool = False) -> L.PoolDesc:
+    d = L.PoolDesc()
+    d.max_loras, d.max_rank, d.in_dim = case.L, case.R, case.H
+    d.n_slices = case.n_slices
+    for j, o in enumerate(case.out_dims):
+        d.out_dims[j] = o
+    d.is_lm_head = int(lm_head)
+    return d
+
+
+def moe_desc(case) -> L.PoolDesc:
+    d = L.PoolDesc()
+    d.max_loras, d.max_rank = case.L, case.R
+    d.num_experts, d.d_model, d.d_mlp = case.E, case.D, case.F
+    d.n_w13_slices, d.w13_slice_width, d.shared_outer = case.n13, case.F13, int(case.shared_outer)
+    return d
+
+
+def upload_dense_slot(pool, case, a, stream=None):
+    r = int(case.ranks[a])
+    A = [np.ascontiguousarray(case.A[j][a, :r, :]) for j in range(case.n_slices)]
+    B = [np.ascontiguousarray(case.B[j][a, :, :r]) for j in range(case.n_slices)]
+    L.lora_set(pool, a, r, float(case.scales[a]), A, B, stream)
+    return A, B
+
+
+def upload_moe_slot(pool, case, a, stream=None):
+    r = int(case.ranks[a])
+    A = [np.ascontiguousarray(x[a][:, :r, :]) for x in case.A13] + [np.ascontiguousarray(case.A2[a][:, :r, :])]
+    B = [np.ascontiguousarray(x[a][:, :, :r]) for x in case.B13] + [np.ascontiguousarray(case.B2[a][:, :, :r])]
+    ae = [x.shape[1] for x in case.A13] + [case.A2.shape[1]]
+    be = [x.shape[1] for x in case.B13] + [case.B2.shape[1]]
+    L.lora_set_moe(pool, a, r, float(case.scales[a]), A, ae, B, be, stream)
+    return A, B
+
+
+class DenseRun:
+    """A dense case resident on the GPU: pool, x, y, idx, meta, workspace."""
+
+    def __init__(self, case, device="cuda", lm_head=False, max_rows=None):
+        self.case = case
+        self.pool = L.lora_pool_create(dense_desc(case, lm_head))
+        for a in range(case.L):
+            if case.ranks[a] > 0 and case.enabled[a]:
+                upload_dense_slot(self.pool, case, a)
+        self.x = to_dev_u16(case.x, device)
+        self.y = to_dev_u16(case.y0, device)
+        self.idx = torch.from_numpy(case.idx).to(device)
+        T = max_rows if max_rows is not None else case.T
+        self.mb = MetaBuffer(max(T, 1), case.L, device)
+        self.ws_bytes = L.lora_workspace_bytes(self.pool, max(T, 1), 1)
+        self.ws = torch.zeros(max(self.ws_bytes, 16), dtype=torch.uint8, device=device)
+
+    def build_meta(self, T=None):
+        T = self.case.T if T is None else T
+        L.lora_build_meta(self.pool, self.idx, T, None, 1, self.mb.meta)
+
+    def apply(self):
+        c = self.case
+        L.lora_apply_slices(self.pool, self.mb.meta, self.x, c.H, self.y, c.out_total, self.ws,
+                            self.ws_bytes)
+
+    def step(self):
+        self.build_meta()
+        self.apply()
+
+    def y_host(self) -> np.ndarray:
+        return from_dev_u16(self.y)
+
+    def status(self) -> int:
+        return L.lora_get_device_status(self.pool)
+
+    def close(self):
+        if self.pool:
+            L.lora_pool_destroy(self.pool)
+            self.pool = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class MoERun:
+    """A MoE case resident on the GPU."""
+
+    def __init__(self, case, device="cuda"):
+        self.case = case
+        self.pool = L.lora_pool_create(moe_desc(case))
+        for a in range(case.L):
+            if case.ranks[a] > 0 and case.enabled[a]:
+                upload_moe_slot(self.pool, case, a)
+        self.x = to_dev_u16(case.x, device)
+        self.ic2 = to_dev_u16(case.ic2, device)
+        self.ic1 = to_dev_u16(case.ic1_0, device)
+        self.ic3 = to_dev_u16(case.ic3_0, device)
+        self.idx = torch.from_numpy(case.idx).to(device)
+        self.topk = torch.from_numpy(np.ascontiguousarray(case.topk_ids)).to(device)
+        self.topk_w = torch.from_numpy(np.ascontiguousarray(case.topk_w).reshape(-1)).to(device)
+        rows = case.T * case.K
+        self.mb = MetaBuffer(max(rows, 1), case.L * case.E, device)
+        self.ws_bytes = L.lora_workspace_bytes(self.pool, max(case.T, 1), case.K)
+        self.ws = torch.zeros(max(self.ws_bytes, 16), dtype=torch.uint8, device=device)
+
+    def build_meta(self):
+        c = self.case
+        L.lora_build_meta(self.pool, self.idx, c.T, self.topk, c.K, self.mb.meta)
+
+    def w13(self):
+        c = self.case
+        L.lora_moe_apply(self.pool, self.mb.meta, L.MOE_W13, self.x, c.D, None, self.ic1,
+                         c.n13 * c.F13, self.ws, self.ws_bytes)
+
+    def w2(self):
+        c = self.case
+        L.lora_moe_apply(self.pool, self.mb.meta, L.MOE_W2, self.ic2, c.F, self.topk_w, self.ic3, c.D,
+                         self.ws, self.ws_bytes)
+
+    def step(self):
+        self.build_meta()
+        self.w13()
+        self.w2()
+
+    def status(self) -> int:
+        return L.lora_get_device_status(self.pool)
+
+    def close(self):
+        if self.pool:
+            L.lora_pool_destroy(self.pool)
+            self.pool = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,281 @@
+/*
+ * liblora_gb300 -- multi-tenant LoRA delta on one GB300 (sm_103a), C ABI.
+ *
+ * For a batch whose rows (tokens, or (token, k) pairs after top-k routing)
+ * each carry an adapter slot a (-1 = none) the library adds, in place,
+ *
+ *     y[t][off_j + o] += scale[a] * sum_k ( sum_h x[t][h] * A_j[a][k][h] ) * B_j[a][o][k]
+ *
+ * for every packed output slice j, k < rank[a].  This is the shrink
+ * (x -> rank, fp32) / expand (rank -> out, added into y) pair of the vLLM LoRA
+ * layer pages (RowParallelLinearWithShardedLoRA.apply: zeroed fp32 buffer
+ * [n_slices][T][rank], add_shrink with scale 1.0, add_expand with
+ * add_input=True at the slice offsets), for packed column layers (QKV,
+ * gate_up; MergedColumnParallelLinearWithLoRA, MergedQKVParallelLinearWithLoRA),
+ * row/replicated layers and lm_head (LogitsProcessorWithLoRA, add_lora_logits),
+ * and for the fused-MoE per-(adapter, expert) variant (FusedMoEWithLoRA,
+ * add_lora_fused_moe) including the shared-outer layout of the Inkling LoRA
+ * PR report.
+ *
+ * Conventions common to every entry point
+ *  - Every call is asynchronous on `stream` (a cudaStream_t, NULL = the legacy
+ *    default stream).  Only lora_get_device_status and lora_pool_destroy
+ *    synchronise.  Calls that take only device pointers launch kernels and
+ *    cudaMemsetAsync/cudaMemcpyAsync only, so they can be captured in a CUDA
+ *    graph.
+ *  - bf16 tensors are passed as `void *` (2-byte elements, row-major).  All
+ *    device tensors given to compute calls must be 16-byte aligned and their
+ *    leading dimensions (in elements) multiples of 8.
+ *  - Host-checked argument errors return synchronously and launch nothing.
+ *    No call throws, traps or asserts on the device.  Bad adapter indices seen
+ *    on the device set the pool's status word (LORA_ERR_DEVICE_INDEX) and the
+ *    row is treated as idx -1; a cross-CTA wait that runs out of iterations
+ *    sets LORA_ERR_TIMEOUT.  Read and clear it with lora_get_device_status.
+ *  - A row is *active* when 0 <= idx < max_loras, the slot is enabled and its
+ *    rank is > 0 (and, for MoE, its expert id is in range).  Inactive rows of
+ *    y / ic1 / ic3 are left bit-identical.
+ */
+#ifndef LORA_GB300_H
+#define LORA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define LORA_API __attribute__((visibility("default")))
+#else
+#define LORA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    LORA_OK = 0,
+    LORA_ERR_INVALID_ARG = 1,   /* null pointer, bad alignment, bad size */
+    LORA_ERR_INDEX = 2,         /* slot outside [0, max_loras) */
+    LORA_ERR_RANK = 3,          /* rank < 0 or rank > max_rank (SGLang validate_new_adapter) */
+    LORA_ERR_SHAPE = 4,         /* dims/expert count do not match the pool; vocab > 257024 */
+    LORA_ERR_LAYOUT = 5,        /* shared-outer pool given per-expert A/B or the reverse */
+    LORA_ERR_NOMEM = 6,         /* device allocation failed */
+    LORA_ERR_CUDA = 7,          /* a CUDA runtime call failed */
+    LORA_ERR_DEVICE_INDEX = 8,  /* (device status) idx or expert id out of range was seen */
+    LORA_ERR_TIMEOUT = 9,       /* (device status) a bounded cross-CTA wait gave up */
+    LORA_ERR_CAPACITY = 10,     /* meta/workspace buffer too small for the call */
+    LORA_ERR_UNSUPPORTED = 11   /* call does not apply to this pool kind */
+} lora_status_t;
+
+#define LORA_MAX_SLICES 8
+#define LORA_MAX_RANK 256
+#define LORA_MAX_VOCAB 257024
+#define LORA_TILE_ROWS 16
+
+/* ------------------------------------------------------------------ pool */
+
+/* Shape of one LoRA-wrapped layer (create_lora_weights of the pages).
+ * Dense pool (num_experts == 0): n_slices packed output slices of widths
+ *   out_dims[j] over one input of width in_dim.  lm_head is n_slices = 1 with
+ *   out_dims[0] = vocab and is_lm_head = 1 (vocab <= 257024; the pages' guard
+ *   in LogitsProcessorWithLoRA.create_lora_weights, read as "reject only
+ *   vocab > 257024").
+ * MoE pool (num_experts > 0): w13 has n_w13_slices (2 = gate and up as in
+ *   FusedMoEWithLoRA; 1 = non-gated or the FusedMoE3DWithLoRA layout) slices
+ *   of width w13_slice_width (d_mlp, or 2*d_mlp for the 3D layout) over input
+ *   d_model; w2 maps d_mlp -> d_model.  shared_outer = 1 gives w13-A and w2-B
+ *   an expert dimension of 1 (enable_moe_shared_loras of the Inkling report).
+ * Every width must be a positive multiple of 8. */
+typedef struct {
+    int32_t max_loras;                  /* L >= 1 */
+    int32_t max_rank;                   /* R in [1, LORA_MAX_RANK] */
+    int32_t in_dim;                     /* dense: H */
+    int32_t n_slices;                   /* dense: 1..LORA_MAX_SLICES */
+    int32_t out_dims[LORA_MAX_SLICES];  /* dense: widths O_j */
+    int32_t is_lm_head;                 /* dense: apply the vocab guard */
+    int32_t num_experts;                /* 0 = dense; MoE: E >= 1 */
+    int32_t d_model;                    /* MoE: D */
+    int32_t d_mlp;                      /* MoE: F (w2 input width) */
+    int32_t n_w13_slices;               /* MoE: 1 or 2 */
+    int32_t w13_slice_width;            /* MoE: width of one w13 slice */
+    int32_t shared_outer;               /* MoE: 0 or 1 */
+} lora_pool_desc_t;
+
+typedef struct lora_pool lora_pool_t;   /* opaque; owns the stacked weights and tables */
+
+/* Allocate a zeroed pool on the current device (every slot reset: zero
+ * weights, rank 0, disabled).  The pool owns its device memory; it keeps its
+ * weights in its own layout (A rows [R][in], B compact [out][ceil8(rank)]).
+ * Errors: LORA_ERR_INVALID_ARG, LORA_ERR_SHAPE, LORA_ERR_NOMEM, LORA_ERR_CUDA. */
+LORA_API lora_status_t lora_pool_create(const lora_pool_desc_t *desc, void *stream, lora_pool_t **out);
+
+/* Synchronise the device and free the pool. */
+LORA_API lora_status_t lora_pool_destroy(lora_pool_t *pool);
+
+/* Copy the descriptor the pool was created with. */
+LORA_API lora_status_t lora_pool_get_desc(const lora_pool_t *pool, lora_pool_desc_t *out);
+
+/* set_lora of a dense pool (MergedColumnParallelLinearWithLoRA.set_lora):
+ * reset the slot, then copy A[j] ([rank][in_dim] bf16, row-major) and B[j]
+ * ([out_dims[j]][rank] bf16) for j < n (n == n_slices); a NULL pair leaves
+ * that slice zero.  Sources may be host or device memory (cudaMemcpyDefault);
+ * host sources must stay valid until the stream reaches the copy.  Sets
+ * rank, scale and enabled = 1.  Errors: LORA_ERR_INDEX (slot), LORA_ERR_RANK
+ * (rank > max_rank or < 0), LORA_ERR_SHAPE (n != n_slices),
+ * LORA_ERR_UNSUPPORTED (MoE pool). */
+LORA_API lora_status_t lora_set(lora_pool_t *pool, int32_t slot, int32_t rank, float scale,
+                       const void *const *A, const void *const *B, int32_t n, void *stream);
+
+/* set_lora of MergedColumnParallelLinearVariableSliceWithLoRA (one checkpoint
+ * tensor for a layer with packed slices): A ([rank][in_dim]) is duplicated to
+ * every slice and B ([sum_j out_dims[j]][rank]) is split along its rows by
+ * the slice widths.  Errors as lora_set. */
+LORA_API lora_status_t lora_set_packed(lora_pool_t *pool, int32_t slot, int32_t rank, float scale,
+                              const void *A, const void *B, void *stream);
+
+/* set_lora of a MoE pool (FusedMoEWithLoRA.set_lora): reset, enable, copy
+ *   A[s] = w13 A of slice s: [a_experts[s]][rank][d_model]          (s < n_w13_slices)
+ *   B[s] = w13 B of slice s: [b_experts[s]][w13_slice_width][rank]
+ *   A[n_w13_slices] = w2 A:  [a_experts[..]][rank][d_mlp]
+ *   B[n_w13_slices] = w2 B:  [b_experts[..]][d_model][rank]
+ * The expert counts must be E, except w13-A and w2-B which must be 1 in a
+ * shared-outer pool (LoRAManager._detect_shared_outer_loras: mixed formats
+ * are an error).  n must equal n_w13_slices + 1.
+ * Errors: LORA_ERR_INDEX, LORA_ERR_RANK, LORA_ERR_SHAPE (expert count or n),
+ * LORA_ERR_LAYOUT (1 where E is expected for w13-A/w2-B or the reverse),
+ * LORA_ERR_UNSUPPORTED (dense pool). */
+LORA_API lora_status_t lora_set_moe(lora_pool_t *pool, int32_t slot, int32_t rank, float scale,
+                           const void *const *A, const int32_t *a_experts,
+                           const void *const *B, const int32_t *b_experts, int32_t n,
+                           void *stream);
+
+/* reset_lora: zero every tensor of the slot, rank 0, scale 0, enabled 0.
+ * Errors: LORA_ERR_INDEX. */
+LORA_API lora_status_t lora_reset(lora_pool_t *pool, int32_t slot, void *stream);
+
+/* ------------------------------------------------------------- metadata */
+
+/* Batch metadata in caller-owned device memory (bind it with lora_meta_bind).
+ * A "row" is a token (dense) or a pair p = t*top_k + k (MoE); a "key" is the
+ * slot a (dense) or a*E + e (MoE).  After lora_build_meta:
+ *   sorted[max_rows]      rows stably sorted by key (keys ascending, rows in
+ *                         original order within a key); inactive rows last,
+ *                         in original order
+ *   key_count[max_keys]   active rows per key
+ *   key_offset[max_keys+1] exclusive prefix sum of key_count
+ *   group_key[max_keys]   the non-empty keys, ascending (one "group" each)
+ *   group_start[max_keys+1] first sorted position of each group; [n_groups] = n_active
+ *   key_group[max_keys]   group index of each key, -1 if empty
+ *   tile_group[max_tiles], tile_row0[max_tiles]: groups cut into tiles of at
+ *                         most LORA_TILE_ROWS rows, in group order
+ *   counters[4]           n_active, n_groups, n_bad, n_tiles
+ * The host fields T, top_k, n_keys and mode (0 dense, 1 MoE) record the last
+ * build.  Buffers stay valid until the next build into the same meta. */
+typedef struct {
+    int32_t max_rows;
+    int32_t max_keys;
+    int32_t max_tiles;
+    int32_t T, top_k, n_keys, mode, reserved;
+    int32_t *sorted;
+    int32_t *key_count;
+    int32_t *key_offset;
+    int32_t *group_key;
+    int32_t *group_start;
+    int32_t *key_group;
+    int32_t *tile_group;
+    int32_t *tile_row0;
+    int32_t *counters;
+} lora_meta_t;
+
+/* Device bytes lora_meta_bind needs for the given capacities. */
+LORA_API size_t lora_meta_bytes(int32_t max_rows, int32_t max_keys);
+
+/* Carve `d_buf` (device, 16-byte aligned, >= lora_meta_bytes) into the meta
+ * arrays.  Errors: LORA_ERR_INVALID_ARG, LORA_ERR_CAPACITY. */
+LORA_API lora_status_t lora_meta_bind(lora_meta_t *meta, void *d_buf, size_t bytes, int32_t max_rows,
+                             int32_t max_keys);
+
+/* Build the metadata on the device (one kernel, no host synchronisation,
+ * graph-capturable).  d_idx: [T] int32 slot per token (-1 = none).  Dense
+ * pool: d_topk_ids must be NULL.  MoE pool: d_topk_ids is [T][top_k] int32.
+ * Rows are counted against the pool's enabled/rank tables as they are on the
+ * stream at launch.  Errors: LORA_ERR_INVALID_ARG, LORA_ERR_CAPACITY
+ * (T*top_k > max_rows, keys > max_keys, or more than 12288 keys). */
+LORA_API lora_status_t lora_build_meta(const lora_pool_t *pool, const int32_t *d_idx, int32_t T,
+                              const int32_t *d_topk_ids, int32_t top_k, lora_meta_t *meta,
+                              void *stream);
+
+/* --------------------------------------------------------- dense compute */
+
+/* add_shrink (scale 1.0) of a dense pool into a zeroed buffer: v is
+ * [n_slices][T][max_rank] fp32 device and is overwritten; for every active
+ * token t with slot a and slice j, v[j][t][k] = sum_h x[t][h] A_j[a][k][h]
+ * for k < rank[a]; every other entry is 0.  The sum over h is split into
+ * chunks accumulated with fp32 atomics, so the last bit may vary between
+ * runs (lora_apply_slices is deterministic).  x: [T][ldx] bf16 device. */
+LORA_API lora_status_t lora_shrink(const lora_pool_t *pool, const lora_meta_t *meta, const void *x,
+                          int64_t ldx, float *v, void *stream);
+
+/* add_expand (add_input=True): for every active token t with slot a,
+ * y[t][off_j + o] += scale[a] * sum_{k<rank[a]} v[j][t][k] * B_j[a][o][k]
+ * with off_j the running sum of the slice widths; y: [T][ldy] bf16 device,
+ * fp32 accumulation, one rounding to bf16 per element. */
+LORA_API lora_status_t lora_expand(const lora_pool_t *pool, const lora_meta_t *meta, const float *v,
+                          void *y, int64_t ldy, void *stream);
+
+/* Workspace bytes for lora_apply_slices / lora_moe_apply on up to T tokens
+ * (top_k = 1 for a dense pool). */
+LORA_API size_t lora_workspace_bytes(const lora_pool_t *pool, int32_t T, int32_t top_k);
+
+/* Zero a workspace (a cudaMemsetAsync).  A workspace must be zero before its
+ * first use; every apply call leaves its control words zero again. */
+LORA_API lora_status_t lora_workspace_init(void *workspace, size_t bytes, void *stream);
+
+/* Shrink and expand of every slice in one persistent kernel (the fused
+ * apply of a LoRA linear layer: QKV, gate_up, o_proj/down_proj, lm_head):
+ * y += delta as in lora_expand.  The fp32 intermediate never leaves the
+ * workspace.  Calls that share a workspace must not overlap on the device.
+ * Errors: LORA_ERR_INVALID_ARG, LORA_ERR_CAPACITY (workspace too small),
+ * LORA_ERR_UNSUPPORTED (MoE pool). */
+LORA_API lora_status_t lora_apply_slices(const lora_pool_t *pool, const lora_meta_t *meta, const void *x,
+                                int64_t ldx, void *y, int64_t ldy, void *workspace,
+                                size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------ MoE compute */
+
+#define LORA_MOE_W13 0
+#define LORA_MOE_W2 1
+
+/* add_lora_fused_moe of a MoE pool after lora_build_meta with topk ids.
+ * W13: in = hidden states x [T][ld_in] (row t of pair p = p / top_k),
+ *      out = ic1 [T*top_k][ld_out], slice s written at columns
+ *      [s*w13_slice_width, (s+1)*w13_slice_width), before the activation:
+ *      ic1[p][s*W + o] += scale[a] * B13_s[a][e] (A13_s[a][e'] x[t]).
+ * W2:  in = ic2 [T*top_k][ld_in], out = ic3 [T*top_k][ld_out], before the
+ *      top-k sum: ic3[p][o] += topk_w[p] * scale[a] * B2[a][e''] (A2[a][e] ic2[p]);
+ *      topk_w is [T*top_k] fp32 device, NULL = 1.
+ * e' = 0 for w13-A and e'' = 0 for w2-B in a shared-outer pool, else e.
+ * Errors: LORA_ERR_INVALID_ARG, LORA_ERR_CAPACITY, LORA_ERR_UNSUPPORTED. */
+LORA_API lora_status_t lora_moe_apply(const lora_pool_t *pool, const lora_meta_t *meta, int32_t which,
+                             const void *in, int64_t ld_in, const float *topk_w, void *out,
+                             int64_t ld_out, void *workspace, size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------ status */
+
+/* Synchronise `stream`, return the pool's device status word (LORA_OK,
+ * LORA_ERR_DEVICE_INDEX or LORA_ERR_TIMEOUT) and clear it. */
+LORA_API lora_status_t lora_get_device_status(const lora_pool_t *pool, void *stream);
+
+/* Bound on the polls of every cross-CTA wait of lora_apply_slices and
+ * lora_moe_apply (default 1 << 20, each poll sleeps up to ~64 ns).  When a wait
+ * gives up, the device status becomes LORA_ERR_TIMEOUT and that work item is
+ * skipped.  A negative value makes every wait that is not already satisfied
+ * give up at once (to exercise the error path).  Process-wide. */
+LORA_API void lora_set_spin_limit(int32_t max_polls);
+
+/* Static string naming a status code. */
+LORA_API const char *lora_status_string(lora_status_t s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LORA_GB300_H */

@@ -1,0 +1,124 @@
+"""Metadata on the GPU must equal the oracle's bit for bit."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle
+from heterogeneous_adapters_lora_gb300 import harness as H
+from heterogeneous_adapters_lora_gb300 import inputs as gen
+from heterogeneous_adapters_lora_gb300 import lora as L
+from gpu_util import tiles_from_groups
+
+pytestmark = pytest.mark.gpu
+
+
+def _dense_pool(Lk, ranks, enabled=None):
+    d = L.PoolDesc()
+    d.max_loras, d.max_rank, d.in_dim, d.n_slices = Lk, 64, 64, 1
+    d.out_dims[0] = 64
+    pool = L.lora_pool_create(d)
+    for a in range(Lk):
+        r = int(ranks[a])
+        if r and (enabled is None or enabled[a]):
+            L.lora_set(pool, a, r, 1.0, [np.zeros((r, 64), np.uint16)], [np.zeros((64, r), np.uint16)])
+    return pool
+
+
+def _check_dense(idx, Lk, ranks, enabled):
+    T = len(idx)
+    pool = _dense_pool(Lk, ranks, enabled)
+    try:
+        mb = H.MetaBuffer(max(T, 1), Lk)
+        L.lora_build_meta(pool, torch.from_numpy(np.asarray(idx, np.int32)).cuda(), T, None, 1, mb.meta)
+        got = mb.read()
+        en = np.array([1 if (ranks[a] and (enabled is None or enabled[a])) else 0 for a in range(Lk)], np.int32)
+        ref = oracle.dense_meta(idx, Lk, en, ranks)
+        assert np.array_equal(got["sorted"], ref.sorted_tok)
+        assert got["n_active"] == ref.n_active
+        assert got["n_groups"] == ref.n_seg
+        assert got["n_bad"] == ref.n_bad
+        assert np.array_equal(got["key_count"], ref.slot_count)
+        assert np.array_equal(got["key_offset"], np.concatenate([[0], np.cumsum(ref.slot_count)]))
+        assert np.array_equal(got["group_key"], ref.seg_slot)
+        assert np.array_equal(got["group_start"], ref.seg_start)
+        assert np.array_equal(got["key_group"], ref.slot_seg)
+        tg, tr = tiles_from_groups(ref.seg_start)
+        assert got["n_tiles"] == len(tg)
+        assert np.array_equal(got["tile_group"], tg) and np.array_equal(got["tile_row0"], tr)
+        st = L.lora_get_device_status(pool)
+        assert st == (L.CODE["LORA_ERR_DEVICE_INDEX"] if ref.n_bad else 0)
+    finally:
+        L.lora_pool_destroy(pool)
+
+
+@pytest.mark.parametrize("preset", [1, 2, 3, 4])
+def test_dense_meta_presets(preset):
+    c = {1: gen.tiny, 2: gen.decode_qkv, 3: lambda: gen.prefill_gate_up(permuted=True),
+         4: gen.many_adapter_down}[preset]() if preset != 4 else None
+    if preset == 4:
+        # ranks and idx of the many-adapter preset without drawing its 2 GB pool
+        rng = np.random.Generator(np.random.PCG64(1004))
+        ranks = rng.choice(np.array([8, 16, 32, 64], np.int32), size=1024).astype(np.int32)
+        idx = rng.choice(1024, size=2048, p=gen.zipf_pmf(1024, 1.2)).astype(np.int32)
+        _check_dense(idx, 1024, ranks, None)
+    else:
+        _check_dense(c.idx, c.L, np.minimum(c.ranks, 64), None)
+
+
+@pytest.mark.parametrize("case", ["all_none", "one_token", "empty", "single_slot", "bad_and_disabled",
+                                  "big_skewed"])
+def test_dense_meta_edges(case):
+    rng = np.random.default_rng(7)
+    Lk, ranks, en = 16, np.full(16, 8, np.int32), None
+    if case == "all_none":
+        idx = np.full(300, -1, np.int32)
+    elif case == "one_token":
+        idx = np.array([3], np.int32)
+    elif case == "empty":
+        idx = np.zeros(0, np.int32)
+    elif case == "single_slot":
+        idx = np.full(1000, 5, np.int32)
+    elif case == "bad_and_disabled":
+        idx = rng.integers(-3, 20, size=777).astype(np.int32)
+        ranks = rng.choice([0, 8, 16], size=16).astype(np.int32)
+        en = (rng.random(16) < 0.7)
+    else:
+        idx = rng.choice(16, size=20000, p=gen.zipf_pmf(16, 1.5)).astype(np.int32)
+    _check_dense(idx, Lk, ranks, en)
+
+
+def test_moe_meta_preset_and_small():
+    for c in (gen.moe(), gen.moe_case(T=77, K=3, E=5, D=16, F=16, L=4, R=8, seed=3, p_none=0.2,
+                                      ranks=(8, 0, 8, 8))):
+        run = H.MoERun(c)
+        try:
+            run.build_meta()
+            got = run.mb.read()
+            ref = oracle.moe_meta(c.topk_ids, c.idx, c.L, c.E, c.enabled, c.ranks)
+            assert np.array_equal(got["sorted"], ref.sorted_pair)
+            assert got["n_active"] == ref.n_active and got["n_groups"] == ref.n_groups
+            assert got["n_bad"] == ref.n_bad
+            assert np.array_equal(got["key_count"], ref.key_count)
+            assert np.array_equal(got["key_offset"], ref.key_offset)
+            assert np.array_equal(got["group_key"], ref.group_key)
+            assert np.array_equal(got["group_start"], ref.group_start)
+            tg, tr = tiles_from_groups(ref.group_start)
+            assert np.array_equal(got["tile_group"], tg) and np.array_equal(got["tile_row0"], tr)
+        finally:
+            run.close()
+
+
+def test_meta_is_deterministic_across_runs():
+    c = gen.decode_qkv()
+    pool = _dense_pool(c.L, np.full(c.L, 16, np.int32))
+    try:
+        mb = H.MetaBuffer(c.T, c.L)
+        d_idx = torch.from_numpy(c.idx).cuda()
+        outs = []
+        for _ in range(3):
+            L.lora_build_meta(pool, d_idx, c.T, None, 1, mb.meta)
+            outs.append(mb.read()["sorted"].copy())
+        assert all(np.array_equal(outs[0], o) for o in outs[1:])
+    finally:
+        L.lora_pool_destroy(pool)

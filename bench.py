@@ -274,6 +274,22 @@ def load_peaks():
         return 6800.0, "fallback"
 
 
+def max_over_ranks(values, world, device=None):
+    """Element-wise maximum of per-rank timings (all ranks get the result)."""
+    if world <= 1:
+        return list(values)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_throughput(tokens_per_step, steps, world, ms):
+    """Tokens of every replica over the slowest rank's time (weak scaling)."""
+    return tokens_per_step * steps * world / (ms * 1e-3)
+
+
 def run_gpu(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -402,18 +418,15 @@ def run_gpu(args, rank, world, local_rank):
         stream.synchronize()
         e2e_ms = f0.elapsed_time(f1)
 
-    if world > 1:
-        t = torch.tensor([ms, e2e_ms, kms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, e2e_ms, kms = t.tolist()
+    ms, e2e_ms, kms = max_over_ranks([ms, e2e_ms, kms], world, dev)
     for r in runs:
         r.close()
     if rank != 0:
         return 0
 
     tokens = c.T
-    value = tokens * args.steps * world / (ms * 1e-3)
-    e2e = tokens * args.steps * world / (e2e_ms * 1e-3)
+    value = whole_job_throughput(tokens, args.steps, world, ms)
+    e2e = whole_job_throughput(tokens, args.steps, world, e2e_ms)
     peak, peak_kind = load_peaks()
     kbytes = (ab["w13"] + ab["w2"]) if moe else (ab["total"] - ab["idx"])
     achieved = kbytes / (kms * 1e-3) / 1e9

@@ -681,3 +681,66 @@ extern "C" lora_status_t lora_moe_apply(const lora_pool_t *pool, const lora_meta
     if (st != LORA_OK) return st;
     return launch<kFused>(pool, g, est_items(g, rows, keys, kFused), (cudaStream_t)stream);
 }
+
+// ------------------------------------------------------------------------
+// Allocation-free variant of lora_apply_slices.
+//
+// Some callers cannot hand the library a workspace: a serving engine that
+// has already reserved every free byte of HBM for its own pools (KV cache,
+// activations) so a further cudaMalloc would fail, a latency-critical path
+// that may not block on an allocation, or a plain C host with no allocator
+// to lend.  For them the fused kernel can run on a fixed scratch array that
+// lives in the library's device image instead.
+//
+// The array is a file-scope __device__ object of kStaticScratchBytes; every
+// GPU that loads this library holds it until the process exits.  Host code
+// must not pass the symbol itself to a kernel (on the host it only names a
+// shadow copy): the first call on each device, with that device current,
+// looks up its device address with cudaGetSymbolAddress and caches it.
+// That first call should therefore come before any stream capture.
+// All calls share the one array and it keeps the previous call's contents,
+// so each call clears the control words it needs at zero; calls that
+// overlap on the GPU (two streams, or two host threads) race on it.
+namespace {
+constexpr size_t kStaticScratchBytes = (size_t)8 << 20;  // 8 MiB
+__device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+void *g_static_scratch_addr[64];
+}  // namespace
+
+extern "C" lora_status_t lora_apply_slices_static(const lora_pool_t *pool, const lora_meta_t *meta,
+                                                  const void *x, int64_t ldx, void *y, int64_t ldy,
+                                                  void *stream) {
+    if (!pool) return LORA_ERR_INVALID_ARG;
+    GArgs g;
+    lora_status_t st = dense_args(pool, meta, g);
+    if (st != LORA_OK) return st;
+    if (meta->T == 0) return LORA_OK;
+    if (!x || !y || !lora_aligned16(x) || !lora_aligned16(y) || ldx % 8 || ldy % 8 ||
+        ldx < pool->desc.in_dim || ldy < out_total(pool))
+        return LORA_ERR_INVALID_ARG;
+    int dev = -1;
+    LORA_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev != pool->device || dev < 0 || dev >= 64) return LORA_ERR_INVALID_ARG;
+    if (!g_static_scratch_addr[dev]) {
+        void *addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, g_static_scratch) != cudaSuccess || !addr) return LORA_ERR_CUDA;
+        g_static_scratch_addr[dev] = addr;
+    }
+    void *scratch = g_static_scratch_addr[dev];
+    const Plan pl = fit_plan(make_plan(pool->num_sms, g.in_dim, g.n_slices, g.R, meta->T,
+                                       pool->desc.max_loras),
+                             g.in_dim, g.n_slices, g.R, meta->T, kStaticScratchBytes);
+    if (ws_bytes_for(pl) > kStaticScratchBytes) return LORA_ERR_CAPACITY;
+    st = bind_workspace(g, pl, scratch, kStaticScratchBytes);
+    if (st != LORA_OK) return st;
+    // ticket, finish count and per-tile counters must start at zero
+    LORA_CUDA_TRY(cudaMemsetAsync(scratch, 0, kCtrlBytes + pl.cnt_ints * 4, (cudaStream_t)stream));
+    g.in = (const uint16_t *)x;
+    g.ld_in = ldx;
+    g.out = (uint16_t *)y;
+    g.ld_out = ldy;
+    return launch<kFused>(pool, g, est_items(g, meta->T, pool->desc.max_loras, kFused),
+                          (cudaStream_t)stream);
+}
+
+extern "C" size_t lora_static_scratch_bytes(void) { return kStaticScratchBytes; }

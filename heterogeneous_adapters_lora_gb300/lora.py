@@ -79,6 +79,8 @@ EXPORTS = {
     "lora_workspace_init": (c_i32, [c_vp, c_size, c_vp]),
     "lora_apply_slices": (c_i32, [c_vp, ctypes.POINTER(Meta), c_vp, c_i64, c_vp, c_i64, c_vp, c_size,
                                   c_vp]),
+    "lora_apply_slices_static": (c_i32, [c_vp, ctypes.POINTER(Meta), c_vp, c_i64, c_vp, c_i64, c_vp]),
+    "lora_static_scratch_bytes": (c_size, []),
     "lora_moe_apply": (c_i32, [c_vp, ctypes.POINTER(Meta), c_i32, c_vp, c_i64, c_vp, c_vp, c_i64, c_vp,
                                c_size, c_vp]),
     "lora_get_device_status": (c_i32, [c_vp, c_vp]),
@@ -212,6 +214,15 @@ def lora_workspace_init(ws, nbytes, stream=None):
 def lora_apply_slices(pool, meta: Meta, x, ldx, y, ldy, ws, ws_bytes, stream=None):
     _check(lib().lora_apply_slices(pool, ctypes.byref(meta), ptr(x), ldx, ptr(y), ldy, ptr(ws), ws_bytes,
                                    stream_ptr(stream)), "lora_apply_slices")
+
+
+def lora_apply_slices_static(pool, meta: Meta, x, ldx, y, ldy, stream=None):
+    _check(lib().lora_apply_slices_static(pool, ctypes.byref(meta), ptr(x), ldx, ptr(y), ldy,
+                                          stream_ptr(stream)), "lora_apply_slices_static")
+
+
+def lora_static_scratch_bytes() -> int:
+    return int(lib().lora_static_scratch_bytes())
 
 
 def lora_moe_apply(pool, meta: Meta, which, inp, ld_in, topk_w, out, ld_out, ws, ws_bytes, stream=None):

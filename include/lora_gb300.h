@@ -240,6 +240,28 @@ LORA_API lora_status_t lora_apply_slices(const lora_pool_t *pool, const lora_met
                                 int64_t ldx, void *y, int64_t ldy, void *workspace,
                                 size_t ws_bytes, void *stream);
 
+/* Same result as lora_apply_slices, but for callers that cannot provide a
+ * workspace: the library allocates nothing and uses one fixed scratch array
+ * in its own device image (lora_static_scratch_bytes() bytes, 8 MiB, held on
+ * every GPU that loads the library until the process exits).  This is for
+ * hosts whose device memory is fully reserved by another allocator (so
+ * cudaMalloc would fail), latency-critical paths that may not block on an
+ * allocation, and C callers with no allocator to lend.  It has no
+ * counterpart in the LoRA layer pages; it is a deployment convenience of
+ * this library.
+ * The first call on a device (with that device current) looks up the array's
+ * device address; make that first call before any stream capture.  All calls
+ * share the array, each call clears the control words it needs, and calls
+ * that overlap on the GPU race.  Errors as lora_apply_slices, plus
+ * LORA_ERR_CAPACITY when the batch needs more scratch than the array holds
+ * and LORA_ERR_CUDA if the address lookup fails. */
+LORA_API lora_status_t lora_apply_slices_static(const lora_pool_t *pool, const lora_meta_t *meta,
+                                                const void *x, int64_t ldx, void *y, int64_t ldy,
+                                                void *stream);
+
+/* Size in bytes of the fixed scratch array used by lora_apply_slices_static. */
+LORA_API size_t lora_static_scratch_bytes(void);
+
 /* ------------------------------------------------------------ MoE compute */
 
 #define LORA_MOE_W13 0

@@ -46,7 +46,8 @@ struct GArgs {
     int B_shared[LORA_MAX_SLICES];
     const int32_t *rank;
     const float *scale;
-    const int32_t *sorted, *group_key, *group_start, *tile_group, *tile_row0, *counters;
+    const int32_t *sorted, *tile_row0, *tile_keyn, *counters;
+    int count_idx;  // counters[count_idx] = number of tiles in the list
     const uint16_t *in;
     long long ld_in;
     uint16_t *out;
@@ -66,10 +67,10 @@ struct TileInfo {
 
 __device__ __forceinline__ TileInfo tile_info(const GArgs &p, int tile) {
     TileInfo ti;
-    const int g = p.tile_group[tile];
     ti.row0 = p.tile_row0[tile];
-    ti.n = min(kTile, p.group_start[g + 1] - ti.row0);
-    const int key = p.group_key[g];
+    const int keyn = p.tile_keyn[tile];
+    ti.n = keyn & 31;
+    const int key = keyn >> 5;
     ti.a = key / p.E;
     ti.e = key - ti.a * p.E;
     ti.r = p.rank[ti.a];
@@ -333,7 +334,7 @@ template <int MODE>
 __global__ void __launch_bounds__(kThreads) grouped_lora_kernel(const __grid_constant__ GArgs p) {
     extern __shared__ __align__(16) char smem[];
     __shared__ int s_item, s_flag, s_last;
-    const int n_tiles = p.counters[3];
+    const int n_tiles = p.counters[p.count_idx];
     const int n_sh = (MODE == kExpandOnly) ? 0 : n_tiles * p.n_slices * p.NC;
     const int n_ex = (MODE == kShrinkAtomic) ? 0 : n_tiles * p.och_start[p.n_slices];
     const int total = n_sh + n_ex;
@@ -470,10 +471,9 @@ lora_status_t dense_args(const lora_pool_t *pool, const lora_meta_t *meta, GArgs
     g.rank = pool->d_rank;
     g.scale = pool->d_scale;
     g.sorted = meta->sorted;
-    g.group_key = meta->group_key;
-    g.group_start = meta->group_start;
-    g.tile_group = meta->tile_group;
     g.tile_row0 = meta->tile_row0;
+    g.tile_keyn = meta->tile_keyn;
+    g.count_idx = 3;
     g.counters = meta->counters;
     g.status = pool->d_status;
     g.rows = meta->T;
@@ -509,6 +509,12 @@ lora_status_t bind_workspace(GArgs &g, const Plan &pl, void *ws, size_t ws_bytes
     return LORA_OK;
 }
 
+// The tensor-core path's bf16 hi/lo rank buffer sits after the split-K region.
+size_t sgmv_region_bytes(const lora_pool_t *pool, int T) {
+    if (pool->is_moe || pool->desc.max_rank != 64) return 0;
+    return (lora_sgmv_ws_bytes(pool, T) + 1023) & ~(size_t)1023;
+}
+
 long long est_items(const GArgs &g, int rows, int n_keys, int mode) {
     const long long tiles = (rows + kTile - 1) / kTile + (rows < n_keys ? rows : n_keys);
     long long n = 0;
@@ -517,7 +523,48 @@ long long est_items(const GArgs &g, int rows, int n_keys, int mode) {
     return n;
 }
 
+LoraProblem to_problem(const GArgs &g, const lora_meta_t *meta, int n_keys) {
+    LoraProblem pr;
+    memset(&pr, 0, sizeof(pr));
+    pr.n_slices = g.n_slices;
+    pr.in_dim = g.in_dim;
+    pr.E = g.E;
+    pr.row_div = g.row_div;
+    pr.R = g.R;
+    pr.T = g.T;
+    pr.rows = g.rows;
+    pr.n_keys = n_keys;
+    for (int j = 0; j < g.n_slices; ++j) {
+        pr.out_w[j] = g.out_w[j];
+        pr.out_off[j] = g.out_off[j];
+        pr.A[j] = g.A[j];
+        pr.A_ss[j] = g.A_ss[j];
+        pr.A_es[j] = g.A_es[j];
+        pr.B[j] = g.B[j];
+        pr.B_ss[j] = g.B_ss[j];
+        pr.B_shared[j] = g.B_shared[j];
+    }
+    pr.rank = g.rank;
+    pr.scale = g.scale;
+    pr.meta = meta;
+    pr.tile_row0 = g.tile_row0;
+    pr.tile_keyn = g.tile_keyn;
+    pr.count_idx = g.count_idx;
+    pr.in = g.in;
+    pr.ld_in = g.ld_in;
+    pr.out = g.out;
+    pr.ld_out = g.ld_out;
+    pr.row_w = g.row_w;
+    pr.status = g.status;
+    pr.spin_limit = g_spin_limit;
+    return pr;
+}
+
 }  // namespace
+
+int g_lora_kernel_policy = 0;
+
+extern "C" void lora_set_kernel_policy(int32_t policy) { g_lora_kernel_policy = policy; }
 
 extern "C" void lora_set_spin_limit(int32_t max_polls) { g_spin_limit = max_polls; }
 
@@ -526,7 +573,7 @@ extern "C" size_t lora_workspace_bytes(const lora_pool_t *pool, int32_t T, int32
     const lora_pool_desc_t &d = pool->desc;
     if (!pool->is_moe) {
         const Plan pl = make_plan(pool->num_sms, d.in_dim, d.n_slices, d.max_rank, T, d.max_loras);
-        return ws_bytes_for(pl);
+        return ws_bytes_for(pl) + sgmv_region_bytes(pool, T);
     }
     if (top_k < 1) return 0;
     const int rows = T * top_k, keys = d.max_loras * d.num_experts;
@@ -553,17 +600,36 @@ extern "C" lora_status_t lora_apply_slices(const lora_pool_t *pool, const lora_m
     if (!x || !y || !lora_aligned16(x) || !lora_aligned16(y) || ldx % 8 || ldy % 8 ||
         ldx < pool->desc.in_dim || ldy < out_total(pool))
         return LORA_ERR_INVALID_ARG;
+    // workspace: [bf16 hi/lo rank buffer of the tensor-core path (1 KB aligned)][split-K region]
+    const size_t sg_bytes = sgmv_region_bytes(pool, meta->T);
+    const bool use_sgmv = g_lora_kernel_policy == 0 && sg_bytes > 0 && meta->T >= LORA_LONG_MIN &&
+                          ws_bytes > sg_bytes && lora_aligned16(workspace) && lora_sgmv_eligible(pool);
+    const size_t ws_splitk = use_sgmv ? ws_bytes - sg_bytes : ws_bytes;
+    void *ws_sk = use_sgmv ? (void *)((char *)workspace + sg_bytes) : workspace;
     const Plan pl = fit_plan(make_plan(pool->num_sms, g.in_dim, g.n_slices, g.R, meta->T,
                                        pool->desc.max_loras),
-                             g.in_dim, g.n_slices, g.R, meta->T, ws_bytes);
-    st = bind_workspace(g, pl, workspace, ws_bytes);
+                             g.in_dim, g.n_slices, g.R, meta->T, ws_splitk);
+    st = bind_workspace(g, pl, ws_sk, ws_splitk);
     if (st != LORA_OK) return st;
     g.in = (const uint16_t *)x;
     g.ld_in = ldx;
     g.out = (uint16_t *)y;
     g.ld_out = ldy;
-    return launch<kFused>(pool, g, est_items(g, meta->T, pool->desc.max_loras, kFused),
-                          (cudaStream_t)stream);
+    cudaStream_t s = (cudaStream_t)stream;
+    if (use_sgmv) {
+        // long contiguous runs on tcgen05; the remaining groups' 16-row tiles below
+        st = lora_sgmv_apply(pool, meta, x, ldx, y, ldy, workspace, g_spin_limit, pool->num_sms, s);
+        if (st != LORA_OK) return st;
+        g.tile_row0 = meta->stile_row0;
+        g.tile_keyn = meta->stile_keyn;
+        g.count_idx = 4;
+    }
+    if (g_lora_kernel_policy == 0) {
+        bool launched = false;
+        st = lora_cluster_apply(pool, to_problem(g, meta, pool->desc.max_loras), s, &launched);
+        if (st != LORA_OK || launched) return st;
+    }
+    return launch<kFused>(pool, g, est_items(g, meta->T, pool->desc.max_loras, kFused), s);
 }
 
 extern "C" lora_status_t lora_shrink(const lora_pool_t *pool, const lora_meta_t *meta,
@@ -664,10 +730,9 @@ extern "C" lora_status_t lora_moe_apply(const lora_pool_t *pool, const lora_meta
     g.rank = pool->d_rank;
     g.scale = pool->d_scale;
     g.sorted = meta->sorted;
-    g.group_key = meta->group_key;
-    g.group_start = meta->group_start;
-    g.tile_group = meta->tile_group;
     g.tile_row0 = meta->tile_row0;
+    g.tile_keyn = meta->tile_keyn;
+    g.count_idx = 3;
     g.counters = meta->counters;
     g.status = pool->d_status;
     g.in = (const uint16_t *)in;
@@ -679,6 +744,11 @@ extern "C" lora_status_t lora_moe_apply(const lora_pool_t *pool, const lora_meta
                              g.n_slices, g.R, rows, ws_bytes);
     lora_status_t st = bind_workspace(g, pl, workspace, ws_bytes);
     if (st != LORA_OK) return st;
+    if (g_lora_kernel_policy == 0) {
+        bool launched = false;
+        st = lora_cluster_apply(pool, to_problem(g, meta, keys), (cudaStream_t)stream, &launched);
+        if (st != LORA_OK || launched) return st;
+    }
     return launch<kFused>(pool, g, est_items(g, rows, keys, kFused), (cudaStream_t)stream);
 }
 

@@ -81,3 +81,41 @@ static inline bool lora_aligned16(const void *p) { return (((uintptr_t)p) & 15u)
 lora_status_t lora_launch_build_meta(const lora_pool_t *pool, const int32_t *d_idx, int32_t T,
                                      const int32_t *d_topk, int32_t top_k, lora_meta_t *meta,
                                      cudaStream_t stream);
+
+// One grouped LoRA problem (a dense layer, or one MoE projection) as the
+// compute kernels see it.  Rows are the sorted entries of the metadata.
+struct LoraProblem {
+    int n_slices, in_dim, E, row_div, R, T, rows, n_keys;
+    int out_w[LORA_MAX_SLICES], out_off[LORA_MAX_SLICES];
+    const uint16_t *A[LORA_MAX_SLICES];
+    long long A_ss[LORA_MAX_SLICES], A_es[LORA_MAX_SLICES];
+    const uint16_t *B[LORA_MAX_SLICES];
+    long long B_ss[LORA_MAX_SLICES];
+    int B_shared[LORA_MAX_SLICES];
+    const int32_t *rank;
+    const float *scale;
+    const lora_meta_t *meta;
+    const int32_t *tile_row0, *tile_keyn;  // tile list the kernel walks
+    int count_idx;                          // meta counter holding its length
+    const uint16_t *in;
+    long long ld_in;
+    uint16_t *out;
+    long long ld_out;
+    const float *row_w;
+    int *status;
+    int spin_limit;
+};
+
+// Cluster kernel (cluster.cu): launches and sets *launched when the shape
+// fits its shared-memory plan; otherwise leaves *launched false.
+lora_status_t lora_cluster_apply(const lora_pool_t *pool, const LoraProblem &pr, cudaStream_t s,
+                                 bool *launched);
+
+// Kernel selection policy (0 = automatic, 1 = split-K kernel only).
+extern int g_lora_kernel_policy;
+
+// Tensor-core SGMV (sgmv.cu) for long contiguous runs of a dense pool.
+bool lora_sgmv_eligible(const lora_pool_t *pool);
+size_t lora_sgmv_ws_bytes(const lora_pool_t *pool, int rows);
+lora_status_t lora_sgmv_apply(const lora_pool_t *pool, const lora_meta_t *meta, const void *x, int64_t ldx,
+                              void *y, int64_t ldy, void *V, int spin_limit, int num_sms, cudaStream_t s);

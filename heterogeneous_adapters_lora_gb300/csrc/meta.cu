@@ -25,14 +25,15 @@ struct MetaArgs {
     const int32_t *rank;
     const int32_t *enabled;
     int32_t *status;
-    int T, K, E, L, n_keys, n_chunks;
+    int T, K, E, L, n_keys, n_chunks, cache_keys;
     lora_meta_t m;
 };
 
 // Exclusive scan of data[0..n) in shared memory; returns the total.
 __device__ int block_exclusive_scan(int *data, int n, int *warp_tot) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int per = (n + kThreads - 1) / kThreads;
+    const int nthreads = blockDim.x, nwarps = nthreads >> 5;
+    const int per = (n + nthreads - 1) / nthreads;
     const int b = min(n, tid * per), e = min(n, b + per);
     int local = 0;
     for (int i = b; i < e; ++i) local += data[i];
@@ -45,7 +46,7 @@ __device__ int block_exclusive_scan(int *data, int n, int *warp_tot) {
     if (lane == 31) warp_tot[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-        int w = warp_tot[lane];
+        int w = lane < nwarps ? warp_tot[lane] : 0;
         int wi = w;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -67,19 +68,19 @@ __device__ int block_exclusive_scan(int *data, int n, int *warp_tot) {
     return total;
 }
 
-__device__ __forceinline__ int row_key(const MetaArgs &a, int row, int *bad) {
-    const int t = row / a.K;
-    const int s = a.idx[t];
+// Key of one row given the slot-activity table in shared memory.
+__device__ __forceinline__ int row_key(const MetaArgs &a, const unsigned char *act, int row, int s,
+                                       int *bad) {
     const bool valid = s >= 0 && s < a.L;
     int b = (s != -1 && !valid && (row % a.K) == 0) ? 1 : 0;
-    bool act = valid && a.enabled[s] != 0 && a.rank[s] > 0;
+    const bool on = valid && act[s];
     int key = a.n_keys;
     if (a.topk) {
         const int e = a.topk[row];
         const bool ev = e >= 0 && e < a.E;
         b += ev ? 0 : 1;
-        if (act && ev) key = s * a.E + e;
-    } else if (act) {
+        if (on && ev) key = s * a.E + e;
+    } else if (on) {
         key = s;
     }
     *bad += b;
@@ -89,27 +90,49 @@ __device__ __forceinline__ int row_key(const MetaArgs &a, int row, int *bad) {
 __global__ void __launch_bounds__(kThreads, 1) build_meta_kernel(MetaArgs a) {
     extern __shared__ int sm[];
     const int NK = a.n_keys, NK1 = NK + 1, W = a.n_chunks;
-    int *hist = sm;                 // [W][NK1]
-    int *cnt = hist + W * NK1;      // [NK1]
-    int *off = cnt + NK1;           // [NK1]
-    int *misc = off + NK1;          // [40]: warp totals(33), n_bad
+    int *hist = sm;                  // [W][NK1]
+    int *cnt = hist + W * NK1;       // [NK1]
+    int *off = cnt + NK1;            // [NK1]
+    int *tmin = off + NK1;           // [NK1] smallest token of each key (dense)
+    int *tmax = tmin + NK1;          // [NK1] largest token of each key (dense)
+    int *misc = tmax + NK1;          // [40]: warp totals (33), n_bad at [36]
+    unsigned char *act = (unsigned char *)(misc + 40);  // [L] slot enabled and rank > 0
+    int *kc = misc + 40 + (a.L + 3) / 4;                // [rows] keys of pass 1 when cached
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nthreads = blockDim.x;
     const int rows = a.T * a.K;
+    // let the apply kernel that follows start its prologue; it waits for
+    // this grid's completion before reading any metadata
+    asm volatile("griddepcontrol.launch_dependents;");
 
-    for (int i = tid; i < W * NK1; i += kThreads) hist[i] = 0;
+    // issue the first row step's slot loads together with the table loads
+    const int chunk = (rows + W - 1) / W;
+    const int r0 = warp * chunk, r1 = min(rows, r0 + chunk);
+    int s_first = -1;
+    if (warp < W && r0 + lane < r1) s_first = a.idx[(r0 + lane) / a.K];
+    for (int i = tid; i < a.L; i += nthreads) act[i] = (a.enabled[i] != 0 && a.rank[i] > 0) ? 1 : 0;
+    for (int i = tid; i < W * NK1; i += nthreads) hist[i] = 0;
+    for (int i = tid; i < NK1; i += nthreads) {
+        tmin[i] = 0x7fffffff;
+        tmax[i] = -1;
+    }
     if (tid == 0) misc[36] = 0;
     __syncthreads();
 
-    const int chunk = (rows + W - 1) / W;
     if (warp < W) {
-        const int r0 = warp * chunk, r1 = min(rows, r0 + chunk);
         int bad = 0;
         for (int base = r0; base < r1; base += 32) {
             const int row = base + lane;
             const bool v = row < r1;
-            const int key = v ? row_key(a, row, &bad) : -1;
+            const int s = base == r0 ? s_first : (v ? a.idx[row / a.K] : -1);
+            const int key = v ? row_key(a, act, row, s, &bad) : -1;
+            if (v && a.cache_keys) kc[row] = key;
             const unsigned peers = __match_any_sync(0xffffffffu, key);
             if (v && lane == __ffs(peers) - 1) hist[warp * NK1 + key] += __popc(peers);
+            if (v && a.K == 1 && key < NK) {
+                atomicMin(&tmin[key], row);
+                atomicMax(&tmax[key], row);
+            }
             __syncwarp();
         }
 #pragma unroll
@@ -118,7 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1) build_meta_kernel(MetaArgs a) {
     }
     __syncthreads();
 
-    for (int b = tid; b < NK1; b += kThreads) {
+    for (int b = tid; b < NK1; b += nthreads) {
         int run = 0;
         for (int w = 0; w < W; ++w) {
             const int c = hist[w * NK1 + b];
@@ -130,24 +153,29 @@ __global__ void __launch_bounds__(kThreads, 1) build_meta_kernel(MetaArgs a) {
     }
     __syncthreads();
     block_exclusive_scan(off, NK1, misc);
-    for (int b = tid; b < NK1; b += kThreads) {
+    for (int b = tid; b < NK1; b += nthreads) {
         const int o = off[b];
         for (int w = 0; w < W; ++w) hist[w * NK1 + b] += o;
-        if (b < NK) {
-            a.m.key_count[b] = cnt[b];
-        }
+        if (b < NK) a.m.key_count[b] = cnt[b];
         a.m.key_offset[b] = o;
     }
     __syncthreads();
 
+    // stable scatter: position = key offset + rows of earlier chunks + earlier lanes
     if (warp < W) {
-        const int r0 = warp * chunk, r1 = min(rows, r0 + chunk);
         const unsigned lt = (1u << lane) - 1u;
         for (int base = r0; base < r1; base += 32) {
             const int row = base + lane;
             const bool v = row < r1;
-            int dummy = 0;
-            const int key = v ? row_key(a, row, &dummy) : -1;
+            int key = -1;
+            if (v) {
+                if (a.cache_keys) {
+                    key = kc[row];
+                } else {
+                    int dummy = 0;
+                    key = row_key(a, act, row, a.idx[row / a.K], &dummy);
+                }
+            }
             const unsigned peers = __match_any_sync(0xffffffffu, key);
             int pos = 0;
             if (v) pos = hist[warp * NK1 + key] + __popc(peers & lt);
@@ -161,18 +189,19 @@ __global__ void __launch_bounds__(kThreads, 1) build_meta_kernel(MetaArgs a) {
     }
     __syncthreads();
 
-    // groups: non-empty keys in ascending order
-    int *gidx = hist;             // [NK1] reuse
-    int *tiles = hist + NK1;      // [NK1]
-    for (int b = tid; b < NK1; b += kThreads) {
-        const bool ne = b < NK && cnt[b] > 0;
-        gidx[b] = ne ? 1 : 0;
-        tiles[b] = ne ? (cnt[b] + LORA_TILE_ROWS - 1) / LORA_TILE_ROWS : 0;
+    // groups (non-empty keys, ascending), 16-row tiles, and the long/short split:
+    // a dense group of >= LORA_LONG_MIN rows whose distinct tokens span exactly
+    // its row count is one contiguous run, cut into 128-row tiles
+    int *gidx = hist, *tiles = hist + NK1;  // reuse of the histogram rows (W >= 2)
+    for (int b = tid; b < NK1; b += nthreads) {
+        const int c = b < NK ? cnt[b] : 0;
+        gidx[b] = c > 0 ? 1 : 0;
+        tiles[b] = (c + LORA_TILE_ROWS - 1) / LORA_TILE_ROWS;
     }
     __syncthreads();
     const int G = block_exclusive_scan(gidx, NK1, misc);
     const int NT = block_exclusive_scan(tiles, NK1, misc);
-    for (int b = tid; b < NK; b += kThreads) {
+    for (int b = tid; b < NK; b += nthreads) {
         const int c = cnt[b];
         if (c > 0) {
             const int g = gidx[b];
@@ -181,16 +210,51 @@ __global__ void __launch_bounds__(kThreads, 1) build_meta_kernel(MetaArgs a) {
             a.m.group_start[g] = off[b];
             const int nt = (c + LORA_TILE_ROWS - 1) / LORA_TILE_ROWS;
             for (int i = 0; i < nt; ++i) {
+                const int rows_i = min(LORA_TILE_ROWS, c - i * LORA_TILE_ROWS);
                 a.m.tile_group[tiles[b] + i] = g;
                 a.m.tile_row0[tiles[b] + i] = off[b] + i * LORA_TILE_ROWS;
+                a.m.tile_keyn[tiles[b] + i] = (b << 5) | rows_i;
             }
         } else {
             a.m.key_group[b] = -1;
         }
     }
+    __syncthreads();
+    int *lt_cnt = gidx, *st_cnt = tiles;  // reuse
+    for (int b = tid; b < NK1; b += nthreads) {
+        int l = 0, sh = 0;
+        const int c = b < NK ? cnt[b] : 0;
+        if (c > 0) {
+            const bool run = a.K == 1 && c >= LORA_LONG_MIN && tmax[b] - tmin[b] == c - 1;
+            if (run) l = (c + LORA_LTILE_ROWS - 1) / LORA_LTILE_ROWS;
+            else sh = (c + LORA_TILE_ROWS - 1) / LORA_TILE_ROWS;
+        }
+        lt_cnt[b] = l;
+        st_cnt[b] = sh;
+    }
+    __syncthreads();
+    const int NL = block_exclusive_scan(lt_cnt, NK1, misc);
+    const int NS = block_exclusive_scan(st_cnt, NK1, misc);
+    for (int b = tid; b < NK; b += nthreads) {
+        const int c = cnt[b];
+        if (c <= 0) continue;
+        for (int i = 0; lt_cnt[b] + i < lt_cnt[b + 1]; ++i) {
+            const int rows_i = min(LORA_LTILE_ROWS, c - i * LORA_LTILE_ROWS);
+            a.m.ltile_row0[lt_cnt[b] + i] = off[b] + i * LORA_LTILE_ROWS;
+            a.m.ltile_keyn[lt_cnt[b] + i] = (b << 8) | rows_i;
+            a.m.ltile_tok0[lt_cnt[b] + i] = tmin[b] + i * LORA_LTILE_ROWS;
+        }
+        for (int i = 0; st_cnt[b] + i < st_cnt[b + 1]; ++i) {
+            const int rows_i = min(LORA_TILE_ROWS, c - i * LORA_TILE_ROWS);
+            a.m.stile_row0[st_cnt[b] + i] = off[b] + i * LORA_TILE_ROWS;
+            a.m.stile_keyn[st_cnt[b] + i] = (b << 5) | rows_i;
+        }
+    }
     if (tid == 0) {
         const int n_active = off[NK];
         const int n_bad = misc[36];
+        a.m.counters[4] = NS;
+        a.m.counters[5] = NL;
         a.m.group_start[G] = n_active;
         a.m.counters[0] = n_active;
         a.m.counters[1] = G;
@@ -211,11 +275,20 @@ lora_status_t lora_launch_build_meta(const lora_pool_t *pool, const int32_t *d_i
     const int n_keys = L * E;
     if (rows > meta->max_rows || n_keys > meta->max_keys || n_keys > LORA_MAX_KEYS)
         return LORA_ERR_CAPACITY;
-    if (!meta->sorted || !meta->counters) return LORA_ERR_INVALID_ARG;
+    if (!meta->sorted || !meta->counters || !meta->tile_keyn || !meta->ltile_keyn || !meta->stile_keyn)
+        return LORA_ERR_INVALID_ARG;
     const int NK1 = n_keys + 1;
-    int W = (kSmemBudgetInts - 2 * NK1 - 40) / NK1;
-    if (W > 32) W = 32;
+    // threads scale with the rows (one warp per 32 rows, 4..32 warps)
+    int nthreads = (int)((rows + 31) / 32) * 32;
+    if (nthreads < 128) nthreads = 128;
+    if (nthreads > kThreads) nthreads = kThreads;
+    const int nwarps = nthreads / 32;
+    const long long fixed = 4LL * NK1 + 40 + (L + 3) / 4;
+    int W = (int)((kSmemBudgetInts - fixed) / NK1);
+    if (W > nwarps) W = nwarps;
     if (W < 2) return LORA_ERR_CAPACITY;  // the group/tile pass reuses two histogram rows
+    const long long used = (long long)W * NK1 + fixed;
+    const int cache = used + rows <= kSmemBudgetInts ? 1 : 0;
     MetaArgs a;
     a.idx = d_idx;
     a.topk = d_topk;
@@ -228,8 +301,9 @@ lora_status_t lora_launch_build_meta(const lora_pool_t *pool, const int32_t *d_i
     a.L = L;
     a.n_keys = n_keys;
     a.n_chunks = W;
+    a.cache_keys = cache;
     a.m = *meta;
-    const size_t smem = (size_t)(W * NK1 + 2 * NK1 + 40) * 4;
+    const size_t smem = (size_t)(used + (cache ? rows : 0)) * 4;
     // raise the kernel's shared-memory limit once per device (outside any capture)
     static int configured[64];
     const int dev = pool->device < 64 ? pool->device : 63;
@@ -238,7 +312,7 @@ lora_status_t lora_launch_build_meta(const lora_pool_t *pool, const int32_t *d_i
                                            kSmemBudgetInts * 4));
         configured[dev] = 1;
     }
-    build_meta_kernel<<<1, kThreads, smem, stream>>>(a);
+    build_meta_kernel<<<1, nthreads, smem, stream>>>(a);
     LORA_CUDA_TRY(cudaGetLastError());
     meta->T = T;
     meta->top_k = top_k;

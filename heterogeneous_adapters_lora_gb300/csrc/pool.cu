@@ -296,23 +296,26 @@ extern "C" const char *lora_status_string(lora_status_t s) {
 
 // ------------------------------------------------------------ meta buffers
 
-static size_t meta_layout(int32_t max_rows, int32_t max_keys, size_t off[10]) {
+static size_t meta_layout(int32_t max_rows, int32_t max_keys, size_t off[16]) {
     const int32_t max_tiles = max_rows / LORA_TILE_ROWS + max_keys + 1;
-    const size_t n[9] = {(size_t)max_rows,     (size_t)max_keys,      (size_t)max_keys + 1,
-                         (size_t)max_keys,     (size_t)max_keys + 1,  (size_t)max_keys,
-                         (size_t)max_tiles,    (size_t)max_tiles,     4};
+    const int32_t max_ltiles = max_rows / LORA_LTILE_ROWS + max_keys + 1;
+    const size_t n[15] = {(size_t)max_rows,   (size_t)max_keys,   (size_t)max_keys + 1,
+                          (size_t)max_keys,   (size_t)max_keys + 1, (size_t)max_keys,
+                          (size_t)max_tiles,  (size_t)max_tiles,  (size_t)max_tiles,
+                          (size_t)max_ltiles, (size_t)max_ltiles, (size_t)max_ltiles,
+                          (size_t)max_tiles,  (size_t)max_tiles,  8};
     size_t b = 0;
-    for (int i = 0; i < 9; ++i) {
+    for (int i = 0; i < 15; ++i) {
         off[i] = b;
         b = align256(b + n[i] * 4);
     }
-    off[9] = b;
+    off[15] = b;
     return b;
 }
 
 extern "C" size_t lora_meta_bytes(int32_t max_rows, int32_t max_keys) {
     if (max_rows < 0 || max_keys < 1) return 0;
-    size_t off[10];
+    size_t off[16];
     return meta_layout(max_rows, max_keys, off);
 }
 
@@ -320,13 +323,14 @@ extern "C" lora_status_t lora_meta_bind(lora_meta_t *m, void *d_buf, size_t byte
                                         int32_t max_rows, int32_t max_keys) {
     if (!m || !d_buf || max_rows < 0 || max_keys < 1 || !lora_aligned16(d_buf))
         return LORA_ERR_INVALID_ARG;
-    size_t off[10];
+    size_t off[16];
     if (meta_layout(max_rows, max_keys, off) > bytes) return LORA_ERR_CAPACITY;
     char *b = (char *)d_buf;
     memset(m, 0, sizeof(*m));
     m->max_rows = max_rows;
     m->max_keys = max_keys;
     m->max_tiles = max_rows / LORA_TILE_ROWS + max_keys + 1;
+    m->max_ltiles = max_rows / LORA_LTILE_ROWS + max_keys + 1;
     m->sorted = (int32_t *)(b + off[0]);
     m->key_count = (int32_t *)(b + off[1]);
     m->key_offset = (int32_t *)(b + off[2]);
@@ -335,7 +339,13 @@ extern "C" lora_status_t lora_meta_bind(lora_meta_t *m, void *d_buf, size_t byte
     m->key_group = (int32_t *)(b + off[5]);
     m->tile_group = (int32_t *)(b + off[6]);
     m->tile_row0 = (int32_t *)(b + off[7]);
-    m->counters = (int32_t *)(b + off[8]);
+    m->tile_keyn = (int32_t *)(b + off[8]);
+    m->ltile_row0 = (int32_t *)(b + off[9]);
+    m->ltile_keyn = (int32_t *)(b + off[10]);
+    m->ltile_tok0 = (int32_t *)(b + off[11]);
+    m->stile_row0 = (int32_t *)(b + off[12]);
+    m->stile_keyn = (int32_t *)(b + off[13]);
+    m->counters = (int32_t *)(b + off[14]);
     m->mode = -1;
     return LORA_OK;
 }

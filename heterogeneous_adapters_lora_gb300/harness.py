@@ -39,8 +39,8 @@ class MetaBuffer:
     def read(self):
         """Copy the metadata arrays to host numpy (synchronises)."""
         m = self.meta
-        cnt = self._arr("counters", 4).cpu().numpy()
-        n_active, G, n_bad, NT = (int(v) for v in cnt)
+        cnt = self._arr("counters", 8).cpu().numpy()
+        n_active, G, n_bad, NT, NS, NL = (int(v) for v in cnt[:6])
         rows = m.T * m.top_k
         K = m.n_keys
         out = dict(n_active=n_active, n_groups=G, n_bad=n_bad, n_tiles=NT,
@@ -51,7 +51,14 @@ class MetaBuffer:
                    group_start=self._arr("group_start", G + 1).cpu().numpy(),
                    key_group=self._arr("key_group", K).cpu().numpy(),
                    tile_group=self._arr("tile_group", NT).cpu().numpy(),
-                   tile_row0=self._arr("tile_row0", NT).cpu().numpy())
+                   tile_row0=self._arr("tile_row0", NT).cpu().numpy(),
+                   tile_keyn=self._arr("tile_keyn", NT).cpu().numpy(),
+                   n_stiles=NS, n_ltiles=NL,
+                   stile_row0=self._arr("stile_row0", NS).cpu().numpy(),
+                   stile_keyn=self._arr("stile_keyn", NS).cpu().numpy(),
+                   ltile_row0=self._arr("ltile_row0", NL).cpu().numpy(),
+                   ltile_keyn=self._arr("ltile_keyn", NL).cpu().numpy(),
+                   ltile_tok0=self._arr("ltile_tok0", NL).cpu().numpy())
         return out
 
 

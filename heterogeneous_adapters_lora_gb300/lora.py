@@ -42,11 +42,12 @@ class PoolDesc(ctypes.Structure):
 
 
 class Meta(ctypes.Structure):
-    _fields_ = [("max_rows", c_i32), ("max_keys", c_i32), ("max_tiles", c_i32), ("T", c_i32),
-                ("top_k", c_i32), ("n_keys", c_i32), ("mode", c_i32), ("reserved", c_i32),
+    _fields_ = [("max_rows", c_i32), ("max_keys", c_i32), ("max_tiles", c_i32), ("max_ltiles", c_i32),
+                ("T", c_i32), ("top_k", c_i32), ("n_keys", c_i32), ("mode", c_i32),
                 ("sorted", c_vp), ("key_count", c_vp), ("key_offset", c_vp), ("group_key", c_vp),
                 ("group_start", c_vp), ("key_group", c_vp), ("tile_group", c_vp),
-                ("tile_row0", c_vp), ("counters", c_vp)]
+                ("tile_row0", c_vp), ("tile_keyn", c_vp), ("ltile_row0", c_vp), ("ltile_keyn", c_vp),
+                ("ltile_tok0", c_vp), ("stile_row0", c_vp), ("stile_keyn", c_vp), ("counters", c_vp)]
 
 
 class LoraError(RuntimeError):
@@ -85,6 +86,7 @@ EXPORTS = {
                                c_size, c_vp]),
     "lora_get_device_status": (c_i32, [c_vp, c_vp]),
     "lora_set_spin_limit": (None, [c_i32]),
+    "lora_set_kernel_policy": (None, [c_i32]),
     "lora_status_string": (ctypes.c_char_p, [c_i32]),
 }
 
@@ -236,6 +238,10 @@ def lora_get_device_status(pool, stream=None) -> int:
 
 def lora_set_spin_limit(max_polls: int):
     lib().lora_set_spin_limit(int(max_polls))
+
+
+def lora_set_kernel_policy(policy: int):
+    lib().lora_set_kernel_policy(int(policy))
 
 
 def lora_status_string(code: int) -> str:

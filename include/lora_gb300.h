@@ -70,6 +70,8 @@ typedef enum {
 #define LORA_MAX_RANK 256
 #define LORA_MAX_VOCAB 257024
 #define LORA_TILE_ROWS 16
+#define LORA_LTILE_ROWS 128
+#define LORA_LONG_MIN 64
 
 /* ------------------------------------------------------------------ pool */
 
@@ -167,14 +169,23 @@ LORA_API lora_status_t lora_reset(lora_pool_t *pool, int32_t slot, void *stream)
  *   key_group[max_keys]   group index of each key, -1 if empty
  *   tile_group[max_tiles], tile_row0[max_tiles]: groups cut into tiles of at
  *                         most LORA_TILE_ROWS rows, in group order
+ *   tile_keyn[max_tiles]  (key << 5) | rows of each tile
+ *   ltile_row0, ltile_keyn ((key << 8) | rows), ltile_tok0 [max_ltiles]: for
+ *                         a dense pool, each group of >= LORA_LONG_MIN rows
+ *                         whose token ids form one contiguous run, cut into
+ *                         tiles of <= 128 rows (tok0 = first token of the tile)
+ *   stile_row0, stile_keyn [max_tiles]: 16-row tiles of the other groups
+ *   counters[8]           n_active, n_groups, n_bad, n_tiles, n_stiles, n_ltiles
  *   counters[4]           n_active, n_groups, n_bad, n_tiles
  * The host fields T, top_k, n_keys and mode (0 dense, 1 MoE) record the last
- * build.  Buffers stay valid until the next build into the same meta. */
+ * build.  Buffers stay valid until the next build into the same meta; rebuild
+ * after lora_set / lora_reset of a slot the batch uses. */
 typedef struct {
     int32_t max_rows;
     int32_t max_keys;
     int32_t max_tiles;
-    int32_t T, top_k, n_keys, mode, reserved;
+    int32_t max_ltiles;
+    int32_t T, top_k, n_keys, mode;
     int32_t *sorted;
     int32_t *key_count;
     int32_t *key_offset;
@@ -183,6 +194,12 @@ typedef struct {
     int32_t *key_group;
     int32_t *tile_group;
     int32_t *tile_row0;
+    int32_t *tile_keyn;
+    int32_t *ltile_row0;
+    int32_t *ltile_keyn;
+    int32_t *ltile_tok0;
+    int32_t *stile_row0;
+    int32_t *stile_keyn;
     int32_t *counters;
 } lora_meta_t;
 
@@ -293,6 +310,12 @@ LORA_API lora_status_t lora_get_device_status(const lora_pool_t *pool, void *str
  * skipped.  A negative value makes every wait that is not already satisfied
  * give up at once (to exercise the error path).  Process-wide. */
 LORA_API void lora_set_spin_limit(int32_t max_polls);
+
+/* Kernel selection for lora_apply_slices / lora_moe_apply (process-wide):
+ * 0 = automatic (the one-pass cluster kernel whenever the layer's shapes fit
+ * its shared-memory plan, otherwise the split-K kernel with a workspace),
+ * 1 = always the split-K kernel.  For tests and tuning. */
+LORA_API void lora_set_kernel_policy(int32_t policy);
 
 /* Static string naming a status code. */
 LORA_API const char *lora_status_string(lora_status_t s);

@@ -45,3 +45,30 @@ def tiles_from_groups(group_start, tile_rows=16):
 
 def active_mask(idx, L, enabled, ranks):
     return np.array([bool(0 <= a < L and enabled[a] and ranks[a] > 0) for a in idx], dtype=bool)
+
+
+def tile_keyn(tg, tr, group_key, group_start, tile_rows=16):
+    """(key << 5) | rows of each tile, from the oracle's groups."""
+    out = []
+    for g, r0 in zip(tg, tr):
+        n = min(tile_rows, group_start[g + 1] - r0)
+        out.append((int(group_key[g]) << 5) | int(n))
+    return np.asarray(out, np.int32)
+
+
+def long_short_tiles(group_key, group_start, sorted_rows, dense=True, long_min=64, lrows=128, srows=16):
+    """Expected long (contiguous-run, 128-row) and short (16-row) tile lists."""
+    lt, st = [], []
+    for g in range(len(group_start) - 1):
+        s0, s1 = int(group_start[g]), int(group_start[g + 1])
+        c = s1 - s0
+        key = int(group_key[g])
+        run = dense and c >= long_min and int(sorted_rows[s1 - 1]) - int(sorted_rows[s0]) == c - 1
+        if run:
+            for r0 in range(s0, s1, lrows):
+                n = min(lrows, s1 - r0)
+                lt.append((r0, (key << 8) | n, int(sorted_rows[s0]) + (r0 - s0)))
+        else:
+            for r0 in range(s0, s1, srows):
+                st.append((r0, (key << 5) | min(srows, s1 - r0)))
+    return lt, st

@@ -8,7 +8,7 @@ import oracle
 from heterogeneous_adapters_lora_gb300 import harness as H
 from heterogeneous_adapters_lora_gb300 import inputs as gen
 from heterogeneous_adapters_lora_gb300 import lora as L
-from gpu_util import tiles_from_groups
+from gpu_util import long_short_tiles, tile_keyn, tiles_from_groups
 
 pytestmark = pytest.mark.gpu
 
@@ -46,6 +46,16 @@ def _check_dense(idx, Lk, ranks, enabled):
         tg, tr = tiles_from_groups(ref.seg_start)
         assert got["n_tiles"] == len(tg)
         assert np.array_equal(got["tile_group"], tg) and np.array_equal(got["tile_row0"], tr)
+        assert np.array_equal(got["tile_keyn"], tile_keyn(tg, tr, ref.seg_slot, ref.seg_start))
+        lt, st = long_short_tiles(ref.seg_slot, ref.seg_start, ref.sorted_tok)
+        assert got["n_ltiles"] == len(lt) and got["n_stiles"] == len(st)
+        if lt:
+            assert np.array_equal(got["ltile_row0"], [x[0] for x in lt])
+            assert np.array_equal(got["ltile_keyn"], [x[1] for x in lt])
+            assert np.array_equal(got["ltile_tok0"], [x[2] for x in lt])
+        if st:
+            assert np.array_equal(got["stile_row0"], [x[0] for x in st])
+            assert np.array_equal(got["stile_keyn"], [x[1] for x in st])
         st = L.lora_get_device_status(pool)
         assert st == (L.CODE["LORA_ERR_DEVICE_INDEX"] if ref.n_bad else 0)
     finally:
@@ -67,7 +77,7 @@ def test_dense_meta_presets(preset):
 
 
 @pytest.mark.parametrize("case", ["all_none", "one_token", "empty", "single_slot", "bad_and_disabled",
-                                  "big_skewed"])
+                                  "big_skewed", "huge_uncached"])
 def test_dense_meta_edges(case):
     rng = np.random.default_rng(7)
     Lk, ranks, en = 16, np.full(16, 8, np.int32), None
@@ -83,8 +93,10 @@ def test_dense_meta_edges(case):
         idx = rng.integers(-3, 20, size=777).astype(np.int32)
         ranks = rng.choice([0, 8, 16], size=16).astype(np.int32)
         en = (rng.random(16) < 0.7)
-    else:
+    elif case == "big_skewed":
         idx = rng.choice(16, size=20000, p=gen.zipf_pmf(16, 1.5)).astype(np.int32)
+    else:  # more rows than the key cache holds: keys are recomputed in the scatter pass
+        idx = rng.integers(-1, 16, size=70000).astype(np.int32)
     _check_dense(idx, Lk, ranks, en)
 
 
@@ -105,6 +117,10 @@ def test_moe_meta_preset_and_small():
             assert np.array_equal(got["group_start"], ref.group_start)
             tg, tr = tiles_from_groups(ref.group_start)
             assert np.array_equal(got["tile_group"], tg) and np.array_equal(got["tile_row0"], tr)
+            assert np.array_equal(got["tile_keyn"], tile_keyn(tg, tr, ref.group_key, ref.group_start))
+            assert got["n_ltiles"] == 0   # pairs of one (slot, expert) are never a contiguous run
+            lt, st = long_short_tiles(ref.group_key, ref.group_start, ref.sorted_pair, dense=False)
+            assert got["n_stiles"] == len(st)
         finally:
             run.close()
 
@@ -122,3 +138,14 @@ def test_meta_is_deterministic_across_runs():
         assert all(np.array_equal(outs[0], o) for o in outs[1:])
     finally:
         L.lora_pool_destroy(pool)
+
+
+def test_long_tiles_need_one_contiguous_run():
+    """Slot 0: one run of 300 tokens (long tiles); slot 1: two runs of 100
+    (short tiles); slot 2: 40 tokens (too few, short tiles)."""
+    idx = np.full(700, -1, np.int32)
+    idx[0:300] = 0
+    idx[300:400] = 1
+    idx[450:550] = 1
+    idx[600:640] = 2
+    _check_dense(idx, 4, np.full(4, 16, np.int32), None)

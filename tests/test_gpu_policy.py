@@ -1,0 +1,92 @@
+"""Both compute paths of lora_apply_slices / lora_moe_apply against the
+oracle: the one-pass cluster kernel (automatic choice for these shapes) and
+the split-K kernel with a workspace (kernel policy 1)."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle
+from heterogeneous_adapters_lora_gb300 import harness as H
+from heterogeneous_adapters_lora_gb300 import inputs as gen
+from heterogeneous_adapters_lora_gb300 import lora as L
+from heterogeneous_adapters_lora_gb300.inputs import bf16_bits_to_f32
+from gpu_util import active_mask, assert_delta, assert_rows_untouched
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(params=[0, 1], ids=["auto", "splitk"])
+def policy(request):
+    L.lora_set_kernel_policy(request.param)
+    yield request.param
+    L.lora_set_kernel_policy(0)
+
+
+def _dense(c):
+    run = H.DenseRun(c)
+    try:
+        run.step()
+        y = run.y_host()
+        assert run.status() == 0
+    finally:
+        run.close()
+    _, d_ref = oracle.dense_delta(c)
+    act = active_mask(c.idx, c.L, c.enabled, c.ranks)
+    assert_rows_untouched(y, c.y0, ~act)
+    assert_delta(bf16_bits_to_f32(y)[act], d_ref[act], c.name)
+
+
+@pytest.mark.parametrize("name", ["decode_qkv", "many_adapter_down", "small_multi_tile", "prefill_gate_up"])
+def test_dense_paths(name, policy):
+    if name == "decode_qkv":
+        c = gen.decode_qkv()
+    elif name == "many_adapter_down":
+        c = gen.many_adapter_down()
+    elif name == "prefill_gate_up":
+        c = gen.prefill_gate_up(permuted=True)
+    else:
+        c = gen.dense_case(name="smt", T=150, H=2056, out_dims=(264, 136, 80), L=4, R=24, seed=41,
+                           ranks=(24, 13, 1, 8), scales=(1.0, 0.5, 2.0, 1.5), p_none=0.1)
+    _dense(c)
+
+
+@pytest.mark.parametrize("shared", [False, True])
+def test_moe_paths(shared, policy):
+    c = gen.moe(shared_outer=shared)
+    run = H.MoERun(c)
+    try:
+        run.step()
+        ic1 = H.from_dev_u16(run.ic1)
+        ic3 = H.from_dev_u16(run.ic3)
+        assert run.status() == 0
+    finally:
+        run.close()
+    _, d13 = oracle.moe_w13(c)
+    _, d2 = oracle.moe_w2(c)
+    assert_delta(bf16_bits_to_f32(ic1), d13, "w13")
+    assert_delta(bf16_bits_to_f32(ic3), d2, "w2")
+
+
+def test_cluster_path_in_a_graph_with_other_streams_idle():
+    """Metadata + cluster apply captured together (programmatic dependent
+    launch edge inside the graph) and replayed three times."""
+    c = gen.decode_qkv()
+    run = H.DenseRun(c)
+    try:
+        s = torch.cuda.Stream()
+        g = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                run.step()
+        run.y.zero_()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        y = run.y_host()
+    finally:
+        run.close()
+    _, d_ref = oracle.dense_delta(c)
+    act = active_mask(c.idx, c.L, c.enabled, c.ranks)
+    assert_delta(bf16_bits_to_f32(y)[act], 3 * d_ref[act], "3 replays")

@@ -1,6 +1,6 @@
 // Cluster BGMV: the multi-tenant LoRA delta for small row groups (decode
 // tokens, MoE (adapter, expert) groups) in one pass, one thread-block
-// cluster per tile of <= 16 rows of one group.
+// cluster of 1, 2, 4 or 8 CTAs per tile of <= 16 rows of one group.
 //
 // The vLLM LoRA layer pages compute it as add_shrink into a zeroed fp32
 // buffer [n_slices][T][rank] and add_expand with add_input=True at the slice
@@ -9,15 +9,18 @@
 //   CTA c of the cluster owns hidden range c and output range c.
 //   1. bulk copies (cp.async.bulk, mbarrier transaction counts) bring the
 //      tile's x rows and the slot's A rows for hidden range c into shared
-//      memory (<= 2 stages), and the slot's B rows for output range c
+//      memory (<= 2 stages in flight), and the slot's B rows for output range c
 //   2. partial v[t][j][k] over hidden range c: m16n8k16 bf16 tensor-core
 //      MMAs (tokens x rank rows x hidden), fragments from ldmatrix, fp32
-//      accumulation
-//   3. cluster barrier; every CTA sums the 8 partials through distributed
-//      shared memory, scales by scale[a] (and the routed weight for MoE w2),
-//      and splits v into bf16 hi + lo parts so the expand keeps fp32 accuracy
+//      accumulation; meanwhile the tile's y rows of output range c are
+//      bulk-copied into the freed stage buffers
+//   3. cluster barrier; every CTA sums the partials of its peers through
+//      distributed shared memory, scales by scale[a] (and the routed weight
+//      for MoE w2), and splits v into bf16 hi + lo parts so the expand keeps
+//      the fp32 intermediate to ~16 bits
 //   4. y[t][o] += v_hi[t] . B[o] + v_lo[t] . B[o] for o in output range c
-//      (MMAs), bf16x2 read-modify-write of y prefetched at kernel start
+//      (MMAs) in shared memory, then bulk copies write the rows back
+// The cluster size is picked per layer so that each CTA moves ~96 KB.
 // Launched with programmatic stream serialization so it starts while the
 // metadata kernel finishes; griddepcontrol.wait orders its metadata reads.
 #include <string.h>
@@ -26,11 +29,10 @@
 
 namespace {
 
-constexpr int kCS = 8;
+constexpr int kMaxCS = 8;  // CTAs per tile (cluster size) is 1, 2, 4 or 8
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kTileRows = LORA_TILE_ROWS;
-constexpr int kYPre = 16;  // output n-blocks per warp whose y is prefetched
 constexpr int kMaxHSplit = 4;  // hidden-range split of the shrink across warps
 
 struct CArgs {
@@ -50,11 +52,12 @@ struct CArgs {
     uint16_t *out;
     long long ld_out;
     const float *row_w;
-    int HCc, OCc, SC;
-    int xs_stride, as_stride, vr_stride;  // elements
-    int off_x, off_a, off_b, off_vp, off_vsum, off_vh, off_vl, x_stage_bytes, a_stage_bytes;
+    int CS, HCc, OCc, SC;
+    int xs_stride, as_stride, vr_stride, ys_stride;  // elements
+    int off_x, off_a, off_b, off_vp, off_ys, off_vsum, off_vh, off_vl, x_stage_bytes, a_stage_bytes;
     int *status;
     int spin_limit;
+    float post_scale;  // extra factor on every delta (lm_head muP); 1 otherwise
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -169,13 +172,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __global__ void __launch_bounds__(kThreads, 2) cluster_lora_kernel(const __grid_constant__ CArgs p) {
     extern __shared__ __align__(128) char smem[];
     __shared__ __align__(8) uint64_t full[2];
-    __shared__ __align__(8) uint64_t bbar;
+    __shared__ __align__(8) uint64_t bbar, ybar;
     __shared__ int s_rows[kTileRows];
     __shared__ const uint16_t *s_Ab[LORA_MAX_SLICES];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, c4 = lane & 3;
-    const int tile = blockIdx.x / kCS;
+    const int tile = blockIdx.x / p.CS;
     const uint32_t crank = cluster_rank();
 
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -207,6 +210,7 @@ __global__ void __launch_bounds__(kThreads, 2) cluster_lora_kernel(const __grid_
         mbar_init(&full[0], 1);
         mbar_init(&full[1], 1);
         mbar_init(&bbar, 1);
+        mbar_init(&ybar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -214,37 +218,9 @@ __global__ void __launch_bounds__(kThreads, 2) cluster_lora_kernel(const __grid_
     // ---- issue every copy that does not wait for a stage to drain
     if (warp == 0) {
         for (int s = 0; s < min(n_sub, 2); ++s) issue_stage(p, smem, full, s, hb, he, n, r, s_rows, s_Ab, lane);
-    } else if (warp == 1) {
-        // B rows of output range [ob, oe), slice by slice, compact rows of rs
-        uint16_t *bs = (uint16_t *)(smem + p.off_b);
-        const uint32_t total = oe > ob ? (uint32_t)(oe - ob) * rs * 2 : 0;
-        if (lane == 0) mbar_expect_tx(&bbar, total);
-        __syncwarp();
-        if (lane < ns) {
-            const int j = lane;
-            const int s0 = max(ob, p.out_off[j]), s1 = min(oe, p.out_off[j] + p.out_w[j]);
-            if (s1 > s0) {
-                const uint16_t *Bj = p.B[j] + (long long)a * p.B_ss[j] +
-                                     (p.B_shared[j] ? 0ll : (long long)e * p.out_w[j] * rs);
-                bulk_g2s(bs + (long long)(s0 - ob) * rs, Bj + (long long)(s0 - p.out_off[j]) * rs,
-                         (uint32_t)(s1 - s0) * rs * 2, &bbar);
-            }
-        }
     }
 
-    // ---- prefetch y at this thread's expand fragment positions
     const int nob = (oe - ob) >> 3;  // output blocks of 8 columns
-    uint32_t ypre[kYPre][2];
-#pragma unroll
-    for (int i = 0; i < kYPre; ++i) {
-        ypre[i][0] = ypre[i][1] = 0;
-        const int ob8 = warp + i * kWarps;
-        if (ob8 < nob) {
-            const int o = ob + ob8 * 8 + 2 * c4;
-            if (g < n) ypre[i][0] = *(const uint32_t *)(p.out + (long long)s_rows[g] * p.ld_out + o);
-            if (g + 8 < n) ypre[i][1] = *(const uint32_t *)(p.out + (long long)s_rows[g + 8] * p.ld_out + o);
-        }
-    }
 
     // ---- partial shrink over this CTA's hidden range (tensor-core MMAs)
     // units: (n-block of 8 rank rows, hidden split); every warp owns <= 2 units
@@ -257,8 +233,9 @@ __global__ void __launch_bounds__(kThreads, 2) cluster_lora_kernel(const __grid_
     for (int u = 0; u < 2; ++u)
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc[u][i] = 0.f;
-    float *vp = (float *)(smem + p.off_vp);  // [hsplit][16][JK]
-    for (int i = tid; i < hsplit * kTileRows * JK; i += kThreads) vp[i] = 0.f;
+    // after the shrink the stage buffers hold the y tile and the partials
+    uint16_t *ys = (uint16_t *)(smem + p.off_ys);  // [16][ys_stride] y rows of [ob, oe)
+    float *vp = (float *)(smem + p.off_vp);        // [hsplit][16][JK]
 
     for (int s = 0; s < n_sub; ++s) {
         const int st = s & 1;
@@ -289,6 +266,34 @@ __global__ void __launch_bounds__(kThreads, 2) cluster_lora_kernel(const __grid_
             issue_stage(p, smem, full, s + 2, hb, he, n, r, s_rows, s_Ab, lane);
         }
     }
+    // stage buffers are free: bring the y rows of this CTA's output range in
+    if (warp == 0) {
+        const uint32_t rowb = oe > ob ? (uint32_t)(oe - ob) * 2 : 0;
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        if (lane == 0) mbar_expect_tx(&ybar, rowb * (uint32_t)n);
+        __syncwarp();
+        if (lane < n && rowb)
+            bulk_g2s(ys + lane * p.ys_stride, p.out + (long long)s_rows[lane] * p.ld_out + ob, rowb, &ybar);
+    } else if (warp == 1) {
+        // B rows of output range [ob, oe), slice by slice, compact rows of rs
+        uint16_t *bsw = (uint16_t *)(smem + p.off_b);
+        const uint32_t total = oe > ob ? (uint32_t)(oe - ob) * rs * 2 : 0;
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        if (lane == 0) mbar_expect_tx(&bbar, total);
+        __syncwarp();
+        if (lane < ns) {
+            const int j = lane;
+            const int s0 = max(ob, p.out_off[j]), s1 = min(oe, p.out_off[j] + p.out_w[j]);
+            if (s1 > s0) {
+                const uint16_t *Bj = p.B[j] + (long long)a * p.B_ss[j] +
+                                     (p.B_shared[j] ? 0ll : (long long)e * p.out_w[j] * rs);
+                bulk_g2s(bsw + (long long)(s0 - ob) * rs, Bj + (long long)(s0 - p.out_off[j]) * rs,
+                         (uint32_t)(s1 - s0) * rs * 2, &bbar);
+            }
+        }
+    }
+    for (int i = tid; i < hsplit * kTileRows * JK; i += kThreads) vp[i] = 0.f;
+    __syncthreads();
     // fragment (row t, rank row q): d0 (g, 2c4), d1 (g, 2c4+1), d2 (g+8, 2c4), d3 (g+8, 2c4+1)
 #pragma unroll
     for (int ui = 0; ui < 2; ++ui) {
@@ -327,17 +332,18 @@ __global__ void __launch_bounds__(kThreads, 2) cluster_lora_kernel(const __grid_
             float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
             if (t < n) {
                 const float *src = vsum + t * JK + q * 4;
-                float4 v[kCS];
+                float4 v[kMaxCS];
 #pragma unroll
-                for (int cc = 0; cc < kCS; ++cc) v[cc] = ld_dsmem_f32x4(src, (uint32_t)cc);
+                for (int cc = 0; cc < kMaxCS; ++cc)
+                    v[cc] = cc < p.CS ? ld_dsmem_f32x4(src, (uint32_t)cc) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                for (int cc = 0; cc < kCS; ++cc) {
+                for (int cc = 0; cc < kMaxCS; ++cc) {
                     s4.x += v[cc].x;
                     s4.y += v[cc].y;
                     s4.z += v[cc].z;
                     s4.w += v[cc].w;
                 }
-                float w = sc;
+                float w = sc * p.post_scale;
                 if (p.row_w) w *= p.row_w[s_rows[t]];
                 s4.x *= w;
                 s4.y *= w;
@@ -363,12 +369,14 @@ __global__ void __launch_bounds__(kThreads, 2) cluster_lora_kernel(const __grid_
     mbar_wait(&bbar, 0, p.spin_limit, p.status);
     const uint16_t *bs = (const uint16_t *)(smem + p.off_b);
     const int ksteps = (rs + 15) >> 4;
-    auto expand_block = [&](int ob8, uint32_t y0, uint32_t y1, bool pre) {
+    mbar_wait(&ybar, 0, p.spin_limit, p.status);
+    const int arow = (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll 1
+    for (int ob8 = warp; ob8 < nob; ob8 += kWarps) {
         const int o0 = ob + ob8 * 8;
         int j = 0;
         while (j + 1 < ns && o0 >= p.out_off[j + 1]) ++j;
         float d[4] = {0.f, 0.f, 0.f, 0.f};
-        const int arow = (lane & 7) + ((lane >> 3) & 1) * 8;
         for (int ks = 0; ks < ksteps; ++ks) {
             const int k0 = ks * 16;
             uint32_t h0, h1, h2, h3, l0, l1, l2, l3, b0, b1;
@@ -380,22 +388,35 @@ __global__ void __launch_bounds__(kThreads, 2) cluster_lora_kernel(const __grid_
             mma16816(d, h0, h1, h2, h3, b0, b1);
             mma16816(d, l0, l1, l2, l3, b0, b1);
         }
-        const int o = o0 + 2 * c4;
+        const int oc = ob8 * 8 + 2 * c4;  // column inside the y tile
         if (g < n) {
-            uint32_t *yp = (uint32_t *)(p.out + (long long)s_rows[g] * p.ld_out + o);
-            const uint32_t u = pre ? y0 : *yp;
+            uint32_t *yp = (uint32_t *)(ys + g * p.ys_stride + oc);
+            const uint32_t u = *yp;
             *yp = pack_bf16x2(bf16lo(u) + d[0], bf16hi(u) + d[1]);
         }
         if (g + 8 < n) {
-            uint32_t *yp = (uint32_t *)(p.out + (long long)s_rows[g + 8] * p.ld_out + o);
-            const uint32_t u = pre ? y1 : *yp;
+            uint32_t *yp = (uint32_t *)(ys + (g + 8) * p.ys_stride + oc);
+            const uint32_t u = *yp;
             *yp = pack_bf16x2(bf16lo(u) + d[2], bf16hi(u) + d[3]);
         }
-    };
-#pragma unroll
-    for (int i = 0; i < kYPre; ++i)
-        if (warp + i * kWarps < nob) expand_block(warp + i * kWarps, ypre[i][0], ypre[i][1], true);
-    for (int i = kYPre; warp + i * kWarps < nob; ++i) expand_block(warp + i * kWarps, 0u, 0u, false);
+    }
+    // write the updated rows back with bulk copies
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();
+    if (warp == 0) {
+        const uint32_t rowb = oe > ob ? (uint32_t)(oe - ob) * 2 : 0;
+        if (lane < n && rowb) {
+            asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                             p.out + (long long)s_rows[lane] * p.ld_out + ob),
+                         "r"(smem_u32(ys + lane * p.ys_stride)), "r"(rowb)
+                         : "memory");
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+            asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+        }
+    }
+    // the next kernel in the stream may start its prologue; it still waits
+    // for this grid to finish before touching memory
+    asm volatile("griddepcontrol.launch_dependents;");
     cluster_wait();  // peers may still read this CTA's partials until here
 }
 
@@ -407,29 +428,32 @@ size_t align128(size_t x) { return (x + 127) & ~(size_t)127; }
 
 struct CPlan {
     bool ok;
-    int HCc, OCc, SC, n_stage, hsplit_max, xs_stride, as_stride, vr_stride;
-    int off_x, off_a, off_b, off_vp, off_vsum, off_vh, off_vl, x_stage_bytes, a_stage_bytes;
+    int CS, HCc, OCc, SC, n_stage, hsplit_max, xs_stride, as_stride, vr_stride, ys_stride;
+    int off_x, off_a, off_b, off_vp, off_ys, off_vsum, off_vh, off_vl, x_stage_bytes, a_stage_bytes;
     size_t smem;
 };
 
 constexpr size_t kBudget2 = 110 * 1024;  // two CTAs per SM
 constexpr size_t kBudget1 = 220 * 1024;  // one CTA per SM
 
-CPlan make_cplan(int ns, int in_dim, int out_total, int R) {
+CPlan make_cplan(int ns, int in_dim, int out_total, int R, int CS) {
     CPlan c;
     memset(&c, 0, sizeof(c));
     const int R8 = lora_round8(R);
     const int JK = ns * R8;
     if (ns * R > 128) return c;  // <= 16 n-blocks of rank rows: two per warp
-    c.HCc = ((lora_ceil_div(in_dim, kCS) + 15) / 16) * 16;
-    c.OCc = lora_round8(lora_ceil_div(out_total, kCS));
+    c.CS = CS;
+    c.HCc = ((lora_ceil_div(in_dim, CS) + 15) / 16) * 16;
+    c.OCc = lora_round8(lora_ceil_div(out_total, CS));
     c.hsplit_max = kMaxHSplit;  // a tile of lower rank has fewer n-blocks and may split more
     c.vr_stride = JK + 8;
+    c.ys_stride = c.OCc + 8;
     const size_t b_bytes = align128((size_t)c.OCc * R8 * 2 + 32);
     const size_t vp_bytes = align128((size_t)c.hsplit_max * kTileRows * JK * 4);
+    const size_t ys_bytes = align128((size_t)kTileRows * c.ys_stride * 2);
     const size_t vsum_bytes = align128((size_t)kTileRows * JK * 4);
     const size_t vh_bytes = align128((size_t)kTileRows * c.vr_stride * 2);
-    const size_t fixed = b_bytes + vp_bytes + vsum_bytes + 2 * vh_bytes;
+    const size_t fixed = vsum_bytes + 2 * vh_bytes;
     const int arows = lora_round8(ns * R);
     const size_t per_elem = (size_t)(kTileRows + arows) * 2;  // x rows + A rows, one stage
     const size_t budgets[2] = {kBudget2, kBudget1};
@@ -447,17 +471,23 @@ CPlan make_cplan(int ns, int in_dim, int out_total, int R) {
         c.as_stride = c.SC + 8;
         c.x_stage_bytes = (int)align128((size_t)kTileRows * c.xs_stride * 2);
         c.a_stage_bytes = (int)align128((size_t)arows * c.as_stride * 2);
+        // the y tile, the partials and the slot's B rows reuse the stage
+        // buffers after the shrink
+        size_t stage_region = (size_t)c.n_stage * (c.x_stage_bytes + c.a_stage_bytes);
+        if (stage_region < ys_bytes + vp_bytes + b_bytes) stage_region = ys_bytes + vp_bytes + b_bytes;
         c.off_x = 0;
         c.off_a = c.n_stage * c.x_stage_bytes;
-        c.off_b = c.off_a + c.n_stage * c.a_stage_bytes;
-        c.off_vp = c.off_b + (int)b_bytes;
-        c.off_vsum = c.off_vp + (int)vp_bytes;
+        c.off_ys = 0;
+        c.off_vp = (int)ys_bytes;
+        c.off_b = (int)(ys_bytes + vp_bytes);
+        c.off_vsum = (int)stage_region;
         c.off_vh = c.off_vsum + (int)vsum_bytes;
         c.off_vl = c.off_vh + (int)vh_bytes;
         c.smem = (size_t)c.off_vl + vh_bytes;
-        c.ok = c.smem <= kBudget1;
-        return c;
+        c.ok = c.smem <= budgets[bi];
+        if (c.ok) return c;
     }
+    c.ok = false;
     return c;
 }
 
@@ -470,7 +500,17 @@ lora_status_t lora_cluster_apply(const lora_pool_t *pool, const LoraProblem &pr,
     *launched = false;
     int out_total = 0;
     for (int j = 0; j < pr.n_slices; ++j) out_total = max(out_total, pr.out_off[j] + pr.out_w[j]);
-    const CPlan cp = make_cplan(pr.n_slices, pr.in_dim, out_total, pr.R);
+    // CTAs per tile: enough that each moves ~96 KB of a full-rank tile (weights,
+    // x rows and y rows), and the smallest such cluster whose plan fits
+    const double tile_bytes = 2.0 * ((double)pr.n_slices * pr.R * pr.in_dim + kTileRows * (double)pr.in_dim +
+                                     (double)out_total * pr.R + 2.0 * kTileRows * out_total);
+    int CS = 1;
+    while (CS < kMaxCS && tile_bytes / CS > 96.0 * 1024) CS *= 2;
+    CPlan cp = make_cplan(pr.n_slices, pr.in_dim, out_total, pr.R, CS);
+    while (!cp.ok && CS < kMaxCS) {
+        CS *= 2;
+        cp = make_cplan(pr.n_slices, pr.in_dim, out_total, pr.R, CS);
+    }
     if (!cp.ok) return LORA_OK;
     CArgs a;
     memset(&a, 0, sizeof(a));
@@ -503,12 +543,15 @@ lora_status_t lora_cluster_apply(const lora_pool_t *pool, const LoraProblem &pr,
     a.out = pr.out;
     a.ld_out = pr.ld_out;
     a.row_w = pr.row_w;
+    a.CS = cp.CS;
     a.HCc = cp.HCc;
     a.OCc = cp.OCc;
     a.SC = cp.SC;
     a.xs_stride = cp.xs_stride;
     a.as_stride = cp.as_stride;
     a.vr_stride = cp.vr_stride;
+    a.ys_stride = cp.ys_stride;
+    a.off_ys = cp.off_ys;
     a.off_x = cp.off_x;
     a.off_a = cp.off_a;
     a.off_b = cp.off_b;
@@ -520,6 +563,7 @@ lora_status_t lora_cluster_apply(const lora_pool_t *pool, const LoraProblem &pr,
     a.a_stage_bytes = cp.a_stage_bytes;
     a.status = pr.status;
     a.spin_limit = pr.spin_limit;
+    a.post_scale = pr.post_scale;
 
     const int dev = pool->device < 64 ? pool->device : 63;
     if (!g_cluster_configured[dev]) {
@@ -534,13 +578,13 @@ lora_status_t lora_cluster_apply(const lora_pool_t *pool, const LoraProblem &pr,
     }
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
-    cfg.gridDim = dim3((unsigned)(max_tiles * kCS), 1, 1);
+    cfg.gridDim = dim3((unsigned)(max_tiles * cp.CS), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = cp.smem;
     cfg.stream = s;
     cudaLaunchAttribute at[2];
     at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = kCS;
+    at[0].val.clusterDim.x = cp.CS;
     at[0].val.clusterDim.y = 1;
     at[0].val.clusterDim.z = 1;
     at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;

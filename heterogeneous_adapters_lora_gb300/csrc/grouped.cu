@@ -59,6 +59,7 @@ struct GArgs {
     int *tile_cnt;
     int *status;
     int spin_limit;
+    float post_scale;
 };
 
 struct TileInfo {
@@ -240,7 +241,7 @@ __device__ void expand_item(const GArgs &p, int tile, int j, int oc, char *smem,
     const int rs = (ti.r + 7) & ~7;
     const int VS = ((p.R + 7) & ~7) + 4;  // row stride of v in shared memory (multiple of 4)
     float *vs = (float *)smem;
-    const float sc = p.scale[ti.a];
+    const float sc = p.scale[ti.a] * p.post_scale;
     for (int i = tid; i < ti.n * rs; i += kThreads) {
         const int t = i / rs, k = i - t * rs;
         float s = 0.f;
@@ -352,6 +353,7 @@ __global__ void __launch_bounds__(kThreads) grouped_lora_kernel(const __grid_con
             run_item<MODE>(p, item, n_sh, smem, &s_flag);
             __syncthreads();
         }
+        asm volatile("griddepcontrol.launch_dependents;");
         if (threadIdx.x == 0) {
             __threadfence();
             s_last = (atomicAdd(p.ctrl + 1, 1) == (int)gridDim.x - 1);
@@ -477,6 +479,7 @@ lora_status_t dense_args(const lora_pool_t *pool, const lora_meta_t *meta, GArgs
     g.counters = meta->counters;
     g.status = pool->d_status;
     g.rows = meta->T;
+    g.post_scale = 1.0f;
     return LORA_OK;
 }
 
@@ -557,6 +560,7 @@ LoraProblem to_problem(const GArgs &g, const lora_meta_t *meta, int n_keys) {
     pr.row_w = g.row_w;
     pr.status = g.status;
     pr.spin_limit = g_spin_limit;
+    pr.post_scale = g.post_scale;
     return pr;
 }
 
@@ -589,9 +593,9 @@ extern "C" lora_status_t lora_workspace_init(void *workspace, size_t bytes, void
     return LORA_OK;
 }
 
-extern "C" lora_status_t lora_apply_slices(const lora_pool_t *pool, const lora_meta_t *meta,
-                                           const void *x, int64_t ldx, void *y, int64_t ldy,
-                                           void *workspace, size_t ws_bytes, void *stream) {
+lora_status_t lora_dense_apply(const lora_pool_t *pool, const lora_meta_t *meta, const void *x, int64_t ldx,
+                               void *y, int64_t ldy, void *workspace, size_t ws_bytes, float post_scale,
+                               cudaStream_t s) {
     if (!pool) return LORA_ERR_INVALID_ARG;
     GArgs g;
     lora_status_t st = dense_args(pool, meta, g);
@@ -600,6 +604,7 @@ extern "C" lora_status_t lora_apply_slices(const lora_pool_t *pool, const lora_m
     if (!x || !y || !lora_aligned16(x) || !lora_aligned16(y) || ldx % 8 || ldy % 8 ||
         ldx < pool->desc.in_dim || ldy < out_total(pool))
         return LORA_ERR_INVALID_ARG;
+    g.post_scale = post_scale;
     // workspace: [bf16 hi/lo rank buffer of the tensor-core path (1 KB aligned)][split-K region]
     const size_t sg_bytes = sgmv_region_bytes(pool, meta->T);
     const bool use_sgmv = g_lora_kernel_policy == 0 && sg_bytes > 0 && meta->T >= LORA_LONG_MIN &&
@@ -615,10 +620,9 @@ extern "C" lora_status_t lora_apply_slices(const lora_pool_t *pool, const lora_m
     g.ld_in = ldx;
     g.out = (uint16_t *)y;
     g.ld_out = ldy;
-    cudaStream_t s = (cudaStream_t)stream;
     if (use_sgmv) {
         // long contiguous runs on tcgen05; the remaining groups' 16-row tiles below
-        st = lora_sgmv_apply(pool, meta, x, ldx, y, ldy, workspace, g_spin_limit, pool->num_sms, s);
+        st = lora_sgmv_apply(pool, meta, x, ldx, y, ldy, workspace, g_spin_limit, pool->num_sms, post_scale, s);
         if (st != LORA_OK) return st;
         g.tile_row0 = meta->stile_row0;
         g.tile_keyn = meta->stile_keyn;
@@ -630,6 +634,12 @@ extern "C" lora_status_t lora_apply_slices(const lora_pool_t *pool, const lora_m
         if (st != LORA_OK || launched) return st;
     }
     return launch<kFused>(pool, g, est_items(g, meta->T, pool->desc.max_loras, kFused), s);
+}
+
+extern "C" lora_status_t lora_apply_slices(const lora_pool_t *pool, const lora_meta_t *meta,
+                                           const void *x, int64_t ldx, void *y, int64_t ldy,
+                                           void *workspace, size_t ws_bytes, void *stream) {
+    return lora_dense_apply(pool, meta, x, ldx, y, ldy, workspace, ws_bytes, 1.0f, (cudaStream_t)stream);
 }
 
 extern "C" lora_status_t lora_shrink(const lora_pool_t *pool, const lora_meta_t *meta,
@@ -688,6 +698,7 @@ extern "C" lora_status_t lora_moe_apply(const lora_pool_t *pool, const lora_meta
     g.R = d.max_rank;
     g.T = meta->T;
     g.rows = rows;
+    g.post_scale = 1.0f;
     int och = 0;
     if (which == LORA_MOE_W13) {
         g.n_slices = n13;

@@ -10,7 +10,7 @@
 // Tensor descriptors: a dense pool has one A/B pair per output slice; a MoE
 // pool has one pair per w13 slice followed by the w2 pair.
 #define LORA_MAX_TENSORS (LORA_MAX_SLICES + 1)
-#define LORA_MAX_KEYS 12288
+#define LORA_MAX_KEYS 6144
 
 struct lora_pool {
     lora_pool_desc_t desc;
@@ -104,6 +104,7 @@ struct LoraProblem {
     const float *row_w;
     int *status;
     int spin_limit;
+    float post_scale;
 };
 
 // Cluster kernel (cluster.cu): launches and sets *launched when the shape
@@ -118,4 +119,10 @@ extern int g_lora_kernel_policy;
 bool lora_sgmv_eligible(const lora_pool_t *pool);
 size_t lora_sgmv_ws_bytes(const lora_pool_t *pool, int rows);
 lora_status_t lora_sgmv_apply(const lora_pool_t *pool, const lora_meta_t *meta, const void *x, int64_t ldx,
-                              void *y, int64_t ldy, void *V, int spin_limit, int num_sms, cudaStream_t s);
+                              void *y, int64_t ldy, void *V, int spin_limit, int num_sms, float post_scale,
+                              cudaStream_t s);
+
+// Dense apply shared by lora_apply_slices and lora_logits_apply (grouped.cu).
+lora_status_t lora_dense_apply(const lora_pool_t *pool, const lora_meta_t *meta, const void *x, int64_t ldx,
+                               void *y, int64_t ldy, void *workspace, size_t ws_bytes, float post_scale,
+                               cudaStream_t s);

@@ -12,6 +12,8 @@
 //   2. per-key prefix over the chunks, block scan over keys -> key offsets
 //   3. scatter: position = key offset + earlier chunks + earlier lanes
 //   4. groups = non-empty keys, tiles of LORA_TILE_ROWS rows per group
+#include <string.h>
+
 #include "lora_internal.cuh"
 
 namespace {
@@ -28,45 +30,6 @@ struct MetaArgs {
     int T, K, E, L, n_keys, n_chunks, cache_keys;
     lora_meta_t m;
 };
-
-// Exclusive scan of data[0..n) in shared memory; returns the total.
-__device__ int block_exclusive_scan(int *data, int n, int *warp_tot) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int nthreads = blockDim.x, nwarps = nthreads >> 5;
-    const int per = (n + nthreads - 1) / nthreads;
-    const int b = min(n, tid * per), e = min(n, b + per);
-    int local = 0;
-    for (int i = b; i < e; ++i) local += data[i];
-    int incl = local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-    }
-    if (lane == 31) warp_tot[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-        int w = lane < nwarps ? warp_tot[lane] : 0;
-        int wi = w;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            int v = __shfl_up_sync(0xffffffffu, wi, o);
-            if (lane >= o) wi += v;
-        }
-        warp_tot[lane] = wi - w;     // exclusive warp base
-        if (lane == 31) warp_tot[32] = wi;
-    }
-    __syncthreads();
-    int run = warp_tot[warp] + incl - local;
-    for (int i = b; i < e; ++i) {
-        int v = data[i];
-        data[i] = run;
-        run += v;
-    }
-    const int total = warp_tot[32];
-    __syncthreads();
-    return total;
-}
 
 // Key of one row given the slot-activity table in shared memory.
 __device__ __forceinline__ int row_key(const MetaArgs &a, const unsigned char *act, int row, int s,
@@ -90,8 +53,8 @@ __device__ __forceinline__ int row_key(const MetaArgs &a, const unsigned char *a
 __global__ void __launch_bounds__(kThreads, 1) build_meta_kernel(MetaArgs a) {
     extern __shared__ int sm[];
     const int NK = a.n_keys, NK1 = NK + 1, W = a.n_chunks;
-    int *hist = sm;                  // [W][NK1]
-    int *cnt = hist + W * NK1;       // [NK1]
+    int *hist = sm;                  // [W][NK1] per-chunk histograms, then 4 scratch rows
+    int *cnt = hist + (W + 4) * NK1; // [NK1]
     int *off = cnt + NK1;            // [NK1]
     int *tmin = off + NK1;           // [NK1] smallest token of each key (dense)
     int *tmax = tmin + NK1;          // [NK1] largest token of each key (dense)
@@ -104,6 +67,9 @@ __global__ void __launch_bounds__(kThreads, 1) build_meta_kernel(MetaArgs a) {
     // let the apply kernel that follows start its prologue; it waits for
     // this grid's completion before reading any metadata
     asm volatile("griddepcontrol.launch_dependents;");
+    // launched with programmatic stream serialization: everything above
+    // overlaps the previous kernel; nothing is read before it has finished
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // issue the first row step's slot loads together with the table loads
     const int chunk = (rows + W - 1) / W;
@@ -141,6 +107,7 @@ __global__ void __launch_bounds__(kThreads, 1) build_meta_kernel(MetaArgs a) {
     }
     __syncthreads();
 
+    // per key: exclusive prefix over the chunks (in place) and the count
     for (int b = tid; b < NK1; b += nthreads) {
         int run = 0;
         for (int w = 0; w < W; ++w) {
@@ -149,10 +116,66 @@ __global__ void __launch_bounds__(kThreads, 1) build_meta_kernel(MetaArgs a) {
             run += c;
         }
         cnt[b] = run;
-        off[b] = run;
     }
     __syncthreads();
-    block_exclusive_scan(off, NK1, misc);
+
+    // every key-space prefix sum in one pass of warp 0: row offsets, group
+    // index, 16-row tiles, long-run tiles and short tiles.  Lane l owns a
+    // contiguous block of keys.
+    int *gidx = hist + W * NK1;  // the four scratch rows after the chunk histograms
+    int *tiles = gidx + NK1;
+    int *lt_cnt = tiles + NK1;
+    int *st_cnt = lt_cnt + NK1;
+    if (warp == 0) {
+        const int per = (NK1 + 31) / 32;
+        const int b0 = min(NK1, lane * per), b1 = min(NK1, b0 + per);
+        int s0 = 0, s1 = 0, s2 = 0, s3 = 0, s4 = 0;
+        for (int b = b0; b < b1; ++b) {
+            const int c = b < NK ? cnt[b] : 0;
+            const bool run = c > 0 && a.K == 1 && c >= LORA_LONG_MIN && tmax[b] - tmin[b] == c - 1;
+            s0 += cnt[b];
+            s1 += c > 0 ? 1 : 0;
+            s2 += (c + LORA_TILE_ROWS - 1) / LORA_TILE_ROWS;
+            s3 += run ? (c + LORA_LTILE_ROWS - 1) / LORA_LTILE_ROWS : 0;
+            s4 += (c > 0 && !run) ? (c + LORA_TILE_ROWS - 1) / LORA_TILE_ROWS : 0;
+        }
+        int e0 = s0, e1 = s1, e2 = s2, e3 = s3, e4 = s4;  // inclusive scans over lanes
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v0 = __shfl_up_sync(0xffffffffu, e0, o), v1 = __shfl_up_sync(0xffffffffu, e1, o);
+            const int v2 = __shfl_up_sync(0xffffffffu, e2, o), v3 = __shfl_up_sync(0xffffffffu, e3, o);
+            const int v4 = __shfl_up_sync(0xffffffffu, e4, o);
+            if (lane >= o) {
+                e0 += v0;
+                e1 += v1;
+                e2 += v2;
+                e3 += v3;
+                e4 += v4;
+            }
+        }
+        int r0s = e0 - s0, r1s = e1 - s1, r2s = e2 - s2, r3s = e3 - s3, r4s = e4 - s4;
+        for (int b = b0; b < b1; ++b) {
+            const int c = b < NK ? cnt[b] : 0;
+            const bool run = c > 0 && a.K == 1 && c >= LORA_LONG_MIN && tmax[b] - tmin[b] == c - 1;
+            off[b] = r0s;
+            gidx[b] = r1s;
+            tiles[b] = r2s;
+            lt_cnt[b] = r3s;
+            st_cnt[b] = r4s;
+            r0s += cnt[b];
+            r1s += c > 0 ? 1 : 0;
+            r2s += (c + LORA_TILE_ROWS - 1) / LORA_TILE_ROWS;
+            r3s += run ? (c + LORA_LTILE_ROWS - 1) / LORA_LTILE_ROWS : 0;
+            r4s += (c > 0 && !run) ? (c + LORA_TILE_ROWS - 1) / LORA_TILE_ROWS : 0;
+        }
+        if (lane == 31) {
+            misc[32] = e1;  // groups
+            misc[33] = e2;  // tiles
+            misc[34] = e3;  // long tiles
+            misc[35] = e4;  // short tiles
+        }
+    }
+    __syncthreads();
     for (int b = tid; b < NK1; b += nthreads) {
         const int o = off[b];
         for (int w = 0; w < W; ++w) hist[w * NK1 + b] += o;
@@ -187,20 +210,9 @@ __global__ void __launch_bounds__(kThreads, 1) build_meta_kernel(MetaArgs a) {
             __syncwarp();
         }
     }
-    __syncthreads();
 
-    // groups (non-empty keys, ascending), 16-row tiles, and the long/short split:
-    // a dense group of >= LORA_LONG_MIN rows whose distinct tokens span exactly
-    // its row count is one contiguous run, cut into 128-row tiles
-    int *gidx = hist, *tiles = hist + NK1;  // reuse of the histogram rows (W >= 2)
-    for (int b = tid; b < NK1; b += nthreads) {
-        const int c = b < NK ? cnt[b] : 0;
-        gidx[b] = c > 0 ? 1 : 0;
-        tiles[b] = (c + LORA_TILE_ROWS - 1) / LORA_TILE_ROWS;
-    }
-    __syncthreads();
-    const int G = block_exclusive_scan(gidx, NK1, misc);
-    const int NT = block_exclusive_scan(tiles, NK1, misc);
+    // groups (non-empty keys, ascending), 16-row tiles, long-run and short tiles
+    const int G = misc[32], NT = misc[33], NL = misc[34], NS = misc[35];
     for (int b = tid; b < NK; b += nthreads) {
         const int c = cnt[b];
         if (c > 0) {
@@ -215,51 +227,31 @@ __global__ void __launch_bounds__(kThreads, 1) build_meta_kernel(MetaArgs a) {
                 a.m.tile_row0[tiles[b] + i] = off[b] + i * LORA_TILE_ROWS;
                 a.m.tile_keyn[tiles[b] + i] = (b << 5) | rows_i;
             }
+            for (int i = 0; lt_cnt[b] + i < lt_cnt[b + 1]; ++i) {
+                const int rows_i = min(LORA_LTILE_ROWS, c - i * LORA_LTILE_ROWS);
+                a.m.ltile_row0[lt_cnt[b] + i] = off[b] + i * LORA_LTILE_ROWS;
+                a.m.ltile_keyn[lt_cnt[b] + i] = (b << 8) | rows_i;
+                a.m.ltile_tok0[lt_cnt[b] + i] = tmin[b] + i * LORA_LTILE_ROWS;
+            }
+            for (int i = 0; st_cnt[b] + i < st_cnt[b + 1]; ++i) {
+                const int rows_i = min(LORA_TILE_ROWS, c - i * LORA_TILE_ROWS);
+                a.m.stile_row0[st_cnt[b] + i] = off[b] + i * LORA_TILE_ROWS;
+                a.m.stile_keyn[st_cnt[b] + i] = (b << 5) | rows_i;
+            }
         } else {
             a.m.key_group[b] = -1;
-        }
-    }
-    __syncthreads();
-    int *lt_cnt = gidx, *st_cnt = tiles;  // reuse
-    for (int b = tid; b < NK1; b += nthreads) {
-        int l = 0, sh = 0;
-        const int c = b < NK ? cnt[b] : 0;
-        if (c > 0) {
-            const bool run = a.K == 1 && c >= LORA_LONG_MIN && tmax[b] - tmin[b] == c - 1;
-            if (run) l = (c + LORA_LTILE_ROWS - 1) / LORA_LTILE_ROWS;
-            else sh = (c + LORA_TILE_ROWS - 1) / LORA_TILE_ROWS;
-        }
-        lt_cnt[b] = l;
-        st_cnt[b] = sh;
-    }
-    __syncthreads();
-    const int NL = block_exclusive_scan(lt_cnt, NK1, misc);
-    const int NS = block_exclusive_scan(st_cnt, NK1, misc);
-    for (int b = tid; b < NK; b += nthreads) {
-        const int c = cnt[b];
-        if (c <= 0) continue;
-        for (int i = 0; lt_cnt[b] + i < lt_cnt[b + 1]; ++i) {
-            const int rows_i = min(LORA_LTILE_ROWS, c - i * LORA_LTILE_ROWS);
-            a.m.ltile_row0[lt_cnt[b] + i] = off[b] + i * LORA_LTILE_ROWS;
-            a.m.ltile_keyn[lt_cnt[b] + i] = (b << 8) | rows_i;
-            a.m.ltile_tok0[lt_cnt[b] + i] = tmin[b] + i * LORA_LTILE_ROWS;
-        }
-        for (int i = 0; st_cnt[b] + i < st_cnt[b + 1]; ++i) {
-            const int rows_i = min(LORA_TILE_ROWS, c - i * LORA_TILE_ROWS);
-            a.m.stile_row0[st_cnt[b] + i] = off[b] + i * LORA_TILE_ROWS;
-            a.m.stile_keyn[st_cnt[b] + i] = (b << 5) | rows_i;
         }
     }
     if (tid == 0) {
         const int n_active = off[NK];
         const int n_bad = misc[36];
-        a.m.counters[4] = NS;
-        a.m.counters[5] = NL;
         a.m.group_start[G] = n_active;
         a.m.counters[0] = n_active;
         a.m.counters[1] = G;
         a.m.counters[2] = n_bad;
         a.m.counters[3] = NT;
+        a.m.counters[4] = NS;
+        a.m.counters[5] = NL;
         if (n_bad) atomicExch(a.status, (int)LORA_ERR_DEVICE_INDEX);
     }
 }
@@ -283,10 +275,11 @@ lora_status_t lora_launch_build_meta(const lora_pool_t *pool, const int32_t *d_i
     if (nthreads < 128) nthreads = 128;
     if (nthreads > kThreads) nthreads = kThreads;
     const int nwarps = nthreads / 32;
-    const long long fixed = 4LL * NK1 + 40 + (L + 3) / 4;
+    // chunk histograms [W][NK1] + 4 scratch rows + cnt, off, tmin, tmax + misc + slot table
+    const long long fixed = 8LL * NK1 + 40 + (L + 3) / 4;
     int W = (int)((kSmemBudgetInts - fixed) / NK1);
     if (W > nwarps) W = nwarps;
-    if (W < 2) return LORA_ERR_CAPACITY;  // the group/tile pass reuses two histogram rows
+    if (W < 1) return LORA_ERR_CAPACITY;
     const long long used = (long long)W * NK1 + fixed;
     const int cache = used + rows <= kSmemBudgetInts ? 1 : 0;
     MetaArgs a;
@@ -312,8 +305,18 @@ lora_status_t lora_launch_build_meta(const lora_pool_t *pool, const int32_t *d_i
                                            kSmemBudgetInts * 4));
         configured[dev] = 1;
     }
-    build_meta_kernel<<<1, nthreads, smem, stream>>>(a);
-    LORA_CUDA_TRY(cudaGetLastError());
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(1, 1, 1);
+    cfg.blockDim = dim3((unsigned)nthreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    LORA_CUDA_TRY(cudaLaunchKernelEx(&cfg, build_meta_kernel, a));
     meta->T = T;
     meta->top_k = top_k;
     meta->n_keys = n_keys;

@@ -47,6 +47,7 @@ struct alignas(64) ShrinkArgs {
     long long v_slice;                   // elements per slice of V
     int *status;
     int spin_limit;
+    float post_scale;
 };
 
 struct alignas(64) ExpandArgs {
@@ -143,7 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1) sgmv_shrink_kernel(const __grid_c
         const int t = q * 32 + lane;
         wait_or_flag(&acc_full, 0, p.spin_limit, p.status);
         tc::tc_fence_after();
-        const float sc = p.scale[key];
+        const float sc = p.scale[key] * p.post_scale;
         for (int c = 0; c < N / 32; ++c) {
             uint32_t r[32];
             tc::tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), r);
@@ -344,6 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1) sgmv_expand_kernel(const __grid_c
         }
         if (leader) tc::bulk_wait0();
     }
+    asm volatile("griddepcontrol.launch_dependents;");
     tc::tc_fence_before();
     __syncthreads();
     if (warp == 1) tc::tmem_dealloc(tmem, 256);
@@ -398,7 +400,8 @@ size_t lora_sgmv_ws_bytes(const lora_pool_t *pool, int rows) {
 }
 
 lora_status_t lora_sgmv_apply(const lora_pool_t *pool, const lora_meta_t *meta, const void *x, int64_t ldx,
-                              void *y, int64_t ldy, void *V, int spin_limit, int num_sms, cudaStream_t s) {
+                              void *y, int64_t ldy, void *V, int spin_limit, int num_sms, float post_scale,
+                              cudaStream_t s) {
     const lora_pool_desc_t &d = pool->desc;
     const int T = meta->T, R = d.max_rank, ns = d.n_slices;
     int out_total = 0;
@@ -432,6 +435,7 @@ lora_status_t lora_sgmv_apply(const lora_pool_t *pool, const lora_meta_t *meta, 
     sa.v_slice = (long long)T * 2 * R;
     sa.status = pool->d_status;
     sa.spin_limit = spin_limit;
+    sa.post_scale = post_scale;
     const size_t a_bytes = (size_t)ns * R * 128;
     const size_t stage = kTileBytes + ((a_bytes + 1023) & ~(size_t)1023);
     const size_t smem_s = kStages * stage + 1024;

@@ -82,8 +82,11 @@ EXPORTS = {
                                   c_vp]),
     "lora_apply_slices_static": (c_i32, [c_vp, ctypes.POINTER(Meta), c_vp, c_i64, c_vp, c_i64, c_vp]),
     "lora_static_scratch_bytes": (c_size, []),
+    "lora_logits_apply": (c_i32, [c_vp, ctypes.POINTER(Meta), c_vp, c_i64, c_vp, c_i64, c_i32, c_vp, c_vp, c_i64,
+                                  c_i32, ctypes.c_float, c_vp, c_size, c_vp]),
     "lora_moe_apply": (c_i32, [c_vp, ctypes.POINTER(Meta), c_i32, c_vp, c_i64, c_vp, c_vp, c_i64, c_vp,
                                c_size, c_vp]),
+    "lora_moe_align_padded": (c_i32, [c_vp, ctypes.POINTER(Meta), c_i32, c_i32, c_vp, c_vp, c_vp, c_vp]),
     "lora_get_device_status": (c_i32, [c_vp, c_vp]),
     "lora_set_spin_limit": (None, [c_i32]),
     "lora_set_kernel_policy": (None, [c_i32]),
@@ -227,9 +230,21 @@ def lora_static_scratch_bytes() -> int:
     return int(lib().lora_static_scratch_bytes())
 
 
+def lora_logits_apply(pool, meta: Meta, hidden, ld_h, logits_in, ld_in, in_cols, mapping, logits_out, ld_out,
+                      vocab_size, mup, ws, ws_bytes, stream=None):
+    _check(lib().lora_logits_apply(pool, ctypes.byref(meta), ptr(hidden), ld_h, ptr(logits_in), ld_in, in_cols,
+                                   ptr(mapping), ptr(logits_out), ld_out, vocab_size, float(mup), ptr(ws),
+                                   ws_bytes, stream_ptr(stream)), "lora_logits_apply")
+
+
 def lora_moe_apply(pool, meta: Meta, which, inp, ld_in, topk_w, out, ld_out, ws, ws_bytes, stream=None):
     _check(lib().lora_moe_apply(pool, ctypes.byref(meta), which, ptr(inp), ld_in, ptr(topk_w), ptr(out),
                                 ld_out, ptr(ws), ws_bytes, stream_ptr(stream)), "lora_moe_apply")
+
+
+def lora_moe_align_padded(pool, meta: Meta, block_m, cap, d_sorted, d_expert, d_npp, stream=None):
+    _check(lib().lora_moe_align_padded(pool, ctypes.byref(meta), block_m, cap, ptr(d_sorted), ptr(d_expert),
+                                       ptr(d_npp), stream_ptr(stream)), "lora_moe_align_padded")
 
 
 def lora_get_device_status(pool, stream=None) -> int:

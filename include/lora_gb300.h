@@ -216,7 +216,7 @@ LORA_API lora_status_t lora_meta_bind(lora_meta_t *meta, void *d_buf, size_t byt
  * pool: d_topk_ids must be NULL.  MoE pool: d_topk_ids is [T][top_k] int32.
  * Rows are counted against the pool's enabled/rank tables as they are on the
  * stream at launch.  Errors: LORA_ERR_INVALID_ARG, LORA_ERR_CAPACITY
- * (T*top_k > max_rows, keys > max_keys, or more than 12288 keys). */
+ * (T*top_k > max_rows, keys > max_keys, or more than 6144 keys). */
 LORA_API lora_status_t lora_build_meta(const lora_pool_t *pool, const int32_t *d_idx, int32_t T,
                               const int32_t *d_topk_ids, int32_t top_k, lora_meta_t *meta,
                               void *stream);
@@ -279,6 +279,28 @@ LORA_API lora_status_t lora_apply_slices_static(const lora_pool_t *pool, const l
 /* Size in bytes of the fixed scratch array used by lora_apply_slices_static. */
 LORA_API size_t lora_static_scratch_bytes(void);
 
+/* lm_head with LoRA, end to end (LogitsProcessorWithLoRA._get_logits of the
+ * vLLM LoRA layer page, with the muP multiplier of the Inkling report's
+ * _lora_forward).  For every token t and column i < vocab_size:
+ *   out[t][i] = mup * ( in[t][mapping[i]] + delta[t][i] )
+ * where in is the gathered base logits [T][ld_in] bf16 (in_cols valid
+ * columns, sharded order), mapping is the device int32 gather index
+ * (sharded_to_full_mapping applied as logits[:, mapping]; NULL = identity),
+ * and delta is the LoRA delta of the pool (a dense pool with one slice whose
+ * width is the padded vocab; add_lora_logits uses scale 1.0, so set_lora the
+ * lm_head adapters with scale 1 for that behaviour).  mup = 1 when the model
+ * has no muP multiplier.  hidden is [T][ld_h] bf16.  logits_out is
+ * [T][ld_out] bf16 with ld_out >= the pool's width; columns in
+ * [vocab_size, width) are scratch.  A mapping entry outside [0, in_cols) sets
+ * LORA_ERR_DEVICE_INDEX and reads column 0.  Workspace as lora_apply_slices.
+ * Errors: LORA_ERR_INVALID_ARG, LORA_ERR_SHAPE (vocab_size > width or
+ * > 257024, in_cols), LORA_ERR_UNSUPPORTED (not a one-slice dense pool). */
+LORA_API lora_status_t lora_logits_apply(const lora_pool_t *pool, const lora_meta_t *meta, const void *hidden,
+                                         int64_t ld_h, const void *logits_in, int64_t ld_in, int32_t in_cols,
+                                         const int32_t *mapping, void *logits_out, int64_t ld_out,
+                                         int32_t vocab_size, float mup, void *workspace, size_t ws_bytes,
+                                         void *stream);
+
 /* ------------------------------------------------------------ MoE compute */
 
 #define LORA_MOE_W13 0
@@ -297,6 +319,21 @@ LORA_API size_t lora_static_scratch_bytes(void);
 LORA_API lora_status_t lora_moe_apply(const lora_pool_t *pool, const lora_meta_t *meta, int32_t which,
                              const void *in, int64_t ld_in, const float *topk_w, void *out,
                              int64_t ld_out, void *workspace, size_t ws_bytes, void *stream);
+
+/* The block-padded form of moe_lora_align_block_size (vLLM
+ * FusedMoEWithLoRA: sorted_token_ids_lora and expert_ids_lora viewed as
+ * (max_loras, -1), num_tokens_post_padded_lora), derived on the device from a
+ * MoE metadata build: for every adapter a, the (token, k) pairs of its keys
+ * (a, e) in ascending expert order, each expert's run padded with the
+ * sentinel T*top_k to a multiple of block_m.
+ *   d_sorted [L][cap]            pair ids and sentinels (unused entries T*top_k)
+ *   d_expert [L][cap / block_m]  expert of each block (unused entries -1)
+ *   d_npp    [L]                 padded length of each adapter (0 if none)
+ * cap must be a multiple of block_m and >= T*top_k + E*(block_m - 1).
+ * Errors: LORA_ERR_INVALID_ARG, LORA_ERR_CAPACITY, LORA_ERR_UNSUPPORTED. */
+LORA_API lora_status_t lora_moe_align_padded(const lora_pool_t *pool, const lora_meta_t *meta, int32_t block_m,
+                                             int32_t cap, int32_t *d_sorted, int32_t *d_expert,
+                                             int32_t *d_npp, void *stream);
 
 /* ------------------------------------------------------------ status */
 

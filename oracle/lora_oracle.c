@@ -321,3 +321,70 @@ void lo_moe_w2(int32_t T, int32_t K, int32_t D, int32_t F, int32_t E, int32_t L,
         free(v);
     }
 }
+
+/* ---------------------------------------------------------------- lm_head */
+
+/* LoRA logits of LogitsProcessorWithLoRA._get_logits (vLLM LoRA layer page),
+ * with the muP multiplier of the Inkling report's _lora_forward:
+ *   full[t][i] = logits_in[t][map[i]]          (sharded_to_full_mapping; map
+ *                                               NULL = identity)
+ *   full[t][i] += delta[t][i]                  (add_lora_logits, scale 1.0:
+ *                                               the delta of lo_dense_delta)
+ *   out[t][i]  = mup * full[t][i]  for i < vocab_size   (slice, then x 1/mup)
+ * delta is the fp32 [T][ld_delta] output of lo_dense_delta on the same tokens. */
+void lo_logits(int32_t T, int32_t vocab_size, const int32_t *map, const uint16_t *logits_in,
+               int64_t ld_in, const float *delta, int64_t ld_delta, float mup, float *out,
+               int64_t ld_out) {
+    for (int32_t t = 0; t < T; ++t) {
+        for (int32_t i = 0; i < vocab_size; ++i) {
+            const int32_t src = map ? map[i] : i;
+            const float full = bf(logits_in[(int64_t)t * ld_in + src]) + delta[(int64_t)t * ld_delta + i];
+            out[(int64_t)t * ld_out + i] = mup * full;
+        }
+    }
+}
+
+/* -------------------------------------------------- MoE block-padded align */
+
+/* The padded per-adapter form of moe_lora_align_block_size (vLLM
+ * FusedMoEWithLoRA._inject_lora_into_fused_moe views sorted_token_ids_lora and
+ * expert_ids_lora as (max_loras, -1) and passes num_tokens_post_padded_lora):
+ * for every enabled adapter a (rank > 0), its pairs p = t*K + k in ascending
+ * expert order (pair order kept within an expert); each expert's run is
+ * padded with the sentinel T*K to a multiple of block_m.
+ *   sorted[a][cap]           pair ids and sentinels; unused entries = T*K
+ *   expert[a][cap / block_m] expert id of each block; unused = -1
+ *   npp[a]                   padded length of adapter a (0 if none)
+ * cap must be a multiple of block_m; returns -1 if an adapter overflows it. */
+int32_t lo_moe_align_padded(int32_t T, int32_t K, int32_t E, int32_t L, const int32_t *topk_ids,
+                            const int32_t *idx, const int32_t *enabled, const int32_t *rank,
+                            int32_t block_m, int32_t cap, int32_t *sorted, int32_t *expert, int32_t *npp) {
+    const int64_t P = (int64_t)T * K;
+    const int32_t nb = cap / block_m;
+    int32_t rc = 0;
+    for (int32_t a = 0; a < L; ++a) {
+        int32_t pos = 0;
+        for (int32_t i = 0; i < cap; ++i) sorted[(int64_t)a * cap + i] = (int32_t)P;
+        for (int32_t b = 0; b < nb; ++b) expert[(int64_t)a * nb + b] = -1;
+        if (is_active(a, L, enabled, rank)) {
+            for (int32_t e = 0; e < E; ++e) {
+                const int32_t start = pos;
+                for (int64_t p = 0; p < P; ++p) {
+                    if (idx[p / K] == a && topk_ids[p] == e) {
+                        if (pos >= cap) return -1;
+                        sorted[(int64_t)a * cap + pos++] = (int32_t)p;
+                    }
+                }
+                if (pos > start) {
+                    const int32_t padded = ((pos - start + block_m - 1) / block_m) * block_m;
+                    if (start + padded > cap) return -1;
+                    for (int32_t b = start / block_m; b < (start + padded) / block_m; ++b)
+                        expert[(int64_t)a * nb + b] = e;
+                    pos = start + padded;
+                }
+            }
+        }
+        npp[a] = pos;
+    }
+    return rc;
+}

@@ -60,6 +60,12 @@ def _bind(path):
     lib.lo_moe_w13.argtypes = [_I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32,
                                _I32P, _I32P, _I32P, _I32P, _F32P, _U16P, _I64, _PP, _PP,
                                _U16P, _I64, _F32P, _F32P, ctypes.c_int]
+    lib.lo_moe_align_padded.restype = _I32
+    lib.lo_moe_align_padded.argtypes = [_I32, _I32, _I32, _I32, _I32P, _I32P, _I32P, _I32P, _I32, _I32, _I32P,
+                                        _I32P, _I32P]
+    lib.lo_logits.restype = None
+    lib.lo_logits.argtypes = [_I32, _I32, ctypes.c_void_p, _U16P, _I64, _F32P, _I64, ctypes.c_float, _F32P,
+                              _I64]
     lib.lo_moe_w2.restype = None
     lib.lo_moe_w2.argtypes = [_I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32,
                               _I32P, _I32P, _F32P, _I32P, _I32P, _F32P, _U16P, _I64,
@@ -224,4 +230,32 @@ def moe_w2(c, *, ic3_in=None, threads: int = 0, idx=None, enabled=None):
     return out, dl
 
 
-__all__ = ["build", "use_library", "compile_variant", "source_text", "max_threads", "dense_meta", "dense_delta", "moe_meta", "moe_w13", "moe_w2"]
+def moe_align_padded(topk_ids, idx, L, E, enabled, rank, block_m, cap):
+    """Block-padded per-adapter alignment (see lora_oracle.c)."""
+    lib = _load()
+    topk_ids = _c(topk_ids, np.int32)
+    T, K = topk_ids.shape
+    sorted_ = np.empty((L, cap), np.int32)
+    expert = np.empty((L, cap // block_m), np.int32)
+    npp = np.empty(L, np.int32)
+    rc = lib.lo_moe_align_padded(T, K, E, L, topk_ids, _c(idx, np.int32), _c(enabled, np.int32),
+                                 _c(rank, np.int32), block_m, cap, sorted_, expert, npp)
+    assert rc == 0, "capacity"
+    return SimpleNamespace(sorted=sorted_, expert=expert, npp=npp)
+
+
+def logits(logits_in, delta, vocab_size, mapping=None, mup=1.0):
+    """lm_head with LoRA: reindex the sharded logits, add the delta (from
+    dense_delta), keep the first vocab_size columns, multiply by mup."""
+    lib = _load()
+    logits_in = _c(logits_in, np.uint16)
+    delta = _c(delta, np.float32)
+    T = logits_in.shape[0]
+    out = np.empty((T, vocab_size), np.float32)
+    m = None if mapping is None else _c(mapping, np.int32)
+    lib.lo_logits(T, vocab_size, None if m is None else m.ctypes.data, logits_in, logits_in.shape[1], delta,
+                  delta.shape[1], float(mup), out, vocab_size)
+    return out
+
+
+__all__ = ["logits", "moe_align_padded", "build", "use_library", "compile_variant", "source_text", "max_threads", "dense_meta", "dense_delta", "moe_meta", "moe_w13", "moe_w2"]

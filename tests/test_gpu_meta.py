@@ -149,3 +149,25 @@ def test_long_tiles_need_one_contiguous_run():
     idx[450:550] = 1
     idx[600:640] = 2
     _check_dense(idx, 4, np.full(4, 16, np.int32), None)
+
+
+@pytest.mark.parametrize("bm", [4, 16, 64])
+def test_moe_align_padded_matches_oracle(bm):
+    for c in (gen.moe(), gen.moe_case(T=57, K=3, E=7, D=16, F=16, L=4, R=8, seed=9, p_none=0.2,
+                                      ranks=(8, 0, 8, 8))):
+        run = H.MoERun(c)
+        try:
+            run.build_meta()
+            P = c.T * c.K
+            cap = ((P + c.E * (bm - 1) + bm - 1) // bm) * bm
+            ds = torch.empty((c.L, cap), dtype=torch.int32, device="cuda")
+            de = torch.empty((c.L, cap // bm), dtype=torch.int32, device="cuda")
+            dn = torch.empty(c.L, dtype=torch.int32, device="cuda")
+            L.lora_moe_align_padded(run.pool, run.mb.meta, bm, cap, ds, de, dn)
+            got_s, got_e, got_n = ds.cpu().numpy(), de.cpu().numpy(), dn.cpu().numpy()
+        finally:
+            run.close()
+        ref = oracle.moe_align_padded(c.topk_ids, c.idx, c.L, c.E, c.enabled, c.ranks, bm, cap)
+        assert np.array_equal(got_n, ref.npp)
+        assert np.array_equal(got_s, ref.sorted)
+        assert np.array_equal(got_e, ref.expert)

@@ -276,6 +276,10 @@ MUTANTS = {
     "moe_w13_wrong_token": ("acc += bf(x[(int64_t)t * ldx + h])", "acc += bf(x[(int64_t)(p % T) * ldx + h])"),
     "moe_w2_shared_b_per_expert": ("const int32_t eb = shared_outer ? 0 : e;",
                                    "const int32_t eb = shared_outer ? (e % EB) : (E - 1 - e);"),
+    "logits_reindex_inverted": ("const int32_t src = map ? map[i] : i;",
+                                "const int32_t src = map ? (map[i] ^ 1) : i;"),
+    "logits_mup_on_base_only": ("out[(int64_t)t * ld_out + i] = mup * full;",
+                                "out[(int64_t)t * ld_out + i] = full + (mup - 1.0f) * bf(logits_in[(int64_t)t * ld_in + src]);"),
 }
 
 
@@ -284,7 +288,8 @@ def _pin_suite_passes():
               lambda: test_dense_bruteforce_fp64(0), lambda: test_moe_bruteforce_fp64(0, False),
               lambda: test_moe_bruteforce_fp64(1, True), test_merged_weight_identity_tiny_preset,
               test_packed_slices_equal_separate_application,
-              lambda: test_dense_meta_matches_numpy_stable_argsort(0)]
+              lambda: test_dense_meta_matches_numpy_stable_argsort(0),
+              test_golden_logits_reindex_example, test_logits_adds_delta_then_scales_everything_by_mup]
     for chk in checks:
         try:
             chk()
@@ -301,3 +306,68 @@ def test_planted_mistake_is_caught(name, tmp_path):
     lib = oracle.compile_variant(src.replace(old, new), str(tmp_path / f"mut_{name}.so"))
     with oracle.use_library(lib):
         assert not _pin_suite_passes(), f"pins did not catch mutant {name}"
+
+
+# ----------------------------------------------------------------- lm_head
+
+def test_golden_logits_reindex_example():
+    g = load_golden("logits_reindex.json")
+    sharded = np.asarray(g["sharded_token_ids"])
+    full = np.asarray(g["full_token_ids"])
+    # the two printed mappings: a gather reproduces the printed orders with the
+    # derived mapping, and a scatter with the printed one
+    assert np.array_equal(sharded[np.asarray(g["gather_mapping"])], full)
+    scat = np.empty_like(sharded)
+    scat[np.asarray(g["printed_mapping"])] = sharded
+    assert np.array_equal(scat, full)
+    row = np.where(sharded < 0, 100.0, sharded).astype(np.float32)
+    lin = f32_to_bf16_bits(np.stack([row, row * 2]))
+    out = oracle.logits(lin, np.zeros((2, 8), np.float32), g["vocab_size"], mapping=g["gather_mapping"])
+    np.testing.assert_array_equal(out[0], np.asarray(g["expected_row"], np.float32))
+    np.testing.assert_array_equal(out[1], 2 * np.asarray(g["expected_row"], np.float32))
+
+
+def test_logits_adds_delta_then_scales_everything_by_mup():
+    """The Inkling report's _lora_forward multiplies base + LoRA logits by
+    1/mup_multiplier, so the delta is scaled too."""
+    rng = np.random.default_rng(3)
+    base = f32_to_bf16_bits(rng.normal(0, 1, (3, 16)).astype(np.float32))
+    delta = rng.normal(0, 0.1, (3, 16)).astype(np.float32)
+    out = oracle.logits(base, delta, 12, mup=0.25)
+    exp = 0.25 * (bf16_bits_to_f32(base)[:, :12].astype(np.float64) + delta[:, :12])
+    assert np.allclose(out, exp, rtol=1e-6, atol=1e-7)
+    out1 = oracle.logits(base, np.zeros_like(delta), 12, mup=1.0)
+    assert np.array_equal(out1, bf16_bits_to_f32(base)[:, :12])
+
+
+# ----------------------------------------------------------------- MoE block-padded alignment
+
+def test_golden_moe_align_padded_by_hand():
+    g = load_golden("moe_align_padded_by_hand.json")
+    m = oracle.moe_align_padded(np.asarray(g["topk_ids"], np.int32), np.asarray(g["idx"], np.int32), g["L"], g["E"],
+                                np.asarray(g["enabled"], np.int32), np.asarray(g["rank"], np.int32), g["block_m"],
+                                g["cap"])
+    assert m.sorted.tolist() == g["sorted"]
+    assert m.expert.tolist() == g["expert"]
+    assert m.npp.tolist() == g["npp"]
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_moe_align_padded_consistent_with_unpadded_meta(seed):
+    """Dropping the sentinels of adapter a's padded list gives exactly the
+    unpadded sorted pairs of a's keys; block counts follow ceil(count / BM)."""
+    rng = np.random.default_rng(200 + seed)
+    T, K, E, L, BM = 37, 3, 6, 4, 8
+    topk = rng.integers(0, E, size=(T, K)).astype(np.int32)
+    idx = rng.integers(-1, L, size=T).astype(np.int32)
+    en, rk = np.array([1, 1, 0, 1], np.int32), np.array([8, 0, 8, 8], np.int32)
+    cap = ((T * K + E * (BM - 1) + BM - 1) // BM) * BM
+    pad = oracle.moe_align_padded(topk, idx, L, E, en, rk, BM, cap)
+    un = oracle.moe_meta(topk, idx, L, E, en, rk)
+    for a in range(L):
+        got = pad.sorted[a][pad.sorted[a] != T * K]
+        lo, hi = un.key_offset[a * E], un.key_offset[(a + 1) * E]
+        assert np.array_equal(got, un.sorted_pair[lo:hi])
+        blocks = sum(-(-int(c) // BM) for c in un.key_count[a * E:(a + 1) * E])
+        assert pad.npp[a] == blocks * BM
+        assert np.sum(pad.expert[a] >= 0) == blocks

@@ -65,6 +65,20 @@ def is_moe(name):
     return name.startswith("moe")
 
 
+def apply_kernels(name, policy):
+    """The kernels one apply call launches for this workload (the roofline's
+    'dominant kernel': the apply's launches, timed together)."""
+    if policy == 1:
+        k = "grouped_lora_kernel (persistent split-K)"
+    elif policy == 2:
+        k = "cluster_lora_kernel (one pass, cluster DSMEM reduction)"
+    else:
+        k = "bgmv_shrink_kernel + bgmv_expand_kernel (chained by programmatic dependent launch)"
+    if name == "prefill_gate_up" and policy != 1:
+        k = "sgmv_shrink_kernel + sgmv_expand_kernel (tcgen05, 128-row runs); short tiles: " + k
+    return k + (" for w13 and w2" if is_moe(name) else "")
+
+
 # ----------------------------------------------------------------- algorithmic bytes
 
 def dense_algorithmic_bytes(c):
@@ -299,6 +313,7 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     L.lib()
+    L.lora_set_kernel_policy(args.kernel_policy)
     name = args.workload
     c = make_case(name)
     moe = is_moe(name)
@@ -325,8 +340,10 @@ def run_gpu(args, rank, world, local_rank):
         graphs = []
         for r in runs:
             g = torch.cuda.CUDAGraph()
+            n0 = L.lora_kernel_launch_count()
             with torch.cuda.graph(g, stream=stream):
                 step(r)
+            launches_per_step = L.lora_kernel_launch_count() - n0
             graphs.append(g)
         for i in range(args.warmup):
             graphs[i % n_rot].replay()
@@ -430,7 +447,6 @@ def run_gpu(args, rank, world, local_rank):
     peak, peak_kind = load_peaks()
     kbytes = (ab["w13"] + ab["w2"]) if moe else (ab["total"] - ab["idx"])
     achieved = kbytes / (kms * 1e-3) / 1e9
-    launches_per_step = 3 if moe else 2
     line = {
         "metric": "LoRA-delta tokens/s", "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
@@ -444,8 +460,8 @@ def run_gpu(args, rank, world, local_rank):
                          f"({n_rot * foot / 1e6:.0f} MB of algorithmic bytes, L2 {l2 / 1e6:.0f} MB)",
                    "timing": "CUDA graph per step (metadata + apply), K replays between CUDA events",
                    "parallelism": f"replicas{world}"},
-        "roofline": {"bound": "hbm", "kernel": "grouped_lora_kernel (fused shrink+expand)" if not moe
-                     else "grouped_lora_kernel (w13 + w2)", "achieved": achieved, "peak": peak,
+        "roofline": {"bound": "hbm", "kernel": apply_kernels(name, args.kernel_policy),
+                     "achieved": achieved, "peak": peak,
                      "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s", "frac": achieved / peak,
                      "traffic": ncu_traffic(name, kname),
                      "algorithmic_bytes_per_launch": kbytes, "avg_launch_us": kms * 1e3},
@@ -471,6 +487,8 @@ def main():
     ap.add_argument("--clock-seconds", type=float, default=1.0)
     ap.add_argument("--cpu-seconds", type=float, default=2.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel-policy", type=int, default=0, choices=[0, 1, 2],
+                    help="0 automatic, 1 persistent split-K kernel, 2 cluster kernel first (tuning)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -1,0 +1,516 @@
+// Split BGMV: the multi-tenant LoRA delta for small row groups (decode
+// tokens, MoE (adapter, expert) groups) as two kernels chained by
+// programmatic dependent launch, so that the expand's weight and output
+// traffic overlaps the shrink.
+//
+// The vLLM LoRA layer pages compute add_shrink into a zeroed fp32 buffer
+// [n_slices][T][rank] (scale 1.0) and add_expand with add_input=True at the
+// slice offsets; add_lora_fused_moe does the same per (adapter, expert).
+//
+//   bgmv_shrink_kernel: one CTA per (16-row tile, slice j, hidden chunk c).
+//     Bulk copies (cp.async.bulk + mbarrier) bring the tile's x rows and the
+//     slot's A_j rows of chunk c; m16n8k16 bf16 MMAs (fp32 accumulate) give
+//     the partial v; the CTA that finishes last for (tile, j) -- found with an
+//     arrival counter it resets afterwards -- sums the chunks in order, scales
+//     by scale[a] (and the routed weight for MoE w2) and stores fp32 v.
+//   bgmv_expand_kernel: one CTA per (tile, 256 output columns).  Before it
+//     waits for the shrink it bulk-copies its B rows and y rows; then it
+//     reads v, splits it into bf16 hi + lo (the expand keeps the fp32
+//     intermediate to ~16 bits), runs the MMAs, updates y in shared memory
+//     and writes the rows back with bulk copies.
+#include <string.h>
+
+#include "lora_internal.cuh"
+#include "mma_common.cuh"
+
+namespace {
+
+using namespace bgmv;
+
+constexpr int kThreads = 128;
+constexpr int kWarps = kThreads / 32;
+constexpr int kTileRows = LORA_TILE_ROWS;
+constexpr int kOC = 256;  // output columns per expand CTA
+
+struct SArgs {
+    int n_slices, in_dim, E, row_div, R, R8;
+    const uint16_t *A[LORA_MAX_SLICES];
+    long long A_ss[LORA_MAX_SLICES], A_es[LORA_MAX_SLICES];
+    const int32_t *rank;
+    const float *scale;
+    const int32_t *sorted, *tile_row0, *tile_keyn, *counters;
+    int count_idx;
+    const uint16_t *in;
+    long long ld_in;
+    const float *row_w;
+    float post_scale;
+    int NC, HC, SC;          // hidden chunks, chunk length, stage length (elements)
+    int xs_stride, as_stride;
+    int off_x, off_a, x_stage_bytes, a_stage_bytes, off_red;
+    float *part;             // [NC][n_slices][rows][R8]
+    float *v;                // [n_slices][rows][R8] scaled
+    int *arrive;             // [max_tiles][n_slices]
+    int rows;
+    int *status;
+    int spin_limit;
+};
+
+struct EArgs {
+    int n_slices, R, R8, E, out_total;
+    int out_w[LORA_MAX_SLICES], out_off[LORA_MAX_SLICES];
+    const uint16_t *B[LORA_MAX_SLICES];
+    long long B_ss[LORA_MAX_SLICES];
+    int B_shared[LORA_MAX_SLICES];
+    const int32_t *rank;
+    const int32_t *sorted, *tile_row0, *tile_keyn, *counters;
+    int count_idx;
+    uint16_t *out;
+    long long ld_out;
+    const float *v;
+    int rows;
+    int n_oc;
+    int ys_stride, vr_stride;
+    int off_b, off_ys, off_vh, off_vl;
+    int *status;
+    int spin_limit;
+};
+
+// ---------------------------------------------------------------- shrink
+
+__global__ void __launch_bounds__(kThreads) bgmv_shrink_kernel(const __grid_constant__ SArgs p) {
+    extern __shared__ __align__(128) char smem[];
+    __shared__ __align__(8) uint64_t full[2];
+    __shared__ int s_rows[kTileRows];
+    __shared__ int s_last;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, c4 = lane & 3;
+    const int per_tile = p.n_slices * p.NC;
+    const int tile = blockIdx.x / per_tile;
+    const int rem = blockIdx.x - tile * per_tile;
+    const int j = rem / p.NC, c = rem - j * p.NC;
+
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int n_tiles = p.counters[p.count_idx];
+    const int row0 = p.tile_row0[tile];
+    const int keyn = p.tile_keyn[tile];
+    if (tile >= n_tiles) return;
+    // the expand may launch and prefetch its weights and outputs now
+    asm volatile("griddepcontrol.launch_dependents;");
+    const int n = keyn & 31, key = keyn >> 5;
+    const int a = key / p.E, e = key - a * p.E;
+    const int r = p.rank[a];
+    const uint16_t *Ab = p.A[j] + (long long)a * p.A_ss[j] + (long long)e * p.A_es[j];
+    const int hb = c * p.HC, he = min(p.in_dim, hb + p.HC);
+    const int n_sub = (he - hb + p.SC - 1) / p.SC;
+    if (tid < n) s_rows[tid] = p.sorted[row0 + tid];
+    if (tid == 0) {
+        mbar_init(&full[0], 1);
+        mbar_init(&full[1], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    auto issue = [&](int s) {
+        const int h0 = hb + s * p.SC, len = min(p.SC, he - h0), st = s & 1;
+        uint16_t *xs = (uint16_t *)(smem + p.off_x + st * p.x_stage_bytes);
+        uint16_t *as = (uint16_t *)(smem + p.off_a + st * p.a_stage_bytes);
+        const uint32_t rowb = (uint32_t)len * 2;
+        if (lane == 0) mbar_expect_tx(&full[st], rowb * (uint32_t)(n + r));
+        __syncwarp();
+        for (int i = lane; i < n + r; i += 32) {
+            if (i < n)
+                bulk_g2s(xs + i * p.xs_stride, p.in + (long long)(s_rows[i] / p.row_div) * p.ld_in + h0, rowb,
+                         &full[st]);
+            else
+                bulk_g2s(as + (i - n) * p.as_stride, Ab + (long long)(i - n) * p.in_dim + h0, rowb, &full[st]);
+        }
+    };
+    if (warp == 0)
+        for (int s = 0; s < min(n_sub, 2); ++s) issue(s);
+
+    // units: (n-block of 8 ranks, hidden split) spread over the 4 warps, <= 2 each
+    const int nnb = (r + 7) >> 3;
+    int hsplit = 1;
+    while (nnb * hsplit * 2 <= 2 * kWarps && hsplit < 4) hsplit *= 2;
+    const int units = nnb * hsplit;
+    float acc[2][4];
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[u][i] = 0.f;
+    for (int s = 0; s < n_sub; ++s) {
+        const int st = s & 1;
+        mbar_wait(&full[st], (uint32_t)((s >> 1) & 1), p.spin_limit, p.status);
+        const int len = min(p.SC, he - hb - s * p.SC);
+        const int steps = (len + 15) >> 4;
+        const uint16_t *xs = (const uint16_t *)(smem + p.off_x + st * p.x_stage_bytes);
+        const uint16_t *as = (const uint16_t *)(smem + p.off_a + st * p.a_stage_bytes);
+#pragma unroll
+        for (int ui = 0; ui < 2; ++ui) {
+            const int u = warp + ui * kWarps;
+            if (u < units) {
+                const int nb = u / hsplit, hs = u - nb * hsplit;
+                for (int i = hs; i < steps; i += hsplit) {
+                    const int k0 = i * 16;
+                    uint32_t a0, a1, a2, a3, b0, b1;
+                    ldsm_x4(xs + ((lane & 7) + ((lane >> 3) & 1) * 8) * p.xs_stride + k0 + (lane >> 4) * 8,
+                            a0, a1, a2, a3);
+                    ldsm_x2(as + (nb * 8 + (lane & 7)) * p.as_stride + k0 + ((lane >> 3) & 1) * 8, b0, b1);
+                    if (k0 + 8 >= len) a2 = a3 = b1 = 0u;
+                    mma16816(acc[ui], a0, a1, a2, a3, b0, b1);
+                }
+            }
+        }
+        __syncthreads();
+        if (warp == 0 && s + 2 < n_sub) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue(s + 2);
+        }
+    }
+
+    // partials of this chunk: [hsplit][16][R8] in shared memory, summed over
+    // the hidden split, then one row of R8 floats per token to global memory
+    float *red = (float *)(smem + p.off_red);
+    for (int i = tid; i < hsplit * kTileRows * p.R8; i += kThreads) red[i] = 0.f;
+    __syncthreads();
+#pragma unroll
+    for (int ui = 0; ui < 2; ++ui) {
+        const int u = warp + ui * kWarps;
+        if (u < units) {
+            const int nb = u / hsplit, hs = u - nb * hsplit;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int k = nb * 8 + 2 * c4 + h;
+                if (k < r) {
+                    float *dst = red + (hs * kTileRows) * p.R8 + k;
+                    if (g < n) dst[g * p.R8] = acc[ui][h];
+                    if (g + 8 < n) dst[(g + 8) * p.R8] = acc[ui][2 + h];
+                }
+            }
+        }
+    }
+    __syncthreads();
+    const long long vrow0 = (long long)j * p.rows + row0;  // row of v / of this chunk's partial
+    float *dst = p.NC == 1 ? p.v : p.part + (long long)c * p.n_slices * p.rows * p.R8;
+    const float sc = p.scale[a] * p.post_scale;
+    for (int i = tid; i < n * p.R8; i += kThreads) {
+        const int t = i / p.R8, k = i - t * p.R8;
+        float s = 0.f;
+        for (int hs = 0; hs < hsplit; ++hs) s += red[(hs * kTileRows + t) * p.R8 + k];
+        if (p.NC == 1) {
+            float w = sc;
+            if (p.row_w) w *= p.row_w[s_rows[t]];
+            s *= w;
+        }
+        dst[(vrow0 + t) * p.R8 + k] = s;
+    }
+    if (p.NC == 1) return;
+
+    // the last chunk CTA of (tile, j) sums the chunks in order and stores v
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        s_last = atomicAdd(p.arrive + tile * p.n_slices + j, 1) == p.NC - 1;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    const long long cstride = (long long)p.n_slices * p.rows * p.R8;
+    for (int i = tid; i < n * p.R8; i += kThreads) {
+        const int t = i / p.R8, k = i - t * p.R8;
+        const float *src = p.part + (vrow0 + t) * p.R8 + k;
+        float s = 0.f;
+        for (int cc = 0; cc < p.NC; ++cc) s += __ldcg(src + cc * cstride);
+        float w = sc;
+        if (p.row_w) w *= p.row_w[s_rows[t]];
+        p.v[(vrow0 + t) * p.R8 + k] = s * w;
+    }
+    if (tid == 0) p.arrive[tile * p.n_slices + j] = 0;  // ready for the next call
+}
+
+// ---------------------------------------------------------------- expand
+
+__global__ void __launch_bounds__(kThreads) bgmv_expand_kernel(const __grid_constant__ EArgs p) {
+    extern __shared__ __align__(128) char smem[];
+    __shared__ __align__(8) uint64_t bbar, ybar;
+    __shared__ int s_rows[kTileRows];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, c4 = lane & 3;
+    const int tile = blockIdx.x / p.n_oc;
+    const int oc = blockIdx.x - tile * p.n_oc;
+
+    // the metadata was complete before the shrink started: read it at once
+    const int n_tiles = p.counters[p.count_idx];
+    const int row0 = p.tile_row0[tile];
+    const int keyn = p.tile_keyn[tile];
+    if (tile >= n_tiles) return;
+    const int n = keyn & 31, key = keyn >> 5;
+    const int a = key / p.E, e = key - a * p.E;
+    const int r = p.rank[a];
+    const int rs = (r + 7) & ~7;
+    const int ns = p.n_slices;
+    const int ob = oc * kOC, oe = min(p.out_total, ob + kOC);
+    if (tid < n) s_rows[tid] = p.sorted[row0 + tid];
+    if (tid == 0) {
+        mbar_init(&bbar, 1);
+        mbar_init(&ybar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    uint16_t *bs = (uint16_t *)(smem + p.off_b);
+    uint16_t *ys = (uint16_t *)(smem + p.off_ys);
+    // weights and outputs do not depend on the shrink: fetch them first
+    if (warp == 0) {
+        const uint32_t rowb = (uint32_t)(oe - ob) * 2;
+        if (lane == 0) mbar_expect_tx(&ybar, rowb * (uint32_t)n);
+        __syncwarp();
+        if (lane < n) bulk_g2s(ys + lane * p.ys_stride, p.out + (long long)s_rows[lane] * p.ld_out + ob, rowb, &ybar);
+    } else if (warp == 1) {
+        if (lane == 0) mbar_expect_tx(&bbar, (uint32_t)(oe - ob) * rs * 2);
+        __syncwarp();
+        if (lane < ns) {
+            const int jj = lane;
+            const int s0 = max(ob, p.out_off[jj]), s1 = min(oe, p.out_off[jj] + p.out_w[jj]);
+            if (s1 > s0) {
+                const uint16_t *Bj = p.B[jj] + (long long)a * p.B_ss[jj] +
+                                     (p.B_shared[jj] ? 0ll : (long long)e * p.out_w[jj] * rs);
+                bulk_g2s(bs + (long long)(s0 - ob) * rs, Bj + (long long)(s0 - p.out_off[jj]) * rs,
+                         (uint32_t)(s1 - s0) * rs * 2, &bbar);
+            }
+        }
+    }
+
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // v of the shrink is complete
+    // v of the slices this CTA touches -> bf16 hi / lo, [16][vr_stride] at j * R8 + k
+    uint16_t *vh = (uint16_t *)(smem + p.off_vh);
+    uint16_t *vl = (uint16_t *)(smem + p.off_vl);
+    int j0 = 0, j1 = 0;
+    while (j0 + 1 < ns && ob >= p.out_off[j0 + 1]) ++j0;
+    j1 = j0;
+    while (j1 + 1 < ns && oe > p.out_off[j1 + 1]) ++j1;
+    const int per_t = (j1 - j0 + 1) * p.R8 / 4;
+    for (int i = tid; i < kTileRows * per_t; i += kThreads) {
+        const int t = i / per_t, q = i - t * per_t;
+        const int jj = j0 + (q * 4) / p.R8, k = (q * 4) % p.R8;
+        float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (t < n) s4 = __ldcg((const float4 *)(p.v + ((long long)jj * p.rows + row0 + t) * p.R8 + k));
+        const __nv_bfloat162 h01 = __floats2bfloat162_rn(s4.x, s4.y);
+        const __nv_bfloat162 h23 = __floats2bfloat162_rn(s4.z, s4.w);
+        const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+        uint2 hv, lv;
+        hv.x = *(const uint32_t *)&h01;
+        hv.y = *(const uint32_t *)&h23;
+        lv.x = pack_bf16x2(s4.x - f01.x, s4.y - f01.y);
+        lv.y = pack_bf16x2(s4.z - f23.x, s4.w - f23.y);
+        *(uint2 *)(vh + t * p.vr_stride + jj * p.R8 + k) = hv;
+        *(uint2 *)(vl + t * p.vr_stride + jj * p.R8 + k) = lv;
+    }
+    __syncthreads();
+    mbar_wait(&bbar, 0, p.spin_limit, p.status);
+    mbar_wait(&ybar, 0, p.spin_limit, p.status);
+
+    const int nob = (oe - ob) >> 3;
+    const int ksteps = (rs + 15) >> 4;
+    const int arow = (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll 1
+    for (int ob8 = warp; ob8 < nob; ob8 += kWarps) {
+        const int o0 = ob + ob8 * 8;
+        int jj = j0;
+        while (jj + 1 < ns && o0 >= p.out_off[jj + 1]) ++jj;
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int ks = 0; ks < ksteps; ++ks) {
+            const int k0 = ks * 16;
+            uint32_t h0, h1, h2, h3, l0, l1, l2, l3, b0, b1;
+            const int acol = jj * p.R8 + k0 + (lane >> 4) * 8;
+            ldsm_x4(vh + arow * p.vr_stride + acol, h0, h1, h2, h3);
+            ldsm_x4(vl + arow * p.vr_stride + acol, l0, l1, l2, l3);
+            ldsm_x2(bs + (ob8 * 8 + (lane & 7)) * rs + k0 + ((lane >> 3) & 1) * 8, b0, b1);
+            if (k0 + 8 >= rs) h2 = h3 = l2 = l3 = b1 = 0u;
+            mma16816(d, h0, h1, h2, h3, b0, b1);
+            mma16816(d, l0, l1, l2, l3, b0, b1);
+        }
+        const int ocol = ob8 * 8 + 2 * c4;
+        if (g < n) {
+            uint32_t *yp = (uint32_t *)(ys + g * p.ys_stride + ocol);
+            const uint32_t u = *yp;
+            *yp = pack_bf16x2(bf16lo(u) + d[0], bf16hi(u) + d[1]);
+        }
+        if (g + 8 < n) {
+            uint32_t *yp = (uint32_t *)(ys + (g + 8) * p.ys_stride + ocol);
+            const uint32_t u = *yp;
+            *yp = pack_bf16x2(bf16lo(u) + d[2], bf16hi(u) + d[3]);
+        }
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();
+    if (warp == 0 && lane < n) {
+        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                         p.out + (long long)s_rows[lane] * p.ld_out + ob),
+                     "r"(smem_u32(ys + lane * p.ys_stride)), "r"((uint32_t)(oe - ob) * 2)
+                     : "memory");
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    }
+    asm volatile("griddepcontrol.launch_dependents;");
+}
+
+size_t a128(size_t x) { return (x + 127) & ~(size_t)127; }
+
+int g_split_configured[64];
+
+}  // namespace
+
+size_t lora_split_ws_bytes(int n_slices, int in_dim, int R, int rows, int max_tiles) {
+    const int R8 = lora_round8(R);
+    int HC = (16384 / (R8 > 0 ? R8 : 8) + 63) / 64 * 64;
+    if (HC < 256) HC = 256;
+    int NC = lora_ceil_div(in_dim, HC);
+    if (NC > 8) NC = 8;
+    const size_t part = NC > 1 ? (size_t)NC * n_slices * rows * R8 * 4 : 0;
+    const size_t v = (size_t)n_slices * rows * R8 * 4;
+    const size_t arrive = (size_t)max_tiles * n_slices * 4;
+    return a128(part) + a128(v) + a128(arrive);
+}
+
+lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, void *ws, size_t ws_bytes,
+                               cudaStream_t s, bool *launched) {
+    *launched = false;
+    const int ns = pr.n_slices, R = pr.R, R8 = lora_round8(R);
+    int out_total = 0;
+    for (int j = 0; j < ns; ++j) out_total = max(out_total, pr.out_off[j] + pr.out_w[j]);
+    const long long max_tiles = pr.rows / kTileRows + (pr.rows < pr.n_keys ? pr.rows : pr.n_keys);
+    // the shrink holds at most two 8-rank MMA column blocks per warp
+    if (R8 > 2 * kWarps * 8 || max_tiles <= 0) return LORA_OK;
+    // hidden chunks: ~32 KB of A rows per shrink CTA at full rank, at most 8
+    int HC = (16384 / R8 + 63) / 64 * 64;
+    if (HC < 256) HC = 256;
+    int NC = lora_ceil_div(pr.in_dim, HC);
+    if (NC > 8) NC = 8;
+    HC = ((lora_ceil_div(pr.in_dim, NC) + 15) / 16) * 16;
+    NC = lora_ceil_div(pr.in_dim, HC);
+    const size_t need = lora_split_ws_bytes(ns, pr.in_dim, R, pr.rows, (int)max_tiles + 1);
+    if (!ws || ws_bytes < need || !lora_aligned16(ws)) return LORA_OK;
+    // shrink shared memory: 2 stages of (16 x rows + R x rows) of SC elements, then the partial sums
+    int SC = HC;
+    const int red_bytes = 4 * kTileRows * R8 * 4;
+    auto stage_total = [&](int sc) { return 2 * (a128((size_t)kTileRows * (sc + 8) * 2) + a128((size_t)R8 * (sc + 8) * 2)); };
+    while (SC > 256 && stage_total(SC) + red_bytes > 100 * 1024) SC = ((SC / 2) + 15) / 16 * 16;
+    const size_t s_smem = stage_total(SC) + red_bytes;
+    if (s_smem > 200 * 1024) return LORA_OK;
+    // expand shared memory: B rows, y rows, v hi/lo
+    const int vr_stride = ns * R8 + 8;
+    const size_t e_b = a128((size_t)kOC * R8 * 2 + 32), e_y = a128((size_t)kTileRows * (kOC + 8) * 2);
+    const size_t e_v = a128((size_t)kTileRows * vr_stride * 2);
+    const size_t e_smem = e_b + e_y + 2 * e_v;
+
+    char *w = (char *)ws;
+    float *part = NC > 1 ? (float *)w : nullptr;
+    w += a128(NC > 1 ? (size_t)NC * ns * pr.rows * R8 * 4 : 0);
+    float *v = (float *)w;
+    w += a128((size_t)ns * pr.rows * R8 * 4);
+    int *arrive = (int *)w;
+
+    const int dev = pool->device < 64 ? pool->device : 63;
+    if (!g_split_configured[dev]) {
+        LORA_CUDA_TRY(cudaFuncSetAttribute(bgmv_shrink_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           200 * 1024));
+        LORA_CUDA_TRY(cudaFuncSetAttribute(bgmv_expand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           200 * 1024));
+        g_split_configured[dev] = 1;
+    }
+
+    SArgs sa;
+    memset(&sa, 0, sizeof(sa));
+    sa.n_slices = ns;
+    sa.in_dim = pr.in_dim;
+    sa.E = pr.E;
+    sa.row_div = pr.row_div;
+    sa.R = R;
+    sa.R8 = R8;
+    for (int j = 0; j < ns; ++j) {
+        sa.A[j] = pr.A[j];
+        sa.A_ss[j] = pr.A_ss[j];
+        sa.A_es[j] = pr.A_es[j];
+    }
+    sa.rank = pr.rank;
+    sa.scale = pr.scale;
+    sa.sorted = pr.meta->sorted;
+    sa.tile_row0 = pr.tile_row0;
+    sa.tile_keyn = pr.tile_keyn;
+    sa.counters = pr.meta->counters;
+    sa.count_idx = pr.count_idx;
+    sa.in = pr.in;
+    sa.ld_in = pr.ld_in;
+    sa.row_w = pr.row_w;
+    sa.post_scale = pr.post_scale;
+    sa.NC = NC;
+    sa.HC = HC;
+    sa.SC = SC;
+    sa.xs_stride = SC + 8;
+    sa.as_stride = SC + 8;
+    sa.x_stage_bytes = (int)a128((size_t)kTileRows * (SC + 8) * 2);
+    sa.a_stage_bytes = (int)a128((size_t)R8 * (SC + 8) * 2);
+    sa.off_x = 0;
+    sa.off_a = 2 * sa.x_stage_bytes;
+    sa.off_red = sa.off_a + 2 * sa.a_stage_bytes;
+    sa.part = part;
+    sa.v = v;
+    sa.arrive = arrive;
+    sa.rows = pr.rows;
+    sa.status = pr.status;
+    sa.spin_limit = pr.spin_limit;
+
+    EArgs ea;
+    memset(&ea, 0, sizeof(ea));
+    ea.n_slices = ns;
+    ea.R = R;
+    ea.R8 = R8;
+    ea.E = pr.E;
+    ea.out_total = out_total;
+    for (int j = 0; j < ns; ++j) {
+        ea.out_w[j] = pr.out_w[j];
+        ea.out_off[j] = pr.out_off[j];
+        ea.B[j] = pr.B[j];
+        ea.B_ss[j] = pr.B_ss[j];
+        ea.B_shared[j] = pr.B_shared[j];
+    }
+    ea.rank = pr.rank;
+    ea.sorted = pr.meta->sorted;
+    ea.tile_row0 = pr.tile_row0;
+    ea.tile_keyn = pr.tile_keyn;
+    ea.counters = pr.meta->counters;
+    ea.count_idx = pr.count_idx;
+    ea.out = pr.out;
+    ea.ld_out = pr.ld_out;
+    ea.v = v;
+    ea.rows = pr.rows;
+    ea.n_oc = lora_ceil_div(out_total, kOC);
+    ea.ys_stride = kOC + 8;
+    ea.vr_stride = vr_stride;
+    ea.off_b = 0;
+    ea.off_ys = (int)e_b;
+    ea.off_vh = (int)(e_b + e_y);
+    ea.off_vl = (int)(e_b + e_y + e_v);
+    ea.status = pr.status;
+    ea.spin_limit = pr.spin_limit;
+
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.stream = s;
+    cfg.gridDim = dim3((unsigned)(max_tiles * ns * NC), 1, 1);
+    cfg.dynamicSmemBytes = s_smem;
+    LORA_CUDA_TRY(cudaLaunchKernelEx(&cfg, bgmv_shrink_kernel, sa));
+    lora_note_launch();
+    cfg.gridDim = dim3((unsigned)(max_tiles * ea.n_oc), 1, 1);
+    cfg.dynamicSmemBytes = e_smem;
+    LORA_CUDA_TRY(cudaLaunchKernelEx(&cfg, bgmv_expand_kernel, ea));
+    lora_note_launch();
+    *launched = true;
+    return LORA_OK;
+}

@@ -20,6 +20,7 @@
 // lower tickets, which are held by running CTAs, so the schedule cannot
 // deadlock whatever the residency.  The last CTA to finish zeroes the
 // control words so the workspace is ready for the next call.
+#include <atomic>
 #include <stdlib.h>
 #include <string.h>
 
@@ -440,6 +441,7 @@ lora_status_t launch(const lora_pool_t *pool, GArgs &g, long long est_items, cud
     g.spin_limit = g_spin_limit;
     grouped_lora_kernel<MODE><<<(unsigned)grid, kThreads, smem, s>>>(g);
     LORA_CUDA_TRY(cudaGetLastError());
+    lora_note_launch();
     return LORA_OK;
 }
 
@@ -512,7 +514,14 @@ lora_status_t bind_workspace(GArgs &g, const Plan &pl, void *ws, size_t ws_bytes
     return LORA_OK;
 }
 
-// The tensor-core path's bf16 hi/lo rank buffer sits after the split-K region.
+size_t align1k(size_t x) { return (x + 1023) & ~(size_t)1023; }
+int max_tiles(int rows, int keys) { return rows / kTile + (rows < keys ? rows : keys) + 1; }
+
+// Workspace of a dense/MoE apply, in this order: [bf16 hi/lo rank buffer of the
+// tensor-core path][split-K region (self-cleaning control words)][split
+// shrink/expand region (partials, v, self-cleaning arrival counters)].  Each
+// path keeps to its own region so one workspace can serve layers that take
+// different paths.
 size_t sgmv_region_bytes(const lora_pool_t *pool, int T) {
     if (pool->is_moe || pool->desc.max_rank != 64) return 0;
     return (lora_sgmv_ws_bytes(pool, T) + 1023) & ~(size_t)1023;
@@ -567,6 +576,9 @@ LoraProblem to_problem(const GArgs &g, const lora_meta_t *meta, int n_keys) {
 }  // namespace
 
 int g_lora_kernel_policy = 0;
+static std::atomic<unsigned long long> g_lora_launches{0};
+void lora_note_launch() { g_lora_launches.fetch_add(1, std::memory_order_relaxed); }
+extern "C" unsigned long long lora_kernel_launch_count(void) { return g_lora_launches.load(); }
 
 extern "C" void lora_set_kernel_policy(int32_t policy) { g_lora_kernel_policy = policy; }
 
@@ -577,13 +589,16 @@ extern "C" size_t lora_workspace_bytes(const lora_pool_t *pool, int32_t T, int32
     const lora_pool_desc_t &d = pool->desc;
     if (!pool->is_moe) {
         const Plan pl = make_plan(pool->num_sms, d.in_dim, d.n_slices, d.max_rank, T, d.max_loras);
-        return ws_bytes_for(pl) + sgmv_region_bytes(pool, T);
+        return sgmv_region_bytes(pool, T) + align1k(ws_bytes_for(pl)) +
+               lora_split_ws_bytes(d.n_slices, d.in_dim, d.max_rank, T, max_tiles(T, d.max_loras));
     }
     if (top_k < 1) return 0;
     const int rows = T * top_k, keys = d.max_loras * d.num_experts;
     const Plan p13 = make_plan(pool->num_sms, d.d_model, d.n_w13_slices, d.max_rank, rows, keys);
     const Plan p2 = make_plan(pool->num_sms, d.d_mlp, 1, d.max_rank, rows, keys);
-    const size_t a = ws_bytes_for(p13), b = ws_bytes_for(p2);
+    const size_t a = align1k(ws_bytes_for(p13)) +
+                     lora_split_ws_bytes(d.n_w13_slices, d.d_model, d.max_rank, rows, max_tiles(rows, keys));
+    const size_t b = align1k(ws_bytes_for(p2)) + lora_split_ws_bytes(1, d.d_mlp, d.max_rank, rows, max_tiles(rows, keys));
     return a > b ? a : b;
 }
 
@@ -606,14 +621,20 @@ lora_status_t lora_dense_apply(const lora_pool_t *pool, const lora_meta_t *meta,
         return LORA_ERR_INVALID_ARG;
     g.post_scale = post_scale;
     // workspace: [bf16 hi/lo rank buffer of the tensor-core path (1 KB aligned)][split-K region]
+    if (!workspace || !lora_aligned16(workspace)) return LORA_ERR_INVALID_ARG;
     const size_t sg_bytes = sgmv_region_bytes(pool, meta->T);
-    const bool use_sgmv = g_lora_kernel_policy == 0 && sg_bytes > 0 && meta->T >= LORA_LONG_MIN &&
-                          ws_bytes > sg_bytes && lora_aligned16(workspace) && lora_sgmv_eligible(pool);
-    const size_t ws_splitk = use_sgmv ? ws_bytes - sg_bytes : ws_bytes;
-    void *ws_sk = use_sgmv ? (void *)((char *)workspace + sg_bytes) : workspace;
-    const Plan pl = fit_plan(make_plan(pool->num_sms, g.in_dim, g.n_slices, g.R, meta->T,
-                                       pool->desc.max_loras),
-                             g.in_dim, g.n_slices, g.R, meta->T, ws_splitk);
+    const bool use_sgmv = g_lora_kernel_policy != 1 && sg_bytes > 0 && meta->T >= LORA_LONG_MIN &&
+                          ws_bytes > sg_bytes && lora_sgmv_eligible(pool);
+    const Plan pl0 = make_plan(pool->num_sms, g.in_dim, g.n_slices, g.R, meta->T, pool->desc.max_loras);
+    const size_t sk_bytes = align1k(ws_bytes_for(pl0));
+    const size_t sp_bytes = lora_split_ws_bytes(g.n_slices, g.in_dim, g.R, meta->T,
+                                                max_tiles(meta->T, pool->desc.max_loras));
+    size_t avail = ws_bytes > sg_bytes ? ws_bytes - sg_bytes : 0;
+    const bool have_split_region = avail >= sk_bytes + sp_bytes;
+    void *ws_sk = (char *)workspace + sg_bytes;
+    void *ws_sp = (char *)ws_sk + sk_bytes;
+    const size_t ws_splitk = have_split_region ? sk_bytes : avail;
+    const Plan pl = fit_plan(pl0, g.in_dim, g.n_slices, g.R, meta->T, ws_splitk);
     st = bind_workspace(g, pl, ws_sk, ws_splitk);
     if (st != LORA_OK) return st;
     g.in = (const uint16_t *)x;
@@ -628,9 +649,14 @@ lora_status_t lora_dense_apply(const lora_pool_t *pool, const lora_meta_t *meta,
         g.tile_keyn = meta->stile_keyn;
         g.count_idx = 4;
     }
-    if (g_lora_kernel_policy == 0) {
+    if (g_lora_kernel_policy != 1) {
         bool launched = false;
-        st = lora_cluster_apply(pool, to_problem(g, meta, pool->desc.max_loras), s, &launched);
+        const LoraProblem pr = to_problem(g, meta, pool->desc.max_loras);
+        if (g_lora_kernel_policy == 0 && have_split_region) {
+            st = lora_split_apply(pool, pr, ws_sp, sp_bytes, s, &launched);
+            if (st != LORA_OK || launched) return st;
+        }
+        st = lora_cluster_apply(pool, pr, s, &launched);
         if (st != LORA_OK || launched) return st;
     }
     return launch<kFused>(pool, g, est_items(g, meta->T, pool->desc.max_loras, kFused), s);
@@ -751,16 +777,27 @@ extern "C" lora_status_t lora_moe_apply(const lora_pool_t *pool, const lora_meta
     g.out = (uint16_t *)out;
     g.ld_out = ld_out;
     const int keys = d.max_loras * E;
-    const Plan pl = fit_plan(make_plan(pool->num_sms, g.in_dim, g.n_slices, g.R, rows, keys), g.in_dim,
-                             g.n_slices, g.R, rows, ws_bytes);
-    lora_status_t st = bind_workspace(g, pl, workspace, ws_bytes);
+    if (!workspace || !lora_aligned16(workspace)) return LORA_ERR_INVALID_ARG;
+    const Plan pl0 = make_plan(pool->num_sms, g.in_dim, g.n_slices, g.R, rows, keys);
+    const size_t sk_bytes = align1k(ws_bytes_for(pl0));
+    const size_t sp_bytes = lora_split_ws_bytes(g.n_slices, g.in_dim, g.R, rows, max_tiles(rows, keys));
+    const bool have_split_region = ws_bytes >= sk_bytes + sp_bytes;
+    const size_t ws_splitk = have_split_region ? sk_bytes : ws_bytes;
+    const Plan pl = fit_plan(pl0, g.in_dim, g.n_slices, g.R, rows, ws_splitk);
+    lora_status_t st = bind_workspace(g, pl, workspace, ws_splitk);
     if (st != LORA_OK) return st;
-    if (g_lora_kernel_policy == 0) {
+    cudaStream_t s = (cudaStream_t)stream;
+    if (g_lora_kernel_policy != 1) {
         bool launched = false;
-        st = lora_cluster_apply(pool, to_problem(g, meta, keys), (cudaStream_t)stream, &launched);
+        const LoraProblem pr = to_problem(g, meta, keys);
+        if (g_lora_kernel_policy == 0 && have_split_region) {
+            st = lora_split_apply(pool, pr, (char *)workspace + sk_bytes, sp_bytes, s, &launched);
+            if (st != LORA_OK || launched) return st;
+        }
+        st = lora_cluster_apply(pool, pr, s, &launched);
         if (st != LORA_OK || launched) return st;
     }
-    return launch<kFused>(pool, g, est_items(g, rows, keys, kFused), (cudaStream_t)stream);
+    return launch<kFused>(pool, g, est_items(g, rows, keys, kFused), s);
 }
 
 // ------------------------------------------------------------------------

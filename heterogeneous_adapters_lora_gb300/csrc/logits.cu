@@ -77,5 +77,6 @@ extern "C" lora_status_t lora_logits_apply(const lora_pool_t *pool, const lora_m
                                                     (uint16_t *)logits_out, ld_out, vocab_size, mup,
                                                     pool->d_status);
     LORA_CUDA_TRY(cudaGetLastError());
+    lora_note_launch();
     return lora_dense_apply(pool, meta, hidden, ld_h, logits_out, ld_out, workspace, ws_bytes, mup, s);
 }

@@ -112,8 +112,18 @@ struct LoraProblem {
 lora_status_t lora_cluster_apply(const lora_pool_t *pool, const LoraProblem &pr, cudaStream_t s,
                                  bool *launched);
 
-// Kernel selection policy (0 = automatic, 1 = split-K kernel only).
+// Host-side count of kernel launches made by this library (all devices).
+void lora_note_launch();
+
+// Kernel selection policy (0 = automatic: split shrink/expand kernels when
+// the shapes fit, 1 = persistent split-K kernel only, 2 = cluster kernel
+// preferred).
 extern int g_lora_kernel_policy;
+
+// Split shrink/expand kernels (bgmv.cu): workspace bytes and launcher.
+size_t lora_split_ws_bytes(int n_slices, int in_dim, int R, int rows, int max_tiles);
+lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, void *ws, size_t ws_bytes,
+                               cudaStream_t s, bool *launched);
 
 // Tensor-core SGMV (sgmv.cu) for long contiguous runs of a dense pool.
 bool lora_sgmv_eligible(const lora_pool_t *pool);

@@ -317,6 +317,7 @@ lora_status_t lora_launch_build_meta(const lora_pool_t *pool, const int32_t *d_i
     cfg.attrs = at;
     cfg.numAttrs = 1;
     LORA_CUDA_TRY(cudaLaunchKernelEx(&cfg, build_meta_kernel, a));
+    lora_note_launch();
     meta->T = T;
     meta->top_k = top_k;
     meta->n_keys = n_keys;

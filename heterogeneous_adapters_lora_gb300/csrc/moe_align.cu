@@ -78,5 +78,6 @@ extern "C" lora_status_t lora_moe_align_padded(const lora_pool_t *pool, const lo
     moe_align_padded_kernel<<<L, kThreads, 0, (cudaStream_t)stream>>>(
         meta->sorted, meta->key_count, meta->key_offset, E, (int)P, block_m, cap, d_sorted, d_expert, d_npp);
     LORA_CUDA_TRY(cudaGetLastError());
+    lora_note_launch();
     return LORA_OK;
 }

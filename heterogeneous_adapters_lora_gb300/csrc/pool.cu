@@ -153,6 +153,7 @@ static lora_status_t reset_slot(lora_pool_t *p, int slot, cudaStream_t s) {
     }
     lora_set_tables_kernel<<<1, 1, 0, s>>>(p->d_rank, p->d_scale, p->d_enabled, slot, 0, 0.0f, 0);
     LORA_CUDA_TRY(cudaGetLastError());
+    lora_note_launch();
     p->h_rank[slot] = 0;
     return LORA_OK;
 }
@@ -188,6 +189,7 @@ static lora_status_t copy_pair(lora_pool_t *p, int i, int slot, int rank, int ex
 static lora_status_t finish_set(lora_pool_t *p, int slot, int rank, float scale, cudaStream_t s) {
     lora_set_tables_kernel<<<1, 1, 0, s>>>(p->d_rank, p->d_scale, p->d_enabled, slot, rank, scale, 1);
     LORA_CUDA_TRY(cudaGetLastError());
+    lora_note_launch();
     p->h_rank[slot] = rank;
     return LORA_OK;
 }

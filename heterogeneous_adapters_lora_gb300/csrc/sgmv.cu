@@ -7,8 +7,8 @@
 // group (adapter slot) whose tokens form one contiguous run of >= 64 tokens
 // the metadata cuts the run into tiles of up to 128 tokens; per tile:
 //
-//   shrink:  D[t][(j,k)] = sum_h x[t][h] * A_j[a][k][h]        M = 128 tokens,
-//            N = n_slices * R, K = hidden in blocks of 64, 4-stage TMA ring.
+//   shrink:  D[t][k] = sum_h x[t][h] * A_j[a][k][h]   one CTA per (tile, slice j):
+//            M = 128 tokens, N = R, K = hidden in blocks of 64, 4-stage TMA ring.
 //            Epilogue: v = scale[a] * D, split into bf16 hi + lo (v - hi), so
 //            that the expand keeps the fp32 intermediate to ~16 bits.
 //   expand:  y[t][off_j + o] += v_hi[t] . B_j[a][o] + v_lo[t] . B_j[a][o]
@@ -16,10 +16,11 @@
 //            tile is read by TMA, updated in shared memory and written back
 //            by TMA (or row by row for a partial last tile of a run).
 //
-// Warp roles (192 threads): warp 0 issues TMA, warp 1 allocates tensor
-// memory and issues the MMAs, warps 2..5 run the epilogue (warp w reads the
-// accumulator lanes 32*(w%4) .. +31).  Every wait is a bounded poll that
-// records LORA_ERR_TIMEOUT in the status word instead of hanging.
+// Warp roles: warp 0 issues TMA, warp 1 allocates tensor memory and issues
+// the MMAs, the other warps run the epilogue (warp w reads the accumulator
+// lanes 32*(w%4) .. +31; 4 epilogue warps in the shrink, 8 in the expand,
+// where two warps share a lane quarter and split the columns).  Every wait is
+// a bounded poll that records LORA_ERR_TIMEOUT in the status word.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <string.h>
@@ -32,7 +33,9 @@ namespace {
 constexpr int kRows = LORA_LTILE_ROWS;  // 128 tokens per tile (MMA M)
 constexpr int kBK = 64;                 // hidden elements per K block (one 128-byte swizzle row)
 constexpr int kStages = 4;
-constexpr int kThreads = 192;
+constexpr int kThreads = 192;          // shrink: TMA warp, MMA warp, 4 epilogue warps
+constexpr int kEThreads = 320;         // expand: TMA warp, MMA warp, 8 epilogue warps
+constexpr int kNY = 3;                 // y tiles in flight in the expand
 constexpr int kOT = 128;                // outputs per expand tile (MMA N)
 constexpr int kOG = 8;                  // expand tiles per work unit
 constexpr uint32_t kTileBytes = kRows * kBK * 2;  // 16 KB: 128 rows x 128 B
@@ -82,11 +85,11 @@ __global__ void __launch_bounds__(kThreads, 1) sgmv_shrink_kernel(const __grid_c
     char *smem = (char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tile = blockIdx.x;
+    const int tile = blockIdx.x / p.n_slices, js = blockIdx.x - tile * p.n_slices;  // one slice per CTA
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (tile >= p.counters[5]) return;
 
-    const int N = p.n_slices * p.R;  // accumulator columns
+    const int N = p.R;  // accumulator columns: the ranks of slice js
     const uint32_t a_bytes = (uint32_t)N * 128;
     const uint32_t stage_bytes = kTileBytes + ((a_bytes + 1023) & ~1023u);
     const int keyn = p.ltile_keyn[tile];
@@ -121,8 +124,7 @@ __global__ void __launch_bounds__(kThreads, 1) sgmv_shrink_kernel(const __grid_c
             char *st = smem + (size_t)s * stage_bytes;
             tc::mbar_expect_tx(&full[s], kTileBytes + a_bytes);
             tc::tma_load_2d(st, &p.tm_x, kb * kBK, tok0, &full[s]);
-            for (int j = 0; j < p.n_slices; ++j)
-                tc::tma_load_2d(st + kTileBytes + (size_t)j * p.R * 128, &p.tm_a[j], kb * kBK, key * p.R, &full[s]);
+            tc::tma_load_2d(st + kTileBytes, &p.tm_a[js], kb * kBK, key * p.R, &full[s]);
         }
     } else if (warp == 1 && lane == 0) {
         const uint32_t idesc = tc::idesc_bf16(kRows, N);
@@ -150,7 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1) sgmv_shrink_kernel(const __grid_c
             tc::tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), r);
             tc::tmem_wait_ld();
             if (t < n) {
-                const int col = c * 32, j = col / p.R, k0 = col - j * p.R;
+                const int j = js, k0 = c * 32;
                 uint16_t *vrow = p.V + (long long)j * p.v_slice + (long long)(row0 + t) * (2 * p.R);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
@@ -176,15 +178,15 @@ __global__ void __launch_bounds__(kThreads, 1) sgmv_shrink_kernel(const __grid_c
 
 // ------------------------------------------------------------------ expand
 
-__global__ void __launch_bounds__(kThreads, 1) sgmv_expand_kernel(const __grid_constant__ ExpandArgs p) {
+__global__ void __launch_bounds__(kEThreads, 1) sgmv_expand_kernel(const __grid_constant__ ExpandArgs p) {
     extern __shared__ __align__(1024) char smem_raw[];
-    __shared__ __align__(8) uint64_t v_full, v_empty, b_full[2], b_empty[2], y_full[2], y_empty[2],
+    __shared__ __align__(8) uint64_t v_full, v_empty, b_full[2], b_empty[2], y_full[kNY], y_empty[kNY],
         acc_full[2], acc_empty[2];
     __shared__ uint32_t s_tmem;
     char *smem = (char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     char *vt = smem;                           // V hi tile (16 KB) then lo tile (16 KB)
     char *bt = smem + 2 * kTileBytes;          // 2 x B tile (16 KB)
-    char *yt = smem + 4 * kTileBytes;          // 2 x y tile (2 boxes of 16 KB each)
+    char *yt = smem + 4 * kTileBytes;          // kNY x y tile (2 boxes of 16 KB each)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -203,10 +205,12 @@ __global__ void __launch_bounds__(kThreads, 1) sgmv_expand_kernel(const __grid_c
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(&b_full[b], 1);
             tc::mbar_init(&b_empty[b], 1);
+            tc::mbar_init(&acc_full[b], 1);
+            tc::mbar_init(&acc_empty[b], 8);
+        }
+        for (int b = 0; b < kNY; ++b) {
             tc::mbar_init(&y_full[b], 1);
             tc::mbar_init(&y_empty[b], 1);
-            tc::mbar_init(&acc_full[b], 1);
-            tc::mbar_init(&acc_empty[b], 4);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -237,16 +241,17 @@ __global__ void __launch_bounds__(kThreads, 1) sgmv_expand_kernel(const __grid_c
             tc::tma_load_2d(vt, &p.tm_v[j], 0, row0, &v_full);
             tc::tma_load_2d(vt + kTileBytes, &p.tm_v[j], kBK, row0, &v_full);
             for (int i = 0; i < n_ot; ++i, ++it) {
-                const int b = it & 1;
+                const int b = it & 1, yb = it % kNY;
                 const int o_local = (ot0 + i) * kOT;
                 if (it >= 2) wait_or_flag(&b_empty[b], (uint32_t)(((it >> 1) - 1) & 1), p.spin_limit, p.status);
                 tc::mbar_expect_tx(&b_full[b], kTileBytes);
                 tc::tma_load_2d(bt + b * kTileBytes, &p.tm_b[j], 0, key * p.out_w[j] + o_local, &b_full[b]);
-                if (it >= 2) wait_or_flag(&y_empty[b], (uint32_t)(((it >> 1) - 1) & 1), p.spin_limit, p.status);
-                char *yb = yt + (size_t)b * 2 * kTileBytes;
-                tc::mbar_expect_tx(&y_full[b], 2 * kTileBytes);
-                tc::tma_load_2d(yb, &p.tm_y, p.out_off[j] + o_local, tok0, &y_full[b]);
-                tc::tma_load_2d(yb + kTileBytes, &p.tm_y, p.out_off[j] + o_local + kBK, tok0, &y_full[b]);
+                if (it >= kNY)
+                    wait_or_flag(&y_empty[yb], (uint32_t)((it / kNY - 1) & 1), p.spin_limit, p.status);
+                char *yb_ptr = yt + (size_t)yb * 2 * kTileBytes;
+                tc::mbar_expect_tx(&y_full[yb], 2 * kTileBytes);
+                tc::tma_load_2d(yb_ptr, &p.tm_y, p.out_off[j] + o_local, tok0, &y_full[yb]);
+                tc::tma_load_2d(yb_ptr + kTileBytes, &p.tm_y, p.out_off[j] + o_local + kBK, tok0, &y_full[yb]);
             }
         }
     } else if (warp == 1 && lane == 0) {
@@ -277,8 +282,10 @@ __global__ void __launch_bounds__(kThreads, 1) sgmv_expand_kernel(const __grid_c
             tc::mma_commit(&v_empty);
         }
     } else if (warp >= 2) {
-        const int q = warp & 3;
-        const int t = q * 32 + lane;  // token row of the tile = accumulator lane
+        // 8 epilogue warps: warp w reads accumulator lanes 32*(w%4).. (token
+        // rows) and half (w-2)/4 of the 128 columns of each tile
+        const int q = warp & 3, half = (warp - 2) >> 2;
+        const int t = q * 32 + lane;
         const bool leader = (warp == 2 && lane == 0);
         int it = 0;
         for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
@@ -287,29 +294,29 @@ __global__ void __launch_bounds__(kThreads, 1) sgmv_expand_kernel(const __grid_c
             const int n = p.ltile_keyn[lt] & 255;
             const int tok0 = p.ltile_tok0[lt];
             for (int i = 0; i < n_ot; ++i, ++it) {
-                const int b = it & 1;
+                const int b = it & 1, yb = it % kNY;
                 const int col0 = p.out_off[j] + (ot0 + i) * kOT;
-                char *yb = yt + (size_t)b * 2 * kTileBytes;
+                char *ybuf = yt + (size_t)yb * 2 * kTileBytes;
                 wait_or_flag(&acc_full[b], (uint32_t)((it >> 1) & 1), p.spin_limit, p.status);
-                wait_or_flag(&y_full[b], (uint32_t)((it >> 1) & 1), p.spin_limit, p.status);
+                wait_or_flag(&y_full[yb], (uint32_t)((it / kNY) & 1), p.spin_limit, p.status);
                 tc::tc_fence_after();
+                // this warp's columns half*64 .. +63 are box `half`, 16-byte units 0..7
+                char *row = ybuf + (size_t)half * kTileBytes + (size_t)t * 128;
 #pragma unroll 1
-                for (int c = 0; c < kOT / 32; ++c) {
+                for (int c = 0; c < 2; ++c) {
                     uint32_t r[32];
-                    tc::tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * kOT + c * 32), r);
+                    tc::tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * kOT + half * 64 + c * 32), r);
                     tc::tmem_wait_ld();
-                    // columns c*32 .. +31 live in box (c >> 1), 16-byte units (c & 1) * 4 + i
-                    char *row = yb + (size_t)(c >> 1) * kTileBytes + (size_t)t * 128;
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int unit = ((c & 1) * 4 + i) ^ (t & 7);
+                    for (int i4 = 0; i4 < 4; ++i4) {
+                        const int unit = (c * 4 + i4) ^ (t & 7);
                         uint4 *ptr = (uint4 *)(row + unit * 16);
                         uint4 yv = *ptr;
                         uint32_t w[4] = {yv.x, yv.y, yv.z, yv.w};
 #pragma unroll
                         for (int e2 = 0; e2 < 4; ++e2)
-                            w[e2] = pack2(bf16lo(w[e2]) + __uint_as_float(r[i * 8 + 2 * e2]),
-                                          bf16hi(w[e2]) + __uint_as_float(r[i * 8 + 2 * e2 + 1]));
+                            w[e2] = pack2(bf16lo(w[e2]) + __uint_as_float(r[i4 * 8 + 2 * e2]),
+                                          bf16hi(w[e2]) + __uint_as_float(r[i4 * 8 + 2 * e2 + 1]));
                         *ptr = make_uint4(w[0], w[1], w[2], w[3]);
                     }
                 }
@@ -318,28 +325,27 @@ __global__ void __launch_bounds__(kThreads, 1) sgmv_expand_kernel(const __grid_c
                 if (lane == 0) tc::mbar_arrive(&acc_empty[b]);
                 if (n == kRows) {
                     tc::fence_proxy_async();
-                    asm volatile("bar.sync 1, 128;" ::: "memory");
+                    asm volatile("bar.sync 1, 256;" ::: "memory");
                     if (leader) {
-                        tc::tma_store_2d(&p.tm_y, col0, tok0, yb);
-                        tc::tma_store_2d(&p.tm_y, col0 + kBK, tok0, yb + kTileBytes);
+                        tc::tma_store_2d(&p.tm_y, col0, tok0, ybuf);
+                        tc::tma_store_2d(&p.tm_y, col0 + kBK, tok0, ybuf + kTileBytes);
                         tc::bulk_commit();
                         tc::bulk_wait_read0();
-                        tc::mbar_arrive(&y_empty[b]);
+                        tc::mbar_arrive(&y_empty[yb]);
                     }
                 } else {
                     // partial last tile of a run: write back only its own rows
                     if (t < n) {
-                        uint16_t *dst = p.y + (long long)(tok0 + t) * p.ld_y + col0;
+                        uint16_t *dst = p.y + (long long)(tok0 + t) * p.ld_y + col0 + half * 64;
 #pragma unroll
-                        for (int u16 = 0; u16 < 16; ++u16) {
-                            const int box = u16 >> 3, unit = (u16 & 7) ^ (t & 7);
-                            *(uint4 *)(dst + u16 * 8) =
-                                *(const uint4 *)(yb + (size_t)box * kTileBytes + (size_t)t * 128 + unit * 16);
+                        for (int u16 = 0; u16 < 8; ++u16) {
+                            const int unit = u16 ^ (t & 7);
+                            *(uint4 *)(dst + u16 * 8) = *(const uint4 *)(row + unit * 16);
                         }
                     }
                     tc::fence_proxy_async();  // generic reads before the next TMA write
-                    asm volatile("bar.sync 1, 128;" ::: "memory");
-                    if (leader) tc::mbar_arrive(&y_empty[b]);
+                    asm volatile("bar.sync 1, 256;" ::: "memory");
+                    if (leader) tc::mbar_arrive(&y_empty[yb]);
                 }
             }
         }
@@ -436,7 +442,7 @@ lora_status_t lora_sgmv_apply(const lora_pool_t *pool, const lora_meta_t *meta, 
     sa.status = pool->d_status;
     sa.spin_limit = spin_limit;
     sa.post_scale = post_scale;
-    const size_t a_bytes = (size_t)ns * R * 128;
+    const size_t a_bytes = (size_t)R * 128;
     const size_t stage = kTileBytes + ((a_bytes + 1023) & ~(size_t)1023);
     const size_t smem_s = kStages * stage + 1024;
     cudaLaunchConfig_t cfg;
@@ -446,11 +452,12 @@ lora_status_t lora_sgmv_apply(const lora_pool_t *pool, const lora_meta_t *meta, 
     at[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    cfg.gridDim = dim3((unsigned)max_lt, 1, 1);
+    cfg.gridDim = dim3((unsigned)(max_lt * ns), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem_s;
     cfg.stream = s;
     LORA_CUDA_TRY(cudaLaunchKernelEx(&cfg, sgmv_shrink_kernel, sa));
+    lora_note_launch();
 
     ExpandArgs ea;
     memset(&ea, 0, sizeof(ea));
@@ -480,11 +487,13 @@ lora_status_t lora_sgmv_apply(const lora_pool_t *pool, const lora_meta_t *meta, 
     ea.ld_y = ldy;
     ea.status = pool->d_status;
     ea.spin_limit = spin_limit;
-    const size_t smem_e = 8 * (size_t)kTileBytes + 1024;
+    const size_t smem_e = (4 + 2 * kNY) * (size_t)kTileBytes + 1024;
     long long units = (long long)max_lt * g;
     cfg.gridDim = dim3((unsigned)(units < num_sms ? units : num_sms), 1, 1);
+    cfg.blockDim = dim3(kEThreads, 1, 1);
     cfg.dynamicSmemBytes = smem_e;
     cfg.numAttrs = 0;  // the expand reads the shrink's V: plain stream order
     LORA_CUDA_TRY(cudaLaunchKernelEx(&cfg, sgmv_expand_kernel, ea));
+    lora_note_launch();
     return LORA_OK;
 }

@@ -90,6 +90,7 @@ EXPORTS = {
     "lora_get_device_status": (c_i32, [c_vp, c_vp]),
     "lora_set_spin_limit": (None, [c_i32]),
     "lora_set_kernel_policy": (None, [c_i32]),
+    "lora_kernel_launch_count": (ctypes.c_ulonglong, []),
     "lora_status_string": (ctypes.c_char_p, [c_i32]),
 }
 
@@ -257,6 +258,10 @@ def lora_set_spin_limit(max_polls: int):
 
 def lora_set_kernel_policy(policy: int):
     lib().lora_set_kernel_policy(int(policy))
+
+
+def lora_kernel_launch_count() -> int:
+    return int(lib().lora_kernel_launch_count())
 
 
 def lora_status_string(code: int) -> str:

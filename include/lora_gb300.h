@@ -349,10 +349,19 @@ LORA_API lora_status_t lora_get_device_status(const lora_pool_t *pool, void *str
 LORA_API void lora_set_spin_limit(int32_t max_polls);
 
 /* Kernel selection for lora_apply_slices / lora_moe_apply (process-wide):
- * 0 = automatic (the one-pass cluster kernel whenever the layer's shapes fit
- * its shared-memory plan, otherwise the split-K kernel with a workspace),
- * 1 = always the split-K kernel.  For tests and tuning. */
+ * 0 = automatic (tcgen05 for long contiguous runs of a rank-64 dense pool;
+ *     otherwise the split shrink/expand kernels when the workspace holds
+ *     their region, else the one-pass cluster kernel, else the persistent
+ *     split-K kernel),
+ * 1 = always the persistent split-K kernel,
+ * 2 = like 0 but the one-pass cluster kernel before the split kernels.
+ * For tests and tuning. */
 LORA_API void lora_set_kernel_policy(int32_t policy);
+
+/* Number of kernel launches this library has issued since it was loaded
+ * (all pools, all devices; host-side counter, launches captured into a CUDA
+ * graph count once at capture).  A diagnostic: never fails. */
+LORA_API unsigned long long lora_kernel_launch_count(void);
 
 /* Static string naming a status code. */
 LORA_API const char *lora_status_string(lora_status_t s);

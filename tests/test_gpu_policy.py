@@ -1,6 +1,7 @@
-"""Both compute paths of lora_apply_slices / lora_moe_apply against the
-oracle: the one-pass cluster kernel (automatic choice for these shapes) and
-the split-K kernel with a workspace (kernel policy 1)."""
+"""Every compute path of lora_apply_slices / lora_moe_apply against the
+oracle: the automatic choice (split shrink/expand kernels for these shapes,
+tcgen05 for long runs), the persistent split-K kernel (kernel policy 1) and
+the one-pass cluster kernel (kernel policy 2)."""
 import numpy as np
 import pytest
 
@@ -16,7 +17,7 @@ from gpu_util import active_mask, assert_delta, assert_rows_untouched
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(params=[0, 1], ids=["auto", "splitk"])
+@pytest.fixture(params=[0, 1, 2], ids=["auto", "splitk", "cluster"])
 def policy(request):
     L.lora_set_kernel_policy(request.param)
     yield request.param
@@ -68,9 +69,13 @@ def test_moe_paths(shared, policy):
     assert_delta(bf16_bits_to_f32(ic3), d2, "w2")
 
 
-def test_cluster_path_in_a_graph_with_other_streams_idle():
-    """Metadata + cluster apply captured together (programmatic dependent
-    launch edge inside the graph) and replayed three times."""
+@pytest.mark.parametrize("pol", [0, 2], ids=["split", "cluster"])
+def test_apply_in_a_graph_replayed(pol):
+    """Metadata + apply captured together (programmatic dependent launch
+    edges inside the graph) and replayed three times: the split kernels'
+    arrival counters and the split-K control words clean up after
+    themselves."""
+    L.lora_set_kernel_policy(pol)
     c = gen.decode_qkv()
     run = H.DenseRun(c)
     try:
@@ -87,6 +92,7 @@ def test_cluster_path_in_a_graph_with_other_streams_idle():
         y = run.y_host()
     finally:
         run.close()
+        L.lora_set_kernel_policy(0)
     _, d_ref = oracle.dense_delta(c)
     act = active_mask(c.idx, c.L, c.enabled, c.ranks)
     assert_delta(bf16_bits_to_f32(y)[act], 3 * d_ref[act], "3 replays")

@@ -10,14 +10,15 @@
 //   bgmv_shrink_kernel: one CTA per (16-row tile, slice j, hidden chunk c).
 //     Bulk copies (cp.async.bulk + mbarrier) bring the tile's x rows and the
 //     slot's A_j rows of chunk c; m16n8k16 bf16 MMAs (fp32 accumulate) give
-//     the partial v; the CTA that finishes last for (tile, j) -- found with an
-//     arrival counter it resets afterwards -- sums the chunks in order, scales
-//     by scale[a] (and the routed weight for MoE w2) and stores fp32 v.
+//     the partial v of chunk c, stored unscaled in fp32.
 //   bgmv_expand_kernel: one CTA per (tile, 256 output columns).  Before it
-//     waits for the shrink it bulk-copies its B rows and y rows; then it
-//     reads v, splits it into bf16 hi + lo (the expand keeps the fp32
-//     intermediate to ~16 bits), runs the MMAs, updates y in shared memory
-//     and writes the rows back with bulk copies.
+//     waits for the shrink it bulk-copies its B rows and y rows; then it sums
+//     the chunk partials of the slices it touches in chunk order, scales them
+//     by scale[a] (and the routed weight for MoE w2), splits v into bf16 hi +
+//     lo (the expand keeps the fp32 intermediate to ~16 bits), runs the MMAs,
+//     updates y in shared memory and writes the rows back with bulk copies.
+//   No counters: the workspace holds only the partials, so it needs no
+//   initial state.
 #include <string.h>
 
 #include "lora_internal.cuh"
@@ -37,36 +38,34 @@ struct SArgs {
     const uint16_t *A[LORA_MAX_SLICES];
     long long A_ss[LORA_MAX_SLICES], A_es[LORA_MAX_SLICES];
     const int32_t *rank;
-    const float *scale;
     const int32_t *sorted, *tile_row0, *tile_keyn, *counters;
     int count_idx;
     const uint16_t *in;
     long long ld_in;
-    const float *row_w;
-    float post_scale;
     int NC, HC, SC;          // hidden chunks, chunk length, stage length (elements)
     int xs_stride, as_stride;
     int off_x, off_a, x_stage_bytes, a_stage_bytes, off_red;
-    float *part;             // [NC][n_slices][rows][R8]
-    float *v;                // [n_slices][rows][R8] scaled
-    int *arrive;             // [max_tiles][n_slices]
+    float *part;             // [NC][n_slices][rows][R8], unscaled
     int rows;
     int *status;
     int spin_limit;
 };
 
 struct EArgs {
-    int n_slices, R, R8, E, out_total;
+    int n_slices, R, R8, E, out_total, NC;
     int out_w[LORA_MAX_SLICES], out_off[LORA_MAX_SLICES];
     const uint16_t *B[LORA_MAX_SLICES];
     long long B_ss[LORA_MAX_SLICES];
     int B_shared[LORA_MAX_SLICES];
     const int32_t *rank;
+    const float *scale;
+    const float *row_w;
+    float post_scale;
     const int32_t *sorted, *tile_row0, *tile_keyn, *counters;
     int count_idx;
     uint16_t *out;
     long long ld_out;
-    const float *v;
+    const float *part;
     int rows;
     int n_oc;
     int ys_stride, vr_stride;
@@ -81,7 +80,6 @@ __global__ void __launch_bounds__(kThreads) bgmv_shrink_kernel(const __grid_cons
     extern __shared__ __align__(128) char smem[];
     __shared__ __align__(8) uint64_t full[2];
     __shared__ int s_rows[kTileRows];
-    __shared__ int s_last;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, c4 = lane & 3;
     const int per_tile = p.n_slices * p.NC;
@@ -190,42 +188,14 @@ __global__ void __launch_bounds__(kThreads) bgmv_shrink_kernel(const __grid_cons
         }
     }
     __syncthreads();
-    const long long vrow0 = (long long)j * p.rows + row0;  // row of v / of this chunk's partial
-    float *dst = p.NC == 1 ? p.v : p.part + (long long)c * p.n_slices * p.rows * p.R8;
-    const float sc = p.scale[a] * p.post_scale;
+    // this chunk's partial: part[c][j][row0 + t][k]
+    float *dst = p.part + ((long long)c * p.n_slices + j) * p.rows * p.R8 + (long long)row0 * p.R8;
     for (int i = tid; i < n * p.R8; i += kThreads) {
         const int t = i / p.R8, k = i - t * p.R8;
         float s = 0.f;
         for (int hs = 0; hs < hsplit; ++hs) s += red[(hs * kTileRows + t) * p.R8 + k];
-        if (p.NC == 1) {
-            float w = sc;
-            if (p.row_w) w *= p.row_w[s_rows[t]];
-            s *= w;
-        }
-        dst[(vrow0 + t) * p.R8 + k] = s;
+        dst[i] = s;
     }
-    if (p.NC == 1) return;
-
-    // the last chunk CTA of (tile, j) sums the chunks in order and stores v
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-        s_last = atomicAdd(p.arrive + tile * p.n_slices + j, 1) == p.NC - 1;
-    }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    const long long cstride = (long long)p.n_slices * p.rows * p.R8;
-    for (int i = tid; i < n * p.R8; i += kThreads) {
-        const int t = i / p.R8, k = i - t * p.R8;
-        const float *src = p.part + (vrow0 + t) * p.R8 + k;
-        float s = 0.f;
-        for (int cc = 0; cc < p.NC; ++cc) s += __ldcg(src + cc * cstride);
-        float w = sc;
-        if (p.row_w) w *= p.row_w[s_rows[t]];
-        p.v[(vrow0 + t) * p.R8 + k] = s * w;
-    }
-    if (tid == 0) p.arrive[tile * p.n_slices + j] = 0;  // ready for the next call
 }
 
 // ---------------------------------------------------------------- expand
@@ -280,8 +250,12 @@ __global__ void __launch_bounds__(kThreads) bgmv_expand_kernel(const __grid_cons
         }
     }
 
-    asm volatile("griddepcontrol.wait;" ::: "memory");  // v of the shrink is complete
-    // v of the slices this CTA touches -> bf16 hi / lo, [16][vr_stride] at j * R8 + k
+    __shared__ float s_w[kTileRows];
+    if (tid < kTileRows) s_w[tid] = tid < n ? p.scale[a] * p.post_scale * (p.row_w ? p.row_w[s_rows[tid]] : 1.f) : 0.f;
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the shrink's partials are complete
+    __syncthreads();
+    // v of the slices this CTA touches (chunk partials summed in order, scaled)
+    // -> bf16 hi / lo, [16][vr_stride] at j * R8 + k
     uint16_t *vh = (uint16_t *)(smem + p.off_vh);
     uint16_t *vl = (uint16_t *)(smem + p.off_vl);
     int j0 = 0, j1 = 0;
@@ -293,7 +267,22 @@ __global__ void __launch_bounds__(kThreads) bgmv_expand_kernel(const __grid_cons
         const int t = i / per_t, q = i - t * per_t;
         const int jj = j0 + (q * 4) / p.R8, k = (q * 4) % p.R8;
         float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (t < n) s4 = __ldcg((const float4 *)(p.v + ((long long)jj * p.rows + row0 + t) * p.R8 + k));
+        if (t < n) {
+            const float4 *src = (const float4 *)(p.part + ((long long)jj * p.rows + row0 + t) * p.R8 + k);
+            const long long cstride = (long long)ns * p.rows * p.R8 / 4;
+            for (int cc = 0; cc < p.NC; ++cc) {
+                const float4 q = __ldcg(src + cc * cstride);
+                s4.x += q.x;
+                s4.y += q.y;
+                s4.z += q.z;
+                s4.w += q.w;
+            }
+            const float w = s_w[t];
+            s4.x *= w;
+            s4.y *= w;
+            s4.z *= w;
+            s4.w *= w;
+        }
         const __nv_bfloat162 h01 = __floats2bfloat162_rn(s4.x, s4.y);
         const __nv_bfloat162 h23 = __floats2bfloat162_rn(s4.z, s4.w);
         const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
@@ -366,10 +355,8 @@ size_t lora_split_ws_bytes(int n_slices, int in_dim, int R, int rows, int max_ti
     if (HC < 256) HC = 256;
     int NC = lora_ceil_div(in_dim, HC);
     if (NC > 8) NC = 8;
-    const size_t part = NC > 1 ? (size_t)NC * n_slices * rows * R8 * 4 : 0;
-    const size_t v = (size_t)n_slices * rows * R8 * 4;
-    const size_t arrive = (size_t)max_tiles * n_slices * 4;
-    return a128(part) + a128(v) + a128(arrive);
+    (void)max_tiles;
+    return a128((size_t)NC * n_slices * rows * R8 * 4);
 }
 
 lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, void *ws, size_t ws_bytes,
@@ -403,12 +390,7 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     const size_t e_v = a128((size_t)kTileRows * vr_stride * 2);
     const size_t e_smem = e_b + e_y + 2 * e_v;
 
-    char *w = (char *)ws;
-    float *part = NC > 1 ? (float *)w : nullptr;
-    w += a128(NC > 1 ? (size_t)NC * ns * pr.rows * R8 * 4 : 0);
-    float *v = (float *)w;
-    w += a128((size_t)ns * pr.rows * R8 * 4);
-    int *arrive = (int *)w;
+    float *part = (float *)ws;
 
     const int dev = pool->device < 64 ? pool->device : 63;
     if (!g_split_configured[dev]) {
@@ -433,7 +415,6 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
         sa.A_es[j] = pr.A_es[j];
     }
     sa.rank = pr.rank;
-    sa.scale = pr.scale;
     sa.sorted = pr.meta->sorted;
     sa.tile_row0 = pr.tile_row0;
     sa.tile_keyn = pr.tile_keyn;
@@ -441,8 +422,6 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     sa.count_idx = pr.count_idx;
     sa.in = pr.in;
     sa.ld_in = pr.ld_in;
-    sa.row_w = pr.row_w;
-    sa.post_scale = pr.post_scale;
     sa.NC = NC;
     sa.HC = HC;
     sa.SC = SC;
@@ -454,8 +433,6 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     sa.off_a = 2 * sa.x_stage_bytes;
     sa.off_red = sa.off_a + 2 * sa.a_stage_bytes;
     sa.part = part;
-    sa.v = v;
-    sa.arrive = arrive;
     sa.rows = pr.rows;
     sa.status = pr.status;
     sa.spin_limit = pr.spin_limit;
@@ -475,6 +452,10 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
         ea.B_shared[j] = pr.B_shared[j];
     }
     ea.rank = pr.rank;
+    ea.scale = pr.scale;
+    ea.row_w = pr.row_w;
+    ea.post_scale = pr.post_scale;
+    ea.NC = NC;
     ea.sorted = pr.meta->sorted;
     ea.tile_row0 = pr.tile_row0;
     ea.tile_keyn = pr.tile_keyn;
@@ -482,7 +463,7 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     ea.count_idx = pr.count_idx;
     ea.out = pr.out;
     ea.ld_out = pr.ld_out;
-    ea.v = v;
+    ea.part = part;
     ea.rows = pr.rows;
     ea.n_oc = lora_ceil_div(out_total, kOC);
     ea.ys_stride = kOC + 8;

@@ -20,6 +20,7 @@
 // lower tickets, which are held by running CTAs, so the schedule cannot
 // deadlock whatever the residency.  The last CTA to finish zeroes the
 // control words so the workspace is ready for the next call.
+#include <algorithm>
 #include <atomic>
 #include <stdlib.h>
 #include <string.h>
@@ -493,8 +494,8 @@ int out_total(const lora_pool_t *pool) {
 
 // A workspace sized for T tokens always fits a smaller batch once the hidden
 // chunks are widened (fewer chunks, fewer partials).
-Plan fit_plan(Plan pl, int in_dim, int n_slices, int R, int rows, size_t ws_bytes) {
-    while (ws_bytes_for(pl) > ws_bytes && pl.HC < kMaxHC) {
+Plan fit_plan(Plan pl, int in_dim, int n_slices, int R, int rows, size_t part_cap_bytes) {
+    while (pl.part_floats * 4 > part_cap_bytes && pl.HC < kMaxHC) {
         pl.HC = pl.HC * 2 > kMaxHC ? kMaxHC : pl.HC * 2;
         pl.NC = lora_ceil_div(in_dim, pl.HC);
         pl.part_floats = (size_t)pl.NC * n_slices * R * (size_t)rows;
@@ -502,26 +503,57 @@ Plan fit_plan(Plan pl, int in_dim, int n_slices, int R, int rows, size_t ws_byte
     return pl;
 }
 
-lora_status_t bind_workspace(GArgs &g, const Plan &pl, void *ws, size_t ws_bytes) {
-    if (!ws || !lora_aligned16(ws)) return LORA_ERR_INVALID_ARG;
-    if (ws_bytes < ws_bytes_for(pl)) return LORA_ERR_CAPACITY;
-    char *b = (char *)ws;
-    g.ctrl = (int *)b;
-    g.tile_cnt = (int *)(b + kCtrlBytes);
-    g.part = (float *)(b + kCtrlBytes + ((pl.cnt_ints * 4 + 255) & ~(size_t)255));
+void bind_splitk(GArgs &g, const Plan &pl, int *ctrl, int *cnt, float *part) {
+    g.ctrl = ctrl;
+    g.tile_cnt = cnt;
+    g.part = part;
     g.NC = pl.NC;
     g.HC = pl.HC;
-    return LORA_OK;
 }
 
 size_t align1k(size_t x) { return (x + 1023) & ~(size_t)1023; }
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 int max_tiles(int rows, int keys) { return rows / kTile + (rows < keys ? rows : keys) + 1; }
 
-// Workspace of a dense/MoE apply, in this order: [bf16 hi/lo rank buffer of the
-// tensor-core path][split-K region (self-cleaning control words)][split
-// shrink/expand region (partials, v, self-cleaning arrival counters)].  Each
-// path keeps to its own region so one workspace can serve layers that take
-// different paths.
+// Workspace of an apply call.  Its first part holds the words that must be
+// zero when a call starts (the split-K kernel's ticket, finish count and
+// per-tile counters; every call leaves them zero again).  The size of that
+// part depends only on the workspace size, so calls with different token
+// counts or layer types that share one workspace agree on where it is.  The
+// rest is scratch with no state between calls: [bf16 hi/lo rank buffer of
+// the tensor-core path][split-K partials, or the split kernels' chunk
+// partials].
+struct Carve {
+    int *ctrl, *cnt;
+    size_t cnt_cap;  // ints
+    char *data;
+    size_t data_bytes;
+};
+
+size_t counter_reserve(size_t ws_bytes) {
+    const size_t r = align256(ws_bytes / 8);
+    return r < 512 ? 512 : r;
+}
+
+bool carve(void *ws, size_t ws_bytes, Carve &c) {
+    const size_t res = counter_reserve(ws_bytes);
+    if (!ws || ws_bytes < res) return false;
+    c.ctrl = (int *)ws;
+    c.cnt = (int *)((char *)ws + kCtrlBytes);
+    c.cnt_cap = (res - kCtrlBytes) / 4;
+    c.data = (char *)ws + res;
+    c.data_bytes = ws_bytes - res;
+    return true;
+}
+
+// Smallest workspace whose carve holds data_bytes of scratch and cnt_ints counters.
+size_t ws_total(size_t data_bytes, size_t cnt_ints) {
+    const size_t need = kCtrlBytes + cnt_ints * 4;
+    size_t w = data_bytes + align256(need) + 512;
+    while (counter_reserve(w) < need || w - counter_reserve(w) < data_bytes) w += align256(w / 16 + 256);
+    return w;
+}
+
 size_t sgmv_region_bytes(const lora_pool_t *pool, int T) {
     if (pool->is_moe || pool->desc.max_rank != 64) return 0;
     return (lora_sgmv_ws_bytes(pool, T) + 1023) & ~(size_t)1023;
@@ -589,17 +621,19 @@ extern "C" size_t lora_workspace_bytes(const lora_pool_t *pool, int32_t T, int32
     const lora_pool_desc_t &d = pool->desc;
     if (!pool->is_moe) {
         const Plan pl = make_plan(pool->num_sms, d.in_dim, d.n_slices, d.max_rank, T, d.max_loras);
-        return sgmv_region_bytes(pool, T) + align1k(ws_bytes_for(pl)) +
-               lora_split_ws_bytes(d.n_slices, d.in_dim, d.max_rank, T, max_tiles(T, d.max_loras));
+        const size_t sp = lora_split_ws_bytes(d.n_slices, d.in_dim, d.max_rank, T, max_tiles(T, d.max_loras));
+        const size_t pk = align256(pl.part_floats * 4);
+        return ws_total(sgmv_region_bytes(pool, T) + (pk > sp ? pk : sp), pl.cnt_ints);
     }
     if (top_k < 1) return 0;
     const int rows = T * top_k, keys = d.max_loras * d.num_experts;
     const Plan p13 = make_plan(pool->num_sms, d.d_model, d.n_w13_slices, d.max_rank, rows, keys);
     const Plan p2 = make_plan(pool->num_sms, d.d_mlp, 1, d.max_rank, rows, keys);
-    const size_t a = align1k(ws_bytes_for(p13)) +
-                     lora_split_ws_bytes(d.n_w13_slices, d.d_model, d.max_rank, rows, max_tiles(rows, keys));
-    const size_t b = align1k(ws_bytes_for(p2)) + lora_split_ws_bytes(1, d.d_mlp, d.max_rank, rows, max_tiles(rows, keys));
-    return a > b ? a : b;
+    size_t data = align256(p13.part_floats * 4);
+    data = std::max(data, align256(p2.part_floats * 4));
+    data = std::max(data, lora_split_ws_bytes(d.n_w13_slices, d.d_model, d.max_rank, rows, max_tiles(rows, keys)));
+    data = std::max(data, lora_split_ws_bytes(1, d.d_mlp, d.max_rank, rows, max_tiles(rows, keys)));
+    return ws_total(data, std::max(p13.cnt_ints, p2.cnt_ints));
 }
 
 extern "C" lora_status_t lora_workspace_init(void *workspace, size_t bytes, void *stream) {
@@ -620,30 +654,29 @@ lora_status_t lora_dense_apply(const lora_pool_t *pool, const lora_meta_t *meta,
         ldx < pool->desc.in_dim || ldy < out_total(pool))
         return LORA_ERR_INVALID_ARG;
     g.post_scale = post_scale;
-    // workspace: [bf16 hi/lo rank buffer of the tensor-core path (1 KB aligned)][split-K region]
     if (!workspace || !lora_aligned16(workspace)) return LORA_ERR_INVALID_ARG;
+    Carve cv;
+    if (!carve(workspace, ws_bytes, cv)) return LORA_ERR_CAPACITY;
     const size_t sg_bytes = sgmv_region_bytes(pool, meta->T);
     const bool use_sgmv = g_lora_kernel_policy != 1 && sg_bytes > 0 && meta->T >= LORA_LONG_MIN &&
-                          ws_bytes > sg_bytes && lora_sgmv_eligible(pool);
-    const Plan pl0 = make_plan(pool->num_sms, g.in_dim, g.n_slices, g.R, meta->T, pool->desc.max_loras);
-    const size_t sk_bytes = align1k(ws_bytes_for(pl0));
+                          cv.data_bytes >= sg_bytes && lora_sgmv_eligible(pool);
+    char *scratch = cv.data + (use_sgmv ? sg_bytes : 0);
+    const size_t scratch_bytes = cv.data_bytes - (use_sgmv ? sg_bytes : 0);
+    const Plan pl = fit_plan(make_plan(pool->num_sms, g.in_dim, g.n_slices, g.R, meta->T, pool->desc.max_loras),
+                             g.in_dim, g.n_slices, g.R, meta->T, scratch_bytes);
+    // the split-K kernel is the fallback for every shape: its plan must fit
+    if (pl.cnt_ints > cv.cnt_cap || pl.part_floats * 4 > scratch_bytes) return LORA_ERR_CAPACITY;
+    bind_splitk(g, pl, cv.ctrl, cv.cnt, (float *)scratch);
     const size_t sp_bytes = lora_split_ws_bytes(g.n_slices, g.in_dim, g.R, meta->T,
                                                 max_tiles(meta->T, pool->desc.max_loras));
-    size_t avail = ws_bytes > sg_bytes ? ws_bytes - sg_bytes : 0;
-    const bool have_split_region = avail >= sk_bytes + sp_bytes;
-    void *ws_sk = (char *)workspace + sg_bytes;
-    void *ws_sp = (char *)ws_sk + sk_bytes;
-    const size_t ws_splitk = have_split_region ? sk_bytes : avail;
-    const Plan pl = fit_plan(pl0, g.in_dim, g.n_slices, g.R, meta->T, ws_splitk);
-    st = bind_workspace(g, pl, ws_sk, ws_splitk);
-    if (st != LORA_OK) return st;
+    const bool have_split_region = sp_bytes <= scratch_bytes;
     g.in = (const uint16_t *)x;
     g.ld_in = ldx;
     g.out = (uint16_t *)y;
     g.ld_out = ldy;
     if (use_sgmv) {
         // long contiguous runs on tcgen05; the remaining groups' 16-row tiles below
-        st = lora_sgmv_apply(pool, meta, x, ldx, y, ldy, workspace, g_spin_limit, pool->num_sms, post_scale, s);
+        st = lora_sgmv_apply(pool, meta, x, ldx, y, ldy, cv.data, g_spin_limit, pool->num_sms, post_scale, s);
         if (st != LORA_OK) return st;
         g.tile_row0 = meta->stile_row0;
         g.tile_keyn = meta->stile_keyn;
@@ -653,7 +686,7 @@ lora_status_t lora_dense_apply(const lora_pool_t *pool, const lora_meta_t *meta,
         bool launched = false;
         const LoraProblem pr = to_problem(g, meta, pool->desc.max_loras);
         if (g_lora_kernel_policy == 0 && have_split_region) {
-            st = lora_split_apply(pool, pr, ws_sp, sp_bytes, s, &launched);
+            st = lora_split_apply(pool, pr, scratch, scratch_bytes, s, &launched);
             if (st != LORA_OK || launched) return st;
         }
         st = lora_cluster_apply(pool, pr, s, &launched);
@@ -778,20 +811,21 @@ extern "C" lora_status_t lora_moe_apply(const lora_pool_t *pool, const lora_meta
     g.ld_out = ld_out;
     const int keys = d.max_loras * E;
     if (!workspace || !lora_aligned16(workspace)) return LORA_ERR_INVALID_ARG;
-    const Plan pl0 = make_plan(pool->num_sms, g.in_dim, g.n_slices, g.R, rows, keys);
-    const size_t sk_bytes = align1k(ws_bytes_for(pl0));
+    Carve cv;
+    if (!carve(workspace, ws_bytes, cv)) return LORA_ERR_CAPACITY;
+    const Plan pl = fit_plan(make_plan(pool->num_sms, g.in_dim, g.n_slices, g.R, rows, keys), g.in_dim,
+                             g.n_slices, g.R, rows, cv.data_bytes);
+    if (pl.cnt_ints > cv.cnt_cap || pl.part_floats * 4 > cv.data_bytes) return LORA_ERR_CAPACITY;
+    bind_splitk(g, pl, cv.ctrl, cv.cnt, (float *)cv.data);
     const size_t sp_bytes = lora_split_ws_bytes(g.n_slices, g.in_dim, g.R, rows, max_tiles(rows, keys));
-    const bool have_split_region = ws_bytes >= sk_bytes + sp_bytes;
-    const size_t ws_splitk = have_split_region ? sk_bytes : ws_bytes;
-    const Plan pl = fit_plan(pl0, g.in_dim, g.n_slices, g.R, rows, ws_splitk);
-    lora_status_t st = bind_workspace(g, pl, workspace, ws_splitk);
-    if (st != LORA_OK) return st;
+    const bool have_split_region = sp_bytes <= cv.data_bytes;
+    lora_status_t st = LORA_OK;
     cudaStream_t s = (cudaStream_t)stream;
     if (g_lora_kernel_policy != 1) {
         bool launched = false;
         const LoraProblem pr = to_problem(g, meta, keys);
         if (g_lora_kernel_policy == 0 && have_split_region) {
-            st = lora_split_apply(pool, pr, (char *)workspace + sk_bytes, sp_bytes, s, &launched);
+            st = lora_split_apply(pool, pr, cv.data, cv.data_bytes, s, &launched);
             if (st != LORA_OK || launched) return st;
         }
         st = lora_cluster_apply(pool, pr, s, &launched);
@@ -845,12 +879,13 @@ extern "C" lora_status_t lora_apply_slices_static(const lora_pool_t *pool, const
         g_static_scratch_addr[dev] = addr;
     }
     void *scratch = g_static_scratch_addr[dev];
-    const Plan pl = fit_plan(make_plan(pool->num_sms, g.in_dim, g.n_slices, g.R, meta->T,
-                                       pool->desc.max_loras),
-                             g.in_dim, g.n_slices, g.R, meta->T, kStaticScratchBytes);
+    const Plan pl0 = make_plan(pool->num_sms, g.in_dim, g.n_slices, g.R, meta->T, pool->desc.max_loras);
+    const size_t cnt_bytes = align256(pl0.cnt_ints * 4);
+    if (kCtrlBytes + cnt_bytes >= kStaticScratchBytes) return LORA_ERR_CAPACITY;
+    const Plan pl = fit_plan(pl0, g.in_dim, g.n_slices, g.R, meta->T, kStaticScratchBytes - kCtrlBytes - cnt_bytes);
     if (ws_bytes_for(pl) > kStaticScratchBytes) return LORA_ERR_CAPACITY;
-    st = bind_workspace(g, pl, scratch, kStaticScratchBytes);
-    if (st != LORA_OK) return st;
+    bind_splitk(g, pl, (int *)scratch, (int *)((char *)scratch + kCtrlBytes),
+                (float *)((char *)scratch + kCtrlBytes + cnt_bytes));
     // ticket, finish count and per-tile counters must start at zero
     LORA_CUDA_TRY(cudaMemsetAsync(scratch, 0, kCtrlBytes + pl.cnt_ints * 4, (cudaStream_t)stream));
     g.in = (const uint16_t *)x;

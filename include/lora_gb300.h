@@ -240,7 +240,10 @@ LORA_API lora_status_t lora_expand(const lora_pool_t *pool, const lora_meta_t *m
                           void *y, int64_t ldy, void *stream);
 
 /* Workspace bytes for lora_apply_slices / lora_moe_apply on up to T tokens
- * (top_k = 1 for a dense pool). */
+ * (top_k = 1 for a dense pool).  The first eighth of a workspace holds
+ * counters that every call leaves zero; the rest is scratch.  One workspace
+ * may serve every layer of a pool and any batch of up to T tokens, as long
+ * as every call passes the same (workspace, ws_bytes) pair. */
 LORA_API size_t lora_workspace_bytes(const lora_pool_t *pool, int32_t T, int32_t top_k);
 
 /* Zero a workspace (a cudaMemsetAsync).  A workspace must be zero before its

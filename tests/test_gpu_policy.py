@@ -96,3 +96,44 @@ def test_apply_in_a_graph_replayed(pol):
     _, d_ref = oracle.dense_delta(c)
     act = active_mask(c.idx, c.L, c.enabled, c.ranks)
     assert_delta(bf16_bits_to_f32(y)[act], 3 * d_ref[act], "3 replays")
+
+
+def test_moe_repeated_steps_share_workspace(policy):
+    """w13 and w2 calls alternate on one workspace for three steps: every call
+    type and path leaves the workspace ready for the next call."""
+    c = gen.moe(shared_outer=False)
+    run = H.MoERun(c)
+    try:
+        for _ in range(3):
+            run.step()
+        ic1 = H.from_dev_u16(run.ic1)
+        ic3 = H.from_dev_u16(run.ic3)
+        assert run.status() == 0
+    finally:
+        run.close()
+    _, d13 = oracle.moe_w13(c)
+    _, d2 = oracle.moe_w2(c)
+    assert_delta(bf16_bits_to_f32(ic1), 3 * d13, "w13 x3")
+    assert_delta(bf16_bits_to_f32(ic3), 3 * d2, "w2 x3")
+
+
+def test_dense_token_counts_share_workspace(policy):
+    """Batches of 256, 100 and 256 tokens on one workspace sized for 256."""
+    c = gen.decode_qkv()
+    run = H.DenseRun(c)
+    try:
+        run.build_meta(c.T)
+        run.apply()
+        run.build_meta(100)
+        run.apply()
+        run.build_meta(c.T)
+        run.apply()
+        y = run.y_host()
+        assert run.status() == 0
+    finally:
+        run.close()
+    _, d_ref = oracle.dense_delta(c)
+    w = np.full(c.T, 2.0)
+    w[:100] = 3.0
+    act = active_mask(c.idx, c.L, c.enabled, c.ranks)
+    assert_delta(bf16_bits_to_f32(y)[act] - bf16_bits_to_f32(c.y0)[act], (w[:, None] * d_ref)[act], "256+100+256")

@@ -28,10 +28,21 @@ namespace {
 
 using namespace bgmv;
 
-constexpr int kThreads = 128;
+constexpr int kSThreads = 256;            // shrink: 8 warps
+constexpr int kSWarps = kSThreads / 32;
+constexpr int kStages = 4;                // shrink bulk-copy ring depth
+constexpr int kMaxUnits = 4;              // MMA column blocks per shrink warp
+constexpr int kThreads = 128;             // expand: 4 warps
 constexpr int kWarps = kThreads / 32;
 constexpr int kTileRows = LORA_TILE_ROWS;
-constexpr int kOC = 256;  // output columns per expand CTA
+constexpr int kOC = 256;                  // output columns per expand CTA
+
+// Hidden chunks per tile, decided on the device from the real tile count so
+// that the shrink fills about one wave of CTAs: the expand recomputes it.
+__device__ __forceinline__ int chunks_for(int n_tiles, int slots, int nc_max) {
+    const int q = slots / (n_tiles > 0 ? n_tiles : 1);
+    return q < 1 ? 1 : (q > nc_max ? nc_max : q);
+}
 
 struct SArgs {
     int n_slices, in_dim, E, row_div, R, R8;
@@ -42,17 +53,17 @@ struct SArgs {
     int count_idx;
     const uint16_t *in;
     long long ld_in;
-    int NC, HC, SC;          // hidden chunks, chunk length, stage length (elements)
-    int xs_stride, as_stride;
-    int off_x, off_a, x_stage_bytes, a_stage_bytes, off_red;
-    float *part;             // [NC][n_slices][rows][R8], unscaled
+    int nc_max, slots;       // chunk bound and target CTAs (see chunks_for)
+    int SC, stride;          // stage length (elements), smem row stride (elements)
+    int nst, stage_bytes, off_red, hsplit;  // ring depth (<= kStages), ...
+    float *part;             // [nc][n_slices][rows][R8], unscaled
     int rows;
     int *status;
     int spin_limit;
 };
 
 struct EArgs {
-    int n_slices, R, R8, E, out_total, NC;
+    int n_slices, R, R8, E, out_total, nc_max, slots;
     int out_w[LORA_MAX_SLICES], out_off[LORA_MAX_SLICES];
     const uint16_t *B[LORA_MAX_SLICES];
     long long B_ss[LORA_MAX_SLICES];
@@ -75,270 +86,302 @@ struct EArgs {
 };
 
 // ---------------------------------------------------------------- shrink
+//
+// One CTA per (16-row tile, hidden chunk c), all slices: the x rows of the
+// chunk are read once for every slice.  Shared memory holds kStages stages
+// of [16 x rows | slice 0 A rows (R8) | slice 1 A rows | ...] x SC columns.
+// MMA units (slice, 8-rank column block, hidden split) are spread over the
+// 8 warps, at most kMaxUnits each.
 
-__global__ void __launch_bounds__(kThreads) bgmv_shrink_kernel(const __grid_constant__ SArgs p) {
+__global__ void __launch_bounds__(kSThreads) bgmv_shrink_kernel(const __grid_constant__ SArgs p) {
     extern __shared__ __align__(128) char smem[];
-    __shared__ __align__(8) uint64_t full[2];
+    __shared__ __align__(8) uint64_t full[kStages];
     __shared__ int s_rows[kTileRows];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, c4 = lane & 3;
-    const int per_tile = p.n_slices * p.NC;
-    const int tile = blockIdx.x / per_tile;
-    const int rem = blockIdx.x - tile * per_tile;
-    const int j = rem / p.NC, c = rem - j * p.NC;
+    const int ns = p.n_slices, W = ns * p.R8;
 
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int n_tiles = p.counters[p.count_idx];
-    const int row0 = p.tile_row0[tile];
-    const int keyn = p.tile_keyn[tile];
-    if (tile >= n_tiles) return;
+    const int nc = chunks_for(n_tiles, p.slots, p.nc_max);
+    const int total = n_tiles * nc;
+    if ((int)blockIdx.x >= total) return;
     // the expand may launch and prefetch its weights and outputs now
     asm volatile("griddepcontrol.launch_dependents;");
-    const int n = keyn & 31, key = keyn >> 5;
-    const int a = key / p.E, e = key - a * p.E;
-    const int r = p.rank[a];
-    const uint16_t *Ab = p.A[j] + (long long)a * p.A_ss[j] + (long long)e * p.A_es[j];
-    const int hb = c * p.HC, he = min(p.in_dim, hb + p.HC);
-    const int n_sub = (he - hb + p.SC - 1) / p.SC;
-    if (tid < n) s_rows[tid] = p.sorted[row0 + tid];
-    if (tid == 0) {
-        mbar_init(&full[0], 1);
-        mbar_init(&full[1], 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    __syncthreads();
+    if (tid < p.nst) mbar_init(&full[tid], 1);
+    if (tid == 0) asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    const int HC = ((p.in_dim + nc - 1) / nc + 15) & ~15;
+    const long long cstride = (long long)p.rows * p.R8;
+    float *red = (float *)(smem + p.off_red);
+    int gs = 0;  // sub-stages consumed by this CTA so far (ring slot and phase)
 
-    auto issue = [&](int s) {
-        const int h0 = hb + s * p.SC, len = min(p.SC, he - h0), st = s & 1;
-        uint16_t *xs = (uint16_t *)(smem + p.off_x + st * p.x_stage_bytes);
-        uint16_t *as = (uint16_t *)(smem + p.off_a + st * p.a_stage_bytes);
-        const uint32_t rowb = (uint32_t)len * 2;
-        if (lane == 0) mbar_expect_tx(&full[st], rowb * (uint32_t)(n + r));
-        __syncwarp();
-        for (int i = lane; i < n + r; i += 32) {
-            if (i < n)
-                bulk_g2s(xs + i * p.xs_stride, p.in + (long long)(s_rows[i] / p.row_div) * p.ld_in + h0, rowb,
-                         &full[st]);
-            else
-                bulk_g2s(as + (i - n) * p.as_stride, Ab + (long long)(i - n) * p.in_dim + h0, rowb, &full[st]);
+    for (int item = blockIdx.x; item < total; item += gridDim.x) {
+        const int tile = item / nc, c = item - tile * nc;
+        const int row0 = p.tile_row0[tile];
+        const int keyn = p.tile_keyn[tile];
+        const int n = keyn & 31, key = keyn >> 5;
+        const int a = key / p.E, e = key - a * p.E;
+        const int r = p.rank[a];
+        const int hb = min(p.in_dim, c * HC), he = min(p.in_dim, hb + HC);
+        const int n_sub = (he - hb + p.SC - 1) / p.SC;
+        __syncthreads();  // the previous item is done with s_rows, the stages and red
+        if (tid < n) s_rows[tid] = p.sorted[row0 + tid];
+        for (int i = tid; i < p.hsplit * kTileRows * W; i += kSThreads) red[i] = 0.f;
+        __syncthreads();
+
+        // sub-stage s: x rows 0..n-1, then for slice j rows 16 + j*R8 + (0..r-1)
+        const int n_copies = n + ns * r;
+        auto issue = [&](int s) {
+            const int h0 = hb + s * p.SC, len = min(p.SC, he - h0), st = (gs + s) % p.nst;
+            uint16_t *buf = (uint16_t *)(smem + st * p.stage_bytes);
+            const uint32_t rowb = (uint32_t)len * 2;
+            if (lane == 0) mbar_expect_tx(&full[st], rowb * (uint32_t)n_copies);
+            __syncwarp();
+            for (int i = lane; i < n_copies; i += 32) {
+                if (i < n) {
+                    bulk_g2s(buf + i * p.stride, p.in + (long long)(s_rows[i] / p.row_div) * p.ld_in + h0, rowb,
+                             &full[st]);
+                } else {
+                    const int q = i - n, j = q / r, k = q - j * r;
+                    const uint16_t *Ab = p.A[j] + (long long)a * p.A_ss[j] + (long long)e * p.A_es[j];
+                    bulk_g2s(buf + (kTileRows + j * p.R8 + k) * p.stride, Ab + (long long)k * p.in_dim + h0, rowb,
+                             &full[st]);
+                }
+            }
+        };
+        if (warp == 0) {
+            // the stages were last read through the generic proxy
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            for (int s = 0; s < min(n_sub, p.nst); ++s) issue(s);
         }
-    };
-    if (warp == 0)
-        for (int s = 0; s < min(n_sub, 2); ++s) issue(s);
 
-    // units: (n-block of 8 ranks, hidden split) spread over the 4 warps, <= 2 each
-    const int nnb = (r + 7) >> 3;
-    int hsplit = 1;
-    while (nnb * hsplit * 2 <= 2 * kWarps && hsplit < 4) hsplit *= 2;
-    const int units = nnb * hsplit;
-    float acc[2][4];
+        const int nnb = (r + 7) >> 3;  // 8-rank column blocks of this slot
+        const int hsplit = p.hsplit;
+        const int units = ns * nnb * hsplit;
+        float acc[kMaxUnits][4];
 #pragma unroll
-    for (int u = 0; u < 2; ++u)
+        for (int u = 0; u < kMaxUnits; ++u)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) acc[u][i] = 0.f;
-    for (int s = 0; s < n_sub; ++s) {
-        const int st = s & 1;
-        mbar_wait(&full[st], (uint32_t)((s >> 1) & 1), p.spin_limit, p.status);
-        const int len = min(p.SC, he - hb - s * p.SC);
-        const int steps = (len + 15) >> 4;
-        const uint16_t *xs = (const uint16_t *)(smem + p.off_x + st * p.x_stage_bytes);
-        const uint16_t *as = (const uint16_t *)(smem + p.off_a + st * p.a_stage_bytes);
+            for (int i = 0; i < 4; ++i) acc[u][i] = 0.f;
+        for (int s = 0; s < n_sub; ++s) {
+            const int st = (gs + s) % p.nst;
+            mbar_wait(&full[st], (uint32_t)(((gs + s) / p.nst) & 1), p.spin_limit, p.status);
+            const int len = min(p.SC, he - hb - s * p.SC);
+            const int steps = (len + 15) >> 4;
+            const uint16_t *buf = (const uint16_t *)(smem + st * p.stage_bytes);
 #pragma unroll
-        for (int ui = 0; ui < 2; ++ui) {
-            const int u = warp + ui * kWarps;
+            for (int ui = 0; ui < kMaxUnits; ++ui) {
+                const int u = warp + ui * kSWarps;
+                if (u < units) {
+                    const int cb = u / hsplit, hs = u - cb * hsplit;
+                    const int j = cb / nnb, nb = cb - j * nnb;
+                    const uint16_t *bq = buf + (kTileRows + j * p.R8 + nb * 8 + (lane & 7)) * p.stride +
+                                         ((lane >> 3) & 1) * 8;
+                    const uint16_t *aq = buf + ((lane & 7) + ((lane >> 3) & 1) * 8) * p.stride + (lane >> 4) * 8;
+                    for (int i = hs; i < steps; i += hsplit) {
+                        const int k0 = i * 16;
+                        uint32_t a0, a1, a2, a3, b0, b1;
+                        ldsm_x4(aq + k0, a0, a1, a2, a3);
+                        ldsm_x2(bq + k0, b0, b1);
+                        if (k0 + 8 >= len) a2 = a3 = b1 = 0u;
+                        mma16816(acc[ui], a0, a1, a2, a3, b0, b1);
+                    }
+                }
+            }
+            __syncthreads();
+            if (warp == 0 && s + p.nst < n_sub) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                issue(s + p.nst);
+            }
+        }
+        gs += n_sub;
+
+        // partial sums [hsplit][16][ns*R8] in shared memory, reduced over the
+        // hidden split, then stored as this chunk's part[c][j][row0 + t][k]
+#pragma unroll
+        for (int ui = 0; ui < kMaxUnits; ++ui) {
+            const int u = warp + ui * kSWarps;
             if (u < units) {
-                const int nb = u / hsplit, hs = u - nb * hsplit;
-                for (int i = hs; i < steps; i += hsplit) {
-                    const int k0 = i * 16;
-                    uint32_t a0, a1, a2, a3, b0, b1;
-                    ldsm_x4(xs + ((lane & 7) + ((lane >> 3) & 1) * 8) * p.xs_stride + k0 + (lane >> 4) * 8,
-                            a0, a1, a2, a3);
-                    ldsm_x2(as + (nb * 8 + (lane & 7)) * p.as_stride + k0 + ((lane >> 3) & 1) * 8, b0, b1);
-                    if (k0 + 8 >= len) a2 = a3 = b1 = 0u;
-                    mma16816(acc[ui], a0, a1, a2, a3, b0, b1);
+                const int cb = u / hsplit, hs = u - cb * hsplit;
+                const int j = cb / nnb, nb = cb - j * nnb;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int k = nb * 8 + 2 * c4 + h;
+                    if (k < r) {
+                        float *dst = red + (hs * kTileRows) * W + j * p.R8 + k;
+                        if (g < n) dst[g * W] = acc[ui][h];
+                        if (g + 8 < n) dst[(g + 8) * W] = acc[ui][2 + h];
+                    }
                 }
             }
         }
         __syncthreads();
-        if (warp == 0 && s + 2 < n_sub) {
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            issue(s + 2);
+        float *base = p.part + (long long)c * ns * cstride + (long long)row0 * p.R8;
+        for (int i = tid; i < n * W; i += kSThreads) {
+            const int t = i / W, q = i - t * W;
+            const int j = q / p.R8, k = q - j * p.R8;
+            float sum = 0.f;
+            for (int hs = 0; hs < hsplit; ++hs) sum += red[(hs * kTileRows + t) * W + q];
+            base[j * cstride + t * p.R8 + k] = sum;
         }
-    }
-
-    // partials of this chunk: [hsplit][16][R8] in shared memory, summed over
-    // the hidden split, then one row of R8 floats per token to global memory
-    float *red = (float *)(smem + p.off_red);
-    for (int i = tid; i < hsplit * kTileRows * p.R8; i += kThreads) red[i] = 0.f;
-    __syncthreads();
-#pragma unroll
-    for (int ui = 0; ui < 2; ++ui) {
-        const int u = warp + ui * kWarps;
-        if (u < units) {
-            const int nb = u / hsplit, hs = u - nb * hsplit;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int k = nb * 8 + 2 * c4 + h;
-                if (k < r) {
-                    float *dst = red + (hs * kTileRows) * p.R8 + k;
-                    if (g < n) dst[g * p.R8] = acc[ui][h];
-                    if (g + 8 < n) dst[(g + 8) * p.R8] = acc[ui][2 + h];
-                }
-            }
-        }
-    }
-    __syncthreads();
-    // this chunk's partial: part[c][j][row0 + t][k]
-    float *dst = p.part + ((long long)c * p.n_slices + j) * p.rows * p.R8 + (long long)row0 * p.R8;
-    for (int i = tid; i < n * p.R8; i += kThreads) {
-        const int t = i / p.R8, k = i - t * p.R8;
-        float s = 0.f;
-        for (int hs = 0; hs < hsplit; ++hs) s += red[(hs * kTileRows + t) * p.R8 + k];
-        dst[i] = s;
     }
 }
 
 // ---------------------------------------------------------------- expand
+//
+// Items (tile, 256 output columns), tile-major, strided over the grid.  The
+// first item's B rows and y rows are requested before the shrink is waited
+// for; the metadata was complete before the shrink started.
 
 __global__ void __launch_bounds__(kThreads) bgmv_expand_kernel(const __grid_constant__ EArgs p) {
     extern __shared__ __align__(128) char smem[];
     __shared__ __align__(8) uint64_t bbar, ybar;
     __shared__ int s_rows[kTileRows];
+    __shared__ float s_w[kTileRows];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, c4 = lane & 3;
-    const int tile = blockIdx.x / p.n_oc;
-    const int oc = blockIdx.x - tile * p.n_oc;
-
-    // the metadata was complete before the shrink started: read it at once
-    const int n_tiles = p.counters[p.count_idx];
-    const int row0 = p.tile_row0[tile];
-    const int keyn = p.tile_keyn[tile];
-    if (tile >= n_tiles) return;
-    const int n = keyn & 31, key = keyn >> 5;
-    const int a = key / p.E, e = key - a * p.E;
-    const int r = p.rank[a];
-    const int rs = (r + 7) & ~7;
     const int ns = p.n_slices;
-    const int ob = oc * kOC, oe = min(p.out_total, ob + kOC);
-    if (tid < n) s_rows[tid] = p.sorted[row0 + tid];
+    const int n_tiles = p.counters[p.count_idx];
+    const int total = n_tiles * p.n_oc;
+    if ((int)blockIdx.x >= total) return;
     if (tid == 0) {
         mbar_init(&bbar, 1);
         mbar_init(&ybar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    __syncthreads();
     uint16_t *bs = (uint16_t *)(smem + p.off_b);
     uint16_t *ys = (uint16_t *)(smem + p.off_ys);
-    // weights and outputs do not depend on the shrink: fetch them first
-    if (warp == 0) {
-        const uint32_t rowb = (uint32_t)(oe - ob) * 2;
-        if (lane == 0) mbar_expect_tx(&ybar, rowb * (uint32_t)n);
-        __syncwarp();
-        if (lane < n) bulk_g2s(ys + lane * p.ys_stride, p.out + (long long)s_rows[lane] * p.ld_out + ob, rowb, &ybar);
-    } else if (warp == 1) {
-        if (lane == 0) mbar_expect_tx(&bbar, (uint32_t)(oe - ob) * rs * 2);
-        __syncwarp();
-        if (lane < ns) {
-            const int jj = lane;
-            const int s0 = max(ob, p.out_off[jj]), s1 = min(oe, p.out_off[jj] + p.out_w[jj]);
-            if (s1 > s0) {
-                const uint16_t *Bj = p.B[jj] + (long long)a * p.B_ss[jj] +
-                                     (p.B_shared[jj] ? 0ll : (long long)e * p.out_w[jj] * rs);
-                bulk_g2s(bs + (long long)(s0 - ob) * rs, Bj + (long long)(s0 - p.out_off[jj]) * rs,
-                         (uint32_t)(s1 - s0) * rs * 2, &bbar);
-            }
-        }
-    }
-
-    __shared__ float s_w[kTileRows];
-    if (tid < kTileRows) s_w[tid] = tid < n ? p.scale[a] * p.post_scale * (p.row_w ? p.row_w[s_rows[tid]] : 1.f) : 0.f;
-    asm volatile("griddepcontrol.wait;" ::: "memory");  // the shrink's partials are complete
-    __syncthreads();
-    // v of the slices this CTA touches (chunk partials summed in order, scaled)
-    // -> bf16 hi / lo, [16][vr_stride] at j * R8 + k
     uint16_t *vh = (uint16_t *)(smem + p.off_vh);
     uint16_t *vl = (uint16_t *)(smem + p.off_vl);
-    int j0 = 0, j1 = 0;
-    while (j0 + 1 < ns && ob >= p.out_off[j0 + 1]) ++j0;
-    j1 = j0;
-    while (j1 + 1 < ns && oe > p.out_off[j1 + 1]) ++j1;
-    const int per_t = (j1 - j0 + 1) * p.R8 / 4;
-    for (int i = tid; i < kTileRows * per_t; i += kThreads) {
-        const int t = i / per_t, q = i - t * per_t;
-        const int jj = j0 + (q * 4) / p.R8, k = (q * 4) % p.R8;
-        float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (t < n) {
-            const float4 *src = (const float4 *)(p.part + ((long long)jj * p.rows + row0 + t) * p.R8 + k);
-            const long long cstride = (long long)ns * p.rows * p.R8 / 4;
-            for (int cc = 0; cc < p.NC; ++cc) {
-                const float4 q = __ldcg(src + cc * cstride);
-                s4.x += q.x;
-                s4.y += q.y;
-                s4.z += q.z;
-                s4.w += q.w;
-            }
-            const float w = s_w[t];
-            s4.x *= w;
-            s4.y *= w;
-            s4.z *= w;
-            s4.w *= w;
-        }
-        const __nv_bfloat162 h01 = __floats2bfloat162_rn(s4.x, s4.y);
-        const __nv_bfloat162 h23 = __floats2bfloat162_rn(s4.z, s4.w);
-        const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
-        uint2 hv, lv;
-        hv.x = *(const uint32_t *)&h01;
-        hv.y = *(const uint32_t *)&h23;
-        lv.x = pack_bf16x2(s4.x - f01.x, s4.y - f01.y);
-        lv.y = pack_bf16x2(s4.z - f23.x, s4.w - f23.y);
-        *(uint2 *)(vh + t * p.vr_stride + jj * p.R8 + k) = hv;
-        *(uint2 *)(vl + t * p.vr_stride + jj * p.R8 + k) = lv;
-    }
-    __syncthreads();
-    mbar_wait(&bbar, 0, p.spin_limit, p.status);
-    mbar_wait(&ybar, 0, p.spin_limit, p.status);
-
-    const int nob = (oe - ob) >> 3;
-    const int ksteps = (rs + 15) >> 4;
     const int arow = (lane & 7) + ((lane >> 3) & 1) * 8;
+    int nc = 0;
+    uint32_t phase = 0;
+
+    for (int item = blockIdx.x; item < total; item += gridDim.x, phase ^= 1u) {
+        const int tile = item / p.n_oc, oc = item - tile * p.n_oc;
+        const int row0 = p.tile_row0[tile];
+        const int keyn = p.tile_keyn[tile];
+        const int n = keyn & 31, key = keyn >> 5;
+        const int a = key / p.E, e = key - a * p.E;
+        const int r = p.rank[a];
+        const int rs = (r + 7) & ~7;
+        const int ob = oc * kOC, oe = min(p.out_total, ob + kOC);
+        __syncthreads();  // the previous item's stores have been issued and its buffers read
+        if (tid < n) s_rows[tid] = p.sorted[row0 + tid];
+        __syncthreads();
+        // weights and outputs do not depend on the shrink: fetch them first
+        if (warp == 0) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            const uint32_t rowb = (uint32_t)(oe - ob) * 2;
+            if (lane == 0) mbar_expect_tx(&ybar, rowb * (uint32_t)n);
+            __syncwarp();
+            if (lane < n)
+                bulk_g2s(ys + lane * p.ys_stride, p.out + (long long)s_rows[lane] * p.ld_out + ob, rowb, &ybar);
+        } else if (warp == 1) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            if (lane == 0) mbar_expect_tx(&bbar, (uint32_t)(oe - ob) * rs * 2);
+            __syncwarp();
+            if (lane < ns) {
+                const int jj = lane;
+                const int s0 = max(ob, p.out_off[jj]), s1 = min(oe, p.out_off[jj] + p.out_w[jj]);
+                if (s1 > s0) {
+                    const uint16_t *Bj = p.B[jj] + (long long)a * p.B_ss[jj] +
+                                         (p.B_shared[jj] ? 0ll : (long long)e * p.out_w[jj] * rs);
+                    bulk_g2s(bs + (long long)(s0 - ob) * rs, Bj + (long long)(s0 - p.out_off[jj]) * rs,
+                             (uint32_t)(s1 - s0) * rs * 2, &bbar);
+                }
+            }
+        }
+        if (tid < kTileRows)
+            s_w[tid] = tid < n ? p.scale[a] * p.post_scale * (p.row_w ? p.row_w[s_rows[tid]] : 1.f) : 0.f;
+        if (nc == 0) {
+            asm volatile("griddepcontrol.wait;" ::: "memory");  // the shrink's partials are complete
+            nc = chunks_for(n_tiles, p.slots, p.nc_max);
+        }
+        __syncthreads();
+        // v of the slices this item touches (chunk partials summed in order,
+        // scaled) -> bf16 hi / lo, [16][vr_stride] at j * R8 + k
+        int j0 = 0;
+        while (j0 + 1 < ns && ob >= p.out_off[j0 + 1]) ++j0;
+        int j1 = j0;
+        while (j1 + 1 < ns && oe > p.out_off[j1 + 1]) ++j1;
+        const int per_t = (j1 - j0 + 1) * p.R8 / 4;
+        const long long cstride = (long long)ns * p.rows * p.R8 / 4;
+        for (int i = tid; i < kTileRows * per_t; i += kThreads) {
+            const int t = i / per_t, q = i - t * per_t;
+            const int jj = j0 + (q * 4) / p.R8, k = (q * 4) % p.R8;
+            float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (t < n) {
+                const float4 *src = (const float4 *)(p.part + ((long long)jj * p.rows + row0 + t) * p.R8 + k);
+                for (int cc = 0; cc < nc; ++cc) {
+                    const float4 v = __ldcg(src + cc * cstride);
+                    s4.x += v.x;
+                    s4.y += v.y;
+                    s4.z += v.z;
+                    s4.w += v.w;
+                }
+                const float w = s_w[t];
+                s4.x *= w;
+                s4.y *= w;
+                s4.z *= w;
+                s4.w *= w;
+            }
+            const __nv_bfloat162 h01 = __floats2bfloat162_rn(s4.x, s4.y);
+            const __nv_bfloat162 h23 = __floats2bfloat162_rn(s4.z, s4.w);
+            const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+            uint2 hv, lv;
+            hv.x = *(const uint32_t *)&h01;
+            hv.y = *(const uint32_t *)&h23;
+            lv.x = pack_bf16x2(s4.x - f01.x, s4.y - f01.y);
+            lv.y = pack_bf16x2(s4.z - f23.x, s4.w - f23.y);
+            *(uint2 *)(vh + t * p.vr_stride + jj * p.R8 + k) = hv;
+            *(uint2 *)(vl + t * p.vr_stride + jj * p.R8 + k) = lv;
+        }
+        __syncthreads();
+        mbar_wait(&bbar, phase, p.spin_limit, p.status);
+        mbar_wait(&ybar, phase, p.spin_limit, p.status);
+
+        const int nob = (oe - ob) >> 3;
+        const int ksteps = (rs + 15) >> 4;
 #pragma unroll 1
-    for (int ob8 = warp; ob8 < nob; ob8 += kWarps) {
-        const int o0 = ob + ob8 * 8;
-        int jj = j0;
-        while (jj + 1 < ns && o0 >= p.out_off[jj + 1]) ++jj;
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int ks = 0; ks < ksteps; ++ks) {
-            const int k0 = ks * 16;
-            uint32_t h0, h1, h2, h3, l0, l1, l2, l3, b0, b1;
-            const int acol = jj * p.R8 + k0 + (lane >> 4) * 8;
-            ldsm_x4(vh + arow * p.vr_stride + acol, h0, h1, h2, h3);
-            ldsm_x4(vl + arow * p.vr_stride + acol, l0, l1, l2, l3);
-            ldsm_x2(bs + (ob8 * 8 + (lane & 7)) * rs + k0 + ((lane >> 3) & 1) * 8, b0, b1);
-            if (k0 + 8 >= rs) h2 = h3 = l2 = l3 = b1 = 0u;
-            mma16816(d, h0, h1, h2, h3, b0, b1);
-            mma16816(d, l0, l1, l2, l3, b0, b1);
+        for (int ob8 = warp; ob8 < nob; ob8 += kWarps) {
+            const int o0 = ob + ob8 * 8;
+            int jj = j0;
+            while (jj + 1 < ns && o0 >= p.out_off[jj + 1]) ++jj;
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int ks = 0; ks < ksteps; ++ks) {
+                const int k0 = ks * 16;
+                uint32_t h0, h1, h2, h3, l0, l1, l2, l3, b0, b1;
+                const int acol = jj * p.R8 + k0 + (lane >> 4) * 8;
+                ldsm_x4(vh + arow * p.vr_stride + acol, h0, h1, h2, h3);
+                ldsm_x4(vl + arow * p.vr_stride + acol, l0, l1, l2, l3);
+                ldsm_x2(bs + (ob8 * 8 + (lane & 7)) * rs + k0 + ((lane >> 3) & 1) * 8, b0, b1);
+                if (k0 + 8 >= rs) h2 = h3 = l2 = l3 = b1 = 0u;
+                mma16816(d, h0, h1, h2, h3, b0, b1);
+                mma16816(d, l0, l1, l2, l3, b0, b1);
+            }
+            const int ocol = ob8 * 8 + 2 * c4;
+            if (g < n) {
+                uint32_t *yp = (uint32_t *)(ys + g * p.ys_stride + ocol);
+                const uint32_t u = *yp;
+                *yp = pack_bf16x2(bf16lo(u) + d[0], bf16hi(u) + d[1]);
+            }
+            if (g + 8 < n) {
+                uint32_t *yp = (uint32_t *)(ys + (g + 8) * p.ys_stride + ocol);
+                const uint32_t u = *yp;
+                *yp = pack_bf16x2(bf16lo(u) + d[2], bf16hi(u) + d[3]);
+            }
         }
-        const int ocol = ob8 * 8 + 2 * c4;
-        if (g < n) {
-            uint32_t *yp = (uint32_t *)(ys + g * p.ys_stride + ocol);
-            const uint32_t u = *yp;
-            *yp = pack_bf16x2(bf16lo(u) + d[0], bf16hi(u) + d[1]);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncthreads();
+        if (warp == 0 && lane < n) {
+            asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                             p.out + (long long)s_rows[lane] * p.ld_out + ob),
+                         "r"(smem_u32(ys + lane * p.ys_stride)), "r"((uint32_t)(oe - ob) * 2)
+                         : "memory");
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+            asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
         }
-        if (g + 8 < n) {
-            uint32_t *yp = (uint32_t *)(ys + (g + 8) * p.ys_stride + ocol);
-            const uint32_t u = *yp;
-            *yp = pack_bf16x2(bf16lo(u) + d[2], bf16hi(u) + d[3]);
-        }
-    }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    __syncthreads();
-    if (warp == 0 && lane < n) {
-        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
-                         p.out + (long long)s_rows[lane] * p.ld_out + ob),
-                     "r"(smem_u32(ys + lane * p.ys_stride)), "r"((uint32_t)(oe - ob) * 2)
-                     : "memory");
-        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     }
     asm volatile("griddepcontrol.launch_dependents;");
 }
@@ -349,14 +392,14 @@ int g_split_configured[64];
 
 }  // namespace
 
+int nc_max_for(int in_dim) {
+    const int q = in_dim / 256;
+    return q < 1 ? 1 : (q > 8 ? 8 : q);
+}
+
 size_t lora_split_ws_bytes(int n_slices, int in_dim, int R, int rows, int max_tiles) {
-    const int R8 = lora_round8(R);
-    int HC = (16384 / (R8 > 0 ? R8 : 8) + 63) / 64 * 64;
-    if (HC < 256) HC = 256;
-    int NC = lora_ceil_div(in_dim, HC);
-    if (NC > 8) NC = 8;
     (void)max_tiles;
-    return a128((size_t)NC * n_slices * rows * R8 * 4);
+    return a128((size_t)nc_max_for(in_dim) * n_slices * rows * lora_round8(R) * 4);
 }
 
 lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, void *ws, size_t ws_bytes,
@@ -366,31 +409,39 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     int out_total = 0;
     for (int j = 0; j < ns; ++j) out_total = max(out_total, pr.out_off[j] + pr.out_w[j]);
     const long long max_tiles = pr.rows / kTileRows + (pr.rows < pr.n_keys ? pr.rows : pr.n_keys);
-    // the shrink holds at most two 8-rank MMA column blocks per warp
-    if (R8 > 2 * kWarps * 8 || max_tiles <= 0) return LORA_OK;
-    // hidden chunks: ~32 KB of A rows per shrink CTA at full rank, at most 8
-    int HC = (16384 / R8 + 63) / 64 * 64;
-    if (HC < 256) HC = 256;
-    int NC = lora_ceil_div(pr.in_dim, HC);
-    if (NC > 8) NC = 8;
-    HC = ((lora_ceil_div(pr.in_dim, NC) + 15) / 16) * 16;
-    NC = lora_ceil_div(pr.in_dim, HC);
-    const size_t need = lora_split_ws_bytes(ns, pr.in_dim, R, pr.rows, (int)max_tiles + 1);
-    if (!ws || ws_bytes < need || !lora_aligned16(ws)) return LORA_OK;
-    // shrink shared memory: 2 stages of (16 x rows + R x rows) of SC elements, then the partial sums
-    int SC = HC;
-    const int red_bytes = 4 * kTileRows * R8 * 4;
-    auto stage_total = [&](int sc) { return 2 * (a128((size_t)kTileRows * (sc + 8) * 2) + a128((size_t)R8 * (sc + 8) * 2)); };
-    while (SC > 256 && stage_total(SC) + red_bytes > 100 * 1024) SC = ((SC / 2) + 15) / 16 * 16;
-    const size_t s_smem = stage_total(SC) + red_bytes;
-    if (s_smem > 200 * 1024) return LORA_OK;
+    // MMA column blocks of all slices must fit kMaxUnits per shrink warp
+    const int nb_tot = ns * (R8 / 8);
+    if (nb_tot > kSWarps * kMaxUnits || max_tiles <= 0) return LORA_OK;
+    const int nc_max = nc_max_for(pr.in_dim);
+    if (!ws || ws_bytes < lora_split_ws_bytes(ns, pr.in_dim, R, pr.rows, 0) || !lora_aligned16(ws)) return LORA_OK;
+    int hsplit = 1;
+    while (hsplit < 4 && nb_tot * hsplit * 2 <= 2 * kSWarps) hsplit *= 2;
+    // shrink shared memory: nst stages of (16 + ns*R8) rows x SC columns, then
+    // the partial sums; about 72 KB so that three CTAs share an SM (else 110 KB
+    // for two), with the deepest ring whose stages still move >= 128 columns
+    // (256-byte copies)
+    const int rows_s = kTileRows + ns * R8;
+    const size_t red_bytes = (size_t)hsplit * kTileRows * ns * R8 * 4;
+    auto smem_for = [&](int nst, int sc) { return nst * a128((size_t)rows_s * (sc + 8) * 2) + red_bytes; };
+    int SC = 0, nst = 0;
+    for (size_t budget : {(size_t)72 * 1024, (size_t)110 * 1024, (size_t)200 * 1024}) {
+        for (int d = kStages; d >= 2 && !nst; --d) {
+            int sc = 512;
+            while (sc > 128 && smem_for(d, sc) > budget) sc -= 16;
+            if (smem_for(d, sc) <= budget) {
+                SC = sc;
+                nst = d;
+            }
+        }
+        if (nst) break;
+    }
+    if (!nst) return LORA_OK;
+    const size_t s_smem = smem_for(nst, SC);
     // expand shared memory: B rows, y rows, v hi/lo
     const int vr_stride = ns * R8 + 8;
     const size_t e_b = a128((size_t)kOC * R8 * 2 + 32), e_y = a128((size_t)kTileRows * (kOC + 8) * 2);
     const size_t e_v = a128((size_t)kTileRows * vr_stride * 2);
     const size_t e_smem = e_b + e_y + 2 * e_v;
-
-    float *part = (float *)ws;
 
     const int dev = pool->device < 64 ? pool->device : 63;
     if (!g_split_configured[dev]) {
@@ -400,6 +451,12 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
                                            200 * 1024));
         g_split_configured[dev] = 1;
     }
+    int occ = 0;
+    LORA_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, bgmv_shrink_kernel, kSThreads, s_smem));
+    if (occ < 1) occ = 1;
+    int occ_e = 0;
+    LORA_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_e, bgmv_expand_kernel, kThreads, e_smem));
+    const long long e_slots = (long long)pool->num_sms * (occ_e < 1 ? 1 : occ_e);
 
     SArgs sa;
     memset(&sa, 0, sizeof(sa));
@@ -422,17 +479,15 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     sa.count_idx = pr.count_idx;
     sa.in = pr.in;
     sa.ld_in = pr.ld_in;
-    sa.NC = NC;
-    sa.HC = HC;
+    sa.nc_max = nc_max;
+    sa.slots = pool->num_sms * occ;
     sa.SC = SC;
-    sa.xs_stride = SC + 8;
-    sa.as_stride = SC + 8;
-    sa.x_stage_bytes = (int)a128((size_t)kTileRows * (SC + 8) * 2);
-    sa.a_stage_bytes = (int)a128((size_t)R8 * (SC + 8) * 2);
-    sa.off_x = 0;
-    sa.off_a = 2 * sa.x_stage_bytes;
-    sa.off_red = sa.off_a + 2 * sa.a_stage_bytes;
-    sa.part = part;
+    sa.stride = SC + 8;
+    sa.stage_bytes = (int)a128((size_t)rows_s * (SC + 8) * 2);
+    sa.nst = nst;
+    sa.off_red = nst * sa.stage_bytes;
+    sa.hsplit = hsplit;
+    sa.part = (float *)ws;
     sa.rows = pr.rows;
     sa.status = pr.status;
     sa.spin_limit = pr.spin_limit;
@@ -455,7 +510,8 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     ea.scale = pr.scale;
     ea.row_w = pr.row_w;
     ea.post_scale = pr.post_scale;
-    ea.NC = NC;
+    ea.nc_max = nc_max;
+    ea.slots = sa.slots;
     ea.sorted = pr.meta->sorted;
     ea.tile_row0 = pr.tile_row0;
     ea.tile_keyn = pr.tile_keyn;
@@ -463,7 +519,7 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     ea.count_idx = pr.count_idx;
     ea.out = pr.out;
     ea.ld_out = pr.ld_out;
-    ea.part = part;
+    ea.part = sa.part;
     ea.rows = pr.rows;
     ea.n_oc = lora_ceil_div(out_total, kOC);
     ea.ys_stride = kOC + 8;
@@ -482,13 +538,16 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     at[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(kSThreads, 1, 1);
     cfg.stream = s;
-    cfg.gridDim = dim3((unsigned)(max_tiles * ns * NC), 1, 1);
+    // grids of at most one wave; the kernels stride over their items
+    const long long s_items = max_tiles * nc_max, e_items = max_tiles * ea.n_oc;
+    cfg.gridDim = dim3((unsigned)(s_items < sa.slots ? s_items : sa.slots), 1, 1);
     cfg.dynamicSmemBytes = s_smem;
     LORA_CUDA_TRY(cudaLaunchKernelEx(&cfg, bgmv_shrink_kernel, sa));
     lora_note_launch();
-    cfg.gridDim = dim3((unsigned)(max_tiles * ea.n_oc), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.gridDim = dim3((unsigned)(e_items < e_slots ? e_items : e_slots), 1, 1);
     cfg.dynamicSmemBytes = e_smem;
     LORA_CUDA_TRY(cudaLaunchKernelEx(&cfg, bgmv_expand_kernel, ea));
     lora_note_launch();

@@ -50,6 +50,24 @@ __device__ __forceinline__ int row_key(const MetaArgs &a, const unsigned char *a
     return key;
 }
 
+// The same key from an already loaded slot s and expert e (e unused when dense).
+__device__ __forceinline__ int row_key_e(const MetaArgs &a, const unsigned char *act, int row, int s, int e,
+                                         int *bad) {
+    const bool valid = s >= 0 && s < a.L;
+    int b = (s != -1 && !valid && (row % a.K) == 0) ? 1 : 0;
+    const bool on = valid && act[s];
+    int key = a.n_keys;
+    if (a.topk) {
+        const bool ev = e >= 0 && e < a.E;
+        b += ev ? 0 : 1;
+        if (on && ev) key = s * a.E + e;
+    } else if (on) {
+        key = s;
+    }
+    *bad += b;
+    return key;
+}
+
 __global__ void __launch_bounds__(kThreads, 1) build_meta_kernel(MetaArgs a) {
     extern __shared__ int sm[];
     const int NK = a.n_keys, NK1 = NK + 1, W = a.n_chunks;
@@ -75,7 +93,16 @@ __global__ void __launch_bounds__(kThreads, 1) build_meta_kernel(MetaArgs a) {
     const int chunk = (rows + W - 1) / W;
     const int r0 = warp * chunk, r1 = min(rows, r0 + chunk);
     int s_first = -1;
-    if (warp < W && r0 + lane < r1) s_first = a.idx[(r0 + lane) / a.K];
+    if (!a.cache_keys && warp < W && r0 + lane < r1) s_first = a.idx[(r0 + lane) / a.K];
+    int sv[8], ev[8];
+    if (a.cache_keys) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int row = u * nthreads + tid;
+            sv[u] = row < rows ? a.idx[row / a.K] : -1;
+            ev[u] = (row < rows && a.topk) ? a.topk[row] : 0;
+        }
+    }
     for (int i = tid; i < a.L; i += nthreads) act[i] = (a.enabled[i] != 0 && a.rank[i] > 0) ? 1 : 0;
     for (int i = tid; i < W * NK1; i += nthreads) hist[i] = 0;
     for (int i = tid; i < NK1; i += nthreads) {
@@ -85,14 +112,42 @@ __global__ void __launch_bounds__(kThreads, 1) build_meta_kernel(MetaArgs a) {
     if (tid == 0) misc[36] = 0;
     __syncthreads();
 
+    // with the key cache: every row's key first, with the slot and expert
+    // loads of up to 8 rows per thread issued back to back (the first batch
+    // was issued before the tables were filled)
+    int bad = 0;
+    if (a.cache_keys) {
+        for (int base = 0; base < rows; base += 8 * nthreads) {
+            if (base > 0) {
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int row = base + u * nthreads + tid;
+                    sv[u] = row < rows ? a.idx[row / a.K] : -1;
+                    ev[u] = (row < rows && a.topk) ? a.topk[row] : 0;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int row = base + u * nthreads + tid;
+                if (row < rows) kc[row] = row_key_e(a, act, row, sv[u], ev[u], &bad);
+            }
+        }
+        __syncthreads();
+    }
+
     if (warp < W) {
-        int bad = 0;
         for (int base = r0; base < r1; base += 32) {
             const int row = base + lane;
             const bool v = row < r1;
-            const int s = base == r0 ? s_first : (v ? a.idx[row / a.K] : -1);
-            const int key = v ? row_key(a, act, row, s, &bad) : -1;
-            if (v && a.cache_keys) kc[row] = key;
+            int key = -1;
+            if (v) {
+                if (a.cache_keys) {
+                    key = kc[row];
+                } else {
+                    const int s = base == r0 ? s_first : a.idx[row / a.K];
+                    key = row_key(a, act, row, s, &bad);
+                }
+            }
             const unsigned peers = __match_any_sync(0xffffffffu, key);
             if (v && lane == __ffs(peers) - 1) hist[warp * NK1 + key] += __popc(peers);
             if (v && a.K == 1 && key < NK) {
@@ -101,10 +156,10 @@ __global__ void __launch_bounds__(kThreads, 1) build_meta_kernel(MetaArgs a) {
             }
             __syncwarp();
         }
-#pragma unroll
-        for (int o = 16; o; o >>= 1) bad += __shfl_xor_sync(0xffffffffu, bad, o);
-        if (lane == 0 && bad) atomicAdd(&misc[36], bad);
     }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) bad += __shfl_xor_sync(0xffffffffu, bad, o);
+    if (lane == 0 && bad) atomicAdd(&misc[36], bad);
     __syncthreads();
 
     // per key: exclusive prefix over the chunks (in place) and the count

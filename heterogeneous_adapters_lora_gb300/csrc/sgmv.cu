@@ -32,7 +32,7 @@ namespace {
 
 constexpr int kRows = LORA_LTILE_ROWS;  // 128 tokens per tile (MMA M)
 constexpr int kBK = 64;                 // hidden elements per K block (one 128-byte swizzle row)
-constexpr int kStages = 4;
+constexpr int kStages = 8;                 // shrink TMA ring: 8 x (16 KB x + R x 128 B A)
 constexpr int kThreads = 192;          // shrink: TMA warp, MMA warp, 4 epilogue warps
 constexpr int kEThreads = 320;         // expand: TMA warp, MMA warp, 8 epilogue warps
 constexpr int kNY = 3;                 // y tiles in flight in the expand

@@ -7,10 +7,11 @@
 // [n_slices][T][rank] (scale 1.0) and add_expand with add_input=True at the
 // slice offsets; add_lora_fused_moe does the same per (adapter, expert).
 //
-//   bgmv_shrink_kernel: one CTA per (16-row tile, slice j, hidden chunk c).
-//     Bulk copies (cp.async.bulk + mbarrier) bring the tile's x rows and the
-//     slot's A_j rows of chunk c; m16n8k16 bf16 MMAs (fp32 accumulate) give
-//     the partial v of chunk c, stored unscaled in fp32.
+//   bgmv_shrink_kernel: items (16-row tile, hidden chunk c), all slices at
+//     once.  Per 256-column stage, the slot's A rows of every slice arrive as
+//     8 x 256 tensor-map boxes (one TMA per 8 ranks) and the tile's x rows as
+//     one bulk copy each; m16n8k16 bf16 MMAs (fp32 accumulate) give the
+//     partial v of chunk c, stored unscaled in fp32.
 //   bgmv_expand_kernel: one CTA per (tile, 256 output columns).  Before it
 //     waits for the shrink it bulk-copies its B rows and y rows; then it sums
 //     the chunk partials of the slices it touches in chunk order, scales them
@@ -23,6 +24,7 @@
 
 #include "lora_internal.cuh"
 #include "mma_common.cuh"
+#include "tc_common.cuh"
 
 namespace {
 
@@ -30,8 +32,10 @@ using namespace bgmv;
 
 constexpr int kSThreads = 256;            // shrink: 8 warps
 constexpr int kSWarps = kSThreads / 32;
-constexpr int kStages = 4;                // shrink bulk-copy ring depth
+constexpr int kStages = 4;                // shrink ring depth bound
 constexpr int kMaxUnits = 4;              // MMA column blocks per shrink warp
+constexpr int kSC = 256;                  // hidden columns per shrink stage (tensor-map box width)
+constexpr int kBoxRows = 8;               // A rows per tensor-map box
 constexpr int kThreads = 128;             // expand: 4 warps
 constexpr int kWarps = kThreads / 32;
 constexpr int kTileRows = LORA_TILE_ROWS;
@@ -45,17 +49,17 @@ __device__ __forceinline__ int chunks_for(int n_tiles, int slots, int nc_max) {
 }
 
 struct SArgs {
+    CUtensorMap tm_a[LORA_MAX_SLICES];  // A_j as [slots * experts * R rows][in_dim], 8 x 256 boxes
     int n_slices, in_dim, E, row_div, R, R8;
-    const uint16_t *A[LORA_MAX_SLICES];
-    long long A_ss[LORA_MAX_SLICES], A_es[LORA_MAX_SLICES];
+    int a_rows_slot[LORA_MAX_SLICES], a_rows_expert[LORA_MAX_SLICES];
     const int32_t *rank;
     const int32_t *sorted, *tile_row0, *tile_keyn, *counters;
     int count_idx;
     const uint16_t *in;
     long long ld_in;
     int nc_max, slots;       // chunk bound and target CTAs (see chunks_for)
-    int SC, stride;          // stage length (elements), smem row stride (elements)
-    int nst, stage_bytes, off_red, hsplit;  // ring depth (<= kStages), ...
+    int xs_stride;           // x row stride in shared memory (elements)
+    int nst, stage_bytes, off_x, off_red, hsplit;  // ring depth, stage size, x offset in a stage
     float *part;             // [nc][n_slices][rows][R8], unscaled
     int rows;
     int *status;
@@ -87,14 +91,15 @@ struct EArgs {
 
 // ---------------------------------------------------------------- shrink
 //
-// One CTA per (16-row tile, hidden chunk c), all slices: the x rows of the
-// chunk are read once for every slice.  Shared memory holds kStages stages
-// of [16 x rows | slice 0 A rows (R8) | slice 1 A rows | ...] x SC columns.
-// MMA units (slice, 8-rank column block, hidden split) are spread over the
-// 8 warps, at most kMaxUnits each.
+// One CTA strides over items (16-row tile, hidden chunk c), all slices: the x
+// rows of a chunk are read once for every slice.  A stage of shared memory
+// holds [slice j A rows (R8 per slice) x 256 columns, dense][16 x rows x
+// 264].  MMA units (slice, 8-rank column block, hidden split) are spread over
+// the 8 warps, at most kMaxUnits each.
 
 __global__ void __launch_bounds__(kSThreads) bgmv_shrink_kernel(const __grid_constant__ SArgs p) {
-    extern __shared__ __align__(128) char smem[];
+    extern __shared__ __align__(128) char smem_raw[];
+    char *smem = (char *)(((uintptr_t)smem_raw + 127) & ~(uintptr_t)127);  // tensor-map boxes want 128 B
     __shared__ __align__(8) uint64_t full[kStages];
     __shared__ int s_rows[kTileRows];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -123,30 +128,29 @@ __global__ void __launch_bounds__(kSThreads) bgmv_shrink_kernel(const __grid_con
         const int a = key / p.E, e = key - a * p.E;
         const int r = p.rank[a];
         const int hb = min(p.in_dim, c * HC), he = min(p.in_dim, hb + HC);
-        const int n_sub = (he - hb + p.SC - 1) / p.SC;
+        const int n_sub = (he - hb + kSC - 1) / kSC;
         __syncthreads();  // the previous item is done with s_rows, the stages and red
         if (tid < n) s_rows[tid] = p.sorted[row0 + tid];
         for (int i = tid; i < p.hsplit * kTileRows * W; i += kSThreads) red[i] = 0.f;
         __syncthreads();
 
-        // sub-stage s: x rows 0..n-1, then for slice j rows 16 + j*R8 + (0..r-1)
-        const int n_copies = n + ns * r;
+        // sub-stage s: A boxes of every slice at rows j*R8 + 8q, x rows at off_x
+        const int nbox = (r + kBoxRows - 1) / kBoxRows;
         auto issue = [&](int s) {
-            const int h0 = hb + s * p.SC, len = min(p.SC, he - h0), st = (gs + s) % p.nst;
-            uint16_t *buf = (uint16_t *)(smem + st * p.stage_bytes);
+            const int h0 = hb + s * kSC, len = min(kSC, he - h0), st = (gs + s) % p.nst;
+            char *buf = smem + st * p.stage_bytes;
+            uint16_t *xs = (uint16_t *)(buf + p.off_x);
             const uint32_t rowb = (uint32_t)len * 2;
-            if (lane == 0) mbar_expect_tx(&full[st], rowb * (uint32_t)n_copies);
+            if (lane == 0)
+                mbar_expect_tx(&full[st], rowb * (uint32_t)n + (uint32_t)(ns * nbox) * (kBoxRows * kSC * 2));
             __syncwarp();
-            for (int i = lane; i < n_copies; i += 32) {
-                if (i < n) {
-                    bulk_g2s(buf + i * p.stride, p.in + (long long)(s_rows[i] / p.row_div) * p.ld_in + h0, rowb,
-                             &full[st]);
-                } else {
-                    const int q = i - n, j = q / r, k = q - j * r;
-                    const uint16_t *Ab = p.A[j] + (long long)a * p.A_ss[j] + (long long)e * p.A_es[j];
-                    bulk_g2s(buf + (kTileRows + j * p.R8 + k) * p.stride, Ab + (long long)k * p.in_dim + h0, rowb,
-                             &full[st]);
-                }
+            if (lane < n)
+                bulk_g2s(xs + lane * p.xs_stride, p.in + (long long)(s_rows[lane] / p.row_div) * p.ld_in + h0, rowb,
+                         &full[st]);
+            for (int i = lane; i < ns * nbox; i += 32) {
+                const int j = i / nbox, q = i - j * nbox;
+                const int y = a * p.a_rows_slot[j] + e * p.a_rows_expert[j] + q * kBoxRows;
+                tc::tma_load_2d(buf + (size_t)(j * p.R8 + q * kBoxRows) * (kSC * 2), &p.tm_a[j], h0, y, &full[st]);
             }
         };
         if (warp == 0) {
@@ -166,18 +170,18 @@ __global__ void __launch_bounds__(kSThreads) bgmv_shrink_kernel(const __grid_con
         for (int s = 0; s < n_sub; ++s) {
             const int st = (gs + s) % p.nst;
             mbar_wait(&full[st], (uint32_t)(((gs + s) / p.nst) & 1), p.spin_limit, p.status);
-            const int len = min(p.SC, he - hb - s * p.SC);
+            const int len = min(kSC, he - hb - s * kSC);
             const int steps = (len + 15) >> 4;
             const uint16_t *buf = (const uint16_t *)(smem + st * p.stage_bytes);
+            const uint16_t *xs = (const uint16_t *)(smem + st * p.stage_bytes + p.off_x);
 #pragma unroll
             for (int ui = 0; ui < kMaxUnits; ++ui) {
                 const int u = warp + ui * kSWarps;
                 if (u < units) {
                     const int cb = u / hsplit, hs = u - cb * hsplit;
                     const int j = cb / nnb, nb = cb - j * nnb;
-                    const uint16_t *bq = buf + (kTileRows + j * p.R8 + nb * 8 + (lane & 7)) * p.stride +
-                                         ((lane >> 3) & 1) * 8;
-                    const uint16_t *aq = buf + ((lane & 7) + ((lane >> 3) & 1) * 8) * p.stride + (lane >> 4) * 8;
+                    const uint16_t *bq = buf + (j * p.R8 + nb * 8 + (lane & 7)) * kSC + ((lane >> 3) & 1) * 8;
+                    const uint16_t *aq = xs + ((lane & 7) + ((lane >> 3) & 1) * 8) * p.xs_stride + (lane >> 4) * 8;
                     for (int i = hs; i < steps; i += hsplit) {
                         const int k0 = i * 16;
                         uint32_t a0, a1, a2, a3, b0, b1;
@@ -416,27 +420,20 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     if (!ws || ws_bytes < lora_split_ws_bytes(ns, pr.in_dim, R, pr.rows, 0) || !lora_aligned16(ws)) return LORA_OK;
     int hsplit = 1;
     while (hsplit < 4 && nb_tot * hsplit * 2 <= 2 * kSWarps) hsplit *= 2;
-    // shrink shared memory: nst stages of (16 + ns*R8) rows x SC columns, then
-    // the partial sums; about 72 KB so that three CTAs share an SM (else 110 KB
-    // for two), with the deepest ring whose stages still move >= 128 columns
-    // (256-byte copies)
-    const int rows_s = kTileRows + ns * R8;
+    // shrink shared memory: nst stages of [ns*R8 A rows x 256][16 x rows x 264],
+    // then the partial sums: about 72 KB so that three CTAs share an SM (else
+    // 110 KB for two), with the deepest ring (2..4 stages) that fits
+    const size_t a_part = a128((size_t)ns * R8 * kSC * 2), x_part = a128((size_t)kTileRows * (kSC + 8) * 2);
+    const size_t stage_bytes = a_part + x_part;
     const size_t red_bytes = (size_t)hsplit * kTileRows * ns * R8 * 4;
-    auto smem_for = [&](int nst, int sc) { return nst * a128((size_t)rows_s * (sc + 8) * 2) + red_bytes; };
-    int SC = 0, nst = 0;
+    int nst = 0;
     for (size_t budget : {(size_t)72 * 1024, (size_t)110 * 1024, (size_t)200 * 1024}) {
-        for (int d = kStages; d >= 2 && !nst; --d) {
-            int sc = 512;
-            while (sc > 128 && smem_for(d, sc) > budget) sc -= 16;
-            if (smem_for(d, sc) <= budget) {
-                SC = sc;
-                nst = d;
-            }
-        }
+        for (int d = kStages; d >= 2 && !nst; --d)
+            if (d * stage_bytes + red_bytes + 128 <= budget) nst = d;
         if (nst) break;
     }
     if (!nst) return LORA_OK;
-    const size_t s_smem = smem_for(nst, SC);
+    const size_t s_smem = nst * stage_bytes + red_bytes + 128;
     // expand shared memory: B rows, y rows, v hi/lo
     const int vr_stride = ns * R8 + 8;
     const size_t e_b = a128((size_t)kOC * R8 * 2 + 32), e_y = a128((size_t)kTileRows * (kOC + 8) * 2);
@@ -460,17 +457,20 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
 
     SArgs sa;
     memset(&sa, 0, sizeof(sa));
+    for (int j = 0; j < ns; ++j) {
+        if (pr.A_ss[j] % pr.in_dim || pr.A_es[j] % pr.in_dim) return LORA_OK;
+        sa.a_rows_slot[j] = (int)(pr.A_ss[j] / pr.in_dim);
+        sa.a_rows_expert[j] = (int)(pr.A_es[j] / pr.in_dim);
+        const long long a_rows = (long long)pool->desc.max_loras * sa.a_rows_slot[j];
+        if (!lora_make_tmap_2d(&sa.tm_a[j], pr.A[j], pr.in_dim, a_rows, pr.in_dim, kSC, kBoxRows, false))
+            return LORA_OK;
+    }
     sa.n_slices = ns;
     sa.in_dim = pr.in_dim;
     sa.E = pr.E;
     sa.row_div = pr.row_div;
     sa.R = R;
     sa.R8 = R8;
-    for (int j = 0; j < ns; ++j) {
-        sa.A[j] = pr.A[j];
-        sa.A_ss[j] = pr.A_ss[j];
-        sa.A_es[j] = pr.A_es[j];
-    }
     sa.rank = pr.rank;
     sa.sorted = pr.meta->sorted;
     sa.tile_row0 = pr.tile_row0;
@@ -481,9 +481,9 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     sa.ld_in = pr.ld_in;
     sa.nc_max = nc_max;
     sa.slots = pool->num_sms * occ;
-    sa.SC = SC;
-    sa.stride = SC + 8;
-    sa.stage_bytes = (int)a128((size_t)rows_s * (SC + 8) * 2);
+    sa.xs_stride = kSC + 8;
+    sa.stage_bytes = (int)stage_bytes;
+    sa.off_x = (int)a_part;
     sa.nst = nst;
     sa.off_red = nst * sa.stage_bytes;
     sa.hsplit = hsplit;

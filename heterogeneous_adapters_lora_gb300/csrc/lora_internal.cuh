@@ -1,6 +1,7 @@
 // Internal definitions shared by the CUDA translation units of liblora_gb300.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -119,6 +120,11 @@ void lora_note_launch();
 // the shapes fit, 1 = persistent split-K kernel only, 2 = cluster kernel
 // preferred).
 extern int g_lora_kernel_policy;
+
+// 2D bf16 tensor map over rows x cols (row stride in elements), optional
+// 128-byte swizzle (sgmv.cu).
+bool lora_make_tmap_2d(CUtensorMap *m, const void *base, long long cols, long long rows, long long stride,
+                       int box_cols, int box_rows, bool swizzle128);
 
 // Split shrink/expand kernels (bgmv.cu): workspace bytes and launcher.
 size_t lora_split_ws_bytes(int n_slices, int in_dim, int R, int rows, int max_tiles);

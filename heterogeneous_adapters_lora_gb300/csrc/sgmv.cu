@@ -390,6 +390,19 @@ int g_sgmv_configured[64];
 
 }  // namespace
 
+bool lora_make_tmap_2d(CUtensorMap *m, const void *base, long long cols, long long rows, long long stride,
+                       int box_cols, int box_rows, bool swizzle128) {
+    PFN_cuTensorMapEncodeTiled_v12000 f = encode_fn();
+    if (!f) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)stride * 2};
+    cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool lora_sgmv_eligible(const lora_pool_t *pool) {
     const lora_pool_desc_t &d = pool->desc;
     if (pool->is_moe || d.max_rank != 64 || pool->R8 != 64) return false;

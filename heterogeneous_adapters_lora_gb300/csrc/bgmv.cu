@@ -7,13 +7,12 @@
 // [n_slices][T][rank] (scale 1.0) and add_expand with add_input=True at the
 // slice offsets; add_lora_fused_moe does the same per (adapter, expert).
 //
-//   bgmv_shrink_kernel: items (16-row tile, hidden chunk c), all slices at
-//     once.  Per 256-column stage, the slot's A rows of every slice arrive as
-//     8 x 256 tensor-map boxes (one TMA per 8 ranks) and the tile's x rows as
-//     one bulk copy each; m16n8k16 bf16 MMAs (fp32 accumulate) give the
-//     partial v of chunk c, stored unscaled in fp32.
-//   bgmv_expand_kernel: one CTA per (tile, 256 output columns).  Before it
-//     waits for the shrink it bulk-copies its B rows and y rows; then it sums
+//   bgmv_shrink_kernel: items (16-row tile, slice j, hidden chunk c).  Bulk
+//     copies (cp.async.bulk + mbarrier) bring the tile's x rows and the
+//     slot's A_j rows of chunk c; m16n8k16 bf16 MMAs (fp32 accumulate) give
+//     the partial v of chunk c, stored unscaled in fp32.
+//   bgmv_expand_kernel: items (tile, 256 output columns).  Before it waits
+//     for the shrink it bulk-copies its first item's B rows and y rows; it sums
 //     the chunk partials of the slices it touches in chunk order, scales them
 //     by scale[a] (and the routed weight for MoE w2), splits v into bf16 hi +
 //     lo (the expand keeps the fp32 intermediate to ~16 bits), runs the MMAs,
@@ -24,50 +23,38 @@
 
 #include "lora_internal.cuh"
 #include "mma_common.cuh"
-#include "tc_common.cuh"
 
 namespace {
 
 using namespace bgmv;
 
-constexpr int kSThreads = 256;            // shrink: 8 warps
+constexpr int kSThreads = 128;            // shrink: 4 warps
 constexpr int kSWarps = kSThreads / 32;
-constexpr int kStages = 4;                // shrink ring depth bound
-constexpr int kMaxUnits = 4;              // MMA column blocks per shrink warp
-constexpr int kSC = 256;                  // hidden columns per shrink stage (tensor-map box width)
-constexpr int kBoxRows = 8;               // A rows per tensor-map box
 constexpr int kThreads = 128;             // expand: 4 warps
 constexpr int kWarps = kThreads / 32;
 constexpr int kTileRows = LORA_TILE_ROWS;
 constexpr int kOC = 256;                  // output columns per expand CTA
 
-// Hidden chunks per tile, decided on the device from the real tile count so
-// that the shrink fills about one wave of CTAs: the expand recomputes it.
-__device__ __forceinline__ int chunks_for(int n_tiles, int slots, int nc_max) {
-    const int q = slots / (n_tiles > 0 ? n_tiles : 1);
-    return q < 1 ? 1 : (q > nc_max ? nc_max : q);
-}
-
 struct SArgs {
-    CUtensorMap tm_a[LORA_MAX_SLICES];  // A_j as [slots * experts * R rows][in_dim], 8 x 256 boxes
     int n_slices, in_dim, E, row_div, R, R8;
-    int a_rows_slot[LORA_MAX_SLICES], a_rows_expert[LORA_MAX_SLICES];
+    const uint16_t *A[LORA_MAX_SLICES];
+    long long A_ss[LORA_MAX_SLICES], A_es[LORA_MAX_SLICES];
     const int32_t *rank;
     const int32_t *sorted, *tile_row0, *tile_keyn, *counters;
     int count_idx;
     const uint16_t *in;
     long long ld_in;
-    int nc_max, slots;       // chunk bound and target CTAs (see chunks_for)
-    int xs_stride;           // x row stride in shared memory (elements)
-    int nst, stage_bytes, off_x, off_red, hsplit;  // ring depth, stage size, x offset in a stage
-    float *part;             // [nc][n_slices][rows][R8], unscaled
+    int NC, HC, SC;          // hidden chunks, chunk length, stage length (elements)
+    int xs_stride, as_stride;
+    int off_x, off_a, x_stage_bytes, a_stage_bytes, off_red;
+    float *part;             // [NC][n_slices][rows][R8], unscaled
     int rows;
     int *status;
     int spin_limit;
 };
 
 struct EArgs {
-    int n_slices, R, R8, E, out_total, nc_max, slots;
+    int n_slices, R, R8, E, out_total, NC;
     int out_w[LORA_MAX_SLICES], out_off[LORA_MAX_SLICES];
     const uint16_t *B[LORA_MAX_SLICES];
     long long B_ss[LORA_MAX_SLICES];
@@ -91,142 +78,134 @@ struct EArgs {
 
 // ---------------------------------------------------------------- shrink
 //
-// One CTA strides over items (16-row tile, hidden chunk c), all slices: the x
-// rows of a chunk are read once for every slice.  A stage of shared memory
-// holds [slice j A rows (R8 per slice) x 256 columns, dense][16 x rows x
-// 264].  MMA units (slice, 8-rank column block, hidden split) are spread over
-// the 8 warps, at most kMaxUnits each.
+// Items (16-row tile, slice j, hidden chunk c), strided over a grid of at
+// most a few waves.  Two stages of [16 x rows][r A rows] x SC columns, rows
+// padded by 16 bytes so ldmatrix reads are free of bank conflicts; units
+// (8-rank column block, hidden split) spread over the 4 warps, <= 2 each.
 
 __global__ void __launch_bounds__(kSThreads) bgmv_shrink_kernel(const __grid_constant__ SArgs p) {
-    extern __shared__ __align__(128) char smem_raw[];
-    char *smem = (char *)(((uintptr_t)smem_raw + 127) & ~(uintptr_t)127);  // tensor-map boxes want 128 B
-    __shared__ __align__(8) uint64_t full[kStages];
+    extern __shared__ __align__(128) char smem[];
+    __shared__ __align__(8) uint64_t full[2];
     __shared__ int s_rows[kTileRows];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, c4 = lane & 3;
-    const int ns = p.n_slices, W = ns * p.R8;
+    const int per_tile = p.n_slices * p.NC;
 
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int n_tiles = p.counters[p.count_idx];
-    const int nc = chunks_for(n_tiles, p.slots, p.nc_max);
-    const int total = n_tiles * nc;
+    const int total = n_tiles * per_tile;
     if ((int)blockIdx.x >= total) return;
     // the expand may launch and prefetch its weights and outputs now
     asm volatile("griddepcontrol.launch_dependents;");
-    if (tid < p.nst) mbar_init(&full[tid], 1);
+    if (tid < 2) mbar_init(&full[tid], 1);
     if (tid == 0) asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    const int HC = ((p.in_dim + nc - 1) / nc + 15) & ~15;
-    const long long cstride = (long long)p.rows * p.R8;
     float *red = (float *)(smem + p.off_red);
     int gs = 0;  // sub-stages consumed by this CTA so far (ring slot and phase)
 
     for (int item = blockIdx.x; item < total; item += gridDim.x) {
-        const int tile = item / nc, c = item - tile * nc;
+        const int tile = item / per_tile, rem = item - tile * per_tile;
+        const int j = rem / p.NC, c = rem - j * p.NC;
         const int row0 = p.tile_row0[tile];
         const int keyn = p.tile_keyn[tile];
         const int n = keyn & 31, key = keyn >> 5;
         const int a = key / p.E, e = key - a * p.E;
         const int r = p.rank[a];
-        const int hb = min(p.in_dim, c * HC), he = min(p.in_dim, hb + HC);
-        const int n_sub = (he - hb + kSC - 1) / kSC;
+        const uint16_t *Ab = p.A[j] + (long long)a * p.A_ss[j] + (long long)e * p.A_es[j];
+        const int hb = c * p.HC, he = min(p.in_dim, hb + p.HC);
+        const int n_sub = (he - hb + p.SC - 1) / p.SC;
         __syncthreads();  // the previous item is done with s_rows, the stages and red
         if (tid < n) s_rows[tid] = p.sorted[row0 + tid];
-        for (int i = tid; i < p.hsplit * kTileRows * W; i += kSThreads) red[i] = 0.f;
         __syncthreads();
 
-        // sub-stage s: A boxes of every slice at rows j*R8 + 8q, x rows at off_x
-        const int nbox = (r + kBoxRows - 1) / kBoxRows;
         auto issue = [&](int s) {
-            const int h0 = hb + s * kSC, len = min(kSC, he - h0), st = (gs + s) % p.nst;
-            char *buf = smem + st * p.stage_bytes;
-            uint16_t *xs = (uint16_t *)(buf + p.off_x);
+            const int h0 = hb + s * p.SC, len = min(p.SC, he - h0), st = (gs + s) & 1;
+            uint16_t *xs = (uint16_t *)(smem + p.off_x + st * p.x_stage_bytes);
+            uint16_t *as = (uint16_t *)(smem + p.off_a + st * p.a_stage_bytes);
             const uint32_t rowb = (uint32_t)len * 2;
-            if (lane == 0)
-                mbar_expect_tx(&full[st], rowb * (uint32_t)n + (uint32_t)(ns * nbox) * (kBoxRows * kSC * 2));
+            if (lane == 0) mbar_expect_tx(&full[st], rowb * (uint32_t)(n + r));
             __syncwarp();
-            if (lane < n)
-                bulk_g2s(xs + lane * p.xs_stride, p.in + (long long)(s_rows[lane] / p.row_div) * p.ld_in + h0, rowb,
-                         &full[st]);
-            for (int i = lane; i < ns * nbox; i += 32) {
-                const int j = i / nbox, q = i - j * nbox;
-                const int y = a * p.a_rows_slot[j] + e * p.a_rows_expert[j] + q * kBoxRows;
-                tc::tma_load_2d(buf + (size_t)(j * p.R8 + q * kBoxRows) * (kSC * 2), &p.tm_a[j], h0, y, &full[st]);
+            for (int i = lane; i < n + r; i += 32) {
+                if (i < n)
+                    bulk_g2s(xs + i * p.xs_stride, p.in + (long long)(s_rows[i] / p.row_div) * p.ld_in + h0, rowb,
+                             &full[st]);
+                else
+                    bulk_g2s(as + (i - n) * p.as_stride, Ab + (long long)(i - n) * p.in_dim + h0, rowb, &full[st]);
             }
         };
         if (warp == 0) {
             // the stages were last read through the generic proxy
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            for (int s = 0; s < min(n_sub, p.nst); ++s) issue(s);
+            for (int s = 0; s < min(n_sub, 2); ++s) issue(s);
         }
 
-        const int nnb = (r + 7) >> 3;  // 8-rank column blocks of this slot
-        const int hsplit = p.hsplit;
-        const int units = ns * nnb * hsplit;
-        float acc[kMaxUnits][4];
+        const int nnb = (r + 7) >> 3;
+        int hsplit = 1;
+        while (nnb * hsplit * 2 <= 2 * kSWarps && hsplit < 4) hsplit *= 2;
+        const int units = nnb * hsplit;
+        float acc[2][4];
 #pragma unroll
-        for (int u = 0; u < kMaxUnits; ++u)
+        for (int u = 0; u < 2; ++u)
 #pragma unroll
             for (int i = 0; i < 4; ++i) acc[u][i] = 0.f;
         for (int s = 0; s < n_sub; ++s) {
-            const int st = (gs + s) % p.nst;
-            mbar_wait(&full[st], (uint32_t)(((gs + s) / p.nst) & 1), p.spin_limit, p.status);
-            const int len = min(kSC, he - hb - s * kSC);
+            const int st = (gs + s) & 1;
+            mbar_wait(&full[st], (uint32_t)(((gs + s) >> 1) & 1), p.spin_limit, p.status);
+            const int len = min(p.SC, he - hb - s * p.SC);
             const int steps = (len + 15) >> 4;
-            const uint16_t *buf = (const uint16_t *)(smem + st * p.stage_bytes);
-            const uint16_t *xs = (const uint16_t *)(smem + st * p.stage_bytes + p.off_x);
+            const uint16_t *xs = (const uint16_t *)(smem + p.off_x + st * p.x_stage_bytes);
+            const uint16_t *as = (const uint16_t *)(smem + p.off_a + st * p.a_stage_bytes);
 #pragma unroll
-            for (int ui = 0; ui < kMaxUnits; ++ui) {
+            for (int ui = 0; ui < 2; ++ui) {
                 const int u = warp + ui * kSWarps;
                 if (u < units) {
-                    const int cb = u / hsplit, hs = u - cb * hsplit;
-                    const int j = cb / nnb, nb = cb - j * nnb;
-                    const uint16_t *bq = buf + (j * p.R8 + nb * 8 + (lane & 7)) * kSC + ((lane >> 3) & 1) * 8;
-                    const uint16_t *aq = xs + ((lane & 7) + ((lane >> 3) & 1) * 8) * p.xs_stride + (lane >> 4) * 8;
+                    const int nb = u / hsplit, hs = u - nb * hsplit;
                     for (int i = hs; i < steps; i += hsplit) {
                         const int k0 = i * 16;
                         uint32_t a0, a1, a2, a3, b0, b1;
-                        ldsm_x4(aq + k0, a0, a1, a2, a3);
-                        ldsm_x2(bq + k0, b0, b1);
+                        ldsm_x4(xs + ((lane & 7) + ((lane >> 3) & 1) * 8) * p.xs_stride + k0 + (lane >> 4) * 8,
+                                a0, a1, a2, a3);
+                        ldsm_x2(as + (nb * 8 + (lane & 7)) * p.as_stride + k0 + ((lane >> 3) & 1) * 8, b0, b1);
                         if (k0 + 8 >= len) a2 = a3 = b1 = 0u;
                         mma16816(acc[ui], a0, a1, a2, a3, b0, b1);
                     }
                 }
             }
             __syncthreads();
-            if (warp == 0 && s + p.nst < n_sub) {
+            if (warp == 0 && s + 2 < n_sub) {
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                issue(s + p.nst);
+                issue(s + 2);
             }
         }
         gs += n_sub;
 
-        // partial sums [hsplit][16][ns*R8] in shared memory, reduced over the
-        // hidden split, then stored as this chunk's part[c][j][row0 + t][k]
+        // partials of this chunk: [hsplit][16][R8] in shared memory, summed over
+        // the hidden split, then one row of R8 floats per token to global memory
+        for (int i = tid; i < hsplit * kTileRows * p.R8; i += kSThreads) red[i] = 0.f;
+        __syncthreads();
 #pragma unroll
-        for (int ui = 0; ui < kMaxUnits; ++ui) {
+        for (int ui = 0; ui < 2; ++ui) {
             const int u = warp + ui * kSWarps;
             if (u < units) {
-                const int cb = u / hsplit, hs = u - cb * hsplit;
-                const int j = cb / nnb, nb = cb - j * nnb;
+                const int nb = u / hsplit, hs = u - nb * hsplit;
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const int k = nb * 8 + 2 * c4 + h;
                     if (k < r) {
-                        float *dst = red + (hs * kTileRows) * W + j * p.R8 + k;
-                        if (g < n) dst[g * W] = acc[ui][h];
-                        if (g + 8 < n) dst[(g + 8) * W] = acc[ui][2 + h];
+                        float *dst = red + (hs * kTileRows) * p.R8 + k;
+                        if (g < n) dst[g * p.R8] = acc[ui][h];
+                        if (g + 8 < n) dst[(g + 8) * p.R8] = acc[ui][2 + h];
                     }
                 }
             }
         }
         __syncthreads();
-        float *base = p.part + (long long)c * ns * cstride + (long long)row0 * p.R8;
-        for (int i = tid; i < n * W; i += kSThreads) {
-            const int t = i / W, q = i - t * W;
-            const int j = q / p.R8, k = q - j * p.R8;
+        // this chunk's partial: part[c][j][row0 + t][k]
+        float *dst = p.part + ((long long)c * p.n_slices + j) * p.rows * p.R8 + (long long)row0 * p.R8;
+        for (int i = tid; i < n * p.R8; i += kSThreads) {
+            const int t = i / p.R8, k = i - t * p.R8;
             float sum = 0.f;
-            for (int hs = 0; hs < hsplit; ++hs) sum += red[(hs * kTileRows + t) * W + q];
-            base[j * cstride + t * p.R8 + k] = sum;
+            for (int hs = 0; hs < hsplit; ++hs) sum += red[(hs * kTileRows + t) * p.R8 + k];
+            dst[i] = sum;
         }
     }
 }
@@ -258,7 +237,8 @@ __global__ void __launch_bounds__(kThreads) bgmv_expand_kernel(const __grid_cons
     uint16_t *vh = (uint16_t *)(smem + p.off_vh);
     uint16_t *vl = (uint16_t *)(smem + p.off_vl);
     const int arow = (lane & 7) + ((lane >> 3) & 1) * 8;
-    int nc = 0;
+    bool waited = false;
+    const int nc = p.NC;
     uint32_t phase = 0;
 
     for (int item = blockIdx.x; item < total; item += gridDim.x, phase ^= 1u) {
@@ -298,9 +278,9 @@ __global__ void __launch_bounds__(kThreads) bgmv_expand_kernel(const __grid_cons
         }
         if (tid < kTileRows)
             s_w[tid] = tid < n ? p.scale[a] * p.post_scale * (p.row_w ? p.row_w[s_rows[tid]] : 1.f) : 0.f;
-        if (nc == 0) {
+        if (!waited) {
             asm volatile("griddepcontrol.wait;" ::: "memory");  // the shrink's partials are complete
-            nc = chunks_for(n_tiles, p.slots, p.nc_max);
+            waited = true;
         }
         __syncthreads();
         // v of the slices this item touches (chunk partials summed in order,
@@ -394,16 +374,25 @@ size_t a128(size_t x) { return (x + 127) & ~(size_t)127; }
 
 int g_split_configured[64];
 
-}  // namespace
-
-int nc_max_for(int in_dim) {
-    const int q = in_dim / 256;
-    return q < 1 ? 1 : (q > 8 ? 8 : q);
+// Hidden chunks of a shrink item: ~32 KB of A rows at full rank, >= 256
+// columns, at most 8.
+void chunking(int in_dim, int R8, int *NC, int *HC) {
+    int hc = (16384 / R8 + 63) / 64 * 64;
+    if (hc < 256) hc = 256;
+    int nc = lora_ceil_div(in_dim, hc);
+    if (nc > 8) nc = 8;
+    hc = ((lora_ceil_div(in_dim, nc) + 15) / 16) * 16;
+    *NC = lora_ceil_div(in_dim, hc);
+    *HC = hc;
 }
+
+}  // namespace
 
 size_t lora_split_ws_bytes(int n_slices, int in_dim, int R, int rows, int max_tiles) {
     (void)max_tiles;
-    return a128((size_t)nc_max_for(in_dim) * n_slices * rows * lora_round8(R) * 4);
+    int NC, HC;
+    chunking(in_dim, lora_round8(R), &NC, &HC);
+    return a128((size_t)NC * n_slices * rows * lora_round8(R) * 4);
 }
 
 lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, void *ws, size_t ws_bytes,
@@ -413,27 +402,21 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     int out_total = 0;
     for (int j = 0; j < ns; ++j) out_total = max(out_total, pr.out_off[j] + pr.out_w[j]);
     const long long max_tiles = pr.rows / kTileRows + (pr.rows < pr.n_keys ? pr.rows : pr.n_keys);
-    // MMA column blocks of all slices must fit kMaxUnits per shrink warp
-    const int nb_tot = ns * (R8 / 8);
-    if (nb_tot > kSWarps * kMaxUnits || max_tiles <= 0) return LORA_OK;
-    const int nc_max = nc_max_for(pr.in_dim);
+    // the shrink holds at most two 8-rank MMA column blocks per warp
+    if (R8 > 2 * kSWarps * 8 || max_tiles <= 0) return LORA_OK;
+    int NC, HC;
+    chunking(pr.in_dim, R8, &NC, &HC);
     if (!ws || ws_bytes < lora_split_ws_bytes(ns, pr.in_dim, R, pr.rows, 0) || !lora_aligned16(ws)) return LORA_OK;
-    int hsplit = 1;
-    while (hsplit < 4 && nb_tot * hsplit * 2 <= 2 * kSWarps) hsplit *= 2;
-    // shrink shared memory: nst stages of [ns*R8 A rows x 256][16 x rows x 264],
-    // then the partial sums: about 72 KB so that three CTAs share an SM (else
-    // 110 KB for two), with the deepest ring (2..4 stages) that fits
-    const size_t a_part = a128((size_t)ns * R8 * kSC * 2), x_part = a128((size_t)kTileRows * (kSC + 8) * 2);
-    const size_t stage_bytes = a_part + x_part;
-    const size_t red_bytes = (size_t)hsplit * kTileRows * ns * R8 * 4;
-    int nst = 0;
-    for (size_t budget : {(size_t)72 * 1024, (size_t)110 * 1024, (size_t)200 * 1024}) {
-        for (int d = kStages; d >= 2 && !nst; --d)
-            if (d * stage_bytes + red_bytes + 128 <= budget) nst = d;
-        if (nst) break;
-    }
-    if (!nst) return LORA_OK;
-    const size_t s_smem = nst * stage_bytes + red_bytes + 128;
+    // shrink shared memory: 2 stages of (16 + R8) rows x SC columns (rows
+    // padded by 16 bytes), then the partial sums
+    int SC = HC;
+    const int red_bytes = 4 * kTileRows * R8 * 4;
+    auto stage_total = [&](int sc) {
+        return 2 * (a128((size_t)kTileRows * (sc + 8) * 2) + a128((size_t)R8 * (sc + 8) * 2));
+    };
+    while (SC > 256 && stage_total(SC) + red_bytes > 100 * 1024) SC = ((SC / 2) + 15) / 16 * 16;
+    const size_t s_smem = stage_total(SC) + red_bytes;
+    if (s_smem > 200 * 1024) return LORA_OK;
     // expand shared memory: B rows, y rows, v hi/lo
     const int vr_stride = ns * R8 + 8;
     const size_t e_b = a128((size_t)kOC * R8 * 2 + 32), e_y = a128((size_t)kTileRows * (kOC + 8) * 2);
@@ -450,27 +433,24 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     }
     int occ = 0;
     LORA_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, bgmv_shrink_kernel, kSThreads, s_smem));
-    if (occ < 1) occ = 1;
+    const long long s_slots = (long long)pool->num_sms * (occ < 1 ? 1 : occ);
     int occ_e = 0;
     LORA_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_e, bgmv_expand_kernel, kThreads, e_smem));
     const long long e_slots = (long long)pool->num_sms * (occ_e < 1 ? 1 : occ_e);
 
     SArgs sa;
     memset(&sa, 0, sizeof(sa));
-    for (int j = 0; j < ns; ++j) {
-        if (pr.A_ss[j] % pr.in_dim || pr.A_es[j] % pr.in_dim) return LORA_OK;
-        sa.a_rows_slot[j] = (int)(pr.A_ss[j] / pr.in_dim);
-        sa.a_rows_expert[j] = (int)(pr.A_es[j] / pr.in_dim);
-        const long long a_rows = (long long)pool->desc.max_loras * sa.a_rows_slot[j];
-        if (!lora_make_tmap_2d(&sa.tm_a[j], pr.A[j], pr.in_dim, a_rows, pr.in_dim, kSC, kBoxRows, false))
-            return LORA_OK;
-    }
     sa.n_slices = ns;
     sa.in_dim = pr.in_dim;
     sa.E = pr.E;
     sa.row_div = pr.row_div;
     sa.R = R;
     sa.R8 = R8;
+    for (int j = 0; j < ns; ++j) {
+        sa.A[j] = pr.A[j];
+        sa.A_ss[j] = pr.A_ss[j];
+        sa.A_es[j] = pr.A_es[j];
+    }
     sa.rank = pr.rank;
     sa.sorted = pr.meta->sorted;
     sa.tile_row0 = pr.tile_row0;
@@ -479,14 +459,16 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     sa.count_idx = pr.count_idx;
     sa.in = pr.in;
     sa.ld_in = pr.ld_in;
-    sa.nc_max = nc_max;
-    sa.slots = pool->num_sms * occ;
-    sa.xs_stride = kSC + 8;
-    sa.stage_bytes = (int)stage_bytes;
-    sa.off_x = (int)a_part;
-    sa.nst = nst;
-    sa.off_red = nst * sa.stage_bytes;
-    sa.hsplit = hsplit;
+    sa.NC = NC;
+    sa.HC = HC;
+    sa.SC = SC;
+    sa.xs_stride = SC + 8;
+    sa.as_stride = SC + 8;
+    sa.x_stage_bytes = (int)a128((size_t)kTileRows * (SC + 8) * 2);
+    sa.a_stage_bytes = (int)a128((size_t)R8 * (SC + 8) * 2);
+    sa.off_x = 0;
+    sa.off_a = 2 * sa.x_stage_bytes;
+    sa.off_red = sa.off_a + 2 * sa.a_stage_bytes;
     sa.part = (float *)ws;
     sa.rows = pr.rows;
     sa.status = pr.status;
@@ -510,8 +492,7 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     ea.scale = pr.scale;
     ea.row_w = pr.row_w;
     ea.post_scale = pr.post_scale;
-    ea.nc_max = nc_max;
-    ea.slots = sa.slots;
+    ea.NC = NC;
     ea.sorted = pr.meta->sorted;
     ea.tile_row0 = pr.tile_row0;
     ea.tile_keyn = pr.tile_keyn;
@@ -541,8 +522,9 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     cfg.blockDim = dim3(kSThreads, 1, 1);
     cfg.stream = s;
     // grids of at most one wave; the kernels stride over their items
-    const long long s_items = max_tiles * nc_max, e_items = max_tiles * ea.n_oc;
-    cfg.gridDim = dim3((unsigned)(s_items < sa.slots ? s_items : sa.slots), 1, 1);
+    // grids of at most four waves (one for the expand); the kernels stride over their items
+    const long long s_items = max_tiles * ns * NC, e_items = max_tiles * ea.n_oc;
+    cfg.gridDim = dim3((unsigned)(s_items < 4 * s_slots ? s_items : 4 * s_slots), 1, 1);
     cfg.dynamicSmemBytes = s_smem;
     LORA_CUDA_TRY(cudaLaunchKernelEx(&cfg, bgmv_shrink_kernel, sa));
     lora_note_launch();

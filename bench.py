@@ -345,18 +345,30 @@ def run_gpu(args, rank, world, local_rank):
                 step(r)
             launches_per_step = L.lora_kernel_launch_count() - n0
             graphs.append(g)
+        # a serving loop captures many layers per graph: time graphs of spg
+        # steps (rotating copies) so that graph launch gaps are amortised
+        spg = n_rot * max(1, -(-max(1, args.steps_per_graph) // n_rot))
+        gm = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gm, stream=stream):
+            for i in range(spg):
+                step(runs[i % n_rot])
+
+        def run_steps(k_steps):
+            for _ in range(k_steps // spg):
+                gm.replay()
+            for k in range(k_steps % spg):
+                graphs[k % n_rot].replay()
+
         for i in range(args.warmup):
             graphs[i % n_rot].replay()
+        gm.replay()
         stream.synchronize()
 
         # clocks: ~1 s of the same work right before the timed region, and during it
         with ClockSampler(local_rank) as cs:
             t_end = time.perf_counter() + args.clock_seconds
-            i = 0
             while time.perf_counter() < t_end:
-                for _ in range(200):
-                    graphs[i % n_rot].replay()
-                    i += 1
+                run_steps(200)
                 stream.synchronize()
             if world > 1:
                 dist.barrier()
@@ -364,8 +376,7 @@ def run_gpu(args, rank, world, local_rank):
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            for k in range(args.steps):
-                graphs[k % n_rot].replay()
+            run_steps(args.steps)
             e1.record(stream)
             torch.cuda.synchronize(dev)
             if world > 1:
@@ -399,6 +410,20 @@ def run_gpu(args, rank, world, local_rank):
         a1.record(stream)
         stream.synchronize()
         kms = a0.elapsed_time(a1) / (reps * KA)
+
+        # the metadata build alone, the same way
+        gmeta = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gmeta, stream=stream):
+            for k in range(KA):
+                runs[k % n_rot].build_meta()
+        gmeta.replay()
+        stream.synchronize()
+        a0.record(stream)
+        for _ in range(reps):
+            gmeta.replay()
+        a1.record(stream)
+        stream.synchronize()
+        meta_ms = a0.elapsed_time(a1) / (reps * KA)
 
         # end to end through the public API with host buffers: H2D of the
         # step's inputs from pinned memory, the calls, D2H of the result
@@ -446,7 +471,7 @@ def run_gpu(args, rank, world, local_rank):
         stream.synchronize()
         e2e_ms = f0.elapsed_time(f1)
 
-    ms, e2e_ms, kms = max_over_ranks([ms, e2e_ms, kms], world, dev)
+    ms, e2e_ms, kms, meta_ms = max_over_ranks([ms, e2e_ms, kms, meta_ms], world, dev)
     for r in runs:
         r.close()
     if rank != 0:
@@ -469,8 +494,10 @@ def run_gpu(args, rank, world, local_rank):
                    "hbm_gbs_per_step": ab["total"] / (ms / args.steps * 1e-3) / 1e9,
                    "l2": f"inputs rotate over {n_rot} resident copies "
                          f"({n_rot * foot / 1e6:.0f} MB of algorithmic bytes, L2 {l2 / 1e6:.0f} MB)",
-                   "timing": "CUDA graph per step (metadata + apply), K replays between CUDA events",
-                   "parallelism": f"replicas{world}"},
+                   "timing": f"CUDA graphs of {spg} steps (metadata + apply each, rotating copies) "
+                             f"replayed to K steps between CUDA events",
+                   "parallelism": f"replicas{world}",
+                   "metadata_us_alone": meta_ms * 1e3, "apply_us_alone": kms * 1e3},
         "roofline": {"bound": "hbm", "kernel": apply_kernels(name, args.kernel_policy),
                      "achieved": achieved, "peak": peak,
                      "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s", "frac": achieved / peak,
@@ -498,6 +525,7 @@ def main():
     ap.add_argument("--clock-seconds", type=float, default=1.0)
     ap.add_argument("--cpu-seconds", type=float, default=2.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--steps-per-graph", type=int, default=16)
     ap.add_argument("--kernel-policy", type=int, default=0, choices=[0, 1, 2],
                     help="0 automatic, 1 persistent split-K kernel, 2 cluster kernel first (tuning)")
     args = ap.parse_args()

@@ -407,22 +407,6 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     int NC, HC;
     chunking(pr.in_dim, R8, &NC, &HC);
     if (!ws || ws_bytes < lora_split_ws_bytes(ns, pr.in_dim, R, pr.rows, 0) || !lora_aligned16(ws)) return LORA_OK;
-    // shrink shared memory: 2 stages of (16 + R8) rows x SC columns (rows
-    // padded by 16 bytes), then the partial sums
-    int SC = HC;
-    const int red_bytes = 4 * kTileRows * R8 * 4;
-    auto stage_total = [&](int sc) {
-        return 2 * (a128((size_t)kTileRows * (sc + 8) * 2) + a128((size_t)R8 * (sc + 8) * 2));
-    };
-    while (SC > 256 && stage_total(SC) + red_bytes > 100 * 1024) SC = ((SC / 2) + 15) / 16 * 16;
-    const size_t s_smem = stage_total(SC) + red_bytes;
-    if (s_smem > 200 * 1024) return LORA_OK;
-    // expand shared memory: B rows, y rows, v hi/lo
-    const int vr_stride = ns * R8 + 8;
-    const size_t e_b = a128((size_t)kOC * R8 * 2 + 32), e_y = a128((size_t)kTileRows * (kOC + 8) * 2);
-    const size_t e_v = a128((size_t)kTileRows * vr_stride * 2);
-    const size_t e_smem = e_b + e_y + 2 * e_v;
-
     const int dev = pool->device < 64 ? pool->device : 63;
     if (!g_split_configured[dev]) {
         LORA_CUDA_TRY(cudaFuncSetAttribute(bgmv_shrink_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -431,8 +415,43 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
                                            200 * 1024));
         g_split_configured[dev] = 1;
     }
-    int occ = 0;
-    LORA_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, bgmv_shrink_kernel, kSThreads, s_smem));
+    // shrink shared memory: 2 stages of (16 + R8) rows x SC columns (rows
+    // padded by 16 bytes), then the partial sums.  SC: the widest stage (up
+    // to the chunk, <= 100 KB) whose occupancy still runs every item in one
+    // wave, else the widest that fits
+    const int red_bytes = 4 * kTileRows * R8 * 4;
+    auto smem_for = [&](int sc) {
+        return 2 * (a128((size_t)kTileRows * (sc + 8) * 2) + a128((size_t)R8 * (sc + 8) * 2)) + red_bytes;
+    };
+    const long long s_items = max_tiles * ns * NC;
+    int SC = 0, occ = 0, first = 0, first_occ = 0;
+    for (int sc = (HC < 1024 ? HC : 1024); sc >= 64; sc -= 64) {
+        if (smem_for(sc) > 100 * 1024) continue;
+        int o = 0;
+        LORA_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, bgmv_shrink_kernel, kSThreads, smem_for(sc)));
+        if (!first) {
+            first = sc;
+            first_occ = o;
+        }
+        if (sc < 256) break;  // narrower stages only when nothing wider fits
+        if ((long long)o * pool->num_sms >= s_items) {
+            SC = sc;
+            occ = o;
+            break;
+        }
+    }
+    if (!SC) {
+        SC = first;
+        occ = first_occ;
+    }
+    if (!SC) return LORA_OK;
+    const size_t s_smem = smem_for(SC);
+    // expand shared memory: B rows, y rows, v hi/lo
+    const int vr_stride = ns * R8 + 8;
+    const size_t e_b = a128((size_t)kOC * R8 * 2 + 32), e_y = a128((size_t)kTileRows * (kOC + 8) * 2);
+    const size_t e_v = a128((size_t)kTileRows * vr_stride * 2);
+    const size_t e_smem = e_b + e_y + 2 * e_v;
+
     const long long s_slots = (long long)pool->num_sms * (occ < 1 ? 1 : occ);
     int occ_e = 0;
     LORA_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_e, bgmv_expand_kernel, kThreads, e_smem));
@@ -522,14 +541,14 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     cfg.blockDim = dim3(kSThreads, 1, 1);
     cfg.stream = s;
     // grids of at most one wave; the kernels stride over their items
-    // grids of at most four waves (one for the expand); the kernels stride over their items
-    const long long s_items = max_tiles * ns * NC, e_items = max_tiles * ea.n_oc;
+    // grids of at most four waves; the kernels stride over their items
+    const long long e_items = max_tiles * ea.n_oc;
     cfg.gridDim = dim3((unsigned)(s_items < 4 * s_slots ? s_items : 4 * s_slots), 1, 1);
     cfg.dynamicSmemBytes = s_smem;
     LORA_CUDA_TRY(cudaLaunchKernelEx(&cfg, bgmv_shrink_kernel, sa));
     lora_note_launch();
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.gridDim = dim3((unsigned)(e_items < e_slots ? e_items : e_slots), 1, 1);
+    cfg.gridDim = dim3((unsigned)(e_items < 4 * e_slots ? e_items : 4 * e_slots), 1, 1);
     cfg.dynamicSmemBytes = e_smem;
     LORA_CUDA_TRY(cudaLaunchKernelEx(&cfg, bgmv_expand_kernel, ea));
     lora_note_launch();

@@ -51,6 +51,9 @@ struct SArgs {
     int rows;
     int *status;
     int spin_limit;
+    // slot-major variant
+    const int32_t *enabled, *key_count, *key_offset;
+    int n_slots, x_stages;
 };
 
 struct EArgs {
@@ -205,6 +208,147 @@ __global__ void __launch_bounds__(kSThreads) bgmv_shrink_kernel(const __grid_con
             const int t = i / p.R8, k = i - t * p.R8;
             float sum = 0.f;
             for (int hs = 0; hs < hsplit; ++hs) sum += red[(hs * kTileRows + t) * p.R8 + k];
+            dst[i] = sum;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- shrink, slot-major
+//
+// For small pools whose slots are mostly active (decode batches): one CTA per
+// (slot a, slice j, hidden chunk c).  The slot's A rows of the chunk do not
+// depend on this batch's metadata, so they are requested before the kernel
+// waits for the metadata build; then every 16-row tile of the slot's rows is
+// multiplied against them (A read once per slot, not once per tile).  The
+// partials land where the per-tile shrink would put them.
+
+__global__ void __launch_bounds__(kSThreads) bgmv_shrink_slot_kernel(const __grid_constant__ SArgs p) {
+    extern __shared__ __align__(128) char smem[];
+    __shared__ __align__(8) uint64_t abar, xbar[2];
+    __shared__ int s_rows[2][kTileRows];
+    const int XS = p.x_stages;  // 1 or 2
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, c4 = lane & 3;
+    const int c = blockIdx.x % p.NC, j = (blockIdx.x / p.NC) % p.n_slices, a = blockIdx.x / (p.NC * p.n_slices);
+    const int hb = c * p.HC, he = min(p.in_dim, hb + p.HC), len = he - hb;
+    const uint16_t *Ab = p.A[j] + (long long)a * p.A_ss[j];
+    uint16_t *as = (uint16_t *)(smem + p.off_a);
+    // tables written before the metadata build started (never by it): read through L2
+    const int r = (__ldcg(p.enabled + a) != 0) ? __ldcg(p.rank + a) : 0;
+    if (r <= 0) {
+        asm volatile("griddepcontrol.launch_dependents;");
+        return;
+    }
+    if (tid == 0) {
+        mbar_init(&abar, 1);
+        mbar_init(&xbar[0], 1);
+        mbar_init(&xbar[1], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    const uint32_t rowb = (uint32_t)len * 2;
+    if (warp == 0) {
+        if (lane == 0) mbar_expect_tx(&abar, rowb * (uint32_t)r);
+        __syncwarp();
+        for (int k = lane; k < r; k += 32)
+            bulk_g2s(as + k * p.as_stride, Ab + (long long)k * p.in_dim + hb, rowb, &abar);
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
+    const int cnt = p.key_count[a], off = p.key_offset[a];
+    const int n_t = (cnt + kTileRows - 1) / kTileRows;
+
+    auto load_x = [&](int t) {  // x rows of tile t into stage t % XS (warp 0)
+        const int st = t % XS, n = min(kTileRows, cnt - t * kTileRows);
+        uint16_t *xs = (uint16_t *)(smem + p.off_x + st * p.x_stage_bytes);
+        if (lane < n) s_rows[st][lane] = p.sorted[off + t * kTileRows + lane];
+        __syncwarp();
+        if (lane == 0) mbar_expect_tx(&xbar[st], rowb * (uint32_t)n);
+        __syncwarp();
+        if (lane < n)
+            bulk_g2s(xs + lane * p.xs_stride, p.in + (long long)(s_rows[st][lane] / p.row_div) * p.ld_in + hb, rowb,
+                     &xbar[st]);
+    };
+    if (warp == 0) {
+        if (n_t > 0) load_x(0);
+        if (n_t > 1 && XS > 1) load_x(1);
+    }
+    mbar_wait(&abar, 0, p.spin_limit, p.status);  // also before any exit: no copy may be in flight
+
+    const int nnb = (r + 7) >> 3;
+    int hsplit = 1;
+    while (nnb * hsplit * 2 <= 2 * kSWarps && hsplit < 4) hsplit *= 2;
+    const int units = nnb * hsplit;
+    const int steps = (len + 15) >> 4;
+    float *red = (float *)(smem + p.off_red);
+    for (int t = 0; t < n_t; ++t) {
+        const int st = t % XS, row0 = off + t * kTileRows, n = min(kTileRows, cnt - t * kTileRows);
+        mbar_wait(&xbar[st], (uint32_t)((t / XS) & 1), p.spin_limit, p.status);
+        const uint16_t *xs = (const uint16_t *)(smem + p.off_x + st * p.x_stage_bytes);
+        float acc[2][2][4];
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int q = 0; q < 2; ++q)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc[u][q][i] = 0.f;
+#pragma unroll
+        for (int ui = 0; ui < 2; ++ui) {
+            const int u = warp + ui * kSWarps;
+            if (u < units) {
+                const int nb = u / hsplit, hs = u - nb * hsplit;
+                const uint16_t *xq = xs + ((lane & 7) + ((lane >> 3) & 1) * 8) * p.xs_stride + (lane >> 4) * 8;
+                const uint16_t *aq = as + (nb * 8 + (lane & 7)) * p.as_stride + ((lane >> 3) & 1) * 8;
+                int i = hs;
+                // two independent accumulator chains
+                for (; i + hsplit < steps; i += 2 * hsplit) {
+                    uint32_t a0, a1, a2, a3, b0, b1, e0, e1, e2, e3, f0, f1;
+                    ldsm_x4(xq + i * 16, a0, a1, a2, a3);
+                    ldsm_x2(aq + i * 16, b0, b1);
+                    ldsm_x4(xq + (i + hsplit) * 16, e0, e1, e2, e3);
+                    ldsm_x2(aq + (i + hsplit) * 16, f0, f1);
+                    if ((i + hsplit) * 16 + 8 >= len) e2 = e3 = f1 = 0u;
+                    mma16816(acc[ui][0], a0, a1, a2, a3, b0, b1);
+                    mma16816(acc[ui][1], e0, e1, e2, e3, f0, f1);
+                }
+                if (i < steps) {
+                    uint32_t a0, a1, a2, a3, b0, b1;
+                    ldsm_x4(xq + i * 16, a0, a1, a2, a3);
+                    ldsm_x2(aq + i * 16, b0, b1);
+                    if (i * 16 + 8 >= len) a2 = a3 = b1 = 0u;
+                    mma16816(acc[ui][0], a0, a1, a2, a3, b0, b1);
+                }
+            }
+        }
+        __syncthreads();  // every warp is done with x stage st and with red of the previous tile
+        if (warp == 0 && t + XS < n_t) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            load_x(t + XS);
+        }
+        for (int i = tid; i < hsplit * kTileRows * p.R8; i += kSThreads) red[i] = 0.f;
+        __syncthreads();
+#pragma unroll
+        for (int ui = 0; ui < 2; ++ui) {
+            const int u = warp + ui * kSWarps;
+            if (u < units) {
+                const int nb = u / hsplit, hs = u - nb * hsplit;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int k = nb * 8 + 2 * c4 + h;
+                    if (k < r) {
+                        float *dst = red + (hs * kTileRows) * p.R8 + k;
+                        if (g < n) dst[g * p.R8] = acc[ui][0][h] + acc[ui][1][h];
+                        if (g + 8 < n) dst[(g + 8) * p.R8] = acc[ui][0][2 + h] + acc[ui][1][2 + h];
+                    }
+                }
+            }
+        }
+        __syncthreads();
+        float *dst = p.part + ((long long)c * p.n_slices + j) * p.rows * p.R8 + (long long)row0 * p.R8;
+        for (int i = tid; i < n * p.R8; i += kSThreads) {
+            const int t2 = i / p.R8, k = i - t2 * p.R8;
+            float sum = 0.f;
+            for (int hs = 0; hs < hsplit; ++hs) sum += red[(hs * kTileRows + t2) * p.R8 + k];
             dst[i] = sum;
         }
     }
@@ -413,6 +557,8 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
                                            200 * 1024));
         LORA_CUDA_TRY(cudaFuncSetAttribute(bgmv_expand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            200 * 1024));
+        LORA_CUDA_TRY(cudaFuncSetAttribute(bgmv_shrink_slot_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           200 * 1024));
         g_split_configured[dev] = 1;
     }
     // shrink shared memory: 2 stages of (16 + R8) rows x SC columns (rows
@@ -456,6 +602,19 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     int occ_e = 0;
     LORA_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_e, bgmv_expand_kernel, kThreads, e_smem));
     const long long e_slots = (long long)pool->num_sms * (occ_e < 1 ? 1 : occ_e);
+
+    // slot-major shrink for dense batches of a small pool: the slot's A chunk
+    // is fetched while the metadata is still being built
+    const int L = pool->desc.max_loras;
+    const size_t x_stage = a128((size_t)kTileRows * (HC + 8) * 2);
+    const int x_stages = a128((size_t)R8 * (HC + 8) * 2) + 2 * x_stage + red_bytes <= 100 * 1024 ? 2 : 1;
+    const size_t slot_smem = a128((size_t)R8 * (HC + 8) * 2) + x_stages * x_stage + red_bytes;
+    bool slot_major = pr.E == 1 && pr.count_idx == 3 && pr.rows >= 2 * L && slot_smem <= 100 * 1024;
+    if (slot_major) {
+        int o = 0;
+        LORA_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, bgmv_shrink_slot_kernel, kSThreads, slot_smem));
+        slot_major = (long long)L * ns * NC <= (long long)o * pool->num_sms;
+    }
 
     SArgs sa;
     memset(&sa, 0, sizeof(sa));
@@ -543,9 +702,26 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     // grids of at most one wave; the kernels stride over their items
     // grids of at most four waves; the kernels stride over their items
     const long long e_items = max_tiles * ea.n_oc;
-    cfg.gridDim = dim3((unsigned)(s_items < 4 * s_slots ? s_items : 4 * s_slots), 1, 1);
-    cfg.dynamicSmemBytes = s_smem;
-    LORA_CUDA_TRY(cudaLaunchKernelEx(&cfg, bgmv_shrink_kernel, sa));
+    if (slot_major) {
+        sa.enabled = pool->d_enabled;
+        sa.key_count = pr.meta->key_count;
+        sa.key_offset = pr.meta->key_offset;
+        sa.n_slots = L;
+        sa.x_stages = x_stages;
+        sa.xs_stride = HC + 8;
+        sa.as_stride = HC + 8;
+        sa.x_stage_bytes = (int)a128((size_t)kTileRows * (HC + 8) * 2);
+        sa.off_a = 0;
+        sa.off_x = (int)a128((size_t)R8 * (HC + 8) * 2);
+        sa.off_red = sa.off_x + 2 * sa.x_stage_bytes;
+        cfg.gridDim = dim3((unsigned)(L * ns * NC), 1, 1);
+        cfg.dynamicSmemBytes = slot_smem;
+        LORA_CUDA_TRY(cudaLaunchKernelEx(&cfg, bgmv_shrink_slot_kernel, sa));
+    } else {
+        cfg.gridDim = dim3((unsigned)(s_items < 4 * s_slots ? s_items : 4 * s_slots), 1, 1);
+        cfg.dynamicSmemBytes = s_smem;
+        LORA_CUDA_TRY(cudaLaunchKernelEx(&cfg, bgmv_shrink_kernel, sa));
+    }
     lora_note_launch();
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.gridDim = dim3((unsigned)(e_items < 4 * e_slots ? e_items : 4 * e_slots), 1, 1);

@@ -137,3 +137,18 @@ def test_dense_token_counts_share_workspace(policy):
     w[:100] = 3.0
     act = active_mask(c.idx, c.L, c.enabled, c.ranks)
     assert_delta(bf16_bits_to_f32(y)[act] - bf16_bits_to_f32(c.y0)[act], (w[:, None] * d_ref)[act], "256+100+256")
+
+
+def test_dense_idle_and_disabled_slots(policy):
+    """Enabled slots with no tokens, a disabled slot and a rank-0 slot next to
+    busy slots with several 16-row tiles each (the slot-major shrink reads A
+    of every enabled slot before it knows the batch)."""
+    rng = np.random.default_rng(77)
+    T, L = 160, 8
+    idx = rng.choice(np.array([0, 3, 5, -1], np.int32), size=T, p=[0.4, 0.3, 0.2, 0.1]).astype(np.int32)
+    idx[7] = 6   # disabled slot: no delta
+    idx[9] = 7   # rank-0 slot: no delta
+    c = gen.dense_case(name="idle_slots", T=T, H=1032, out_dims=(264, 520), L=L, R=16, seed=78,
+                       ranks=(16, 8, 16, 13, 16, 16, 16, 0), scales=(1.0, 2.0, 0.5, 1.5, 1.0, 0.25, 1.0, 1.0),
+                       enabled=(1, 1, 1, 1, 1, 1, 0, 1), idx=idx)
+    _dense(c)

@@ -145,11 +145,11 @@ __global__ void __launch_bounds__(kSThreads) bgmv_shrink_kernel(const __grid_con
         int hsplit = 1;
         while (nnb * hsplit * 2 <= 2 * kSWarps && hsplit < 4) hsplit *= 2;
         const int units = nnb * hsplit;
-        float acc[2][4];
+        float acc[2][4], acc2[2][4];
 #pragma unroll
         for (int u = 0; u < 2; ++u)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) acc[u][i] = 0.f;
+            for (int i = 0; i < 4; ++i) acc[u][i] = acc2[u][i] = 0.f;
         for (int s = 0; s < n_sub; ++s) {
             const int st = (gs + s) & 1;
             mbar_wait(&full[st], (uint32_t)(((gs + s) >> 1) & 1), p.spin_limit, p.status);
@@ -162,13 +162,25 @@ __global__ void __launch_bounds__(kSThreads) bgmv_shrink_kernel(const __grid_con
                 const int u = warp + ui * kSWarps;
                 if (u < units) {
                     const int nb = u / hsplit, hs = u - nb * hsplit;
-                    for (int i = hs; i < steps; i += hsplit) {
-                        const int k0 = i * 16;
+                    const uint16_t *xq = xs + ((lane & 7) + ((lane >> 3) & 1) * 8) * p.xs_stride + (lane >> 4) * 8;
+                    const uint16_t *aq = as + (nb * 8 + (lane & 7)) * p.as_stride + ((lane >> 3) & 1) * 8;
+                    int i = hs;
+                    // two independent accumulator chains
+                    for (; i + hsplit < steps; i += 2 * hsplit) {
+                        uint32_t a0, a1, a2, a3, b0, b1, e0, e1, e2, e3, f0, f1;
+                        ldsm_x4(xq + i * 16, a0, a1, a2, a3);
+                        ldsm_x2(aq + i * 16, b0, b1);
+                        ldsm_x4(xq + (i + hsplit) * 16, e0, e1, e2, e3);
+                        ldsm_x2(aq + (i + hsplit) * 16, f0, f1);
+                        if ((i + hsplit) * 16 + 8 >= len) e2 = e3 = f1 = 0u;
+                        mma16816(acc[ui], a0, a1, a2, a3, b0, b1);
+                        mma16816(acc2[ui], e0, e1, e2, e3, f0, f1);
+                    }
+                    if (i < steps) {
                         uint32_t a0, a1, a2, a3, b0, b1;
-                        ldsm_x4(xs + ((lane & 7) + ((lane >> 3) & 1) * 8) * p.xs_stride + k0 + (lane >> 4) * 8,
-                                a0, a1, a2, a3);
-                        ldsm_x2(as + (nb * 8 + (lane & 7)) * p.as_stride + k0 + ((lane >> 3) & 1) * 8, b0, b1);
-                        if (k0 + 8 >= len) a2 = a3 = b1 = 0u;
+                        ldsm_x4(xq + i * 16, a0, a1, a2, a3);
+                        ldsm_x2(aq + i * 16, b0, b1);
+                        if (i * 16 + 8 >= len) a2 = a3 = b1 = 0u;
                         mma16816(acc[ui], a0, a1, a2, a3, b0, b1);
                     }
                 }
@@ -195,8 +207,8 @@ __global__ void __launch_bounds__(kSThreads) bgmv_shrink_kernel(const __grid_con
                     const int k = nb * 8 + 2 * c4 + h;
                     if (k < r) {
                         float *dst = red + (hs * kTileRows) * p.R8 + k;
-                        if (g < n) dst[g * p.R8] = acc[ui][h];
-                        if (g + 8 < n) dst[(g + 8) * p.R8] = acc[ui][2 + h];
+                        if (g < n) dst[g * p.R8] = acc[ui][h] + acc2[ui][h];
+                        if (g + 8 < n) dst[(g + 8) * p.R8] = acc[ui][2 + h] + acc2[ui][2 + h];
                     }
                 }
             }
@@ -471,33 +483,49 @@ __global__ void __launch_bounds__(kThreads) bgmv_expand_kernel(const __grid_cons
 
         const int nob = (oe - ob) >> 3;
         const int ksteps = (rs + 15) >> 4;
+        // two 8-column blocks per pass: their loads are issued before either MMA chain
 #pragma unroll 1
-        for (int ob8 = warp; ob8 < nob; ob8 += kWarps) {
-            const int o0 = ob + ob8 * 8;
-            int jj = j0;
-            while (jj + 1 < ns && o0 >= p.out_off[jj + 1]) ++jj;
-            float d[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int ob8 = warp; ob8 < nob; ob8 += 2 * kWarps) {
+            const int obB = ob8 + kWarps;
+            const bool hasB = obB < nob;
+            int jA = j0, jB = j0;
+            while (jA + 1 < ns && ob + ob8 * 8 >= p.out_off[jA + 1]) ++jA;
+            while (jB + 1 < ns && ob + obB * 8 >= p.out_off[jB + 1]) ++jB;
+            float dA[4] = {0.f, 0.f, 0.f, 0.f}, dB[4] = {0.f, 0.f, 0.f, 0.f};
             for (int ks = 0; ks < ksteps; ++ks) {
                 const int k0 = ks * 16;
-                uint32_t h0, h1, h2, h3, l0, l1, l2, l3, b0, b1;
-                const int acol = jj * p.R8 + k0 + (lane >> 4) * 8;
-                ldsm_x4(vh + arow * p.vr_stride + acol, h0, h1, h2, h3);
-                ldsm_x4(vl + arow * p.vr_stride + acol, l0, l1, l2, l3);
-                ldsm_x2(bs + (ob8 * 8 + (lane & 7)) * rs + k0 + ((lane >> 3) & 1) * 8, b0, b1);
-                if (k0 + 8 >= rs) h2 = h3 = l2 = l3 = b1 = 0u;
-                mma16816(d, h0, h1, h2, h3, b0, b1);
-                mma16816(d, l0, l1, l2, l3, b0, b1);
+                const bool tail = k0 + 8 >= rs;
+                uint32_t h[4], l[4], b[2], hB[4], lB[4], bB[2];
+                const int colA = jA * p.R8 + k0 + (lane >> 4) * 8, colB = jB * p.R8 + k0 + (lane >> 4) * 8;
+                ldsm_x4(vh + arow * p.vr_stride + colA, h[0], h[1], h[2], h[3]);
+                ldsm_x4(vl + arow * p.vr_stride + colA, l[0], l[1], l[2], l[3]);
+                ldsm_x2(bs + (ob8 * 8 + (lane & 7)) * rs + k0 + ((lane >> 3) & 1) * 8, b[0], b[1]);
+                if (hasB) {
+                    ldsm_x4(vh + arow * p.vr_stride + colB, hB[0], hB[1], hB[2], hB[3]);
+                    ldsm_x4(vl + arow * p.vr_stride + colB, lB[0], lB[1], lB[2], lB[3]);
+                    ldsm_x2(bs + (obB * 8 + (lane & 7)) * rs + k0 + ((lane >> 3) & 1) * 8, bB[0], bB[1]);
+                }
+                if (tail) h[2] = h[3] = l[2] = l[3] = b[1] = hB[2] = hB[3] = lB[2] = lB[3] = bB[1] = 0u;
+                mma16816(dA, h[0], h[1], h[2], h[3], b[0], b[1]);
+                if (hasB) mma16816(dB, hB[0], hB[1], hB[2], hB[3], bB[0], bB[1]);
+                mma16816(dA, l[0], l[1], l[2], l[3], b[0], b[1]);
+                if (hasB) mma16816(dB, lB[0], lB[1], lB[2], lB[3], bB[0], bB[1]);
             }
-            const int ocol = ob8 * 8 + 2 * c4;
-            if (g < n) {
-                uint32_t *yp = (uint32_t *)(ys + g * p.ys_stride + ocol);
-                const uint32_t u = *yp;
-                *yp = pack_bf16x2(bf16lo(u) + d[0], bf16hi(u) + d[1]);
-            }
-            if (g + 8 < n) {
-                uint32_t *yp = (uint32_t *)(ys + (g + 8) * p.ys_stride + ocol);
-                const uint32_t u = *yp;
-                *yp = pack_bf16x2(bf16lo(u) + d[2], bf16hi(u) + d[3]);
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                if (q == 1 && !hasB) break;
+                const float *d = q ? dB : dA;
+                const int ocol = (q ? obB : ob8) * 8 + 2 * c4;
+                if (g < n) {
+                    uint32_t *yp = (uint32_t *)(ys + g * p.ys_stride + ocol);
+                    const uint32_t u = *yp;
+                    *yp = pack_bf16x2(bf16lo(u) + d[0], bf16hi(u) + d[1]);
+                }
+                if (g + 8 < n) {
+                    uint32_t *yp = (uint32_t *)(ys + (g + 8) * p.ys_stride + ocol);
+                    const uint32_t u = *yp;
+                    *yp = pack_bf16x2(bf16lo(u) + d[2], bf16hi(u) + d[3]);
+                }
             }
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -508,7 +536,9 @@ __global__ void __launch_bounds__(kThreads) bgmv_expand_kernel(const __grid_cons
                          "r"(smem_u32(ys + lane * p.ys_stride)), "r"((uint32_t)(oe - ob) * 2)
                          : "memory");
             asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-            asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+            // the rows may be reused once the copy has read them; the writes
+            // are complete when the grid is
+            asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
         }
     }
     asm volatile("griddepcontrol.launch_dependents;");
@@ -713,11 +743,13 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
         sa.x_stage_bytes = (int)a128((size_t)kTileRows * (HC + 8) * 2);
         sa.off_a = 0;
         sa.off_x = (int)a128((size_t)R8 * (HC + 8) * 2);
-        sa.off_red = sa.off_x + 2 * sa.x_stage_bytes;
+        sa.off_red = sa.off_x + x_stages * sa.x_stage_bytes;
+        if ((size_t)sa.off_red + red_bytes > slot_smem) return LORA_ERR_INVALID_ARG;  // layout check
         cfg.gridDim = dim3((unsigned)(L * ns * NC), 1, 1);
         cfg.dynamicSmemBytes = slot_smem;
         LORA_CUDA_TRY(cudaLaunchKernelEx(&cfg, bgmv_shrink_slot_kernel, sa));
     } else {
+        if ((size_t)sa.off_red + red_bytes > s_smem) return LORA_ERR_INVALID_ARG;  // layout check
         cfg.gridDim = dim3((unsigned)(s_items < 4 * s_slots ? s_items : 4 * s_slots), 1, 1);
         cfg.dynamicSmemBytes = s_smem;
         LORA_CUDA_TRY(cudaLaunchKernelEx(&cfg, bgmv_shrink_kernel, sa));

@@ -28,6 +28,7 @@ struct MetaArgs {
     const int32_t *enabled;
     int32_t *status;
     int T, K, E, L, n_keys, n_chunks, cache_keys;
+    int key_bits;  // smallest b with 2^b > n_keys + 1: the pattern of key -1 matches no key
     lora_meta_t m;
 };
 
@@ -68,6 +69,18 @@ __device__ __forceinline__ int row_key_e(const MetaArgs &a, const unsigned char 
     return key;
 }
 
+// Lanes of the warp holding the same key (a ballot per key bit; the cost does
+// not grow with the number of distinct keys in the warp).
+__device__ __forceinline__ unsigned key_peers(int key, int bits) {
+    unsigned m = 0xffffffffu;
+    for (int b = 0; b < bits; ++b) {
+        const bool bit = (key >> b) & 1;
+        const unsigned bal = __ballot_sync(0xffffffffu, bit);
+        m &= bit ? bal : ~bal;
+    }
+    return m;
+}
+
 __global__ void __launch_bounds__(kThreads, 1) build_meta_kernel(MetaArgs a) {
     extern __shared__ int sm[];
     const int NK = a.n_keys, NK1 = NK + 1, W = a.n_chunks;
@@ -76,9 +89,9 @@ __global__ void __launch_bounds__(kThreads, 1) build_meta_kernel(MetaArgs a) {
     int *off = cnt + NK1;            // [NK1]
     int *tmin = off + NK1;           // [NK1] smallest token of each key (dense)
     int *tmax = tmin + NK1;          // [NK1] largest token of each key (dense)
-    int *misc = tmax + NK1;          // [40]: warp totals (33), n_bad at [36]
-    unsigned char *act = (unsigned char *)(misc + 40);  // [L] slot enabled and rank > 0
-    int *kc = misc + 40 + (a.L + 3) / 4;                // [rows] keys of pass 1 when cached
+    int *misc = tmax + NK1;          // [200]: totals at [32..35], n_bad at [36], warp scan totals at [40..199]
+    unsigned char *act = (unsigned char *)(misc + 200);  // [L] slot enabled and rank > 0
+    int *kc = misc + 200 + (a.L + 3) / 4;                // [rows] keys of pass 1 when cached
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nthreads = blockDim.x;
     const int rows = a.T * a.K;
@@ -104,7 +117,8 @@ __global__ void __launch_bounds__(kThreads, 1) build_meta_kernel(MetaArgs a) {
         }
     }
     for (int i = tid; i < a.L; i += nthreads) act[i] = (a.enabled[i] != 0 && a.rank[i] > 0) ? 1 : 0;
-    for (int i = tid; i < W * NK1; i += nthreads) hist[i] = 0;
+    for (int i = tid; i < (W * NK1) / 4; i += nthreads) ((int4 *)hist)[i] = make_int4(0, 0, 0, 0);
+    for (int i = (W * NK1) / 4 * 4 + tid; i < W * NK1; i += nthreads) hist[i] = 0;
     for (int i = tid; i < NK1; i += nthreads) {
         tmin[i] = 0x7fffffff;
         tmax[i] = -1;
@@ -148,11 +162,14 @@ __global__ void __launch_bounds__(kThreads, 1) build_meta_kernel(MetaArgs a) {
                     key = row_key(a, act, row, s, &bad);
                 }
             }
-            const unsigned peers = __match_any_sync(0xffffffffu, key);
-            if (v && lane == __ffs(peers) - 1) hist[warp * NK1 + key] += __popc(peers);
-            if (v && a.K == 1 && key < NK) {
-                atomicMin(&tmin[key], row);
-                atomicMax(&tmax[key], row);
+            const unsigned peers = key_peers(key, a.key_bits);
+            const int leader = __ffs(peers) - 1;
+            if (v && lane == leader) {
+                hist[warp * NK1 + key] += __popc(peers);
+                if (a.K == 1 && key < NK) {  // the rows of a warp step are consecutive
+                    atomicMin(&tmin[key], base + leader);
+                    atomicMax(&tmax[key], base + 31 - __clz(peers));
+                }
             }
             __syncwarp();
         }
@@ -174,60 +191,75 @@ __global__ void __launch_bounds__(kThreads, 1) build_meta_kernel(MetaArgs a) {
     }
     __syncthreads();
 
-    // every key-space prefix sum in one pass of warp 0: row offsets, group
-    // index, 16-row tiles, long-run tiles and short tiles.  Lane l owns a
+    // every key-space prefix sum in one block-wide scan: row offsets, group
+    // index, 16-row tiles, long-run tiles and short tiles.  Thread t owns a
     // contiguous block of keys.
     int *gidx = hist + W * NK1;  // the four scratch rows after the chunk histograms
     int *tiles = gidx + NK1;
     int *lt_cnt = tiles + NK1;
     int *st_cnt = lt_cnt + NK1;
-    if (warp == 0) {
-        const int per = (NK1 + 31) / 32;
-        const int b0 = min(NK1, lane * per), b1 = min(NK1, b0 + per);
-        int s0 = 0, s1 = 0, s2 = 0, s3 = 0, s4 = 0;
+    int *wt = misc + 40;         // [5][32] per-warp totals, then their exclusive offsets
+    {
+        const int per = (NK1 + nthreads - 1) / nthreads;
+        const int b0 = min(NK1, tid * per), b1 = min(NK1, b0 + per);
+        int sv5[5] = {0, 0, 0, 0, 0};
         for (int b = b0; b < b1; ++b) {
             const int c = b < NK ? cnt[b] : 0;
             const bool run = c > 0 && a.K == 1 && c >= LORA_LONG_MIN && tmax[b] - tmin[b] == c - 1;
-            s0 += cnt[b];
-            s1 += c > 0 ? 1 : 0;
-            s2 += (c + LORA_TILE_ROWS - 1) / LORA_TILE_ROWS;
-            s3 += run ? (c + LORA_LTILE_ROWS - 1) / LORA_LTILE_ROWS : 0;
-            s4 += (c > 0 && !run) ? (c + LORA_TILE_ROWS - 1) / LORA_TILE_ROWS : 0;
+            sv5[0] += cnt[b];
+            sv5[1] += c > 0 ? 1 : 0;
+            sv5[2] += (c + LORA_TILE_ROWS - 1) / LORA_TILE_ROWS;
+            sv5[3] += run ? (c + LORA_LTILE_ROWS - 1) / LORA_LTILE_ROWS : 0;
+            sv5[4] += (c > 0 && !run) ? (c + LORA_TILE_ROWS - 1) / LORA_TILE_ROWS : 0;
         }
-        int e0 = s0, e1 = s1, e2 = s2, e3 = s3, e4 = s4;  // inclusive scans over lanes
+        int inc[5];
+#pragma unroll
+        for (int q = 0; q < 5; ++q) inc[q] = sv5[q];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int v0 = __shfl_up_sync(0xffffffffu, e0, o), v1 = __shfl_up_sync(0xffffffffu, e1, o);
-            const int v2 = __shfl_up_sync(0xffffffffu, e2, o), v3 = __shfl_up_sync(0xffffffffu, e3, o);
-            const int v4 = __shfl_up_sync(0xffffffffu, e4, o);
-            if (lane >= o) {
-                e0 += v0;
-                e1 += v1;
-                e2 += v2;
-                e3 += v3;
-                e4 += v4;
+#pragma unroll
+            for (int q = 0; q < 5; ++q) {
+                const int v = __shfl_up_sync(0xffffffffu, inc[q], o);
+                if (lane >= o) inc[q] += v;
             }
         }
-        int r0s = e0 - s0, r1s = e1 - s1, r2s = e2 - s2, r3s = e3 - s3, r4s = e4 - s4;
+        if (lane == 31) {
+#pragma unroll
+            for (int q = 0; q < 5; ++q) wt[q * 32 + warp] = inc[q];
+        }
+        __syncthreads();
+        if (warp == 0) {
+            const int nw = nthreads / 32;
+#pragma unroll
+            for (int q = 0; q < 5; ++q) {
+                const int v0 = lane < nw ? wt[q * 32 + lane] : 0;
+                int x = v0;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int v = __shfl_up_sync(0xffffffffu, x, o);
+                    if (lane >= o) x += v;
+                }
+                if (lane < nw) wt[q * 32 + lane] = x - v0;
+                if (lane == 31 && q > 0) misc[31 + q] = x;  // groups, tiles, long tiles, short tiles
+            }
+        }
+        __syncthreads();
+        int ex[5];
+#pragma unroll
+        for (int q = 0; q < 5; ++q) ex[q] = wt[q * 32 + warp] + inc[q] - sv5[q];
         for (int b = b0; b < b1; ++b) {
             const int c = b < NK ? cnt[b] : 0;
             const bool run = c > 0 && a.K == 1 && c >= LORA_LONG_MIN && tmax[b] - tmin[b] == c - 1;
-            off[b] = r0s;
-            gidx[b] = r1s;
-            tiles[b] = r2s;
-            lt_cnt[b] = r3s;
-            st_cnt[b] = r4s;
-            r0s += cnt[b];
-            r1s += c > 0 ? 1 : 0;
-            r2s += (c + LORA_TILE_ROWS - 1) / LORA_TILE_ROWS;
-            r3s += run ? (c + LORA_LTILE_ROWS - 1) / LORA_LTILE_ROWS : 0;
-            r4s += (c > 0 && !run) ? (c + LORA_TILE_ROWS - 1) / LORA_TILE_ROWS : 0;
-        }
-        if (lane == 31) {
-            misc[32] = e1;  // groups
-            misc[33] = e2;  // tiles
-            misc[34] = e3;  // long tiles
-            misc[35] = e4;  // short tiles
+            off[b] = ex[0];
+            gidx[b] = ex[1];
+            tiles[b] = ex[2];
+            lt_cnt[b] = ex[3];
+            st_cnt[b] = ex[4];
+            ex[0] += cnt[b];
+            ex[1] += c > 0 ? 1 : 0;
+            ex[2] += (c + LORA_TILE_ROWS - 1) / LORA_TILE_ROWS;
+            ex[3] += run ? (c + LORA_LTILE_ROWS - 1) / LORA_LTILE_ROWS : 0;
+            ex[4] += (c > 0 && !run) ? (c + LORA_TILE_ROWS - 1) / LORA_TILE_ROWS : 0;
         }
     }
     __syncthreads();
@@ -254,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1) build_meta_kernel(MetaArgs a) {
                     key = row_key(a, act, row, a.idx[row / a.K], &dummy);
                 }
             }
-            const unsigned peers = __match_any_sync(0xffffffffu, key);
+            const unsigned peers = key_peers(key, a.key_bits);
             int pos = 0;
             if (v) pos = hist[warp * NK1 + key] + __popc(peers & lt);
             __syncwarp();
@@ -331,7 +363,7 @@ lora_status_t lora_launch_build_meta(const lora_pool_t *pool, const int32_t *d_i
     if (nthreads > kThreads) nthreads = kThreads;
     const int nwarps = nthreads / 32;
     // chunk histograms [W][NK1] + 4 scratch rows + cnt, off, tmin, tmax + misc + slot table
-    const long long fixed = 8LL * NK1 + 40 + (L + 3) / 4;
+    const long long fixed = 8LL * NK1 + 200 + (L + 3) / 4;
     int W = (int)((kSmemBudgetInts - fixed) / NK1);
     if (W > nwarps) W = nwarps;
     if (W < 1) return LORA_ERR_CAPACITY;
@@ -350,6 +382,8 @@ lora_status_t lora_launch_build_meta(const lora_pool_t *pool, const int32_t *d_i
     a.n_keys = n_keys;
     a.n_chunks = W;
     a.cache_keys = cache;
+    a.key_bits = 1;
+    while ((1LL << a.key_bits) <= (long long)NK1) ++a.key_bits;
     a.m = *meta;
     const size_t smem = (size_t)(used + (cache ? rows : 0)) * 4;
     // raise the kernel's shared-memory limit once per device (outside any capture)

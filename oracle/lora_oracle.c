@@ -30,6 +30,11 @@
  *    adapter; counts, exclusive offsets and the list of non-empty keys
  *    (vLLM FusedMoEWithLoRA: moe_lora_align_block_size, unpadded form).
  *
+ *  - lo_sink_act: the Inkling sink-expert activation between the w13 and w2
+ *    LoRA layers (InklingSinkExpertsLinear.forward: gate_up split in halves,
+ *    SiLU(gate) * up, times the per-expert gamma of column c, expert c / d_mlp
+ *    by _gamma_expand), rounded to bf16 where the page's tensors are bf16.
+ *
  *  - lo_moe_w13 / lo_moe_w2: the fused-MoE LoRA deltas (vLLM
  *    FusedMoEWithLoRA._inject_lora_into_fused_moe: add_lora_fused_moe into
  *    the pre-activation cache for w13, into the per-(token, k) w2 output
@@ -47,6 +52,7 @@
  * -ffp-contract=off), so results are identical on every host and for every
  * thread count (OpenMP only splits independent tokens/pairs).
  */
+#include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -387,4 +393,43 @@ int32_t lo_moe_align_padded(int32_t T, int32_t K, int32_t E, int32_t L, const in
         npp[a] = pos;
     }
     return rc;
+}
+
+/* -------------------------------------------------- Inkling sink experts */
+
+/* Round to the nearest bf16 value, ties to even (8 significant bits), from an
+ * exact double; the result is returned as a double. */
+static double round_bf16(double v) {
+    if (v == 0.0 || !isfinite(v)) return v;
+    int e;
+    frexp(v, &e);    /* v = f * 2^e with 0.5 <= |f| < 1 */
+    int q = e - 8;   /* spacing of bf16 values in this binade */
+    if (q < -133) q = -133;
+    return ldexp(rint(ldexp(v, -q)), q); /* rint rounds half to even */
+}
+
+/* InklingSinkExpertsLinear.forward between its two linear layers, with
+ * n = n_experts and W = n * d_mlp columns per half:
+ *   gate = gate_up[t][c], up = gate_up[t][W + c]          (chunk(2, dim=-1))
+ *   s    = bf16(silu(gate))      silu(g) = g / (1 + exp(-g)), exact in double
+ *   p    = bf16(s * up)
+ *   h[t][c] = bf16(p * gammas[t][c / d_mlp])              (_gamma_expand, .to(bf16))
+ * Outputs are bf16 bits. */
+void lo_sink_act(int32_t T, int32_t n_experts, int32_t d_mlp, const uint16_t *gate_up, int64_t ld_gu,
+                 const float *gammas, int64_t ld_gamma, uint16_t *h, int64_t ld_h) {
+    const int64_t W = (int64_t)n_experts * d_mlp;
+    for (int32_t t = 0; t < T; ++t) {
+        for (int64_t c = 0; c < W; ++c) {
+            const double g = (double)bf(gate_up[(int64_t)t * ld_gu + c]);
+            const double u = (double)bf(gate_up[(int64_t)t * ld_gu + W + c]);
+            const double sg = round_bf16(g / (1.0 + exp(-g)));
+            const double pr = round_bf16(sg * u);
+            const double v = round_bf16(pr * (double)gammas[(int64_t)t * ld_gamma + c / d_mlp]);
+            /* v is a bf16 value: its float has zero low 16 bits */
+            const float f = (float)v;
+            uint32_t bits;
+            memcpy(&bits, &f, 4);
+            h[(int64_t)t * ld_h + c] = (uint16_t)(bits >> 16);
+        }
+    }
 }

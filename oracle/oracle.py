@@ -37,7 +37,7 @@ def build(force: bool = False) -> str:
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + f".{os.getpid()}.tmp"
         cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fopenmp",
-               "-fPIC", "-shared", _SRC, "-o", tmp]
+               "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"]
         subprocess.run(cmd, check=True)
         os.replace(tmp, _LIB)
     return _LIB
@@ -66,6 +66,8 @@ def _bind(path):
     lib.lo_logits.restype = None
     lib.lo_logits.argtypes = [_I32, _I32, ctypes.c_void_p, _U16P, _I64, _F32P, _I64, ctypes.c_float, _F32P,
                               _I64]
+    lib.lo_sink_act.restype = None
+    lib.lo_sink_act.argtypes = [_I32, _I32, _I32, _U16P, _I64, _F32P, _I64, _U16P, _I64]
     lib.lo_moe_w2.restype = None
     lib.lo_moe_w2.argtypes = [_I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32,
                               _I32P, _I32P, _F32P, _I32P, _I32P, _F32P, _U16P, _I64,
@@ -94,7 +96,7 @@ def compile_variant(src_text: str, out_path: str) -> str:
     with open(src, "w") as f:
         f.write(src_text)
     subprocess.run(["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fopenmp",
-                    "-fPIC", "-shared", src, "-o", out_path], check=True)
+                    "-fPIC", "-shared", src, "-o", out_path, "-lm"], check=True)
     return out_path
 
 
@@ -258,4 +260,18 @@ def logits(logits_in, delta, vocab_size, mapping=None, mup=1.0):
     return out
 
 
-__all__ = ["logits", "moe_align_padded", "build", "use_library", "compile_variant", "source_text", "max_threads", "dense_meta", "dense_delta", "moe_meta", "moe_w13", "moe_w2"]
+def sink_act(gate_up, gammas, n_experts, d_mlp):
+    """Inkling sink-expert activation: bf16 bits h[T][n*d_mlp] from bf16 bits
+    gate_up[T][2*n*d_mlp] and fp32 gammas[T][n]."""
+    lib = _load()
+    gate_up = _c(gate_up, np.uint16)
+    gammas = _c(gammas, np.float32)
+    T = gate_up.shape[0]
+    W = n_experts * d_mlp
+    assert gate_up.shape[1] >= 2 * W and gammas.shape[1] >= n_experts
+    h = np.empty((T, W), np.uint16)
+    lib.lo_sink_act(T, n_experts, d_mlp, gate_up, gate_up.shape[1], gammas, gammas.shape[1], h, W)
+    return h
+
+
+__all__ = ["sink_act", "logits", "moe_align_padded", "build", "use_library", "compile_variant", "source_text", "max_threads", "dense_meta", "dense_delta", "moe_meta", "moe_w13", "moe_w2"]

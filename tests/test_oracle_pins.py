@@ -278,6 +278,10 @@ MUTANTS = {
                                    "const int32_t eb = shared_outer ? (e % EB) : (E - 1 - e);"),
     "logits_reindex_inverted": ("const int32_t src = map ? map[i] : i;",
                                 "const int32_t src = map ? (map[i] ^ 1) : i;"),
+    "sink_gate_up_swapped": ("const double g = (double)bf(gate_up[(int64_t)t * ld_gu + c]);\n            const double u = (double)bf(gate_up[(int64_t)t * ld_gu + W + c]);",
+                             "const double u = (double)bf(gate_up[(int64_t)t * ld_gu + c]);\n            const double g = (double)bf(gate_up[(int64_t)t * ld_gu + W + c]);"),
+    "sink_gamma_by_column_mod": ("gammas[(int64_t)t * ld_gamma + c / d_mlp]", "gammas[(int64_t)t * ld_gamma + c % n_experts]"),
+    "sink_sigmoid_only": ("round_bf16(g / (1.0 + exp(-g)))", "round_bf16(1.0 / (1.0 + exp(-g)))"),
     "logits_mup_on_base_only": ("out[(int64_t)t * ld_out + i] = mup * full;",
                                 "out[(int64_t)t * ld_out + i] = full + (mup - 1.0f) * bf(logits_in[(int64_t)t * ld_in + src]);"),
 }
@@ -289,7 +293,8 @@ def _pin_suite_passes():
               lambda: test_moe_bruteforce_fp64(1, True), test_merged_weight_identity_tiny_preset,
               test_packed_slices_equal_separate_application,
               lambda: test_dense_meta_matches_numpy_stable_argsort(0),
-              test_golden_logits_reindex_example, test_logits_adds_delta_then_scales_everything_by_mup]
+              test_golden_logits_reindex_example, test_logits_adds_delta_then_scales_everything_by_mup,
+              test_golden_sink_act_by_hand, test_sink_act_expert_of_each_column]
     for chk in checks:
         try:
             chk()
@@ -371,3 +376,39 @@ def test_moe_align_padded_consistent_with_unpadded_meta(seed):
         blocks = sum(-(-int(c) // BM) for c in un.key_count[a * E:(a + 1) * E])
         assert pad.npp[a] == blocks * BM
         assert np.sum(pad.expert[a] >= 0) == blocks
+
+
+# ----------------------------------------------------------------- Inkling sink experts
+
+def test_golden_sink_act_by_hand():
+    g = load_golden("sink_act_by_hand.json")
+    gu = f32_to_bf16_bits(np.asarray(g["gate_up"], np.float32))
+    h = oracle.sink_act(gu, np.asarray(g["gammas"], np.float32), g["n_experts"], g["d_mlp"])
+    np.testing.assert_array_equal(bf16_bits_to_f32(h), np.asarray(g["expected_h"], np.float32))
+
+
+def test_sink_act_expert_of_each_column():
+    """gate large (silu(g) = g to bf16 precision), up = 1, one power of two per
+    expert: h[t][c] = g * gamma[c // d_mlp] exactly, for d_mlp not a power of two."""
+    n, d = 3, 5
+    T = 2
+    gate = np.full((T, n * d), 20.0, np.float32)
+    up = np.ones((T, n * d), np.float32)
+    gam = np.array([[0.5, 4.0, 0.125], [2.0, 1.0, 8.0]], np.float32)
+    h = bf16_bits_to_f32(oracle.sink_act(f32_to_bf16_bits(np.concatenate([gate, up], 1)), gam, n, d))
+    want = 20.0 * gam[:, np.arange(n * d) // d]
+    np.testing.assert_array_equal(h, want)
+
+
+def test_sink_act_reduces_to_logistic_silu():
+    """up = 1 and gamma = 1: h = bf16(g * logistic(g)), within half a bf16 ulp
+    of the library logistic function."""
+    scipy_special = pytest.importorskip("scipy.special")
+    rng = np.random.default_rng(5)
+    n, d, T = 2, 8, 3
+    gate_bits = f32_to_bf16_bits(rng.normal(0, 3, (T, n * d)).astype(np.float32))
+    g = bf16_bits_to_f32(gate_bits).astype(np.float64)
+    gu = np.concatenate([gate_bits, f32_to_bf16_bits(np.ones((T, n * d), np.float32))], 1)
+    h = bf16_bits_to_f32(oracle.sink_act(gu, np.ones((T, n), np.float32), n, d)).astype(np.float64)
+    exact = g * scipy_special.expit(g)
+    assert np.all(np.abs(h - exact) <= np.abs(exact) * 2.0 ** -8 + 1e-30)

@@ -42,6 +42,9 @@ WORKLOADS = {
     "moe": "MoE-LoRA: E=64, top-8 of softmax(N(0,1)), D=2048, F=1408, 8 adapters rank 16, T=1024, "
            "w13 (gate+up) and w2",
     "moe_shared": "MoE-LoRA as 'moe' in the shared-outer layout (w13-A and w2-B expert dim 1)",
+    "inkling_sink": "Inkling sink experts at decode: T=256, d_model 2048, 2 sink experts of d_mlp 1408: "
+                    "w13 LoRA (2048 -> 2x2816) + SiLU(gate)*up*gamma + w2 LoRA (2816 -> 2048), "
+                    "8 adapters rank 16, scale 2, 10% -1",
 }
 
 
@@ -58,11 +61,17 @@ def make_case(name):
         return gen.moe()
     if name == "moe_shared":
         return gen.moe(shared_outer=True)
+    if name == "inkling_sink":
+        return gen.inkling_sink()
     raise ValueError(name)
 
 
 def is_moe(name):
     return name.startswith("moe")
+
+
+def is_sink(name):
+    return name == "inkling_sink"
 
 
 def apply_kernels(name, policy):
@@ -74,6 +83,8 @@ def apply_kernels(name, policy):
         k = "cluster_lora_kernel (one pass, cluster DSMEM reduction)"
     else:
         k = "bgmv_shrink_kernel + bgmv_expand_kernel (chained by programmatic dependent launch)"
+    if is_sink(name):
+        return k + " on w13, sink_act_kernel, the same on w2"
     if name == "prefill_gate_up" and policy != 1:
         k = "sgmv_shrink_kernel + sgmv_expand_kernel (tcgen05, 128-row runs); short tiles: " + k
     return k + (" for w13 and w2" if is_moe(name) else "")
@@ -93,6 +104,17 @@ def dense_algorithmic_bytes(c):
     B = int(r.sum()) * c.out_total * 2
     return dict(x=n * c.H * 2, A=A, B=B, y=2 * n * c.out_total * 2, idx=c.T * 4,
                 total=n * c.H * 2 + A + B + 2 * n * c.out_total * 2 + c.T * 4, active=n)
+
+
+def sink_algorithmic_bytes(c):
+    """w13 apply + activation (gate_up read, h written, gammas) + w2 apply
+    (its x rows are h rows)."""
+    a13 = dense_algorithmic_bytes(c.w13)
+    a2 = dense_algorithmic_bytes(c.w2)
+    W = c.n_experts * c.d_mlp
+    act = c.T * (2 * W * 2 + W * 2 + c.n_experts * 4)
+    total = a13["total"] + act + a2["total"] - a2["idx"]
+    return dict(total=total, idx=a13["idx"], active=a13["active"], act=act)
 
 
 def moe_algorithmic_bytes(c):
@@ -179,6 +201,15 @@ def oracle_step_fn(name, c):
             oracle.moe_meta(c.topk_ids, c.idx, c.L, c.E, c.enabled, c.ranks)
             oracle.moe_w13(c)
             oracle.moe_w2(c)
+        return step, c.T
+    if is_sink(name):
+        from heterogeneous_adapters_lora_gb300.inputs import f32_to_bf16_bits
+
+        def step():
+            oracle.dense_meta(c.w13.idx, c.w13.L, c.w13.enabled, c.w13.ranks)
+            y13, _ = oracle.dense_delta(c.w13)
+            h = oracle.sink_act(f32_to_bf16_bits(y13), c.gammas, c.n_experts, c.d_mlp)
+            oracle.dense_delta(c.w2, x=h)
         return step, c.T
     if name == "many_adapter_down":
         # bounded sample: the first 256 tokens (the oracle is per-token)
@@ -317,15 +348,17 @@ def run_gpu(args, rank, world, local_rank):
     name = args.workload
     c = make_case(name)
     moe = is_moe(name)
+    sink = is_sink(name)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    ab = moe_algorithmic_bytes(c) if moe else dense_algorithmic_bytes(c)
+    ab = moe_algorithmic_bytes(c) if moe else (sink_algorithmic_bytes(c) if sink else dense_algorithmic_bytes(c))
     foot = ab["total"]
     n_rot = max(1, math.ceil(2 * l2 / max(foot, 1)))
     n_rot = min(n_rot, args.max_copies)
 
     runs = []
     for _ in range(n_rot):
-        runs.append(Hn.MoERun(c, device=dev) if moe else Hn.DenseRun(c, device=dev))
+        runs.append(Hn.MoERun(c, device=dev) if moe else (Hn.SinkRun(c, device=dev) if sink
+                                                          else Hn.DenseRun(c, device=dev)))
     torch.cuda.synchronize(dev)
 
     def step(r):
@@ -440,6 +473,15 @@ def run_gpu(args, rank, world, local_rank):
             h_out = [torch.empty_like(r.ic1, device="cpu").pin_memory(),
                      torch.empty_like(r.ic3, device="cpu").pin_memory()]
             d_out = [r.ic1, r.ic3]
+        elif sink:
+            h_in = [torch.from_numpy(np.ascontiguousarray(c.w13.x).view(np.int16)).pin_memory(),
+                    torch.from_numpy(c.w13.idx).pin_memory(),
+                    torch.from_numpy(c.w13.y0.view(np.int16)).pin_memory(),
+                    torch.from_numpy(c.gammas).pin_memory(),
+                    torch.from_numpy(c.w2.y0.view(np.int16)).pin_memory()]
+            d_in = [r.r13.x, r.r13.idx, r.r13.y, r.gammas, r.r2.y]
+            h_out = [torch.empty_like(r.r2.y, device="cpu").pin_memory()]
+            d_out = [r.r2.y]
         else:
             h_in = [torch.from_numpy(np.ascontiguousarray(c.x).view(np.int16)).pin_memory(),
                     torch.from_numpy(c.idx).pin_memory(),

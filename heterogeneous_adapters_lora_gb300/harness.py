@@ -199,3 +199,42 @@ class MoERun:
             self.close()
         except Exception:
             pass
+
+
+class SinkRun:
+    """An Inkling sink-expert case on the GPU: the w13 and w2 pools, one batch
+    metadata (built against the w13 pool: both pools hold the same slots),
+    base gate_up, gammas, h and the w2 output."""
+
+    def __init__(self, case, device="cuda"):
+        self.case = case
+        self.r13 = DenseRun(case.w13, device=device)
+        self.r2 = DenseRun(case.w2, device=device)
+        W = case.n_experts * case.d_mlp
+        self.W = W
+        self.gammas = torch.from_numpy(case.gammas).to(device)
+        self.h = torch.zeros((case.T, W), dtype=torch.int16, device=device)
+
+    def build_meta(self):
+        self.r13.build_meta()
+
+    def apply(self):
+        c = self.case
+        m = self.r13.mb.meta
+        L.lora_apply_slices(self.r13.pool, m, self.r13.x, c.w13.H, self.r13.y, 2 * self.W, self.r13.ws,
+                            self.r13.ws_bytes)
+        L.lora_sink_experts_act(self.r13.y, 2 * self.W, self.gammas, c.n_experts, c.T, c.n_experts, c.d_mlp,
+                                self.h, self.W)
+        L.lora_apply_slices(self.r2.pool, m, self.h, self.W, self.r2.y, c.w2.out_total,
+                            self.r2.ws, self.r2.ws_bytes)
+
+    def step(self):
+        self.build_meta()
+        self.apply()
+
+    def status(self) -> int:
+        return self.r13.status() | self.r2.status()
+
+    def close(self):
+        self.r13.close()
+        self.r2.close()

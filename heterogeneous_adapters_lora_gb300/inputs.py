@@ -354,5 +354,45 @@ def moe(shared_outer: bool = False, base: str = "zero", T: int = 1024) -> MoECas
                     shared_outer=shared_outer, base=base)
 
 
+class SinkCase:
+    """Inkling sink experts around their two LoRA layers: w13 (gate_up, two
+    slices of n*d_mlp) and w2 (n*d_mlp -> d_model) share one batch (idx)."""
+
+    def __init__(self, name, w13: DenseCase, w2: DenseCase, n_experts: int, d_mlp: int, gammas: np.ndarray):
+        self.name = name
+        self.w13 = w13            # y0 = base gate_up (bf16 bits), x = the layer input
+        self.w2 = w2              # y0 = base w2 output; x unused (the input is h)
+        self.n_experts = n_experts
+        self.d_mlp = d_mlp
+        self.gammas = gammas      # [T][n_experts] fp32
+        self.T = w13.T
+
+
+def sink_case(*, name="sink", T: int, D: int, n_experts: int, d_mlp: int, L: int, R: int, seed: int,
+              p_none: float = 0.1, std: float = 0.1) -> SinkCase:
+    """Seeded sink-expert case: x, A, B ~ N(0, std); base gate_up ~ N(0, 1);
+    base w2 output ~ N(0, 0.02); gammas uniform in [0.5, 1.5]."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    W = n_experts * d_mlp
+    idx = rng.integers(0, L, size=T).astype(np.int32)
+    idx[rng.random(T) < p_none] = -1
+    scales = np.full(L, 2.0, np.float32)
+    w13 = dense_case(name=name + "_w13", T=T, H=D, out_dims=(W, W), L=L, R=R, seed=seed + 1, scales=scales,
+                     idx=idx, std=std)
+    w13.y0 = _normal_bf16(rng, (T, 2 * W), 1.0)
+    w2 = dense_case(name=name + "_w2", T=T, H=W, out_dims=(D,), L=L, R=R, seed=seed + 2, scales=scales,
+                    idx=idx, std=std)
+    w2.y0 = _normal_bf16(rng, (T, D), 0.02)
+    gammas = rng.uniform(0.5, 1.5, size=(T, n_experts)).astype(np.float32)
+    return SinkCase(name, w13, w2, n_experts, d_mlp, gammas)
+
+
+def inkling_sink(T: int = 256) -> SinkCase:
+    """Sink experts at decode: 256 tokens, d_model 2048, 2 sink experts of
+    d_mlp 1408 (gate_up 2048 -> 2 x 2816, w2 2816 -> 2048), 8 slots of rank 16,
+    scale 2.0, 10% of tokens without an adapter."""
+    return sink_case(name="inkling_sink", T=T, D=2048, n_experts=2, d_mlp=1408, L=8, R=16, seed=1006)
+
+
 def preset(n: int, **kw):
     return {1: tiny, 2: decode_qkv, 3: prefill_gate_up, 4: many_adapter_down, 5: moe}[n](**kw)

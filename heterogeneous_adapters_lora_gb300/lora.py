@@ -91,6 +91,7 @@ EXPORTS = {
     "lora_set_spin_limit": (None, [c_i32]),
     "lora_set_kernel_policy": (None, [c_i32]),
     "lora_kernel_launch_count": (ctypes.c_ulonglong, []),
+    "lora_sink_experts_act": (c_i32, [c_vp, c_i64, c_vp, c_i64, c_i32, c_i32, c_i32, c_vp, c_i64, c_vp]),
     "lora_status_string": (ctypes.c_char_p, [c_i32]),
 }
 
@@ -258,6 +259,13 @@ def lora_set_spin_limit(max_polls: int):
 
 def lora_set_kernel_policy(policy: int):
     lib().lora_set_kernel_policy(int(policy))
+
+
+def lora_sink_experts_act(gate_up, ld_gate_up, gammas, ld_gammas, T, n_experts, d_mlp, h, ld_h, stream=None):
+    """Inkling sink-expert activation between the w13 and w2 LoRA layers."""
+    _check(lib().lora_sink_experts_act(ptr(gate_up), int(ld_gate_up), ptr(gammas), int(ld_gammas), int(T),
+                                       int(n_experts), int(d_mlp), ptr(h), int(ld_h), stream_ptr(stream)),
+           "lora_sink_experts_act")
 
 
 def lora_kernel_launch_count() -> int:

@@ -351,6 +351,22 @@ LORA_API lora_status_t lora_get_device_status(const lora_pool_t *pool, void *str
  * give up at once (to exercise the error path).  Process-wide. */
 LORA_API void lora_set_spin_limit(int32_t max_polls);
 
+/* Inkling sink experts between their two LoRA-wrapped linear layers (Inkling
+ * LoRA PR report, InklingSinkExpertsLinear.forward and _gamma_expand).  With
+ * W = n_experts * d_mlp, gate_up is the w13 output [T][ld_gate_up] bf16
+ * (base + LoRA delta: gate in columns [0, W), up in [W, 2W)), gammas is
+ * [T][ld_gammas] fp32 (one factor per token and expert) and h is the w2 input
+ * [T][ld_h] bf16:
+ *   h[t][c] = bf16( bf16( bf16(silu(gate[t][c])) * up[t][c] ) * gammas[t][c / d_mlp] )
+ * The caller owns every buffer (device memory); asynchronous on the stream.
+ * Errors (synchronous): LORA_ERR_INVALID_ARG for a null or misaligned pointer
+ * (gate_up and h 16-byte aligned, gammas 4-byte aligned), T < 0,
+ * n_experts < 1, d_mlp < 1, W not a multiple of 8, ld_gate_up < 2W or not a
+ * multiple of 8, ld_h < W or not a multiple of 8, ld_gammas < n_experts. */
+LORA_API lora_status_t lora_sink_experts_act(const void *gate_up, int64_t ld_gate_up, const float *gammas,
+                                             int64_t ld_gammas, int32_t T, int32_t n_experts, int32_t d_mlp,
+                                             void *h, int64_t ld_h, void *stream);
+
 /* Kernel selection for lora_apply_slices / lora_moe_apply (process-wide):
  * 0 = automatic (tcgen05 for long contiguous runs of a rank-64 dense pool;
  *     otherwise the split shrink/expand kernels when the workspace holds

@@ -225,14 +225,14 @@ __global__ void __launch_bounds__(kSThreads) bgmv_shrink_kernel(const __grid_con
     }
 }
 
-// ---------------------------------------------------------------- shrink, slot-major
+// ---------------------------------------------------------------- shrink, key-major
 //
-// For small pools whose slots are mostly active (decode batches): one CTA per
-// (slot a, slice j, hidden chunk c).  The slot's A rows of the chunk do not
-// depend on this batch's metadata, so they are requested before the kernel
-// waits for the metadata build; then every 16-row tile of the slot's rows is
-// multiplied against them (A read once per slot, not once per tile).  The
-// partials land where the per-tile shrink would put them.
+// For pools whose keys (slot, or slot x expert for MoE) are mostly busy in
+// the batch: one CTA per (key, slice j, hidden chunk c).  The key's A rows of
+// the chunk do not depend on this batch's metadata, so they are requested
+// before the kernel waits for the metadata build; then every 16-row tile of
+// the key's rows is multiplied against them (A read once per key, not once
+// per tile).  The partials land where the per-tile shrink would put them.
 
 __global__ void __launch_bounds__(kSThreads) bgmv_shrink_slot_kernel(const __grid_constant__ SArgs p) {
     extern __shared__ __align__(128) char smem[];
@@ -241,9 +241,10 @@ __global__ void __launch_bounds__(kSThreads) bgmv_shrink_slot_kernel(const __gri
     const int XS = p.x_stages;  // 1 or 2
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, c4 = lane & 3;
-    const int c = blockIdx.x % p.NC, j = (blockIdx.x / p.NC) % p.n_slices, a = blockIdx.x / (p.NC * p.n_slices);
+    const int c = blockIdx.x % p.NC, j = (blockIdx.x / p.NC) % p.n_slices, key = blockIdx.x / (p.NC * p.n_slices);
+    const int a = key / p.E, e = key - a * p.E;
     const int hb = c * p.HC, he = min(p.in_dim, hb + p.HC), len = he - hb;
-    const uint16_t *Ab = p.A[j] + (long long)a * p.A_ss[j];
+    const uint16_t *Ab = p.A[j] + (long long)a * p.A_ss[j] + (long long)e * p.A_es[j];
     uint16_t *as = (uint16_t *)(smem + p.off_a);
     // tables written before the metadata build started (never by it): read through L2
     const int r = (__ldcg(p.enabled + a) != 0) ? __ldcg(p.rank + a) : 0;
@@ -267,7 +268,7 @@ __global__ void __launch_bounds__(kSThreads) bgmv_shrink_slot_kernel(const __gri
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
-    const int cnt = p.key_count[a], off = p.key_offset[a];
+    const int cnt = p.key_count[key], off = p.key_offset[key];
     const int n_t = (cnt + kTileRows - 1) / kTileRows;
 
     auto load_x = [&](int t) {  // x rows of tile t into stage t % XS (warp 0)
@@ -547,6 +548,7 @@ __global__ void __launch_bounds__(kThreads) bgmv_expand_kernel(const __grid_cons
 size_t a128(size_t x) { return (x + 127) & ~(size_t)127; }
 
 int g_split_configured[64];
+int g_key_major_waves = 8;  // most waves of the key-major shrink grid
 
 // Hidden chunks of a shrink item: ~32 KB of A rows at full rank, >= 256
 // columns, at most 8.
@@ -633,17 +635,18 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     LORA_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_e, bgmv_expand_kernel, kThreads, e_smem));
     const long long e_slots = (long long)pool->num_sms * (occ_e < 1 ? 1 : occ_e);
 
-    // slot-major shrink for dense batches of a small pool: the slot's A chunk
-    // is fetched while the metadata is still being built
-    const int L = pool->desc.max_loras;
+    // key-major shrink when the batch keeps most keys busy and the grid is a
+    // few waves at most: the key's A chunk is fetched while the metadata is
+    // still being built, and read once per key
+    const int L = pr.n_keys;
     const size_t x_stage = a128((size_t)kTileRows * (HC + 8) * 2);
     const int x_stages = a128((size_t)R8 * (HC + 8) * 2) + 2 * x_stage + red_bytes <= 100 * 1024 ? 2 : 1;
     const size_t slot_smem = a128((size_t)R8 * (HC + 8) * 2) + x_stages * x_stage + red_bytes;
-    bool slot_major = pr.E == 1 && pr.count_idx == 3 && pr.rows >= 2 * L && slot_smem <= 100 * 1024;
+    bool slot_major = pr.count_idx == 3 && pr.rows >= 2 * L && slot_smem <= 100 * 1024;
     if (slot_major) {
         int o = 0;
         LORA_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, bgmv_shrink_slot_kernel, kSThreads, slot_smem));
-        slot_major = (long long)L * ns * NC <= (long long)o * pool->num_sms;
+        slot_major = (long long)L * ns * NC <= (long long)g_key_major_waves * o * pool->num_sms;
     }
 
     SArgs sa;

@@ -162,14 +162,18 @@ __global__ void __launch_bounds__(kThreads, 1) build_meta_kernel(MetaArgs a) {
                     key = row_key(a, act, row, s, &bad);
                 }
             }
-            const unsigned peers = key_peers(key, a.key_bits);
-            const int leader = __ffs(peers) - 1;
-            if (v && lane == leader) {
-                hist[warp * NK1 + key] += __popc(peers);
-                if (a.K == 1 && key < NK) {  // the rows of a warp step are consecutive
-                    atomicMin(&tmin[key], base + leader);
-                    atomicMax(&tmax[key], base + 31 - __clz(peers));
+            if (a.K == 1) {
+                const unsigned peers = key_peers(key, a.key_bits);
+                const int leader = __ffs(peers) - 1;
+                if (v && lane == leader) {
+                    hist[warp * NK1 + key] += __popc(peers);
+                    if (key < NK) {  // the rows of a warp step are consecutive
+                        atomicMin(&tmin[key], base + leader);
+                        atomicMax(&tmax[key], base + 31 - __clz(peers));
+                    }
                 }
+            } else if (v) {
+                atomicAdd(&hist[warp * NK1 + key], 1);  // counts only: order does not matter here
             }
             __syncwarp();
         }
@@ -198,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1) build_meta_kernel(MetaArgs a) {
     int *tiles = gidx + NK1;
     int *lt_cnt = tiles + NK1;
     int *st_cnt = lt_cnt + NK1;
-    int *wt = misc + 40;         // [5][32] per-warp totals, then their exclusive offsets
+    int *wt = misc + 40;         // [5][32] per-warp totals
     {
         const int per = (NK1 + nthreads - 1) / nthreads;
         const int b0 = min(NK1, tid * per), b1 = min(NK1, b0 + per);
@@ -228,25 +232,21 @@ __global__ void __launch_bounds__(kThreads, 1) build_meta_kernel(MetaArgs a) {
             for (int q = 0; q < 5; ++q) wt[q * 32 + warp] = inc[q];
         }
         __syncthreads();
-        if (warp == 0) {
-            const int nw = nthreads / 32;
-#pragma unroll
-            for (int q = 0; q < 5; ++q) {
-                const int v0 = lane < nw ? wt[q * 32 + lane] : 0;
-                int x = v0;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int v = __shfl_up_sync(0xffffffffu, x, o);
-                    if (lane >= o) x += v;
-                }
-                if (lane < nw) wt[q * 32 + lane] = x - v0;
-                if (lane == 31 && q > 0) misc[31 + q] = x;  // groups, tiles, long tiles, short tiles
-            }
-        }
-        __syncthreads();
+        // every warp sums the totals of the warps before it (no single-warp phase)
+        const int nw = nthreads / 32;
         int ex[5];
 #pragma unroll
-        for (int q = 0; q < 5; ++q) ex[q] = wt[q * 32 + warp] + inc[q] - sv5[q];
+        for (int q = 0; q < 5; ++q) {
+            int before = lane < warp ? wt[q * 32 + lane] : 0;
+            int all = lane < nw ? wt[q * 32 + lane] : 0;
+#pragma unroll
+            for (int o = 16; o; o >>= 1) {
+                before += __shfl_xor_sync(0xffffffffu, before, o);
+                all += __shfl_xor_sync(0xffffffffu, all, o);
+            }
+            ex[q] = before + inc[q] - sv5[q];
+            if (tid == 0 && q > 0) misc[31 + q] = all;  // groups, tiles, long tiles, short tiles
+        }
         for (int b = b0; b < b1; ++b) {
             const int c = b < NK ? cnt[b] : 0;
             const bool run = c > 0 && a.K == 1 && c >= LORA_LONG_MIN && tmax[b] - tmin[b] == c - 1;

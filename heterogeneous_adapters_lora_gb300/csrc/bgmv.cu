@@ -72,7 +72,7 @@ struct EArgs {
     long long ld_out;
     const float *part;
     int rows;
-    int n_oc;
+    int n_oc, oc_w;          // output column chunks per tile and their width
     int ys_stride, vr_stride;
     int off_b, off_ys, off_vh, off_vl;
     int *status;
@@ -406,7 +406,7 @@ __global__ void __launch_bounds__(kThreads) bgmv_expand_kernel(const __grid_cons
         const int a = key / p.E, e = key - a * p.E;
         const int r = p.rank[a];
         const int rs = (r + 7) & ~7;
-        const int ob = oc * kOC, oe = min(p.out_total, ob + kOC);
+        const int ob = oc * p.oc_w, oe = min(p.out_total, ob + p.oc_w);
         __syncthreads();  // the previous item's stores have been issued and its buffers read
         if (tid < n) s_rows[tid] = p.sorted[row0 + tid];
         __syncthreads();
@@ -446,37 +446,39 @@ __global__ void __launch_bounds__(kThreads) bgmv_expand_kernel(const __grid_cons
         while (j0 + 1 < ns && ob >= p.out_off[j0 + 1]) ++j0;
         int j1 = j0;
         while (j1 + 1 < ns && oe > p.out_off[j1 + 1]) ++j1;
-        const int per_t = (j1 - j0 + 1) * p.R8 / 4;
+        // 16 rows x 8 threads, 4 ranks per thread and step: no divisions
+        const int tq = tid >> 3, lq = tid & 7;
         const long long cstride = (long long)ns * p.rows * p.R8 / 4;
-        for (int i = tid; i < kTileRows * per_t; i += kThreads) {
-            const int t = i / per_t, q = i - t * per_t;
-            const int jj = j0 + (q * 4) / p.R8, k = (q * 4) % p.R8;
-            float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (t < n) {
-                const float4 *src = (const float4 *)(p.part + ((long long)jj * p.rows + row0 + t) * p.R8 + k);
-                for (int cc = 0; cc < nc; ++cc) {
-                    const float4 v = __ldcg(src + cc * cstride);
-                    s4.x += v.x;
-                    s4.y += v.y;
-                    s4.z += v.z;
-                    s4.w += v.w;
+        for (int jj = j0; jj <= j1; ++jj) {
+            for (int k = lq * 4; k < p.R8; k += 32) {
+                float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (tq < n) {
+                    const float4 *src =
+                        (const float4 *)(p.part + ((long long)jj * p.rows + row0 + tq) * p.R8 + k);
+                    for (int cc = 0; cc < nc; ++cc) {
+                        const float4 v = __ldcg(src + cc * cstride);
+                        s4.x += v.x;
+                        s4.y += v.y;
+                        s4.z += v.z;
+                        s4.w += v.w;
+                    }
+                    const float w = s_w[tq];
+                    s4.x *= w;
+                    s4.y *= w;
+                    s4.z *= w;
+                    s4.w *= w;
                 }
-                const float w = s_w[t];
-                s4.x *= w;
-                s4.y *= w;
-                s4.z *= w;
-                s4.w *= w;
+                const __nv_bfloat162 h01 = __floats2bfloat162_rn(s4.x, s4.y);
+                const __nv_bfloat162 h23 = __floats2bfloat162_rn(s4.z, s4.w);
+                const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+                uint2 hv, lv;
+                hv.x = *(const uint32_t *)&h01;
+                hv.y = *(const uint32_t *)&h23;
+                lv.x = pack_bf16x2(s4.x - f01.x, s4.y - f01.y);
+                lv.y = pack_bf16x2(s4.z - f23.x, s4.w - f23.y);
+                *(uint2 *)(vh + tq * p.vr_stride + jj * p.R8 + k) = hv;
+                *(uint2 *)(vl + tq * p.vr_stride + jj * p.R8 + k) = lv;
             }
-            const __nv_bfloat162 h01 = __floats2bfloat162_rn(s4.x, s4.y);
-            const __nv_bfloat162 h23 = __floats2bfloat162_rn(s4.z, s4.w);
-            const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
-            uint2 hv, lv;
-            hv.x = *(const uint32_t *)&h01;
-            hv.y = *(const uint32_t *)&h23;
-            lv.x = pack_bf16x2(s4.x - f01.x, s4.y - f01.y);
-            lv.y = pack_bf16x2(s4.z - f23.x, s4.w - f23.y);
-            *(uint2 *)(vh + t * p.vr_stride + jj * p.R8 + k) = hv;
-            *(uint2 *)(vl + t * p.vr_stride + jj * p.R8 + k) = lv;
         }
         __syncthreads();
         mbar_wait(&bbar, phase, p.spin_limit, p.status);
@@ -626,7 +628,9 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     const size_t s_smem = smem_for(SC);
     // expand shared memory: B rows, y rows, v hi/lo
     const int vr_stride = ns * R8 + 8;
-    const size_t e_b = a128((size_t)kOC * R8 * 2 + 32), e_y = a128((size_t)kTileRows * (kOC + 8) * 2);
+    // 512 output columns per expand item for small ranks (fewer items, less fixed work per column)
+    const int oc_w = R8 <= 32 ? 512 : kOC;
+    const size_t e_b = a128((size_t)oc_w * R8 * 2 + 32), e_y = a128((size_t)kTileRows * (oc_w + 8) * 2);
     const size_t e_v = a128((size_t)kTileRows * vr_stride * 2);
     const size_t e_smem = e_b + e_y + 2 * e_v;
 
@@ -713,8 +717,9 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     ea.ld_out = pr.ld_out;
     ea.part = sa.part;
     ea.rows = pr.rows;
-    ea.n_oc = lora_ceil_div(out_total, kOC);
-    ea.ys_stride = kOC + 8;
+    ea.oc_w = oc_w;
+    ea.n_oc = lora_ceil_div(out_total, oc_w);
+    ea.ys_stride = oc_w + 8;
     ea.vr_stride = vr_stride;
     ea.off_b = 0;
     ea.off_ys = (int)e_b;

@@ -373,6 +373,8 @@ __global__ void __launch_bounds__(kSThreads) bgmv_shrink_slot_kernel(const __gri
 // first item's B rows and y rows are requested before the shrink is waited
 // for; the metadata was complete before the shrink started.
 
+// KS: the most 16-rank k steps of any slot (ceil(R8 / 16), 1..4).
+template <int KS>
 __global__ void __launch_bounds__(kThreads) bgmv_expand_kernel(const __grid_constant__ EArgs p) {
     extern __shared__ __align__(128) char smem[];
     __shared__ __align__(8) uint64_t bbar, ybar;
@@ -485,49 +487,92 @@ __global__ void __launch_bounds__(kThreads) bgmv_expand_kernel(const __grid_cons
         mbar_wait(&ybar, phase, p.spin_limit, p.status);
 
         const int nob = (oe - ob) >> 3;
-        const int ksteps = (rs + 15) >> 4;
-        // two 8-column blocks per pass: their loads are issued before either MMA chain
+        const int ksteps = (rs + 15) >> 4;  // <= KS
+        // The v fragments (hi, lo) depend only on the slice and the k step: kept in
+        // registers while a warp's blocks stay in one slice.  Two 8-column blocks per
+        // pass, so their B loads and MMA chains overlap.
+        uint32_t hf[KS][4], lf[KS][4];
+        int cur = -1;
+        auto load_v = [&](int jj, uint32_t (&hh)[KS][4], uint32_t (&ll)[KS][4]) {
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                if (ks < ksteps) {
+                    const int col = jj * p.R8 + ks * 16 + (lane >> 4) * 8;
+                    ldsm_x4(vh + arow * p.vr_stride + col, hh[ks][0], hh[ks][1], hh[ks][2], hh[ks][3]);
+                    ldsm_x4(vl + arow * p.vr_stride + col, ll[ks][0], ll[ks][1], ll[ks][2], ll[ks][3]);
+                    if (ks * 16 + 8 >= rs) hh[ks][2] = hh[ks][3] = ll[ks][2] = ll[ks][3] = 0u;
+                }
+            }
+        };
+        int jA = j0;
 #pragma unroll 1
         for (int ob8 = warp; ob8 < nob; ob8 += 2 * kWarps) {
             const int obB = ob8 + kWarps;
             const bool hasB = obB < nob;
-            int jA = j0, jB = j0;
             while (jA + 1 < ns && ob + ob8 * 8 >= p.out_off[jA + 1]) ++jA;
+            int jB = jA;
             while (jB + 1 < ns && ob + obB * 8 >= p.out_off[jB + 1]) ++jB;
+            if (jA != cur) {
+                load_v(jA, hf, lf);
+                cur = jA;
+            }
             float dA[4] = {0.f, 0.f, 0.f, 0.f}, dB[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int ks = 0; ks < ksteps; ++ks) {
-                const int k0 = ks * 16;
-                const bool tail = k0 + 8 >= rs;
-                uint32_t h[4], l[4], b[2], hB[4], lB[4], bB[2];
-                const int colA = jA * p.R8 + k0 + (lane >> 4) * 8, colB = jB * p.R8 + k0 + (lane >> 4) * 8;
-                ldsm_x4(vh + arow * p.vr_stride + colA, h[0], h[1], h[2], h[3]);
-                ldsm_x4(vl + arow * p.vr_stride + colA, l[0], l[1], l[2], l[3]);
-                ldsm_x2(bs + (ob8 * 8 + (lane & 7)) * rs + k0 + ((lane >> 3) & 1) * 8, b[0], b[1]);
-                if (hasB) {
-                    ldsm_x4(vh + arow * p.vr_stride + colB, hB[0], hB[1], hB[2], hB[3]);
-                    ldsm_x4(vl + arow * p.vr_stride + colB, lB[0], lB[1], lB[2], lB[3]);
-                    ldsm_x2(bs + (obB * 8 + (lane & 7)) * rs + k0 + ((lane >> 3) & 1) * 8, bB[0], bB[1]);
+            if (jB == jA || !hasB) {
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks) {
+                    if (ks < ksteps) {
+                        const int k0 = ks * 16;
+                        uint32_t b[2], bB[2];
+                        ldsm_x2(bs + (ob8 * 8 + (lane & 7)) * rs + k0 + ((lane >> 3) & 1) * 8, b[0], b[1]);
+                        if (hasB) ldsm_x2(bs + (obB * 8 + (lane & 7)) * rs + k0 + ((lane >> 3) & 1) * 8, bB[0], bB[1]);
+                        if (k0 + 8 >= rs) b[1] = bB[1] = 0u;
+                        mma16816(dA, hf[ks][0], hf[ks][1], hf[ks][2], hf[ks][3], b[0], b[1]);
+                        if (hasB) mma16816(dB, hf[ks][0], hf[ks][1], hf[ks][2], hf[ks][3], bB[0], bB[1]);
+                        mma16816(dA, lf[ks][0], lf[ks][1], lf[ks][2], lf[ks][3], b[0], b[1]);
+                        if (hasB) mma16816(dB, lf[ks][0], lf[ks][1], lf[ks][2], lf[ks][3], bB[0], bB[1]);
+                    }
                 }
-                if (tail) h[2] = h[3] = l[2] = l[3] = b[1] = hB[2] = hB[3] = lB[2] = lB[3] = bB[1] = 0u;
-                mma16816(dA, h[0], h[1], h[2], h[3], b[0], b[1]);
-                if (hasB) mma16816(dB, hB[0], hB[1], hB[2], hB[3], bB[0], bB[1]);
-                mma16816(dA, l[0], l[1], l[2], l[3], b[0], b[1]);
-                if (hasB) mma16816(dB, lB[0], lB[1], lB[2], lB[3], bB[0], bB[1]);
+            } else {  // the pair straddles a slice boundary: A with this slice's v, then B with the next
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks) {
+                    if (ks < ksteps) {
+                        const int k0 = ks * 16;
+                        uint32_t b[2];
+                        ldsm_x2(bs + (ob8 * 8 + (lane & 7)) * rs + k0 + ((lane >> 3) & 1) * 8, b[0], b[1]);
+                        if (k0 + 8 >= rs) b[1] = 0u;
+                        mma16816(dA, hf[ks][0], hf[ks][1], hf[ks][2], hf[ks][3], b[0], b[1]);
+                        mma16816(dA, lf[ks][0], lf[ks][1], lf[ks][2], lf[ks][3], b[0], b[1]);
+                    }
+                }
+                load_v(jB, hf, lf);
+                cur = jB;
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks) {
+                    if (ks < ksteps) {
+                        const int k0 = ks * 16;
+                        uint32_t bB[2];
+                        ldsm_x2(bs + (obB * 8 + (lane & 7)) * rs + k0 + ((lane >> 3) & 1) * 8, bB[0], bB[1]);
+                        if (k0 + 8 >= rs) bB[1] = 0u;
+                        mma16816(dB, hf[ks][0], hf[ks][1], hf[ks][2], hf[ks][3], bB[0], bB[1]);
+                        mma16816(dB, lf[ks][0], lf[ks][1], lf[ks][2], lf[ks][3], bB[0], bB[1]);
+                    }
+                }
             }
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
                 if (q == 1 && !hasB) break;
-                const float *d = q ? dB : dA;
                 const int ocol = (q ? obB : ob8) * 8 + 2 * c4;
+                const float d0 = q ? dB[0] : dA[0], d1 = q ? dB[1] : dA[1];
+                const float d2 = q ? dB[2] : dA[2], d3 = q ? dB[3] : dA[3];
                 if (g < n) {
                     uint32_t *yp = (uint32_t *)(ys + g * p.ys_stride + ocol);
                     const uint32_t u = *yp;
-                    *yp = pack_bf16x2(bf16lo(u) + d[0], bf16hi(u) + d[1]);
+                    *yp = pack_bf16x2(bf16lo(u) + d0, bf16hi(u) + d1);
                 }
                 if (g + 8 < n) {
                     uint32_t *yp = (uint32_t *)(ys + (g + 8) * p.ys_stride + ocol);
                     const uint32_t u = *yp;
-                    *yp = pack_bf16x2(bf16lo(u) + d[2], bf16hi(u) + d[3]);
+                    *yp = pack_bf16x2(bf16lo(u) + d2, bf16hi(u) + d3);
                 }
             }
         }
@@ -589,7 +634,13 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     if (!g_split_configured[dev]) {
         LORA_CUDA_TRY(cudaFuncSetAttribute(bgmv_shrink_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            200 * 1024));
-        LORA_CUDA_TRY(cudaFuncSetAttribute(bgmv_expand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        LORA_CUDA_TRY(cudaFuncSetAttribute(bgmv_expand_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           200 * 1024));
+        LORA_CUDA_TRY(cudaFuncSetAttribute(bgmv_expand_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           200 * 1024));
+        LORA_CUDA_TRY(cudaFuncSetAttribute(bgmv_expand_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           200 * 1024));
+        LORA_CUDA_TRY(cudaFuncSetAttribute(bgmv_expand_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            200 * 1024));
         LORA_CUDA_TRY(cudaFuncSetAttribute(bgmv_shrink_slot_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            200 * 1024));
@@ -636,7 +687,10 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
 
     const long long s_slots = (long long)pool->num_sms * (occ < 1 ? 1 : occ);
     int occ_e = 0;
-    LORA_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_e, bgmv_expand_kernel, kThreads, e_smem));
+    const int KS = (R8 + 15) / 16;
+    void (*expand_fn)(EArgs) = KS == 1 ? bgmv_expand_kernel<1> : KS == 2 ? bgmv_expand_kernel<2>
+                             : KS == 3 ? bgmv_expand_kernel<3> : bgmv_expand_kernel<4>;
+    LORA_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_e, expand_fn, kThreads, e_smem));
     const long long e_slots = (long long)pool->num_sms * (occ_e < 1 ? 1 : occ_e);
 
     // key-major shrink when the batch keeps most keys busy and the grid is a
@@ -766,7 +820,7 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.gridDim = dim3((unsigned)(e_items < 4 * e_slots ? e_items : 4 * e_slots), 1, 1);
     cfg.dynamicSmemBytes = e_smem;
-    LORA_CUDA_TRY(cudaLaunchKernelEx(&cfg, bgmv_expand_kernel, ea));
+    LORA_CUDA_TRY(cudaLaunchKernelEx(&cfg, expand_fn, ea));
     lora_note_launch();
     *launched = true;
     return LORA_OK;

@@ -79,12 +79,58 @@ struct EArgs {
     int spin_limit;
 };
 
+// MMA part of a shrink stage: warp w takes the k steps i = w (mod 4) of the
+// stage for every 8-rank block of the slot, so each x fragment is loaded once
+// and feeds nnb independent accumulator chains.
+__device__ __forceinline__ void shrink_stage_mma(const uint16_t *xs, int xs_stride, const uint16_t *as,
+                                                 int as_stride, int len, int nnb, int warp, int lane,
+                                                 float (&acc)[8][4]) {
+    const int steps = (len + 15) >> 4;
+    const uint16_t *xq = xs + ((lane & 7) + ((lane >> 3) & 1) * 8) * xs_stride + (lane >> 4) * 8;
+    const uint16_t *aq = as + (lane & 7) * as_stride + ((lane >> 3) & 1) * 8;
+    for (int i = warp; i < steps; i += kSWarps) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(xq + i * 16, a0, a1, a2, a3);
+        const bool tail = i * 16 + 8 >= len;
+        if (tail) a2 = a3 = 0u;
+#pragma unroll
+        for (int nb = 0; nb < 8; ++nb) {
+            if (nb < nnb) {
+                uint32_t b0, b1;
+                ldsm_x2(aq + nb * 8 * as_stride + i * 16, b0, b1);
+                if (tail) b1 = 0u;
+                mma16816(acc[nb], a0, a1, a2, a3, b0, b1);
+            }
+        }
+    }
+}
+
+// Writes a warp's accumulators (rows < n, ranks < r) into its [16][R8] slice of red.
+__device__ __forceinline__ void shrink_store_red(float *red, int R8, int nnb, int r, int n, int warp, int lane,
+                                                 const float (&acc)[8][4]) {
+    const int g = lane >> 2, c4 = lane & 3;
+    float *base = red + warp * kTileRows * R8;
+#pragma unroll
+    for (int nb = 0; nb < 8; ++nb) {
+        if (nb < nnb) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int k = nb * 8 + 2 * c4 + h;
+                if (k < r) {
+                    if (g < n) base[g * R8 + k] = acc[nb][h];
+                    if (g + 8 < n) base[(g + 8) * R8 + k] = acc[nb][2 + h];
+                }
+            }
+        }
+    }
+}
+
 // ---------------------------------------------------------------- shrink
 //
 // Items (16-row tile, slice j, hidden chunk c), strided over a grid of at
 // most a few waves.  Two stages of [16 x rows][r A rows] x SC columns, rows
-// padded by 16 bytes so ldmatrix reads are free of bank conflicts; units
-// (8-rank column block, hidden split) spread over the 4 warps, <= 2 each.
+// padded by 16 bytes so ldmatrix reads are free of bank conflicts; the MMAs
+// as in shrink_stage_mma, the four warps' partial sums added in shared memory.
 
 __global__ void __launch_bounds__(kSThreads) bgmv_shrink_kernel(const __grid_constant__ SArgs p) {
     extern __shared__ __align__(128) char smem[];
@@ -142,49 +188,18 @@ __global__ void __launch_bounds__(kSThreads) bgmv_shrink_kernel(const __grid_con
         }
 
         const int nnb = (r + 7) >> 3;
-        int hsplit = 1;
-        while (nnb * hsplit * 2 <= 2 * kSWarps && hsplit < 4) hsplit *= 2;
-        const int units = nnb * hsplit;
-        float acc[2][4], acc2[2][4];
+        float acc[8][4];
 #pragma unroll
-        for (int u = 0; u < 2; ++u)
+        for (int u = 0; u < 8; ++u)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) acc[u][i] = acc2[u][i] = 0.f;
+            for (int q = 0; q < 4; ++q) acc[u][q] = 0.f;
         for (int s = 0; s < n_sub; ++s) {
             const int st = (gs + s) & 1;
             mbar_wait(&full[st], (uint32_t)(((gs + s) >> 1) & 1), p.spin_limit, p.status);
             const int len = min(p.SC, he - hb - s * p.SC);
-            const int steps = (len + 15) >> 4;
             const uint16_t *xs = (const uint16_t *)(smem + p.off_x + st * p.x_stage_bytes);
             const uint16_t *as = (const uint16_t *)(smem + p.off_a + st * p.a_stage_bytes);
-#pragma unroll
-            for (int ui = 0; ui < 2; ++ui) {
-                const int u = warp + ui * kSWarps;
-                if (u < units) {
-                    const int nb = u / hsplit, hs = u - nb * hsplit;
-                    const uint16_t *xq = xs + ((lane & 7) + ((lane >> 3) & 1) * 8) * p.xs_stride + (lane >> 4) * 8;
-                    const uint16_t *aq = as + (nb * 8 + (lane & 7)) * p.as_stride + ((lane >> 3) & 1) * 8;
-                    int i = hs;
-                    // two independent accumulator chains
-                    for (; i + hsplit < steps; i += 2 * hsplit) {
-                        uint32_t a0, a1, a2, a3, b0, b1, e0, e1, e2, e3, f0, f1;
-                        ldsm_x4(xq + i * 16, a0, a1, a2, a3);
-                        ldsm_x2(aq + i * 16, b0, b1);
-                        ldsm_x4(xq + (i + hsplit) * 16, e0, e1, e2, e3);
-                        ldsm_x2(aq + (i + hsplit) * 16, f0, f1);
-                        if ((i + hsplit) * 16 + 8 >= len) e2 = e3 = f1 = 0u;
-                        mma16816(acc[ui], a0, a1, a2, a3, b0, b1);
-                        mma16816(acc2[ui], e0, e1, e2, e3, f0, f1);
-                    }
-                    if (i < steps) {
-                        uint32_t a0, a1, a2, a3, b0, b1;
-                        ldsm_x4(xq + i * 16, a0, a1, a2, a3);
-                        ldsm_x2(aq + i * 16, b0, b1);
-                        if (i * 16 + 8 >= len) a2 = a3 = b1 = 0u;
-                        mma16816(acc[ui], a0, a1, a2, a3, b0, b1);
-                    }
-                }
-            }
+            shrink_stage_mma(xs, p.xs_stride, as, p.as_stride, len, nnb, warp, lane, acc);
             __syncthreads();
             if (warp == 0 && s + 2 < n_sub) {
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -193,33 +208,18 @@ __global__ void __launch_bounds__(kSThreads) bgmv_shrink_kernel(const __grid_con
         }
         gs += n_sub;
 
-        // partials of this chunk: [hsplit][16][R8] in shared memory, summed over
-        // the hidden split, then one row of R8 floats per token to global memory
-        for (int i = tid; i < hsplit * kTileRows * p.R8; i += kSThreads) red[i] = 0.f;
+        // partials of this chunk: [4 warps][16][R8] in shared memory, summed
+        // over the warps, then one row of R8 floats per token to global memory
+        for (int i = tid; i < kSWarps * kTileRows * p.R8; i += kSThreads) red[i] = 0.f;
         __syncthreads();
-#pragma unroll
-        for (int ui = 0; ui < 2; ++ui) {
-            const int u = warp + ui * kSWarps;
-            if (u < units) {
-                const int nb = u / hsplit, hs = u - nb * hsplit;
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int k = nb * 8 + 2 * c4 + h;
-                    if (k < r) {
-                        float *dst = red + (hs * kTileRows) * p.R8 + k;
-                        if (g < n) dst[g * p.R8] = acc[ui][h] + acc2[ui][h];
-                        if (g + 8 < n) dst[(g + 8) * p.R8] = acc[ui][2 + h] + acc2[ui][2 + h];
-                    }
-                }
-            }
-        }
+        shrink_store_red(red, p.R8, nnb, r, n, warp, lane, acc);
         __syncthreads();
         // this chunk's partial: part[c][j][row0 + t][k]
         float *dst = p.part + ((long long)c * p.n_slices + j) * p.rows * p.R8 + (long long)row0 * p.R8;
         for (int i = tid; i < n * p.R8; i += kSThreads) {
             const int t = i / p.R8, k = i - t * p.R8;
             float sum = 0.f;
-            for (int hs = 0; hs < hsplit; ++hs) sum += red[(hs * kTileRows + t) * p.R8 + k];
+            for (int w = 0; w < kSWarps; ++w) sum += red[(w * kTileRows + t) * p.R8 + k];
             dst[i] = sum;
         }
     }
@@ -289,79 +289,31 @@ __global__ void __launch_bounds__(kSThreads) bgmv_shrink_slot_kernel(const __gri
     mbar_wait(&abar, 0, p.spin_limit, p.status);  // also before any exit: no copy may be in flight
 
     const int nnb = (r + 7) >> 3;
-    int hsplit = 1;
-    while (nnb * hsplit * 2 <= 2 * kSWarps && hsplit < 4) hsplit *= 2;
-    const int units = nnb * hsplit;
-    const int steps = (len + 15) >> 4;
     float *red = (float *)(smem + p.off_red);
     for (int t = 0; t < n_t; ++t) {
         const int st = t % XS, row0 = off + t * kTileRows, n = min(kTileRows, cnt - t * kTileRows);
         mbar_wait(&xbar[st], (uint32_t)((t / XS) & 1), p.spin_limit, p.status);
         const uint16_t *xs = (const uint16_t *)(smem + p.off_x + st * p.x_stage_bytes);
-        float acc[2][2][4];
+        float acc[8][4];
 #pragma unroll
-        for (int u = 0; u < 2; ++u)
+        for (int u = 0; u < 8; ++u)
 #pragma unroll
-            for (int q = 0; q < 2; ++q)
-#pragma unroll
-                for (int i = 0; i < 4; ++i) acc[u][q][i] = 0.f;
-#pragma unroll
-        for (int ui = 0; ui < 2; ++ui) {
-            const int u = warp + ui * kSWarps;
-            if (u < units) {
-                const int nb = u / hsplit, hs = u - nb * hsplit;
-                const uint16_t *xq = xs + ((lane & 7) + ((lane >> 3) & 1) * 8) * p.xs_stride + (lane >> 4) * 8;
-                const uint16_t *aq = as + (nb * 8 + (lane & 7)) * p.as_stride + ((lane >> 3) & 1) * 8;
-                int i = hs;
-                // two independent accumulator chains
-                for (; i + hsplit < steps; i += 2 * hsplit) {
-                    uint32_t a0, a1, a2, a3, b0, b1, e0, e1, e2, e3, f0, f1;
-                    ldsm_x4(xq + i * 16, a0, a1, a2, a3);
-                    ldsm_x2(aq + i * 16, b0, b1);
-                    ldsm_x4(xq + (i + hsplit) * 16, e0, e1, e2, e3);
-                    ldsm_x2(aq + (i + hsplit) * 16, f0, f1);
-                    if ((i + hsplit) * 16 + 8 >= len) e2 = e3 = f1 = 0u;
-                    mma16816(acc[ui][0], a0, a1, a2, a3, b0, b1);
-                    mma16816(acc[ui][1], e0, e1, e2, e3, f0, f1);
-                }
-                if (i < steps) {
-                    uint32_t a0, a1, a2, a3, b0, b1;
-                    ldsm_x4(xq + i * 16, a0, a1, a2, a3);
-                    ldsm_x2(aq + i * 16, b0, b1);
-                    if (i * 16 + 8 >= len) a2 = a3 = b1 = 0u;
-                    mma16816(acc[ui][0], a0, a1, a2, a3, b0, b1);
-                }
-            }
-        }
+            for (int q = 0; q < 4; ++q) acc[u][q] = 0.f;
+        shrink_stage_mma(xs, p.xs_stride, as, p.as_stride, len, nnb, warp, lane, acc);
         __syncthreads();  // every warp is done with x stage st and with red of the previous tile
         if (warp == 0 && t + XS < n_t) {
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             load_x(t + XS);
         }
-        for (int i = tid; i < hsplit * kTileRows * p.R8; i += kSThreads) red[i] = 0.f;
+        for (int i = tid; i < kSWarps * kTileRows * p.R8; i += kSThreads) red[i] = 0.f;
         __syncthreads();
-#pragma unroll
-        for (int ui = 0; ui < 2; ++ui) {
-            const int u = warp + ui * kSWarps;
-            if (u < units) {
-                const int nb = u / hsplit, hs = u - nb * hsplit;
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int k = nb * 8 + 2 * c4 + h;
-                    if (k < r) {
-                        float *dst = red + (hs * kTileRows) * p.R8 + k;
-                        if (g < n) dst[g * p.R8] = acc[ui][0][h] + acc[ui][1][h];
-                        if (g + 8 < n) dst[(g + 8) * p.R8] = acc[ui][0][2 + h] + acc[ui][1][2 + h];
-                    }
-                }
-            }
-        }
+        shrink_store_red(red, p.R8, nnb, r, n, warp, lane, acc);
         __syncthreads();
         float *dst = p.part + ((long long)c * p.n_slices + j) * p.rows * p.R8 + (long long)row0 * p.R8;
         for (int i = tid; i < n * p.R8; i += kSThreads) {
             const int t2 = i / p.R8, k = i - t2 * p.R8;
             float sum = 0.f;
-            for (int hs = 0; hs < hsplit; ++hs) sum += red[(hs * kTileRows + t2) * p.R8 + k];
+            for (int w = 0; w < kSWarps; ++w) sum += red[(w * kTileRows + t2) * p.R8 + k];
             dst[i] = sum;
         }
     }

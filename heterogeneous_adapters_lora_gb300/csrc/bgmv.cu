@@ -81,44 +81,76 @@ struct EArgs {
 
 // MMA part of a shrink stage: warp w takes the k steps i = w (mod 4) of the
 // stage for every 8-rank block of the slot, so each x fragment is loaded once
-// and feeds nnb independent accumulator chains.
+// and feeds every block.  NBMAX is the pool's most 8-rank blocks (1, 2, 4, 8);
+// with few blocks, consecutive k steps go to SETS separate accumulators, so
+// SETS * nnb MMA chains are in flight instead of nnb.
+template <int NBMAX>
+struct ShrinkAcc {
+    static constexpr int SETS = NBMAX >= 8 ? 1 : (NBMAX >= 4 ? 2 : 4);
+    float v[SETS * NBMAX][4];
+};
+
+template <int NBMAX>
+__device__ __forceinline__ void shrink_acc_zero(ShrinkAcc<NBMAX> &acc) {
+#pragma unroll
+    for (int u = 0; u < ShrinkAcc<NBMAX>::SETS * NBMAX; ++u)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc.v[u][q] = 0.f;
+}
+
+template <int NBMAX>
 __device__ __forceinline__ void shrink_stage_mma(const uint16_t *xs, int xs_stride, const uint16_t *as,
                                                  int as_stride, int len, int nnb, int warp, int lane,
-                                                 float (&acc)[8][4]) {
+                                                 ShrinkAcc<NBMAX> &acc) {
+    constexpr int SETS = ShrinkAcc<NBMAX>::SETS;
     const int steps = (len + 15) >> 4;
     const uint16_t *xq = xs + ((lane & 7) + ((lane >> 3) & 1) * 8) * xs_stride + (lane >> 4) * 8;
     const uint16_t *aq = as + (lane & 7) * as_stride + ((lane >> 3) & 1) * 8;
-    for (int i = warp; i < steps; i += kSWarps) {
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4(xq + i * 16, a0, a1, a2, a3);
-        const bool tail = i * 16 + 8 >= len;
-        if (tail) a2 = a3 = 0u;
+    for (int i0 = warp; i0 < steps; i0 += kSWarps * SETS) {
 #pragma unroll
-        for (int nb = 0; nb < 8; ++nb) {
-            if (nb < nnb) {
-                uint32_t b0, b1;
-                ldsm_x2(aq + nb * 8 * as_stride + i * 16, b0, b1);
-                if (tail) b1 = 0u;
-                mma16816(acc[nb], a0, a1, a2, a3, b0, b1);
+        for (int q = 0; q < SETS; ++q) {
+            const int i = i0 + q * kSWarps;
+            if (i < steps) {
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(xq + i * 16, a0, a1, a2, a3);
+                const bool tail = i * 16 + 8 >= len;
+                if (tail) a2 = a3 = 0u;
+#pragma unroll
+                for (int nb = 0; nb < NBMAX; ++nb) {
+                    if (nb < nnb) {
+                        uint32_t b0, b1;
+                        ldsm_x2(aq + nb * 8 * as_stride + i * 16, b0, b1);
+                        if (tail) b1 = 0u;
+                        mma16816(acc.v[q * NBMAX + nb], a0, a1, a2, a3, b0, b1);
+                    }
+                }
             }
         }
     }
 }
 
 // Writes a warp's accumulators (rows < n, ranks < r) into its [16][R8] slice of red.
+template <int NBMAX>
 __device__ __forceinline__ void shrink_store_red(float *red, int R8, int nnb, int r, int n, int warp, int lane,
-                                                 const float (&acc)[8][4]) {
+                                                 const ShrinkAcc<NBMAX> &acc) {
+    constexpr int SETS = ShrinkAcc<NBMAX>::SETS;
     const int g = lane >> 2, c4 = lane & 3;
     float *base = red + warp * kTileRows * R8;
 #pragma unroll
-    for (int nb = 0; nb < 8; ++nb) {
+    for (int nb = 0; nb < NBMAX; ++nb) {
         if (nb < nnb) {
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int k = nb * 8 + 2 * c4 + h;
+                float lo = 0.f, hi = 0.f;
+#pragma unroll
+                for (int q = 0; q < SETS; ++q) {
+                    lo += acc.v[q * NBMAX + nb][h];
+                    hi += acc.v[q * NBMAX + nb][2 + h];
+                }
                 if (k < r) {
-                    if (g < n) base[g * R8 + k] = acc[nb][h];
-                    if (g + 8 < n) base[(g + 8) * R8 + k] = acc[nb][2 + h];
+                    if (g < n) base[g * R8 + k] = lo;
+                    if (g + 8 < n) base[(g + 8) * R8 + k] = hi;
                 }
             }
         }
@@ -132,6 +164,7 @@ __device__ __forceinline__ void shrink_store_red(float *red, int R8, int nnb, in
 // padded by 16 bytes so ldmatrix reads are free of bank conflicts; the MMAs
 // as in shrink_stage_mma, the four warps' partial sums added in shared memory.
 
+template <int NBMAX>
 __global__ void __launch_bounds__(kSThreads) bgmv_shrink_kernel(const __grid_constant__ SArgs p) {
     extern __shared__ __align__(128) char smem[];
     __shared__ __align__(8) uint64_t full[2];
@@ -188,11 +221,8 @@ __global__ void __launch_bounds__(kSThreads) bgmv_shrink_kernel(const __grid_con
         }
 
         const int nnb = (r + 7) >> 3;
-        float acc[8][4];
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) acc[u][q] = 0.f;
+        ShrinkAcc<NBMAX> acc;
+        shrink_acc_zero(acc);
         for (int s = 0; s < n_sub; ++s) {
             const int st = (gs + s) & 1;
             mbar_wait(&full[st], (uint32_t)(((gs + s) >> 1) & 1), p.spin_limit, p.status);
@@ -234,6 +264,7 @@ __global__ void __launch_bounds__(kSThreads) bgmv_shrink_kernel(const __grid_con
 // the key's rows is multiplied against them (A read once per key, not once
 // per tile).  The partials land where the per-tile shrink would put them.
 
+template <int NBMAX>
 __global__ void __launch_bounds__(kSThreads) bgmv_shrink_slot_kernel(const __grid_constant__ SArgs p) {
     extern __shared__ __align__(128) char smem[];
     __shared__ __align__(8) uint64_t abar, xbar[2];
@@ -294,11 +325,8 @@ __global__ void __launch_bounds__(kSThreads) bgmv_shrink_slot_kernel(const __gri
         const int st = t % XS, row0 = off + t * kTileRows, n = min(kTileRows, cnt - t * kTileRows);
         mbar_wait(&xbar[st], (uint32_t)((t / XS) & 1), p.spin_limit, p.status);
         const uint16_t *xs = (const uint16_t *)(smem + p.off_x + st * p.x_stage_bytes);
-        float acc[8][4];
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) acc[u][q] = 0.f;
+        ShrinkAcc<NBMAX> acc;
+        shrink_acc_zero(acc);
         shrink_stage_mma(xs, p.xs_stride, as, p.as_stride, len, nnb, warp, lane, acc);
         __syncthreads();  // every warp is done with x stage st and with red of the previous tile
         if (warp == 0 && t + XS < n_t) {
@@ -468,7 +496,9 @@ __global__ void __launch_bounds__(kThreads) bgmv_expand_kernel(const __grid_cons
                 load_v(jA, hf, lf);
                 cur = jA;
             }
+            // hi and lo parts into separate accumulators: four independent MMA chains
             float dA[4] = {0.f, 0.f, 0.f, 0.f}, dB[4] = {0.f, 0.f, 0.f, 0.f};
+            float eA[4] = {0.f, 0.f, 0.f, 0.f}, eB[4] = {0.f, 0.f, 0.f, 0.f};
             if (jB == jA || !hasB) {
 #pragma unroll
                 for (int ks = 0; ks < KS; ++ks) {
@@ -479,9 +509,11 @@ __global__ void __launch_bounds__(kThreads) bgmv_expand_kernel(const __grid_cons
                         if (hasB) ldsm_x2(bs + (obB * 8 + (lane & 7)) * rs + k0 + ((lane >> 3) & 1) * 8, bB[0], bB[1]);
                         if (k0 + 8 >= rs) b[1] = bB[1] = 0u;
                         mma16816(dA, hf[ks][0], hf[ks][1], hf[ks][2], hf[ks][3], b[0], b[1]);
-                        if (hasB) mma16816(dB, hf[ks][0], hf[ks][1], hf[ks][2], hf[ks][3], bB[0], bB[1]);
-                        mma16816(dA, lf[ks][0], lf[ks][1], lf[ks][2], lf[ks][3], b[0], b[1]);
-                        if (hasB) mma16816(dB, lf[ks][0], lf[ks][1], lf[ks][2], lf[ks][3], bB[0], bB[1]);
+                        mma16816(eA, lf[ks][0], lf[ks][1], lf[ks][2], lf[ks][3], b[0], b[1]);
+                        if (hasB) {
+                            mma16816(dB, hf[ks][0], hf[ks][1], hf[ks][2], hf[ks][3], bB[0], bB[1]);
+                            mma16816(eB, lf[ks][0], lf[ks][1], lf[ks][2], lf[ks][3], bB[0], bB[1]);
+                        }
                     }
                 }
             } else {  // the pair straddles a slice boundary: A with this slice's v, then B with the next
@@ -493,7 +525,7 @@ __global__ void __launch_bounds__(kThreads) bgmv_expand_kernel(const __grid_cons
                         ldsm_x2(bs + (ob8 * 8 + (lane & 7)) * rs + k0 + ((lane >> 3) & 1) * 8, b[0], b[1]);
                         if (k0 + 8 >= rs) b[1] = 0u;
                         mma16816(dA, hf[ks][0], hf[ks][1], hf[ks][2], hf[ks][3], b[0], b[1]);
-                        mma16816(dA, lf[ks][0], lf[ks][1], lf[ks][2], lf[ks][3], b[0], b[1]);
+                        mma16816(eA, lf[ks][0], lf[ks][1], lf[ks][2], lf[ks][3], b[0], b[1]);
                     }
                 }
                 load_v(jB, hf, lf);
@@ -506,9 +538,14 @@ __global__ void __launch_bounds__(kThreads) bgmv_expand_kernel(const __grid_cons
                         ldsm_x2(bs + (obB * 8 + (lane & 7)) * rs + k0 + ((lane >> 3) & 1) * 8, bB[0], bB[1]);
                         if (k0 + 8 >= rs) bB[1] = 0u;
                         mma16816(dB, hf[ks][0], hf[ks][1], hf[ks][2], hf[ks][3], bB[0], bB[1]);
-                        mma16816(dB, lf[ks][0], lf[ks][1], lf[ks][2], lf[ks][3], bB[0], bB[1]);
+                        mma16816(eB, lf[ks][0], lf[ks][1], lf[ks][2], lf[ks][3], bB[0], bB[1]);
                     }
                 }
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                dA[q] += eA[q];
+                dB[q] += eB[q];
             }
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
@@ -582,10 +619,20 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     int NC, HC;
     chunking(pr.in_dim, R8, &NC, &HC);
     if (!ws || ws_bytes < lora_split_ws_bytes(ns, pr.in_dim, R, pr.rows, 0) || !lora_aligned16(ws)) return LORA_OK;
+    // kernel instances for the pool's most 8-rank blocks (rounded up to 1, 2, 4, 8)
+    const int nbr = R8 / 8;
+    const int NBM = nbr <= 1 ? 1 : nbr <= 2 ? 2 : nbr <= 4 ? 4 : 8;
+    void (*shrink_fn)(SArgs) = NBM == 1 ? bgmv_shrink_kernel<1> : NBM == 2 ? bgmv_shrink_kernel<2>
+                             : NBM == 4 ? bgmv_shrink_kernel<4> : bgmv_shrink_kernel<8>;
+    void (*slot_fn)(SArgs) = NBM == 1 ? bgmv_shrink_slot_kernel<1> : NBM == 2 ? bgmv_shrink_slot_kernel<2>
+                           : NBM == 4 ? bgmv_shrink_slot_kernel<4> : bgmv_shrink_slot_kernel<8>;
     const int dev = pool->device < 64 ? pool->device : 63;
     if (!g_split_configured[dev]) {
-        LORA_CUDA_TRY(cudaFuncSetAttribute(bgmv_shrink_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           200 * 1024));
+        void (*const fns[])(SArgs) = {bgmv_shrink_kernel<1>, bgmv_shrink_kernel<2>, bgmv_shrink_kernel<4>,
+                                      bgmv_shrink_kernel<8>, bgmv_shrink_slot_kernel<1>, bgmv_shrink_slot_kernel<2>,
+                                      bgmv_shrink_slot_kernel<4>, bgmv_shrink_slot_kernel<8>};
+        for (auto f : fns)
+            LORA_CUDA_TRY(cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024));
         LORA_CUDA_TRY(cudaFuncSetAttribute(bgmv_expand_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            200 * 1024));
         LORA_CUDA_TRY(cudaFuncSetAttribute(bgmv_expand_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -593,8 +640,6 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
         LORA_CUDA_TRY(cudaFuncSetAttribute(bgmv_expand_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            200 * 1024));
         LORA_CUDA_TRY(cudaFuncSetAttribute(bgmv_expand_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           200 * 1024));
-        LORA_CUDA_TRY(cudaFuncSetAttribute(bgmv_shrink_slot_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            200 * 1024));
         g_split_configured[dev] = 1;
     }
@@ -611,7 +656,7 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     for (int sc = (HC < 1024 ? HC : 1024); sc >= 64; sc -= 64) {
         if (smem_for(sc) > 100 * 1024) continue;
         int o = 0;
-        LORA_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, bgmv_shrink_kernel, kSThreads, smem_for(sc)));
+        LORA_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, shrink_fn, kSThreads, smem_for(sc)));
         if (!first) {
             first = sc;
             first_occ = o;
@@ -655,7 +700,7 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     bool slot_major = pr.count_idx == 3 && pr.rows >= 2 * L && slot_smem <= 100 * 1024;
     if (slot_major) {
         int o = 0;
-        LORA_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, bgmv_shrink_slot_kernel, kSThreads, slot_smem));
+        LORA_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, slot_fn, kSThreads, slot_smem));
         slot_major = (long long)L * ns * NC <= (long long)g_key_major_waves * o * pool->num_sms;
     }
 
@@ -761,12 +806,12 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
         if ((size_t)sa.off_red + red_bytes > slot_smem) return LORA_ERR_INVALID_ARG;  // layout check
         cfg.gridDim = dim3((unsigned)(L * ns * NC), 1, 1);
         cfg.dynamicSmemBytes = slot_smem;
-        LORA_CUDA_TRY(cudaLaunchKernelEx(&cfg, bgmv_shrink_slot_kernel, sa));
+        LORA_CUDA_TRY(cudaLaunchKernelEx(&cfg, slot_fn, sa));
     } else {
         if ((size_t)sa.off_red + red_bytes > s_smem) return LORA_ERR_INVALID_ARG;  // layout check
         cfg.gridDim = dim3((unsigned)(s_items < 4 * s_slots ? s_items : 4 * s_slots), 1, 1);
         cfg.dynamicSmemBytes = s_smem;
-        LORA_CUDA_TRY(cudaLaunchKernelEx(&cfg, bgmv_shrink_kernel, sa));
+        LORA_CUDA_TRY(cudaLaunchKernelEx(&cfg, shrink_fn, sa));
     }
     lora_note_launch();
     cfg.blockDim = dim3(kThreads, 1, 1);

@@ -82,11 +82,12 @@ struct EArgs {
 // MMA part of a shrink stage: warp w takes the k steps i = w (mod 4) of the
 // stage for every 8-rank block of the slot, so each x fragment is loaded once
 // and feeds every block.  NBMAX is the pool's most 8-rank blocks (1, 2, 4, 8);
-// with few blocks, consecutive k steps go to SETS separate accumulators, so
-// SETS * nnb MMA chains are in flight instead of nnb.
+// consecutive k steps go to SETS separate accumulators, so SETS * nnb MMA
+// chains are in flight instead of nnb (a warp-level MMA has a latency of
+// hundreds of cycles here, so independent chains are what keeps it busy).
 template <int NBMAX>
 struct ShrinkAcc {
-    static constexpr int SETS = NBMAX >= 8 ? 1 : (NBMAX >= 4 ? 2 : 4);
+    static constexpr int SETS = NBMAX >= 8 ? 2 : (NBMAX >= 4 ? 4 : 8);  // 8-16 chains per warp
     float v[SETS * NBMAX][4];
 };
 
@@ -355,7 +356,7 @@ __global__ void __launch_bounds__(kSThreads) bgmv_shrink_slot_kernel(const __gri
 
 // KS: the most 16-rank k steps of any slot (ceil(R8 / 16), 1..4).
 template <int KS>
-__global__ void __launch_bounds__(kThreads) bgmv_expand_kernel(const __grid_constant__ EArgs p) {
+__global__ void __launch_bounds__(kThreads, 3) bgmv_expand_kernel(const __grid_constant__ EArgs p) {
     extern __shared__ __align__(128) char smem[];
     __shared__ __align__(8) uint64_t bbar, ybar;
     __shared__ int s_rows[kTileRows];
@@ -469,99 +470,109 @@ __global__ void __launch_bounds__(kThreads) bgmv_expand_kernel(const __grid_cons
         const int nob = (oe - ob) >> 3;
         const int ksteps = (rs + 15) >> 4;  // <= KS
         // The v fragments (hi, lo) depend only on the slice and the k step: kept in
-        // registers while a warp's blocks stay in one slice.  Two 8-column blocks per
-        // pass, so their B loads and MMA chains overlap.
+        // registers while a warp's blocks stay in one slice.  A warp-level MMA has
+        // a latency of hundreds of cycles here, so each pass issues the MMAs of up
+        // to 8 of the warp's 8-column blocks before it reads any result, and then
+        // does all their y updates (loads first, then stores).
         uint32_t hf[KS][4], lf[KS][4];
         int cur = -1;
-        auto load_v = [&](int jj, uint32_t (&hh)[KS][4], uint32_t (&ll)[KS][4]) {
+        auto load_v = [&](int jj) {
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
                 if (ks < ksteps) {
                     const int col = jj * p.R8 + ks * 16 + (lane >> 4) * 8;
-                    ldsm_x4(vh + arow * p.vr_stride + col, hh[ks][0], hh[ks][1], hh[ks][2], hh[ks][3]);
-                    ldsm_x4(vl + arow * p.vr_stride + col, ll[ks][0], ll[ks][1], ll[ks][2], ll[ks][3]);
-                    if (ks * 16 + 8 >= rs) hh[ks][2] = hh[ks][3] = ll[ks][2] = ll[ks][3] = 0u;
+                    ldsm_x4(vh + arow * p.vr_stride + col, hf[ks][0], hf[ks][1], hf[ks][2], hf[ks][3]);
+                    ldsm_x4(vl + arow * p.vr_stride + col, lf[ks][0], lf[ks][1], lf[ks][2], lf[ks][3]);
+                    if (ks * 16 + 8 >= rs) hf[ks][2] = hf[ks][3] = lf[ks][2] = lf[ks][3] = 0u;
                 }
             }
         };
+        const uint16_t *bq = bs + (lane & 7) * rs + ((lane >> 3) & 1) * 8;
         int jA = j0;
 #pragma unroll 1
-        for (int ob8 = warp; ob8 < nob; ob8 += 2 * kWarps) {
-            const int obB = ob8 + kWarps;
-            const bool hasB = obB < nob;
-            while (jA + 1 < ns && ob + ob8 * 8 >= p.out_off[jA + 1]) ++jA;
-            int jB = jA;
-            while (jB + 1 < ns && ob + obB * 8 >= p.out_off[jB + 1]) ++jB;
-            if (jA != cur) {
-                load_v(jA, hf, lf);
-                cur = jA;
+        for (int p0 = warp; p0 < nob; p0 += 8 * kWarps) {
+            int jq[8];
+            bool same = true;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const int o8 = p0 + q * kWarps;
+                jq[q] = jA;
+                if (o8 < nob) {
+                    while (jA + 1 < ns && ob + o8 * 8 >= p.out_off[jA + 1]) ++jA;
+                    jq[q] = jA;
+                    same = same && jq[q] == jq[0];
+                }
             }
-            // hi and lo parts into separate accumulators: four independent MMA chains
-            float dA[4] = {0.f, 0.f, 0.f, 0.f}, dB[4] = {0.f, 0.f, 0.f, 0.f};
-            float eA[4] = {0.f, 0.f, 0.f, 0.f}, eB[4] = {0.f, 0.f, 0.f, 0.f};
-            if (jB == jA || !hasB) {
+            float acc[8][4];
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+#pragma unroll
+                for (int e2 = 0; e2 < 4; ++e2) acc[q][e2] = 0.f;
+            if (same) {
+                if (jq[0] != cur) {
+                    load_v(jq[0]);
+                    cur = jq[0];
+                }
 #pragma unroll
                 for (int ks = 0; ks < KS; ++ks) {
                     if (ks < ksteps) {
-                        const int k0 = ks * 16;
-                        uint32_t b[2], bB[2];
-                        ldsm_x2(bs + (ob8 * 8 + (lane & 7)) * rs + k0 + ((lane >> 3) & 1) * 8, b[0], b[1]);
-                        if (hasB) ldsm_x2(bs + (obB * 8 + (lane & 7)) * rs + k0 + ((lane >> 3) & 1) * 8, bB[0], bB[1]);
-                        if (k0 + 8 >= rs) b[1] = bB[1] = 0u;
-                        mma16816(dA, hf[ks][0], hf[ks][1], hf[ks][2], hf[ks][3], b[0], b[1]);
-                        mma16816(eA, lf[ks][0], lf[ks][1], lf[ks][2], lf[ks][3], b[0], b[1]);
-                        if (hasB) {
-                            mma16816(dB, hf[ks][0], hf[ks][1], hf[ks][2], hf[ks][3], bB[0], bB[1]);
-                            mma16816(eB, lf[ks][0], lf[ks][1], lf[ks][2], lf[ks][3], bB[0], bB[1]);
+                        const bool tail = ks * 16 + 8 >= rs;
+                        uint32_t b[8][2];
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            if (p0 + q * kWarps < nob) {
+                                ldsm_x2(bq + (p0 + q * kWarps) * 8 * rs + ks * 16, b[q][0], b[q][1]);
+                                if (tail) b[q][1] = 0u;
+                                mma16816(acc[q], hf[ks][0], hf[ks][1], hf[ks][2], hf[ks][3], b[q][0], b[q][1]);
+                            }
+                        }
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            if (p0 + q * kWarps < nob)
+                                mma16816(acc[q], lf[ks][0], lf[ks][1], lf[ks][2], lf[ks][3], b[q][0], b[q][1]);
+                    }
+                }
+            } else {  // the pass crosses a slice boundary: block by block
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    if (p0 + q * kWarps < nob) {
+                        if (jq[q] != cur) {
+                            load_v(jq[q]);
+                            cur = jq[q];
+                        }
+#pragma unroll
+                        for (int ks = 0; ks < KS; ++ks) {
+                            if (ks < ksteps) {
+                                uint32_t b0, b1;
+                                ldsm_x2(bq + (p0 + q * kWarps) * 8 * rs + ks * 16, b0, b1);
+                                if (ks * 16 + 8 >= rs) b1 = 0u;
+                                mma16816(acc[q], hf[ks][0], hf[ks][1], hf[ks][2], hf[ks][3], b0, b1);
+                                mma16816(acc[q], lf[ks][0], lf[ks][1], lf[ks][2], lf[ks][3], b0, b1);
+                            }
                         }
                     }
                 }
-            } else {  // the pair straddles a slice boundary: A with this slice's v, then B with the next
+            }
+            uint32_t u0[8], u1[8];
 #pragma unroll
-                for (int ks = 0; ks < KS; ++ks) {
-                    if (ks < ksteps) {
-                        const int k0 = ks * 16;
-                        uint32_t b[2];
-                        ldsm_x2(bs + (ob8 * 8 + (lane & 7)) * rs + k0 + ((lane >> 3) & 1) * 8, b[0], b[1]);
-                        if (k0 + 8 >= rs) b[1] = 0u;
-                        mma16816(dA, hf[ks][0], hf[ks][1], hf[ks][2], hf[ks][3], b[0], b[1]);
-                        mma16816(eA, lf[ks][0], lf[ks][1], lf[ks][2], lf[ks][3], b[0], b[1]);
-                    }
-                }
-                load_v(jB, hf, lf);
-                cur = jB;
-#pragma unroll
-                for (int ks = 0; ks < KS; ++ks) {
-                    if (ks < ksteps) {
-                        const int k0 = ks * 16;
-                        uint32_t bB[2];
-                        ldsm_x2(bs + (obB * 8 + (lane & 7)) * rs + k0 + ((lane >> 3) & 1) * 8, bB[0], bB[1]);
-                        if (k0 + 8 >= rs) bB[1] = 0u;
-                        mma16816(dB, hf[ks][0], hf[ks][1], hf[ks][2], hf[ks][3], bB[0], bB[1]);
-                        mma16816(eB, lf[ks][0], lf[ks][1], lf[ks][2], lf[ks][3], bB[0], bB[1]);
-                    }
+            for (int q = 0; q < 8; ++q) {
+                const int ocol = (p0 + q * kWarps) * 8 + 2 * c4;
+                u0[q] = u1[q] = 0u;
+                if (p0 + q * kWarps < nob) {
+                    if (g < n) u0[q] = *(const uint32_t *)(ys + g * p.ys_stride + ocol);
+                    if (g + 8 < n) u1[q] = *(const uint32_t *)(ys + (g + 8) * p.ys_stride + ocol);
                 }
             }
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                dA[q] += eA[q];
-                dB[q] += eB[q];
-            }
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                if (q == 1 && !hasB) break;
-                const int ocol = (q ? obB : ob8) * 8 + 2 * c4;
-                const float d0 = q ? dB[0] : dA[0], d1 = q ? dB[1] : dA[1];
-                const float d2 = q ? dB[2] : dA[2], d3 = q ? dB[3] : dA[3];
-                if (g < n) {
-                    uint32_t *yp = (uint32_t *)(ys + g * p.ys_stride + ocol);
-                    const uint32_t u = *yp;
-                    *yp = pack_bf16x2(bf16lo(u) + d0, bf16hi(u) + d1);
-                }
-                if (g + 8 < n) {
-                    uint32_t *yp = (uint32_t *)(ys + (g + 8) * p.ys_stride + ocol);
-                    const uint32_t u = *yp;
-                    *yp = pack_bf16x2(bf16lo(u) + d2, bf16hi(u) + d3);
+            for (int q = 0; q < 8; ++q) {
+                const int ocol = (p0 + q * kWarps) * 8 + 2 * c4;
+                if (p0 + q * kWarps < nob) {
+                    if (g < n)
+                        *(uint32_t *)(ys + g * p.ys_stride + ocol) =
+                            pack_bf16x2(bf16lo(u0[q]) + acc[q][0], bf16hi(u0[q]) + acc[q][1]);
+                    if (g + 8 < n)
+                        *(uint32_t *)(ys + (g + 8) * p.ys_stride + ocol) =
+                            pack_bf16x2(bf16lo(u1[q]) + acc[q][2], bf16hi(u1[q]) + acc[q][3]);
                 }
             }
         }

@@ -85,6 +85,16 @@ struct EArgs {
 // consecutive k steps go to SETS separate accumulators, so SETS * nnb MMA
 // chains are in flight instead of nnb (a warp-level MMA has a latency of
 // hundreds of cycles here, so independent chains are what keeps it busy).
+// A rows of (slot a, expert e) for slice j, read from the parameters with
+// constant indices (a run-time index into a parameter array is slow).
+__device__ __forceinline__ const uint16_t *a_rows(const SArgs &p, int j, int a, int e) {
+    const uint16_t *r = p.A[0] + (long long)a * p.A_ss[0] + (long long)e * p.A_es[0];
+#pragma unroll
+    for (int q = 1; q < LORA_MAX_SLICES; ++q)
+        if (q == j) r = p.A[q] + (long long)a * p.A_ss[q] + (long long)e * p.A_es[q];
+    return r;
+}
+
 template <int NBMAX>
 struct ShrinkAcc {
     static constexpr int SETS = NBMAX >= 8 ? 2 : (NBMAX >= 4 ? 4 : 8);  // 8-16 chains per warp
@@ -193,7 +203,7 @@ __global__ void __launch_bounds__(kSThreads) bgmv_shrink_kernel(const __grid_con
         const int n = keyn & 31, key = keyn >> 5;
         const int a = key / p.E, e = key - a * p.E;
         const int r = p.rank[a];
-        const uint16_t *Ab = p.A[j] + (long long)a * p.A_ss[j] + (long long)e * p.A_es[j];
+        const uint16_t *Ab = a_rows(p, j, a, e);
         const int hb = c * p.HC, he = min(p.in_dim, hb + p.HC);
         const int n_sub = (he - hb + p.SC - 1) / p.SC;
         __syncthreads();  // the previous item is done with s_rows, the stages and red
@@ -276,7 +286,7 @@ __global__ void __launch_bounds__(kSThreads) bgmv_shrink_slot_kernel(const __gri
     const int c = blockIdx.x % p.NC, j = (blockIdx.x / p.NC) % p.n_slices, key = blockIdx.x / (p.NC * p.n_slices);
     const int a = key / p.E, e = key - a * p.E;
     const int hb = c * p.HC, he = min(p.in_dim, hb + p.HC), len = he - hb;
-    const uint16_t *Ab = p.A[j] + (long long)a * p.A_ss[j] + (long long)e * p.A_es[j];
+    const uint16_t *Ab = a_rows(p, j, a, e);
     uint16_t *as = (uint16_t *)(smem + p.off_a);
     // tables written before the metadata build started (never by it): read through L2
     const int r = (__ldcg(p.enabled + a) != 0) ? __ldcg(p.rank + a) : 0;
@@ -349,6 +359,27 @@ __global__ void __launch_bounds__(kSThreads) bgmv_shrink_slot_kernel(const __gri
 }
 
 // ---------------------------------------------------------------- expand
+
+// Slice of output column o (slices are contiguous and ascending).  The loop has
+// constant indices into the parameter array: an indexed parameter load with a
+// run-time index costs hundreds of cycles.
+__device__ __forceinline__ int slice_of(const EArgs &p, int o) {
+    int j = 0;
+#pragma unroll
+    for (int q = 1; q < LORA_MAX_SLICES; ++q)
+        if (q < p.n_slices && o >= p.out_off[q]) j = q;
+    return j;
+}
+
+__device__ __forceinline__ uint32_t lds32(const void *a) {
+    uint32_t v;
+    asm("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(a)));
+    return v;
+}
+__device__ __forceinline__ void sts32(void *a, uint32_t v) {
+    asm volatile("st.shared.u32 [%0], %1;" ::"r"(smem_u32(a)), "r"(v) : "memory");
+}
+
 //
 // Items (tile, 256 output columns), tile-major, strided over the grid.  The
 // first item's B rows and y rows are requested before the shrink is waited
@@ -405,14 +436,16 @@ __global__ void __launch_bounds__(kThreads, 3) bgmv_expand_kernel(const __grid_c
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             if (lane == 0) mbar_expect_tx(&bbar, (uint32_t)(oe - ob) * rs * 2);
             __syncwarp();
-            if (lane < ns) {
-                const int jj = lane;
-                const int s0 = max(ob, p.out_off[jj]), s1 = min(oe, p.out_off[jj] + p.out_w[jj]);
-                if (s1 > s0) {
-                    const uint16_t *Bj = p.B[jj] + (long long)a * p.B_ss[jj] +
-                                         (p.B_shared[jj] ? 0ll : (long long)e * p.out_w[jj] * rs);
-                    bulk_g2s(bs + (long long)(s0 - ob) * rs, Bj + (long long)(s0 - p.out_off[jj]) * rs,
-                             (uint32_t)(s1 - s0) * rs * 2, &bbar);
+#pragma unroll
+            for (int jj = 0; jj < LORA_MAX_SLICES; ++jj) {  // constant parameter indices
+                if (jj < ns && lane == jj) {
+                    const int s0 = max(ob, p.out_off[jj]), s1 = min(oe, p.out_off[jj] + p.out_w[jj]);
+                    if (s1 > s0) {
+                        const uint16_t *Bj = p.B[jj] + (long long)a * p.B_ss[jj] +
+                                             (p.B_shared[jj] ? 0ll : (long long)e * p.out_w[jj] * rs);
+                        bulk_g2s(bs + (long long)(s0 - ob) * rs, Bj + (long long)(s0 - p.out_off[jj]) * rs,
+                                 (uint32_t)(s1 - s0) * rs * 2, &bbar);
+                    }
                 }
             }
         }
@@ -425,10 +458,7 @@ __global__ void __launch_bounds__(kThreads, 3) bgmv_expand_kernel(const __grid_c
         __syncthreads();
         // v of the slices this item touches (chunk partials summed in order,
         // scaled) -> bf16 hi / lo, [16][vr_stride] at j * R8 + k
-        int j0 = 0;
-        while (j0 + 1 < ns && ob >= p.out_off[j0 + 1]) ++j0;
-        int j1 = j0;
-        while (j1 + 1 < ns && oe > p.out_off[j1 + 1]) ++j1;
+        const int j0 = slice_of(p, ob), j1 = slice_of(p, oe - 1);
         // 16 rows x 8 threads, 4 ranks per thread and step: no divisions
         const int tq = tid >> 3, lq = tid & 7;
         const long long cstride = (long long)ns * p.rows * p.R8 / 4;
@@ -488,19 +518,18 @@ __global__ void __launch_bounds__(kThreads, 3) bgmv_expand_kernel(const __grid_c
             }
         };
         const uint16_t *bq = bs + (lane & 7) * rs + ((lane >> 3) & 1) * 8;
-        int jA = j0;
 #pragma unroll 1
         for (int p0 = warp; p0 < nob; p0 += 8 * kWarps) {
             int jq[8];
             bool same = true;
+            const int jfirst = slice_of(p, ob + p0 * 8);
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
                 const int o8 = p0 + q * kWarps;
-                jq[q] = jA;
-                if (o8 < nob) {
-                    while (jA + 1 < ns && ob + o8 * 8 >= p.out_off[jA + 1]) ++jA;
-                    jq[q] = jA;
-                    same = same && jq[q] == jq[0];
+                jq[q] = jfirst;
+                if (j1 > j0 && o8 < nob) {
+                    jq[q] = slice_of(p, ob + o8 * 8);
+                    same = same && jq[q] == jfirst;
                 }
             }
             float acc[8][4];
@@ -523,9 +552,12 @@ __global__ void __launch_bounds__(kThreads, 3) bgmv_expand_kernel(const __grid_c
                             if (p0 + q * kWarps < nob) {
                                 ldsm_x2(bq + (p0 + q * kWarps) * 8 * rs + ks * 16, b[q][0], b[q][1]);
                                 if (tail) b[q][1] = 0u;
-                                mma16816(acc[q], hf[ks][0], hf[ks][1], hf[ks][2], hf[ks][3], b[q][0], b[q][1]);
                             }
                         }
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            if (p0 + q * kWarps < nob)
+                                mma16816(acc[q], hf[ks][0], hf[ks][1], hf[ks][2], hf[ks][3], b[q][0], b[q][1]);
 #pragma unroll
                         for (int q = 0; q < 8; ++q)
                             if (p0 + q * kWarps < nob)
@@ -559,8 +591,8 @@ __global__ void __launch_bounds__(kThreads, 3) bgmv_expand_kernel(const __grid_c
                 const int ocol = (p0 + q * kWarps) * 8 + 2 * c4;
                 u0[q] = u1[q] = 0u;
                 if (p0 + q * kWarps < nob) {
-                    if (g < n) u0[q] = *(const uint32_t *)(ys + g * p.ys_stride + ocol);
-                    if (g + 8 < n) u1[q] = *(const uint32_t *)(ys + (g + 8) * p.ys_stride + ocol);
+                    if (g < n) u0[q] = lds32(ys + g * p.ys_stride + ocol);
+                    if (g + 8 < n) u1[q] = lds32(ys + (g + 8) * p.ys_stride + ocol);
                 }
             }
 #pragma unroll
@@ -568,11 +600,10 @@ __global__ void __launch_bounds__(kThreads, 3) bgmv_expand_kernel(const __grid_c
                 const int ocol = (p0 + q * kWarps) * 8 + 2 * c4;
                 if (p0 + q * kWarps < nob) {
                     if (g < n)
-                        *(uint32_t *)(ys + g * p.ys_stride + ocol) =
-                            pack_bf16x2(bf16lo(u0[q]) + acc[q][0], bf16hi(u0[q]) + acc[q][1]);
+                        sts32(ys + g * p.ys_stride + ocol, pack_bf16x2(bf16lo(u0[q]) + acc[q][0], bf16hi(u0[q]) + acc[q][1]));
                     if (g + 8 < n)
-                        *(uint32_t *)(ys + (g + 8) * p.ys_stride + ocol) =
-                            pack_bf16x2(bf16lo(u1[q]) + acc[q][2], bf16hi(u1[q]) + acc[q][3]);
+                        sts32(ys + (g + 8) * p.ys_stride + ocol,
+                              pack_bf16x2(bf16lo(u1[q]) + acc[q][2], bf16hi(u1[q]) + acc[q][3]));
                 }
             }
         }

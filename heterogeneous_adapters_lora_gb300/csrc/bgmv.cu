@@ -386,8 +386,8 @@ __device__ __forceinline__ void sts32(void *a, uint32_t v) {
 // for; the metadata was complete before the shrink started.
 
 // KS: the most 16-rank k steps of any slot (ceil(R8 / 16), 1..4).
-template <int KS>
-__global__ void __launch_bounds__(kThreads, 3) bgmv_expand_kernel(const __grid_constant__ EArgs p) {
+template <int KS, int PW>
+__global__ void __launch_bounds__(kThreads, PW == 8 ? 3 : 5) bgmv_expand_kernel(const __grid_constant__ EArgs p) {
     extern __shared__ __align__(128) char smem[];
     __shared__ __align__(8) uint64_t bbar, ybar;
     __shared__ int s_rows[kTileRows];
@@ -502,8 +502,9 @@ __global__ void __launch_bounds__(kThreads, 3) bgmv_expand_kernel(const __grid_c
         // The v fragments (hi, lo) depend only on the slice and the k step: kept in
         // registers while a warp's blocks stay in one slice.  A warp-level MMA has
         // a latency of hundreds of cycles here, so each pass issues the MMAs of up
-        // to 8 of the warp's 8-column blocks before it reads any result, and then
-        // does all their y updates (loads first, then stores).
+        // to PW of the warp's 8-column blocks before it reads any result, and then
+        // does all their y updates (loads first, then stores).  PW = 8 for batches
+        // that fit one wave, 4 (fewer registers, more resident CTAs) otherwise.
         uint32_t hf[KS][4], lf[KS][4];
         int cur = -1;
         auto load_v = [&](int jj) {
@@ -519,12 +520,12 @@ __global__ void __launch_bounds__(kThreads, 3) bgmv_expand_kernel(const __grid_c
         };
         const uint16_t *bq = bs + (lane & 7) * rs + ((lane >> 3) & 1) * 8;
 #pragma unroll 1
-        for (int p0 = warp; p0 < nob; p0 += 8 * kWarps) {
-            int jq[8];
+        for (int p0 = warp; p0 < nob; p0 += PW * kWarps) {
+            int jq[PW];
             bool same = true;
             const int jfirst = slice_of(p, ob + p0 * 8);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
+            for (int q = 0; q < PW; ++q) {
                 const int o8 = p0 + q * kWarps;
                 jq[q] = jfirst;
                 if (j1 > j0 && o8 < nob) {
@@ -532,9 +533,9 @@ __global__ void __launch_bounds__(kThreads, 3) bgmv_expand_kernel(const __grid_c
                     same = same && jq[q] == jfirst;
                 }
             }
-            float acc[8][4];
+            float acc[PW][4];
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
+            for (int q = 0; q < PW; ++q)
 #pragma unroll
                 for (int e2 = 0; e2 < 4; ++e2) acc[q][e2] = 0.f;
             if (same) {
@@ -546,27 +547,27 @@ __global__ void __launch_bounds__(kThreads, 3) bgmv_expand_kernel(const __grid_c
                 for (int ks = 0; ks < KS; ++ks) {
                     if (ks < ksteps) {
                         const bool tail = ks * 16 + 8 >= rs;
-                        uint32_t b[8][2];
+                        uint32_t b[PW][2];
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) {
+                        for (int q = 0; q < PW; ++q) {
                             if (p0 + q * kWarps < nob) {
                                 ldsm_x2(bq + (p0 + q * kWarps) * 8 * rs + ks * 16, b[q][0], b[q][1]);
                                 if (tail) b[q][1] = 0u;
                             }
                         }
 #pragma unroll
-                        for (int q = 0; q < 8; ++q)
+                        for (int q = 0; q < PW; ++q)
                             if (p0 + q * kWarps < nob)
                                 mma16816(acc[q], hf[ks][0], hf[ks][1], hf[ks][2], hf[ks][3], b[q][0], b[q][1]);
 #pragma unroll
-                        for (int q = 0; q < 8; ++q)
+                        for (int q = 0; q < PW; ++q)
                             if (p0 + q * kWarps < nob)
                                 mma16816(acc[q], lf[ks][0], lf[ks][1], lf[ks][2], lf[ks][3], b[q][0], b[q][1]);
                     }
                 }
             } else {  // the pass crosses a slice boundary: block by block
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
+                for (int q = 0; q < PW; ++q) {
                     if (p0 + q * kWarps < nob) {
                         if (jq[q] != cur) {
                             load_v(jq[q]);
@@ -585,9 +586,9 @@ __global__ void __launch_bounds__(kThreads, 3) bgmv_expand_kernel(const __grid_c
                     }
                 }
             }
-            uint32_t u0[8], u1[8];
+            uint32_t u0[PW], u1[PW];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
+            for (int q = 0; q < PW; ++q) {
                 const int ocol = (p0 + q * kWarps) * 8 + 2 * c4;
                 u0[q] = u1[q] = 0u;
                 if (p0 + q * kWarps < nob) {
@@ -596,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 3) bgmv_expand_kernel(const __grid_c
                 }
             }
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
+            for (int q = 0; q < PW; ++q) {
                 const int ocol = (p0 + q * kWarps) * 8 + 2 * c4;
                 if (p0 + q * kWarps < nob) {
                     if (g < n)
@@ -675,14 +676,11 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
                                       bgmv_shrink_slot_kernel<4>, bgmv_shrink_slot_kernel<8>};
         for (auto f : fns)
             LORA_CUDA_TRY(cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024));
-        LORA_CUDA_TRY(cudaFuncSetAttribute(bgmv_expand_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           200 * 1024));
-        LORA_CUDA_TRY(cudaFuncSetAttribute(bgmv_expand_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           200 * 1024));
-        LORA_CUDA_TRY(cudaFuncSetAttribute(bgmv_expand_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           200 * 1024));
-        LORA_CUDA_TRY(cudaFuncSetAttribute(bgmv_expand_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           200 * 1024));
+        void (*const efns[])(EArgs) = {bgmv_expand_kernel<1, 8>, bgmv_expand_kernel<2, 8>, bgmv_expand_kernel<3, 8>,
+                                       bgmv_expand_kernel<4, 8>, bgmv_expand_kernel<1, 4>, bgmv_expand_kernel<2, 4>,
+                                       bgmv_expand_kernel<3, 4>, bgmv_expand_kernel<4, 4>};
+        for (auto f : efns)
+            LORA_CUDA_TRY(cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024));
         g_split_configured[dev] = 1;
     }
     // shrink shared memory: 2 stages of (16 + R8) rows x SC columns (rows
@@ -727,9 +725,15 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     const long long s_slots = (long long)pool->num_sms * (occ < 1 ? 1 : occ);
     int occ_e = 0;
     const int KS = (R8 + 15) / 16;
-    void (*expand_fn)(EArgs) = KS == 1 ? bgmv_expand_kernel<1> : KS == 2 ? bgmv_expand_kernel<2>
-                             : KS == 3 ? bgmv_expand_kernel<3> : bgmv_expand_kernel<4>;
+    // wide passes when the expand items fit about one wave of the wide kernel
+    void (*expand_fn)(EArgs) = KS == 1 ? bgmv_expand_kernel<1, 8> : KS == 2 ? bgmv_expand_kernel<2, 8>
+                             : KS == 3 ? bgmv_expand_kernel<3, 8> : bgmv_expand_kernel<4, 8>;
     LORA_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_e, expand_fn, kThreads, e_smem));
+    if (max_tiles * lora_ceil_div(out_total, oc_w) > (long long)pool->num_sms * (occ_e < 1 ? 1 : occ_e)) {
+        expand_fn = KS == 1 ? bgmv_expand_kernel<1, 4> : KS == 2 ? bgmv_expand_kernel<2, 4>
+                  : KS == 3 ? bgmv_expand_kernel<3, 4> : bgmv_expand_kernel<4, 4>;
+        LORA_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_e, expand_fn, kThreads, e_smem));
+    }
     const long long e_slots = (long long)pool->num_sms * (occ_e < 1 ? 1 : occ_e);
 
     // key-major shrink when the batch keeps most keys busy and the grid is a

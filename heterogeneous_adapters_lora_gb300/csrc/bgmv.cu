@@ -504,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, PW == 8 ? 3 : 5) bgmv_expand_kernel(
         // a latency of hundreds of cycles here, so each pass issues the MMAs of up
         // to PW of the warp's 8-column blocks before it reads any result, and then
         // does all their y updates (loads first, then stores).  PW = 8 for batches
-        // that fit one wave, 4 (fewer registers, more resident CTAs) otherwise.
+        // that fit two waves, 4 (fewer registers, more resident CTAs) otherwise.
         uint32_t hf[KS][4], lf[KS][4];
         int cur = -1;
         auto load_v = [&](int jj) {
@@ -725,11 +725,11 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     const long long s_slots = (long long)pool->num_sms * (occ < 1 ? 1 : occ);
     int occ_e = 0;
     const int KS = (R8 + 15) / 16;
-    // wide passes when the expand items fit about one wave of the wide kernel
+    // wide passes when the expand items fit two waves of the wide kernel
     void (*expand_fn)(EArgs) = KS == 1 ? bgmv_expand_kernel<1, 8> : KS == 2 ? bgmv_expand_kernel<2, 8>
                              : KS == 3 ? bgmv_expand_kernel<3, 8> : bgmv_expand_kernel<4, 8>;
     LORA_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_e, expand_fn, kThreads, e_smem));
-    if (max_tiles * lora_ceil_div(out_total, oc_w) > (long long)pool->num_sms * (occ_e < 1 ? 1 : occ_e)) {
+    if (max_tiles * lora_ceil_div(out_total, oc_w) > 2LL * pool->num_sms * (occ_e < 1 ? 1 : occ_e)) {
         expand_fn = KS == 1 ? bgmv_expand_kernel<1, 4> : KS == 2 ? bgmv_expand_kernel<2, 4>
                   : KS == 3 ? bgmv_expand_kernel<3, 4> : bgmv_expand_kernel<4, 4>;
         LORA_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_e, expand_fn, kThreads, e_smem));

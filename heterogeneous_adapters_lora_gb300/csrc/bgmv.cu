@@ -54,6 +54,7 @@ struct SArgs {
     // slot-major variant
     const int32_t *enabled, *key_count, *key_offset;
     int n_slots, x_stages;
+    int *ticket;             // [0] next item, [1] finished CTAs; zero between calls
 };
 
 struct EArgs {
@@ -75,9 +76,29 @@ struct EArgs {
     int n_oc, oc_w;          // output column chunks per tile and their width
     int ys_stride, vr_stride;
     int off_b, off_ys, off_vh, off_vl;
+    int *ticket;             // [0] next item, [1] finished CTAs; zero between calls
     int *status;
     int spin_limit;
 };
+
+// Dynamic work distribution: the CTAs of a one-wave grid take items from a
+// counter in the workspace; the last CTA to finish puts the counter back to
+// zero for the next call (calls that share a workspace do not overlap).
+__device__ __forceinline__ int take_item(int *ticket, int *s_item) {
+    if (threadIdx.x == 0) *s_item = atomicAdd(ticket, 1);
+    __syncthreads();
+    return *s_item;
+}
+__device__ __forceinline__ void finish_items(int *ticket) {
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(ticket + 1, 1) == (int)gridDim.x - 1) {
+            ticket[0] = 0;
+            ticket[1] = 0;
+            __threadfence();
+        }
+    }
+}
 
 // MMA part of a shrink stage: warp w takes the k steps i = w (mod 4) of the
 // stage for every 8-rank block of the slot, so each x fragment is loaded once
@@ -181,13 +202,13 @@ __global__ void __launch_bounds__(kSThreads) bgmv_shrink_kernel(const __grid_con
     __shared__ __align__(8) uint64_t full[2];
     __shared__ int s_rows[kTileRows];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int g = lane >> 2, c4 = lane & 3;
+
     const int per_tile = p.n_slices * p.NC;
 
+    __shared__ int s_item;
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int n_tiles = p.counters[p.count_idx];
     const int total = n_tiles * per_tile;
-    if ((int)blockIdx.x >= total) return;
     // the expand may launch and prefetch its weights and outputs now
     asm volatile("griddepcontrol.launch_dependents;");
     if (tid < 2) mbar_init(&full[tid], 1);
@@ -195,7 +216,7 @@ __global__ void __launch_bounds__(kSThreads) bgmv_shrink_kernel(const __grid_con
     float *red = (float *)(smem + p.off_red);
     int gs = 0;  // sub-stages consumed by this CTA so far (ring slot and phase)
 
-    for (int item = blockIdx.x; item < total; item += gridDim.x) {
+    for (int item = take_item(p.ticket, &s_item); item < total; item = take_item(p.ticket, &s_item)) {
         const int tile = item / per_tile, rem = item - tile * per_tile;
         const int j = rem / p.NC, c = rem - j * p.NC;
         const int row0 = p.tile_row0[tile];
@@ -264,6 +285,7 @@ __global__ void __launch_bounds__(kSThreads) bgmv_shrink_kernel(const __grid_con
             dst[i] = sum;
         }
     }
+    finish_items(p.ticket);
 }
 
 // ---------------------------------------------------------------- shrink, key-major
@@ -282,7 +304,7 @@ __global__ void __launch_bounds__(kSThreads) bgmv_shrink_slot_kernel(const __gri
     __shared__ int s_rows[2][kTileRows];
     const int XS = p.x_stages;  // 1 or 2
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int g = lane >> 2, c4 = lane & 3;
+
     const int c = blockIdx.x % p.NC, j = (blockIdx.x / p.NC) % p.n_slices, key = blockIdx.x / (p.NC * p.n_slices);
     const int a = key / p.E, e = key - a * p.E;
     const int hb = c * p.HC, he = min(p.in_dim, hb + p.HC), len = he - hb;
@@ -395,9 +417,9 @@ __global__ void __launch_bounds__(kThreads, PW == 8 ? 3 : 5) bgmv_expand_kernel(
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, c4 = lane & 3;
     const int ns = p.n_slices;
+    __shared__ int s_item;
     const int n_tiles = p.counters[p.count_idx];
     const int total = n_tiles * p.n_oc;
-    if ((int)blockIdx.x >= total) return;
     if (tid == 0) {
         mbar_init(&bbar, 1);
         mbar_init(&ybar, 1);
@@ -412,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, PW == 8 ? 3 : 5) bgmv_expand_kernel(
     const int nc = p.NC;
     uint32_t phase = 0;
 
-    for (int item = blockIdx.x; item < total; item += gridDim.x, phase ^= 1u) {
+    for (int item = take_item(p.ticket, &s_item); item < total; item = take_item(p.ticket, &s_item), phase ^= 1u) {
         const int tile = item / p.n_oc, oc = item - tile * p.n_oc;
         const int row0 = p.tile_row0[tile];
         const int keyn = p.tile_keyn[tile];
@@ -621,6 +643,7 @@ __global__ void __launch_bounds__(kThreads, PW == 8 ? 3 : 5) bgmv_expand_kernel(
             asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
         }
     }
+    finish_items(p.ticket);
     asm volatile("griddepcontrol.launch_dependents;");
 }
 
@@ -651,7 +674,7 @@ size_t lora_split_ws_bytes(int n_slices, int in_dim, int R, int rows, int max_ti
 }
 
 lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, void *ws, size_t ws_bytes,
-                               cudaStream_t s, bool *launched) {
+                               int *tickets, cudaStream_t s, bool *launched) {
     *launched = false;
     const int ns = pr.n_slices, R = pr.R, R8 = lora_round8(R);
     int out_total = 0;
@@ -661,7 +684,8 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     if (R8 > 2 * kSWarps * 8 || max_tiles <= 0) return LORA_OK;
     int NC, HC;
     chunking(pr.in_dim, R8, &NC, &HC);
-    if (!ws || ws_bytes < lora_split_ws_bytes(ns, pr.in_dim, R, pr.rows, 0) || !lora_aligned16(ws)) return LORA_OK;
+    if (!ws || ws_bytes < lora_split_ws_bytes(ns, pr.in_dim, R, pr.rows, 0) || !lora_aligned16(ws) || !tickets)
+        return LORA_OK;
     // kernel instances for the pool's most 8-rank blocks (rounded up to 1, 2, 4, 8)
     const int nbr = R8 / 8;
     const int NBM = nbr <= 1 ? 1 : nbr <= 2 ? 2 : nbr <= 4 ? 4 : 8;
@@ -743,7 +767,7 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     const size_t x_stage = a128((size_t)kTileRows * (HC + 8) * 2);
     const int x_stages = a128((size_t)R8 * (HC + 8) * 2) + 2 * x_stage + red_bytes <= 100 * 1024 ? 2 : 1;
     const size_t slot_smem = a128((size_t)R8 * (HC + 8) * 2) + x_stages * x_stage + red_bytes;
-    bool slot_major = pr.count_idx == 3 && pr.rows >= 2 * L && slot_smem <= 100 * 1024;
+    bool slot_major = pr.count_idx == 3 && pr.rows >= 4 * L && slot_smem <= 100 * 1024;
     if (slot_major) {
         int o = 0;
         LORA_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, slot_fn, kSThreads, slot_smem));
@@ -782,6 +806,7 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     sa.off_a = 2 * sa.x_stage_bytes;
     sa.off_red = sa.off_a + 2 * sa.a_stage_bytes;
     sa.part = (float *)ws;
+    sa.ticket = tickets;
     sa.rows = pr.rows;
     sa.status = pr.status;
     sa.spin_limit = pr.spin_limit;
@@ -813,6 +838,7 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     ea.out = pr.out;
     ea.ld_out = pr.ld_out;
     ea.part = sa.part;
+    ea.ticket = tickets + 2;
     ea.rows = pr.rows;
     ea.oc_w = oc_w;
     ea.n_oc = lora_ceil_div(out_total, oc_w);
@@ -835,7 +861,7 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     cfg.blockDim = dim3(kSThreads, 1, 1);
     cfg.stream = s;
     // grids of at most one wave; the kernels stride over their items
-    // grids of at most four waves; the kernels stride over their items
+    // one-wave grids (the key-major shrink: one CTA per item); CTAs take items from counters
     const long long e_items = max_tiles * ea.n_oc;
     if (slot_major) {
         sa.enabled = pool->d_enabled;
@@ -855,13 +881,13 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
         LORA_CUDA_TRY(cudaLaunchKernelEx(&cfg, slot_fn, sa));
     } else {
         if ((size_t)sa.off_red + red_bytes > s_smem) return LORA_ERR_INVALID_ARG;  // layout check
-        cfg.gridDim = dim3((unsigned)(s_items < 4 * s_slots ? s_items : 4 * s_slots), 1, 1);
+        cfg.gridDim = dim3((unsigned)(s_items < s_slots ? s_items : s_slots), 1, 1);
         cfg.dynamicSmemBytes = s_smem;
         LORA_CUDA_TRY(cudaLaunchKernelEx(&cfg, shrink_fn, sa));
     }
     lora_note_launch();
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.gridDim = dim3((unsigned)(e_items < 4 * e_slots ? e_items : 4 * e_slots), 1, 1);
+    cfg.gridDim = dim3((unsigned)(e_items < e_slots ? e_items : e_slots), 1, 1);
     cfg.dynamicSmemBytes = e_smem;
     LORA_CUDA_TRY(cudaLaunchKernelEx(&cfg, expand_fn, ea));
     lora_note_launch();

@@ -686,7 +686,7 @@ lora_status_t lora_dense_apply(const lora_pool_t *pool, const lora_meta_t *meta,
         bool launched = false;
         const LoraProblem pr = to_problem(g, meta, pool->desc.max_loras);
         if (g_lora_kernel_policy == 0 && have_split_region) {
-            st = lora_split_apply(pool, pr, scratch, scratch_bytes, s, &launched);
+            st = lora_split_apply(pool, pr, scratch, scratch_bytes, cv.ctrl + 2, s, &launched);
             if (st != LORA_OK || launched) return st;
         }
         st = lora_cluster_apply(pool, pr, s, &launched);
@@ -825,7 +825,7 @@ extern "C" lora_status_t lora_moe_apply(const lora_pool_t *pool, const lora_meta
         bool launched = false;
         const LoraProblem pr = to_problem(g, meta, keys);
         if (g_lora_kernel_policy == 0 && have_split_region) {
-            st = lora_split_apply(pool, pr, cv.data, cv.data_bytes, s, &launched);
+            st = lora_split_apply(pool, pr, cv.data, cv.data_bytes, cv.ctrl + 2, s, &launched);
             if (st != LORA_OK || launched) return st;
         }
         st = lora_cluster_apply(pool, pr, s, &launched);

@@ -128,8 +128,9 @@ bool lora_make_tmap_2d(CUtensorMap *m, const void *base, long long cols, long lo
 
 // Split shrink/expand kernels (bgmv.cu): workspace bytes and launcher.
 size_t lora_split_ws_bytes(int n_slices, int in_dim, int R, int rows, int max_tiles);
+// tickets: 4 ints of the workspace's zeroed control words (left zero again).
 lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, void *ws, size_t ws_bytes,
-                               cudaStream_t s, bool *launched);
+                               int *tickets, cudaStream_t s, bool *launched);
 
 // Tensor-core SGMV (sgmv.cu) for long contiguous runs of a dense pool.
 bool lora_sgmv_eligible(const lora_pool_t *pool);

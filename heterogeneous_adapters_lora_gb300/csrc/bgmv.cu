@@ -45,6 +45,7 @@ struct SArgs {
     const uint16_t *in;
     long long ld_in;
     int NC, HC, SC;          // hidden chunks, chunk length, stage length (elements)
+    int nst;                 // per-tile shrink: bulk-copy ring depth (2..4)
     int xs_stride, as_stride;
     int off_x, off_a, x_stage_bytes, a_stage_bytes, off_red;
     float *part;             // [NC][n_slices][rows][R8], unscaled
@@ -199,7 +200,7 @@ __device__ __forceinline__ void shrink_store_red(float *red, int R8, int nnb, in
 template <int NBMAX>
 __global__ void __launch_bounds__(kSThreads) bgmv_shrink_kernel(const __grid_constant__ SArgs p) {
     extern __shared__ __align__(128) char smem[];
-    __shared__ __align__(8) uint64_t full[2];
+    __shared__ __align__(8) uint64_t full[4];
     __shared__ int s_rows[kTileRows];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
@@ -211,7 +212,7 @@ __global__ void __launch_bounds__(kSThreads) bgmv_shrink_kernel(const __grid_con
     const int total = n_tiles * per_tile;
     // the expand may launch and prefetch its weights and outputs now
     asm volatile("griddepcontrol.launch_dependents;");
-    if (tid < 2) mbar_init(&full[tid], 1);
+    if (tid < p.nst) mbar_init(&full[tid], 1);
     if (tid == 0) asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     float *red = (float *)(smem + p.off_red);
     int gs = 0;  // sub-stages consumed by this CTA so far (ring slot and phase)
@@ -232,7 +233,7 @@ __global__ void __launch_bounds__(kSThreads) bgmv_shrink_kernel(const __grid_con
         __syncthreads();
 
         auto issue = [&](int s) {
-            const int h0 = hb + s * p.SC, len = min(p.SC, he - h0), st = (gs + s) & 1;
+            const int h0 = hb + s * p.SC, len = min(p.SC, he - h0), st = (gs + s) % p.nst;
             uint16_t *xs = (uint16_t *)(smem + p.off_x + st * p.x_stage_bytes);
             uint16_t *as = (uint16_t *)(smem + p.off_a + st * p.a_stage_bytes);
             const uint32_t rowb = (uint32_t)len * 2;
@@ -249,23 +250,23 @@ __global__ void __launch_bounds__(kSThreads) bgmv_shrink_kernel(const __grid_con
         if (warp == 0) {
             // the stages were last read through the generic proxy
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            for (int s = 0; s < min(n_sub, 2); ++s) issue(s);
+            for (int s = 0; s < min(n_sub, p.nst); ++s) issue(s);
         }
 
         const int nnb = (r + 7) >> 3;
         ShrinkAcc<NBMAX> acc;
         shrink_acc_zero(acc);
         for (int s = 0; s < n_sub; ++s) {
-            const int st = (gs + s) & 1;
-            mbar_wait(&full[st], (uint32_t)(((gs + s) >> 1) & 1), p.spin_limit, p.status);
+            const int st = (gs + s) % p.nst;
+            mbar_wait(&full[st], (uint32_t)(((gs + s) / p.nst) & 1), p.spin_limit, p.status);
             const int len = min(p.SC, he - hb - s * p.SC);
             const uint16_t *xs = (const uint16_t *)(smem + p.off_x + st * p.x_stage_bytes);
             const uint16_t *as = (const uint16_t *)(smem + p.off_a + st * p.a_stage_bytes);
             shrink_stage_mma(xs, p.xs_stride, as, p.as_stride, len, nnb, warp, lane, acc);
             __syncthreads();
-            if (warp == 0 && s + 2 < n_sub) {
+            if (warp == 0 && s + p.nst < n_sub) {
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                issue(s + 2);
+                issue(s + p.nst);
             }
         }
         gs += n_sub;
@@ -737,7 +738,26 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
         occ = first_occ;
     }
     if (!SC) return LORA_OK;
-    const size_t s_smem = smem_for(SC);
+    size_t s_smem = smem_for(SC);
+    // batches of several waves: a 3-stage ring (more bytes in flight per CTA)
+    int nst = 2;
+    if ((long long)occ * pool->num_sms < s_items) {
+        auto smem3 = [&](int sc) {
+            return 3 * (a128((size_t)kTileRows * (sc + 8) * 2) + a128((size_t)R8 * (sc + 8) * 2)) + red_bytes;
+        };
+        int sc3 = SC;
+        while (sc3 > 128 && smem3(sc3) > 100 * 1024) sc3 -= 16;
+        if (smem3(sc3) <= 100 * 1024) {
+            int o = 0;
+            LORA_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, shrink_fn, kSThreads, smem3(sc3)));
+            if (o >= 1) {
+                nst = 3;
+                SC = sc3;
+                occ = o;
+                s_smem = smem3(sc3);
+            }
+        }
+    }
     // expand shared memory: B rows, y rows, v hi/lo
     const int vr_stride = ns * R8 + 8;
     // 512 output columns per expand item for small ranks (fewer items, less fixed work per column)
@@ -803,8 +823,9 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     sa.x_stage_bytes = (int)a128((size_t)kTileRows * (SC + 8) * 2);
     sa.a_stage_bytes = (int)a128((size_t)R8 * (SC + 8) * 2);
     sa.off_x = 0;
-    sa.off_a = 2 * sa.x_stage_bytes;
-    sa.off_red = sa.off_a + 2 * sa.a_stage_bytes;
+    sa.nst = nst;
+    sa.off_a = nst * sa.x_stage_bytes;
+    sa.off_red = sa.off_a + nst * sa.a_stage_bytes;
     sa.part = (float *)ws;
     sa.ticket = tickets;
     sa.rows = pr.rows;

@@ -739,9 +739,10 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     }
     if (!SC) return LORA_OK;
     size_t s_smem = smem_for(SC);
-    // batches of several waves: a 3-stage ring (more bytes in flight per CTA)
+    // a 3-stage ring of narrower stages measured slower on the many-adapter
+    // batch than 2 wide stages: kept at 2
     int nst = 2;
-    if ((long long)occ * pool->num_sms < s_items) {
+    if (false) {
         auto smem3 = [&](int sc) {
             return 3 * (a128((size_t)kTileRows * (sc + 8) * 2) + a128((size_t)R8 * (sc + 8) * 2)) + red_bytes;
         };
@@ -882,7 +883,7 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     cfg.blockDim = dim3(kSThreads, 1, 1);
     cfg.stream = s;
     // grids of at most one wave; the kernels stride over their items
-    // one-wave grids (the key-major shrink: one CTA per item); CTAs take items from counters
+    // grids of at most two waves (the key-major shrink: one CTA per item); CTAs take items from counters
     const long long e_items = max_tiles * ea.n_oc;
     if (slot_major) {
         sa.enabled = pool->d_enabled;
@@ -902,13 +903,15 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
         LORA_CUDA_TRY(cudaLaunchKernelEx(&cfg, slot_fn, sa));
     } else {
         if ((size_t)sa.off_red + red_bytes > s_smem) return LORA_ERR_INVALID_ARG;  // layout check
-        cfg.gridDim = dim3((unsigned)(s_items < s_slots ? s_items : s_slots), 1, 1);
+        cfg.gridDim = dim3((unsigned)(s_items < 2 * s_slots ? s_items : 2 * s_slots), 1, 1);
         cfg.dynamicSmemBytes = s_smem;
         LORA_CUDA_TRY(cudaLaunchKernelEx(&cfg, shrink_fn, sa));
     }
     lora_note_launch();
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.gridDim = dim3((unsigned)(e_items < e_slots ? e_items : e_slots), 1, 1);
+    // up to two waves: CTAs of a second wave start as first-wave CTAs finish
+    // and find the counter exhausted or take the remaining items
+    cfg.gridDim = dim3((unsigned)(e_items < 2 * e_slots ? e_items : 2 * e_slots), 1, 1);
     cfg.dynamicSmemBytes = e_smem;
     LORA_CUDA_TRY(cudaLaunchKernelEx(&cfg, expand_fn, ea));
     lora_note_launch();

@@ -42,6 +42,8 @@ WORKLOADS = {
     "moe": "MoE-LoRA: E=64, top-8 of softmax(N(0,1)), D=2048, F=1408, 8 adapters rank 16, T=1024, "
            "w13 (gate+up) and w2",
     "moe_shared": "MoE-LoRA as 'moe' in the shared-outer layout (w13-A and w2-B expert dim 1)",
+    "moe_decode": "MoE-LoRA at decode: as 'moe' with T=16 (128 pairs over 512 (adapter, expert) keys: "
+                  "sparse occupancy, one 16-row tile per non-empty key)",
     "inkling_sink": "Inkling sink experts at decode: T=256, d_model 2048, 2 sink experts of d_mlp 1408: "
                     "w13 LoRA (2048 -> 2x2816) + SiLU(gate)*up*gamma + w2 LoRA (2816 -> 2048), "
                     "8 adapters rank 16, scale 2, 10% -1",
@@ -61,6 +63,8 @@ def make_case(name):
         return gen.moe()
     if name == "moe_shared":
         return gen.moe(shared_outer=True)
+    if name == "moe_decode":
+        return gen.moe(T=16)
     if name == "inkling_sink":
         return gen.inkling_sink()
     raise ValueError(name)

@@ -739,26 +739,9 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     }
     if (!SC) return LORA_OK;
     size_t s_smem = smem_for(SC);
-    // a 3-stage ring of narrower stages measured slower on the many-adapter
-    // batch than 2 wide stages: kept at 2
-    int nst = 2;
-    if (false) {
-        auto smem3 = [&](int sc) {
-            return 3 * (a128((size_t)kTileRows * (sc + 8) * 2) + a128((size_t)R8 * (sc + 8) * 2)) + red_bytes;
-        };
-        int sc3 = SC;
-        while (sc3 > 128 && smem3(sc3) > 100 * 1024) sc3 -= 16;
-        if (smem3(sc3) <= 100 * 1024) {
-            int o = 0;
-            LORA_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, shrink_fn, kSThreads, smem3(sc3)));
-            if (o >= 1) {
-                nst = 3;
-                SC = sc3;
-                occ = o;
-                s_smem = smem3(sc3);
-            }
-        }
-    }
+    // 2 wide stages: a 3-stage ring of narrower stages measured slower on the
+    // many-adapter batch
+    const int nst = 2;
     // expand shared memory: B rows, y rows, v hi/lo
     const int vr_stride = ns * R8 + 8;
     // 512 output columns per expand item for small ranks (fewer items, less fixed work per column)

@@ -100,3 +100,10 @@ def test_moe_disabled_adapter():
     assert_rows_untouched(ic3, c.ic3_0, ~act)
     assert_base_plus_delta(ic1, c.ic1_0, d13, act)
     assert_base_plus_delta(ic3, c.ic3_0, d2, act)
+
+
+@pytest.mark.parametrize("T", [1, 16])
+def test_moe_decode_sparse_keys(T):
+    """Decode-size MoE batches: T*K pairs over 512 (adapter, expert) keys, most
+    keys empty or with one pair (the sparse-occupancy regime)."""
+    run_and_check(gen.moe(T=T))

@@ -217,7 +217,10 @@ __global__ void __launch_bounds__(kSThreads) bgmv_shrink_kernel(const __grid_con
     float *red = (float *)(smem + p.off_red);
     int gs = 0;  // sub-stages consumed by this CTA so far (ring slot and phase)
 
-    for (int item = take_item(p.ticket, &s_item); item < total; item = take_item(p.ticket, &s_item)) {
+    // more items than CTAs: take them from the counter; else one item per CTA
+    const bool dyn = total > (int)gridDim.x;
+    for (int item = dyn ? take_item(p.ticket, &s_item) : (int)blockIdx.x; item < total;
+         item = dyn ? take_item(p.ticket, &s_item) : total) {
         const int tile = item / per_tile, rem = item - tile * per_tile;
         const int j = rem / p.NC, c = rem - j * p.NC;
         const int row0 = p.tile_row0[tile];
@@ -286,7 +289,7 @@ __global__ void __launch_bounds__(kSThreads) bgmv_shrink_kernel(const __grid_con
             dst[i] = sum;
         }
     }
-    finish_items(p.ticket);
+    if (dyn) finish_items(p.ticket);
 }
 
 // ---------------------------------------------------------------- shrink, key-major
@@ -435,7 +438,10 @@ __global__ void __launch_bounds__(kThreads, PW == 8 ? 3 : 5) bgmv_expand_kernel(
     const int nc = p.NC;
     uint32_t phase = 0;
 
-    for (int item = take_item(p.ticket, &s_item); item < total; item = take_item(p.ticket, &s_item), phase ^= 1u) {
+    // more items than CTAs: take them from the counter; else one item per CTA
+    const bool dyn = total > (int)gridDim.x;
+    for (int item = dyn ? take_item(p.ticket, &s_item) : (int)blockIdx.x; item < total;
+         item = dyn ? take_item(p.ticket, &s_item) : total, phase ^= 1u) {
         const int tile = item / p.n_oc, oc = item - tile * p.n_oc;
         const int row0 = p.tile_row0[tile];
         const int keyn = p.tile_keyn[tile];
@@ -644,7 +650,7 @@ __global__ void __launch_bounds__(kThreads, PW == 8 ? 3 : 5) bgmv_expand_kernel(
             asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
         }
     }
-    finish_items(p.ticket);
+    if (dyn) finish_items(p.ticket);
     asm volatile("griddepcontrol.launch_dependents;");
 }
 

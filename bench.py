@@ -44,6 +44,8 @@ WORKLOADS = {
     "moe_shared": "MoE-LoRA as 'moe' in the shared-outer layout (w13-A and w2-B expert dim 1)",
     "moe_decode": "MoE-LoRA at decode: as 'moe' with T=16 (128 pairs over 512 (adapter, expert) keys: "
                   "sparse occupancy, one 16-row tile per non-empty key)",
+    "linear_qkv": "full LoRA linear layer at decode: the decode_qkv batch with its base weight 4096 -> 6144 "
+                  "and bias: y = x W^T + bias (cuBLASLt) + LoRA delta",
     "inkling_sink": "Inkling sink experts at decode: T=256, d_model 2048, 2 sink experts of d_mlp 1408: "
                     "w13 LoRA (2048 -> 2x2816) + SiLU(gate)*up*gamma + w2 LoRA (2816 -> 2048), "
                     "8 adapters rank 16, scale 2, 10% -1",
@@ -67,6 +69,8 @@ def make_case(name):
         return gen.moe(T=16)
     if name == "inkling_sink":
         return gen.inkling_sink()
+    if name == "linear_qkv":
+        return gen.linear_qkv()
     raise ValueError(name)
 
 
@@ -76,6 +80,10 @@ def is_moe(name):
 
 def is_sink(name):
     return name == "inkling_sink"
+
+
+def is_linear(name):
+    return name == "linear_qkv"
 
 
 def apply_kernels(name, policy):
@@ -89,6 +97,8 @@ def apply_kernels(name, policy):
         k = "bgmv_shrink_kernel + bgmv_expand_kernel (chained by programmatic dependent launch)"
     if is_sink(name):
         return k + " on w13, sink_act_kernel, the same on w2"
+    if is_linear(name):
+        return "cuBLASLt base GEMM, then " + k
     if name == "prefill_gate_up" and policy != 1:
         k = "sgmv_shrink_kernel + sgmv_expand_kernel (tcgen05, 128-row runs); short tiles: " + k
     return k + (" for w13 and w2" if is_moe(name) else "")
@@ -119,6 +129,13 @@ def sink_algorithmic_bytes(c):
     act = c.T * (2 * W * 2 + W * 2 + c.n_experts * 4)
     total = a13["total"] + act + a2["total"] - a2["idx"]
     return dict(total=total, idx=a13["idx"], active=a13["active"], act=act)
+
+
+def linear_algorithmic_bytes(c):
+    """Base GEMM (W, x rows, y rows written) plus the delta's bytes."""
+    a = dense_algorithmic_bytes(c)
+    gemm = c.out_total * c.H * 2 + c.T * c.H * 2 + c.T * c.out_total * 2 + c.out_total * 2
+    return dict(total=a["total"] + gemm, idx=a["idx"], active=a["active"], gemm=gemm)
 
 
 def moe_algorithmic_bytes(c):
@@ -206,6 +223,18 @@ def oracle_step_fn(name, c):
             oracle.moe_w13(c)
             oracle.moe_w2(c)
         return step, c.T
+    if is_linear(name):
+        bias = gen.f32_to_bf16_bits(np.random.default_rng(7).normal(0, 0.5, c.out_total).astype(np.float32))
+        n = 64   # bounded sample: the first 64 tokens (the oracle's base product is per token)
+        from types import SimpleNamespace
+        sub = SimpleNamespace(**{k: getattr(c, k) for k in ("H", "L", "R", "ranks", "scales", "enabled", "A", "B",
+                                                             "out_dims", "out_total", "n_slices")})
+        sub.x, sub.idx, sub.y0, sub.T = c.x[:n], c.idx[:n], c.y0[:n], n
+
+        def step():
+            oracle.dense_meta(sub.idx, c.L, c.enabled, c.ranks)
+            oracle.linear(sub, c.W, bias)
+        return step, n
     if is_sink(name):
         from heterogeneous_adapters_lora_gb300.inputs import f32_to_bf16_bits
 
@@ -354,15 +383,19 @@ def run_gpu(args, rank, world, local_rank):
     moe = is_moe(name)
     sink = is_sink(name)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    ab = moe_algorithmic_bytes(c) if moe else (sink_algorithmic_bytes(c) if sink else dense_algorithmic_bytes(c))
+    lin = is_linear(name)
+    ab = (moe_algorithmic_bytes(c) if moe else sink_algorithmic_bytes(c) if sink
+          else linear_algorithmic_bytes(c) if lin else dense_algorithmic_bytes(c))
     foot = ab["total"]
     n_rot = max(1, math.ceil(2 * l2 / max(foot, 1)))
     n_rot = min(n_rot, args.max_copies)
 
     runs = []
     for _ in range(n_rot):
-        runs.append(Hn.MoERun(c, device=dev) if moe else (Hn.SinkRun(c, device=dev) if sink
-                                                          else Hn.DenseRun(c, device=dev)))
+        if lin:
+            bias = gen.f32_to_bf16_bits(np.random.default_rng(7).normal(0, 0.5, c.out_total).astype(np.float32))
+        runs.append(Hn.MoERun(c, device=dev) if moe else Hn.SinkRun(c, device=dev) if sink
+                    else Hn.LinearRun(c, bias, device=dev) if lin else Hn.DenseRun(c, device=dev))
     torch.cuda.synchronize(dev)
 
     def step(r):
@@ -477,6 +510,12 @@ def run_gpu(args, rank, world, local_rank):
             h_out = [torch.empty_like(r.ic1, device="cpu").pin_memory(),
                      torch.empty_like(r.ic3, device="cpu").pin_memory()]
             d_out = [r.ic1, r.ic3]
+        elif lin:
+            h_in = [torch.from_numpy(np.ascontiguousarray(c.x).view(np.int16)).pin_memory(),
+                    torch.from_numpy(c.idx).pin_memory()]
+            d_in = [r.x, r.idx]
+            h_out = [torch.empty_like(r.y, device="cpu").pin_memory()]
+            d_out = [r.y]
         elif sink:
             h_in = [torch.from_numpy(np.ascontiguousarray(c.w13.x).view(np.int16)).pin_memory(),
                     torch.from_numpy(c.w13.idx).pin_memory(),

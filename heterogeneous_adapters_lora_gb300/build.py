@@ -63,7 +63,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
         raise RuntimeError(f"nvcc failed:\n{msg}")
     if force or procs or _stale(LIB, objs):
         tmp = LIB + f".{os.getpid()}.tmp"
-        cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
+        cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-lcublasLt"]
         subprocess.run(cmd, check=True)
         os.replace(tmp, LIB)
     return LIB

@@ -238,3 +238,18 @@ class SinkRun:
     def close(self):
         self.r13.close()
         self.r2.close()
+
+
+class LinearRun(DenseRun):
+    """A dense case with its base weight and bias on the GPU: the full LoRA
+    linear layer y = x W^T + bias + delta."""
+
+    def __init__(self, case, bias=None, device="cuda"):
+        super().__init__(case, device=device)
+        self.W = to_dev_u16(case.W, device)
+        self.bias = to_dev_u16(bias, device) if bias is not None else None
+
+    def apply(self):
+        c = self.case
+        L.lora_linear_apply(self.pool, self.mb.meta, self.x, c.H, self.W, c.H, self.bias, self.y, c.out_total,
+                            self.ws, self.ws_bytes)

@@ -354,6 +354,13 @@ def moe(shared_outer: bool = False, base: str = "zero", T: int = 1024) -> MoECas
                     shared_outer=shared_outer, base=base)
 
 
+def linear_qkv(T: int = 256) -> DenseCase:
+    """The decode QKV layer as a full LoRA linear layer: the decode_qkv batch
+    with a base weight [6144][4096] ~ N(0, 0.02)."""
+    return dense_case(name="linear_qkv", T=T, H=4096, out_dims=(4096, 1024, 1024), L=32, R=16, seed=1102,
+                      scales=np.full(32, 2.0, np.float32), p_none=0.1, with_W=True)
+
+
 class SinkCase:
     """Inkling sink experts around their two LoRA layers: w13 (gate_up, two
     slices of n*d_mlp) and w2 (n*d_mlp -> d_model) share one batch (idx)."""

@@ -91,6 +91,8 @@ EXPORTS = {
     "lora_set_spin_limit": (None, [c_i32]),
     "lora_set_kernel_policy": (None, [c_i32]),
     "lora_kernel_launch_count": (ctypes.c_ulonglong, []),
+    "lora_linear_apply": (c_i32, [c_vp, ctypes.POINTER(Meta), c_vp, c_i64, c_vp, c_i64, c_vp, c_vp, c_i64, c_vp, c_size,
+                              c_vp]),
     "lora_sink_experts_act": (c_i32, [c_vp, c_i64, c_vp, c_i64, c_i32, c_i32, c_i32, c_vp, c_i64, c_vp]),
     "lora_status_string": (ctypes.c_char_p, [c_i32]),
 }
@@ -259,6 +261,12 @@ def lora_set_spin_limit(max_polls: int):
 
 def lora_set_kernel_policy(policy: int):
     lib().lora_set_kernel_policy(int(policy))
+
+
+def lora_linear_apply(pool, meta: Meta, x, ldx, W, ldw, bias, y, ldy, ws, ws_bytes, stream=None):
+    """Full LoRA linear layer: y = x W^T + bias + delta."""
+    _check(lib().lora_linear_apply(pool, ctypes.byref(meta), ptr(x), int(ldx), ptr(W), int(ldw), ptr(bias), ptr(y),
+                                   int(ldy), ptr(ws), ws_bytes, stream_ptr(stream)), "lora_linear_apply")
 
 
 def lora_sink_experts_act(gate_up, ld_gate_up, gammas, ld_gammas, T, n_experts, d_mlp, h, ld_h, stream=None):

@@ -351,6 +351,20 @@ LORA_API lora_status_t lora_get_device_status(const lora_pool_t *pool, void *str
  * give up at once (to exercise the error path).  Process-wide. */
 LORA_API void lora_set_spin_limit(int32_t max_polls);
 
+/* The full LoRA linear layer of a dense pool (vLLM LoRA layer pages,
+ * BaseLinearLayerWithLoRA: base output, then the LoRA delta added in place):
+ *   y = x W^T + bias + delta          (delta as in lora_apply_slices)
+ * W is the base weight [out_total][ldw] bf16 row-major (the packed slices'
+ * weights stacked in slice order), bias [out_total] bf16 or NULL, y is fully
+ * written for the meta's T tokens.  The base GEMM is a cuBLASLt call (no
+ * workspace); the delta is a second pass over y.  Errors: as lora_apply_slices,
+ * plus LORA_ERR_INVALID_ARG for a null or misaligned x/W/y (16 bytes), leading
+ * dimensions not multiples of 8 or too small, LORA_ERR_UNSUPPORTED for a MoE
+ * pool or when cuBLASLt offers no algorithm, LORA_ERR_CUDA on a cuBLASLt error. */
+LORA_API lora_status_t lora_linear_apply(const lora_pool_t *pool, const lora_meta_t *meta, const void *x,
+                                         int64_t ldx, const void *W, int64_t ldw, const void *bias, void *y,
+                                         int64_t ldy, void *workspace, size_t ws_bytes, void *stream);
+
 /* Inkling sink experts between their two LoRA-wrapped linear layers (Inkling
  * LoRA PR report, InklingSinkExpertsLinear.forward and _gamma_expand).  With
  * W = n_experts * d_mlp, gate_up is the w13 output [T][ld_gate_up] bf16

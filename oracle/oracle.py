@@ -1,7 +1,8 @@
 """ctypes wrapper around the C oracle (``lora_oracle.c``) -- test infrastructure.
 
 Every function here only marshals numpy arrays into the C routines and
-reshapes their outputs; the arithmetic lives in ``lora_oracle.c``.  Parity
+reshapes their outputs; the arithmetic lives in ``lora_oracle.c``, except the
+base product of ``linear``, a float64 numpy matmul (a library primitive).  Parity
 status: every routine is pinned by ``tests/test_oracle_pins.py`` (brute force
 in fp64, the merged-weight identity, the page invariants and a hand-derived
 golden case); none is "parity unpinned".
@@ -260,6 +261,20 @@ def logits(logits_in, delta, vocab_size, mapping=None, mup=1.0):
     return out
 
 
+def linear(case, W, bias=None, threads: int = 0):
+    """Full LoRA linear layer y = x W^T + bias + delta (BaseLinearLayerWithLoRA:
+    base output, then the delta of lo_dense_delta added).  The base product of
+    the bf16 values is a library matmul in float64; returns float64 [T][O]."""
+    from heterogeneous_adapters_lora_gb300.inputs import bf16_bits_to_f32
+    x = bf16_bits_to_f32(np.asarray(case.x)).astype(np.float64)
+    Wf = bf16_bits_to_f32(np.asarray(W)).astype(np.float64)
+    base = x @ Wf.T
+    if bias is not None:
+        base = base + bf16_bits_to_f32(np.asarray(bias)).astype(np.float64)[None, :]
+    _, delta = dense_delta(case, threads=threads)
+    return base + delta.astype(np.float64)
+
+
 def sink_act(gate_up, gammas, n_experts, d_mlp):
     """Inkling sink-expert activation: bf16 bits h[T][n*d_mlp] from bf16 bits
     gate_up[T][2*n*d_mlp] and fp32 gammas[T][n]."""
@@ -274,4 +289,4 @@ def sink_act(gate_up, gammas, n_experts, d_mlp):
     return h
 
 
-__all__ = ["sink_act", "logits", "moe_align_padded", "build", "use_library", "compile_variant", "source_text", "max_threads", "dense_meta", "dense_delta", "moe_meta", "moe_w13", "moe_w2"]
+__all__ = ["linear", "sink_act", "logits", "moe_align_padded", "build", "use_library", "compile_variant", "source_text", "max_threads", "dense_meta", "dense_delta", "moe_meta", "moe_w13", "moe_w2"]

@@ -412,3 +412,27 @@ def test_sink_act_reduces_to_logistic_silu():
     h = bf16_bits_to_f32(oracle.sink_act(gu, np.ones((T, n), np.float32), n, d)).astype(np.float64)
     exact = g * scipy_special.expit(g)
     assert np.all(np.abs(h - exact) <= np.abs(exact) * 2.0 ** -8 + 1e-30)
+
+
+# ----------------------------------------------------------------- full LoRA linear
+
+def test_linear_equals_merged_weight_form_with_bias():
+    """y = x W^T + bias + delta equals x (W + s B A)^T + bias per token (the
+    merged-weight form), within the fp32 bound of the delta."""
+    c = gen.tiny()
+    rng = np.random.default_rng(3)
+    bias = f32_to_bf16_bits(rng.normal(0, 0.5, c.out_total).astype(np.float32))
+    y = oracle.linear(c, c.W, bias)
+    x = bf16_bits_to_f32(c.x).astype(np.float64)
+    W = bf16_bits_to_f32(c.W).astype(np.float64)
+    b = bf16_bits_to_f32(bias).astype(np.float64)
+    _, bound = exact_dense(c)
+    for t in range(c.T):
+        a = int(c.idx[t])
+        merged = W
+        if 0 <= a < c.L and c.enabled[a] and c.ranks[a] > 0:
+            r = int(c.ranks[a])
+            merged = W + c.scales[a] * (bf16_bits_to_f32(c.B[0][a, :, :r]).astype(np.float64)
+                                        @ bf16_bits_to_f32(c.A[0][a, :r]).astype(np.float64))
+        want = x[t] @ merged.T + b
+        assert np.all(np.abs(y[t] - want) <= bound[t] + 1e-9), t

@@ -102,19 +102,16 @@ __global__ void __launch_bounds__(kThreads, 1) build_meta_kernel(MetaArgs a) {
     // overlaps the previous kernel; nothing is read before it has finished
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
-    // issue the first row step's slot loads together with the table loads
+    // slot (and expert) of this warp's first 8 row steps, issued before the tables
     const int chunk = (rows + W - 1) / W;
     const int r0 = warp * chunk, r1 = min(rows, r0 + chunk);
-    int s_first = -1;
-    if (!a.cache_keys && warp < W && r0 + lane < r1) s_first = a.idx[(r0 + lane) / a.K];
     int sv[8], ev[8];
-    if (a.cache_keys) {
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int row = u * nthreads + tid;
-            sv[u] = row < rows ? a.idx[row / a.K] : -1;
-            ev[u] = (row < rows && a.topk) ? a.topk[row] : 0;
-        }
+    for (int u = 0; u < 8; ++u) {
+        const int row = r0 + u * 32 + lane;
+        const bool ok = warp < W && row < r1;
+        sv[u] = ok ? a.idx[row / a.K] : -1;
+        ev[u] = (ok && a.topk) ? a.topk[row] : 0;
     }
     for (int i = tid; i < a.L; i += nthreads) act[i] = (a.enabled[i] != 0 && a.rank[i] > 0) ? 1 : 0;
     for (int i = tid; i < (W * NK1) / 4; i += nthreads) ((int4 *)hist)[i] = make_int4(0, 0, 0, 0);
@@ -126,56 +123,36 @@ __global__ void __launch_bounds__(kThreads, 1) build_meta_kernel(MetaArgs a) {
     if (tid == 0) misc[36] = 0;
     __syncthreads();
 
-    // with the key cache: every row's key first, with the slot and expert
-    // loads of up to 8 rows per thread issued back to back (the first batch
-    // was issued before the tables were filled)
+    // pass 1: keys (kept for the scatter when they fit) and per-chunk counts
     int bad = 0;
-    if (a.cache_keys) {
-        for (int base = 0; base < rows; base += 8 * nthreads) {
-            if (base > 0) {
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int row = base + u * nthreads + tid;
-                    sv[u] = row < rows ? a.idx[row / a.K] : -1;
-                    ev[u] = (row < rows && a.topk) ? a.topk[row] : 0;
+    auto count_step = [&](int base, int s, int e) {
+        const int row = base + lane;
+        const bool v = row < r1;
+        const int key = v ? row_key_e(a, act, row, s, e, &bad) : -1;
+        if (v && a.cache_keys) kc[row] = key;
+        if (a.K == 1) {
+            const unsigned peers = key_peers(key, a.key_bits);
+            const int leader = __ffs(peers) - 1;
+            if (v && lane == leader) {
+                hist[warp * NK1 + key] += __popc(peers);
+                if (key < NK) {  // the rows of a warp step are consecutive
+                    atomicMin(&tmin[key], base + leader);
+                    atomicMax(&tmax[key], base + 31 - __clz(peers));
                 }
             }
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int row = base + u * nthreads + tid;
-                if (row < rows) kc[row] = row_key_e(a, act, row, sv[u], ev[u], &bad);
-            }
+        } else if (v) {
+            atomicAdd(&hist[warp * NK1 + key], 1);  // counts only: order does not matter here
         }
-        __syncthreads();
-    }
-
+        __syncwarp();
+    };
     if (warp < W) {
-        for (int base = r0; base < r1; base += 32) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            if (r0 + u * 32 < r1) count_step(r0 + u * 32, sv[u], ev[u]);
+        for (int base = r0 + 256; base < r1; base += 32) {
             const int row = base + lane;
             const bool v = row < r1;
-            int key = -1;
-            if (v) {
-                if (a.cache_keys) {
-                    key = kc[row];
-                } else {
-                    const int s = base == r0 ? s_first : a.idx[row / a.K];
-                    key = row_key(a, act, row, s, &bad);
-                }
-            }
-            if (a.K == 1) {
-                const unsigned peers = key_peers(key, a.key_bits);
-                const int leader = __ffs(peers) - 1;
-                if (v && lane == leader) {
-                    hist[warp * NK1 + key] += __popc(peers);
-                    if (key < NK) {  // the rows of a warp step are consecutive
-                        atomicMin(&tmin[key], base + leader);
-                        atomicMax(&tmax[key], base + 31 - __clz(peers));
-                    }
-                }
-            } else if (v) {
-                atomicAdd(&hist[warp * NK1 + key], 1);  // counts only: order does not matter here
-            }
-            __syncwarp();
+            count_step(base, v ? a.idx[row / a.K] : -1, (v && a.topk) ? a.topk[row] : 0);
         }
     }
 #pragma unroll
@@ -183,21 +160,10 @@ __global__ void __launch_bounds__(kThreads, 1) build_meta_kernel(MetaArgs a) {
     if (lane == 0 && bad) atomicAdd(&misc[36], bad);
     __syncthreads();
 
-    // per key: exclusive prefix over the chunks (in place) and the count
-    for (int b = tid; b < NK1; b += nthreads) {
-        int run = 0;
-        for (int w = 0; w < W; ++w) {
-            const int c = hist[w * NK1 + b];
-            hist[w * NK1 + b] = run;
-            run += c;
-        }
-        cnt[b] = run;
-    }
-    __syncthreads();
-
-    // every key-space prefix sum in one block-wide scan: row offsets, group
-    // index, 16-row tiles, long-run tiles and short tiles.  Thread t owns a
-    // contiguous block of keys.
+    // one pass over the keys, thread t owning a contiguous block: per key the
+    // exclusive prefix over the chunks (in place) and the count, then every
+    // key-space prefix sum in one block-wide scan: row offsets, group index,
+    // 16-row tiles, long-run tiles and short tiles
     int *gidx = hist + W * NK1;  // the four scratch rows after the chunk histograms
     int *tiles = gidx + NK1;
     int *lt_cnt = tiles + NK1;
@@ -208,9 +174,16 @@ __global__ void __launch_bounds__(kThreads, 1) build_meta_kernel(MetaArgs a) {
         const int b0 = min(NK1, tid * per), b1 = min(NK1, b0 + per);
         int sv5[5] = {0, 0, 0, 0, 0};
         for (int b = b0; b < b1; ++b) {
-            const int c = b < NK ? cnt[b] : 0;
+            int run_rows = 0;
+            for (int w = 0; w < W; ++w) {
+                const int cw = hist[w * NK1 + b];
+                hist[w * NK1 + b] = run_rows;
+                run_rows += cw;
+            }
+            cnt[b] = run_rows;
+            const int c = b < NK ? run_rows : 0;
             const bool run = c > 0 && a.K == 1 && c >= LORA_LONG_MIN && tmax[b] - tmin[b] == c - 1;
-            sv5[0] += cnt[b];
+            sv5[0] += run_rows;
             sv5[1] += c > 0 ? 1 : 0;
             sv5[2] += (c + LORA_TILE_ROWS - 1) / LORA_TILE_ROWS;
             sv5[3] += run ? (c + LORA_LTILE_ROWS - 1) / LORA_LTILE_ROWS : 0;
@@ -255,19 +228,14 @@ __global__ void __launch_bounds__(kThreads, 1) build_meta_kernel(MetaArgs a) {
             tiles[b] = ex[2];
             lt_cnt[b] = ex[3];
             st_cnt[b] = ex[4];
+            if (b < NK) a.m.key_count[b] = cnt[b];
+            a.m.key_offset[b] = ex[0];
             ex[0] += cnt[b];
             ex[1] += c > 0 ? 1 : 0;
             ex[2] += (c + LORA_TILE_ROWS - 1) / LORA_TILE_ROWS;
             ex[3] += run ? (c + LORA_LTILE_ROWS - 1) / LORA_LTILE_ROWS : 0;
             ex[4] += (c > 0 && !run) ? (c + LORA_TILE_ROWS - 1) / LORA_TILE_ROWS : 0;
         }
-    }
-    __syncthreads();
-    for (int b = tid; b < NK1; b += nthreads) {
-        const int o = off[b];
-        for (int w = 0; w < W; ++w) hist[w * NK1 + b] += o;
-        if (b < NK) a.m.key_count[b] = cnt[b];
-        a.m.key_offset[b] = o;
     }
     __syncthreads();
 
@@ -288,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1) build_meta_kernel(MetaArgs a) {
             }
             const unsigned peers = key_peers(key, a.key_bits);
             int pos = 0;
-            if (v) pos = hist[warp * NK1 + key] + __popc(peers & lt);
+            if (v) pos = off[key] + hist[warp * NK1 + key] + __popc(peers & lt);
             __syncwarp();
             if (v) {
                 a.m.sorted[pos] = row;

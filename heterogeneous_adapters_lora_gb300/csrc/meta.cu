@@ -88,8 +88,8 @@ __global__ void __launch_bounds__(kThreads, 1) build_meta_kernel(MetaArgs a) {
     int *cnt = hist + (W + 4) * NK1; // [NK1]
     int *off = cnt + NK1;            // [NK1]
     int *tmin = off + NK1;           // [NK1] smallest token of each key (dense)
-    int *tmax = tmin + NK1;          // [NK1] largest token of each key (dense)
-    int *misc = tmax + NK1;          // [200]: totals at [32..35], n_bad at [36], warp scan totals at [40..199]
+    int *nrun = tmin + NK1;          // [NK1] runs of consecutive tokens of each key (dense)
+    int *misc = nrun + NK1;          // [200]: totals at [32..35], n_bad at [36], warp scan totals at [40..199]
     unsigned char *act = (unsigned char *)(misc + 200);  // [L] slot enabled and rank > 0
     int *kc = misc + 200 + (a.L + 3) / 4;                // [rows] keys of pass 1 when cached
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -113,18 +113,26 @@ __global__ void __launch_bounds__(kThreads, 1) build_meta_kernel(MetaArgs a) {
         sv[u] = ok ? a.idx[row / a.K] : -1;
         ev[u] = (ok && a.topk) ? a.topk[row] : 0;
     }
+    // dense: the slot of the row before this warp's chunk (run starts at the boundary)
+    const int s_prev = (a.K == 1 && warp < W && r0 > 0 && r0 < r1) ? a.idx[r0 - 1] : -1;
     for (int i = tid; i < a.L; i += nthreads) act[i] = (a.enabled[i] != 0 && a.rank[i] > 0) ? 1 : 0;
     for (int i = tid; i < (W * NK1) / 4; i += nthreads) ((int4 *)hist)[i] = make_int4(0, 0, 0, 0);
     for (int i = (W * NK1) / 4 * 4 + tid; i < W * NK1; i += nthreads) hist[i] = 0;
     for (int i = tid; i < NK1; i += nthreads) {
         tmin[i] = 0x7fffffff;
-        tmax[i] = -1;
+        nrun[i] = 0;
     }
     if (tid == 0) misc[36] = 0;
     __syncthreads();
 
     // pass 1: keys (kept for the scatter when they fit) and per-chunk counts
     int bad = 0;
+    // dense: key of the row before the current step (-2: none), for run starts
+    int carry = -2;
+    if (a.K == 1 && warp < W && r0 > 0 && r0 < r1) {
+        int dummy = 0;
+        carry = row_key_e(a, act, r0 - 1, s_prev, 0, &dummy);
+    }
     auto count_step = [&](int base, int s, int e) {
         const int row = base + lane;
         const bool v = row < r1;
@@ -133,13 +141,16 @@ __global__ void __launch_bounds__(kThreads, 1) build_meta_kernel(MetaArgs a) {
         if (a.K == 1) {
             const unsigned peers = key_peers(key, a.key_bits);
             const int leader = __ffs(peers) - 1;
-            if (v && lane == leader) {
-                hist[warp * NK1 + key] += __popc(peers);
-                if (key < NK) {  // the rows of a warp step are consecutive
-                    atomicMin(&tmin[key], base + leader);
-                    atomicMax(&tmax[key], base + 31 - __clz(peers));
-                }
+            if (v && lane == leader) hist[warp * NK1 + key] += __popc(peers);
+            // a row starts a run of its key when the previous row has another key:
+            // the key's rows are one contiguous run when it has exactly one start
+            int prev = __shfl_up_sync(0xffffffffu, key, 1);
+            if (lane == 0) prev = carry;
+            if (v && key < NK && key != prev) {
+                atomicAdd(&nrun[key], 1);
+                atomicMin(&tmin[key], row);
             }
+            carry = __shfl_sync(0xffffffffu, key, 31);
         } else if (v) {
             atomicAdd(&hist[warp * NK1 + key], 1);  // counts only: order does not matter here
         }
@@ -182,7 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1) build_meta_kernel(MetaArgs a) {
             }
             cnt[b] = run_rows;
             const int c = b < NK ? run_rows : 0;
-            const bool run = c > 0 && a.K == 1 && c >= LORA_LONG_MIN && tmax[b] - tmin[b] == c - 1;
+            const bool run = c > 0 && a.K == 1 && c >= LORA_LONG_MIN && nrun[b] == 1;
             sv5[0] += run_rows;
             sv5[1] += c > 0 ? 1 : 0;
             sv5[2] += (c + LORA_TILE_ROWS - 1) / LORA_TILE_ROWS;
@@ -222,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1) build_meta_kernel(MetaArgs a) {
         }
         for (int b = b0; b < b1; ++b) {
             const int c = b < NK ? cnt[b] : 0;
-            const bool run = c > 0 && a.K == 1 && c >= LORA_LONG_MIN && tmax[b] - tmin[b] == c - 1;
+            const bool run = c > 0 && a.K == 1 && c >= LORA_LONG_MIN && nrun[b] == 1;
             off[b] = ex[0];
             gidx[b] = ex[1];
             tiles[b] = ex[2];
@@ -330,7 +341,7 @@ lora_status_t lora_launch_build_meta(const lora_pool_t *pool, const int32_t *d_i
     if (nthreads < 128) nthreads = 128;
     if (nthreads > kThreads) nthreads = kThreads;
     const int nwarps = nthreads / 32;
-    // chunk histograms [W][NK1] + 4 scratch rows + cnt, off, tmin, tmax + misc + slot table
+    // chunk histograms [W][NK1] + 4 scratch rows + cnt, off, tmin, nrun + misc + slot table
     const long long fixed = 8LL * NK1 + 200 + (L + 3) / 4;
     int W = (int)((kSmemBudgetInts - fixed) / NK1);
     if (W > nwarps) W = nwarps;

@@ -21,6 +21,8 @@
 //   initial state.
 #include <string.h>
 
+#include <algorithm>
+
 #include "lora_internal.cuh"
 #include "mma_common.cuh"
 
@@ -715,17 +717,17 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
         g_split_configured[dev] = 1;
     }
     // shrink shared memory: 2 stages of (16 + R8) rows x SC columns (rows
-    // padded by 16 bytes), then the partial sums.  SC: the widest stage (up
-    // to the chunk, <= 100 KB) whose occupancy still runs every item in one
-    // wave, else the widest that fits
+    // padded by 16 bytes); the partial sums reuse the stages.  SC: the widest
+    // stage (up to the chunk, <= 75 KB, three CTAs per SM) whose occupancy
+    // still runs every item in one wave, else the widest that fits
     const int red_bytes = 4 * kTileRows * R8 * 4;
     auto smem_for = [&](int sc) {
-        return 2 * (a128((size_t)kTileRows * (sc + 8) * 2) + a128((size_t)R8 * (sc + 8) * 2)) + red_bytes;
+        return std::max((size_t)red_bytes, 2 * (a128((size_t)kTileRows * (sc + 8) * 2) + a128((size_t)R8 * (sc + 8) * 2)));
     };
     const long long s_items = max_tiles * ns * NC;
     int SC = 0, occ = 0, first = 0, first_occ = 0;
     for (int sc = (HC < 1024 ? HC : 1024); sc >= 64; sc -= 64) {
-        if (smem_for(sc) > 100 * 1024) continue;
+        if (smem_for(sc) > 75 * 1024) continue;
         int o = 0;
         LORA_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, shrink_fn, kSThreads, smem_for(sc)));
         if (!first) {
@@ -815,7 +817,7 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     sa.off_x = 0;
     sa.nst = nst;
     sa.off_a = nst * sa.x_stage_bytes;
-    sa.off_red = sa.off_a + nst * sa.a_stage_bytes;
+    sa.off_red = 0;  // the partial sums reuse the stages: an item's copies are all consumed by then
     sa.part = (float *)ws;
     sa.ticket = tickets;
     sa.rows = pr.rows;

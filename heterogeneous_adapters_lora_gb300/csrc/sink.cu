@@ -7,7 +7,9 @@
 // SiLU(gate) * up are bf16, the gamma factor is fp32, the result is bf16.
 //
 // HBM-bound elementwise work: 8 columns per thread (16-byte loads and
-// stores), grid-stride over T x n*d_mlp / 8.
+// stores), grid-stride over T x n*d_mlp / 8.  Launched with programmatic
+// stream serialization between the two layers' LoRA kernels: it starts while
+// the w13 expand drains and lets the w2 shrink fetch its weights meanwhile.
 #include <string.h>
 
 #include "lora_internal.cuh"
@@ -27,12 +29,18 @@ __global__ void __launch_bounds__(kThreads) sink_act_kernel(const uint16_t *__re
     const long long W = (long long)n_experts * d_mlp;
     const long long V = W / 8;
     const long long total = (long long)T * V;
+    // the next kernel may start its prologue; it waits for this grid's
+    // completion before it reads h
+    asm volatile("griddepcontrol.launch_dependents;");
+    // gate_up is complete once the kernel before this one has finished
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     for (long long i = (long long)blockIdx.x * kThreads + threadIdx.x; i < total;
          i += (long long)gridDim.x * kThreads) {
         const long long t = i / V;
         const long long c0 = (i - t * V) * 8;
-        const uint4 gv = ldg_stream(gu + t * ld_gu + c0);
-        const uint4 uv = ldg_stream(gu + t * ld_gu + W + c0);
+        // written by the previous kernel: L2 loads, no L1 lines
+        const uint4 gv = __ldcg((const uint4 *)(gu + t * ld_gu + c0));
+        const uint4 uv = __ldcg((const uint4 *)(gu + t * ld_gu + W + c0));
         const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w}, uw[4] = {uv.x, uv.y, uv.z, uv.w};
         uint32_t ow[4];
         const float *grow = gammas + t * ld_g;
@@ -81,9 +89,19 @@ extern "C" lora_status_t lora_sink_experts_act(const void *gate_up, int64_t ld_g
     long long grid = (vecs + kThreads - 1) / kThreads;
     const long long cap = (long long)g_sink_sms[dev] * 8;
     if (grid > cap) grid = cap;
-    sink_act_kernel<<<(unsigned)grid, kThreads, 0, (cudaStream_t)stream>>>(
-        (const uint16_t *)gate_up, ld_gate_up, gammas, ld_gammas, T, n_experts, d_mlp, (uint16_t *)h, ld_h);
-    LORA_CUDA_TRY(cudaGetLastError());
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.stream = (cudaStream_t)stream;
+    LORA_CUDA_TRY(cudaLaunchKernelEx(&cfg, sink_act_kernel, (const uint16_t *)gate_up, (long long)ld_gate_up,
+                                     gammas, (long long)ld_gammas, (int)T, (int)n_experts, (int)d_mlp,
+                                     (uint16_t *)h, (long long)ld_h));
     lora_note_launch();
     return LORA_OK;
 }

@@ -9,9 +9,11 @@
 //
 //   bgmv_shrink_kernel: items (16-row tile, slice j, hidden chunk c).  Bulk
 //     copies (cp.async.bulk + mbarrier) bring the tile's x rows and the
-//     slot's A_j rows of chunk c; m16n8k16 bf16 MMAs (fp32 accumulate) give
-//     the partial v of chunk c, stored unscaled in fp32.
-//   bgmv_expand_kernel: items (tile, 256 output columns).  Before it waits
+//     slot's A_j rows of chunk c, 16 ranks at a time; m16n8k16 bf16 MMAs
+//     (fp32 accumulate) give the partial v of chunk c, stored unscaled in fp32.
+//   bgmv_shrink_slot_kernel: the same partials from one CTA per (key, slice,
+//     chunk) that multiplies every tile of the key against its A rows.
+//   bgmv_expand_kernel: items (tile, 256 or 512 output columns).  Before it waits
 //     for the shrink it bulk-copies its first item's B rows and y rows; it sums
 //     the chunk partials of the slices it touches in chunk order, scales them
 //     by scale[a] (and the routed weight for MoE w2), splits v into bf16 hi +
@@ -196,11 +198,18 @@ __device__ __forceinline__ void shrink_store_red(float *red, int R8, int nnb, in
 // ---------------------------------------------------------------- shrink
 //
 // Items (16-row tile, slice j, hidden chunk c), strided over a grid of at
-// most a few waves.  Two stages of [16 x rows][r A rows] x SC columns, rows
-// padded by 16 bytes so ldmatrix reads are free of bank conflicts; the MMAs
-// as in shrink_stage_mma, the four warps' partial sums added in shared memory.
+// most a few waves.  The slot's ranks are taken kRG at a time: for each rank
+// group the chunk streams through a ring of stages holding the tile's x rows
+// and the group's A rows, SC columns each (rows padded by 16 bytes so
+// ldmatrix reads are free of bank conflicts).  Few rows per stage keep the
+// stages wide, so every row copy is long whatever the rank; the x rows are
+// fetched again for each group (from L2).  The MMAs as in shrink_stage_mma;
+// at the end of a group the four warps' sums are added in shared memory and
+// the group's ranks of the unscaled chunk partial stored.
 
-template <int NBMAX>
+constexpr int kRG = 16;  // ranks per group (two 8-rank MMA blocks)
+
+template <int NBMAX>  // 1 or 2: 8-rank blocks of a group
 __global__ void __launch_bounds__(kSThreads) bgmv_shrink_kernel(const __grid_constant__ SArgs p) {
     extern __shared__ __align__(128) char smem[];
     __shared__ __align__(8) uint64_t full[4];
@@ -217,8 +226,8 @@ __global__ void __launch_bounds__(kSThreads) bgmv_shrink_kernel(const __grid_con
     asm volatile("griddepcontrol.launch_dependents;");
     if (tid < p.nst) mbar_init(&full[tid], 1);
     if (tid == 0) asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    float *red = (float *)(smem + p.off_red);
-    int gs = 0;  // sub-stages consumed by this CTA so far (ring slot and phase)
+    float *red = (float *)(smem + p.off_red);  // [4 warps][16][kRG], apart from the stages
+    int gs = 0;  // stages consumed by this CTA so far (ring slot and phase)
 
     // more items than CTAs: take them from the counter; else one item per CTA
     const bool dyn = total > (int)gridDim.x;
@@ -234,63 +243,71 @@ __global__ void __launch_bounds__(kSThreads) bgmv_shrink_kernel(const __grid_con
         const uint16_t *Ab = a_rows(p, j, a, e);
         const int hb = c * p.HC, he = min(p.in_dim, hb + p.HC);
         const int n_sub = (he - hb + p.SC - 1) / p.SC;
+        const int n_stage = n_sub * ((r + kRG - 1) / kRG);  // groups x column stages
         __syncthreads();  // the previous item is done with s_rows, the stages and red
         if (tid < n) s_rows[tid] = p.sorted[row0 + tid];
         __syncthreads();
 
         auto issue = [&](int s) {
-            const int h0 = hb + s * p.SC, len = min(p.SC, he - h0), st = (gs + s) % p.nst;
+            const int g = s / n_sub, sub = s - g * n_sub;
+            const int h0 = hb + sub * p.SC, len = min(p.SC, he - h0), st = (gs + s) % p.nst;
+            const int rg = min(kRG, r - g * kRG);
             uint16_t *xs = (uint16_t *)(smem + p.off_x + st * p.x_stage_bytes);
             uint16_t *as = (uint16_t *)(smem + p.off_a + st * p.a_stage_bytes);
+            const uint16_t *Ag = Ab + (long long)g * kRG * p.in_dim + h0;
             const uint32_t rowb = (uint32_t)len * 2;
-            if (lane == 0) mbar_expect_tx(&full[st], rowb * (uint32_t)(n + r));
+            if (lane == 0) mbar_expect_tx(&full[st], rowb * (uint32_t)(n + rg));
             __syncwarp();
-            for (int i = lane; i < n + r; i += 32) {
+            for (int i = lane; i < n + rg; i += 32) {
                 if (i < n)
                     bulk_g2s(xs + i * p.xs_stride, p.in + (long long)(s_rows[i] / p.row_div) * p.ld_in + h0, rowb,
                              &full[st]);
                 else
-                    bulk_g2s(as + (i - n) * p.as_stride, Ab + (long long)(i - n) * p.in_dim + h0, rowb, &full[st]);
+                    bulk_g2s(as + (i - n) * p.as_stride, Ag + (long long)(i - n) * p.in_dim, rowb, &full[st]);
             }
         };
         if (warp == 0) {
             // the stages were last read through the generic proxy
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            for (int s = 0; s < min(n_sub, p.nst); ++s) issue(s);
+            for (int s = 0; s < min(n_stage, p.nst); ++s) issue(s);
         }
 
-        const int nnb = (r + 7) >> 3;
         ShrinkAcc<NBMAX> acc;
         shrink_acc_zero(acc);
-        for (int s = 0; s < n_sub; ++s) {
+        for (int s = 0; s < n_stage; ++s) {
             const int st = (gs + s) % p.nst;
+            const int g = s / n_sub, sub = s - g * n_sub;
+            const int rg = min(kRG, r - g * kRG), nnb = (rg + 7) >> 3;
             mbar_wait(&full[st], (uint32_t)(((gs + s) / p.nst) & 1), p.spin_limit, p.status);
-            const int len = min(p.SC, he - hb - s * p.SC);
+            const int len = min(p.SC, he - hb - sub * p.SC);
             const uint16_t *xs = (const uint16_t *)(smem + p.off_x + st * p.x_stage_bytes);
             const uint16_t *as = (const uint16_t *)(smem + p.off_a + st * p.a_stage_bytes);
             shrink_stage_mma(xs, p.xs_stride, as, p.as_stride, len, nnb, warp, lane, acc);
-            __syncthreads();
-            if (warp == 0 && s + p.nst < n_sub) {
+            __syncthreads();  // every warp is done with stage st (and with red of the last group)
+            if (warp == 0 && s + p.nst < n_stage) {
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 issue(s + p.nst);
             }
+            if (sub == n_sub - 1) {
+                // group g of this chunk: the warps' sums, then ranks g*kRG.. of
+                // each row to part[c][j][row0 + t][g*kRG + k]
+                for (int i = tid; i < kSWarps * kTileRows * kRG; i += kSThreads) red[i] = 0.f;
+                __syncthreads();
+                shrink_store_red(red, kRG, nnb, rg, n, warp, lane, acc);
+                __syncthreads();
+                const int gw = min(kRG, p.R8 - g * kRG);
+                float *dst = p.part + ((long long)c * p.n_slices + j) * p.rows * p.R8 + (long long)row0 * p.R8 +
+                             g * kRG;
+                for (int i = tid; i < n * gw; i += kSThreads) {
+                    const int t = i / gw, k = i - t * gw;
+                    float sum = 0.f;
+                    for (int w = 0; w < kSWarps; ++w) sum += red[(w * kTileRows + t) * kRG + k];
+                    dst[(long long)t * p.R8 + k] = sum;
+                }
+                shrink_acc_zero(acc);
+            }
         }
-        gs += n_sub;
-
-        // partials of this chunk: [4 warps][16][R8] in shared memory, summed
-        // over the warps, then one row of R8 floats per token to global memory
-        for (int i = tid; i < kSWarps * kTileRows * p.R8; i += kSThreads) red[i] = 0.f;
-        __syncthreads();
-        shrink_store_red(red, p.R8, nnb, r, n, warp, lane, acc);
-        __syncthreads();
-        // this chunk's partial: part[c][j][row0 + t][k]
-        float *dst = p.part + ((long long)c * p.n_slices + j) * p.rows * p.R8 + (long long)row0 * p.R8;
-        for (int i = tid; i < n * p.R8; i += kSThreads) {
-            const int t = i / p.R8, k = i - t * p.R8;
-            float sum = 0.f;
-            for (int w = 0; w < kSWarps; ++w) sum += red[(w * kTileRows + t) * p.R8 + k];
-            dst[i] = sum;
-        }
+        gs += n_stage;
     }
     if (dyn) finish_items(p.ticket);
 }
@@ -415,8 +432,11 @@ __device__ __forceinline__ void sts32(void *a, uint32_t v) {
 // for; the metadata was complete before the shrink started.
 
 // KS: the most 16-rank k steps of any slot (ceil(R8 / 16), 1..4).
+// Narrow passes keep 5 CTAs per SM, except for ranks above 32, whose larger v
+// fragments would spill there: 4 (the many-adapter batch measured 6% faster).
 template <int KS, int PW>
-__global__ void __launch_bounds__(kThreads, PW == 8 ? 3 : 5) bgmv_expand_kernel(const __grid_constant__ EArgs p) {
+__global__ void __launch_bounds__(kThreads, PW == 8 ? 3 : (KS >= 3 ? 4 : 5))
+    bgmv_expand_kernel(const __grid_constant__ EArgs p) {
     extern __shared__ __align__(128) char smem[];
     __shared__ __align__(8) uint64_t bbar, ybar;
     __shared__ int s_rows[kTileRows];
@@ -700,15 +720,16 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     // kernel instances for the pool's most 8-rank blocks (rounded up to 1, 2, 4, 8)
     const int nbr = R8 / 8;
     const int NBM = nbr <= 1 ? 1 : nbr <= 2 ? 2 : nbr <= 4 ? 4 : 8;
-    void (*shrink_fn)(SArgs) = NBM == 1 ? bgmv_shrink_kernel<1> : NBM == 2 ? bgmv_shrink_kernel<2>
-                             : NBM == 4 ? bgmv_shrink_kernel<4> : bgmv_shrink_kernel<8>;
+    // the per-tile shrink takes the ranks in groups of kRG
+    void (*shrink_fn)(SArgs) = R8 <= 8 ? bgmv_shrink_kernel<1> : bgmv_shrink_kernel<2>;
+    const int RG8 = std::min(R8, kRG);
     void (*slot_fn)(SArgs) = NBM == 1 ? bgmv_shrink_slot_kernel<1> : NBM == 2 ? bgmv_shrink_slot_kernel<2>
                            : NBM == 4 ? bgmv_shrink_slot_kernel<4> : bgmv_shrink_slot_kernel<8>;
     const int dev = pool->device < 64 ? pool->device : 63;
     if (!g_split_configured[dev]) {
-        void (*const fns[])(SArgs) = {bgmv_shrink_kernel<1>, bgmv_shrink_kernel<2>, bgmv_shrink_kernel<4>,
-                                      bgmv_shrink_kernel<8>, bgmv_shrink_slot_kernel<1>, bgmv_shrink_slot_kernel<2>,
-                                      bgmv_shrink_slot_kernel<4>, bgmv_shrink_slot_kernel<8>};
+        void (*const fns[])(SArgs) = {bgmv_shrink_kernel<1>, bgmv_shrink_kernel<2>, bgmv_shrink_slot_kernel<1>,
+                                      bgmv_shrink_slot_kernel<2>, bgmv_shrink_slot_kernel<4>,
+                                      bgmv_shrink_slot_kernel<8>};
         for (auto f : fns)
             LORA_CUDA_TRY(cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024));
         void (*const efns[])(EArgs) = {bgmv_expand_kernel<1, 8>, bgmv_expand_kernel<2, 8>, bgmv_expand_kernel<3, 8>,
@@ -718,18 +739,23 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
             LORA_CUDA_TRY(cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024));
         g_split_configured[dev] = 1;
     }
-    // shrink shared memory: 2 stages of (16 + R8) rows x SC columns (rows
-    // padded by 16 bytes); the partial sums reuse the stages.  SC: the widest
+    // per-tile shrink shared memory: 2 stages of (16 + min(R8, kRG)) rows x SC
+    // columns (rows padded by 16 bytes) and the group sums.  SC: the widest
     // stage (up to the chunk, <= 75 KB, three CTAs per SM) whose occupancy
     // still runs every item in one wave, else the widest that fits
-    const int red_bytes = 4 * kTileRows * R8 * 4;
+    const int red_bytes = 4 * kTileRows * R8 * 4;  // key-major shrink: [4 warps][16][R8] sums
+    const size_t red_g = a128((size_t)4 * kTileRows * kRG * 4);
+    // 2 wide stages: a 3-stage ring of narrower stages measured slower on the
+    // many-adapter batch
+    const int nst = 2;
+    const size_t s_budget = 75 * 1024;
     auto smem_for = [&](int sc) {
-        return std::max((size_t)red_bytes, 2 * (a128((size_t)kTileRows * (sc + 8) * 2) + a128((size_t)R8 * (sc + 8) * 2)));
+        return nst * (a128((size_t)kTileRows * (sc + 8) * 2) + a128((size_t)RG8 * (sc + 8) * 2)) + red_g;
     };
     const long long s_items = max_tiles * ns * NC;
     int SC = 0, occ = 0, first = 0, first_occ = 0;
     for (int sc = (HC < 1024 ? HC : 1024); sc >= 64; sc -= 64) {
-        if (smem_for(sc) > 75 * 1024) continue;
+        if (smem_for(sc) > s_budget) continue;
         int o = 0;
         LORA_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, shrink_fn, kSThreads, smem_for(sc)));
         if (!first) {
@@ -749,9 +775,6 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     }
     if (!SC) return LORA_OK;
     size_t s_smem = smem_for(SC);
-    // 2 wide stages: a 3-stage ring of narrower stages measured slower on the
-    // many-adapter batch
-    const int nst = 2;
     // expand shared memory: B rows, y rows, v hi/lo
     const int vr_stride = ns * R8 + 8;
     // 512 output columns per expand item for small ranks (fewer items, less fixed work per column)
@@ -815,11 +838,11 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     sa.xs_stride = SC + 8;
     sa.as_stride = SC + 8;
     sa.x_stage_bytes = (int)a128((size_t)kTileRows * (SC + 8) * 2);
-    sa.a_stage_bytes = (int)a128((size_t)R8 * (SC + 8) * 2);
+    sa.a_stage_bytes = (int)a128((size_t)RG8 * (SC + 8) * 2);
     sa.off_x = 0;
     sa.nst = nst;
     sa.off_a = nst * sa.x_stage_bytes;
-    sa.off_red = 0;  // the partial sums reuse the stages: an item's copies are all consumed by then
+    sa.off_red = sa.off_a + nst * sa.a_stage_bytes;  // group sums apart from the stages (the next group's copies are in flight)
     sa.part = (float *)ws;
     sa.ticket = tickets;
     sa.rows = pr.rows;
@@ -895,7 +918,7 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
         cfg.dynamicSmemBytes = slot_smem;
         LORA_CUDA_TRY(cudaLaunchKernelEx(&cfg, slot_fn, sa));
     } else {
-        if ((size_t)sa.off_red + red_bytes > s_smem) return LORA_ERR_INVALID_ARG;  // layout check
+        if ((size_t)sa.off_red + red_g > s_smem) return LORA_ERR_INVALID_ARG;  // layout check
         cfg.gridDim = dim3((unsigned)(s_items < 2 * s_slots ? s_items : 2 * s_slots), 1, 1);
         cfg.dynamicSmemBytes = s_smem;
         LORA_CUDA_TRY(cudaLaunchKernelEx(&cfg, shrink_fn, sa));

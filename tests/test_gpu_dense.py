@@ -55,6 +55,15 @@ def test_tiny_token_counts(T):
     run_and_check(small_case(11, T=T, p_none=0.0))
 
 
+@pytest.mark.parametrize("T,seed", [(8, 23), (24, 21)])
+def test_per_tile_rank_groups(T, seed):
+    # fewer rows than 4 per slot: the per-tile shrink, which takes the ranks 16
+    # at a time; ranks that end inside a group, a single rank, and rank 0 (the
+    # seeds give tokens to slots 0, 1, 2, 3 and 5)
+    run_and_check(small_case(seed, T=T, H=3000, out_dims=(264,), Lk=8, R=64,
+                             ranks=(64, 40, 57, 1, 24, 33, 16, 0), p_none=0.1))
+
+
 def test_preset_tiny():
     run_and_check(gen.tiny())
 

@@ -197,117 +197,182 @@ __device__ __forceinline__ void shrink_store_red(float *red, int R8, int nnb, in
 
 // ---------------------------------------------------------------- shrink
 //
-// Items (16-row tile, slice j, hidden chunk c), strided over a grid of at
+// Items (16-row tile, slice j, hidden chunk c), spread over a grid of at
 // most a few waves.  The slot's ranks are taken kRG at a time: for each rank
 // group the chunk streams through a ring of stages holding the tile's x rows
 // and the group's A rows, SC columns each (rows padded by 16 bytes so
 // ldmatrix reads are free of bank conflicts).  Few rows per stage keep the
 // stages wide, so every row copy is long whatever the rank; the x rows are
-// fetched again for each group (from L2).  The MMAs as in shrink_stage_mma;
-// at the end of a group the four warps' sums are added in shared memory and
-// the group's ranks of the unscaled chunk partial stored.
+// fetched again for each group (from L2).
+//
+// Warp-specialized: a copy warp takes the items (from the counter), hands
+// each to the MMA warps through a two-entry descriptor ring and issues its
+// stages as ring slots come free, running ahead across items; the four MMA
+// warps wait for full stages, multiply (as in shrink_stage_mma), release the
+// slot, and at the end of a rank group add their sums in shared memory and
+// store the group's ranks of the unscaled chunk partial.  No CTA-wide barrier
+// sits between stages or items.
 
-constexpr int kRG = 16;  // ranks per group (two 8-rank MMA blocks)
+constexpr int kRG = 16;                      // ranks per group (two 8-rank MMA blocks)
+constexpr int kPThreads = kSThreads + 32;    // per-tile shrink: 4 MMA warps + 1 copy warp
+
+struct ShrinkItem {
+    int valid, row0, n, r, j, c;
+};
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 
 template <int NBMAX>  // 1 or 2: 8-rank blocks of a group
-__global__ void __launch_bounds__(kSThreads) bgmv_shrink_kernel(const __grid_constant__ SArgs p) {
+__global__ void __launch_bounds__(kPThreads) bgmv_shrink_kernel(const __grid_constant__ SArgs p) {
     extern __shared__ __align__(128) char smem[];
-    __shared__ __align__(8) uint64_t full[4];
-    __shared__ int s_rows[kTileRows];
+    __shared__ __align__(8) uint64_t full[4], empty[4], ifull[2], iempty[2];
+    __shared__ ShrinkItem s_info[2];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-
     const int per_tile = p.n_slices * p.NC;
-
-    __shared__ int s_item;
+    const int nst = p.nst;
+    if (tid == 0) {
+        for (int q = 0; q < nst; ++q) {
+            mbar_init(&full[q], 1);
+            mbar_init(&empty[q], kSWarps);
+        }
+        for (int q = 0; q < 2; ++q) {
+            mbar_init(&ifull[q], 1);
+            mbar_init(&iempty[q], kSWarps);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int n_tiles = p.counters[p.count_idx];
     const int total = n_tiles * per_tile;
     // the expand may launch and prefetch its weights and outputs now
     asm volatile("griddepcontrol.launch_dependents;");
-    if (tid < p.nst) mbar_init(&full[tid], 1);
-    if (tid == 0) asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    float *red = (float *)(smem + p.off_red);  // [4 warps][16][kRG], apart from the stages
-    int gs = 0;  // stages consumed by this CTA so far (ring slot and phase)
-
     // more items than CTAs: take them from the counter; else one item per CTA
     const bool dyn = total > (int)gridDim.x;
-    for (int item = dyn ? take_item(p.ticket, &s_item) : (int)blockIdx.x; item < total;
-         item = dyn ? take_item(p.ticket, &s_item) : total) {
-        const int tile = item / per_tile, rem = item - tile * per_tile;
-        const int j = rem / p.NC, c = rem - j * p.NC;
-        const int row0 = p.tile_row0[tile];
-        const int keyn = p.tile_keyn[tile];
-        const int n = keyn & 31, key = keyn >> 5;
-        const int a = key / p.E, e = key - a * p.E;
-        const int r = p.rank[a];
-        const uint16_t *Ab = a_rows(p, j, a, e);
+
+    if (warp == kSWarps) {
+        // ---------------- copy warp
+        int gs = 0;  // stages issued by this CTA (ring slot and phase)
+        int item = (int)blockIdx.x;
+        if (dyn) {
+            int t = 0;
+            if (lane == 0) t = atomicAdd(p.ticket, 1);
+            item = __shfl_sync(~0u, t, 0);
+        }
+        for (int ii = 0;; ++ii) {
+            const int k = ii & 1;
+            mbar_wait(&iempty[k], ((ii >> 1) & 1) ^ 1, p.spin_limit, p.status);
+            if (item >= total) {
+                if (lane == 0) {
+                    s_info[k].valid = 0;
+                    mbar_arrive(&ifull[k]);
+                }
+                break;
+            }
+            const int tile = item / per_tile, rem = item - tile * per_tile;
+            const int j = rem / p.NC, c = rem - j * p.NC;
+            const int row0 = p.tile_row0[tile];
+            const int keyn = p.tile_keyn[tile];
+            const int n = keyn & 31, key = keyn >> 5;
+            const int a = key / p.E, e = key - a * p.E;
+            const int r = p.rank[a];
+            if (lane == 0) {
+                s_info[k].valid = 1;
+                s_info[k].row0 = row0;
+                s_info[k].n = n;
+                s_info[k].r = r;
+                s_info[k].j = j;
+                s_info[k].c = c;
+                mbar_arrive(&ifull[k]);  // release: the MMA warps read the descriptor after their wait
+            }
+            // lane i < n copies x row i of the tile
+            const long long xrow = lane < n ? (long long)(p.sorted[row0 + lane] / p.row_div) * p.ld_in : 0ll;
+            const uint16_t *Ab = a_rows(p, j, a, e);
+            const int hb = c * p.HC, he = min(p.in_dim, hb + p.HC);
+            const int n_sub = (he - hb + p.SC - 1) / p.SC;
+            const int n_stage = n_sub * ((r + kRG - 1) / kRG);  // groups x column stages
+            for (int s = 0; s < n_stage; ++s, ++gs) {
+                const int st = gs % nst;
+                mbar_wait(&empty[st], ((gs / nst) & 1) ^ 1, p.spin_limit, p.status);
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                const int g = s / n_sub, sub = s - g * n_sub;
+                const int h0 = hb + sub * p.SC, len = min(p.SC, he - h0);
+                const int rg = min(kRG, r - g * kRG);
+                uint16_t *xs = (uint16_t *)(smem + p.off_x + st * p.x_stage_bytes);
+                uint16_t *as = (uint16_t *)(smem + p.off_a + st * p.a_stage_bytes);
+                const uint16_t *Ag = Ab + (long long)g * kRG * p.in_dim + h0;
+                const uint32_t rowb = (uint32_t)len * 2;
+                if (lane == 0) mbar_expect_tx(&full[st], rowb * (uint32_t)(n + rg));
+                __syncwarp();
+                for (int i = lane; i < n + rg; i += 32) {
+                    if (i < n)
+                        bulk_g2s(xs + i * p.xs_stride, p.in + xrow + h0, rowb, &full[st]);
+                    else
+                        bulk_g2s(as + (i - n) * p.as_stride, Ag + (long long)(i - n) * p.in_dim, rowb, &full[st]);
+                }
+            }
+            if (dyn) {
+                int t = 0;
+                if (lane == 0) t = atomicAdd(p.ticket, 1);
+                item = __shfl_sync(~0u, t, 0);
+            } else {
+                item = total;
+            }
+        }
+        return;  // the MMA warps synchronise among themselves from here on
+    }
+
+    // ---------------- MMA warps
+    float *red = (float *)(smem + p.off_red);  // [2][4 warps][16][kRG], apart from the stages
+    int gs = 0, gg = 0;                        // stages and rank groups consumed
+    for (int ii = 0;; ++ii) {
+        const int k = ii & 1;
+        mbar_wait(&ifull[k], (ii >> 1) & 1, p.spin_limit, p.status);
+        const ShrinkItem it = s_info[k];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&iempty[k]);
+        if (!it.valid) break;
+        const int n = it.n, r = it.r, j = it.j, c = it.c, row0 = it.row0;
         const int hb = c * p.HC, he = min(p.in_dim, hb + p.HC);
         const int n_sub = (he - hb + p.SC - 1) / p.SC;
-        const int n_stage = n_sub * ((r + kRG - 1) / kRG);  // groups x column stages
-        __syncthreads();  // the previous item is done with s_rows, the stages and red
-        if (tid < n) s_rows[tid] = p.sorted[row0 + tid];
-        __syncthreads();
-
-        auto issue = [&](int s) {
-            const int g = s / n_sub, sub = s - g * n_sub;
-            const int h0 = hb + sub * p.SC, len = min(p.SC, he - h0), st = (gs + s) % p.nst;
-            const int rg = min(kRG, r - g * kRG);
-            uint16_t *xs = (uint16_t *)(smem + p.off_x + st * p.x_stage_bytes);
-            uint16_t *as = (uint16_t *)(smem + p.off_a + st * p.a_stage_bytes);
-            const uint16_t *Ag = Ab + (long long)g * kRG * p.in_dim + h0;
-            const uint32_t rowb = (uint32_t)len * 2;
-            if (lane == 0) mbar_expect_tx(&full[st], rowb * (uint32_t)(n + rg));
-            __syncwarp();
-            for (int i = lane; i < n + rg; i += 32) {
-                if (i < n)
-                    bulk_g2s(xs + i * p.xs_stride, p.in + (long long)(s_rows[i] / p.row_div) * p.ld_in + h0, rowb,
-                             &full[st]);
-                else
-                    bulk_g2s(as + (i - n) * p.as_stride, Ag + (long long)(i - n) * p.in_dim, rowb, &full[st]);
-            }
-        };
-        if (warp == 0) {
-            // the stages were last read through the generic proxy
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            for (int s = 0; s < min(n_stage, p.nst); ++s) issue(s);
-        }
-
+        const int n_stage = n_sub * ((r + kRG - 1) / kRG);
         ShrinkAcc<NBMAX> acc;
         shrink_acc_zero(acc);
-        for (int s = 0; s < n_stage; ++s) {
-            const int st = (gs + s) % p.nst;
+        for (int s = 0; s < n_stage; ++s, ++gs) {
+            const int st = gs % nst;
             const int g = s / n_sub, sub = s - g * n_sub;
             const int rg = min(kRG, r - g * kRG), nnb = (rg + 7) >> 3;
-            mbar_wait(&full[st], (uint32_t)(((gs + s) / p.nst) & 1), p.spin_limit, p.status);
+            mbar_wait(&full[st], (uint32_t)((gs / nst) & 1), p.spin_limit, p.status);
             const int len = min(p.SC, he - hb - sub * p.SC);
             const uint16_t *xs = (const uint16_t *)(smem + p.off_x + st * p.x_stage_bytes);
             const uint16_t *as = (const uint16_t *)(smem + p.off_a + st * p.a_stage_bytes);
             shrink_stage_mma(xs, p.xs_stride, as, p.as_stride, len, nnb, warp, lane, acc);
-            __syncthreads();  // every warp is done with stage st (and with red of the last group)
-            if (warp == 0 && s + p.nst < n_stage) {
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                issue(s + p.nst);
-            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[st]);  // this warp is done with the slot
             if (sub == n_sub - 1) {
-                // group g of this chunk: the warps' sums, then ranks g*kRG.. of
-                // each row to part[c][j][row0 + t][g*kRG + k]
-                for (int i = tid; i < kSWarps * kTileRows * kRG; i += kSThreads) red[i] = 0.f;
-                __syncthreads();
-                shrink_store_red(red, kRG, nnb, rg, n, warp, lane, acc);
-                __syncthreads();
+                // group g of this chunk: the warps' sums (double-buffered: the
+                // barrier of the next group orders this group's reads before
+                // the buffer is written again), then ranks g*kRG.. of each row
+                // to part[c][j][row0 + t][g*kRG + k]
+                float *rb = red + (gg & 1) * (kSWarps * kTileRows * kRG);
+                shrink_store_red(rb, kRG, nnb, rg, n, warp, lane, acc);
+                asm volatile("bar.sync 1, %0;" ::"n"(kSThreads) : "memory");
                 const int gw = min(kRG, p.R8 - g * kRG);
                 float *dst = p.part + ((long long)c * p.n_slices + j) * p.rows * p.R8 + (long long)row0 * p.R8 +
                              g * kRG;
                 for (int i = tid; i < n * gw; i += kSThreads) {
-                    const int t = i / gw, k = i - t * gw;
+                    const int t = i / gw, kk = i - t * gw;
                     float sum = 0.f;
-                    for (int w = 0; w < kSWarps; ++w) sum += red[(w * kTileRows + t) * kRG + k];
-                    dst[(long long)t * p.R8 + k] = sum;
+                    if (kk < rg)
+                        for (int w = 0; w < kSWarps; ++w) sum += rb[(w * kTileRows + t) * kRG + kk];
+                    dst[(long long)t * p.R8 + kk] = sum;
                 }
                 shrink_acc_zero(acc);
+                ++gg;
             }
         }
-        gs += n_stage;
     }
     if (dyn) finish_items(p.ticket);
 }
@@ -744,7 +809,7 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     // stage (up to the chunk, <= 75 KB, three CTAs per SM) whose occupancy
     // still runs every item in one wave, else the widest that fits
     const int red_bytes = 4 * kTileRows * R8 * 4;  // key-major shrink: [4 warps][16][R8] sums
-    const size_t red_g = a128((size_t)4 * kTileRows * kRG * 4);
+    const size_t red_g = a128((size_t)2 * 4 * kTileRows * kRG * 4);  // two group-sum buffers
     // 2 wide stages: a 3-stage ring of narrower stages measured slower on the
     // many-adapter batch
     const int nst = 2;
@@ -757,7 +822,7 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     for (int sc = (HC < 1024 ? HC : 1024); sc >= 64; sc -= 64) {
         if (smem_for(sc) > s_budget) continue;
         int o = 0;
-        LORA_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, shrink_fn, kSThreads, smem_for(sc)));
+        LORA_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, shrink_fn, kPThreads, smem_for(sc)));
         if (!first) {
             first = sc;
             first_occ = o;
@@ -920,6 +985,7 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     } else {
         if ((size_t)sa.off_red + red_g > s_smem) return LORA_ERR_INVALID_ARG;  // layout check
         cfg.gridDim = dim3((unsigned)(s_items < 2 * s_slots ? s_items : 2 * s_slots), 1, 1);
+        cfg.blockDim = dim3(kPThreads, 1, 1);
         cfg.dynamicSmemBytes = s_smem;
         LORA_CUDA_TRY(cudaLaunchKernelEx(&cfg, shrink_fn, sa));
     }

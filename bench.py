@@ -94,7 +94,8 @@ def apply_kernels(name, policy):
     elif policy == 2:
         k = "cluster_lora_kernel (one pass, cluster DSMEM reduction)"
     else:
-        k = ("split shrink (bgmv_shrink_slot_kernel key-major, or bgmv_shrink_kernel per tile) + "
+        k = ("split shrink (bgmv_shrink_slot_kernel key-major, or bgmv_shrink_kernel / bgmv_shrink_tile_kernel "
+             "per tile) + "
              "bgmv_expand_kernel, chained by programmatic dependent launch")
     if is_sink(name):
         return k + " on w13, sink_act_kernel, the same on w2"

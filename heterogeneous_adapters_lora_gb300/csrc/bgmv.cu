@@ -11,6 +11,8 @@
 //     copies (cp.async.bulk + mbarrier) bring the tile's x rows and the
 //     slot's A_j rows of chunk c, 16 ranks at a time; m16n8k16 bf16 MMAs
 //     (fp32 accumulate) give the partial v of chunk c, stored unscaled in fp32.
+//   bgmv_shrink_tile_kernel: the same items when they fit the grid (one per
+//     CTA), all ranks of the slot per stage.
 //   bgmv_shrink_slot_kernel: the same partials from one CTA per (key, slice,
 //     chunk) that multiplies every tile of the key against its A rows.
 //   bgmv_expand_kernel: items (tile, 256 or 512 output columns).  Before it waits
@@ -193,6 +195,111 @@ __device__ __forceinline__ void shrink_store_red(float *red, int R8, int nnb, in
             }
         }
     }
+}
+
+// ---------------------------------------------------------------- shrink, one item per CTA
+//
+// For batches whose per-tile items fit the grid (one item per CTA): items
+// (16-row tile, slice j, hidden chunk c), two stages of [16 x rows][r A rows]
+// x SC columns, rows padded by 16 bytes so ldmatrix reads are free of bank
+// conflicts; the MMAs as in shrink_stage_mma, the four warps' partial sums
+// added in shared memory (reusing the stages).  With one item per CTA there
+// is nothing to run ahead to, and this shorter chain starts sooner than the
+// copy-warp kernel below.
+
+template <int NBMAX>
+__global__ void __launch_bounds__(kSThreads) bgmv_shrink_tile_kernel(const __grid_constant__ SArgs p) {
+    extern __shared__ __align__(128) char smem[];
+    __shared__ __align__(8) uint64_t full[4];
+    __shared__ int s_rows[kTileRows];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    const int per_tile = p.n_slices * p.NC;
+
+    __shared__ int s_item;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int n_tiles = p.counters[p.count_idx];
+    const int total = n_tiles * per_tile;
+    // the expand may launch and prefetch its weights and outputs now
+    asm volatile("griddepcontrol.launch_dependents;");
+    if (tid < p.nst) mbar_init(&full[tid], 1);
+    if (tid == 0) asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    float *red = (float *)(smem + p.off_red);
+    int gs = 0;  // sub-stages consumed by this CTA so far (ring slot and phase)
+
+    // more items than CTAs: take them from the counter; else one item per CTA
+    const bool dyn = total > (int)gridDim.x;
+    for (int item = dyn ? take_item(p.ticket, &s_item) : (int)blockIdx.x; item < total;
+         item = dyn ? take_item(p.ticket, &s_item) : total) {
+        const int tile = item / per_tile, rem = item - tile * per_tile;
+        const int j = rem / p.NC, c = rem - j * p.NC;
+        const int row0 = p.tile_row0[tile];
+        const int keyn = p.tile_keyn[tile];
+        const int n = keyn & 31, key = keyn >> 5;
+        const int a = key / p.E, e = key - a * p.E;
+        const int r = p.rank[a];
+        const uint16_t *Ab = a_rows(p, j, a, e);
+        const int hb = c * p.HC, he = min(p.in_dim, hb + p.HC);
+        const int n_sub = (he - hb + p.SC - 1) / p.SC;
+        __syncthreads();  // the previous item is done with s_rows, the stages and red
+        if (tid < n) s_rows[tid] = p.sorted[row0 + tid];
+        __syncthreads();
+
+        auto issue = [&](int s) {
+            const int h0 = hb + s * p.SC, len = min(p.SC, he - h0), st = (gs + s) % p.nst;
+            uint16_t *xs = (uint16_t *)(smem + p.off_x + st * p.x_stage_bytes);
+            uint16_t *as = (uint16_t *)(smem + p.off_a + st * p.a_stage_bytes);
+            const uint32_t rowb = (uint32_t)len * 2;
+            if (lane == 0) mbar_expect_tx(&full[st], rowb * (uint32_t)(n + r));
+            __syncwarp();
+            for (int i = lane; i < n + r; i += 32) {
+                if (i < n)
+                    bulk_g2s(xs + i * p.xs_stride, p.in + (long long)(s_rows[i] / p.row_div) * p.ld_in + h0, rowb,
+                             &full[st]);
+                else
+                    bulk_g2s(as + (i - n) * p.as_stride, Ab + (long long)(i - n) * p.in_dim + h0, rowb, &full[st]);
+            }
+        };
+        if (warp == 0) {
+            // the stages were last read through the generic proxy
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            for (int s = 0; s < min(n_sub, p.nst); ++s) issue(s);
+        }
+
+        const int nnb = (r + 7) >> 3;
+        ShrinkAcc<NBMAX> acc;
+        shrink_acc_zero(acc);
+        for (int s = 0; s < n_sub; ++s) {
+            const int st = (gs + s) % p.nst;
+            mbar_wait(&full[st], (uint32_t)(((gs + s) / p.nst) & 1), p.spin_limit, p.status);
+            const int len = min(p.SC, he - hb - s * p.SC);
+            const uint16_t *xs = (const uint16_t *)(smem + p.off_x + st * p.x_stage_bytes);
+            const uint16_t *as = (const uint16_t *)(smem + p.off_a + st * p.a_stage_bytes);
+            shrink_stage_mma(xs, p.xs_stride, as, p.as_stride, len, nnb, warp, lane, acc);
+            __syncthreads();
+            if (warp == 0 && s + p.nst < n_sub) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                issue(s + p.nst);
+            }
+        }
+        gs += n_sub;
+
+        // partials of this chunk: [4 warps][16][R8] in shared memory, summed
+        // over the warps, then one row of R8 floats per token to global memory
+        for (int i = tid; i < kSWarps * kTileRows * p.R8; i += kSThreads) red[i] = 0.f;
+        __syncthreads();
+        shrink_store_red(red, p.R8, nnb, r, n, warp, lane, acc);
+        __syncthreads();
+        // this chunk's partial: part[c][j][row0 + t][k]
+        float *dst = p.part + ((long long)c * p.n_slices + j) * p.rows * p.R8 + (long long)row0 * p.R8;
+        for (int i = tid; i < n * p.R8; i += kSThreads) {
+            const int t = i / p.R8, k = i - t * p.R8;
+            float sum = 0.f;
+            for (int w = 0; w < kSWarps; ++w) sum += red[(w * kTileRows + t) * p.R8 + k];
+            dst[i] = sum;
+        }
+    }
+    if (dyn) finish_items(p.ticket);
 }
 
 // ---------------------------------------------------------------- shrink
@@ -792,9 +899,11 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
                            : NBM == 4 ? bgmv_shrink_slot_kernel<4> : bgmv_shrink_slot_kernel<8>;
     const int dev = pool->device < 64 ? pool->device : 63;
     if (!g_split_configured[dev]) {
-        void (*const fns[])(SArgs) = {bgmv_shrink_kernel<1>, bgmv_shrink_kernel<2>, bgmv_shrink_slot_kernel<1>,
-                                      bgmv_shrink_slot_kernel<2>, bgmv_shrink_slot_kernel<4>,
-                                      bgmv_shrink_slot_kernel<8>};
+        void (*const fns[])(SArgs) = {bgmv_shrink_kernel<1>,      bgmv_shrink_kernel<2>,
+                                      bgmv_shrink_tile_kernel<1>, bgmv_shrink_tile_kernel<2>,
+                                      bgmv_shrink_tile_kernel<4>, bgmv_shrink_tile_kernel<8>,
+                                      bgmv_shrink_slot_kernel<1>, bgmv_shrink_slot_kernel<2>,
+                                      bgmv_shrink_slot_kernel<4>, bgmv_shrink_slot_kernel<8>};
         for (auto f : fns)
             LORA_CUDA_TRY(cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024));
         void (*const efns[])(EArgs) = {bgmv_expand_kernel<1, 8>, bgmv_expand_kernel<2, 8>, bgmv_expand_kernel<3, 8>,
@@ -840,6 +949,38 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     }
     if (!SC) return LORA_OK;
     size_t s_smem = smem_for(SC);
+    // every per-tile item fits two waves: one item per CTA, the CTA-synchronous
+    // kernel with full-rank stages (the partial sums reuse them)
+    void (*tile_fn)(SArgs) = NBM == 1 ? bgmv_shrink_tile_kernel<1> : NBM == 2 ? bgmv_shrink_tile_kernel<2>
+                           : NBM == 4 ? bgmv_shrink_tile_kernel<4> : bgmv_shrink_tile_kernel<8>;
+    const int red_t = 4 * kTileRows * R8 * 4;
+    auto smem_t = [&](int sc) {
+        return std::max((size_t)red_t, 2 * (a128((size_t)kTileRows * (sc + 8) * 2) + a128((size_t)R8 * (sc + 8) * 2)));
+    };
+    int SC_t = 0, occ_t = 0;
+    {
+        int first_t = 0, first_occ_t = 0;
+        for (int sc = (HC < 1024 ? HC : 1024); sc >= 64; sc -= 64) {
+            if (smem_t(sc) > 75 * 1024) continue;
+            int o = 0;
+            LORA_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, tile_fn, kSThreads, smem_t(sc)));
+            if (!first_t) {
+                first_t = sc;
+                first_occ_t = o;
+            }
+            if (sc < 256) break;  // narrower stages only when nothing wider fits
+            if ((long long)o * pool->num_sms >= s_items) {
+                SC_t = sc;
+                occ_t = o;
+                break;
+            }
+        }
+        if (!SC_t) {
+            SC_t = first_t;
+            occ_t = first_occ_t;
+        }
+    }
+    const bool tile_static = SC_t > 0 && occ_t > 0 && s_items <= 2LL * pool->num_sms * occ_t;
     // expand shared memory: B rows, y rows, v hi/lo
     const int vr_stride = ns * R8 + 8;
     // 512 output columns per expand item for small ranks (fewer items, less fixed work per column)
@@ -993,11 +1134,27 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
         cfg.dynamicSmemBytes = slot_smem;
         LORA_CUDA_TRY(cudaLaunchKernelEx(&cfg, slot_fn, sa));
     } else {
-        if ((size_t)sa.off_red + red_g > s_smem) return LORA_ERR_INVALID_ARG;  // layout check
-        cfg.gridDim = dim3((unsigned)(s_items < 2 * s_slots ? s_items : 2 * s_slots), 1, 1);
-        cfg.blockDim = dim3(kPThreads, 1, 1);
-        cfg.dynamicSmemBytes = s_smem;
-        LORA_CUDA_TRY(cudaLaunchKernelEx(&cfg, shrink_fn, sa));
+        if (tile_static) {
+            sa.SC = SC_t;
+            sa.xs_stride = SC_t + 8;
+            sa.as_stride = SC_t + 8;
+            sa.x_stage_bytes = (int)a128((size_t)kTileRows * (SC_t + 8) * 2);
+            sa.a_stage_bytes = (int)a128((size_t)R8 * (SC_t + 8) * 2);
+            sa.off_x = 0;
+            sa.off_a = nst * sa.x_stage_bytes;
+            sa.off_red = 0;  // the partial sums reuse the stages: an item's copies are all consumed by then
+            if ((size_t)sa.off_a + nst * sa.a_stage_bytes > smem_t(SC_t) || (size_t)red_t > smem_t(SC_t))
+                return LORA_ERR_INVALID_ARG;  // layout check
+            cfg.gridDim = dim3((unsigned)s_items, 1, 1);
+            cfg.dynamicSmemBytes = smem_t(SC_t);
+            LORA_CUDA_TRY(cudaLaunchKernelEx(&cfg, tile_fn, sa));
+        } else {
+            if ((size_t)sa.off_red + red_g > s_smem) return LORA_ERR_INVALID_ARG;  // layout check
+            cfg.gridDim = dim3((unsigned)(s_items < 2 * s_slots ? s_items : 2 * s_slots), 1, 1);
+            cfg.blockDim = dim3(kPThreads, 1, 1);
+            cfg.dynamicSmemBytes = s_smem;
+            LORA_CUDA_TRY(cudaLaunchKernelEx(&cfg, shrink_fn, sa));
+        }
     }
     lora_note_launch();
     cfg.blockDim = dim3(kThreads, 1, 1);

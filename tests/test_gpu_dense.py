@@ -56,12 +56,20 @@ def test_tiny_token_counts(T):
 
 
 @pytest.mark.parametrize("T,seed", [(8, 23), (24, 21)])
-def test_per_tile_rank_groups(T, seed):
-    # fewer rows than 4 per slot: the per-tile shrink, which takes the ranks 16
-    # at a time; ranks that end inside a group, a single rank, and rank 0 (the
-    # seeds give tokens to slots 0, 1, 2, 3 and 5)
+def test_per_tile_one_item_per_cta(T, seed):
+    # fewer rows than 4 per slot and few tiles: the per-tile shrink with one
+    # item per CTA; ranks that end inside an 8-rank block, a single rank and
+    # rank 0 (the seeds give tokens to slots 0, 1, 2, 3 and 5)
     run_and_check(small_case(seed, T=T, H=3000, out_dims=(264,), Lk=8, R=64,
                              ranks=(64, 40, 57, 1, 24, 33, 16, 0), p_none=0.1))
+
+
+def test_per_tile_rank_groups_many_items():
+    # 512 tokens over 1024 slots: more per-tile items than two waves, so the
+    # copy-warp shrink that takes the ranks 16 at a time; ranks that end inside
+    # a group (40, 57, 24, 33), a single rank and rank 0
+    ranks = tuple((64, 40, 57, 1, 24, 33, 16, 0)[i % 8] for i in range(1024))
+    run_and_check(small_case(31, T=512, H=1024, out_dims=(264,), Lk=1024, R=64, ranks=ranks, p_none=0.1))
 
 
 def test_preset_tiny():

@@ -497,63 +497,92 @@ def run_gpu(args, rank, world, local_rank):
         stream.synchronize()
         meta_ms = a0.elapsed_time(a1) / (reps * KA)
 
-        # end to end through the public API with host buffers: H2D of the
-        # step's inputs from pinned memory, the calls, D2H of the result
-        r = runs[0]
+        # end to end through the public API with host buffers: every step copies
+        # its inputs in from pinned host memory, makes the calls and copies its
+        # result out.  As a serving loop does, consecutive steps are pipelined
+        # over two sets of device buffers: step i's copies in (one copy
+        # stream), step i-1's calls (the compute stream) and step i-2's copy
+        # out (a second copy stream) run at the same time; a buffer set is
+        # refilled only once its previous result has been copied out.
+        e_runs = [runs[0], runs[1] if len(runs) > 1 else None]
+        if e_runs[1] is None:
+            e_runs[1] = (Hn.MoERun(c, device=dev) if moe else Hn.SinkRun(c, device=dev) if sink
+                         else Hn.LinearRun(c, bias, device=dev) if lin else Hn.DenseRun(c, device=dev))
+
+        def pin(a):
+            return torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+
         if moe:
-            h_in = [torch.from_numpy(np.ascontiguousarray(c.x).view(np.int16)).pin_memory(),
-                    torch.from_numpy(np.ascontiguousarray(c.ic2).view(np.int16)).pin_memory(),
-                    torch.from_numpy(c.idx).pin_memory(),
-                    torch.from_numpy(np.ascontiguousarray(c.topk_ids)).pin_memory(),
-                    torch.from_numpy(np.ascontiguousarray(c.topk_w).reshape(-1)).pin_memory(),
-                    torch.from_numpy(c.ic1_0.view(np.int16)).pin_memory(),
-                    torch.from_numpy(c.ic3_0.view(np.int16)).pin_memory()]
-            d_in = [r.x, r.ic2, r.idx, r.topk, r.topk_w, r.ic1, r.ic3]
-            h_out = [torch.empty_like(r.ic1, device="cpu").pin_memory(),
-                     torch.empty_like(r.ic3, device="cpu").pin_memory()]
-            d_out = [r.ic1, r.ic3]
+            h_in = [pin(c.x.view(np.int16)), pin(c.ic2.view(np.int16)), pin(c.idx), pin(c.topk_ids),
+                    pin(c.topk_w.reshape(-1)), pin(c.ic1_0.view(np.int16)), pin(c.ic3_0.view(np.int16))]
+
+            def io(r):
+                return [r.x, r.ic2, r.idx, r.topk, r.topk_w, r.ic1, r.ic3], [r.ic1, r.ic3]
         elif lin:
-            h_in = [torch.from_numpy(np.ascontiguousarray(c.x).view(np.int16)).pin_memory(),
-                    torch.from_numpy(c.idx).pin_memory()]
-            d_in = [r.x, r.idx]
-            h_out = [torch.empty_like(r.y, device="cpu").pin_memory()]
-            d_out = [r.y]
+            h_in = [pin(c.x.view(np.int16)), pin(c.idx)]
+
+            def io(r):
+                return [r.x, r.idx], [r.y]
         elif sink:
-            h_in = [torch.from_numpy(np.ascontiguousarray(c.w13.x).view(np.int16)).pin_memory(),
-                    torch.from_numpy(c.w13.idx).pin_memory(),
-                    torch.from_numpy(c.w13.y0.view(np.int16)).pin_memory(),
-                    torch.from_numpy(c.gammas).pin_memory(),
-                    torch.from_numpy(c.w2.y0.view(np.int16)).pin_memory()]
-            d_in = [r.r13.x, r.r13.idx, r.r13.y, r.gammas, r.r2.y]
-            h_out = [torch.empty_like(r.r2.y, device="cpu").pin_memory()]
-            d_out = [r.r2.y]
+            h_in = [pin(c.w13.x.view(np.int16)), pin(c.w13.idx), pin(c.w13.y0.view(np.int16)), pin(c.gammas),
+                    pin(c.w2.y0.view(np.int16))]
+
+            def io(r):
+                return [r.r13.x, r.r13.idx, r.r13.y, r.gammas, r.r2.y], [r.r2.y]
         else:
-            h_in = [torch.from_numpy(np.ascontiguousarray(c.x).view(np.int16)).pin_memory(),
-                    torch.from_numpy(c.idx).pin_memory(),
-                    torch.from_numpy(c.y0.view(np.int16)).pin_memory()]
-            d_in = [r.x, r.idx, r.y]
-            h_out = [torch.empty_like(r.y, device="cpu").pin_memory()]
-            d_out = [r.y]
+            h_in = [pin(c.x.view(np.int16)), pin(c.idx), pin(c.y0.view(np.int16))]
+
+            def io(r):
+                return [r.x, r.idx, r.y], [r.y]
+        h_out = [[torch.empty_like(d, device="cpu").pin_memory() for d in io(r)[1]] for r in e_runs]
         bi = sum(t.numel() * t.element_size() for t in h_in)
-        bo = sum(t.numel() * t.element_size() for t in h_out)
+        bo = sum(t.numel() * t.element_size() for t in h_out[0])
+        s_in = torch.cuda.Stream(device=dev)
+        s_out = torch.cuda.Stream(device=dev)
 
-        def e2e_step():
-            for h, d in zip(h_in, d_in):
-                d.copy_(h, non_blocking=True)
-            step(r)
-            for h, d in zip(h_out, d_out):
-                h.copy_(d, non_blocking=True)
+        def e2e_steps(n):
+            """n pipelined steps; every stream joins the current one at the end."""
+            ev_in = [torch.cuda.Event() for _ in range(n)]
+            ev_calls = [torch.cuda.Event() for _ in range(n)]
+            ev_out = [torch.cuda.Event() for _ in range(n)]
+            start = torch.cuda.Event()
+            start.record(stream)
+            s_in.wait_event(start)
+            s_out.wait_event(start)
+            for i in range(n):
+                b = i % 2
+                r = e_runs[b]
+                d_in, d_out = io(r)
+                if i >= 2:
+                    s_in.wait_event(ev_out[i - 2])  # set b's last result is out, its calls done
+                with torch.cuda.stream(s_in):
+                    for h, d in zip(h_in, d_in):
+                        d.copy_(h, non_blocking=True)
+                    ev_in[i].record(s_in)
+                stream.wait_event(ev_in[i])
+                with torch.cuda.stream(stream):
+                    step(r)
+                    ev_calls[i].record(stream)
+                s_out.wait_event(ev_calls[i])
+                with torch.cuda.stream(s_out):
+                    for h, d in zip(h_out[b], d_out):
+                        h.copy_(d, non_blocking=True)
+                    ev_out[i].record(s_out)
+            stream.wait_event(ev_in[n - 1])
+            stream.wait_event(ev_out[n - 1])
 
-        for _ in range(max(1, args.warmup)):
-            e2e_step()
+        with torch.cuda.stream(stream):
+            for _ in range(max(1, args.warmup)):
+                e2e_steps(2)
         stream.synchronize()
-        # the step with its copies captured as one CUDA graph (pinned-memory
-        # copies are graph nodes), as a serving loop would replay it
+        # the pipelined steps captured as one CUDA graph of G steps (pinned-memory
+        # copies and the cross-stream waits are graph nodes), replayed
+        G = 16
         e2e_graph = None
         try:
             ge = torch.cuda.CUDAGraph()
             with torch.cuda.graph(ge, stream=stream):
-                e2e_step()
+                e2e_steps(G)
             ge.replay()
             stream.synchronize()
             e2e_graph = ge
@@ -564,12 +593,15 @@ def run_gpu(args, rank, world, local_rank):
             dist.barrier()
         f0 = torch.cuda.Event(enable_timing=True)
         f1 = torch.cuda.Event(enable_timing=True)
+        reps = max(1, -(-args.steps // G))
+        e2e_n = reps * G
         f0.record(stream)
-        for _ in range(args.steps):
-            if e2e_graph is not None:
-                e2e_graph.replay()
-            else:
-                e2e_step()
+        with torch.cuda.stream(stream):
+            for _ in range(reps):
+                if e2e_graph is not None:
+                    e2e_graph.replay()
+                else:
+                    e2e_steps(G)
         f1.record(stream)
         stream.synchronize()
         e2e_ms = f0.elapsed_time(f1)
@@ -582,7 +614,7 @@ def run_gpu(args, rank, world, local_rank):
 
     tokens = c.T
     value = whole_job_throughput(tokens, args.steps, world, ms)
-    e2e = whole_job_throughput(tokens, args.steps, world, e2e_ms)
+    e2e = whole_job_throughput(tokens, e2e_n, world, e2e_ms)
     peak, peak_kind = load_peaks()
     kbytes = (ab["w13"] + ab["w2"]) if moe else (ab["total"] - ab["idx"])
     achieved = kbytes / (kms * 1e-3) / 1e9
@@ -608,8 +640,10 @@ def run_gpu(args, rank, world, local_rank):
                      "algorithmic_bytes_per_launch": kbytes, "avg_launch_us": kms * 1e3},
         "clocks": cs.summary(),
         "e2e": {"value": e2e, "unit": "tokens/s", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
-                "timing": "one CUDA graph per step: pinned H2D copies, metadata, apply, D2H copy"
-                          if e2e_graph is not None else "eager calls per step"},
+                "steps": e2e_n,
+                "timing": (f"CUDA graphs of {G} steps pipelined over two buffer sets: pinned H2D copies "
+                           "(copy stream), metadata + apply (compute stream), D2H copy (second copy stream)")
+                          if e2e_graph is not None else "eager pipelined calls"},
         "gpu_launches": launches_per_step * args.steps,
     }
     if not args.no_cpu_baseline:

@@ -27,6 +27,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "lora_internal.cuh"
 #include "mma_common.cuh"
@@ -509,6 +510,11 @@ __global__ void __launch_bounds__(kSThreads) bgmv_shrink_slot_kernel(const __gri
     // tables written before the metadata build started (never by it): read through L2
     const int r = (__ldcg(p.enabled + a) != 0) ? __ldcg(p.rank + a) : 0;
     if (r <= 0) {
+        // Even with nothing to do, trigger the expand only once the metadata
+        // build is complete: the expand reads the tile lists and rewrites y
+        // rows before its own wait, which is safe only because every CTA of
+        // this grid has waited before it triggers.
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         asm volatile("griddepcontrol.launch_dependents;");
         return;
     }
@@ -851,7 +857,8 @@ __global__ void __launch_bounds__(kThreads, PW == 8 ? 3 : (KS >= 3 ? 4 : 5))
 
 size_t a128(size_t x) { return (x + 127) & ~(size_t)127; }
 
-int g_split_configured[64];
+// per device: shared-memory limits raised (first calls from several host threads may race)
+std::atomic<int> g_split_configured[64];
 int g_key_major_waves = 8;  // most waves of the key-major shrink grid
 
 // Hidden chunks of a shrink item: ~32 KB of A rows at full rank, >= 256
@@ -898,7 +905,7 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     void (*slot_fn)(SArgs) = NBM == 1 ? bgmv_shrink_slot_kernel<1> : NBM == 2 ? bgmv_shrink_slot_kernel<2>
                            : NBM == 4 ? bgmv_shrink_slot_kernel<4> : bgmv_shrink_slot_kernel<8>;
     const int dev = pool->device < 64 ? pool->device : 63;
-    if (!g_split_configured[dev]) {
+    if (!g_split_configured[dev].load(std::memory_order_acquire)) {
         void (*const fns[])(SArgs) = {bgmv_shrink_kernel<1>,      bgmv_shrink_kernel<2>,
                                       bgmv_shrink_tile_kernel<1>, bgmv_shrink_tile_kernel<2>,
                                       bgmv_shrink_tile_kernel<4>, bgmv_shrink_tile_kernel<8>,
@@ -911,7 +918,7 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
                                        bgmv_expand_kernel<3, 4>, bgmv_expand_kernel<4, 4>};
         for (auto f : efns)
             LORA_CUDA_TRY(cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024));
-        g_split_configured[dev] = 1;
+        g_split_configured[dev].store(1, std::memory_order_release);
     }
     // per-tile shrink shared memory: 2 stages of (16 + min(R8, kRG)) rows x SC
     // columns (rows padded by 16 bytes) and the group sums.  SC: the widest

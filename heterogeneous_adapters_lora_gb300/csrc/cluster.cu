@@ -25,6 +25,8 @@
 // metadata kernel finishes; griddepcontrol.wait orders its metadata reads.
 #include <string.h>
 
+#include <atomic>
+
 #include "lora_internal.cuh"
 #include "mma_common.cuh"
 
@@ -409,7 +411,7 @@ CPlan make_cplan(int ns, int in_dim, int out_total, int R, int CS) {
     return c;
 }
 
-int g_cluster_configured[64];
+std::atomic<int> g_cluster_configured[64];
 
 }  // namespace
 
@@ -484,10 +486,10 @@ lora_status_t lora_cluster_apply(const lora_pool_t *pool, const LoraProblem &pr,
     a.post_scale = pr.post_scale;
 
     const int dev = pool->device < 64 ? pool->device : 63;
-    if (!g_cluster_configured[dev]) {
+    if (!g_cluster_configured[dev].load(std::memory_order_acquire)) {
         LORA_CUDA_TRY(cudaFuncSetAttribute(cluster_lora_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)kBudget1));
-        g_cluster_configured[dev] = 1;
+        g_cluster_configured[dev].store(1, std::memory_order_release);
     }
     const long long max_tiles = pr.rows / kTileRows + (pr.rows < pr.n_keys ? pr.rows : pr.n_keys);
     if (max_tiles <= 0) {

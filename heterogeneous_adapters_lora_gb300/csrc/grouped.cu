@@ -423,18 +423,19 @@ static_assert(kMaxSmem <= 48 * 1024, "grouped kernel must fit the default shared
 static_assert((size_t)kTile * (((LORA_MAX_RANK + 7) & ~7) + 4) * 4 <= kMaxSmem, "v tile");
 
 // Occupancy per (device, mode), queried once outside any stream capture.
-int g_occ[64][3];
+std::atomic<int> g_occ[64][3];
 
 template <int MODE>
 lora_status_t launch(const lora_pool_t *pool, GArgs &g, long long est_items, cudaStream_t s) {
     const size_t smem = smem_bytes(g);
     int dev = pool->device < 64 ? pool->device : 63;
-    int &occ = g_occ[dev][MODE];
+    int occ = g_occ[dev][MODE].load(std::memory_order_relaxed);
     if (occ == 0) {
         int o = 0;
         LORA_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, grouped_lora_kernel<MODE>,
                                                                     kThreads, kMaxSmem));
         occ = o < 1 ? 1 : o;
+        g_occ[dev][MODE].store(occ, std::memory_order_relaxed);  // every thread computes the same value
     }
     long long grid = (long long)pool->num_sms * occ;
     if (est_items < grid) grid = est_items;
@@ -856,7 +857,7 @@ extern "C" lora_status_t lora_moe_apply(const lora_pool_t *pool, const lora_meta
 namespace {
 constexpr size_t kStaticScratchBytes = (size_t)8 << 20;  // 8 MiB
 __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
-void *g_static_scratch_addr[64];
+std::atomic<void *> g_static_scratch_addr[64];  // looked up once per device
 }  // namespace
 
 extern "C" lora_status_t lora_apply_slices_static(const lora_pool_t *pool, const lora_meta_t *meta,
@@ -873,12 +874,13 @@ extern "C" lora_status_t lora_apply_slices_static(const lora_pool_t *pool, const
     int dev = -1;
     LORA_CUDA_TRY(cudaGetDevice(&dev));
     if (dev != pool->device || dev < 0 || dev >= 64) return LORA_ERR_INVALID_ARG;
-    if (!g_static_scratch_addr[dev]) {
-        void *addr = nullptr;
-        if (cudaGetSymbolAddress(&addr, g_static_scratch) != cudaSuccess || !addr) return LORA_ERR_CUDA;
-        g_static_scratch_addr[dev] = addr;
+    void *scratch = g_static_scratch_addr[dev].load(std::memory_order_acquire);
+    if (!scratch) {
+        // two host threads making their first call on this device at once
+        // both look the address up and store the same value
+        if (cudaGetSymbolAddress(&scratch, g_static_scratch) != cudaSuccess || !scratch) return LORA_ERR_CUDA;
+        g_static_scratch_addr[dev].store(scratch, std::memory_order_release);
     }
-    void *scratch = g_static_scratch_addr[dev];
     const Plan pl0 = make_plan(pool->num_sms, g.in_dim, g.n_slices, g.R, meta->T, pool->desc.max_loras);
     const size_t cnt_bytes = align256(pl0.cnt_ints * 4);
     if (kCtrlBytes + cnt_bytes >= kStaticScratchBytes) return LORA_ERR_CAPACITY;

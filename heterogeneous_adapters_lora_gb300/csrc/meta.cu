@@ -14,6 +14,8 @@
 //   4. groups = non-empty keys, tiles of LORA_TILE_ROWS rows per group
 #include <string.h>
 
+#include <atomic>
+
 #include "lora_internal.cuh"
 
 namespace {
@@ -366,12 +368,12 @@ lora_status_t lora_launch_build_meta(const lora_pool_t *pool, const int32_t *d_i
     a.m = *meta;
     const size_t smem = (size_t)(used + (cache ? rows : 0)) * 4;
     // raise the kernel's shared-memory limit once per device (outside any capture)
-    static int configured[64];
+    static std::atomic<int> configured[64];
     const int dev = pool->device < 64 ? pool->device : 63;
-    if (!configured[dev]) {
+    if (!configured[dev].load(std::memory_order_acquire)) {
         LORA_CUDA_TRY(cudaFuncSetAttribute(build_meta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            kSmemBudgetInts * 4));
-        configured[dev] = 1;
+        configured[dev].store(1, std::memory_order_release);
     }
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));

@@ -25,6 +25,8 @@
 #include <cudaTypedefs.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "lora_internal.cuh"
 #include "tc_common.cuh"
 
@@ -386,7 +388,7 @@ bool make_map(CUtensorMap *m, const void *base, long long cols, long long rows, 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int g_sgmv_configured[64];
+std::atomic<int> g_sgmv_configured[64];
 
 }  // namespace
 
@@ -426,12 +428,12 @@ lora_status_t lora_sgmv_apply(const lora_pool_t *pool, const lora_meta_t *meta, 
     int out_total = 0;
     for (int j = 0; j < ns; ++j) out_total += d.out_dims[j];
     const int dev = pool->device < 64 ? pool->device : 63;
-    if (!g_sgmv_configured[dev]) {
+    if (!g_sgmv_configured[dev].load(std::memory_order_acquire)) {
         LORA_CUDA_TRY(cudaFuncSetAttribute(sgmv_shrink_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            200 * 1024));
         LORA_CUDA_TRY(cudaFuncSetAttribute(sgmv_expand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            200 * 1024));
-        g_sgmv_configured[dev] = 1;
+        g_sgmv_configured[dev].store(1, std::memory_order_release);
     }
     const int max_lt = T / kRows + d.max_loras + 1;
     if (spin_limit > (1 << 18)) spin_limit = 1 << 18;  // each poll may suspend the thread for a while

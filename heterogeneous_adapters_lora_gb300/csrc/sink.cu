@@ -12,6 +12,8 @@
 // the w13 expand drains and lets the w2 shrink fetch its weights meanwhile.
 #include <string.h>
 
+#include <atomic>
+
 #include "lora_internal.cuh"
 
 namespace {
@@ -63,7 +65,7 @@ __global__ void __launch_bounds__(kThreads) sink_act_kernel(const uint16_t *__re
     }
 }
 
-int g_sink_sms[64];
+std::atomic<int> g_sink_sms[64];  // SM count per device, looked up once
 
 }  // namespace
 
@@ -80,14 +82,15 @@ extern "C" lora_status_t lora_sink_experts_act(const void *gate_up, int64_t ld_g
     int dev = 0;
     LORA_CUDA_TRY(cudaGetDevice(&dev));
     if (dev < 0 || dev >= 64) return LORA_ERR_INVALID_ARG;
-    if (!g_sink_sms[dev]) {
-        int sms = 0;
-        LORA_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-        g_sink_sms[dev] = sms > 0 ? sms : 1;
+    int n_sms = g_sink_sms[dev].load(std::memory_order_relaxed);
+    if (!n_sms) {
+        LORA_CUDA_TRY(cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev));
+        n_sms = n_sms > 0 ? n_sms : 1;
+        g_sink_sms[dev].store(n_sms, std::memory_order_relaxed);
     }
     const long long vecs = (long long)T * (W / 8);
     long long grid = (vecs + kThreads - 1) / kThreads;
-    const long long cap = (long long)g_sink_sms[dev] * 8;
+    const long long cap = (long long)n_sms * 8;
     if (grid > cap) grid = cap;
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));

@@ -22,6 +22,21 @@ def from_dev_u16(t: torch.Tensor) -> np.ndarray:
     return t.cpu().numpy().view(np.uint16)
 
 
+# bf16 bits written into the padding columns of padded rows: a NaN, so a
+# kernel that read padding into a product would show it in its output
+PAD_BITS = 0x7FC1
+
+
+def to_dev_u16_padded(a: np.ndarray, pad: int, device="cuda") -> torch.Tensor:
+    """[rows][cols] bf16 bits -> device [rows][cols + pad]; pad columns hold PAD_BITS."""
+    if pad == 0:
+        return to_dev_u16(a, device)
+    rows, cols = a.shape
+    host = np.full((rows, cols + pad), PAD_BITS, np.uint16)
+    host[:, :cols] = a
+    return to_dev_u16(host, device)
+
+
 class MetaBuffer:
     """Caller-owned metadata buffer bound to a ``lora_meta_t``."""
 
@@ -101,14 +116,18 @@ def upload_moe_slot(pool, case, a, stream=None):
 class DenseRun:
     """A dense case resident on the GPU: pool, x, y, idx, meta, workspace."""
 
-    def __init__(self, case, device="cuda", lm_head=False, max_rows=None):
+    def __init__(self, case, device="cuda", lm_head=False, max_rows=None, x_pad=0, y_pad=0):
         self.case = case
         self.pool = L.lora_pool_create(dense_desc(case, lm_head))
         for a in range(case.L):
             if case.ranks[a] > 0 and case.enabled[a]:
                 upload_dense_slot(self.pool, case, a)
-        self.x = to_dev_u16(case.x, device)
-        self.y = to_dev_u16(case.y0, device)
+        # rows of x and y may be wider than the layer (leading dimensions
+        # ldx = H + x_pad, ldy = out_total + y_pad)
+        self.ldx = case.H + x_pad
+        self.ldy = case.out_total + y_pad
+        self.x = to_dev_u16_padded(case.x, x_pad, device)
+        self.y = to_dev_u16_padded(case.y0, y_pad, device)
         self.idx = torch.from_numpy(case.idx).to(device)
         T = max_rows if max_rows is not None else case.T
         self.mb = MetaBuffer(max(T, 1), case.L, device)
@@ -120,16 +139,19 @@ class DenseRun:
         L.lora_build_meta(self.pool, self.idx, T, None, 1, self.mb.meta)
 
     def apply(self):
-        c = self.case
-        L.lora_apply_slices(self.pool, self.mb.meta, self.x, c.H, self.y, c.out_total, self.ws,
+        L.lora_apply_slices(self.pool, self.mb.meta, self.x, self.ldx, self.y, self.ldy, self.ws,
                             self.ws_bytes)
 
     def step(self):
         self.build_meta()
         self.apply()
 
-    def y_host(self) -> np.ndarray:
+    def y_full_host(self) -> np.ndarray:
+        """All ldy columns of y, padding included."""
         return from_dev_u16(self.y)
+
+    def y_host(self) -> np.ndarray:
+        return np.ascontiguousarray(self.y_full_host()[:, :self.case.out_total])
 
     def status(self) -> int:
         return L.lora_get_device_status(self.pool)
@@ -149,16 +171,19 @@ class DenseRun:
 class MoERun:
     """A MoE case resident on the GPU."""
 
-    def __init__(self, case, device="cuda"):
+    def __init__(self, case, device="cuda", in_pad=0, out_pad=0):
         self.case = case
         self.pool = L.lora_pool_create(moe_desc(case))
         for a in range(case.L):
             if case.ranks[a] > 0 and case.enabled[a]:
                 upload_moe_slot(self.pool, case, a)
-        self.x = to_dev_u16(case.x, device)
-        self.ic2 = to_dev_u16(case.ic2, device)
-        self.ic1 = to_dev_u16(case.ic1_0, device)
-        self.ic3 = to_dev_u16(case.ic3_0, device)
+        # rows of the inputs (x, ic2) and outputs (ic1, ic3) may be wider than
+        # the layer: ld_in = width + in_pad, ld_out = width + out_pad
+        self.in_pad, self.out_pad = in_pad, out_pad
+        self.x = to_dev_u16_padded(case.x, in_pad, device)
+        self.ic2 = to_dev_u16_padded(case.ic2, in_pad, device)
+        self.ic1 = to_dev_u16_padded(case.ic1_0, out_pad, device)
+        self.ic3 = to_dev_u16_padded(case.ic3_0, out_pad, device)
         self.idx = torch.from_numpy(case.idx).to(device)
         self.topk = torch.from_numpy(np.ascontiguousarray(case.topk_ids)).to(device)
         self.topk_w = torch.from_numpy(np.ascontiguousarray(case.topk_w).reshape(-1)).to(device)
@@ -173,13 +198,19 @@ class MoERun:
 
     def w13(self):
         c = self.case
-        L.lora_moe_apply(self.pool, self.mb.meta, L.MOE_W13, self.x, c.D, None, self.ic1,
-                         c.n13 * c.F13, self.ws, self.ws_bytes)
+        L.lora_moe_apply(self.pool, self.mb.meta, L.MOE_W13, self.x, c.D + self.in_pad, None, self.ic1,
+                         c.n13 * c.F13 + self.out_pad, self.ws, self.ws_bytes)
 
     def w2(self):
         c = self.case
-        L.lora_moe_apply(self.pool, self.mb.meta, L.MOE_W2, self.ic2, c.F, self.topk_w, self.ic3, c.D,
-                         self.ws, self.ws_bytes)
+        L.lora_moe_apply(self.pool, self.mb.meta, L.MOE_W2, self.ic2, c.F + self.in_pad, self.topk_w, self.ic3,
+                         c.D + self.out_pad, self.ws, self.ws_bytes)
+
+    def ic1_host(self) -> np.ndarray:
+        return np.ascontiguousarray(from_dev_u16(self.ic1)[:, :self.case.n13 * self.case.F13])
+
+    def ic3_host(self) -> np.ndarray:
+        return np.ascontiguousarray(from_dev_u16(self.ic3)[:, :self.case.D])
 
     def step(self):
         self.build_meta()

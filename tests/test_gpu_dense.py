@@ -231,3 +231,27 @@ def test_cuda_graph_capture_of_meta_and_apply():
     _, d_ref = oracle.dense_delta(c)
     act = active_mask(c.idx, c.L, c.enabled, c.ranks)
     assert_delta(bf16_bits_to_f32(y)[act], d_ref[act], "graph")
+
+
+def test_apply_after_every_slot_reset_leaves_y():
+    # Every slot reset: the key-major shrink's CTAs all find rank 0 and leave
+    # at once.  They must still let the expand start only after the metadata
+    # build is complete, so the expand neither reads the previous build's
+    # tile lists nor rewrites y rows the previous apply is still storing.
+    c = gen.decode_qkv()
+    run = H.DenseRun(c)
+    try:
+        run.step()
+        y1 = run.y_host()
+        for a in range(c.L):
+            L.lora_reset(run.pool, a)
+        for _ in range(3):
+            run.step()
+        y2 = run.y_host()
+        assert run.status() == 0
+    finally:
+        run.close()
+    assert np.array_equal(y1, y2)
+    _, d_ref = oracle.dense_delta(c)
+    act = active_mask(c.idx, c.L, c.enabled, c.ranks)
+    assert_delta(bf16_bits_to_f32(y1)[act], d_ref[act], "before reset")

@@ -15,27 +15,45 @@ from gpu_util import active_mask, assert_delta
 pytestmark = pytest.mark.gpu
 
 
-def _run(c, with_bias):
+def _run(c, with_bias, bias_std=0.5, ldx=None, ldy=None):
+    """Run the full linear layer; returns (y as float64 [T][out_total], base of
+    the oracle (x W^T + bias, float64), delta of the oracle, active rows)."""
     rng = np.random.default_rng(c.T)
-    bias = f32_to_bf16_bits(rng.normal(0, 0.5, c.out_total).astype(np.float32)) if with_bias else None
+    bias = f32_to_bf16_bits(rng.normal(0, bias_std, c.out_total).astype(np.float32)) if with_bias else None
     y_ref = oracle.linear(c, c.W, bias)
+    _, d_ref = oracle.dense_delta(c)
+    d_ref = d_ref.astype(np.float64)
+    base = y_ref - d_ref
+    ldx = c.H if ldx is None else ldx
+    ldy = c.out_total if ldy is None else ldy
     run = H.DenseRun(c)
     try:
         run.build_meta()
+        x = torch.zeros((c.T, ldx), dtype=torch.int16, device="cuda")
+        x[:, :c.H] = run.x
+        y = torch.full((c.T, ldy), 0x7fc0, dtype=torch.int16, device="cuda")  # NaN fill: all of y is written
         d_w = H.to_dev_u16(c.W)
         d_b = H.to_dev_u16(bias) if with_bias else None
-        L.lora_linear_apply(run.pool, run.mb.meta, run.x, c.H, d_w, c.H, d_b, run.y, c.out_total, run.ws,
-                            run.ws_bytes)
-        y = run.y_host()
+        L.lora_linear_apply(run.pool, run.mb.meta, x, ldx, d_w, c.H, d_b, y, ldy, run.ws, run.ws_bytes)
+        yh = H.from_dev_u16(y)
         assert run.status() == 0
     finally:
         run.close()
-    got = bf16_bits_to_f32(y).astype(np.float64)
-    assert_delta(got, y_ref, c.name + " full linear")
-    # rows without an adapter are the base layer's output alone
+    # the padding columns of y are not the layer's: left as they were
+    assert np.all(yh[:, c.out_total:] == 0x7fc0)
+    got = bf16_bits_to_f32(np.ascontiguousarray(yh[:, :c.out_total])).astype(np.float64)
     act = active_mask(c.idx, c.L, c.enabled, c.ranks)
-    base = oracle.linear(c, c.W, bias) - oracle.dense_delta(c)[1].astype(np.float64)
+    # whole output within the delta tolerance, rows without an adapter = base alone
+    assert_delta(got, y_ref, c.name + " full linear")
     assert_delta(got[~act], base[~act], c.name + " base rows")
+    return got, base, d_ref, act
+
+
+def _small_base(c, w_std, seed):
+    """Replace the case's base weight by one whose output is of the delta's size."""
+    rng = np.random.default_rng(seed)
+    c.W = f32_to_bf16_bits(rng.normal(0, w_std, (c.out_total, c.H)).astype(np.float32))
+    return c
 
 
 @pytest.mark.parametrize("with_bias", [False, True])
@@ -47,6 +65,36 @@ def test_linear_decode_qkv_shapes():
     c = gen.dense_case(name="linear_qkv", T=256, H=4096, out_dims=(4096, 1024, 1024), L=32, R=16, seed=1102,
                        scales=np.full(32, 2.0, np.float32), p_none=0.1, with_W=True, std=0.05)
     _run(c, True)
+
+
+@pytest.mark.parametrize("shape", ["tiny", "qkv"])
+def test_linear_delta_isolated(shape):
+    # The base output x W^T + bias is made about as large as the delta, so the
+    # delta y - base (base from the oracle) is checked at the delta tolerance
+    # on its own: a delta a few percent wrong fails here, where a large base
+    # would hide it in the whole-output norm.  Padded leading dimensions of x
+    # and y are exercised at the same time.
+    if shape == "tiny":
+        c = _small_base(gen.tiny(), 0.002, 3)
+        ldx, ldy = c.H + 24, c.out_total + 40
+    else:
+        c = gen.dense_case(name="linear_qkv_small_base", T=256, H=4096, out_dims=(4096, 1024, 1024), L=32, R=16,
+                           seed=1103, scales=np.full(32, 2.0, np.float32), p_none=0.1, with_W=True, std=0.02)
+        c = _small_base(c, 0.002, 4)
+        ldx, ldy = c.H + 64, c.out_total + 8
+    got, base, d_ref, act = _run(c, True, bias_std=0.002, ldx=ldx, ldy=ldy)
+    assert np.abs(base[act]).max() < 4 * np.abs(d_ref[act]).max()  # the base does not dominate
+    assert_delta(got[act] - base[act], d_ref[act], c.name + " delta alone")
+
+
+def test_linear_zero_base_is_the_delta():
+    # W = 0 and no bias: the layer's output is the delta itself
+    c = gen.tiny()
+    c.W = np.zeros_like(c.W)
+    got, base, d_ref, act = _run(c, False)
+    assert np.all(base == 0)
+    assert np.all(got[~act] == 0)
+    assert_delta(got[act], d_ref[act], "zero base")
 
 
 def test_linear_argument_errors():

@@ -9,6 +9,7 @@ from heterogeneous_adapters_lora_gb300 import harness as H
 from heterogeneous_adapters_lora_gb300 import inputs as gen
 from heterogeneous_adapters_lora_gb300 import lora as L
 from gpu_util import long_short_tiles, tile_keyn, tiles_from_groups
+from oracle_pins_util import load_golden
 
 pytestmark = pytest.mark.gpu
 
@@ -123,6 +124,57 @@ def test_moe_meta_preset_and_small():
             assert got["n_stiles"] == len(st)
         finally:
             run.close()
+
+
+def _check_moe_meta(c, expect):
+    """GPU MoE metadata of case c against the oracle (and, if given, against
+    the expected arrays of a hand-worked case)."""
+    run = H.MoERun(c)
+    try:
+        run.build_meta()
+        got = run.mb.read()
+        st = run.status()
+    finally:
+        run.close()
+    ref = oracle.moe_meta(c.topk_ids, c.idx, c.L, c.E, c.enabled, c.ranks)
+    assert np.array_equal(got["sorted"], ref.sorted_pair)
+    assert (got["n_active"], got["n_groups"], got["n_bad"]) == (ref.n_active, ref.n_groups, ref.n_bad)
+    assert np.array_equal(got["key_count"], ref.key_count)
+    assert np.array_equal(got["key_offset"], ref.key_offset)
+    assert np.array_equal(got["group_key"], ref.group_key)
+    assert np.array_equal(got["group_start"], ref.group_start)
+    tg, tr = tiles_from_groups(ref.group_start)
+    assert np.array_equal(got["tile_group"], tg) and np.array_equal(got["tile_row0"], tr)
+    assert np.array_equal(got["tile_keyn"], tile_keyn(tg, tr, ref.group_key, ref.group_start))
+    assert st == (L.CODE["LORA_ERR_DEVICE_INDEX"] if ref.n_bad else 0)
+    if expect is not None:
+        assert got["sorted"].tolist() == expect["sorted_pair"]
+        assert got["key_count"].tolist() == expect["key_count"]
+        assert got["group_key"].tolist() == expect["group_key"]
+        assert got["group_start"].tolist() == expect["group_start"]
+        assert got["n_bad"] == expect["n_bad"]
+
+
+def test_moe_meta_out_of_range_ids_hand_case():
+    # the hand-worked case of the oracle pins: expert ids -1, E, E+1 and -3,
+    # slot id L, an idx -1 token with a bad expert id
+    g = load_golden("moe_meta_bad_ids_by_hand.json")
+    c = gen.moe_case(T=g["T"], K=g["K"], E=g["E"], D=16, F=16, L=g["L"], R=4, seed=5, n13=1)
+    c.idx[:] = np.asarray(g["idx"], np.int32)
+    c.topk_ids[:] = np.asarray(g["topk_ids"], np.int32)
+    _check_moe_meta(c, g)
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_moe_meta_out_of_range_ids_random(seed):
+    rng = np.random.default_rng(70 + seed)
+    c = gen.moe_case(T=300, K=4, E=7, D=16, F=16, L=5, R=8, seed=seed, n13=1, ranks=(8, 0, 8, 8, 8),
+                     p_none=0.1)
+    bad = rng.random(c.topk_ids.shape) < 0.1
+    c.topk_ids[bad] = rng.choice(np.array([-2, -1, 7, 8, 100], np.int32), size=int(bad.sum()))
+    tb = rng.random(c.T) < 0.05
+    c.idx[tb] = rng.choice(np.array([-7, 5, 6], np.int32), size=int(tb.sum()))
+    _check_moe_meta(c, None)
 
 
 def test_meta_is_deterministic_across_runs():

@@ -107,3 +107,34 @@ def test_moe_decode_sparse_keys(T):
     """Decode-size MoE batches: T*K pairs over 512 (adapter, expert) keys, most
     keys empty or with one pair (the sparse-occupancy regime)."""
     run_and_check(gen.moe(T=T))
+
+
+@pytest.mark.parametrize("shared", [False, True])
+def test_out_of_range_ids_are_skipped_and_reported(shared):
+    # expert ids -1 and E, and slot ids L and -5, on some rows: those pairs get
+    # no delta (their rows stay bit-identical), the rest match the oracle, and
+    # the device status reports the bad ids
+    c = gen.moe_case(name="moe_bad_ids", T=70, K=3, E=6, D=1040, F=272, L=4, R=16, seed=41, shared_outer=shared,
+                     scales=(1.5, 0.5, 2.0, 1.0), p_none=0.1)
+    c.topk_ids[3, 0] = -1
+    c.topk_ids[10, 2] = c.E
+    c.topk_ids[11, 1] = c.E + 7
+    c.idx[20] = c.L
+    c.idx[21] = -5
+    run = H.MoERun(c)
+    try:
+        run.step()
+        ic1 = H.from_dev_u16(run.ic1)
+        ic3 = H.from_dev_u16(run.ic3)
+        st = run.status()
+    finally:
+        run.close()
+    assert st == H.L.CODE["LORA_ERR_DEVICE_INDEX"]
+    act = pair_active(c)
+    assert not act[3 * c.K] and not act[10 * c.K + 2] and not act[20 * c.K]
+    _, d13 = oracle.moe_w13(c)
+    _, d2 = oracle.moe_w2(c)
+    assert_rows_untouched(ic1, c.ic1_0, ~act)
+    assert_rows_untouched(ic3, c.ic3_0, ~act)
+    assert_delta(bf16_bits_to_f32(ic1)[act], d13[act], "bad ids w13")
+    assert_delta(bf16_bits_to_f32(ic3)[act], d2[act], "bad ids w2")

@@ -49,6 +49,18 @@ def test_golden_meta_by_hand():
     assert m.n_bad == g["n_bad"]
 
 
+def test_golden_moe_meta_bad_ids_by_hand():
+    g = load_golden("moe_meta_bad_ids_by_hand.json")
+    m = oracle.moe_meta(np.asarray(g["topk_ids"], np.int32), np.asarray(g["idx"], np.int32), g["L"], g["E"],
+                        np.asarray(g["enabled"], np.int32), np.asarray(g["rank"], np.int32))
+    assert m.sorted_pair.tolist() == g["sorted_pair"]
+    assert m.key_count.tolist() == g["key_count"]
+    assert m.key_offset.tolist() == g["key_offset"]
+    assert m.group_key.tolist() == g["group_key"]
+    assert m.group_start.tolist() == g["group_start"]
+    assert (m.n_active, m.n_groups, m.n_bad) == (g["n_active"], g["n_groups"], g["n_bad"])
+
+
 # ----------------------------------------------------------------- fp64 brute force
 
 def _tiny_dense(seed, T=7, H=48, out_dims=(16, 8, 8), L=3, R=4, ranks=(4, 2, 3), p_none=0.2):
@@ -236,25 +248,30 @@ def test_dense_meta_matches_numpy_stable_argsort(seed):
     assert m.n_bad == int(np.sum((idx != -1) & ((idx < 0) | (idx >= L))))
 
 
-@pytest.mark.parametrize("seed", range(4))
-def test_moe_meta_matches_numpy_lexsort(seed):
+@pytest.mark.parametrize("seed,bad_ids", [(s, b) for s in range(4) for b in (False, True)])
+def test_moe_meta_matches_numpy_lexsort(seed, bad_ids):
     rng = np.random.default_rng(100 + seed)
     T, K, E, L = int(rng.integers(1, 64)), int(rng.integers(1, 5)), int(rng.integers(1, 9)), 4
-    topk = rng.integers(0, E, size=(T, K)).astype(np.int32)
-    idx = rng.integers(-1, L, size=T).astype(np.int32)
+    # with bad_ids, expert ids run from -2 to E + 1 and slot ids from -2 to L + 1
+    lo, hi = (-2, 2) if bad_ids else (0, 0)
+    topk = rng.integers(lo, E + hi, size=(T, K)).astype(np.int32)
+    idx = rng.integers(-1 + lo, L + hi, size=T).astype(np.int32)
     enabled = np.array([1, 0, 1, 1], np.int32)
     rank = np.array([4, 4, 0, 4], np.int32)
     m = oracle.moe_meta(topk, idx, L, E, enabled, rank)
     pt = np.repeat(np.arange(T), K)
     a = idx[pt]
-    act = (a >= 0) & np.isin(a, np.nonzero(enabled & (rank > 0))[0])
-    key = np.where(act, a * E + topk.reshape(-1), L * E)
+    e = topk.reshape(-1)
+    act = (a >= 0) & np.isin(a, np.nonzero(enabled & (rank > 0))[0]) & (e >= 0) & (e < E)
+    key = np.where(act, a * E + e, L * E)
     assert np.array_equal(m.sorted_pair, np.argsort(key, kind="stable"))
     cnt = np.bincount(key[act], minlength=L * E)
     assert np.array_equal(m.key_count, cnt)
     assert np.array_equal(m.key_offset, np.concatenate([[0], np.cumsum(cnt)]))
     assert np.array_equal(m.group_key, np.nonzero(cnt)[0])
     assert m.n_active == int(act.sum())
+    n_bad = int(np.sum((idx != -1) & ((idx < 0) | (idx >= L)))) + int(np.sum((e < 0) | (e >= E)))
+    assert m.n_bad == n_bad
 
 
 # ----------------------------------------------------------------- planted mistakes
@@ -282,6 +299,9 @@ MUTANTS = {
                              "const double u = (double)bf(gate_up[(int64_t)t * ld_gu + c]);\n            const double g = (double)bf(gate_up[(int64_t)t * ld_gu + W + c]);"),
     "sink_gamma_by_column_mod": ("gammas[(int64_t)t * ld_gamma + c / d_mlp]", "gammas[(int64_t)t * ld_gamma + c % n_experts]"),
     "sink_sigmoid_only": ("round_bf16(g / (1.0 + exp(-g)))", "round_bf16(1.0 / (1.0 + exp(-g)))"),
+    "moe_meta_high_expert_not_bad": ("if (e < 0 || e >= E) ++bad;", "if (e < 0) ++bad;"),
+    "moe_meta_bad_expert_kept_active": ("if (!(is_active(idx[t], L, enabled, rank) && e >= 0 && e < E)) sorted_pair[pos++] = (int32_t)p;",
+                                        "if (!is_active(idx[t], L, enabled, rank)) sorted_pair[pos++] = (int32_t)p;"),
     "logits_mup_on_base_only": ("out[(int64_t)t * ld_out + i] = mup * full;",
                                 "out[(int64_t)t * ld_out + i] = full + (mup - 1.0f) * bf(logits_in[(int64_t)t * ld_in + src]);"),
 }
@@ -289,6 +309,7 @@ MUTANTS = {
 
 def _pin_suite_passes():
     checks = [test_golden_dense_by_hand, test_golden_moe_by_hand, test_golden_meta_by_hand,
+              test_golden_moe_meta_bad_ids_by_hand, lambda: test_moe_meta_matches_numpy_lexsort(0, True),
               lambda: test_dense_bruteforce_fp64(0), lambda: test_moe_bruteforce_fp64(0, False),
               lambda: test_moe_bruteforce_fp64(1, True), test_merged_weight_identity_tiny_preset,
               test_packed_slices_equal_separate_application,

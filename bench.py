@@ -370,9 +370,126 @@ def whole_job_throughput(tokens_per_step, steps, world, ms):
     return tokens_per_step * steps * world / (ms * 1e-3)
 
 
+# workloads of the per_workload block: one per configuration of the task
+# (tiny, decode QKV, prefill gate_up, many-adapter down_proj, MoE in both
+# layouts), each timed like the headline
+PER_WORKLOAD = ["tiny", "decode_qkv", "prefill_gate_up", "many_adapter_down", "moe", "moe_shared"]
+
+
+def build_runs(name, c, dev, l2, max_copies, Hn):
+    """Resident copies of the workload (pool, inputs, outputs, metadata,
+    workspace), enough that their algorithmic bytes exceed twice the L2."""
+    moe, sink, lin = is_moe(name), is_sink(name), is_linear(name)
+    ab = (moe_algorithmic_bytes(c) if moe else sink_algorithmic_bytes(c) if sink
+          else linear_algorithmic_bytes(c) if lin else dense_algorithmic_bytes(c))
+    n_rot = min(max(1, math.ceil(2 * l2 / max(ab["total"], 1))), max_copies)
+    bias = (gen.f32_to_bf16_bits(np.random.default_rng(7).normal(0, 0.5, c.out_total).astype(np.float32))
+            if lin else None)
+
+    def one():
+        return (Hn.MoERun(c, device=dev) if moe else Hn.SinkRun(c, device=dev) if sink
+                else Hn.LinearRun(c, bias, device=dev) if lin else Hn.DenseRun(c, device=dev))
+    return [one() for _ in range(n_rot)], ab, one
+
+
+def time_graph(torch, stream, body, reps=1):
+    """Capture body() once as a CUDA graph, replay it once untimed, then time
+    reps replays between CUDA events on the launching stream (ms per replay)."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        body()
+    g.replay()
+    stream.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        g.replay()
+    e1.record(stream)
+    stream.synchronize()
+    return e0.elapsed_time(e1) / reps, g
+
+
+def measure(name, runs, ab, args, torch, stream, L, world, dev, sampler=None):
+    """Step time (one CUDA graph of exactly args.steps steps over the rotating
+    copies, timed once after its untimed first replay), the apply alone and the
+    metadata build alone (graphs of KA calls), and kernel launches per step."""
+    moe = is_moe(name)
+    n_rot = len(runs)
+    for r in runs:                       # warm-up outside any graph
+        for _ in range(max(1, args.warmup)):
+            r.step()
+    stream.synchronize()
+    n0 = L.lora_kernel_launch_count()
+    runs[0].step()
+    stream.synchronize()
+    launches_per_step = L.lora_kernel_launch_count() - n0
+
+    def steps(k):
+        for i in range(k):
+            runs[i % n_rot].step()
+
+    # warm-up steps (W >= 3) as a graph, then the clocks are sampled over ~1 s
+    # of the same work, and the K timed steps run while they are still sampled
+    gw = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gw, stream=stream):
+        steps(max(3, args.warmup))
+    gk = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gk, stream=stream):
+        steps(args.steps)
+    gw.replay()
+    gk.replay()
+    stream.synchronize()
+    if sampler is not None:
+        t_end = time.perf_counter() + args.clock_seconds
+        while time.perf_counter() < t_end:
+            gw.replay()
+            stream.synchronize()
+    gw.replay()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    gk.replay()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    ms = e0.elapsed_time(e1)
+
+    # the apply kernels alone (metadata built beforehand) and the metadata alone
+    for r in runs:
+        r.build_meta()
+    KA = max(1, min(args.kernel_launches, 64))
+    reps = max(1, args.kernel_launches // KA)
+
+    def applies():
+        for k in range(KA):
+            r = runs[k % n_rot]
+            if moe:
+                r.w13()
+                r.w2()
+            else:
+                r.apply()
+
+    def metas():
+        for k in range(KA):
+            runs[k % n_rot].build_meta()
+    kms, _ = time_graph(torch, stream, applies, reps)
+    meta_ms, _ = time_graph(torch, stream, metas, reps)
+    return dict(ms=ms, kms=kms / KA, meta_ms=meta_ms / KA, launches_per_step=launches_per_step, n_rot=n_rot)
+
+
+def kernel_bytes(name, ab):
+    return (ab["w13"] + ab["w2"]) if is_moe(name) else (ab["total"] - ab["idx"])
+
+
 def run_gpu(args, rank, world, local_rank):
     import torch
-    import torch.distributed as dist
     from heterogeneous_adapters_lora_gb300 import harness as Hn
     from heterogeneous_adapters_lora_gb300 import lora as L
 
@@ -381,121 +498,18 @@ def run_gpu(args, rank, world, local_rank):
     L.lib()
     L.lora_set_kernel_policy(args.kernel_policy)
     name = args.workload
-    c = make_case(name)
-    moe = is_moe(name)
-    sink = is_sink(name)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    lin = is_linear(name)
-    ab = (moe_algorithmic_bytes(c) if moe else sink_algorithmic_bytes(c) if sink
-          else linear_algorithmic_bytes(c) if lin else dense_algorithmic_bytes(c))
-    foot = ab["total"]
-    n_rot = max(1, math.ceil(2 * l2 / max(foot, 1)))
-    n_rot = min(n_rot, args.max_copies)
-
-    runs = []
-    for _ in range(n_rot):
-        if lin:
-            bias = gen.f32_to_bf16_bits(np.random.default_rng(7).normal(0, 0.5, c.out_total).astype(np.float32))
-        runs.append(Hn.MoERun(c, device=dev) if moe else Hn.SinkRun(c, device=dev) if sink
-                    else Hn.LinearRun(c, bias, device=dev) if lin else Hn.DenseRun(c, device=dev))
-    torch.cuda.synchronize(dev)
-
-    def step(r):
-        r.step()
-
+    peak, peak_kind = load_peaks()
     stream = torch.cuda.Stream(device=dev)
+
+    c = make_case(name)
+    moe, sink, lin = is_moe(name), is_sink(name), is_linear(name)
     with torch.cuda.stream(stream):
-        for r in runs:           # warm-up outside the graph (also resets state)
-            for _ in range(max(1, args.warmup)):
-                step(r)
-        stream.synchronize()
-        graphs = []
-        for r in runs:
-            g = torch.cuda.CUDAGraph()
-            n0 = L.lora_kernel_launch_count()
-            with torch.cuda.graph(g, stream=stream):
-                step(r)
-            launches_per_step = L.lora_kernel_launch_count() - n0
-            graphs.append(g)
-        # a serving loop captures many layers per graph: time graphs of spg
-        # steps (rotating copies) so that graph launch gaps are amortised
-        spg = n_rot * max(1, -(-max(1, args.steps_per_graph) // n_rot))
-        gm = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gm, stream=stream):
-            for i in range(spg):
-                step(runs[i % n_rot])
-
-        def run_steps(k_steps):
-            for _ in range(k_steps // spg):
-                gm.replay()
-            for k in range(k_steps % spg):
-                graphs[k % n_rot].replay()
-
-        for i in range(args.warmup):
-            graphs[i % n_rot].replay()
-        gm.replay()
-        stream.synchronize()
-
-        # clocks: ~1 s of the same work right before the timed region, and during it
+        runs, ab, make_run = build_runs(name, c, dev, l2, args.max_copies, Hn)
+        torch.cuda.synchronize(dev)
         with ClockSampler(local_rank) as cs:
-            t_end = time.perf_counter() + args.clock_seconds
-            while time.perf_counter() < t_end:
-                run_steps(200)
-                stream.synchronize()
-            if world > 1:
-                dist.barrier()
-            torch.cuda.synchronize(dev)
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            run_steps(args.steps)
-            e1.record(stream)
-            torch.cuda.synchronize(dev)
-            if world > 1:
-                dist.barrier()
-        ms = e0.elapsed_time(e1)
-
-        # the apply kernels alone (metadata built beforehand): one CUDA graph of
-        # KA apply calls over the same rotation, replayed between CUDA events
-        kname = "moe" if moe else "apply"
-        for r in runs:
-            r.build_meta()
-        KA = max(1, min(args.kernel_launches, 64))
-        ga = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(ga, stream=stream):
-            for k in range(KA):
-                r = runs[k % n_rot]
-                if moe:
-                    r.w13()
-                    r.w2()
-                else:
-                    r.apply()
-        for _ in range(3):
-            ga.replay()
-        stream.synchronize()
-        reps = max(1, args.kernel_launches // KA)
-        a0 = torch.cuda.Event(enable_timing=True)
-        a1 = torch.cuda.Event(enable_timing=True)
-        a0.record(stream)
-        for _ in range(reps):
-            ga.replay()
-        a1.record(stream)
-        stream.synchronize()
-        kms = a0.elapsed_time(a1) / (reps * KA)
-
-        # the metadata build alone, the same way
-        gmeta = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gmeta, stream=stream):
-            for k in range(KA):
-                runs[k % n_rot].build_meta()
-        gmeta.replay()
-        stream.synchronize()
-        a0.record(stream)
-        for _ in range(reps):
-            gmeta.replay()
-        a1.record(stream)
-        stream.synchronize()
-        meta_ms = a0.elapsed_time(a1) / (reps * KA)
+            m = measure(name, runs, ab, args, torch, stream, L, world, dev, sampler=cs)
+        ms, kms, meta_ms = m["ms"], m["kms"], m["meta_ms"]
 
         # end to end through the public API with host buffers: every step copies
         # its inputs in from pinned host memory, makes the calls and copies its
@@ -504,10 +518,7 @@ def run_gpu(args, rank, world, local_rank):
         # stream), step i-1's calls (the compute stream) and step i-2's copy
         # out (a second copy stream) run at the same time; a buffer set is
         # refilled only once its previous result has been copied out.
-        e_runs = [runs[0], runs[1] if len(runs) > 1 else None]
-        if e_runs[1] is None:
-            e_runs[1] = (Hn.MoERun(c, device=dev) if moe else Hn.SinkRun(c, device=dev) if sink
-                         else Hn.LinearRun(c, bias, device=dev) if lin else Hn.DenseRun(c, device=dev))
+        e_runs = [runs[0], runs[1] if len(runs) > 1 else make_run()]
 
         def pin(a):
             return torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
@@ -561,7 +572,7 @@ def run_gpu(args, rank, world, local_rank):
                     ev_in[i].record(s_in)
                 stream.wait_event(ev_in[i])
                 with torch.cuda.stream(stream):
-                    step(r)
+                    r.step()
                     ev_calls[i].record(stream)
                 s_out.wait_event(ev_calls[i])
                 with torch.cuda.stream(s_out):
@@ -571,9 +582,8 @@ def run_gpu(args, rank, world, local_rank):
             stream.wait_event(ev_in[n - 1])
             stream.wait_event(ev_out[n - 1])
 
-        with torch.cuda.stream(stream):
-            for _ in range(max(1, args.warmup)):
-                e2e_steps(2)
+        for _ in range(max(1, args.warmup)):
+            e2e_steps(2)
         stream.synchronize()
         # the pipelined steps captured as one CUDA graph of G steps (pinned-memory
         # copies and the cross-stream waits are graph nodes), replayed
@@ -590,34 +600,63 @@ def run_gpu(args, rank, world, local_rank):
             e2e_graph = None
             torch.cuda.synchronize(dev)
         if world > 1:
+            import torch.distributed as dist
             dist.barrier()
         f0 = torch.cuda.Event(enable_timing=True)
         f1 = torch.cuda.Event(enable_timing=True)
         reps = max(1, -(-args.steps // G))
         e2e_n = reps * G
         f0.record(stream)
-        with torch.cuda.stream(stream):
-            for _ in range(reps):
-                if e2e_graph is not None:
-                    e2e_graph.replay()
-                else:
-                    e2e_steps(G)
+        for _ in range(reps):
+            if e2e_graph is not None:
+                e2e_graph.replay()
+            else:
+                e2e_steps(G)
         f1.record(stream)
         stream.synchronize()
         e2e_ms = f0.elapsed_time(f1)
+        for r in runs + e_runs[1:]:
+            r.close()
+        del runs, e_runs
+        torch.cuda.synchronize(dev)
+
+        # every other configuration of the task, timed the same way (step graph
+        # of exactly K steps, the apply and the metadata alone)
+        per = {}
+        if not args.no_per_workload and world == 1:
+            for wn in PER_WORKLOAD:
+                if wn == name:
+                    continue
+                wc = make_case(wn)
+                w_runs, w_ab, _ = build_runs(wn, wc, dev, l2, args.max_copies, Hn)
+                torch.cuda.synchronize(dev)
+                wm = measure(wn, w_runs, w_ab, args, torch, stream, L, world, dev)
+                for r in w_runs:
+                    r.close()
+                del w_runs
+                torch.cuda.synchronize(dev)
+                wkb = kernel_bytes(wn, w_ab)
+                ent = {"tokens_per_s": wc.T * args.steps / (wm["ms"] * 1e-3), "step_us": wm["ms"] / args.steps * 1e3,
+                       "apply_us": wm["kms"] * 1e3, "metadata_us": wm["meta_ms"] * 1e3,
+                       "apply_gbs": wkb / (wm["kms"] * 1e-3) / 1e9,
+                       "frac": wkb / (wm["kms"] * 1e-3) / 1e9 / peak,
+                       "algorithmic_bytes_per_apply": wkb, "tokens_per_step": wc.T,
+                       "launches_per_step": wm["launches_per_step"], "copies": wm["n_rot"],
+                       "kernel": apply_kernels(wn, args.kernel_policy)}
+                if not args.no_cpu_baseline:
+                    ent["cpu_baseline"] = time_oracle(wn, wc, min_seconds=args.cpu_seconds)
+                per[wn] = ent
 
     ms, e2e_ms, kms, meta_ms = max_over_ranks([ms, e2e_ms, kms, meta_ms], world, dev)
-    for r in runs:
-        r.close()
     if rank != 0:
         return 0
 
     tokens = c.T
     value = whole_job_throughput(tokens, args.steps, world, ms)
     e2e = whole_job_throughput(tokens, e2e_n, world, e2e_ms)
-    peak, peak_kind = load_peaks()
-    kbytes = (ab["w13"] + ab["w2"]) if moe else (ab["total"] - ab["idx"])
+    kbytes = kernel_bytes(name, ab)
     achieved = kbytes / (kms * 1e-3) / 1e9
+    n_rot = m["n_rot"]
     line = {
         "metric": "LoRA-delta tokens/s", "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
@@ -628,15 +667,16 @@ def run_gpu(args, rank, world, local_rank):
                    "algorithmic_bytes_per_step": ab["total"],
                    "hbm_gbs_per_step": ab["total"] / (ms / args.steps * 1e-3) / 1e9,
                    "l2": f"inputs rotate over {n_rot} resident copies "
-                         f"({n_rot * foot / 1e6:.0f} MB of algorithmic bytes, L2 {l2 / 1e6:.0f} MB)",
-                   "timing": f"CUDA graphs of {spg} steps (metadata + apply each, rotating copies) "
-                             f"replayed to K steps between CUDA events",
+                         f"({n_rot * ab['total'] / 1e6:.0f} MB of algorithmic bytes, L2 {l2 / 1e6:.0f} MB)",
+                   "timing": f"one CUDA graph of exactly {args.steps} steps (metadata + apply each, rotating "
+                             f"copies), replayed once untimed and once between CUDA events",
                    "parallelism": f"replicas{world}",
-                   "metadata_us_alone": meta_ms * 1e3, "apply_us_alone": kms * 1e3},
+                   "metadata_us_alone": meta_ms * 1e3, "apply_us_alone": kms * 1e3,
+                   "per_workload": per},
         "roofline": {"bound": "hbm", "kernel": apply_kernels(name, args.kernel_policy),
                      "achieved": achieved, "peak": peak,
                      "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": ncu_traffic(name, kname),
+                     "traffic": ncu_traffic(name, "moe" if moe else "apply"),
                      "algorithmic_bytes_per_launch": kbytes, "avg_launch_us": kms * 1e3},
         "clocks": cs.summary(),
         "e2e": {"value": e2e, "unit": "tokens/s", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
@@ -644,7 +684,7 @@ def run_gpu(args, rank, world, local_rank):
                 "timing": (f"CUDA graphs of {G} steps pipelined over two buffer sets: pinned H2D copies "
                            "(copy stream), metadata + apply (compute stream), D2H copy (second copy stream)")
                           if e2e_graph is not None else "eager pipelined calls"},
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": m["launches_per_step"] * args.steps,
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = time_oracle(name, c, min_seconds=args.cpu_seconds)
@@ -664,7 +704,8 @@ def main():
     ap.add_argument("--clock-seconds", type=float, default=1.0)
     ap.add_argument("--cpu-seconds", type=float, default=2.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--steps-per-graph", type=int, default=16)
+    ap.add_argument("--no-per-workload", action="store_true",
+                    help="time only --workload (skip the per_workload block of the other configurations)")
     ap.add_argument("--kernel-policy", type=int, default=0, choices=[0, 1, 2],
                     help="0 automatic, 1 persistent split-K kernel, 2 cluster kernel first (tuning)")
     args = ap.parse_args()

@@ -613,6 +613,10 @@ static std::atomic<unsigned long long> g_lora_launches{0};
 void lora_note_launch() { g_lora_launches.fetch_add(1, std::memory_order_relaxed); }
 extern "C" unsigned long long lora_kernel_launch_count(void) { return g_lora_launches.load(); }
 
+static std::atomic<int> g_last_cuda_error{0};
+void lora_note_cuda_error(cudaError_t e) { g_last_cuda_error.store((int)e, std::memory_order_relaxed); }
+extern "C" int32_t lora_last_cuda_error(void) { return g_last_cuda_error.load(std::memory_order_relaxed); }
+
 extern "C" void lora_set_kernel_policy(int32_t policy) { g_lora_kernel_policy = policy; }
 
 extern "C" void lora_set_spin_limit(int32_t max_polls) { g_spin_limit = max_polls; }
@@ -683,10 +687,17 @@ lora_status_t lora_dense_apply(const lora_pool_t *pool, const lora_meta_t *meta,
         g.tile_keyn = meta->stile_keyn;
         g.count_idx = 4;
     }
-    if (g_lora_kernel_policy != 1) {
+    const int pol = g_lora_kernel_policy;
+    if (pol == 0 && !use_sgmv) {
+        // decode-sized batches: shrink, reduction and expand in one launch
+        bool launched = false;
+        st = lora_fused_apply(pool, meta, x, ldx, y, ldy, post_scale, g_spin_limit, s, &launched);
+        if (st != LORA_OK || launched) return st;
+    }
+    if (pol != 1) {
         bool launched = false;
         const LoraProblem pr = to_problem(g, meta, pool->desc.max_loras);
-        if (g_lora_kernel_policy == 0 && have_split_region) {
+        if ((pol == 0 || pol == 3) && have_split_region) {
             st = lora_split_apply(pool, pr, scratch, scratch_bytes, cv.ctrl + 2, s, &launched);
             if (st != LORA_OK || launched) return st;
         }
@@ -825,7 +836,7 @@ extern "C" lora_status_t lora_moe_apply(const lora_pool_t *pool, const lora_meta
     if (g_lora_kernel_policy != 1) {
         bool launched = false;
         const LoraProblem pr = to_problem(g, meta, keys);
-        if (g_lora_kernel_policy == 0 && have_split_region) {
+        if ((g_lora_kernel_policy == 0 || g_lora_kernel_policy == 3) && have_split_region) {
             st = lora_split_apply(pool, pr, cv.data, cv.data_bytes, cv.ctrl + 2, s, &launched);
             if (st != LORA_OK || launched) return st;
         }

@@ -52,6 +52,12 @@ __device__ __forceinline__ uint4 ldg_stream(const void *p) {
     return r;
 }
 
+// Shared-window address of a shared-memory pointer.  Aligning a dynamic
+// shared buffer by adding (pad from this address) to the pointer keeps the
+// compiler's knowledge that it points to shared memory; a round trip through
+// an integer would turn every access through it into a generic one.
+__device__ __forceinline__ uint32_t smem_u32_of(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
 __device__ __forceinline__ int ld_acquire_gpu(const int *p) {
     int v;
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -68,10 +74,17 @@ __device__ __forceinline__ void cp_async_wait_all() {
 
 // ------------------------------------------------------------ host helpers
 
+// Last CUDA runtime error a library call returned LORA_ERR_CUDA for
+// (lora_last_cuda_error reads it).
+void lora_note_cuda_error(cudaError_t e);
+
 #define LORA_CUDA_TRY(expr)                         \
     do {                                            \
         cudaError_t _e = (expr);                    \
-        if (_e != cudaSuccess) return LORA_ERR_CUDA; \
+        if (_e != cudaSuccess) {                    \
+            lora_note_cuda_error(_e);               \
+            return LORA_ERR_CUDA;                   \
+        }                                           \
     } while (0)
 
 static inline int lora_ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
@@ -116,15 +129,23 @@ lora_status_t lora_cluster_apply(const lora_pool_t *pool, const LoraProblem &pr,
 // Host-side count of kernel launches made by this library (all devices).
 void lora_note_launch();
 
-// Kernel selection policy (0 = automatic: split shrink/expand kernels when
-// the shapes fit, 1 = persistent split-K kernel only, 2 = cluster kernel
-// preferred).
+// Kernel selection policy (0 = automatic: the fused decode kernel, else the
+// split shrink/expand kernels when the shapes fit; 1 = persistent split-K
+// kernel only; 2 = cluster kernel preferred; 3 = automatic without the fused
+// decode kernel).
 extern int g_lora_kernel_policy;
 
 // 2D bf16 tensor map over rows x cols (row stride in elements), optional
 // 128-byte swizzle (sgmv.cu).
 bool lora_make_tmap_2d(CUtensorMap *m, const void *base, long long cols, long long rows, long long stride,
                        int box_cols, int box_rows, bool swizzle128);
+
+// 3D bf16 tensor map over a row-major [rows][cols] matrix (cols % 64 == 0)
+// that lands a box of box_rows rows x box_chunks 128-byte column chunks in
+// shared memory chunk-major: for each chunk, the rows as 128-byte lines in
+// the 128-byte swizzle (sgmv.cu).
+bool lora_make_tmap_a_chunks(CUtensorMap *m, const void *base, long long rows, long long cols, int box_rows,
+                             int box_chunks);
 
 // Split shrink/expand kernels (bgmv.cu): workspace bytes and launcher.
 size_t lora_split_ws_bytes(int n_slices, int in_dim, int R, int rows, int max_tiles);
@@ -138,6 +159,14 @@ size_t lora_sgmv_ws_bytes(const lora_pool_t *pool, int rows);
 lora_status_t lora_sgmv_apply(const lora_pool_t *pool, const lora_meta_t *meta, const void *x, int64_t ldx,
                               void *y, int64_t ldy, void *V, int spin_limit, int num_sms, float post_scale,
                               cudaStream_t s);
+
+// Fused decode kernel (fused.cu): one thread-block cluster per adapter slot,
+// shrink, DSMEM reduction and expand in one launch, no workspace.  Launches
+// and sets *launched when the batch and pool fit its plan.
+bool lora_fused_eligible(const lora_pool_t *pool, int T);
+lora_status_t lora_fused_apply(const lora_pool_t *pool, const lora_meta_t *meta, const void *x, int64_t ldx,
+                               void *y, int64_t ldy, float post_scale, int spin_limit, cudaStream_t s,
+                               bool *launched);
 
 // Dense apply shared by lora_apply_slices and lora_logits_apply (grouped.cu).
 lora_status_t lora_dense_apply(const lora_pool_t *pool, const lora_meta_t *meta, const void *x, int64_t ldx,

@@ -84,7 +84,7 @@ __global__ void __launch_bounds__(kThreads, 1) sgmv_shrink_kernel(const __grid_c
     extern __shared__ __align__(1024) char smem_raw[];
     __shared__ __align__(8) uint64_t full[kStages], empty[kStages], acc_full;
     __shared__ uint32_t s_tmem;
-    char *smem = (char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    char *smem = smem_raw + ((1024u - (smem_u32_of(smem_raw) & 1023u)) & 1023u);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tile = blockIdx.x / p.n_slices, js = blockIdx.x - tile * p.n_slices;  // one slice per CTA
@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(kEThreads, 1) sgmv_expand_kernel(const __grid_
     __shared__ __align__(8) uint64_t v_full, v_empty, b_full[2], b_empty[2], y_full[kNY], y_empty[kNY],
         acc_full[2], acc_empty[2];
     __shared__ uint32_t s_tmem;
-    char *smem = (char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    char *smem = smem_raw + ((1024u - (smem_u32_of(smem_raw) & 1023u)) & 1023u);
     char *vt = smem;                           // V hi tile (16 KB) then lo tile (16 KB)
     char *bt = smem + 2 * kTileBytes;          // 2 x B tile (16 KB)
     char *yt = smem + 4 * kTileBytes;          // kNY x y tile (2 boxes of 16 KB each)
@@ -362,15 +362,16 @@ __global__ void __launch_bounds__(kEThreads, 1) sgmv_expand_kernel(const __grid_
 // ------------------------------------------------------------------ host
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
+    // looked up once (thread-safe initialisation of a function-local static)
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
         void *ptr = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = (PFN_cuTensorMapEncodeTiled_v12000)ptr;
-    }
+            return (PFN_cuTensorMapEncodeTiled_v12000)ptr;
+        return nullptr;
+    }();
     return fn;
 }
 
@@ -403,6 +404,20 @@ bool lora_make_tmap_2d(CUtensorMap *m, const void *base, long long cols, long lo
     return f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool lora_make_tmap_a_chunks(CUtensorMap *m, const void *base, long long rows, long long cols, int box_rows,
+                             int box_chunks) {
+    PFN_cuTensorMapEncodeTiled_v12000 f = encode_fn();
+    if (!f || cols % 64) return false;
+    // dims: 64 elements of a 128-byte chunk, the rows, the chunks of a row
+    cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(cols / 64)};
+    cuuint64_t strides[2] = {(cuuint64_t)cols * 2, 128};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)box_chunks};
+    cuuint32_t es[3] = {1, 1, 1};
+    return f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool lora_sgmv_eligible(const lora_pool_t *pool) {

@@ -51,10 +51,12 @@ class Meta(ctypes.Structure):
 
 
 class LoraError(RuntimeError):
-    def __init__(self, code, where):
+    def __init__(self, code, where, cuda_error=None):
         self.code = int(code)
         self.name = STATUS.get(self.code, f"status {code}")
-        super().__init__(f"{where}: {self.name}")
+        self.cuda_error = cuda_error
+        extra = f" (cudaError {cuda_error})" if cuda_error else ""
+        super().__init__(f"{where}: {self.name}{extra}")
 
 
 _lock = threading.Lock()
@@ -91,6 +93,7 @@ EXPORTS = {
     "lora_set_spin_limit": (None, [c_i32]),
     "lora_set_kernel_policy": (None, [c_i32]),
     "lora_kernel_launch_count": (ctypes.c_ulonglong, []),
+    "lora_last_cuda_error": (c_i32, []),
     "lora_linear_apply": (c_i32, [c_vp, ctypes.POINTER(Meta), c_vp, c_i64, c_vp, c_i64, c_vp, c_vp, c_i64, c_vp, c_size,
                               c_vp]),
     "lora_sink_experts_act": (c_i32, [c_vp, c_i64, c_vp, c_i64, c_i32, c_i32, c_i32, c_vp, c_i64, c_vp]),
@@ -117,7 +120,8 @@ def lib():
 
 def _check(code, where):
     if code != 0:
-        raise LoraError(code, where)
+        cuda = int(lib().lora_last_cuda_error()) if code == CODE["LORA_ERR_CUDA"] else None
+        raise LoraError(code, where, cuda)
 
 
 def ptr(obj):
@@ -278,6 +282,10 @@ def lora_sink_experts_act(gate_up, ld_gate_up, gammas, ld_gammas, T, n_experts, 
 
 def lora_kernel_launch_count() -> int:
     return int(lib().lora_kernel_launch_count())
+
+
+def lora_last_cuda_error() -> int:
+    return int(lib().lora_last_cuda_error())
 
 
 def lora_status_string(code: int) -> str:

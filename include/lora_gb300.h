@@ -383,11 +383,15 @@ LORA_API lora_status_t lora_sink_experts_act(const void *gate_up, int64_t ld_gat
 
 /* Kernel selection for lora_apply_slices / lora_moe_apply (process-wide):
  * 0 = automatic (tcgen05 for long contiguous runs of a rank-64 dense pool;
- *     otherwise the split shrink/expand kernels when the workspace holds
- *     their region, else the one-pass cluster kernel, else the persistent
- *     split-K kernel),
+ *     the fused decode kernel -- one thread-block cluster per adapter slot,
+ *     shrink, on-chip reduction and expand in one launch -- for dense
+ *     batches of a few rows per slot; otherwise the split shrink/expand
+ *     kernels when the workspace holds their region, else the one-pass
+ *     cluster kernel, else the persistent split-K kernel),
  * 1 = always the persistent split-K kernel,
- * 2 = like 0 but the one-pass cluster kernel before the split kernels.
+ * 2 = like 0 but the one-pass cluster kernel before the split kernels
+ *     (and no fused decode kernel),
+ * 3 = like 0 without the fused decode kernel.
  * For tests and tuning. */
 LORA_API void lora_set_kernel_policy(int32_t policy);
 
@@ -395,6 +399,11 @@ LORA_API void lora_set_kernel_policy(int32_t policy);
  * (all pools, all devices; host-side counter, launches captured into a CUDA
  * graph count once at capture).  A diagnostic: never fails. */
 LORA_API unsigned long long lora_kernel_launch_count(void);
+
+/* The cudaError_t value of the last CUDA runtime call that made a library
+ * call return LORA_ERR_CUDA (0 if none yet; process-wide, not cleared).
+ * A diagnostic: never fails. */
+LORA_API int32_t lora_last_cuda_error(void);
 
 /* Static string naming a status code. */
 LORA_API const char *lora_status_string(lora_status_t s);

@@ -44,6 +44,7 @@
 #include <atomic>
 
 #include "lora_internal.cuh"
+#include "meta_block.cuh"
 #include "mma_common.cuh"
 
 namespace {
@@ -54,9 +55,9 @@ constexpr int kFThreads = 256;
 constexpr int kFWarps = kFThreads / 32;
 constexpr int kNT = LORA_TILE_ROWS;  // rows per tile: two 8-row N blocks of the shrink, M of the expand
 constexpr int kMaxT = 1024;          // batch rows whose sorted list a CTA stages
-constexpr int kSmem1 = 220 * 1024;   // dynamic shared memory at one CTA per SM (static + dynamic <= 227 KB)
+constexpr int kSmem1 = 212 * 1024;   // dynamic shared memory at one CTA per SM (static + dynamic <= 227 KB)
 constexpr int kPW = 6;               // expand blocks per pass
-constexpr int kSmem2 = 106 * 1024;   // ... at two (with the static shared memory and the 1 KB per CTA the SM keeps)
+constexpr int kSmem2 = 100 * 1024;   // ... at two (with the static shared memory and the 1 KB per CTA the SM keeps)
 
 struct alignas(64) FArgs {
     CUtensorMap tm_a[LORA_MAX_SLICES];  // A_j as [L*R rows][H]: boxes of BR rows x NCH chunks
@@ -78,6 +79,11 @@ struct alignas(64) FArgs {
     int vp, v_bytes;                    // v tile row pitch (elements), bytes of one v tile
     int *status;
     int spin_limit;
+    // batch mode: the slot clusters find their rows in idx, and the CTA of
+    // one more cluster builds the batch metadata (ma) at the same time
+    const int32_t *idx;
+    int idx_mode, meta_steps;
+    MetaArgs ma;
 };
 
 __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int x, int y, int z, uint64_t *bar) {
@@ -120,7 +126,9 @@ __global__ void __launch_bounds__(kFThreads, MINB) bgmv_fused_kernel(const __gri
     extern __shared__ __align__(1024) char smem_raw[];
     char *smem = smem_raw + ((1024u - (smem_u32_of(smem_raw) & 1023u)) & 1023u);  // the swizzled boxes want 1 KB
     __shared__ __align__(8) uint64_t abar;
-    __shared__ int s_sorted[kMaxT];
+    __shared__ int s_sorted[kMaxT];  // the batch's sorted rows, or its slots in batch mode
+    __shared__ int s_list[kMaxT];    // batch mode: this slot's rows
+    __shared__ int s_cnt[32];
     __shared__ int s_oo[LORA_MAX_SLICES + 1];
     __shared__ const uint16_t *s_B[LORA_MAX_SLICES];
     __shared__ int s_nb[2];
@@ -128,6 +136,13 @@ __global__ void __launch_bounds__(kFThreads, MINB) bgmv_fused_kernel(const __gri
     const int g = lane >> 2, c4 = lane & 3;
     const int c = (int)cluster_rank();
     const int a = blockIdx.x / p.CS;
+    if (a == p.L) {
+        // batch mode's last cluster: its first CTA builds the metadata
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        asm volatile("griddepcontrol.launch_dependents;");
+        if (c == 0) dense_meta_block(p.ma, (int *)smem, p.meta_steps);
+        return;
+    }
     const int ns = p.n_slices;
     const int h0 = c * p.HC, hlen = max(0, min(p.H - h0, p.HC));
     const int ob0 = min(p.out_total, c * p.OB), olen = min(p.out_total - ob0, p.OB);
@@ -175,10 +190,14 @@ __global__ void __launch_bounds__(kFThreads, MINB) bgmv_fused_kernel(const __gri
     // ---------------- the metadata (and everything before it) is complete
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
-    for (int i = tid; i < p.T; i += kFThreads) s_sorted[i] = __ldcg(p.sorted + i);
-    if (tid == 0) {
-        s_nb[0] = __ldcg(p.key_count + a);
-        s_nb[1] = __ldcg(p.key_offset + a);
+    if (p.idx_mode) {
+        for (int i = tid; i < p.T; i += kFThreads) s_sorted[i] = __ldcg(p.idx + i);
+    } else {
+        for (int i = tid; i < p.T; i += kFThreads) s_sorted[i] = __ldcg(p.sorted + i);
+        if (tid == 0) {
+            s_nb[0] = __ldcg(p.key_count + a);
+            s_nb[1] = __ldcg(p.key_offset + a);
+        }
     }
     const int r = en != 0 ? rk : 0;
     const bool act = r > 0;
@@ -215,7 +234,43 @@ __global__ void __launch_bounds__(kFThreads, MINB) bgmv_fused_kernel(const __gri
     const int ngr = act ? (olen >> 5) : 0;
     const int ngw = ngr > warp ? (ngr - warp + kFWarps - 1) / kFWarps : 0;
     __syncthreads();
+    if (p.idx_mode) {
+        // this slot's rows in batch order: rows t = j*256 + tid, so (j, warp,
+        // lane) is row order; a ballot per warp and row step, a scan over
+        // the (step, warp) counts, then each row's place
+        const int nj = (p.T + kFThreads - 1) / kFThreads;
+        unsigned m4[kMaxT / kFThreads];
+#pragma unroll
+        for (int j = 0; j < kMaxT / kFThreads; ++j) {
+            const int t = j * kFThreads + tid;
+            m4[j] = __ballot_sync(0xffffffffu, j < nj && t < p.T && s_sorted[t] == a);
+            if (j < nj && lane == 0) s_cnt[j * kFWarps + warp] = __popc(m4[j]);
+        }
+        __syncthreads();
+        const int ncnt = nj * kFWarps;
+        const int v = lane < ncnt ? s_cnt[lane] : 0;
+        int incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += u;
+        }
+        const int total = __shfl_sync(0xffffffffu, incl, 31);
+#pragma unroll
+        for (int j = 0; j < kMaxT / kFThreads; ++j) {
+            // exclusive prefix of this (step, warp) segment, from its lane of the scan
+            const int before = __shfl_sync(0xffffffffu, incl - v, (j * kFWarps + warp) & 31);
+            if (j < nj && ((m4[j] >> lane) & 1u))
+                s_list[before + __popc(m4[j] & ((1u << lane) - 1u))] = j * kFThreads + tid;
+        }
+        if (tid == 0) {
+            s_nb[0] = total;
+            s_nb[1] = 0;
+        }
+        __syncthreads();
+    }
     const int n = act ? s_nb[0] : 0, off = s_nb[1];
+    const int *rows = p.idx_mode ? s_list : s_sorted;
     if (n <= 0) {  // the same for every CTA of the cluster
         if (hlen > 0) mbar_wait(&abar, 0, p.spin_limit, p.status);  // no copy may be in flight at exit
         return;
@@ -248,7 +303,7 @@ __global__ void __launch_bounds__(kFThreads, MINB) bgmv_fused_kernel(const __gri
     for (int tile = 0; tile < n_tiles; ++tile) {
         const int nt = min(kNT, n - tile * kNT);
         if (tile > 0) __syncthreads();  // the previous tile is done with the x tile
-        const int *s_tok = s_sorted + off + tile * kNT;
+        const int *s_tok = rows + off + tile * kNT;
         // x rows of chunk c (swizzled like the A boxes): a warp per row, the
         // lanes over its 16-byte units
         for (int t = warp; t < nt; t += kFWarps) {
@@ -570,13 +625,20 @@ bool lora_fused_eligible(const lora_pool_t *pool, int T) {
     return fused_plan(pool, T, &pl);
 }
 
-lora_status_t lora_fused_apply(const lora_pool_t *pool, const lora_meta_t *meta, const void *x, int64_t ldx,
-                               void *y, int64_t ldy, float post_scale, int spin_limit, cudaStream_t s,
-                               bool *launched) {
+lora_status_t lora_fused_apply(const lora_pool_t *pool, const lora_meta_t *meta, const int32_t *d_idx, int32_t T,
+                               const void *x, int64_t ldx, void *y, int64_t ldy, float post_scale, int spin_limit,
+                               cudaStream_t s, bool *launched) {
     *launched = false;
     FPlan pl;
-    if (!fused_plan(pool, meta->T, &pl)) return LORA_OK;
+    if (!fused_plan(pool, T, &pl)) return LORA_OK;
     const lora_pool_desc_t &d = pool->desc;
+    const int meta_steps = (T + kFThreads - 1) / kFThreads;
+    if (d_idx) {
+        // batch mode: the metadata is built by one CTA (a key per thread)
+        if (d.max_loras + 1 > kFThreads || meta_steps > kMaxSteps ||
+            dense_meta_smem_bytes(kFThreads, meta_steps, d.max_loras) + 1024 > pl.smem)
+            return LORA_OK;
+    }
     FArgs a;
     memset(&a, 0, sizeof(a));
     a.n_slices = d.n_slices;
@@ -598,8 +660,15 @@ lora_status_t lora_fused_apply(const lora_pool_t *pool, const lora_meta_t *meta,
     if (!g_fused_configured[dev].load(std::memory_order_acquire)) {
         const FusedFn all[] = {bgmv_fused_kernel<1, 3, 2>, bgmv_fused_kernel<2, 1, 2>, bgmv_fused_kernel<4, 1, 2>,
                                bgmv_fused_kernel<1, 6, 1>, bgmv_fused_kernel<2, 3, 1>, bgmv_fused_kernel<4, 1, 1>};
-        for (FusedFn f : all)
-            LORA_CUDA_TRY(cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem1));
+        int optin = 0;
+        LORA_CUDA_TRY(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, pool->device));
+        for (FusedFn f : all) {
+            // the static shared memory counts against the opt-in limit too
+            cudaFuncAttributes fa;
+            LORA_CUDA_TRY(cudaFuncGetAttributes(&fa, f));
+            const int dyn = std::min(kSmem1, optin - (int)fa.sharedSizeBytes);
+            LORA_CUDA_TRY(cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn));
+        }
         g_fused_configured[dev].store(1, std::memory_order_release);
     }
     a.out_total = off;
@@ -607,7 +676,7 @@ lora_status_t lora_fused_apply(const lora_pool_t *pool, const lora_meta_t *meta,
     a.HC = pl.HC;
     a.NCH = pl.NCH;
     a.OB = pl.OB;
-    a.T = meta->T;
+    a.T = T;
     a.L = d.max_loras;
     a.BR = pl.BR;
     a.kgb = pl.kgb;
@@ -617,6 +686,21 @@ lora_status_t lora_fused_apply(const lora_pool_t *pool, const lora_meta_t *meta,
     a.key_count = meta->key_count;
     a.key_offset = meta->key_offset;
     a.sorted = meta->sorted;
+    if (d_idx) {
+        a.idx = d_idx;
+        a.idx_mode = 1;
+        a.meta_steps = meta_steps;
+        a.ma.idx = d_idx;
+        a.ma.rank = pool->d_rank;
+        a.ma.enabled = pool->d_enabled;
+        a.ma.status = pool->d_status;
+        a.ma.T = T;
+        a.ma.K = 1;
+        a.ma.E = 1;
+        a.ma.L = d.max_loras;
+        a.ma.n_keys = d.max_loras;
+        a.ma.m = *meta;
+    }
     a.x = (const uint16_t *)x;
     a.ldx = ldx;
     a.y = (uint16_t *)y;
@@ -634,7 +718,7 @@ lora_status_t lora_fused_apply(const lora_pool_t *pool, const lora_meta_t *meta,
 
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
-    cfg.gridDim = dim3((unsigned)(d.max_loras * pl.CS), 1, 1);
+    cfg.gridDim = dim3((unsigned)((d.max_loras + (d_idx ? 1 : 0)) * pl.CS), 1, 1);
     cfg.blockDim = dim3(kFThreads, 1, 1);
     cfg.dynamicSmemBytes = pl.smem;
     cfg.stream = s;

@@ -691,7 +691,7 @@ lora_status_t lora_dense_apply(const lora_pool_t *pool, const lora_meta_t *meta,
     if (pol == 0 && !use_sgmv) {
         // decode-sized batches: shrink, reduction and expand in one launch
         bool launched = false;
-        st = lora_fused_apply(pool, meta, x, ldx, y, ldy, post_scale, g_spin_limit, s, &launched);
+        st = lora_fused_apply(pool, meta, nullptr, meta->T, x, ldx, y, ldy, post_scale, g_spin_limit, s, &launched);
         if (st != LORA_OK || launched) return st;
     }
     if (pol != 1) {
@@ -711,6 +711,35 @@ extern "C" lora_status_t lora_apply_slices(const lora_pool_t *pool, const lora_m
                                            const void *x, int64_t ldx, void *y, int64_t ldy,
                                            void *workspace, size_t ws_bytes, void *stream) {
     return lora_dense_apply(pool, meta, x, ldx, y, ldy, workspace, ws_bytes, 1.0f, (cudaStream_t)stream);
+}
+
+extern "C" lora_status_t lora_build_meta_apply(const lora_pool_t *pool, const int32_t *d_idx, int32_t T,
+                                               lora_meta_t *meta, const void *x, int64_t ldx, void *y, int64_t ldy,
+                                               void *workspace, size_t ws_bytes, void *stream) {
+    if (!pool || !meta || T < 0 || (T > 0 && !d_idx)) return LORA_ERR_INVALID_ARG;
+    if (pool->is_moe) return LORA_ERR_UNSUPPORTED;
+    cudaStream_t s = (cudaStream_t)stream;
+    const lora_pool_desc_t &d = pool->desc;
+    if (g_lora_kernel_policy == 0 && T > 0 && T <= meta->max_rows && d.max_loras <= meta->max_keys &&
+        meta->sorted && meta->counters && meta->tile_keyn && meta->ltile_keyn && meta->stile_keyn && x && y &&
+        lora_aligned16(x) && lora_aligned16(y) && ldx % 8 == 0 && ldy % 8 == 0 && ldx >= d.in_dim &&
+        ldy >= out_total(pool)) {
+        // one launch: the metadata build and the delta of this layer together
+        bool launched = false;
+        const lora_status_t st =
+            lora_fused_apply(pool, meta, d_idx, T, x, ldx, y, ldy, 1.0f, g_spin_limit, s, &launched);
+        if (st != LORA_OK) return st;
+        if (launched) {
+            meta->T = T;
+            meta->top_k = 1;
+            meta->n_keys = d.max_loras;
+            meta->mode = 0;
+            return LORA_OK;
+        }
+    }
+    lora_status_t st = lora_launch_build_meta(pool, d_idx, T, nullptr, 1, meta, s);
+    if (st != LORA_OK) return st;
+    return lora_dense_apply(pool, meta, x, ldx, y, ldy, workspace, ws_bytes, 1.0f, s);
 }
 
 extern "C" lora_status_t lora_shrink(const lora_pool_t *pool, const lora_meta_t *meta,

@@ -164,9 +164,12 @@ lora_status_t lora_sgmv_apply(const lora_pool_t *pool, const lora_meta_t *meta, 
 // shrink, DSMEM reduction and expand in one launch, no workspace.  Launches
 // and sets *launched when the batch and pool fit its plan.
 bool lora_fused_eligible(const lora_pool_t *pool, int T);
-lora_status_t lora_fused_apply(const lora_pool_t *pool, const lora_meta_t *meta, const void *x, int64_t ldx,
-                               void *y, int64_t ldy, float post_scale, int spin_limit, cudaStream_t s,
-                               bool *launched);
+// With d_idx (batch mode) the kernel also builds the batch metadata into
+// meta (as lora_build_meta would, T rows) in the same launch, and the slot
+// clusters find their rows in d_idx; without it they read meta.
+lora_status_t lora_fused_apply(const lora_pool_t *pool, const lora_meta_t *meta, const int32_t *d_idx, int32_t T,
+                               const void *x, int64_t ldx, void *y, int64_t ldy, float post_scale, int spin_limit,
+                               cudaStream_t s, bool *launched);
 
 // Dense apply shared by lora_apply_slices and lora_logits_apply (grouped.cu).
 lora_status_t lora_dense_apply(const lora_pool_t *pool, const lora_meta_t *meta, const void *x, int64_t ldx,

@@ -18,22 +18,14 @@
 #include <atomic>
 
 #include "lora_internal.cuh"
+#include "meta_block.cuh"
 
 namespace {
 
 constexpr int kThreads = 1024;
 constexpr int kSmemBudgetInts = 56 * 1024;  // 224 KB
 
-struct MetaArgs {
-    const int32_t *idx;
-    const int32_t *topk;
-    const int32_t *rank;
-    const int32_t *enabled;
-    int32_t *status;
-    int T, K, E, L, n_keys, n_chunks, cache_keys;
-    int key_bits;  // smallest b with 2^b > n_keys + 1: the pattern of key -1 matches no key
-    lora_meta_t m;
-};
+
 
 // Key of one row given the slot-activity table in shared memory.
 __device__ __forceinline__ int row_key(const MetaArgs &a, const unsigned char *act, int row, int s,
@@ -322,154 +314,13 @@ __global__ void __launch_bounds__(kThreads, 1) build_meta_kernel(MetaArgs a) {
     }
 }
 
-// Dense batches of at most kSmallRows rows and kSmallRows - 1 slots: the
-// same metadata as build_meta_kernel with one row and one key per thread,
-// which keeps every warp's path short:
-//   1. each thread loads its row's slot; the slot tables load alongside
-//   2. per warp: the lanes sharing a key (one match instruction) -> the
-//      warp's count of each key, the row's rank among them, and the first and
-//      last row of the key (a key's rows form one contiguous run when
-//      last - first + 1 equals its count)
-//   3. per key: its count and the exclusive prefix over the warps, then one
-//      block-wide scan of the row offsets, group index and tile counts
-//   4. stable scatter: key offset + earlier warps + earlier lanes
-constexpr int kSmallRows = 1024;
-
 __global__ void __launch_bounds__(kSmallRows, 1) build_meta_small_kernel(MetaArgs a) {
     extern __shared__ int sm[];
-    const int L = a.L, NK = a.n_keys, NK1 = NK + 1, T = a.T;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int nthreads = blockDim.x, W = nthreads >> 5;
-    int *hist = sm;                   // [W][NK1] per-warp counts -> exclusive prefix over the warps
-    int *off = hist + W * NK1;        // [NK1] row offset of each key
-    int *tmin = off + NK1;            // [NK] first row of each key
-    int *tmax = tmin + NK;            // [NK] last row of each key
-    int *wt = tmax + NK;              // [5][32] warp totals of the key scan
-    int *misc = wt + 160;             // [8]: n_bad
-    unsigned char *act = (unsigned char *)(misc + 8);  // [L] slot enabled with rank > 0
     // let the apply kernel that follows start its prologue; it waits for
     // this grid's completion before reading any metadata
     asm volatile("griddepcontrol.launch_dependents;");
     asm volatile("griddepcontrol.wait;" ::: "memory");
-
-    // 1. this row's slot and the slot tables (one round trip)
-    const int s = tid < T ? a.idx[tid] : -1;
-    for (int i = tid; i < L; i += nthreads) {
-        const int en = a.enabled[i], rk = a.rank[i];
-        act[i] = (en != 0 && rk > 0) ? 1 : 0;
-    }
-    for (int i = tid; i < W * NK1; i += nthreads) hist[i] = 0;
-    for (int i = tid; i < NK; i += nthreads) {
-        tmin[i] = 0x7fffffff;
-        tmax[i] = -1;
-    }
-    if (tid == 0) misc[0] = 0;
-    __syncthreads();
-
-    // 2. keys (inactive rows: NK, so they sort last; no row: -1)
-    const bool valid = s >= 0 && s < L;
-    const int key = tid < T ? ((valid && act[s]) ? s : NK) : -1;
-    const unsigned peers = __match_any_sync(0xffffffffu, key);
-    const int wrank = __popc(peers & ((1u << lane) - 1u));
-    if (key >= 0 && wrank == 0) {
-        hist[warp * NK1 + key] = __popc(peers);
-        if (key < NK) {
-            atomicMin(&tmin[key], (tid - lane) + __ffs(peers) - 1);
-            atomicMax(&tmax[key], (tid - lane) + 31 - __clz(peers));
-        }
-    }
-    const int nb = __reduce_add_sync(0xffffffffu, (tid < T && s != -1 && !valid) ? 1 : 0);
-    if (lane == 0 && nb) atomicAdd(&misc[0], nb);
-    __syncthreads();
-
-    // 3. key k = tid: count and prefix over the warps, then the key-space scan
-    const int k = tid;
-    int c = 0;
-    if (k < NK1)
-        for (int w = 0; w < W; ++w) {
-            const int v = hist[w * NK1 + k];
-            hist[w * NK1 + k] = c;
-            c += v;
-        }
-    const bool real = k < NK, nonempty = real && c > 0;
-    const bool run = nonempty && c >= LORA_LONG_MIN && tmax[k] - tmin[k] + 1 == c;
-    int v5[5];
-    v5[0] = k < NK1 ? c : 0;
-    v5[1] = nonempty ? 1 : 0;
-    v5[2] = real ? (c + LORA_TILE_ROWS - 1) / LORA_TILE_ROWS : 0;
-    v5[3] = run ? (c + LORA_LTILE_ROWS - 1) / LORA_LTILE_ROWS : 0;
-    v5[4] = (nonempty && !run) ? (c + LORA_TILE_ROWS - 1) / LORA_TILE_ROWS : 0;
-    int inc[5];
-#pragma unroll
-    for (int q = 0; q < 5; ++q) inc[q] = v5[q];
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-#pragma unroll
-        for (int q = 0; q < 5; ++q) {
-            const int v = __shfl_up_sync(0xffffffffu, inc[q], o);
-            if (lane >= o) inc[q] += v;
-        }
-    }
-    if (lane == 31)
-#pragma unroll
-        for (int q = 0; q < 5; ++q) wt[q * 32 + warp] = inc[q];
-    __syncthreads();
-    int ex[5], tot[5];
-#pragma unroll
-    for (int q = 0; q < 5; ++q) {
-        int before = lane < warp ? wt[q * 32 + lane] : 0;
-        int all = lane < W ? wt[q * 32 + lane] : 0;
-#pragma unroll
-        for (int o = 16; o; o >>= 1) {
-            before += __shfl_xor_sync(0xffffffffu, before, o);
-            all += __shfl_xor_sync(0xffffffffu, all, o);
-        }
-        ex[q] = before + inc[q] - v5[q];
-        tot[q] = all;
-    }
-    if (k < NK1) {
-        off[k] = ex[0];
-        a.m.key_offset[k] = ex[0];
-    }
-    if (real) {
-        a.m.key_count[k] = c;
-        a.m.key_group[k] = nonempty ? ex[1] : -1;
-        if (nonempty) {
-            const int g = ex[1];
-            a.m.group_key[g] = k;
-            a.m.group_start[g] = ex[0];
-            for (int i = 0; i < v5[2]; ++i) {
-                a.m.tile_group[ex[2] + i] = g;
-                a.m.tile_row0[ex[2] + i] = ex[0] + i * LORA_TILE_ROWS;
-                a.m.tile_keyn[ex[2] + i] = (k << 5) | min(LORA_TILE_ROWS, c - i * LORA_TILE_ROWS);
-            }
-            for (int i = 0; i < v5[3]; ++i) {
-                a.m.ltile_row0[ex[3] + i] = ex[0] + i * LORA_LTILE_ROWS;
-                a.m.ltile_keyn[ex[3] + i] = (k << 8) | min(LORA_LTILE_ROWS, c - i * LORA_LTILE_ROWS);
-                a.m.ltile_tok0[ex[3] + i] = tmin[k] + i * LORA_LTILE_ROWS;
-            }
-            for (int i = 0; i < v5[4]; ++i) {
-                a.m.stile_row0[ex[4] + i] = ex[0] + i * LORA_TILE_ROWS;
-                a.m.stile_keyn[ex[4] + i] = (k << 5) | min(LORA_TILE_ROWS, c - i * LORA_TILE_ROWS);
-            }
-        }
-    }
-    __syncthreads();
-
-    // 4. stable scatter
-    if (key >= 0) a.m.sorted[off[key] + hist[warp * NK1 + key] + wrank] = tid;
-    if (tid == 0) {
-        const int n_active = off[NK];
-        const int n_bad = misc[0];
-        a.m.group_start[tot[1]] = n_active;
-        a.m.counters[0] = n_active;
-        a.m.counters[1] = tot[1];
-        a.m.counters[2] = n_bad;
-        a.m.counters[3] = tot[2];
-        a.m.counters[4] = tot[4];
-        a.m.counters[5] = tot[3];
-        if (n_bad) atomicExch(a.status, (int)LORA_ERR_DEVICE_INDEX);
-    }
+    dense_meta_block(a, sm, 1);
 }
 
 }  // namespace
@@ -490,8 +341,7 @@ lora_status_t lora_launch_build_meta(const lora_pool_t *pool, const int32_t *d_i
         // small dense batch: one row and one key per thread
         int nthreads = (int)(std::max<int64_t>(rows, NK1) + 31) / 32 * 32;
         if (nthreads < 64) nthreads = 64;
-        const int W = nthreads / 32;
-        const size_t smem = ((size_t)W * NK1 + NK1 + 2 * (size_t)n_keys + 160 + 8) * 4 + (size_t)(L + 3) / 4 * 4;
+        const size_t smem = dense_meta_smem_bytes(nthreads, 1, L);
         static std::atomic<int> configured_small[64];
         const int dev = pool->device < 64 ? pool->device : 63;
         if (!configured_small[dev].load(std::memory_order_acquire)) {

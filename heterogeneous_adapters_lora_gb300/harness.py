@@ -146,6 +146,13 @@ class DenseRun:
         self.build_meta()
         self.apply()
 
+    def step_batch(self, T=None):
+        """The same step through the single call that builds the metadata and
+        applies the layer (lora_build_meta_apply)."""
+        T = self.case.T if T is None else T
+        L.lora_build_meta_apply(self.pool, self.idx, T, self.mb.meta, self.x, self.ldx, self.y, self.ldy, self.ws,
+                                self.ws_bytes)
+
     def y_full_host(self) -> np.ndarray:
         """All ldy columns of y, padding included."""
         return from_dev_u16(self.y)

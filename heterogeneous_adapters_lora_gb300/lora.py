@@ -93,6 +93,8 @@ EXPORTS = {
     "lora_set_spin_limit": (None, [c_i32]),
     "lora_set_kernel_policy": (None, [c_i32]),
     "lora_kernel_launch_count": (ctypes.c_ulonglong, []),
+    "lora_build_meta_apply": (c_i32, [c_vp, c_vp, c_i32, ctypes.POINTER(Meta), c_vp, c_i64, c_vp, c_i64, c_vp, c_size,
+                                      c_vp]),
     "lora_last_cuda_error": (c_i32, []),
     "lora_linear_apply": (c_i32, [c_vp, ctypes.POINTER(Meta), c_vp, c_i64, c_vp, c_i64, c_vp, c_vp, c_i64, c_vp, c_size,
                               c_vp]),
@@ -204,6 +206,11 @@ def lora_meta_bind(meta: Meta, d_buf, nbytes, max_rows, max_keys):
 def lora_build_meta(pool, d_idx, T, d_topk_ids, top_k, meta: Meta, stream=None):
     _check(lib().lora_build_meta(pool, ptr(d_idx), T, ptr(d_topk_ids), top_k, ctypes.byref(meta),
                                  stream_ptr(stream)), "lora_build_meta")
+
+
+def lora_build_meta_apply(pool, d_idx, T, meta: Meta, x, ldx, y, ldy, ws, ws_bytes, stream=None):
+    _check(lib().lora_build_meta_apply(pool, ptr(d_idx), T, ctypes.byref(meta), ptr(x), ldx, ptr(y), ldy, ptr(ws),
+                                       ws_bytes, stream_ptr(stream)), "lora_build_meta_apply")
 
 
 def lora_shrink(pool, meta: Meta, x, ldx, v, stream=None):

@@ -260,6 +260,23 @@ LORA_API lora_status_t lora_apply_slices(const lora_pool_t *pool, const lora_met
                                 int64_t ldx, void *y, int64_t ldy, void *workspace,
                                 size_t ws_bytes, void *stream);
 
+/* The first LoRA layer of a serving step in one call: builds the batch
+ * metadata of d_idx ([T] int32 slots, -1 = none) into meta exactly as
+ * lora_build_meta(pool, d_idx, T, NULL, 1, meta, stream) does, and adds the
+ * delta of this dense layer to y as lora_apply_slices(pool, meta, x, ldx, y,
+ * ldy, workspace, ws_bytes, stream) does (the per-batch tables of SGLang's
+ * LoRAManager.prepare_lora_batch followed by the layer's add_shrink /
+ * add_expand).  Later layers of the step reuse meta with lora_apply_slices.
+ * For decode-sized batches of a pool the fused decode kernel serves (see
+ * lora_set_kernel_policy) both happen in one launch: every slot's cluster
+ * finds its rows in d_idx while one more CTA writes the metadata, so the
+ * layer does not wait for the metadata build.  Otherwise the two calls are
+ * made in order.  Arguments, errors and the workspace as the two calls;
+ * LORA_ERR_UNSUPPORTED for a MoE pool. */
+LORA_API lora_status_t lora_build_meta_apply(const lora_pool_t *pool, const int32_t *d_idx, int32_t T,
+                                             lora_meta_t *meta, const void *x, int64_t ldx, void *y, int64_t ldy,
+                                             void *workspace, size_t ws_bytes, void *stream);
+
 /* Same result as lora_apply_slices, but for callers that cannot provide a
  * workspace: the library allocates nothing and uses one fixed scratch array
  * in its own device image (lora_static_scratch_bytes() bytes, 8 MiB, held on

@@ -86,9 +86,26 @@ def is_linear(name):
     return name == "linear_qkv"
 
 
-def apply_kernels(name, policy):
+def is_plain_dense(name):
+    return not (is_moe(name) or is_sink(name) or is_linear(name))
+
+
+def do_step(name, r):
+    """One step of the hot path: a plain dense layer builds the batch metadata
+    and applies the delta through the single call that does both
+    (lora_build_meta_apply); the other workloads make their calls in order."""
+    if is_plain_dense(name):
+        r.step_batch()
+    else:
+        r.step()
+
+
+def apply_kernels(name, policy, fused=False):
     """The kernels one apply call launches for this workload (the roofline's
     'dominant kernel': the apply's launches, timed together)."""
+    if fused:
+        return ("bgmv_fused_kernel in batch mode (one launch: one thread-block cluster per adapter slot does the "
+                "shrink, the DSMEM reduction and the expand, one more CTA builds the batch metadata)")
     if policy == 1:
         k = "grouped_lora_kernel (persistent split-K)"
     elif policy == 2:
@@ -418,16 +435,18 @@ def measure(name, runs, ab, args, torch, stream, L, world, dev, sampler=None):
     n_rot = len(runs)
     for r in runs:                       # warm-up outside any graph
         for _ in range(max(1, args.warmup)):
-            r.step()
+            do_step(name, r)
     stream.synchronize()
     n0 = L.lora_kernel_launch_count()
-    runs[0].step()
+    do_step(name, runs[0])
     stream.synchronize()
     launches_per_step = L.lora_kernel_launch_count() - n0
+    # a plain dense step of one launch is the fused kernel in batch mode
+    fused = is_plain_dense(name) and launches_per_step == 1
 
     def steps(k):
         for i in range(k):
-            runs[i % n_rot].step()
+            do_step(name, runs[i % n_rot])
 
     # warm-up steps (W >= 3) as a graph, then the clocks are sampled over ~1 s
     # of the same work, and the K timed steps run while they are still sampled
@@ -473,6 +492,8 @@ def measure(name, runs, ab, args, torch, stream, L, world, dev, sampler=None):
             if moe:
                 r.w13()
                 r.w2()
+            elif fused:
+                r.step_batch()  # the step's one kernel
             else:
                 r.apply()
 
@@ -481,11 +502,16 @@ def measure(name, runs, ab, args, torch, stream, L, world, dev, sampler=None):
             runs[k % n_rot].build_meta()
     kms, _ = time_graph(torch, stream, applies, reps)
     meta_ms, _ = time_graph(torch, stream, metas, reps)
-    return dict(ms=ms, kms=kms / KA, meta_ms=meta_ms / KA, launches_per_step=launches_per_step, n_rot=n_rot)
+    return dict(ms=ms, kms=kms / KA, meta_ms=meta_ms / KA, launches_per_step=launches_per_step, n_rot=n_rot,
+                fused=fused)
 
 
-def kernel_bytes(name, ab):
-    return (ab["w13"] + ab["w2"]) if is_moe(name) else (ab["total"] - ab["idx"])
+def kernel_bytes(name, ab, fused=False):
+    """Algorithmic bytes of the timed kernels: the apply's (x, A, B, y), plus
+    the idx vector when the metadata build runs in the same launch."""
+    if is_moe(name):
+        return ab["w13"] + ab["w2"]
+    return ab["total"] if fused else ab["total"] - ab["idx"]
 
 
 def run_gpu(args, rank, world, local_rank):
@@ -572,7 +598,7 @@ def run_gpu(args, rank, world, local_rank):
                     ev_in[i].record(s_in)
                 stream.wait_event(ev_in[i])
                 with torch.cuda.stream(stream):
-                    r.step()
+                    do_step(name, r)
                     ev_calls[i].record(stream)
                 s_out.wait_event(ev_calls[i])
                 with torch.cuda.stream(s_out):
@@ -635,14 +661,14 @@ def run_gpu(args, rank, world, local_rank):
                     r.close()
                 del w_runs
                 torch.cuda.synchronize(dev)
-                wkb = kernel_bytes(wn, w_ab)
+                wkb = kernel_bytes(wn, w_ab, wm["fused"])
                 ent = {"tokens_per_s": wc.T * args.steps / (wm["ms"] * 1e-3), "step_us": wm["ms"] / args.steps * 1e3,
                        "apply_us": wm["kms"] * 1e3, "metadata_us": wm["meta_ms"] * 1e3,
                        "apply_gbs": wkb / (wm["kms"] * 1e-3) / 1e9,
                        "frac": wkb / (wm["kms"] * 1e-3) / 1e9 / peak,
                        "algorithmic_bytes_per_apply": wkb, "tokens_per_step": wc.T,
                        "launches_per_step": wm["launches_per_step"], "copies": wm["n_rot"],
-                       "kernel": apply_kernels(wn, args.kernel_policy)}
+                       "kernel": apply_kernels(wn, args.kernel_policy, wm["fused"])}
                 if not args.no_cpu_baseline:
                     ent["cpu_baseline"] = time_oracle(wn, wc, min_seconds=args.cpu_seconds)
                 per[wn] = ent
@@ -654,7 +680,7 @@ def run_gpu(args, rank, world, local_rank):
     tokens = c.T
     value = whole_job_throughput(tokens, args.steps, world, ms)
     e2e = whole_job_throughput(tokens, e2e_n, world, e2e_ms)
-    kbytes = kernel_bytes(name, ab)
+    kbytes = kernel_bytes(name, ab, m["fused"])
     achieved = kbytes / (kms * 1e-3) / 1e9
     n_rot = m["n_rot"]
     line = {
@@ -668,12 +694,12 @@ def run_gpu(args, rank, world, local_rank):
                    "hbm_gbs_per_step": ab["total"] / (ms / args.steps * 1e-3) / 1e9,
                    "l2": f"inputs rotate over {n_rot} resident copies "
                          f"({n_rot * ab['total'] / 1e6:.0f} MB of algorithmic bytes, L2 {l2 / 1e6:.0f} MB)",
-                   "timing": f"one CUDA graph of exactly {args.steps} steps (metadata + apply each, rotating "
+                   "timing": f"one CUDA graph of exactly {args.steps} steps (metadata + apply each, one lora_build_meta_apply call for a dense layer; rotating "
                              f"copies), replayed once untimed and once between CUDA events",
                    "parallelism": f"replicas{world}",
                    "metadata_us_alone": meta_ms * 1e3, "apply_us_alone": kms * 1e3,
                    "per_workload": per},
-        "roofline": {"bound": "hbm", "kernel": apply_kernels(name, args.kernel_policy),
+        "roofline": {"bound": "hbm", "kernel": apply_kernels(name, args.kernel_policy, m["fused"]),
                      "achieved": achieved, "peak": peak,
                      "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s", "frac": achieved / peak,
                      "traffic": ncu_traffic(name, "moe" if moe else "apply"),

@@ -190,9 +190,15 @@ __global__ void __launch_bounds__(kFThreads, MINB) bgmv_fused_kernel(const __gri
     // ---------------- the metadata (and everything before it) is complete
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
-    if (p.idx_mode) {
-        for (int i = tid; i < p.T; i += kFThreads) s_sorted[i] = __ldcg(p.idx + i);
-    } else {
+    // batch mode: the slots of rows j*256 + tid, kept in registers (stored to
+    // shared memory once the work below no longer waits behind them)
+    int iv[kMaxT / kFThreads];
+#pragma unroll
+    for (int j = 0; j < kMaxT / kFThreads; ++j) {
+        const int t = j * kFThreads + tid;
+        iv[j] = (p.idx_mode && t < p.T) ? __ldcg(p.idx + t) : -1;
+    }
+    if (!p.idx_mode) {
         for (int i = tid; i < p.T; i += kFThreads) s_sorted[i] = __ldcg(p.sorted + i);
         if (tid == 0) {
             s_nb[0] = __ldcg(p.key_count + a);
@@ -243,7 +249,7 @@ __global__ void __launch_bounds__(kFThreads, MINB) bgmv_fused_kernel(const __gri
 #pragma unroll
         for (int j = 0; j < kMaxT / kFThreads; ++j) {
             const int t = j * kFThreads + tid;
-            m4[j] = __ballot_sync(0xffffffffu, j < nj && t < p.T && s_sorted[t] == a);
+            m4[j] = __ballot_sync(0xffffffffu, j < nj && t < p.T && iv[j] == a);
             if (j < nj && lane == 0) s_cnt[j * kFWarps + warp] = __popc(m4[j]);
         }
         __syncthreads();
@@ -398,38 +404,6 @@ __global__ void __launch_bounds__(kFThreads, MINB) bgmv_fused_kernel(const __gri
         if (kh == 0) store_pairs(false);
         __syncthreads();
         if (kh == 1) store_pairs(true);
-        // the expand's operands, in flight during the cluster barrier and the
-        // gather: B rows o0 + 4g + q (ranks ks*16 + 4c4 .. +3) of each group
-        // and the y values of rows g and g+8, outputs o0 + 8c4 .. +7
-        const bool r0ok = g < nt, r1ok = g + 8 < nt;
-        const long long yrow0 = r0ok ? (long long)s_tok[g] * p.ldy : 0, yrow1 = r1ok ? (long long)s_tok[g + 8] * p.ldy : 0;
-        uint2 bq[GMAX][4][KSX];
-        uint4 yv[GMAX][2];
-        int gj[GMAX];  // slice of each group
-#pragma unroll
-        for (int i = 0; i < GMAX; ++i) {
-            gj[i] = 0;
-            yv[i][0] = yv[i][1] = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-#pragma unroll
-                for (int ks = 0; ks < KSX; ++ks) bq[i][q][ks] = make_uint2(0u, 0u);
-            if (i < ngw) {
-                const int o0 = ob0 + (warp + kFWarps * i) * 32;
-                int jj = 0;
-                for (int j = 1; j < ns; ++j)
-                    if (o0 >= s_oo[j]) jj = j;
-                gj[i] = jj;
-                const uint16_t *bb = s_B[jj] + (long long)(o0 - s_oo[jj] + 4 * g) * rs + 4 * c4;
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-#pragma unroll
-                    for (int ks = 0; ks < KSX; ++ks)
-                        if (ks * 16 + 4 * c4 < rs) bq[i][q][ks] = __ldg((const uint2 *)(bb + (long long)q * rs + ks * 16));
-                if (r0ok) yv[i][0] = __ldcg((const uint4 *)(p.y + yrow0 + o0 + 8 * c4));
-                if (r1ok) yv[i][1] = __ldcg((const uint4 *)(p.y + yrow1 + o0 + 8 * c4));
-            }
-        }
         __syncthreads();
         cluster_arrive();
         cluster_wait();  // every CTA's P of this tile is complete and visible
@@ -482,6 +456,37 @@ __global__ void __launch_bounds__(kFThreads, MINB) bgmv_fused_kernel(const __gri
             }
         }
         cluster_arrive();  // this CTA has read its peers' P
+        // the expand's operands: B rows o0 + 4g + q (ranks ks*16 + 4c4 .. +3) of each group
+        // and the y values of rows g and g+8, outputs o0 + 8c4 .. +7
+        const bool r0ok = g < nt, r1ok = g + 8 < nt;
+        const long long yrow0 = r0ok ? (long long)s_tok[g] * p.ldy : 0, yrow1 = r1ok ? (long long)s_tok[g + 8] * p.ldy : 0;
+        uint2 bq[GMAX][4][KSX];
+        uint4 yv[GMAX][2];
+        int gj[GMAX];  // slice of each group
+#pragma unroll
+        for (int i = 0; i < GMAX; ++i) {
+            gj[i] = 0;
+            yv[i][0] = yv[i][1] = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int ks = 0; ks < KSX; ++ks) bq[i][q][ks] = make_uint2(0u, 0u);
+            if (i < ngw) {
+                const int o0 = ob0 + (warp + kFWarps * i) * 32;
+                int jj = 0;
+                for (int j = 1; j < ns; ++j)
+                    if (o0 >= s_oo[j]) jj = j;
+                gj[i] = jj;
+                const uint16_t *bb = s_B[jj] + (long long)(o0 - s_oo[jj] + 4 * g) * rs + 4 * c4;
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+#pragma unroll
+                    for (int ks = 0; ks < KSX; ++ks)
+                        if (ks * 16 + 4 * c4 < rs) bq[i][q][ks] = __ldg((const uint2 *)(bb + (long long)q * rs + ks * 16));
+                if (r0ok) yv[i][0] = __ldcg((const uint4 *)(p.y + yrow0 + o0 + 8 * c4));
+                if (r1ok) yv[i][1] = __ldcg((const uint4 *)(p.y + yrow1 + o0 + 8 * c4));
+            }
+        }
         __syncthreads();   // v tiles written
 
         // ---------------- expand of output block c: this warp's groups

@@ -44,6 +44,8 @@ WORKLOADS = {
     "moe_shared": "MoE-LoRA as 'moe' in the shared-outer layout (w13-A and w2-B expert dim 1)",
     "moe_decode": "MoE-LoRA at decode: as 'moe' with T=16 (128 pairs over 512 (adapter, expert) keys: "
                   "sparse occupancy, one 16-row tile per non-empty key)",
+    "moe_sparse": "MoE-LoRA at sparse occupancy: as 'moe' with T=8 (64 pairs, T*top_k*8 = 512 <= 64 experts x "
+                  "8 adapters: the regime of the pages' naive block assignment)",
     "linear_qkv": "full LoRA linear layer at decode: the decode_qkv batch with its base weight 4096 -> 6144 "
                   "and bias: y = x W^T + bias (cuBLASLt) + LoRA delta",
     "inkling_sink": "Inkling sink experts at decode: T=256, d_model 2048, 2 sink experts of d_mlp 1408: "
@@ -67,6 +69,8 @@ def make_case(name):
         return gen.moe(shared_outer=True)
     if name == "moe_decode":
         return gen.moe(T=16)
+    if name == "moe_sparse":
+        return gen.moe(T=8)
     if name == "inkling_sink":
         return gen.inkling_sink()
     if name == "linear_qkv":
@@ -106,6 +110,13 @@ def apply_kernels(name, policy, fused=False):
     if fused:
         return ("bgmv_fused_kernel in batch mode (one launch: one thread-block cluster per adapter slot does the "
                 "shrink, the DSMEM reduction and the expand, one more CTA builds the batch metadata)")
+    if is_moe(name):
+        c = make_case(name)
+        sparse = c.T * c.K * 8 <= c.E * c.L
+        if policy == 5 or (policy == 0 and sparse):
+            return "moe_block_kernel over the metadata's 16-row tiles (one thread-block cluster per tile) for w13 and w2"
+        if policy == 4:
+            return "moe_align_padded_kernel (block_m 1) + moe_block_kernel (one cluster per pair) for w13 and w2"
     if policy == 1:
         k = "grouped_lora_kernel (persistent split-K)"
     elif policy == 2:
@@ -732,8 +743,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-workload", action="store_true",
                     help="time only --workload (skip the per_workload block of the other configurations)")
-    ap.add_argument("--kernel-policy", type=int, default=0, choices=[0, 1, 2],
-                    help="0 automatic, 1 persistent split-K kernel, 2 cluster kernel first (tuning)")
+    ap.add_argument("--kernel-policy", type=int, default=0, choices=[0, 1, 2, 3, 4, 5],
+                    help="lora_set_kernel_policy: 0 automatic, 1 persistent split-K kernel, 2 cluster kernel "
+                         "first, 3 no fused decode / MoE block kernel, 4 MoE per-pair blocks, 5 MoE block kernel "
+                         "over the metadata's tiles (tuning)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

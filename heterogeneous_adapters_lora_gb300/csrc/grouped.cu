@@ -35,6 +35,9 @@ constexpr int kOC = 2 * kThreads;      // output columns per expand item
 constexpr int kMaxHC = 1024;           // hidden chunk cap (shared-memory x tile)
 constexpr int kXPad = 8;               // bf16 padding per staged x row
 constexpr int kRedUnits = 16;
+// vLLM's FusedMoEWithLoRA gives every routed pair a block of its own when
+// num_tokens * top_k * SPARSITY_FACTOR <= num_experts * max_loras
+constexpr long long kSparsityFactor = 8;
 
 enum Mode { kFused = 0, kShrinkAtomic = 1, kExpandOnly = 2 };
 
@@ -862,10 +865,30 @@ extern "C" lora_status_t lora_moe_apply(const lora_pool_t *pool, const lora_meta
     const bool have_split_region = sp_bytes <= cv.data_bytes;
     lora_status_t st = LORA_OK;
     cudaStream_t s = (cudaStream_t)stream;
-    if (g_lora_kernel_policy != 1) {
+    const int pol = g_lora_kernel_policy;
+    const bool sparse = (long long)rows * kSparsityFactor <= keys;
+    if ((pol == 5 || (pol == 0 && sparse)) && lora_moe_block_supported(pool, which)) {
+        // sparse occupancy: one thread-block cluster per (adapter, expert) key's tile
+        return lora_moe_tile_launch(pool, meta, which, in, ld_in, topk_w, out, ld_out, s);
+    }
+    if (pol == 4 && lora_moe_block_supported(pool, which)) {
+        // sparse occupancy: every routed pair a block of its own (block_m 1),
+        // aligned into the workspace, then one cluster per block
+        const size_t L = d.max_loras;
+        const size_t b_sorted = align256(L * rows * 4), b_expert = align256(L * rows * 4);
+        if (b_sorted + b_expert + align256(L * 4) <= cv.data_bytes) {
+            int32_t *ds = (int32_t *)cv.data;
+            int32_t *de = (int32_t *)(cv.data + b_sorted);
+            int32_t *dn = (int32_t *)(cv.data + b_sorted + b_expert);
+            st = lora_moe_align_launch(pool, meta, 1, rows, ds, de, dn, s);
+            if (st != LORA_OK) return st;
+            return lora_moe_block_launch(pool, meta, which, in, ld_in, topk_w, out, ld_out, ds, de, dn, 1, rows, s);
+        }
+    }
+    if (pol != 1) {
         bool launched = false;
         const LoraProblem pr = to_problem(g, meta, keys);
-        if ((g_lora_kernel_policy == 0 || g_lora_kernel_policy == 3) && have_split_region) {
+        if ((pol == 0 || pol == 3 || pol == 4 || pol == 5) && have_split_region) {
             st = lora_split_apply(pool, pr, cv.data, cv.data_bytes, cv.ctrl + 2, s, &launched);
             if (st != LORA_OK || launched) return st;
         }

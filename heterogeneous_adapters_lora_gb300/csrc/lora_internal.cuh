@@ -175,3 +175,19 @@ lora_status_t lora_fused_apply(const lora_pool_t *pool, const lora_meta_t *meta,
 lora_status_t lora_dense_apply(const lora_pool_t *pool, const lora_meta_t *meta, const void *x, int64_t ldx,
                                void *y, int64_t ldy, void *workspace, size_t ws_bytes, float post_scale,
                                cudaStream_t s);
+
+// Block-padded MoE alignment (moe_align.cu), launched with programmatic
+// dependent launch after a metadata build; arguments checked by the caller.
+lora_status_t lora_moe_align_launch(const lora_pool_t *pool, const lora_meta_t *meta, int32_t block_m, int32_t cap,
+                                    int32_t *d_sorted, int32_t *d_expert, int32_t *d_npp, cudaStream_t s);
+// Per-block MoE-LoRA over that alignment (moe_block.cu): whether the kernel
+// takes projection `which` of the pool, and its launch (arguments checked).
+bool lora_moe_block_supported(const lora_pool_t *pool, int which);
+lora_status_t lora_moe_block_launch(const lora_pool_t *pool, const lora_meta_t *meta, int32_t which, const void *in,
+                                    int64_t ld_in, const float *topk_w, void *out, int64_t ld_out,
+                                    const int32_t *d_sorted, const int32_t *d_expert, const int32_t *d_npp,
+                                    int32_t block_m, int32_t cap, cudaStream_t s);
+// The same kernel over the 16-row tiles of the metadata (one block per tile;
+// in the sparse-occupancy regime a tile is an (adapter, expert) key's few pairs).
+lora_status_t lora_moe_tile_launch(const lora_pool_t *pool, const lora_meta_t *meta, int32_t which, const void *in,
+                                   int64_t ld_in, const float *topk_w, void *out, int64_t ld_out, cudaStream_t s);

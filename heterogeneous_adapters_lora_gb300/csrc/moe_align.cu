@@ -21,6 +21,8 @@ __global__ void __launch_bounds__(kThreads) moe_align_padded_kernel(const int32_
     __shared__ int s_warp[kThreads / 32 + 1];
     const int a = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nb = cap / block_m;
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the metadata build is complete
+    asm volatile("griddepcontrol.launch_dependents;");
     // this thread's contiguous range of experts
     const int per = (E + kThreads - 1) / kThreads;
     const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
@@ -65,19 +67,36 @@ __global__ void __launch_bounds__(kThreads) moe_align_padded_kernel(const int32_
 
 }  // namespace
 
+lora_status_t lora_moe_align_launch(const lora_pool_t *pool, const lora_meta_t *meta, int32_t block_m, int32_t cap,
+                                    int32_t *d_sorted, int32_t *d_expert, int32_t *d_npp, cudaStream_t s) {
+    const int E = pool->desc.num_experts, L = pool->desc.max_loras;
+    const long long P = (long long)meta->T * meta->top_k;
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3((unsigned)L, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    LORA_CUDA_TRY(cudaLaunchKernelEx(&cfg, moe_align_padded_kernel, (const int32_t *)meta->sorted,
+                                     (const int32_t *)meta->key_count, (const int32_t *)meta->key_offset, E, (int)P,
+                                     (int)block_m, (int)cap, d_sorted, d_expert, d_npp));
+    lora_note_launch();
+    return LORA_OK;
+}
+
 extern "C" lora_status_t lora_moe_align_padded(const lora_pool_t *pool, const lora_meta_t *meta, int32_t block_m,
                                                int32_t cap, int32_t *d_sorted, int32_t *d_expert,
                                                int32_t *d_npp, void *stream) {
     if (!pool || !meta || !d_sorted || !d_expert || !d_npp) return LORA_ERR_INVALID_ARG;
     if (!pool->is_moe || meta->mode != 1) return LORA_ERR_UNSUPPORTED;
     if (block_m < 1 || cap < block_m || cap % block_m) return LORA_ERR_INVALID_ARG;
-    const int E = pool->desc.num_experts, L = pool->desc.max_loras;
+    const int E = pool->desc.num_experts;
     const long long P = (long long)meta->T * meta->top_k;
     // worst case for one adapter: every pair plus block_m - 1 padding per expert
     if ((long long)cap < P + (long long)E * (block_m - 1)) return LORA_ERR_CAPACITY;
-    moe_align_padded_kernel<<<L, kThreads, 0, (cudaStream_t)stream>>>(
-        meta->sorted, meta->key_count, meta->key_offset, E, (int)P, block_m, cap, d_sorted, d_expert, d_npp);
-    LORA_CUDA_TRY(cudaGetLastError());
-    lora_note_launch();
-    return LORA_OK;
+    return lora_moe_align_launch(pool, meta, block_m, cap, d_sorted, d_expert, d_npp, (cudaStream_t)stream);
 }

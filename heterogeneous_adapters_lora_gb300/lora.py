@@ -89,6 +89,8 @@ EXPORTS = {
     "lora_moe_apply": (c_i32, [c_vp, ctypes.POINTER(Meta), c_i32, c_vp, c_i64, c_vp, c_vp, c_i64, c_vp,
                                c_size, c_vp]),
     "lora_moe_align_padded": (c_i32, [c_vp, ctypes.POINTER(Meta), c_i32, c_i32, c_vp, c_vp, c_vp, c_vp]),
+    "lora_moe_apply_blocks": (c_i32, [c_vp, ctypes.POINTER(Meta), c_i32, c_vp, c_i64, c_vp, c_vp, c_i64, c_vp, c_vp,
+                                      c_vp, c_i32, c_i32, c_vp]),
     "lora_get_device_status": (c_i32, [c_vp, c_vp]),
     "lora_set_spin_limit": (None, [c_i32]),
     "lora_set_kernel_policy": (None, [c_i32]),
@@ -260,6 +262,13 @@ def lora_moe_apply(pool, meta: Meta, which, inp, ld_in, topk_w, out, ld_out, ws,
 def lora_moe_align_padded(pool, meta: Meta, block_m, cap, d_sorted, d_expert, d_npp, stream=None):
     _check(lib().lora_moe_align_padded(pool, ctypes.byref(meta), block_m, cap, ptr(d_sorted), ptr(d_expert),
                                        ptr(d_npp), stream_ptr(stream)), "lora_moe_align_padded")
+
+
+def lora_moe_apply_blocks(pool, meta: Meta, which, inp, ld_in, topk_w, out, ld_out, d_sorted, d_expert, d_npp,
+                          block_m, cap, stream=None):
+    _check(lib().lora_moe_apply_blocks(pool, ctypes.byref(meta), which, ptr(inp), ld_in, ptr(topk_w), ptr(out),
+                                       ld_out, ptr(d_sorted), ptr(d_expert), ptr(d_npp), block_m, cap,
+                                       stream_ptr(stream)), "lora_moe_apply_blocks")
 
 
 def lora_get_device_status(pool, stream=None) -> int:

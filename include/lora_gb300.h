@@ -355,6 +355,23 @@ LORA_API lora_status_t lora_moe_align_padded(const lora_pool_t *pool, const lora
                                              int32_t cap, int32_t *d_sorted, int32_t *d_expert,
                                              int32_t *d_npp, void *stream);
 
+/* add_lora_fused_moe over a block-padded alignment (the schedule vLLM's
+ * FusedMoEWithLoRA runs on sorted_token_ids_lora / expert_ids_lora; with
+ * block_m = 1 every routed pair is a block of its own, the naive assignment
+ * it takes when num_tokens * top_k * 8 <= num_experts * max_loras).
+ * d_sorted, d_expert, d_npp, block_m and cap as written by
+ * lora_moe_align_padded from the same meta; which, in, ld_in, topk_w, out
+ * and ld_out as lora_moe_apply, with the same result.  No workspace.
+ * Entries of d_sorted outside [0, T*top_k) and blocks whose expert is
+ * outside [0, num_experts) are skipped.
+ * Errors: LORA_ERR_INVALID_ARG (also block_m outside [1, 16] or cap not a
+ * multiple of block_m), LORA_ERR_UNSUPPORTED (not a MoE pool; more than two
+ * w13 slices, max_rank above 64, or an input width above 4096). */
+LORA_API lora_status_t lora_moe_apply_blocks(const lora_pool_t *pool, const lora_meta_t *meta, int32_t which,
+                                             const void *in, int64_t ld_in, const float *topk_w, void *out,
+                                             int64_t ld_out, const int32_t *d_sorted, const int32_t *d_expert,
+                                             const int32_t *d_npp, int32_t block_m, int32_t cap, void *stream);
+
 /* ------------------------------------------------------------ status */
 
 /* Synchronise `stream`, return the pool's device status word (LORA_OK,
@@ -402,13 +419,22 @@ LORA_API lora_status_t lora_sink_experts_act(const void *gate_up, int64_t ld_gat
  * 0 = automatic (tcgen05 for long contiguous runs of a rank-64 dense pool;
  *     the fused decode kernel -- one thread-block cluster per adapter slot,
  *     shrink, on-chip reduction and expand in one launch -- for dense
- *     batches of a few rows per slot; otherwise the split shrink/expand
- *     kernels when the workspace holds their region, else the one-pass
- *     cluster kernel, else the persistent split-K kernel),
+ *     batches of a few rows per slot; for a MoE batch with
+ *     T*top_k*8 <= num_experts*max_loras the kernel of
+ *     lora_moe_apply_blocks over the metadata's 16-row tiles (one
+ *     thread-block cluster per (adapter, expert) key); otherwise the split
+ *     shrink/expand kernels when the workspace holds their region, else the
+ *     one-pass cluster kernel, else the persistent split-K kernel),
  * 1 = always the persistent split-K kernel,
  * 2 = like 0 but the one-pass cluster kernel before the split kernels
- *     (and no fused decode kernel),
- * 3 = like 0 without the fused decode kernel.
+ *     (and neither the fused decode kernel nor the MoE block kernel),
+ * 3 = like 0 without the fused decode kernel and the MoE block kernel
+ *     (the split 16-row-tile kernels at every MoE batch size),
+ * 4 = like 0, with the per-pair schedule (lora_moe_align_padded with
+ *     block_m 1, then lora_moe_apply_blocks) for every MoE batch it supports,
+ * 5 = like 0, with the kernel of lora_moe_apply_blocks run over the
+ *     metadata's 16-row tiles (one thread-block cluster per tile) for every
+ *     MoE batch it supports.
  * For tests and tuning. */
 LORA_API void lora_set_kernel_policy(int32_t policy);
 

@@ -17,7 +17,7 @@ from gpu_util import active_mask, assert_delta, assert_rows_untouched
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(params=[0, 1, 2, 3], ids=["auto", "splitk", "cluster", "split"])
+@pytest.fixture(params=[0, 1, 2, 3, 4, 5], ids=["auto", "splitk", "cluster", "split", "perpair", "tilecluster"])
 def policy(request):
     L.lora_set_kernel_policy(request.param)
     yield request.param

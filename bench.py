@@ -48,6 +48,8 @@ WORKLOADS = {
                   "8 adapters: the regime of the pages' naive block assignment)",
     "linear_qkv": "full LoRA linear layer at decode: the decode_qkv batch with its base weight 4096 -> 6144 "
                   "and bias: y = x W^T + bias (cuBLASLt) + LoRA delta",
+    "linear_prefill": "full LoRA linear layer at prefill: the prefill_gate_up batch (~8K tokens in 8 contiguous "
+                      "runs, rank 64) with its base weight 4096 -> 2x14336: y = x W^T + LoRA delta",
     "inkling_sink": "Inkling sink experts at decode: T=256, d_model 2048, 2 sink experts of d_mlp 1408: "
                     "w13 LoRA (2048 -> 2x2816) + SiLU(gate)*up*gamma + w2 LoRA (2816 -> 2048), "
                     "8 adapters rank 16, scale 2, 10% -1",
@@ -75,6 +77,8 @@ def make_case(name):
         return gen.inkling_sink()
     if name == "linear_qkv":
         return gen.linear_qkv()
+    if name == "linear_prefill":
+        return gen.linear_prefill()
     raise ValueError(name)
 
 
@@ -87,7 +91,7 @@ def is_sink(name):
 
 
 def is_linear(name):
-    return name == "linear_qkv"
+    return name.startswith("linear_")
 
 
 def is_plain_dense(name):
@@ -128,7 +132,10 @@ def apply_kernels(name, policy, fused=False):
     if is_sink(name):
         return k + " on w13, sink_act_kernel, the same on w2"
     if is_linear(name):
-        return "cuBLASLt base GEMM, then " + k
+        if policy == 6:
+            return "cuBLASLt base GEMM, then " + k
+        return ("linear_slot_kernel + lora_shrink (grouped_lora_kernel) + linear_lora_kernel (tcgen05 GEMM whose "
+                "accumulator also takes the delta as extra K blocks)")
     if name == "prefill_gate_up" and policy != 1:
         k = "sgmv_shrink_kernel + sgmv_expand_kernel (tcgen05, 128-row runs); short tiles: " + k
     return k + (" for w13 and w2" if is_moe(name) else "")
@@ -380,6 +387,23 @@ def load_peaks():
         return float(p["hbm_gbs"]), "measured"
     except (OSError, ValueError, KeyError):
         return 6800.0, "fallback"
+
+
+def load_tensor_peak():
+    """Sustained dense bf16 TFLOP/s of this GPU (a kernel timed inside a long run)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops_sustained"]), "measured"
+    except (OSError, ValueError, KeyError):
+        return 1700.0, "fallback"
+
+
+def linear_flops(c):
+    """Algorithmic FLOPs of the full linear layer: the base GEMM over every
+    token plus the shrink and expand of the tokens with an active adapter."""
+    delta = sum(2 * int(c.ranks[a]) * (c.H * len(c.out_dims) + c.out_total) for a in c.idx
+                if 0 <= a < c.L and c.enabled[a] and c.ranks[a] > 0)
+    return 2 * c.T * c.H * c.out_total + delta
 
 
 def max_over_ranks(values, world, device=None):
@@ -723,6 +747,15 @@ def run_gpu(args, rank, world, local_rank):
                           if e2e_graph is not None else "eager pipelined calls"},
         "gpu_launches": m["launches_per_step"] * args.steps,
     }
+    if name == "linear_prefill":
+        # a dense contraction: the roofline is the tensor pipe's
+        tpk, tkind = load_tensor_peak()
+        fl = linear_flops(c)
+        line["roofline"] = {"bound": "tensor", "kernel": apply_kernels(name, args.kernel_policy, m["fused"]),
+                            "achieved": fl / (kms * 1e-3) / 1e12, "peak": tpk,
+                            "peak_kind": f"{tkind} bf16_tflops_sustained", "unit": "TFLOP/s",
+                            "frac": fl / (kms * 1e-3) / 1e12 / tpk, "traffic": None,
+                            "algorithmic_flops_per_launch": fl, "avg_launch_us": kms * 1e3}
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = time_oracle(name, c, min_seconds=args.cpu_seconds)
     print(json.dumps(line), flush=True)
@@ -743,10 +776,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-workload", action="store_true",
                     help="time only --workload (skip the per_workload block of the other configurations)")
-    ap.add_argument("--kernel-policy", type=int, default=0, choices=[0, 1, 2, 3, 4, 5],
+    ap.add_argument("--kernel-policy", type=int, default=0, choices=[0, 1, 2, 3, 4, 5, 6],
                     help="lora_set_kernel_policy: 0 automatic, 1 persistent split-K kernel, 2 cluster kernel "
                          "first, 3 no fused decode / MoE block kernel, 4 MoE per-pair blocks, 5 MoE block kernel "
-                         "over the metadata's tiles (tuning)")
+                         "over the metadata's tiles, 6 linear layer as cuBLASLt + second pass (tuning)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -624,6 +624,14 @@ extern "C" void lora_set_kernel_policy(int32_t policy) { g_lora_kernel_policy = 
 
 extern "C" void lora_set_spin_limit(int32_t max_polls) { g_spin_limit = max_polls; }
 
+bool lora_ws_data(void *workspace, size_t ws_bytes, char **data, size_t *data_bytes) {
+    Carve cv;
+    if (!workspace || !lora_aligned16(workspace) || !carve(workspace, ws_bytes, cv)) return false;
+    *data = cv.data;
+    *data_bytes = cv.data_bytes;
+    return true;
+}
+
 extern "C" size_t lora_workspace_bytes(const lora_pool_t *pool, int32_t T, int32_t top_k) {
     if (!pool || T < 0) return 0;
     const lora_pool_desc_t &d = pool->desc;
@@ -631,7 +639,11 @@ extern "C" size_t lora_workspace_bytes(const lora_pool_t *pool, int32_t T, int32
         const Plan pl = make_plan(pool->num_sms, d.in_dim, d.n_slices, d.max_rank, T, d.max_loras);
         const size_t sp = lora_split_ws_bytes(d.n_slices, d.in_dim, d.max_rank, T, max_tiles(T, d.max_loras));
         const size_t pk = align256(pl.part_floats * 4);
-        return ws_total(sgmv_region_bytes(pool, T) + (pk > sp ? pk : sp), pl.cnt_ints);
+        // lora_linear_apply: v [n_slices][T][max_rank] fp32 and one slot per token
+        const size_t lin = align256((size_t)d.n_slices * T * d.max_rank * 4) + align256((size_t)T * 4);
+        size_t data = sgmv_region_bytes(pool, T) + (pk > sp ? pk : sp);
+        if (lin > data) data = lin;
+        return ws_total(data, pl.cnt_ints);
     }
     if (top_k < 1) return 0;
     const int rows = T * top_k, keys = d.max_loras * d.num_experts;

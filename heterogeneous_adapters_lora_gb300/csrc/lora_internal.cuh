@@ -191,3 +191,7 @@ lora_status_t lora_moe_block_launch(const lora_pool_t *pool, const lora_meta_t *
 // in the sparse-occupancy regime a tile is an (adapter, expert) key's few pairs).
 lora_status_t lora_moe_tile_launch(const lora_pool_t *pool, const lora_meta_t *meta, int32_t which, const void *in,
                                    int64_t ld_in, const float *topk_w, void *out, int64_t ld_out, cudaStream_t s);
+
+// The scratch part of an apply workspace (past its control words); false
+// if the workspace is null, misaligned or too small to carve.
+bool lora_ws_data(void *workspace, size_t ws_bytes, char **data, size_t *data_bytes);

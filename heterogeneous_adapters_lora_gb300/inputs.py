@@ -329,6 +329,17 @@ def prefill_gate_up(base_y: str = "zero", permuted: bool = False) -> DenseCase:
     return c
 
 
+def linear_prefill() -> DenseCase:
+    """The prefill gate_up batch as a full LoRA linear layer: base weight
+    [28672][4096] ~ N(0, 0.02)."""
+    lens = prefill_lengths()
+    idx = np.concatenate([np.full(int(n), s, np.int32) for n, s in zip(lens, range(8))])
+    c = dense_case(name="linear_prefill", T=int(lens.sum()), H=4096, out_dims=(14336, 14336), L=8, R=64,
+                   seed=1104, idx=idx, with_W=True)
+    c.meta["lengths"] = lens
+    return c
+
+
 def zipf_pmf(n: int, s: float) -> np.ndarray:
     k = np.arange(1, n + 1, dtype=np.float64)
     p = k ** (-s)

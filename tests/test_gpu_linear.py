@@ -113,3 +113,50 @@ def test_linear_argument_errors():
         assert e.value.code == L.CODE["LORA_ERR_INVALID_ARG"]
     finally:
         run.close()
+
+
+def _segment_idx(T, lengths_slots):
+    idx = np.empty(T, np.int32)
+    t = 0
+    for n, a in lengths_slots:
+        idx[t:t + n] = a
+        t += n
+    assert t == T
+    return idx
+
+
+def test_linear_prefill_segments_wide_tiles():
+    """Prefill-like batch: contiguous runs of one adapter (one run without),
+    mixed ranks up to 64, a ragged last tile, and enough tiles for the
+    256-wide output tiles of the tensor-core GEMM."""
+    T = 2100
+    idx = _segment_idx(T, [(300, 0), (517, 1), (129, 2), (200, -1), (411, 3), (64, 5), (279, 6), (200, 7)])
+    c = gen.dense_case(name="linear_prefill", T=T, H=512, out_dims=(2560, 2560), L=8, R=64, seed=1201,
+                       ranks=(64, 24, 8, 64, 0, 40, 64, 16), scales=(1.0, 0.5, 2.0, 1.0, 1.0, 1.5, 1.0, 0.25),
+                       idx=idx, with_W=True)
+    c = _small_base(c, 0.004, 5)
+    got, base, d_ref, act = _run(c, True, bias_std=0.004)
+    assert np.abs(base[act]).max() < 4 * np.abs(d_ref[act]).max()  # the base does not dominate
+    assert_delta(got[act] - base[act], d_ref[act], c.name + " delta alone")
+
+
+def test_linear_many_slots_per_tile():
+    """160 slots of rank <= 12 over 300 tokens: up to 128 distinct slots in a
+    128-token tile, four slots per delta block, and a hidden size of four K
+    blocks (every delta block after the base blocks)."""
+    rng = np.random.default_rng(77)
+    ranks = rng.choice([12, 5, 0, 8], size=160).astype(np.int32)
+    c = gen.dense_case(name="linear_many", T=300, H=256, out_dims=(384, 128), L=160, R=12, seed=1202,
+                       ranks=ranks, p_none=0.1, with_W=True)
+    c = _small_base(c, 0.0004, 6)
+    got, base, d_ref, act = _run(c, True, bias_std=0.0002, ldy=c.out_total + 8)
+    assert np.abs(base[act]).max() < 4 * np.abs(d_ref[act]).max()  # the base does not dominate
+    assert_delta(got[act] - base[act], d_ref[act], c.name + " delta alone")
+
+
+def test_linear_rank_above_64_uses_the_library_gemm():
+    c = gen.dense_case(name="linear_r72", T=70, H=256, out_dims=(256,), L=3, R=72, seed=1203, with_W=True)
+    c = _small_base(c, 0.002, 7)
+    got, base, d_ref, act = _run(c, False)
+    assert np.abs(base[act]).max() < 4 * np.abs(d_ref[act]).max()  # the base does not dominate
+    assert_delta(got[act] - base[act], d_ref[act], c.name + " delta alone")

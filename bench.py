@@ -133,9 +133,10 @@ def apply_kernels(name, policy, fused=False):
         return k + " on w13, sink_act_kernel, the same on w2"
     if is_linear(name):
         if policy == 6:
-            return "cuBLASLt base GEMM, then " + k
-        return ("linear_slot_kernel + lora_shrink (grouped_lora_kernel) + linear_lora_kernel (tcgen05 GEMM whose "
-                "accumulator also takes the delta as extra K blocks)")
+            return ("linear_slot_kernel + the split shrink (bgmv_shrink_*) + linear_lora_kernel (tcgen05 GEMM whose "
+                    "accumulator also takes the delta as extra K blocks)")
+        return ("cuBLASLt base GEMM, then lora_apply_slices (bgmv_fused_kernel for decode batches, the sgmv "
+                "and split kernels otherwise)")
     if name == "prefill_gate_up" and policy != 1:
         k = "sgmv_shrink_kernel + sgmv_expand_kernel (tcgen05, 128-row runs); short tiles: " + k
     return k + (" for w13 and w2" if is_moe(name) else "")
@@ -779,7 +780,8 @@ def main():
     ap.add_argument("--kernel-policy", type=int, default=0, choices=[0, 1, 2, 3, 4, 5, 6],
                     help="lora_set_kernel_policy: 0 automatic, 1 persistent split-K kernel, 2 cluster kernel "
                          "first, 3 no fused decode / MoE block kernel, 4 MoE per-pair blocks, 5 MoE block kernel "
-                         "over the metadata's tiles, 6 linear layer as cuBLASLt + second pass (tuning)")
+                         "over the metadata's tiles, 6 the linear layer as one tcgen05 GEMM with the delta in its "
+                         "accumulator (tuning)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

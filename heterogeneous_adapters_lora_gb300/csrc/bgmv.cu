@@ -1168,6 +1168,11 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
         }
     }
     lora_note_launch();
+    if (pr.shrink_only) {
+        if (pr.nc_out) *pr.nc_out = NC;
+        *launched = true;
+        return LORA_OK;
+    }
     cfg.blockDim = dim3(kThreads, 1, 1);
     // up to two waves: CTAs of a second wave start as first-wave CTAs finish
     // and find the counter exhausted or take the remaining items

@@ -639,8 +639,9 @@ extern "C" size_t lora_workspace_bytes(const lora_pool_t *pool, int32_t T, int32
         const Plan pl = make_plan(pool->num_sms, d.in_dim, d.n_slices, d.max_rank, T, d.max_loras);
         const size_t sp = lora_split_ws_bytes(d.n_slices, d.in_dim, d.max_rank, T, max_tiles(T, d.max_loras));
         const size_t pk = align256(pl.part_floats * 4);
-        // lora_linear_apply: v [n_slices][T][max_rank] fp32 and one slot per token
-        const size_t lin = align256((size_t)d.n_slices * T * d.max_rank * 4) + align256((size_t)T * 4);
+        // lora_linear_apply: the shrink's sums and a slot and a sorted position per token
+        const size_t lin = std::max(align256(sp), align256((size_t)d.n_slices * T * d.max_rank * 4)) +
+                           2 * align256((size_t)T * 4);
         size_t data = sgmv_region_bytes(pool, T) + (pk > sp ? pk : sp);
         if (lin > data) data = lin;
         return ws_total(data, pl.cnt_ints);
@@ -726,6 +727,47 @@ extern "C" lora_status_t lora_apply_slices(const lora_pool_t *pool, const lora_m
                                            const void *x, int64_t ldx, void *y, int64_t ldy,
                                            void *workspace, size_t ws_bytes, void *stream) {
     return lora_dense_apply(pool, meta, x, ldx, y, ldy, workspace, ws_bytes, 1.0f, (cudaStream_t)stream);
+}
+
+lora_status_t lora_dense_shrink(const lora_pool_t *pool, const lora_meta_t *meta, const void *x, int64_t ldx,
+                                void *workspace, size_t ws_bytes, size_t head_bytes, cudaStream_t s, float **part,
+                                int *nc, int *r8, int *sorted_rows) {
+    GArgs g;
+    lora_status_t st = dense_args(pool, meta, g);
+    if (st != LORA_OK) return st;
+    Carve cv;
+    if (!workspace || !lora_aligned16(workspace) || !carve(workspace, ws_bytes, cv) || head_bytes % 256)
+        return LORA_ERR_CAPACITY;
+    const int T = meta->T;
+    g.in = (const uint16_t *)x;
+    g.ld_in = ldx;
+    char *data = cv.data + head_bytes;
+    const size_t sp = align256(lora_split_ws_bytes(g.n_slices, g.in_dim, g.R, T, max_tiles(T, pool->desc.max_loras)));
+    if (g_lora_kernel_policy != 1 && head_bytes + sp <= cv.data_bytes) {
+        LoraProblem pr = to_problem(g, meta, pool->desc.max_loras);
+        int NC = 0;
+        pr.shrink_only = 1;
+        pr.nc_out = &NC;
+        bool launched = false;
+        st = lora_split_apply(pool, pr, data, sp, cv.ctrl + 2, s, &launched);
+        if (st != LORA_OK) return st;
+        if (launched) {
+            *part = (float *)data;
+            *nc = NC;
+            *r8 = lora_round8(g.R);
+            *sorted_rows = 1;
+            return LORA_OK;
+        }
+    }
+    // the atomic shrink: v [n_slices][T][max_rank] in token order
+    if (head_bytes + align256((size_t)g.n_slices * T * g.R * 4) > cv.data_bytes) return LORA_ERR_CAPACITY;
+    st = lora_shrink(pool, meta, x, ldx, (float *)data, s);
+    if (st != LORA_OK) return st;
+    *part = (float *)data;
+    *nc = 1;
+    *r8 = g.R;
+    *sorted_rows = 0;
+    return LORA_OK;
 }
 
 extern "C" lora_status_t lora_build_meta_apply(const lora_pool_t *pool, const int32_t *d_idx, int32_t T,

@@ -12,11 +12,12 @@
 //   Vhat[t][p*Rw + k] = scale[a_t] * v[t][k]   if a_t is slot p of group g, else 0
 //   Bhat[o][p*Rw + k] = B_j[slot p of group g][o][k]   (0 past the slot's rank)
 // so that Vhat . Bhat^T adds exactly the delta of the group's tokens.  The
-// delta blocks sit in the K-block sequence after every 8 base blocks (the
-// rest at the end), so that building them overlaps the base GEMM.
+// delta blocks are spread through the K-block sequence (see kb_kind), so
+// that building them overlaps the base GEMM.
 //
-// Kernels: linear_slot_kernel writes each token's slot from the batch
-// metadata; lora_shrink writes v (fp32, unscaled); linear_lora_kernel is a
+// Kernels: linear_slot_kernel writes each token's slot and sorted position
+// from the batch metadata; the split shrink (or, when it does not take the
+// pool, the atomic one) writes x A^T in fp32, unscaled; linear_lora_kernel is a
 // persistent tcgen05 GEMM over (128-token, BN-output) tiles with a TMA ring
 // for x and W, a second ring producer that writes the delta blocks, two
 // TMEM accumulators (the epilogue of one tile runs under the next tile's
@@ -30,9 +31,14 @@
 //              into the ring stage in the 128-byte swizzled layout
 // Every wait is a bounded poll that records LORA_ERR_TIMEOUT in the status word.
 //
-// Pools whose shape this kernel does not take (max_rank above 64, a slice
-// width that is not a multiple of 128), and kernel policy 6, run the base
-// GEMM as a cuBLASLt call and the delta as a second pass over y.
+// This kernel runs under kernel policy 6 for pools whose shape it takes
+// (max_rank <= 64, every slice width a multiple of 128).  Otherwise the base
+// GEMM is a cuBLASLt call and the delta a second pass over y (the
+// library's apply), which measured faster on GB300 for both the decode
+// (T=256, 4096 -> 6144) and the prefill (8K tokens, 4096 -> 28672) layers:
+// with one 128 x 128 or 128 x 256 tile per CTA this kernel is bound by the
+// latency of its operand stream (decode) and by L2 bandwidth (prefill), where
+// the library GEMM pairs two SMs on each tile.
 #include <cublasLt.h>
 #include <string.h>
 
@@ -58,9 +64,11 @@ struct LinArgs {
     int out_off[LORA_MAX_SLICES + 1];
     const uint16_t *B[LORA_MAX_SLICES];
     long long B_ss[LORA_MAX_SLICES];
-    int R, Rw, pg;                // v row length (max_rank); slot segment width; slots per delta block
-    const float *v;               // [n_slices][T][R] fp32, unscaled
+    int R, Rw, pg;                // max_rank; slot segment width; slots per delta block
+    const float *part;            // shrink sums [nc][n_slices][T][r8] fp32, unscaled
+    int nc, r8, sorted_rows;      // sorted_rows: row i of part is the metadata's sorted row i
     const int32_t *slot_of;       // [T], -1 for a token without an active adapter
+    const int32_t *pos_of;        // [T], sorted position of each token
     const int32_t *rank;
     const float *scale;
     const uint16_t *bias;         // [O] or null
@@ -72,16 +80,21 @@ struct LinArgs {
 };
 
 // Position kb of a tile's K-block sequence: a base block (>= 0) or delta
-// group -(g + 1).  The delta groups come after every 8 base blocks while
-// base blocks remain, then the rest at the end.
-__device__ __forceinline__ int kb_kind(int kb, int KB, int G) {
-    const int gm = min(G, KB / 8);
-    if (kb < 9 * gm) {
-        const int q = kb / 9, r = kb - 9 * q;
-        return r == 8 ? -(q + 1) : q * 8 + r;
+// group -(g + 1).  The first delta group comes after F = min(KB, 12) base
+// blocks (time for the delta warps to find the tile's slots), the next ones
+// after every sp more base blocks while base blocks remain, the rest at the end.
+__host__ __device__ __forceinline__ int kb_kind(int kb, int KB, int G) {
+    const int F = KB < 12 ? KB : 12;
+    if (kb < F) return kb;
+    const int sp = G > 0 && (KB - F) / G > 1 ? (KB - F) / G : 1;
+    const int gi = G < (KB - F) / sp ? G : (KB - F) / sp;  // interleaved groups
+    const int t = kb - F;
+    if (t < gi * (sp + 1)) {
+        const int q = t / (sp + 1), r = t - q * (sp + 1);
+        return r == 0 ? -(q + 1) : F + q * sp + (r - 1);
     }
-    const int rest = kb - 9 * gm, nb = KB - 8 * gm;
-    return rest < nb ? 8 * gm + rest : -(gm + (rest - nb) + 1);
+    const int rest = t - gi * (sp + 1), nb = KB - F - gi * sp;
+    return rest < nb ? F + gi * sp + rest : -(gi + (rest - nb) + 1);
 }
 
 __device__ __forceinline__ void lwait(uint64_t *bar, uint32_t parity, const LinArgs &p) {
@@ -105,12 +118,12 @@ __device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
     return *(const uint32_t *)&v;
 }
 
-// Each token's slot from the metadata: group g's sorted rows get group_key[g],
-// the inactive tail gets -1.
+// Each token's slot and sorted position from the metadata: group g's sorted
+// rows get group_key[g], the inactive tail gets -1.
 __global__ void __launch_bounds__(kSlotThreads) linear_slot_kernel(const int32_t *sorted, const int32_t *group_key,
                                                                    const int32_t *group_start,
                                                                    const int32_t *counters, int T, int max_groups,
-                                                                   int32_t *slot_of) {
+                                                                   int32_t *slot_of, int32_t *pos_of) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int n_active = counters[0], n_groups = counters[1];
     for (int g = blockIdx.x; g <= max_groups; g += gridDim.x) {
@@ -125,7 +138,11 @@ __global__ void __launch_bounds__(kSlotThreads) linear_slot_kernel(const int32_t
             i1 = T;
             val = -1;
         }
-        for (int i = i0 + (int)threadIdx.x; i < i1; i += kSlotThreads) slot_of[sorted[i]] = val;
+        for (int i = i0 + (int)threadIdx.x; i < i1; i += kSlotThreads) {
+            const int t = sorted[i];
+            slot_of[t] = val;
+            pos_of[t] = i;
+        }
     }
     asm volatile("griddepcontrol.launch_dependents;");
 }
@@ -137,13 +154,13 @@ __global__ void __launch_bounds__(kLThreads, 1) linear_lora_kernel(const __grid_
     // two rings: the base blocks (filled by TMA) and the delta blocks (written
     // by the delta warps), each with its own barriers, so that every producer
     // waits only for the consumption of its own previous fills
-    constexpr int SD = BN == 128 ? 2 : 1;
+    constexpr int SD = 1;
     constexpr int SB = kRingBytes / kStage - SD;
     extern __shared__ __align__(1024) char smem_raw[];
     __shared__ __align__(8) uint64_t fullb[SB], emptyb[SB], fulld[SD], emptyd[SD], accf[2], acce[2];
     __shared__ uint32_t s_tmem;
     __shared__ int s_skip[SD];
-    __shared__ int s_rowslot[kLM], s_uidx[kLM], s_uslot[kLM], s_wcnt[4];
+    __shared__ int s_rowslot[kLM], s_uidx[kLM], s_uslot[kLM], s_urs[kLM], s_wcnt[4];
     char *smem = smem_raw + ((1024u - (smem_u32_of(smem_raw) & 1023u)) & 1023u);
     char *dring = smem + (size_t)SB * kStage;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -328,15 +345,39 @@ __global__ void __launch_bounds__(kLThreads, 1) linear_lora_kernel(const __grid_
             for (int c = 0; c < 8; ++c) vq[c] = make_uint4(0u, 0u, 0u, 0u);
             if (a >= 0) {
                 const float sc = p.scale[a];
-                const float *vr = p.v + ((long long)j * p.T + row) * p.R;
+                const int srow = p.sorted_rows ? p.pos_of[row] : row;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     float e[8];
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) e[k] = c * 8 + k < p.R ? vr[c * 8 + k] * sc : 0.f;
+                    for (int k = 0; k < 8; ++k) e[k] = 0.f;
+                    if (c * 8 < p.R) {
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) {  // the hidden chunks' sums (at most 4), in chunk order
+                            if (h < p.nc) {
+                                const float *vr =
+                                    p.part + (((long long)h * p.n_slices + j) * p.T + srow) * p.r8 + c * 8;
+#pragma unroll
+                                for (int k = 0; k < 8; ++k)
+                                    if (c * 8 + k < p.R) e[k] += vr[k];
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) e[k] *= sc;
                     vq[c] = make_uint4(pack_bf2(e[0], e[1]), pack_bf2(e[2], e[3]), pack_bf2(e[4], e[5]),
                                        pack_bf2(e[6], e[7]));
                 }
+            }
+            // the tile's B rows of every distinct slot into L2, ahead of the delta blocks
+            if (f < nu) s_urs[f] = (p.rank[s_uslot[f]] + 7) & ~7;
+            fill_sync();
+            for (int uu = 0; uu < nu; ++uu) {
+                const int sl = s_uslot[uu];
+                const int rs = s_urs[uu];
+                const char *b0 = (const char *)(p.B[j] + (long long)sl * p.B_ss[j] + (long long)ob * rs);
+                const int lines = (BN * rs * 2 + 127) >> 7;
+                for (int l = f; l < lines; l += kLM) asm volatile("prefetch.global.L2 [%0];" ::"l"(b0 + l * 128));
             }
             for (int kb = 0; kb < NKB; ++kb) {
                 const int kind = kb_kind(kb, p.KB, p.G);
@@ -357,7 +398,7 @@ __global__ void __launch_bounds__(kLThreads, 1) linear_lora_kernel(const __grid_
                         const int uu = g * p.pg + pp;
                         if (uu < nu) {
                             const int sl = s_uslot[uu];
-                            const int rs = (p.rank[sl] + 7) & ~7;
+                            const int rs = s_urs[uu];
                             if (kc * 8 < rs) {
                                 const uint16_t *bs = p.B[j] + (long long)sl * p.B_ss[j] + kc * 8;
 #pragma unroll
@@ -519,14 +560,11 @@ extern "C" lora_status_t lora_linear_apply(const lora_pool_t *pool, const lora_m
     cudaStream_t s = (cudaStream_t)stream;
     const int T = meta->T, R = d.max_rank, ns = d.n_slices;
     const int BN = fused_bn(pool, T, pool->num_sms);
-    char *data = nullptr;
-    size_t data_bytes = 0;
-    const size_t v_bytes = align256((size_t)ns * T * R * 4), slot_bytes = align256((size_t)T * 4);
-    const bool ws_ok = lora_ws_data(workspace, ws_bytes, &data, &data_bytes) && v_bytes + slot_bytes <= data_bytes;
+    const size_t slot_bytes = align256((size_t)T * 4);
     LinArgs a;
     memset(&a, 0, sizeof(a));
     bool maps = false;
-    if (BN && ws_ok && g_lora_kernel_policy != 6) {
+    if (BN && g_lora_kernel_policy == 6) {
         maps = lora_make_tmap_2d(&a.tm_x, x, d.in_dim, T, ldx, kLBK, kLM, true) &&
                lora_make_tmap_2d(&a.tm_w, W, d.in_dim, O, ldw, kLBK, BN, true);
     }
@@ -543,16 +581,24 @@ extern "C" lora_status_t lora_linear_apply(const lora_pool_t *pool, const lora_m
                                            kRingBytes + 1024));
         g_lin_configured[dev].store(1, std::memory_order_release);
     }
-    float *v = (float *)data;
-    int32_t *slot_of = (int32_t *)(data + v_bytes);
-    // each token's slot, then v = x A^T (fp32, unscaled)
+    // each token's slot and sorted position at the head of the workspace's
+    // scratch, then x A^T (fp32, unscaled) past them
+    char *head = nullptr;
+    size_t data_bytes = 0;
+    if (!lora_ws_data(workspace, ws_bytes, &head, &data_bytes) || 2 * slot_bytes > data_bytes)
+        return LORA_ERR_CAPACITY;
+    int32_t *slot_of = (int32_t *)head;
+    int32_t *pos_of = (int32_t *)(head + slot_bytes);
     int sgrid = d.max_loras + 1;
     if (sgrid > 1024) sgrid = 1024;
     linear_slot_kernel<<<sgrid, kSlotThreads, 0, s>>>(meta->sorted, meta->group_key, meta->group_start,
-                                                      meta->counters, T, d.max_loras, slot_of);
+                                                      meta->counters, T, d.max_loras, slot_of, pos_of);
     LORA_CUDA_TRY(cudaGetLastError());
     lora_note_launch();
-    lora_status_t st = lora_shrink(pool, meta, x, ldx, v, stream);
+    float *part = nullptr;
+    int nc = 0, r8 = 0, sorted_rows = 0;
+    lora_status_t st = lora_dense_shrink(pool, meta, x, ldx, workspace, ws_bytes, 2 * slot_bytes, s, &part, &nc,
+                                         &r8, &sorted_rows);
     if (st != LORA_OK) return st;
 
     a.T = T;
@@ -574,8 +620,12 @@ extern "C" lora_status_t lora_linear_apply(const lora_pool_t *pool, const lora_m
         a.B_ss[j] = pool->b_slot_elems[j];
     }
     a.out_off[ns] = off;
-    a.v = v;
+    a.part = part;
+    a.nc = nc;
+    a.r8 = r8;
+    a.sorted_rows = sorted_rows;
     a.slot_of = slot_of;
+    a.pos_of = pos_of;
     a.rank = pool->d_rank;
     a.scale = pool->d_scale;
     a.bias = (const uint16_t *)bias;

@@ -119,6 +119,8 @@ struct LoraProblem {
     int *status;
     int spin_limit;
     float post_scale;
+    int shrink_only;                        // split path: launch the shrink alone
+    int *nc_out;                            // ... and report its hidden chunk count here
 };
 
 // Cluster kernel (cluster.cu): launches and sets *launched when the shape
@@ -195,3 +197,13 @@ lora_status_t lora_moe_tile_launch(const lora_pool_t *pool, const lora_meta_t *m
 // The scratch part of an apply workspace (past its control words); false
 // if the workspace is null, misaligned or too small to carve.
 bool lora_ws_data(void *workspace, size_t ws_bytes, char **data, size_t *data_bytes);
+
+// The shrink of a dense layer alone, for lora_linear_apply: unscaled fp32
+// sums of x A^T over hidden chunks, part[nc][n_slices][T][r8], in the
+// workspace's scratch past its first head_bytes (a multiple of 256).  With
+// *sorted_rows = 1 (the split shrink), row i of a slice is the metadata's
+// sorted row i; otherwise (the atomic shrink, nc = 1, r8 = max_rank) row t
+// is token t.
+lora_status_t lora_dense_shrink(const lora_pool_t *pool, const lora_meta_t *meta, const void *x, int64_t ldx,
+                                void *workspace, size_t ws_bytes, size_t head_bytes, cudaStream_t s, float **part,
+                                int *nc, int *r8, int *sorted_rows);

@@ -392,14 +392,15 @@ LORA_API void lora_set_spin_limit(int32_t max_polls);
  * W is the base weight [out_total][ldw] bf16 row-major (the packed slices'
  * weights stacked in slice order), bias [out_total] bf16 or NULL, y is fully
  * written for the meta's T tokens (meta from a dense lora_build_meta).
- * When max_rank <= 64 and every slice width is a multiple of 128, the delta
- * is accumulated inside a tensor-core GEMM (tcgen05): the shrink writes
- * v = x A^T into the workspace, and the expand runs as extra K blocks of the
- * base GEMM's accumulator (Vhat . Bhat^T over the distinct adapters of each
- * 128-token tile, v rounded to bf16), so y is written once; the workspace
- * must then hold lora_workspace_bytes(pool, T, 1) bytes.  Otherwise (and
- * under lora_set_kernel_policy(6)) the base GEMM is a cuBLASLt call and the
- * delta a second pass over y.  Errors: as lora_apply_slices, plus
+ * By default the base GEMM is a cuBLASLt call and the delta a second pass
+ * over y (lora_apply_slices).  Under lora_set_kernel_policy(6), when
+ * max_rank <= 64 and every slice width is a multiple of 128, the delta is
+ * accumulated inside a tensor-core GEMM of this library (tcgen05) instead:
+ * the shrink writes x A^T into the workspace, and the expand runs as extra K
+ * blocks of the base GEMM's accumulator (Vhat . Bhat^T over the distinct
+ * adapters of each 128-token tile, v rounded to bf16), so y is written once.
+ * The workspace holds lora_workspace_bytes(pool, T, 1) bytes either way.
+ * Errors: as lora_apply_slices, plus
  * LORA_ERR_INVALID_ARG for a null or misaligned x/W/y (16 bytes), leading
  * dimensions not multiples of 8 or too small, or a meta not built for this
  * dense pool, LORA_ERR_UNSUPPORTED for a MoE pool or when cuBLASLt offers no
@@ -444,8 +445,8 @@ LORA_API lora_status_t lora_sink_experts_act(const void *gate_up, int64_t ld_gat
  * 5 = like 0, with the kernel of lora_moe_apply_blocks run over the
  *     metadata's 16-row tiles (one thread-block cluster per tile) for every
  *     MoE batch it supports,
- * 6 = like 0, with lora_linear_apply as a cuBLASLt base GEMM followed by
- *     lora_apply_slices (the delta as a second pass over y).
+ * 6 = like 0, with lora_linear_apply as this library's tcgen05 GEMM that
+ *     takes the delta into its accumulator (see lora_linear_apply).
  * For tests and tuning. */
 LORA_API void lora_set_kernel_policy(int32_t policy);
 

@@ -15,6 +15,15 @@ from gpu_util import active_mask, assert_delta
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(autouse=True, params=[0, 6], ids=["library_gemm", "tcgen05_fused"])
+def linear_path(request):
+    """Kernel policy 0: cuBLASLt base GEMM + the library's apply; policy 6:
+    the tcgen05 GEMM whose accumulator takes the delta."""
+    L.lora_set_kernel_policy(request.param)
+    yield request.param
+    L.lora_set_kernel_policy(0)
+
+
 def _run(c, with_bias, bias_std=0.5, ldx=None, ldy=None):
     """Run the full linear layer; returns (y as float64 [T][out_total], base of
     the oracle (x W^T + bias, float64), delta of the oracle, active rows)."""

@@ -3,10 +3,11 @@
 It serves callers that cannot hand the library a workspace (all device
 memory already reserved by another allocator so cudaMalloc would fail,
 latency-critical paths that may not block on an allocation, C hosts without
-an allocator), by running the fused kernel on a fixed scratch array inside
-the library's device image.  Its result must
-match lora_apply_slices within the tolerance of the other parity tests, on
-two calls in a row (the array keeps the previous call's contents).  This
+an allocator), by running the persistent split-K kernel on a fixed scratch
+array inside the library's device image.  Its result must match the oracle
+(twice the delta after two calls in a row on a zero base: the array keeps
+the previous call's contents) and lora_apply_slices, within the tolerance
+of the other parity tests.  This
 file is collected last so a run that stops at the first failure has already
 run every other test; it passes alone in a fresh process too.
 """
@@ -15,6 +16,7 @@ import pytest
 
 torch = pytest.importorskip("torch")
 
+import oracle
 from heterogeneous_adapters_lora_gb300 import harness as H
 from heterogeneous_adapters_lora_gb300 import inputs as gen
 from heterogeneous_adapters_lora_gb300 import lora as L
@@ -57,6 +59,8 @@ def test_static_scratch_matches_workspace_entry_point(which):
     d_ws = bf16_bits_to_f32(y_ws)[act] - base
     d_st = bf16_bits_to_f32(y_st)[act] - base
     assert_delta(d_st, d_ws, f"static vs workspace ({which})")
+    _, d_ref = oracle.dense_delta(c)
+    assert_delta(d_st, 2 * d_ref[act].astype(np.float64), f"static vs oracle ({which})")
 
 
 def test_static_scratch_rejects_batches_beyond_its_size():

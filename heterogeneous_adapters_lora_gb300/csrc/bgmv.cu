@@ -617,8 +617,9 @@ __global__ void __launch_bounds__(kThreads, PW == 8 ? 3 : (KS >= 3 ? 4 : 5))
     bgmv_expand_kernel(const __grid_constant__ EArgs p) {
     extern __shared__ __align__(128) char smem[];
     __shared__ __align__(8) uint64_t bbar, ybar;
-    __shared__ int s_rows[kTileRows];
+    __shared__ int s_rows[2][kTileRows];  // this item's rows and the next one's
     __shared__ float s_w[kTileRows];
+    __shared__ int s_next, s_ninfo[3];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, c4 = lane & 3;
     const int ns = p.n_slices;
@@ -639,21 +640,30 @@ __global__ void __launch_bounds__(kThreads, PW == 8 ? 3 : (KS >= 3 ? 4 : 5))
     const int nc = p.NC;
     uint32_t phase = 0;
 
-    // more items than CTAs: take them from the counter; else one item per CTA
+    // more items than CTAs: take them from the counter; else one item per CTA.
+    // The next item's ticket, tile words, rank and rows are fetched while this
+    // item converts its partials, runs its MMAs and stores its rows, so an
+    // item starts with its bulk copies instead of a chain of dependent loads.
     const bool dyn = total > (int)gridDim.x;
-    for (int item = dyn ? take_item(p.ticket, &s_item) : (int)blockIdx.x; item < total;
-         item = dyn ? take_item(p.ticket, &s_item) : total, phase ^= 1u) {
+    int item = dyn ? take_item(p.ticket, &s_item) : (int)blockIdx.x;
+    int row0 = 0, keyn = 0, r = 0, buf = 0;
+    if (item < total) {
+        const int tile = item / p.n_oc;
+        row0 = p.tile_row0[tile];
+        keyn = p.tile_keyn[tile];
+        r = p.rank[(keyn >> 5) / p.E];
+        if (tid < (keyn & 31)) s_rows[0][tid] = p.sorted[row0 + tid];
+    }
+    __syncthreads();
+    for (; item < total; phase ^= 1u, buf ^= 1) {
         const int tile = item / p.n_oc, oc = item - tile * p.n_oc;
-        const int row0 = p.tile_row0[tile];
-        const int keyn = p.tile_keyn[tile];
         const int n = keyn & 31, key = keyn >> 5;
         const int a = key / p.E, e = key - a * p.E;
-        const int r = p.rank[a];
         const int rs = (r + 7) & ~7;
         const int ob = oc * p.oc_w, oe = min(p.out_total, ob + p.oc_w);
-        __syncthreads();  // the previous item's stores have been issued and its buffers read
-        if (tid < n) s_rows[tid] = p.sorted[row0 + tid];
-        __syncthreads();
+        const int *rows = s_rows[buf];
+        int nxt_t = total;
+        if (dyn && tid == 0) nxt_t = atomicAdd(p.ticket, 1);  // lands while this item runs
         // weights and outputs do not depend on the shrink: fetch them first
         if (warp == 0) {
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -661,7 +671,7 @@ __global__ void __launch_bounds__(kThreads, PW == 8 ? 3 : (KS >= 3 ? 4 : 5))
             if (lane == 0) mbar_expect_tx(&ybar, rowb * (uint32_t)n);
             __syncwarp();
             if (lane < n)
-                bulk_g2s(ys + lane * p.ys_stride, p.out + (long long)s_rows[lane] * p.ld_out + ob, rowb, &ybar);
+                bulk_g2s(ys + lane * p.ys_stride, p.out + (long long)rows[lane] * p.ld_out + ob, rowb, &ybar);
         } else if (warp == 1) {
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             if (lane == 0) mbar_expect_tx(&bbar, (uint32_t)(oe - ob) * rs * 2);
@@ -680,7 +690,7 @@ __global__ void __launch_bounds__(kThreads, PW == 8 ? 3 : (KS >= 3 ? 4 : 5))
             }
         }
         if (tid < kTileRows)
-            s_w[tid] = tid < n ? p.scale[a] * p.post_scale * (p.row_w ? p.row_w[s_rows[tid]] : 1.f) : 0.f;
+            s_w[tid] = tid < n ? p.scale[a] * p.post_scale * (p.row_w ? p.row_w[rows[tid]] : 1.f) : 0.f;
         if (!waited) {
             asm volatile("griddepcontrol.wait;" ::: "memory");  // the shrink's partials are complete
             waited = true;
@@ -723,7 +733,16 @@ __global__ void __launch_bounds__(kThreads, PW == 8 ? 3 : (KS >= 3 ? 4 : 5))
                 *(uint2 *)(vl + tq * p.vr_stride + jj * p.R8 + k) = lv;
             }
         }
+        if (tid == 0) s_next = nxt_t;
         __syncthreads();
+        // the next item's tile words, in flight during the MMAs
+        const int nitem = s_next;
+        int nrow0 = 0, nkeyn = 0;
+        if (nitem < total && tid < kTileRows) {
+            const int nt = nitem / p.n_oc;
+            nrow0 = p.tile_row0[nt];
+            nkeyn = p.tile_keyn[nt];
+        }
         mbar_wait(&bbar, phase, p.spin_limit, p.status);
         mbar_wait(&ybar, phase, p.spin_limit, p.status);
 
@@ -838,17 +857,38 @@ __global__ void __launch_bounds__(kThreads, PW == 8 ? 3 : (KS >= 3 ? 4 : 5))
                 }
             }
         }
+        // the next item's rows and rank, in flight during the stores
+        int nrank = 0, nrow = 0;
+        if (nitem < total && tid < kTileRows) {
+            nrank = p.rank[(nkeyn >> 5) / p.E];
+            if (tid < (nkeyn & 31)) nrow = p.sorted[nrow0 + tid];
+        }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncthreads();
         if (warp == 0 && lane < n) {
             asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
-                             p.out + (long long)s_rows[lane] * p.ld_out + ob),
+                             p.out + (long long)rows[lane] * p.ld_out + ob),
                          "r"(smem_u32(ys + lane * p.ys_stride)), "r"((uint32_t)(oe - ob) * 2)
                          : "memory");
             asm volatile("cp.async.bulk.commit_group;" ::: "memory");
             // the rows may be reused once the copy has read them; the writes
             // are complete when the grid is
             asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        }
+        if (nitem < total && tid < kTileRows) {
+            if (tid < (nkeyn & 31)) s_rows[buf ^ 1][tid] = nrow;
+            if (tid == 0) {
+                s_ninfo[0] = nrow0;
+                s_ninfo[1] = nkeyn;
+                s_ninfo[2] = nrank;
+            }
+        }
+        __syncthreads();  // this item's buffers are read and the next item's words are in place
+        item = nitem;
+        if (item < total) {
+            row0 = s_ninfo[0];
+            keyn = s_ninfo[1];
+            r = s_ninfo[2];
         }
     }
     if (dyn) finish_items(p.ticket);

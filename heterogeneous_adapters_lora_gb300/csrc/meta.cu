@@ -323,6 +323,365 @@ __global__ void __launch_bounds__(kSmallRows, 1) build_meta_small_kernel(MetaArg
     dense_meta_block(a, sm, 1);
 }
 
+// ---------------------------------------------------------------- cluster build
+//
+// The same metadata from one thread-block cluster of kMetaCL CTAs, for batches
+// of thousands of rows (one CTA's issue rate bounds the single-CTA build
+// there).  CTA c takes rows [c*rows/CL, (c+1)*rows/CL) and owns keys
+// [c*NK1/CL, (c+1)*NK1/CL):
+//   1. its rows' keys and per-warp histograms (as the single-CTA build), then
+//      per key the prefix over its warps and its total tot_c[key]
+//   2. cluster barrier; each owner reads tot_c'[key] (and, dense, the run
+//      starts and first rows) of every CTA through distributed shared memory,
+//      and scans the key-space sums (row offsets, groups, tiles, long and
+//      short tiles) over its keys
+//   3. cluster barrier; each owner adds the totals of the owners before it,
+//      writes its keys' outputs and, into every CTA c', base_c'[key] = row
+//      offset of the key + the rows of the key in CTAs before c'
+//   4. cluster barrier; each CTA scatters its rows: base + earlier warps +
+//      earlier lanes
+// The order is the single-CTA build's: keys ascending, rows in original order
+// within a key, inactive rows last.
+constexpr int kMetaCL = 8;
+constexpr long long kMetaClusterRows = 2048;  // batches of at least this many rows take the cluster build
+
+__device__ __forceinline__ uint32_t meta_cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void meta_cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t meta_peer_addr(const void *p, uint32_t rank) {
+    uint32_t ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"((uint32_t)__cvta_generic_to_shared(p)), "r"(rank));
+    return ra;
+}
+// Volatile (kept after the cluster barrier) but without a memory clobber, so
+// that the loads of all peers are issued back to back.
+__device__ __forceinline__ int meta_ld_peer(const int *p, uint32_t rank) {
+    int v;
+    asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(meta_peer_addr(p, rank)));
+    return v;
+}
+__device__ __forceinline__ void meta_st_peer(int *p, uint32_t rank, int v) {
+    asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(meta_peer_addr(p, rank)), "r"(v) : "memory");
+}
+
+// Shared-memory ints of one CTA of the cluster build.
+static inline long long meta_cluster_ints(int W, int NK1, int L, int rows_cta) {
+    const int own = (NK1 + kMetaCL - 1) / kMetaCL;
+    return (long long)(W + 4) * NK1 + (8LL + kMetaCL) * own + 200 + (L + 3) / 4 + rows_cta;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) build_meta_cluster_kernel(MetaArgs a) {
+    extern __shared__ int sm[];
+    const int NK = a.n_keys, NK1 = NK + 1, W = a.n_chunks;
+    const int CL = kMetaCL;
+    const uint32_t c = meta_cluster_rank();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nthreads = blockDim.x;
+    const int rows = a.T * a.K;
+    const int R0 = (int)((long long)rows * c / CL), R1 = (int)((long long)rows * (c + 1) / CL);
+    const int K0 = (int)((long long)NK1 * c / CL), K1 = (int)((long long)NK1 * (c + 1) / CL);
+    const int OWN = (NK1 + CL - 1) / CL;
+    int *hist = sm;                   // [W][NK1] per-warp counts -> prefix over this CTA's warps
+    int *tot = hist + W * NK1;        // [NK1] rows of each key in this CTA
+    int *base = tot + NK1;            // [NK1] sorted position of this CTA's first row of each key
+    int *tmn = base + NK1;            // [NK1] dense: first row of a run of each key in this CTA
+    int *nrn = tmn + NK1;             // [NK1] dense: run starts of each key in this CTA
+    int *o_cnt = nrn + NK1;           // [OWN] owned keys: rows
+    int *o_nrun = o_cnt + OWN;        //       run starts (dense)
+    int *o_tmin = o_nrun + OWN;       //       first row (dense)
+    int *o_off = o_tmin + OWN;        //       row offset
+    int *o_g = o_off + OWN;           //       group
+    int *o_t = o_g + OWN;             //       first 16-row tile
+    int *o_lt = o_t + OWN;            //       first long tile (-1: not a long run)
+    int *o_st = o_lt + OWN;           //       first short tile (-1: a long run)
+    int *o_vt = o_st + OWN;           // [OWN][CL] owned keys: rows in each CTA
+    int *misc = o_vt + kMetaCL * OWN; // [200]: this owner's 5 totals at [0..4], the earlier owners' at [8..12], n_bad at [36], warp totals at [40..199]
+    unsigned char *act = (unsigned char *)(misc + 200);
+    int *kc = misc + 200 + (a.L + 3) / 4;  // [R1 - R0] keys of this CTA's rows
+    asm volatile("griddepcontrol.launch_dependents;");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    // this warp's contiguous rows within the CTA's range
+    const int crow = R1 - R0;
+    const int chunk = (crow + W - 1) / W;
+    const int r0 = R0 + warp * chunk, r1 = min(R1, r0 + chunk);
+    int sv[8], ev[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const int row = r0 + u * 32 + lane;
+        const bool ok = warp < W && row < r1;
+        sv[u] = ok ? a.idx[row / a.K] : -1;
+        ev[u] = (ok && a.topk) ? a.topk[row] : 0;
+    }
+    const int s_prev = (a.K == 1 && warp < W && r0 > 0 && r0 < r1) ? a.idx[r0 - 1] : -1;
+    for (int i = tid; i < a.L; i += nthreads) {
+        const int en = a.enabled[i], rk = a.rank[i];
+        act[i] = (en != 0 && rk > 0) ? 1 : 0;
+    }
+    for (int i = tid; i < W * NK1; i += nthreads) hist[i] = 0;
+    for (int i = tid; i < NK1; i += nthreads) {
+        tmn[i] = 0x7fffffff;
+        nrn[i] = 0;
+    }
+    if (tid == 0) misc[36] = 0;
+    __syncthreads();
+
+    // 1. keys, per-warp counts, dense run starts
+    int bad = 0;
+    int carry = -2;
+    if (a.K == 1 && warp < W && r0 > 0 && r0 < r1) {
+        int dummy = 0;
+        carry = row_key_e(a, act, r0 - 1, s_prev, 0, &dummy);
+    }
+    auto count_step = [&](int base_row, int s, int e) {
+        const int row = base_row + lane;
+        const bool v = row < r1;
+        const int key = v ? row_key_e(a, act, row, s, e, &bad) : -1;
+        if (v) kc[row - R0] = key;
+        if (a.K == 1) {
+            const unsigned peers = key_peers(key, a.key_bits);
+            const int leader = __ffs(peers) - 1;
+            if (v && lane == leader) hist[warp * NK1 + key] += __popc(peers);
+            int prev = __shfl_up_sync(0xffffffffu, key, 1);
+            if (lane == 0) prev = carry;
+            if (v && key < NK && key != prev) {
+                atomicAdd(&nrn[key], 1);
+                atomicMin(&tmn[key], row);
+            }
+            carry = __shfl_sync(0xffffffffu, key, 31);
+        } else if (v) {
+            atomicAdd(&hist[warp * NK1 + key], 1);
+        }
+        __syncwarp();
+    };
+    if (warp < W) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            if (r0 + u * 32 < r1) count_step(r0 + u * 32, sv[u], ev[u]);
+        for (int b = r0 + 256; b < r1; b += 32) {
+            const int row = b + lane;
+            const bool v = row < r1;
+            count_step(b, v ? a.idx[row / a.K] : -1, (v && a.topk) ? a.topk[row] : 0);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) bad += __shfl_xor_sync(0xffffffffu, bad, o);
+    if (lane == 0 && bad) atomicAdd(&misc[36], bad);
+    __syncthreads();
+    // per key: prefix over this CTA's warps (in place) and the CTA's total
+    for (int b = tid; b < NK1; b += nthreads) {
+        int run_rows = 0;
+        for (int w = 0; w < W; ++w) {
+            const int cw = hist[w * NK1 + b];
+            hist[w * NK1 + b] = run_rows;
+            run_rows += cw;
+        }
+        tot[b] = run_rows;
+    }
+    meta_cluster_sync();  // B1: every CTA's tot, tmn, nrn, n_bad
+
+    // 2. owned keys: totals over the CTAs, then the key-space sums over them
+    const int NO = K1 - K0;
+    const int per = (NO + nthreads - 1) / nthreads;
+    const int b0 = K0 + min(NO, tid * per), b1 = K0 + min(NO, tid * per + per);
+    int *wt = misc + 40;  // [5][32] per-warp totals
+    int sv5[5] = {0, 0, 0, 0, 0};
+    for (int b = b0; b < b1; ++b) {
+        // every CTA's words of key b: all loads issued before any is used
+        int vt[kMetaCL], vn[kMetaCL], vm[kMetaCL];
+#pragma unroll
+        for (int q = 0; q < kMetaCL; ++q) vt[q] = meta_ld_peer(tot + b, (uint32_t)q);
+        if (a.K == 1) {
+#pragma unroll
+            for (int q = 0; q < kMetaCL; ++q) {
+                vn[q] = meta_ld_peer(nrn + b, (uint32_t)q);
+                vm[q] = meta_ld_peer(tmn + b, (uint32_t)q);
+            }
+        }
+        int cnt = 0, nr = 0, tm = 0x7fffffff;
+#pragma unroll
+        for (int q = 0; q < kMetaCL; ++q) {
+            o_vt[(b - K0) * kMetaCL + q] = vt[q];
+            cnt += vt[q];
+            if (a.K == 1) {
+                nr += vn[q];
+                tm = min(tm, vm[q]);
+            }
+        }
+        o_cnt[b - K0] = cnt;
+        o_nrun[b - K0] = nr;
+        o_tmin[b - K0] = tm;
+        const int cc = b < NK ? cnt : 0;
+        const bool run = cc > 0 && a.K == 1 && cc >= LORA_LONG_MIN && nr == 1;
+        sv5[0] += cnt;
+        sv5[1] += cc > 0 ? 1 : 0;
+        sv5[2] += (cc + LORA_TILE_ROWS - 1) / LORA_TILE_ROWS;
+        sv5[3] += run ? (cc + LORA_LTILE_ROWS - 1) / LORA_LTILE_ROWS : 0;
+        sv5[4] += (cc > 0 && !run) ? (cc + LORA_TILE_ROWS - 1) / LORA_TILE_ROWS : 0;
+    }
+    int inc[5];
+#pragma unroll
+    for (int q = 0; q < 5; ++q) inc[q] = sv5[q];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+        for (int q = 0; q < 5; ++q) {
+            const int v = __shfl_up_sync(0xffffffffu, inc[q], o);
+            if (lane >= o) inc[q] += v;
+        }
+    }
+    if (lane == 31) {
+#pragma unroll
+        for (int q = 0; q < 5; ++q) wt[q * 32 + warp] = inc[q];
+    }
+    __syncthreads();
+    const int nw = nthreads / 32;
+    int ex[5];
+#pragma unroll
+    for (int q = 0; q < 5; ++q) {
+        int before = lane < warp ? wt[q * 32 + lane] : 0;
+        int all = lane < nw ? wt[q * 32 + lane] : 0;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            before += __shfl_xor_sync(0xffffffffu, before, o);
+            all += __shfl_xor_sync(0xffffffffu, all, o);
+        }
+        ex[q] = before + inc[q] - sv5[q];
+        if (tid == 0) misc[q] = all;  // this owner's totals
+    }
+    meta_cluster_sync();  // B2: every owner's totals
+
+    // 3. the owners before this one (lane q of warp 0 reads owner q's five
+    // totals, summed over the lanes), then this owner's keys' outputs and the
+    // sorted position of every CTA's first row of each key
+    if (warp == 0) {
+        int pre[5];
+#pragma unroll
+        for (int k = 0; k < 5; ++k) pre[k] = lane < (int)c ? meta_ld_peer(misc + k, (uint32_t)lane) : 0;
+#pragma unroll
+        for (int k = 0; k < 5; ++k) {
+#pragma unroll
+            for (int o = 16; o; o >>= 1) pre[k] += __shfl_xor_sync(0xffffffffu, pre[k], o);
+        }
+        if (lane == 0) {
+#pragma unroll
+            for (int k = 0; k < 5; ++k) misc[8 + k] = pre[k];
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < 5; ++k) ex[k] += misc[8 + k];
+    for (int b = b0; b < b1; ++b) {
+        const int cnt = o_cnt[b - K0];
+        const int cc = b < NK ? cnt : 0;
+        const bool run = cc > 0 && a.K == 1 && cc >= LORA_LONG_MIN && o_nrun[b - K0] == 1;
+        const int off = ex[0];
+        if (b < NK) a.m.key_count[b] = cnt;
+        a.m.key_offset[b] = off;
+        if (b < NK) {
+            if (cc > 0) {
+                a.m.key_group[b] = ex[1];
+                a.m.group_key[ex[1]] = b;
+                a.m.group_start[ex[1]] = off;
+            } else {
+                a.m.key_group[b] = -1;
+            }
+        }
+        o_off[b - K0] = off;
+        o_g[b - K0] = ex[1];
+        o_t[b - K0] = ex[2];
+        o_lt[b - K0] = run ? ex[3] : -1;
+        o_st[b - K0] = run ? -1 : ex[4];
+        int run_pos = off;
+#pragma unroll
+        for (int q = 0; q < kMetaCL; ++q) {
+            meta_st_peer(base + b, (uint32_t)q, run_pos);
+            run_pos += o_vt[(b - K0) * kMetaCL + q];
+        }
+        ex[0] += cnt;
+        ex[1] += cc > 0 ? 1 : 0;
+        ex[2] += (cc + LORA_TILE_ROWS - 1) / LORA_TILE_ROWS;
+        ex[3] += run ? (cc + LORA_LTILE_ROWS - 1) / LORA_LTILE_ROWS : 0;
+        ex[4] += (cc > 0 && !run) ? (cc + LORA_TILE_ROWS - 1) / LORA_TILE_ROWS : 0;
+    }
+    __syncthreads();
+    // the owned keys' tiles: a warp per key, its lanes over the key's tiles
+    for (int k = warp; k < NO; k += nw) {
+        const int b = K0 + k;
+        const int cc = b < NK ? o_cnt[k] : 0;
+        if (cc == 0) continue;
+        const int g = o_g[b - K0], off = o_off[b - K0];
+        const int nt = (cc + LORA_TILE_ROWS - 1) / LORA_TILE_ROWS;
+        for (int i = lane; i < nt; i += 32) {
+            const int rows_i = min(LORA_TILE_ROWS, cc - i * LORA_TILE_ROWS);
+            a.m.tile_group[o_t[b - K0] + i] = g;
+            a.m.tile_row0[o_t[b - K0] + i] = off + i * LORA_TILE_ROWS;
+            a.m.tile_keyn[o_t[b - K0] + i] = (b << 5) | rows_i;
+            if (o_st[b - K0] >= 0) {
+                a.m.stile_row0[o_st[b - K0] + i] = off + i * LORA_TILE_ROWS;
+                a.m.stile_keyn[o_st[b - K0] + i] = (b << 5) | rows_i;
+            }
+        }
+        if (o_lt[b - K0] >= 0) {
+            const int nl = (cc + LORA_LTILE_ROWS - 1) / LORA_LTILE_ROWS;
+            for (int i = lane; i < nl; i += 32) {
+                const int rows_i = min(LORA_LTILE_ROWS, cc - i * LORA_LTILE_ROWS);
+                a.m.ltile_row0[o_lt[b - K0] + i] = off + i * LORA_LTILE_ROWS;
+                a.m.ltile_keyn[o_lt[b - K0] + i] = (b << 8) | rows_i;
+                a.m.ltile_tok0[o_lt[b - K0] + i] = o_tmin[b - K0] + i * LORA_LTILE_ROWS;
+            }
+        }
+    }
+    if ((int)c == CL - 1 && tid == 0) {
+        // key NK (the inactive rows) is this owner's last key: its offset is
+        // the number of active rows
+        int G = 0, NT = 0, NL = 0, NS = 0, n_bad = 0;
+#pragma unroll
+        for (int q = 0; q < kMetaCL; ++q) {
+            G += meta_ld_peer(misc + 1, (uint32_t)q);
+            NT += meta_ld_peer(misc + 2, (uint32_t)q);
+            NL += meta_ld_peer(misc + 3, (uint32_t)q);
+            NS += meta_ld_peer(misc + 4, (uint32_t)q);
+            n_bad += meta_ld_peer(misc + 36, (uint32_t)q);
+        }
+        const int n_active = rows - o_cnt[NK - K0];
+        a.m.group_start[G] = n_active;
+        a.m.counters[0] = n_active;
+        a.m.counters[1] = G;
+        a.m.counters[2] = n_bad;
+        a.m.counters[3] = NT;
+        a.m.counters[4] = NS;
+        a.m.counters[5] = NL;
+        if (n_bad) atomicExch(a.status, (int)LORA_ERR_DEVICE_INDEX);
+    }
+    meta_cluster_sync();  // B3: every base written; no shared-memory access across CTAs after this
+
+    // 4. stable scatter: base + rows of earlier warps + earlier lanes
+    if (warp < W) {
+        const unsigned lt = (1u << lane) - 1u;
+        for (int b = r0; b < r1; b += 32) {
+            const int row = b + lane;
+            const bool v = row < r1;
+            const int key = v ? kc[row - R0] : -1;
+            const unsigned peers = key_peers(key, a.key_bits);
+            int pos = 0;
+            if (v) pos = base[key] + hist[warp * NK1 + key] + __popc(peers & lt);
+            __syncwarp();
+            if (v) {
+                a.m.sorted[pos] = row;
+                if (lane == __ffs(peers) - 1) hist[warp * NK1 + key] += __popc(peers);
+            }
+            __syncwarp();
+        }
+    }
+}
+
 }  // namespace
 
 lora_status_t lora_launch_build_meta(const lora_pool_t *pool, const int32_t *d_idx, int32_t T,
@@ -380,6 +739,65 @@ lora_status_t lora_launch_build_meta(const lora_pool_t *pool, const int32_t *d_i
         meta->n_keys = n_keys;
         meta->mode = 0;
         return LORA_OK;
+    }
+    if (rows >= kMetaClusterRows) {
+        // thousands of rows: the cluster build (8 CTAs)
+        const int rows_cta = (int)((rows + kMetaCL - 1) / kMetaCL);
+        int nt = (rows_cta + 31) / 32 * 32;
+        if (nt < 128) nt = 128;
+        if (nt > kThreads) nt = kThreads;
+        const long long rest = meta_cluster_ints(0, NK1, L, rows_cta);
+        int Wc = (int)((kSmemBudgetInts - rest) / NK1);
+        if (Wc > nt / 32) Wc = nt / 32;
+        if (Wc >= 1) {
+            MetaArgs a;
+            memset(&a, 0, sizeof(a));
+            a.idx = d_idx;
+            a.topk = d_topk;
+            a.rank = pool->d_rank;
+            a.enabled = pool->d_enabled;
+            a.status = pool->d_status;
+            a.T = T;
+            a.K = top_k;
+            a.E = E;
+            a.L = L;
+            a.n_keys = n_keys;
+            a.n_chunks = Wc;
+            a.cache_keys = 1;
+            a.key_bits = 1;
+            while ((1LL << a.key_bits) <= (long long)NK1) ++a.key_bits;
+            a.m = *meta;
+            const size_t smem = (size_t)meta_cluster_ints(Wc, NK1, L, rows_cta) * 4;
+            static std::atomic<int> configured_cl[64];
+            const int dev = pool->device < 64 ? pool->device : 63;
+            if (!configured_cl[dev].load(std::memory_order_acquire)) {
+                LORA_CUDA_TRY(cudaFuncSetAttribute(build_meta_cluster_kernel,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudgetInts * 4));
+                configured_cl[dev].store(1, std::memory_order_release);
+            }
+            cudaLaunchConfig_t cfg;
+            memset(&cfg, 0, sizeof(cfg));
+            cfg.gridDim = dim3(kMetaCL, 1, 1);
+            cfg.blockDim = dim3((unsigned)nt, 1, 1);
+            cfg.dynamicSmemBytes = smem;
+            cfg.stream = stream;
+            cudaLaunchAttribute at[2];
+            at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            at[0].val.programmaticStreamSerializationAllowed = 1;
+            at[1].id = cudaLaunchAttributeClusterDimension;
+            at[1].val.clusterDim.x = kMetaCL;
+            at[1].val.clusterDim.y = 1;
+            at[1].val.clusterDim.z = 1;
+            cfg.attrs = at;
+            cfg.numAttrs = 2;
+            LORA_CUDA_TRY(cudaLaunchKernelEx(&cfg, build_meta_cluster_kernel, a));
+            lora_note_launch();
+            meta->T = T;
+            meta->top_k = top_k;
+            meta->n_keys = n_keys;
+            meta->mode = pool->is_moe ? 1 : 0;
+            return LORA_OK;
+        }
     }
     // threads scale with the rows (one warp per 32 rows, 4..32 warps)
     int nthreads = (int)((rows + 31) / 32) * 32;

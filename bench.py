@@ -37,6 +37,7 @@ WORKLOADS = {
     "tiny": "single 512 -> 512 projection, T=64, 4 adapters rank 8, idx over {-1,0..3}, scale 2",
     "prefill_gate_up": "prefill SGMV gate_up: 8 requests, lengths U[128,2048] contiguous, H=4096 -> 2x14336, "
                        "8 adapters rank 64, request i -> adapter i",
+    "prefill_r16": "prefill SGMV gate_up as 'prefill_gate_up' with rank 16 (the tensor-core path below rank 64)",
     "many_adapter_down": "many-adapter decode down_proj 14336 -> 4096, T=2048, 1024 adapters ranks {8,16,32,64} "
                          "padded to 64, Zipf(1.2) popularity",
     "moe": "MoE-LoRA: E=64, top-8 of softmax(N(0,1)), D=2048, F=1408, 8 adapters rank 16, T=1024, "
@@ -63,6 +64,8 @@ def make_case(name):
         return gen.tiny()
     if name == "prefill_gate_up":
         return gen.prefill_gate_up()
+    if name == "prefill_r16":
+        return gen.prefill_gate_up(rank=16)
     if name == "many_adapter_down":
         return gen.many_adapter_down()
     if name == "moe":
@@ -137,7 +140,7 @@ def apply_kernels(name, policy, fused=False):
                     "accumulator also takes the delta as extra K blocks)")
         return ("cuBLASLt base GEMM, then lora_apply_slices (bgmv_fused_kernel for decode batches, the sgmv "
                 "and split kernels otherwise)")
-    if name == "prefill_gate_up" and policy != 1:
+    if name in ("prefill_gate_up", "prefill_r16") and policy != 1:
         k = "sgmv_shrink_kernel + sgmv_expand_kernel (tcgen05, 128-row runs); short tiles: " + k
     return k + (" for w13 and w2" if is_moe(name) else "")
 

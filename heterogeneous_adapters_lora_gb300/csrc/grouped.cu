@@ -559,7 +559,7 @@ size_t ws_total(size_t data_bytes, size_t cnt_ints) {
 }
 
 size_t sgmv_region_bytes(const lora_pool_t *pool, int T) {
-    if (pool->is_moe || pool->desc.max_rank != 64) return 0;
+    if (pool->is_moe || pool->desc.max_rank > 64) return 0;
     return (lora_sgmv_ws_bytes(pool, T) + 1023) & ~(size_t)1023;
 }
 

@@ -37,6 +37,10 @@ struct lora_pool {
     void *d_base;
     size_t bytes;
     int32_t *h_rank;                  // host mirror of the rank table
+    // dense pools of max_rank <= 64: TMA maps of every slice's B for each
+    // compact row length rs = 8, 16, .., 64 ([slice][rs/8 - 1], device
+    // memory), 3D over (rank, output row, slot); null when not built
+    CUtensorMap *d_bmaps;
 };
 
 // ------------------------------------------------------------ device helpers
@@ -146,6 +150,10 @@ bool lora_make_tmap_2d(CUtensorMap *m, const void *base, long long cols, long lo
 // that lands a box of box_rows rows x box_chunks 128-byte column chunks in
 // shared memory chunk-major: for each chunk, the rows as 128-byte lines in
 // the 128-byte swizzle (sgmv.cu).
+// 3D bf16 map over a B tensor stored compactly per slot: dims {rs, rows,
+// slots}, slot stride slot_elems elements, box {64, 128, 1}, 128-byte swizzle
+// (columns past rs read as zero).
+bool lora_make_tmap_b3d(CUtensorMap *m, const void *base, int rs, int rows, int slots, long long slot_elems);
 bool lora_make_tmap_a_chunks(CUtensorMap *m, const void *base, long long rows, long long cols, int box_rows,
                              int box_chunks);
 

@@ -104,6 +104,10 @@ extern "C" lora_status_t lora_pool_create(const lora_pool_desc_t *desc, void *st
     bytes = align256(bytes + (size_t)L * 4);
     size_t offStatus = bytes;
     bytes = align256(bytes + 4);
+    // TMA maps of B for the tensor-core prefill path (dense, max_rank <= 64)
+    const bool maps = !p->is_moe && desc->max_rank <= 64;
+    const size_t offMaps = bytes;
+    if (maps) bytes = align256(bytes + (size_t)desc->n_slices * 8 * sizeof(CUtensorMap));
     if (cudaMalloc(&p->d_base, bytes) != cudaSuccess) {
         free(p);
         return LORA_ERR_NOMEM;
@@ -124,6 +128,19 @@ extern "C" lora_status_t lora_pool_create(const lora_pool_desc_t *desc, void *st
         free(p->h_rank);
         free(p);
         return LORA_ERR_CUDA;
+    }
+    p->d_bmaps = nullptr;
+    if (maps) {
+        const int ns = desc->n_slices;
+        CUtensorMap *h = (CUtensorMap *)calloc((size_t)ns * 8, sizeof(CUtensorMap));
+        bool ok = h != nullptr;
+        for (int j = 0; ok && j < ns; ++j)
+            for (int q = 0; ok && q < 8; ++q)
+                ok = lora_make_tmap_b3d(&h[j * 8 + q], p->B[j], 8 * (q + 1), desc->out_dims[j], L, p->b_slot_elems[j]);
+        if (ok && cudaStreamSynchronize((cudaStream_t)stream) == cudaSuccess &&
+            cudaMemcpy(base + offMaps, h, (size_t)ns * 8 * sizeof(CUtensorMap), cudaMemcpyHostToDevice) == cudaSuccess)
+            p->d_bmaps = (CUtensorMap *)(base + offMaps);
+        free(h);
     }
     *out = p;
     return LORA_OK;

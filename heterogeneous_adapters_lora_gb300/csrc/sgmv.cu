@@ -41,6 +41,7 @@ constexpr int kNY = 3;                 // y tiles in flight in the expand
 constexpr int kOT = 128;                // outputs per expand tile (MMA N)
 constexpr int kOG = 8;                  // expand tiles per work unit
 constexpr uint32_t kTileBytes = kRows * kBK * 2;  // 16 KB: 128 rows x 128 B
+constexpr int kVRow = 2 * kBK;          // V row: 64 hi columns, then 64 lo columns
 
 struct alignas(64) ShrinkArgs {
     CUtensorMap tm_x;                    // x [T][H]: box {64, 128}
@@ -56,9 +57,10 @@ struct alignas(64) ShrinkArgs {
 };
 
 struct alignas(64) ExpandArgs {
-    CUtensorMap tm_v[LORA_MAX_SLICES];   // V_j [rows][2R]: box {64, 128}
-    CUtensorMap tm_b[LORA_MAX_SLICES];   // B_j [L*O_j][R]: box {64, 128}
+    CUtensorMap tm_v[LORA_MAX_SLICES];   // V_j [rows][128]: box {64, 128}
     CUtensorMap tm_y;                    // y [T][out]: box {64, 128}
+    const CUtensorMap *bmaps;            // the pool's B maps [slice][rs / 8 - 1]: box {64, 128, 1}
+    const int32_t *rank;
     int n_slices, R;
     int out_w[LORA_MAX_SLICES], out_off[LORA_MAX_SLICES];
     int grp_start[LORA_MAX_SLICES + 1];  // prefix over slices of ceil(otiles_j / kOG)
@@ -91,9 +93,9 @@ __global__ void __launch_bounds__(kThreads, 1) sgmv_shrink_kernel(const __grid_c
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (tile >= p.counters[5]) return;
 
-    const int N = p.R;  // accumulator columns: the ranks of slice js
-    const uint32_t a_bytes = (uint32_t)N * 128;
-    const uint32_t stage_bytes = kTileBytes + ((a_bytes + 1023) & ~1023u);
+    const int N = (p.R + 15) & ~15;  // accumulator columns: the ranks of slice js (MMA N: a multiple of 16)
+    const uint32_t a_bytes = (uint32_t)p.R * 128;  // the A box: R rows of 64 hidden elements
+    const uint32_t stage_bytes = kTileBytes + (((uint32_t)N * 128 + 1023) & ~1023u);
     const int keyn = p.ltile_keyn[tile];
     const int key = keyn >> 8, n = keyn & 255;
     const int row0 = p.ltile_row0[tile], tok0 = p.ltile_tok0[tile];
@@ -149,13 +151,19 @@ __global__ void __launch_bounds__(kThreads, 1) sgmv_shrink_kernel(const __grid_c
         wait_or_flag(&acc_full, 0, p.spin_limit, p.status);
         tc::tc_fence_after();
         const float sc = p.scale[key] * p.post_scale;
-        for (int c = 0; c < N / 32; ++c) {
+        // the 64 hi and 64 lo columns of the row, zero past the rank
+        for (int c = 0; c < 2; ++c) {
             uint32_t r[32];
-            tc::tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), r);
-            tc::tmem_wait_ld();
+            if (c * 32 < (int)ncols) {
+                tc::tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), r);
+                tc::tmem_wait_ld();
+            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (c * 32 + i >= p.R) r[i] = 0u;
             if (t < n) {
                 const int j = js, k0 = c * 32;
-                uint16_t *vrow = p.V + (long long)j * p.v_slice + (long long)(row0 + t) * (2 * p.R);
+                uint16_t *vrow = p.V + (long long)j * p.v_slice + (long long)(row0 + t) * kVRow;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     uint32_t hw[4], lw[4];
@@ -168,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1) sgmv_shrink_kernel(const __grid_c
                         lw[e2] = pack2(v0 - h0, v1 - h1);
                     }
                     *(uint4 *)(vrow + k0 + i * 8) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                    *(uint4 *)(vrow + p.R + k0 + i * 8) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                    *(uint4 *)(vrow + kBK + k0 + i * 8) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
                 }
             }
         }
@@ -238,6 +246,8 @@ __global__ void __launch_bounds__(kEThreads, 1) sgmv_expand_kernel(const __grid_
             decode(u, lt, j, ot0, n_ot);
             const int key = p.ltile_keyn[lt] >> 8;
             const int row0 = p.ltile_row0[lt], tok0 = p.ltile_tok0[lt];
+            // the slot's compact B rows (rs = ceil8(rank) columns, the rest read as zero)
+            const CUtensorMap *bm = p.bmaps + j * 8 + (((p.rank[key] + 7) >> 3) - 1);
             if (uc > 0) wait_or_flag(&v_empty, (uint32_t)((uc - 1) & 1), p.spin_limit, p.status);
             tc::mbar_expect_tx(&v_full, 2 * kTileBytes);
             tc::tma_load_2d(vt, &p.tm_v[j], 0, row0, &v_full);
@@ -247,7 +257,7 @@ __global__ void __launch_bounds__(kEThreads, 1) sgmv_expand_kernel(const __grid_
                 const int o_local = (ot0 + i) * kOT;
                 if (it >= 2) wait_or_flag(&b_empty[b], (uint32_t)(((it >> 1) - 1) & 1), p.spin_limit, p.status);
                 tc::mbar_expect_tx(&b_full[b], kTileBytes);
-                tc::tma_load_2d(bt + b * kTileBytes, &p.tm_b[j], 0, key * p.out_w[j] + o_local, &b_full[b]);
+                tc::tma_load_3d(bt + b * kTileBytes, bm, 0, o_local, key, &b_full[b]);
                 if (it >= kNY)
                     wait_or_flag(&y_empty[yb], (uint32_t)((it / kNY - 1) & 1), p.spin_limit, p.status);
                 char *yb_ptr = yt + (size_t)yb * 2 * kTileBytes;
@@ -406,6 +416,18 @@ bool lora_make_tmap_2d(CUtensorMap *m, const void *base, long long cols, long lo
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool lora_make_tmap_b3d(CUtensorMap *m, const void *base, int rs, int rows, int slots, long long slot_elems) {
+    PFN_cuTensorMapEncodeTiled_v12000 f = encode_fn();
+    if (!f || rs % 8 || slot_elems % 8) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)rs, (cuuint64_t)rows, (cuuint64_t)slots};
+    cuuint64_t strides[2] = {(cuuint64_t)rs * 2, (cuuint64_t)slot_elems * 2};
+    cuuint32_t box[3] = {(cuuint32_t)kBK, (cuuint32_t)kOT, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool lora_make_tmap_a_chunks(CUtensorMap *m, const void *base, long long rows, long long cols, int box_rows,
                              int box_chunks) {
     PFN_cuTensorMapEncodeTiled_v12000 f = encode_fn();
@@ -422,17 +444,15 @@ bool lora_make_tmap_a_chunks(CUtensorMap *m, const void *base, long long rows, l
 
 bool lora_sgmv_eligible(const lora_pool_t *pool) {
     const lora_pool_desc_t &d = pool->desc;
-    if (pool->is_moe || d.max_rank != 64 || pool->R8 != 64) return false;
+    if (pool->is_moe || !pool->d_bmaps || d.max_rank > 64) return false;
     if (d.n_slices * d.max_rank > 256 || d.in_dim % kBK) return false;
     for (int j = 0; j < d.n_slices; ++j)
         if (d.out_dims[j] % kOT) return false;
-    for (int a = 0; a < d.max_loras; ++a)
-        if (pool->h_rank[a] != 0 && pool->h_rank[a] != d.max_rank) return false;
     return encode_fn() != nullptr;
 }
 
 size_t lora_sgmv_ws_bytes(const lora_pool_t *pool, int rows) {
-    return (size_t)pool->desc.n_slices * rows * 2 * pool->desc.max_rank * 2;
+    return (size_t)pool->desc.n_slices * rows * kVRow * 2;
 }
 
 lora_status_t lora_sgmv_apply(const lora_pool_t *pool, const lora_meta_t *meta, const void *x, int64_t ldx,
@@ -468,11 +488,11 @@ lora_status_t lora_sgmv_apply(const lora_pool_t *pool, const lora_meta_t *meta, 
     sa.counters = meta->counters;
     sa.scale = pool->d_scale;
     sa.V = (uint16_t *)V;
-    sa.v_slice = (long long)T * 2 * R;
+    sa.v_slice = (long long)T * kVRow;
     sa.status = pool->d_status;
     sa.spin_limit = spin_limit;
     sa.post_scale = post_scale;
-    const size_t a_bytes = (size_t)R * 128;
+    const size_t a_bytes = (size_t)((R + 15) & ~15) * 128;  // the MMA reads N = ceil16(R) rows of A
     const size_t stage = kTileBytes + ((a_bytes + 1023) & ~(size_t)1023);
     const size_t smem_s = kStages * stage + 1024;
     cudaLaunchConfig_t cfg;
@@ -491,12 +511,11 @@ lora_status_t lora_sgmv_apply(const lora_pool_t *pool, const lora_meta_t *meta, 
 
     ExpandArgs ea;
     memset(&ea, 0, sizeof(ea));
-    for (int j = 0; j < ns; ++j) {
-        if (!make_map(&ea.tm_v[j], (const uint16_t *)V + (long long)j * T * 2 * R, 2 * R, T, 2 * R, kBK, kRows))
+    for (int j = 0; j < ns; ++j)
+        if (!make_map(&ea.tm_v[j], (const uint16_t *)V + (long long)j * T * kVRow, kVRow, T, kVRow, kBK, kRows))
             return LORA_ERR_CUDA;
-        if (!make_map(&ea.tm_b[j], pool->B[j], R, (long long)d.max_loras * d.out_dims[j], R, kBK, kOT))
-            return LORA_ERR_CUDA;
-    }
+    ea.bmaps = pool->d_bmaps;
+    ea.rank = pool->d_rank;
     if (!make_map(&ea.tm_y, y, out_total, T, ldy, kBK, kRows)) return LORA_ERR_CUDA;
     ea.n_slices = ns;
     ea.R = R;

@@ -314,17 +314,18 @@ def prefill_lengths(seed: int = 1003, n_req: int = 8, lo: int = 128, hi: int = 2
     return rng.integers(lo, hi + 1, size=n_req).astype(np.int32)
 
 
-def prefill_gate_up(base_y: str = "zero", permuted: bool = False) -> DenseCase:
+def prefill_gate_up(base_y: str = "zero", permuted: bool = False, rank: int = 64) -> DenseCase:
     """gate_up (4096 -> 2 x 14336), 8 requests with lengths uniform in
-    [128, 2048] laid out contiguously, request i uses slot i, rank 64, scale 1.0.
-    ``permuted`` assigns the slots to requests in a shuffled order instead."""
+    [128, 2048] laid out contiguously, request i uses slot i, rank 64 (or
+    ``rank``), scale 1.0.  ``permuted`` assigns the slots to requests in a
+    shuffled order instead."""
     lens = prefill_lengths()
     slots = np.arange(8, dtype=np.int32)
     if permuted:
         slots = np.random.Generator(np.random.PCG64(2003)).permutation(8).astype(np.int32)
     idx = np.concatenate([np.full(int(n), s, np.int32) for n, s in zip(lens, slots)])
-    c = dense_case(name="prefill_gate_up", T=int(lens.sum()), H=4096, out_dims=(14336, 14336),
-                   L=8, R=64, seed=1003 + 11, idx=idx, base_y=base_y)
+    c = dense_case(name="prefill_gate_up" if rank == 64 else f"prefill_gate_up_r{rank}", T=int(lens.sum()), H=4096,
+                   out_dims=(14336, 14336), L=8, R=rank, seed=1003 + 11, idx=idx, base_y=base_y)
     c.meta["lengths"] = lens
     return c
 

@@ -68,10 +68,30 @@ def test_prefill_preset_matches_split_k_kernel():
     assert_delta(bf16_bits_to_f32(y_sk), d_ref, "split-K")
 
 
-def test_mixed_ranks_fall_back_to_other_kernels():
+@pytest.mark.parametrize("ranks", [(64, 32, 64, 16), (8, 40, 24, 56)], ids=["64-32-64-16", "8-40-24-56"])
+def test_mixed_ranks_on_the_tensor_core_path(ranks):
+    """A max_rank-64 pool whose slots have other ranks: the long runs stay on
+    tcgen05 (each slot's compact B rows are read through the map of its row
+    length; the ranks past a slot's rank read as zero)."""
     c = gen.dense_case(name="sgmv_ranks", T=760, H=512, out_dims=(256, 384), L=4, R=64, seed=52,
-                       idx=mixed_idx(), ranks=(64, 32, 64, 16))
-    y, _ = _run(c)
+                       idx=mixed_idx(), ranks=ranks, scales=(1.0, 2.0, 0.5, 1.5))
+    y, meta = _run(c)
+    assert meta["n_ltiles"] == 5
     _, d_ref = oracle.dense_delta(c)
     act = active_mask(c.idx, c.L, c.enabled, c.ranks)
+    assert_rows_untouched(y, c.y0, ~act)
     assert_delta(bf16_bits_to_f32(y)[act], d_ref[act], "mixed ranks")
+
+
+@pytest.mark.parametrize("R", [16, 24, 48])
+def test_pools_below_rank_64_on_the_tensor_core_path(R):
+    """max_rank 16, 24 and 48: the shrink's MMA N is ceil16(R) and v is laid
+    out as 64 hi + 64 lo columns, zero past the rank."""
+    c = gen.dense_case(name=f"sgmv_r{R}", T=760, H=1024, out_dims=(384, 128), L=4, R=R, seed=53 + R,
+                       idx=mixed_idx(), ranks=(R, R, max(1, R // 2), R), scales=(1.0, 2.0, 0.5, 1.5))
+    y, meta = _run(c)
+    assert meta["n_ltiles"] == 5
+    _, d_ref = oracle.dense_delta(c)
+    act = active_mask(c.idx, c.L, c.enabled, c.ranks)
+    assert_rows_untouched(y, c.y0, ~act)
+    assert_delta(bf16_bits_to_f32(y)[act], d_ref[act], f"max_rank {R}")

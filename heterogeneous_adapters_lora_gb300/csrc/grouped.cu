@@ -679,7 +679,10 @@ lora_status_t lora_dense_apply(const lora_pool_t *pool, const lora_meta_t *meta,
     Carve cv;
     if (!carve(workspace, ws_bytes, cv)) return LORA_ERR_CAPACITY;
     const size_t sg_bytes = sgmv_region_bytes(pool, meta->T);
-    const bool use_sgmv = g_lora_kernel_policy != 1 && sg_bytes > 0 && meta->T >= LORA_LONG_MIN &&
+    // decode-sized batches (the fused decode kernel takes them) do not look
+    // for long runs: a batch of a few rows per slot has none worth a tile
+    const bool decode_sized = g_lora_kernel_policy == 0 && lora_fused_eligible(pool, meta->T);
+    const bool use_sgmv = g_lora_kernel_policy != 1 && !decode_sized && sg_bytes > 0 && meta->T >= LORA_LONG_MIN &&
                           cv.data_bytes >= sg_bytes && lora_sgmv_eligible(pool);
     char *scratch = cv.data + (use_sgmv ? sg_bytes : 0);
     const size_t scratch_bytes = cv.data_bytes - (use_sgmv ? sg_bytes : 0);

@@ -470,7 +470,12 @@ lora_status_t lora_sgmv_apply(const lora_pool_t *pool, const lora_meta_t *meta, 
                                            200 * 1024));
         g_sgmv_configured[dev].store(1, std::memory_order_release);
     }
-    const int max_lt = T / kRows + d.max_loras + 1;
+    // long tiles: a run of >= LORA_LONG_MIN tokens of one slot gives at most
+    // ceil(run / 128) of them, so at most T / LORA_LONG_MIN in all (a decode
+    // batch in a large pool launches a few CTAs that find no tile, not one
+    // per slot)
+    int max_lt = T / kRows + d.max_loras + 1;
+    if (max_lt > T / LORA_LONG_MIN + 1) max_lt = T / LORA_LONG_MIN + 1;
     if (spin_limit > (1 << 18)) spin_limit = 1 << 18;  // each poll may suspend the thread for a while
 
     ShrinkArgs sa;

@@ -615,7 +615,13 @@ static bool fused_plan(const lora_pool_t *pool, int T, FPlan *pl) {
         if (d.out_dims[j] % 32) return false;
     if (d.n_slices * ((d.max_rank + 15) & ~15) > 8 * 16) return false;
     const int L = d.max_loras;
-    if (T <= 0 || T > kMaxT || T < 4 * L || T > 32 * L) return false;
+    // a few rows per slot: past 16 on average a slot's cluster runs its chain
+    // of dependent steps once per 16-row tile, and the split kernels, which
+    // spread the tiles over the whole GPU, are faster (the Inkling sink-expert
+    // layers, 32 rows per slot: 40.9 against 33.0 us per step)
+    // (kernel policy 7 keeps the kernel up to 32 rows per slot, for tests)
+    const int per_slot = g_lora_kernel_policy == 7 ? 32 : 16;
+    if (T <= 0 || T > kMaxT || T < 4 * L || T > per_slot * L) return false;
     // the widest cluster whose CTAs all fit one wave, two per SM first
     for (int CS = 8; CS >= 1; CS >>= 1)
         for (int MINB = 2; MINB >= 1; --MINB) {

@@ -612,6 +612,12 @@ LoraProblem to_problem(const GArgs &g, const lora_meta_t *meta, int n_keys) {
 }  // namespace
 
 int g_lora_kernel_policy = 0;
+
+// Kernel policies (lora_set_kernel_policy) under which the fused decode
+// kernel and the split kernels may run: 0 automatic, 3 without the fused
+// kernel, 4-7 automatic apart from their own choice.
+static bool pol_fused(int p) { return p == 0 || p >= 4; }
+static bool pol_split(int p) { return p == 0 || p >= 3; }
 static std::atomic<unsigned long long> g_lora_launches{0};
 void lora_note_launch() { g_lora_launches.fetch_add(1, std::memory_order_relaxed); }
 extern "C" unsigned long long lora_kernel_launch_count(void) { return g_lora_launches.load(); }
@@ -681,7 +687,7 @@ lora_status_t lora_dense_apply(const lora_pool_t *pool, const lora_meta_t *meta,
     const size_t sg_bytes = sgmv_region_bytes(pool, meta->T);
     // decode-sized batches (the fused decode kernel takes them) do not look
     // for long runs: a batch of a few rows per slot has none worth a tile
-    const bool decode_sized = g_lora_kernel_policy == 0 && lora_fused_eligible(pool, meta->T);
+    const bool decode_sized = pol_fused(g_lora_kernel_policy) && lora_fused_eligible(pool, meta->T);
     const bool use_sgmv = g_lora_kernel_policy != 1 && !decode_sized && sg_bytes > 0 && meta->T >= LORA_LONG_MIN &&
                           cv.data_bytes >= sg_bytes && lora_sgmv_eligible(pool);
     char *scratch = cv.data + (use_sgmv ? sg_bytes : 0);
@@ -707,7 +713,7 @@ lora_status_t lora_dense_apply(const lora_pool_t *pool, const lora_meta_t *meta,
         g.count_idx = 4;
     }
     const int pol = g_lora_kernel_policy;
-    if (pol == 0 && !use_sgmv) {
+    if (pol_fused(pol) && !use_sgmv) {
         // decode-sized batches: shrink, reduction and expand in one launch
         bool launched = false;
         st = lora_fused_apply(pool, meta, nullptr, meta->T, x, ldx, y, ldy, post_scale, g_spin_limit, s, &launched);
@@ -716,7 +722,7 @@ lora_status_t lora_dense_apply(const lora_pool_t *pool, const lora_meta_t *meta,
     if (pol != 1) {
         bool launched = false;
         const LoraProblem pr = to_problem(g, meta, pool->desc.max_loras);
-        if ((pol == 0 || pol == 3) && have_split_region) {
+        if (pol_split(pol) && have_split_region) {
             st = lora_split_apply(pool, pr, scratch, scratch_bytes, cv.ctrl + 2, s, &launched);
             if (st != LORA_OK || launched) return st;
         }
@@ -780,7 +786,7 @@ extern "C" lora_status_t lora_build_meta_apply(const lora_pool_t *pool, const in
     if (pool->is_moe) return LORA_ERR_UNSUPPORTED;
     cudaStream_t s = (cudaStream_t)stream;
     const lora_pool_desc_t &d = pool->desc;
-    if (g_lora_kernel_policy == 0 && T > 0 && T <= meta->max_rows && d.max_loras <= meta->max_keys &&
+    if (pol_fused(g_lora_kernel_policy) && T > 0 && T <= meta->max_rows && d.max_loras <= meta->max_keys &&
         meta->sorted && meta->counters && meta->tile_keyn && meta->ltile_keyn && meta->stile_keyn && x && y &&
         lora_aligned16(x) && lora_aligned16(y) && ldx % 8 == 0 && ldy % 8 == 0 && ldx >= d.in_dim &&
         ldy >= out_total(pool)) {
@@ -924,7 +930,7 @@ extern "C" lora_status_t lora_moe_apply(const lora_pool_t *pool, const lora_meta
     cudaStream_t s = (cudaStream_t)stream;
     const int pol = g_lora_kernel_policy;
     const bool sparse = (long long)rows * kSparsityFactor <= keys;
-    if ((pol == 5 || (pol == 0 && sparse)) && lora_moe_block_supported(pool, which)) {
+    if ((pol == 5 || ((pol == 0 || pol >= 6) && sparse)) && lora_moe_block_supported(pool, which)) {
         // sparse occupancy: one thread-block cluster per (adapter, expert) key's tile
         return lora_moe_tile_launch(pool, meta, which, in, ld_in, topk_w, out, ld_out, s);
     }
@@ -945,7 +951,7 @@ extern "C" lora_status_t lora_moe_apply(const lora_pool_t *pool, const lora_meta
     if (pol != 1) {
         bool launched = false;
         const LoraProblem pr = to_problem(g, meta, keys);
-        if ((pol == 0 || pol == 3 || pol == 4 || pol == 5) && have_split_region) {
+        if (pol_split(pol) && have_split_region) {
             st = lora_split_apply(pool, pr, cv.data, cv.data_bytes, cv.ctrl + 2, s, &launched);
             if (st != LORA_OK || launched) return st;
         }

@@ -446,7 +446,10 @@ LORA_API lora_status_t lora_sink_experts_act(const void *gate_up, int64_t ld_gat
  *     metadata's 16-row tiles (one thread-block cluster per tile) for every
  *     MoE batch it supports,
  * 6 = like 0, with lora_linear_apply as this library's tcgen05 GEMM that
- *     takes the delta into its accumulator (see lora_linear_apply).
+ *     takes the delta into its accumulator (see lora_linear_apply),
+ * 7 = like 0, with the fused decode kernel for batches of up to 32 rows per
+ *     slot on average (0 stops at 16, past which the split kernels measured
+ *     faster).
  * For tests and tuning. */
 LORA_API void lora_set_kernel_policy(int32_t policy);
 

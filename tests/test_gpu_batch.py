@@ -102,7 +102,13 @@ def test_several_row_steps_and_tiles(T):
     idx[rng.random(T) < 0.05] = -1
     c = gen.dense_case(name=f"batch{T}", T=T, H=1024, out_dims=(512, 256), L=Lk, R=16, seed=80, idx=idx,
                        scales=np.linspace(0.5, 2.0, Lk).astype(np.float32))
-    _run(c, True)
+    # 30 and 32 rows per slot: past the automatic choice's 16, kept on the
+    # fused kernel by policy 7
+    L.lora_set_kernel_policy(7)
+    try:
+        _run(c, True)
+    finally:
+        L.lora_set_kernel_policy(0)
 
 
 def test_bad_indices_and_reset_slot():
@@ -130,4 +136,9 @@ def test_long_run_slots_in_batch_mode():
     idx[200:256:3] = 3
     c = gen.dense_case(name="batch_runs", T=256, H=1024, out_dims=(256,), L=8, R=16, seed=83, idx=idx,
                        scales=np.ones(8, np.float32))
-    _run(c, True)
+    L.lora_set_kernel_policy(7)  # 32 rows per slot: past the automatic choice's 16
+    try:
+        _run(c, True)
+    finally:
+        L.lora_set_kernel_policy(0)
+    _run(c, False)  # the automatic choice: metadata build, then the split kernels

@@ -69,7 +69,12 @@ def test_several_tiles_per_slot(seed):
     idx[rng.random(120) < 0.05] = -1
     c = gen.dense_case(name=f"tiles{seed}", T=120, H=1024, out_dims=(512, 256), L=4, R=16, seed=60 + seed,
                        idx=idx, scales=(1.0, 2.0, 0.5, 1.5))
-    _run(c)
+    L.lora_set_kernel_policy(7)  # 30 rows per slot: past the automatic choice's 16
+    try:
+        _run(c)
+    finally:
+        L.lora_set_kernel_policy(0)
+    _run(c, expect_fused=False)
 
 
 def test_mixed_ranks_straddling_blocks():

@@ -64,6 +64,10 @@ struct SArgs {
     const int32_t *enabled, *key_count, *key_offset;
     int n_slots, x_stages;
     int *ticket;             // [0] next item, [1] finished CTAs; zero between calls
+    // token mode of the key-major shrink (an MoE projection whose A has
+    // expert dimension 1): keys are slots, each slot's tokens are gathered
+    // from its pair range in the MoE order, and partials land at row = token
+    int tok_K, tok_E, tok_G, tok_T, off_tok;
 };
 
 struct EArgs {
@@ -88,6 +92,7 @@ struct EArgs {
     int *ticket;             // [0] next item, [1] finished CTAs; zero between calls
     int *status;
     int spin_limit;
+    int v_div, v_rows;       // v_div > 0: partials of row r at row sorted[r] / v_div of v_rows
 };
 
 // Dynamic work distribution: the CTAs of a one-wave grid take items from a
@@ -494,15 +499,71 @@ __global__ void __launch_bounds__(kPThreads) bgmv_shrink_kernel(const __grid_con
 // the key's rows is multiplied against them (A read once per key, not once
 // per tile).  The partials land where the per-tile shrink would put them.
 
+// Token mode (tok_K > 0): an MoE projection whose A_j has expert dimension 1
+// (the shared-outer layout) has a shrink that depends on the token and its
+// slot only, so it is computed once per token instead of once per routed
+// pair.  Keys are then the slots; a slot's tokens are the distinct pair / K
+// over its pair range of the MoE order (every expert key of the slot), in
+// ascending token order; tok_G CTAs share a (slot, slice, chunk) and take its
+// tiles round robin; the partials land at row = token of [tok_T] rows.
+
+// This slot's tokens, ascending, into tok[] (a bitmap over the tokens after
+// it); returns their count.  Every thread calls it.
+__device__ int gather_slot_tokens(const SArgs &p, int a, int *tok, int *s_ws) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int T = p.tok_T, nw = (T + 31) >> 5;
+    unsigned *bm = (unsigned *)(tok + T);
+    for (int i = tid; i < nw; i += kSThreads) bm[i] = 0u;
+    __syncthreads();
+    const int s0 = p.key_offset[a * p.tok_E], s1 = p.key_offset[(a + 1) * p.tok_E];
+    for (int q = s0 + tid; q < s1; q += kSThreads) {
+        const int t = p.sorted[q] / p.tok_K;
+        atomicOr(bm + (t >> 5), 1u << (t & 31));
+    }
+    __syncthreads();
+    // each thread a run of words; an exclusive scan of the runs' counts
+    const int wpt = (nw + kSThreads - 1) / kSThreads;
+    const int w0 = min(nw, tid * wpt), w1 = min(nw, w0 + wpt);
+    int mine = 0;
+    for (int w = w0; w < w1; ++w) mine += __popc(bm[w]);
+    int incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += u;
+    }
+    if (lane == 31) s_ws[warp] = incl;
+    __syncthreads();
+    int base = incl - mine, total = 0;
+#pragma unroll
+    for (int w = 0; w < kSWarps; ++w) {
+        if (w < warp) base += s_ws[w];
+        total += s_ws[w];
+    }
+    for (int w = w0; w < w1; ++w) {
+        unsigned m = bm[w];
+        while (m) {
+            tok[base++] = w * 32 + __ffs(m) - 1;
+            m &= m - 1u;
+        }
+    }
+    __syncthreads();
+    return total;
+}
+
 template <int NBMAX>
 __global__ void __launch_bounds__(kSThreads) bgmv_shrink_slot_kernel(const __grid_constant__ SArgs p) {
     extern __shared__ __align__(128) char smem[];
     __shared__ __align__(8) uint64_t abar, xbar[2];
     __shared__ int s_rows[2][kTileRows];
+    __shared__ int s_ws[kSWarps];
     const int XS = p.x_stages;  // 1 or 2
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const bool tmode = p.tok_K > 0;
+    const int G = tmode ? p.tok_G : 1;
+    const int gi = blockIdx.x % G, bid = blockIdx.x / G;
 
-    const int c = blockIdx.x % p.NC, j = (blockIdx.x / p.NC) % p.n_slices, key = blockIdx.x / (p.NC * p.n_slices);
+    const int c = bid % p.NC, j = (bid / p.NC) % p.n_slices, key = bid / (p.NC * p.n_slices);
     const int a = key / p.E, e = key - a * p.E;
     const int hb = c * p.HC, he = min(p.in_dim, hb + p.HC), len = he - hb;
     const uint16_t *Ab = a_rows(p, j, a, e);
@@ -534,13 +595,21 @@ __global__ void __launch_bounds__(kSThreads) bgmv_shrink_slot_kernel(const __gri
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
-    const int cnt = p.key_count[key], off = p.key_offset[key];
+    int *tok = (int *)(smem + p.off_tok);  // token mode: the slot's tokens
+    int cnt, off = 0;
+    if (tmode) {
+        cnt = gather_slot_tokens(p, a, tok, s_ws);
+    } else {
+        cnt = p.key_count[key];
+        off = p.key_offset[key];
+    }
     const int n_t = (cnt + kTileRows - 1) / kTileRows;
+    const int n_my = n_t > gi ? (n_t - gi + G - 1) / G : 0;  // tiles gi, gi + G, ... of the key
 
-    auto load_x = [&](int t) {  // x rows of tile t into stage t % XS (warp 0)
-        const int st = t % XS, n = min(kTileRows, cnt - t * kTileRows);
+    auto load_x = [&](int i) {  // x rows of this CTA's i-th tile into stage i % XS (warp 0)
+        const int st = i % XS, tile = gi + i * G, n = min(kTileRows, cnt - tile * kTileRows);
         uint16_t *xs = (uint16_t *)(smem + p.off_x + st * p.x_stage_bytes);
-        if (lane < n) s_rows[st][lane] = p.sorted[off + t * kTileRows + lane];
+        if (lane < n) s_rows[st][lane] = tmode ? tok[tile * kTileRows + lane] : p.sorted[off + tile * kTileRows + lane];
         __syncwarp();
         if (lane == 0) mbar_expect_tx(&xbar[st], rowb * (uint32_t)n);
         __syncwarp();
@@ -549,35 +618,37 @@ __global__ void __launch_bounds__(kSThreads) bgmv_shrink_slot_kernel(const __gri
                      &xbar[st]);
     };
     if (warp == 0) {
-        if (n_t > 0) load_x(0);
-        if (n_t > 1 && XS > 1) load_x(1);
+        if (n_my > 0) load_x(0);
+        if (n_my > 1 && XS > 1) load_x(1);
     }
     mbar_wait(&abar, 0, p.spin_limit, p.status);  // also before any exit: no copy may be in flight
 
     const int nnb = (r + 7) >> 3;
     float *red = (float *)(smem + p.off_red);
-    for (int t = 0; t < n_t; ++t) {
-        const int st = t % XS, row0 = off + t * kTileRows, n = min(kTileRows, cnt - t * kTileRows);
-        mbar_wait(&xbar[st], (uint32_t)((t / XS) & 1), p.spin_limit, p.status);
+    for (int i = 0; i < n_my; ++i) {
+        const int st = i % XS, tile = gi + i * G;
+        const int row0 = off + tile * kTileRows, n = min(kTileRows, cnt - tile * kTileRows);
+        mbar_wait(&xbar[st], (uint32_t)((i / XS) & 1), p.spin_limit, p.status);
         const uint16_t *xs = (const uint16_t *)(smem + p.off_x + st * p.x_stage_bytes);
         ShrinkAcc<NBMAX> acc;
         shrink_acc_zero(acc);
         shrink_stage_mma(xs, p.xs_stride, as, p.as_stride, len, nnb, warp, lane, acc);
         __syncthreads();  // every warp is done with x stage st and with red of the previous tile
-        if (warp == 0 && t + XS < n_t) {
+        if (warp == 0 && i + XS < n_my) {
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            load_x(t + XS);
+            load_x(i + XS);
         }
-        for (int i = tid; i < kSWarps * kTileRows * p.R8; i += kSThreads) red[i] = 0.f;
+        for (int q = tid; q < kSWarps * kTileRows * p.R8; q += kSThreads) red[q] = 0.f;
         __syncthreads();
         shrink_store_red(red, p.R8, nnb, r, n, warp, lane, acc);
         __syncthreads();
-        float *dst = p.part + ((long long)c * p.n_slices + j) * p.rows * p.R8 + (long long)row0 * p.R8;
-        for (int i = tid; i < n * p.R8; i += kSThreads) {
-            const int t2 = i / p.R8, k = i - t2 * p.R8;
+        float *dst = p.part + ((long long)c * p.n_slices + j) * p.rows * p.R8;
+        for (int q = tid; q < n * p.R8; q += kSThreads) {
+            const int t2 = q / p.R8, k = q - t2 * p.R8;
             float sum = 0.f;
             for (int w = 0; w < kSWarps; ++w) sum += red[(w * kTileRows + t2) * p.R8 + k];
-            dst[i] = sum;
+            const long long prow = tmode ? tok[tile * kTileRows + t2] : row0 + t2;
+            dst[prow * p.R8 + k] = sum;
         }
     }
 }
@@ -701,13 +772,15 @@ __global__ void __launch_bounds__(kThreads, PW == 8 ? 3 : (KS >= 3 ? 4 : 5))
         const int j0 = slice_of(p, ob), j1 = slice_of(p, oe - 1);
         // 16 rows x 8 threads, 4 ranks per thread and step: no divisions
         const int tq = tid >> 3, lq = tid & 7;
-        const long long cstride = (long long)ns * p.rows * p.R8 / 4;
+        const int vrows = p.v_div > 0 ? p.v_rows : p.rows;
+        const long long cstride = (long long)ns * vrows * p.R8 / 4;
+        const int prow = tq < n ? (p.v_div > 0 ? rows[tq] / p.v_div : row0 + tq) : 0;
         for (int jj = j0; jj <= j1; ++jj) {
             for (int k = lq * 4; k < p.R8; k += 32) {
                 float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (tq < n) {
                     const float4 *src =
-                        (const float4 *)(p.part + ((long long)jj * p.rows + row0 + tq) * p.R8 + k);
+                        (const float4 *)(p.part + ((long long)jj * vrows + prow) * p.R8 + k);
                     for (int cc = 0; cc < nc; ++cc) {
                         const float4 v = __ldcg(src + cc * cstride);
                         s4.x += v.x;
@@ -1077,6 +1150,13 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
         LORA_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, slot_fn, kSThreads, slot_smem));
         slot_major = (long long)L * ns * NC <= (long long)g_key_major_waves * o * pool->num_sms;
     }
+    // token mode (shared-outer MoE A): the key-major kernel over slots, with
+    // the slot's token list and a bitmap over the batch's tokens after the
+    // reduction buffer
+    const size_t tok_bytes = a128((size_t)4 * (pr.T + (pr.T + 31) / 32));
+    const bool tmode = pr.tok_dedup && pr.T > 0 && pr.E > 0 && pr.n_keys % pr.E == 0 &&
+                       slot_smem + tok_bytes <= 160 * 1024;
+    if (tmode) slot_major = true;
 
     SArgs sa;
     memset(&sa, 0, sizeof(sa));
@@ -1181,8 +1261,34 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
         sa.off_x = (int)a128((size_t)R8 * (HC + 8) * 2);
         sa.off_red = sa.off_x + x_stages * sa.x_stage_bytes;
         if ((size_t)sa.off_red + red_bytes > slot_smem) return LORA_ERR_INVALID_ARG;  // layout check
-        cfg.gridDim = dim3((unsigned)(L * ns * NC), 1, 1);
-        cfg.dynamicSmemBytes = slot_smem;
+        long long grid = (long long)L * ns * NC;
+        size_t smem_k = slot_smem;
+        if (tmode) {
+            // keys are the slots; tok_G CTAs per (slot, slice, chunk) share
+            // a slot's tiles: about one tile each on an even batch, and at
+            // most two waves in all
+            const int Ls = L / pr.E;
+            smem_k = slot_smem + tok_bytes;
+            int o = 0;
+            LORA_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, slot_fn, kSThreads, smem_k));
+            const long long per_slot = ((long long)pr.T / kTileRows + Ls + Ls - 1) / Ls;
+            const long long cap = 2LL * (o < 1 ? 1 : o) * pool->num_sms / ((long long)Ls * ns * NC);
+            const int G = (int)std::max(1LL, std::min(per_slot, cap));
+            sa.E = 1;
+            sa.row_div = 1;
+            sa.rows = pr.T;
+            sa.n_slots = Ls;
+            sa.tok_K = pr.row_div;
+            sa.tok_E = pr.E;
+            sa.tok_T = pr.T;
+            sa.tok_G = G;
+            sa.off_tok = (int)slot_smem;
+            ea.v_div = pr.row_div;
+            ea.v_rows = pr.T;
+            grid = (long long)Ls * ns * NC * G;
+        }
+        cfg.gridDim = dim3((unsigned)grid, 1, 1);
+        cfg.dynamicSmemBytes = smem_k;
         LORA_CUDA_TRY(cudaLaunchKernelEx(&cfg, slot_fn, sa));
     } else {
         if (tile_static) {

@@ -125,6 +125,7 @@ struct LoraProblem {
     float post_scale;
     int shrink_only;                        // split path: launch the shrink alone
     int *nc_out;                            // ... and report its hidden chunk count here
+    int tok_dedup;                          // MoE with A of expert dimension 1: shrink once per token
 };
 
 // Cluster kernel (cluster.cu): launches and sets *launched when the shape

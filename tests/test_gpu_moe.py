@@ -138,3 +138,43 @@ def test_out_of_range_ids_are_skipped_and_reported(shared):
     assert_rows_untouched(ic3, c.ic3_0, ~act)
     assert_delta(bf16_bits_to_f32(ic1)[act], d13[act], "bad ids w13")
     assert_delta(bf16_bits_to_f32(ic3)[act], d2[act], "bad ids w2")
+
+
+@pytest.mark.parametrize("policy", [0, 2])
+@pytest.mark.parametrize("T", [613, 2500])
+def test_shared_outer_shrink_once_per_token(T, policy):
+    """Shared-outer w13 (A with expert dimension 1): the shrink runs once per
+    token, on slots as keys, with each slot's tokens gathered from its pair
+    range.  Skewed slots (several CTAs share a slot's tiles), a ragged tail, a
+    token whose first routed pair is dropped, a token with every pair dropped
+    and one outside any slot; w2 is the per-expert path on the same batch.
+    Policy 2 runs the same batch on the one-pass cluster kernel."""
+    from heterogeneous_adapters_lora_gb300 import lora as L
+    c = gen.moe_case(name="moe_tok", T=T, K=4, E=8, D=1040, F=272, L=3, R=16, seed=61 + T, shared_outer=True,
+                     ranks=(16, 8, 12), scales=(1.0, 0.5, 2.0), p_none=0.05)
+    rng = np.random.default_rng(T)
+    c.idx[:] = np.where(rng.random(c.T) < 0.7, 0, c.idx)  # most tokens on slot 0
+    c.idx[7] = -1
+    c.idx[5] = 0
+    c.idx[9] = 1
+    c.topk_ids[5, 0] = -1
+    c.topk_ids[9, :] = c.E
+    L.lora_set_kernel_policy(policy)
+    run = H.MoERun(c)
+    try:
+        run.step()
+        ic1 = H.from_dev_u16(run.ic1)
+        ic3 = H.from_dev_u16(run.ic3)
+        st = run.status()
+    finally:
+        run.close()
+        L.lora_set_kernel_policy(0)
+    assert st == H.L.CODE["LORA_ERR_DEVICE_INDEX"]
+    act = pair_active(c)
+    assert not act[5 * c.K] and act[5 * c.K + 1] and not act[9 * c.K:10 * c.K].any()
+    _, d13 = oracle.moe_w13(c)
+    _, d2 = oracle.moe_w2(c)
+    assert_rows_untouched(ic1, c.ic1_0, ~act)
+    assert_rows_untouched(ic3, c.ic3_0, ~act)
+    assert_delta(bf16_bits_to_f32(ic1)[act], d13[act], "token shrink w13")
+    assert_delta(bf16_bits_to_f32(ic3)[act], d2[act], "token shrink w2")

@@ -780,11 +780,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-workload", action="store_true",
                     help="time only --workload (skip the per_workload block of the other configurations)")
-    ap.add_argument("--kernel-policy", type=int, default=0, choices=[0, 1, 2, 3, 4, 5, 6],
+    ap.add_argument("--kernel-policy", type=int, default=0, choices=[0, 1, 2, 3, 4, 5, 6, 7, 8],
                     help="lora_set_kernel_policy: 0 automatic, 1 persistent split-K kernel, 2 cluster kernel "
                          "first, 3 no fused decode / MoE block kernel, 4 MoE per-pair blocks, 5 MoE block kernel "
                          "over the metadata's tiles, 6 the linear layer as one tcgen05 GEMM with the delta in its "
-                         "accumulator (tuning)")
+                         "accumulator, 7 fused decode kernel up to 32 rows per slot, 8 split expand on warp-level MMAs (tuning)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -31,6 +31,7 @@
 
 #include "lora_internal.cuh"
 #include "mma_common.cuh"
+#include "tc_common.cuh"
 
 namespace {
 
@@ -968,6 +969,289 @@ __global__ void __launch_bounds__(kThreads, PW == 8 ? 3 : (KS >= 3 ? 4 : 5))
     asm volatile("griddepcontrol.launch_dependents;");
 }
 
+// ---------------------------------------------------------------- expand on tcgen05
+//
+// The same items as bgmv_expand_kernel (a tile of up to 16 rows of one key,
+// oc_w output columns), with the products on the tensor cores: for every
+// 128-output block m of the item
+//
+//   D_m[o][t] = sum_k B_j[a][o][k] * v_hi[t][j][k] + sum_k B_j[a][o][k] * v_lo[t][j][k]
+//
+// is one tcgen05 MMA pair with M = 128 outputs, N = 16 rows and K = the
+// slot's ranks (16 per instruction), accumulated in tensor memory (16 fp32
+// columns per block).  Both operands are K-major without swizzle: 8-row x
+// 16-byte core matrices, the K-adjacent ones LBO apart and the M/N-adjacent
+// ones SBO = 128 bytes apart.  B_j rows are copied in with 16-byte cp.async
+// (chunk kc of row i at kc * 2048 + i * 16 of its block), v is written by the
+// threads that sum the partials (chunk kc of row t at kc * 256 + t * 16).
+// One thread issues the MMAs; each warp then reads its lane quarter of every
+// block (32 outputs x 16 rows) and adds it to the y rows staged in shared
+// memory, which are stored back with bulk copies as in bgmv_expand_kernel.
+// Every slice width is a multiple of 128, so a block lies in one slice.
+
+constexpr int kTcM = 128;  // outputs per MMA block
+static_assert(kThreads == kTcM, "the tensor-core expand copies one B row per thread");
+
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr >> 4) & 0x3FFFu);        // start address
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;   // K-adjacent core matrices
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;   // M/N-adjacent core matrices
+    d |= (uint64_t)1 << 46;                        // descriptor version for tcgen05; no swizzle
+    return d;
+}
+// 32 lanes x 16 consecutive fp32 columns (this warp's lane quarter).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void cp_async16_cg(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+
+// MT: 128-output blocks per item (oc_w / 128).  Shared memory: B blocks
+// [MT][kcb][128][8], y rows [16][ys_stride], v hi and lo [n_slices][kcb][16][8]
+// with kcb = the pool's 8-rank chunks rounded up to a 16-rank step.
+template <int MT>
+__global__ void __launch_bounds__(kThreads) bgmv_expand_tc_kernel(const __grid_constant__ EArgs p) {
+    extern __shared__ __align__(128) char smem[];
+    __shared__ __align__(8) uint64_t ybar, mbar;
+    __shared__ int s_rows[2][kTileRows];
+    __shared__ int s_next, s_ninfo[3];
+    __shared__ int s_item;
+    __shared__ uint32_t s_tmem;
+    __shared__ const uint16_t *s_bp[MT];  // this item's B rows of block m (row 0 of the block)
+    __shared__ int s_mj[MT];              // ... and its slice
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int ns = p.n_slices;
+    const int n_tiles = p.counters[p.count_idx];
+    const int total = n_tiles * p.n_oc;
+    constexpr uint32_t kCols = MT * 16 < 32 ? 32 : MT * 16;  // tensor-memory columns: 16 per block
+    const int kcb = ((p.R8 + 15) >> 4) * 2;                  // 8-rank chunks per block (16-rank steps)
+    const uint32_t blk_bytes = (uint32_t)kcb * kTcM * 16;    // one B block
+    const uint32_t vsl_bytes = (uint32_t)kcb * kTileRows * 16;  // v of one slice
+    if (warp == 0) {
+        tc::tmem_alloc(&s_tmem, kCols);
+        tc::tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_init(&ybar, 1);
+        mbar_init(&mbar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    char *bs = smem + p.off_b;
+    uint16_t *ys = (uint16_t *)(smem + p.off_ys);
+    char *vh = smem + p.off_vh;
+    char *vl = smem + p.off_vl;
+    bool waited = false;
+    const int nc = p.NC;
+    uint32_t phase = 0;
+
+    const bool dyn = total > (int)gridDim.x;
+    int item = dyn ? take_item(p.ticket, &s_item) : (int)blockIdx.x;  // its barrier also publishes s_tmem
+    int row0 = 0, keyn = 0, r = 0, buf = 0;
+    if (item < total) {
+        const int tile = item / p.n_oc;
+        row0 = p.tile_row0[tile];
+        keyn = p.tile_keyn[tile];
+        r = p.rank[(keyn >> 5) / p.E];
+        if (tid < (keyn & 31)) s_rows[0][tid] = p.sorted[row0 + tid];
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    for (; item < total; phase ^= 1u, buf ^= 1) {
+        const int tile = item / p.n_oc, oc = item - tile * p.n_oc;
+        const int n = keyn & 31, key = keyn >> 5;
+        const int a = key / p.E, e = key - a * p.E;
+        const int rs = (r + 7) & ~7;
+        const int ob = oc * p.oc_w, oe = min(p.out_total, ob + p.oc_w);
+        const int mta = (oe - ob) / kTcM;         // blocks of this item
+        const int kcr = rs >> 3, kcs = ((rs + 15) >> 4) * 2;  // real and stepped 8-rank chunks
+        const int *rows = s_rows[buf];
+        int nxt_t = total;
+        if (dyn && tid == 0) nxt_t = atomicAdd(p.ticket, 1);  // lands while this item runs
+        // y rows: bulk copies (they do not depend on the shrink).  The y
+        // tile's last generic writes were ordered before the async proxy by
+        // the fence ahead of the previous item's stores.
+        if (warp == 0) {
+            const uint32_t rowb = (uint32_t)(oe - ob) * 2;
+            if (lane == 0) mbar_expect_tx(&ybar, rowb * (uint32_t)n);
+            __syncwarp();
+            if (lane < n)
+                bulk_g2s(ys + lane * p.ys_stride, p.out + (long long)rows[lane] * p.ld_out + ob, rowb, &ybar);
+        } else if (warp == 1 && lane < MT) {
+            // each block's slice and B rows (constant parameter indices)
+            const int o0 = ob + lane * kTcM;
+            int jm = 0;
+            const uint16_t *bp = nullptr;
+#pragma unroll
+            for (int jj = 0; jj < LORA_MAX_SLICES; ++jj) {
+                if (jj < ns && o0 >= p.out_off[jj] && o0 < p.out_off[jj] + p.out_w[jj]) {
+                    jm = jj;
+                    bp = p.B[jj] + (long long)a * p.B_ss[jj] +
+                         (p.B_shared[jj] ? 0ll : (long long)e * p.out_w[jj] * rs) + (long long)(o0 - p.out_off[jj]) * rs;
+                }
+            }
+            s_mj[lane] = jm;
+            s_bp[lane] = bp;
+        }
+        // the v row this thread converts, and its weight factors (loads in
+        // flight across the barrier and the copies; multiplied only in the
+        // sum below)
+        const int tq = tid >> 3, lq = tid & 7;
+        const float w_sc = tq < n ? __ldg(p.scale + a) : 0.f;
+        const float w_rw = (tq < n && p.row_w) ? __ldg(p.row_w + rows[tq]) : 1.f;
+        __syncthreads();
+        // B blocks: row i of every block is thread i's, its chunks one after
+        // another; chunks past the rank (up to the 16-rank step) are zero
+        for (int m = 0; m < mta; ++m) {
+            const uint16_t *src = s_bp[m] + (long long)tid * rs;
+            char *dst = bs + m * blk_bytes + tid * 16;
+            for (int kc = 0; kc < kcs; ++kc) {
+                if (kc < kcr)
+                    cp_async16_cg(dst + kc * (kTcM * 16), src + kc * 8);
+                else
+                    *(uint4 *)(dst + kc * (kTcM * 16)) = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        if (!waited) {
+            asm volatile("griddepcontrol.wait;" ::: "memory");  // the shrink's partials are complete
+            waited = true;
+        }
+        // v of every slice a block uses (chunk partials summed in order,
+        // scaled) -> bf16 hi / lo in the core-matrix layout; zero past the rank
+        const int j0 = s_mj[0], j1 = s_mj[mta - 1];
+        const float w_row = w_sc * p.post_scale * w_rw;
+        const int vrows = p.v_div > 0 ? p.v_rows : p.rows;
+        const long long cstride = (long long)ns * vrows * p.R8 / 4;
+        const int prow = tq < n ? (p.v_div > 0 ? rows[tq] / p.v_div : row0 + tq) : 0;
+        for (int jj = j0; jj <= j1; ++jj) {
+            for (int k = lq * 4; k < kcs * 8; k += 32) {
+                float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (tq < n && k < rs) {
+                    const float4 *src = (const float4 *)(p.part + ((long long)jj * vrows + prow) * p.R8 + k);
+                    for (int cc = 0; cc < nc; ++cc) {
+                        const float4 v = __ldcg(src + cc * cstride);
+                        s4.x += v.x;
+                        s4.y += v.y;
+                        s4.z += v.z;
+                        s4.w += v.w;
+                    }
+                    s4.x *= w_row;
+                    s4.y *= w_row;
+                    s4.z *= w_row;
+                    s4.w *= w_row;
+                }
+                const __nv_bfloat162 h01 = __floats2bfloat162_rn(s4.x, s4.y);
+                const __nv_bfloat162 h23 = __floats2bfloat162_rn(s4.z, s4.w);
+                const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+                uint2 hv, lv;
+                hv.x = *(const uint32_t *)&h01;
+                hv.y = *(const uint32_t *)&h23;
+                lv.x = pack_bf16x2(s4.x - f01.x, s4.y - f01.y);
+                lv.y = pack_bf16x2(s4.z - f23.x, s4.w - f23.y);
+                const int off = jj * (int)vsl_bytes + (k >> 3) * (kTileRows * 16) + tq * 16 + (k & 7) * 2;
+                *(uint2 *)(vh + off) = hv;
+                *(uint2 *)(vl + off) = lv;
+            }
+        }
+        if (tid == 0) s_next = nxt_t;
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> tensor core reads
+        tc::tc_fence_before();
+        __syncthreads();
+        tc::tc_fence_after();
+        // the next item's tile words, in flight during the MMAs
+        const int nitem = s_next;
+        int nrow0 = 0, nkeyn = 0;
+        if (nitem < total && tid < kTileRows) {
+            const int nt = nitem / p.n_oc;
+            nrow0 = p.tile_row0[nt];
+            nkeyn = p.tile_keyn[nt];
+        }
+        if (tid == 0) {
+            const uint32_t idesc = tc::idesc_bf16(kTcM, kTileRows);
+            const uint32_t b_addr = smem_u32(bs), vh_addr = smem_u32(vh), vl_addr = smem_u32(vl);
+            const int ksteps = kcs >> 1;
+            for (int m = 0; m < mta; ++m) {
+                const uint32_t ab = b_addr + m * blk_bytes, vo = (uint32_t)s_mj[m] * vsl_bytes;
+                for (int ks = 0; ks < ksteps; ++ks) {
+                    const uint64_t ad = desc_kmajor(ab + ks * 2 * (kTcM * 16), kTcM * 16, 128);
+                    tc::mma_bf16(tmem + m * 16, ad, desc_kmajor(vh_addr + vo + ks * 2 * (kTileRows * 16), kTileRows * 16, 128),
+                                 idesc, ks != 0);
+                    tc::mma_bf16(tmem + m * 16, ad, desc_kmajor(vl_addr + vo + ks * 2 * (kTileRows * 16), kTileRows * 16, 128),
+                                 idesc, 1u);
+                }
+            }
+            tc::mma_commit(&mbar);
+        }
+        mbar_wait(&ybar, phase, p.spin_limit, p.status);
+        mbar_wait(&mbar, phase, p.spin_limit, p.status);
+        tc::tc_fence_after();
+        // this warp's 32 outputs of every block, 16 rows each, added to y
+        for (int m = 0; m < mta; ++m) {
+            uint32_t d[16];
+            tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(m * 16), d);
+            uint16_t *yc = ys + m * kTcM + warp * 32 + lane;
+            uint16_t yv[kTileRows];  // every load before the stores (a run-time row stride hides that they differ)
+#pragma unroll
+            for (int t = 0; t < kTileRows; ++t) yv[t] = t < n ? yc[t * p.ys_stride] : (uint16_t)0;
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int t = 0; t < kTileRows; ++t)
+                if (t < n)
+                    yc[t * p.ys_stride] = __bfloat16_as_ushort(__float2bfloat16_rn(
+                        __bfloat162float(__ushort_as_bfloat16(yv[t])) + __uint_as_float(d[t])));
+        }
+        // the next item's rows and rank, in flight during the stores
+        int nrank = 0, nrow = 0;
+        if (nitem < total && tid < kTileRows) {
+            nrank = p.rank[(nkeyn >> 5) / p.E];
+            if (tid < (nkeyn & 31)) nrow = p.sorted[nrow0 + tid];
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tc::tc_fence_before();
+        __syncthreads();
+        if (warp == 0 && lane < n) {
+            asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                             p.out + (long long)rows[lane] * p.ld_out + ob),
+                         "r"(smem_u32(ys + lane * p.ys_stride)), "r"((uint32_t)(oe - ob) * 2)
+                         : "memory");
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+            asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        }
+        if (nitem < total && tid < kTileRows) {
+            if (tid < (nkeyn & 31)) s_rows[buf ^ 1][tid] = nrow;
+            if (tid == 0) {
+                s_ninfo[0] = nrow0;
+                s_ninfo[1] = nkeyn;
+                s_ninfo[2] = nrank;
+            }
+        }
+        __syncthreads();  // this item's buffers are read and the next item's words are in place
+        tc::tc_fence_after();
+        item = nitem;
+        if (item < total) {
+            row0 = s_ninfo[0];
+            keyn = s_ninfo[1];
+            r = s_ninfo[2];
+        }
+    }
+    if (dyn) finish_items(p.ticket);
+    asm volatile("griddepcontrol.launch_dependents;");
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem, kCols);
+}
+
 size_t a128(size_t x) { return (x + 127) & ~(size_t)127; }
 
 // per device: shared-memory limits raised (first calls from several host threads may race)
@@ -1030,6 +1314,8 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
                                        bgmv_expand_kernel<4, 8>, bgmv_expand_kernel<1, 4>, bgmv_expand_kernel<2, 4>,
                                        bgmv_expand_kernel<3, 4>, bgmv_expand_kernel<4, 4>};
         for (auto f : efns)
+            LORA_CUDA_TRY(cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024));
+        for (auto f : {bgmv_expand_tc_kernel<2>, bgmv_expand_tc_kernel<4>})
             LORA_CUDA_TRY(cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024));
         g_split_configured[dev].store(1, std::memory_order_release);
     }
@@ -1131,6 +1417,30 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
                   : KS == 3 ? bgmv_expand_kernel<3, 4> : bgmv_expand_kernel<4, 4>;
         LORA_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_e, expand_fn, kThreads, e_smem));
     }
+    // the tensor-core expand: every slice a whole number of 128-output
+    // blocks (a block then lies in one slice) and ranks up to 64
+    bool tc_expand = g_lora_kernel_policy != 8 && R8 <= 64 && oc_w % kTcM == 0;
+    for (int j = 0; j < ns; ++j) tc_expand = tc_expand && pr.out_w[j] % kTcM == 0 && pr.out_off[j] % kTcM == 0;
+    const int kcb = ((R8 + 15) / 16) * 2;
+    if (tc_expand) {
+        expand_fn = oc_w == 4 * kTcM ? bgmv_expand_tc_kernel<4> : bgmv_expand_tc_kernel<2>;
+        e_b = a128((size_t)(oc_w / kTcM) * kcb * kTcM * 16);
+        const size_t e_vt = a128((size_t)ns * kcb * kTileRows * 16);
+        e_smem = e_b + e_y + 2 * e_vt;
+        // The occupancy query answers 1 for any kernel that allocates tensor
+        // memory; the CTAs an SM holds are set by shared memory, registers
+        // and threads, and by the 512 tensor-memory columns (a CTA that
+        // finds them taken waits in tcgen05.alloc for one that finishes).
+        cudaFuncAttributes fa;
+        LORA_CUDA_TRY(cudaFuncGetAttributes(&fa, expand_fn));
+        int smem_sm = 0, resv = 0;
+        LORA_CUDA_TRY(cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, pool->device));
+        LORA_CUDA_TRY(cudaDeviceGetAttribute(&resv, cudaDevAttrReservedSharedMemoryPerBlock, pool->device));
+        const int by_smem = (int)(smem_sm / (e_smem + fa.sharedSizeBytes + resv));
+        const int by_regs = 65536 / (std::max(fa.numRegs, 1) * kThreads);
+        const int by_tmem = 512 / std::max(32, (oc_w / kTcM) * 16);
+        occ_e = std::min(std::min(by_smem, by_regs), std::min(by_tmem, 2048 / kThreads));
+    }
     const long long e_slots = (long long)pool->num_sms * (occ_e < 1 ? 1 : occ_e);
 
     // key-major shrink when the batch keeps most keys busy and the grid is a
@@ -1138,7 +1448,8 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     // still being built, and read once per key
     const int L = pr.n_keys;
     const size_t x_stage = a128((size_t)kTileRows * (HC + 8) * 2);
-    const int x_stages = a128((size_t)R8 * (HC + 8) * 2) + 2 * x_stage + red_bytes <= 100 * 1024 ? 2 : 1;
+    // a second x stage only when keys average more than one and a half tiles
+    const int x_stages = pr.rows > 24LL * L && a128((size_t)R8 * (HC + 8) * 2) + 2 * x_stage + red_bytes <= 100 * 1024 ? 2 : 1;
     const size_t slot_smem = a128((size_t)R8 * (HC + 8) * 2) + x_stages * x_stage + red_bytes;
     bool slot_major = pr.count_idx == 3 && pr.rows >= 4 * L && slot_smem <= 100 * 1024;
     // a key-major CTA walks its key's tiles one after another: with fewer of
@@ -1233,6 +1544,11 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     ea.off_ys = (int)e_b;
     ea.off_vh = (int)(e_b + e_y);
     ea.off_vl = (int)(e_b + e_y + e_v);
+    if (tc_expand) {
+        const size_t e_vt = a128((size_t)ns * kcb * kTileRows * 16);
+        ea.off_vl = (int)(e_b + e_y + e_vt);
+        if ((size_t)ea.off_vl + e_vt > e_smem) return LORA_ERR_INVALID_ARG;  // layout check
+    }
     ea.status = pr.status;
     ea.spin_limit = pr.spin_limit;
 

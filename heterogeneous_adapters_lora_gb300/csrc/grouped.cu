@@ -615,7 +615,7 @@ int g_lora_kernel_policy = 0;
 
 // Kernel policies (lora_set_kernel_policy) under which the fused decode
 // kernel and the split kernels may run: 0 automatic, 3 without the fused
-// kernel, 4-7 automatic apart from their own choice.
+// kernel, 4-8 automatic apart from their own choice.
 static bool pol_fused(int p) { return p == 0 || p >= 4; }
 static bool pol_split(int p) { return p == 0 || p >= 3; }
 static std::atomic<unsigned long long> g_lora_launches{0};

@@ -449,7 +449,9 @@ LORA_API lora_status_t lora_sink_experts_act(const void *gate_up, int64_t ld_gat
  *     takes the delta into its accumulator (see lora_linear_apply),
  * 7 = like 0, with the fused decode kernel for batches of up to 32 rows per
  *     slot on average (0 stops at 16, past which the split kernels measured
- *     faster).
+ *     faster),
+ * 8 = like 0, with the split expand on warp-level MMAs (mma.sync) where 0
+ *     runs it on tcgen05 (every slice width a multiple of 128, rank <= 64).
  * For tests and tuning. */
 LORA_API void lora_set_kernel_policy(int32_t policy);
 

@@ -1,7 +1,8 @@
 """Every compute path of lora_apply_slices / lora_moe_apply against the
 oracle: the automatic choice (split shrink/expand kernels for these shapes,
-tcgen05 for long runs), the persistent split-K kernel (kernel policy 1) and
-the one-pass cluster kernel (kernel policy 2)."""
+tcgen05 for long runs), the persistent split-K kernel (kernel policy 1), the
+one-pass cluster kernel (kernel policy 2), the MoE schedules (3-5) and the
+split expand on warp-level MMAs instead of tcgen05 (8)."""
 import numpy as np
 import pytest
 
@@ -17,7 +18,8 @@ from gpu_util import active_mask, assert_delta, assert_rows_untouched
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(params=[0, 1, 2, 3, 4, 5], ids=["auto", "splitk", "cluster", "split", "perpair", "tilecluster"])
+@pytest.fixture(params=[0, 1, 2, 3, 4, 5, 8],
+                ids=["auto", "splitk", "cluster", "split", "perpair", "tilecluster", "warpmma"])
 def policy(request):
     L.lora_set_kernel_policy(request.param)
     yield request.param

@@ -129,9 +129,10 @@ def apply_kernels(name, policy, fused=False):
     elif policy == 2:
         k = "cluster_lora_kernel (one pass, cluster DSMEM reduction)"
     else:
+        expand = ("bgmv_expand_kernel (warp-level MMAs)" if policy == 8 else
+                  "bgmv_expand_tc_kernel (tcgen05; bgmv_expand_kernel where a slice width is not a multiple of 128)")
         k = ("split shrink (bgmv_shrink_slot_kernel key-major, or bgmv_shrink_kernel / bgmv_shrink_tile_kernel "
-             "per tile) + "
-             "bgmv_expand_kernel, chained by programmatic dependent launch")
+             "per tile) + " + expand + ", chained by programmatic dependent launch")
     if is_sink(name):
         return k + " on w13, sink_act_kernel, the same on w2"
     if is_linear(name):

@@ -136,6 +136,11 @@ __global__ void __launch_bounds__(kFThreads, MINB) bgmv_fused_kernel(const __gri
     const int g = lane >> 2, c4 = lane & 3;
     const int c = (int)cluster_rank();
     const int a = blockIdx.x / p.CS;
+    // batch mode: the batch's slot ids into L2 before the wait (a prefetch
+    // cannot return stale data: later loads read L2, which every write
+    // reaches first), one 128-byte line per thread of each cluster's first CTA
+    if (p.idx_mode && c == 0 && tid < (p.T * 4 + 127) / 128)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(p.idx + tid * 32));
     if (a == p.L) {
         // batch mode's last cluster: its first CTA builds the metadata
         asm volatile("griddepcontrol.wait;" ::: "memory");

@@ -151,7 +151,8 @@ __global__ void __launch_bounds__(kFThreads, MINB) bgmv_fused_kernel(const __gri
     const int ns = p.n_slices;
     const int h0 = c * p.HC, hlen = max(0, min(p.H - h0, p.HC));
     const int ob0 = min(p.out_total, c * p.OB), olen = min(p.out_total - ob0, p.OB);
-    // the slot's tables: requested now, first used after the wait
+    // the slot's tables: requested now, first used by the rank-dependent
+    // copies below
     const int en = __ldcg(p.enabled + a), rk = __ldcg(p.rank + a);
     const float sc_slot = __ldcg(p.scale + a);
     if (tid == 0) {
@@ -192,6 +193,37 @@ __global__ void __launch_bounds__(kFThreads, MINB) bgmv_fused_kernel(const __gri
         }
     }
 
+    const int r = en != 0 ? rk : 0;
+    const bool act = r > 0;
+    const int rs = (r + 7) & ~7;
+    const int nbox = act ? (r + p.BR - 1) / p.BR : 0;  // A boxes per slice for this slot's rank
+    if (tid == 0) {
+        const int more = (act && hlen > 0) ? nbox - 1 : 0;
+        mbar_expect_tx(&abar, (uint32_t)(ns * more * p.box_bytes));  // the arrival that completes the phase
+        for (int j = 0; j < ns; ++j)
+            for (int b = 1; b <= more; ++b)
+                tma_load_3d(smem + (long long)(j * p.kgb + b) * p.box_bytes, &p.tm_a[j], 0, a * p.R + b * p.BR,
+                            h0 >> 6, &abar);
+    }
+    // L2 prefetch of this CTA's B rows (slot a, outputs of block c): the
+    // expand's fragments are loaded from L2 after the shrink.  The rank-
+    // dependent copies and prefetches read only the pool (rank and enabled
+    // change only through lora_set / lora_reset, complete before this grid),
+    // so they overlap the previous kernel too.
+    if (act) {
+        int nl[LORA_MAX_SLICES], tot = 0;
+        for (int j = 0; j < ns; ++j) {
+            const int s0 = max(ob0, s_oo[j]), s1 = min(ob0 + olen, s_oo[j] + (j + 1 < ns ? s_oo[j + 1] - s_oo[j] : p.out_total - s_oo[j]));
+            nl[j] = s1 > s0 ? ((s1 - s0) * rs * 2 + 127) >> 7 : 0;
+            tot += nl[j];
+        }
+        for (int i = tid; i < tot; i += kFThreads) {
+            int j = 0, l = i;
+            while (l >= nl[j]) l -= nl[j++];
+            const int s0 = max(ob0, s_oo[j]);
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(s_B[j] + (long long)(s0 - s_oo[j]) * rs + l * 64));
+        }
+    }
     // ---------------- the metadata (and everything before it) is complete
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
@@ -208,34 +240,6 @@ __global__ void __launch_bounds__(kFThreads, MINB) bgmv_fused_kernel(const __gri
         if (tid == 0) {
             s_nb[0] = __ldcg(p.key_count + a);
             s_nb[1] = __ldcg(p.key_offset + a);
-        }
-    }
-    const int r = en != 0 ? rk : 0;
-    const bool act = r > 0;
-    const int rs = (r + 7) & ~7;
-    const int nbox = act ? (r + p.BR - 1) / p.BR : 0;  // A boxes per slice for this slot's rank
-    if (tid == 0) {
-        const int more = (act && hlen > 0) ? nbox - 1 : 0;
-        mbar_expect_tx(&abar, (uint32_t)(ns * more * p.box_bytes));  // the arrival that completes the phase
-        for (int j = 0; j < ns; ++j)
-            for (int b = 1; b <= more; ++b)
-                tma_load_3d(smem + (long long)(j * p.kgb + b) * p.box_bytes, &p.tm_a[j], 0, a * p.R + b * p.BR,
-                            h0 >> 6, &abar);
-    }
-    // L2 prefetch of this CTA's B rows (slot a, outputs of block c): the
-    // expand's fragments are loaded from L2 after the shrink
-    if (act) {
-        int nl[LORA_MAX_SLICES], tot = 0;
-        for (int j = 0; j < ns; ++j) {
-            const int s0 = max(ob0, s_oo[j]), s1 = min(ob0 + olen, s_oo[j] + (j + 1 < ns ? s_oo[j + 1] - s_oo[j] : p.out_total - s_oo[j]));
-            nl[j] = s1 > s0 ? ((s1 - s0) * rs * 2 + 127) >> 7 : 0;
-            tot += nl[j];
-        }
-        for (int i = tid; i < tot; i += kFThreads) {
-            int j = 0, l = i;
-            while (l >= nl[j]) l -= nl[j++];
-            const int s0 = max(ob0, s_oo[j]);
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(s_B[j] + (long long)(s0 - s_oo[j]) * rs + l * 64));
         }
     }
     // this warp's expand groups of 32 outputs G = warp + 8 i.  Within a group

@@ -414,6 +414,39 @@ __global__ void __launch_bounds__(kFThreads, MINB) bgmv_fused_kernel(const __gri
         __syncthreads();
         if (kh == 1) store_pairs(true);
         __syncthreads();
+        // the expand's operands, requested before the cluster barrier so their
+        // latency hides behind it and the gather: B rows o0 + 4g + q (ranks
+        // ks*16 + 4c4 .. +3) of each group and the y values of rows g and g+8,
+        // outputs o0 + 8c4 .. +7
+        const bool r0ok = g < nt, r1ok = g + 8 < nt;
+        const long long yrow0 = r0ok ? (long long)s_tok[g] * p.ldy : 0, yrow1 = r1ok ? (long long)s_tok[g + 8] * p.ldy : 0;
+        uint2 bq[GMAX][4][KSX];
+        uint4 yv[GMAX][2];
+        int gj[GMAX];  // slice of each group
+#pragma unroll
+        for (int i = 0; i < GMAX; ++i) {
+            gj[i] = 0;
+            yv[i][0] = yv[i][1] = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int ks = 0; ks < KSX; ++ks) bq[i][q][ks] = make_uint2(0u, 0u);
+            if (i < ngw) {
+                const int o0 = ob0 + (warp + kFWarps * i) * 32;
+                int jj = 0;
+                for (int j = 1; j < ns; ++j)
+                    if (o0 >= s_oo[j]) jj = j;
+                gj[i] = jj;
+                const uint16_t *bb = s_B[jj] + (long long)(o0 - s_oo[jj] + 4 * g) * rs + 4 * c4;
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+#pragma unroll
+                    for (int ks = 0; ks < KSX; ++ks)
+                        if (ks * 16 + 4 * c4 < rs) bq[i][q][ks] = __ldg((const uint2 *)(bb + (long long)q * rs + ks * 16));
+                if (r0ok) yv[i][0] = __ldcg((const uint4 *)(p.y + yrow0 + o0 + 8 * c4));
+                if (r1ok) yv[i][1] = __ldcg((const uint4 *)(p.y + yrow1 + o0 + 8 * c4));
+            }
+        }
         cluster_arrive();
         cluster_wait();  // every CTA's P of this tile is complete and visible
 
@@ -465,37 +498,6 @@ __global__ void __launch_bounds__(kFThreads, MINB) bgmv_fused_kernel(const __gri
             }
         }
         cluster_arrive();  // this CTA has read its peers' P
-        // the expand's operands: B rows o0 + 4g + q (ranks ks*16 + 4c4 .. +3) of each group
-        // and the y values of rows g and g+8, outputs o0 + 8c4 .. +7
-        const bool r0ok = g < nt, r1ok = g + 8 < nt;
-        const long long yrow0 = r0ok ? (long long)s_tok[g] * p.ldy : 0, yrow1 = r1ok ? (long long)s_tok[g + 8] * p.ldy : 0;
-        uint2 bq[GMAX][4][KSX];
-        uint4 yv[GMAX][2];
-        int gj[GMAX];  // slice of each group
-#pragma unroll
-        for (int i = 0; i < GMAX; ++i) {
-            gj[i] = 0;
-            yv[i][0] = yv[i][1] = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-#pragma unroll
-                for (int ks = 0; ks < KSX; ++ks) bq[i][q][ks] = make_uint2(0u, 0u);
-            if (i < ngw) {
-                const int o0 = ob0 + (warp + kFWarps * i) * 32;
-                int jj = 0;
-                for (int j = 1; j < ns; ++j)
-                    if (o0 >= s_oo[j]) jj = j;
-                gj[i] = jj;
-                const uint16_t *bb = s_B[jj] + (long long)(o0 - s_oo[jj] + 4 * g) * rs + 4 * c4;
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-#pragma unroll
-                    for (int ks = 0; ks < KSX; ++ks)
-                        if (ks * 16 + 4 * c4 < rs) bq[i][q][ks] = __ldg((const uint2 *)(bb + (long long)q * rs + ks * 16));
-                if (r0ok) yv[i][0] = __ldcg((const uint4 *)(p.y + yrow0 + o0 + 8 * c4));
-                if (r1ok) yv[i][1] = __ldcg((const uint4 *)(p.y + yrow1 + o0 + 8 * c4));
-            }
-        }
         __syncthreads();   // v tiles written
 
         // ---------------- expand of output block c: this warp's groups

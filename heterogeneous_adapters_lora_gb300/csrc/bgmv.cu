@@ -1109,6 +1109,21 @@ __global__ void __launch_bounds__(kThreads) bgmv_expand_tc_kernel(const __grid_c
         const float w_sc = tq < n ? __ldg(p.scale + a) : 0.f;
         const float w_rw = (tq < n && p.row_w) ? __ldg(p.row_w + rows[tq]) : 1.f;
         __syncthreads();
+        const int j0 = s_mj[0], j1 = s_mj[mta - 1];
+        const int vrows = p.v_div > 0 ? p.v_rows : p.rows;
+        const long long cstride = (long long)ns * vrows * p.R8 / 4;
+        const int prow = tq < n ? (p.v_div > 0 ? rows[tq] / p.v_div : row0 + tq) : 0;
+        // after the first item: this thread's first partial sums (slice j0,
+        // ranks 4 lq ..) are requested before the B copies, so the two
+        // latencies overlap
+        float4 pre[4];
+        const bool pre_ok = waited && tq < n && lq * 4 < rs;
+        if (pre_ok) {
+            const float4 *src = (const float4 *)(p.part + ((long long)j0 * vrows + prow) * p.R8 + lq * 4);
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc)
+                if (cc < nc) pre[cc] = __ldcg(src + cc * cstride);
+        }
         // B blocks: row i of every block is thread i's, its chunks one after
         // another; chunks past the rank (up to the 16-rank step) are zero
         for (int m = 0; m < mta; ++m) {
@@ -1128,18 +1143,17 @@ __global__ void __launch_bounds__(kThreads) bgmv_expand_tc_kernel(const __grid_c
         }
         // v of every slice a block uses (chunk partials summed in order,
         // scaled) -> bf16 hi / lo in the core-matrix layout; zero past the rank
-        const int j0 = s_mj[0], j1 = s_mj[mta - 1];
         const float w_row = w_sc * p.post_scale * w_rw;
-        const int vrows = p.v_div > 0 ? p.v_rows : p.rows;
-        const long long cstride = (long long)ns * vrows * p.R8 / 4;
-        const int prow = tq < n ? (p.v_div > 0 ? rows[tq] / p.v_div : row0 + tq) : 0;
         for (int jj = j0; jj <= j1; ++jj) {
             for (int k = lq * 4; k < kcs * 8; k += 32) {
                 float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (tq < n && k < rs) {
                     const float4 *src = (const float4 *)(p.part + ((long long)jj * vrows + prow) * p.R8 + k);
-                    for (int cc = 0; cc < nc; ++cc) {
-                        const float4 v = __ldcg(src + cc * cstride);
+                    const bool use_pre = pre_ok && jj == j0 && k == lq * 4;
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {  // at most 4 hidden chunks
+                        if (cc >= nc) break;
+                        const float4 v = use_pre ? pre[cc] : __ldcg(src + cc * cstride);
                         s4.x += v.x;
                         s4.y += v.y;
                         s4.z += v.z;

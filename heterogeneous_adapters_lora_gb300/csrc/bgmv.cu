@@ -1220,10 +1220,13 @@ __global__ void __launch_bounds__(kThreads) bgmv_expand_tc_kernel(const __grid_c
             for (int t = 0; t < kTileRows; ++t) yv[t] = t < n ? yc[t * p.ys_stride] : (uint16_t)0;
             tc::tmem_wait_ld();
 #pragma unroll
-            for (int t = 0; t < kTileRows; ++t)
-                if (t < n)
-                    yc[t * p.ys_stride] = __bfloat16_as_ushort(__float2bfloat16_rn(
-                        __bfloat162float(__ushort_as_bfloat16(yv[t])) + __uint_as_float(d[t])));
+            for (int t = 0; t < kTileRows; t += 2) {  // two rows per conversion
+                const __nv_bfloat162 o2 = __floats2bfloat162_rn(
+                    __bfloat162float(__ushort_as_bfloat16(yv[t])) + __uint_as_float(d[t]),
+                    __bfloat162float(__ushort_as_bfloat16(yv[t + 1])) + __uint_as_float(d[t + 1]));
+                if (t < n) yc[t * p.ys_stride] = __bfloat16_as_ushort(o2.x);
+                if (t + 1 < n) yc[(t + 1) * p.ys_stride] = __bfloat16_as_ushort(o2.y);
+            }
         }
         // the next item's rows and rank, in flight during the stores
         int nrank = 0, nrow = 0;

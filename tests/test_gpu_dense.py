@@ -233,12 +233,16 @@ def test_cuda_graph_capture_of_meta_and_apply():
     assert_delta(bf16_bits_to_f32(y)[act], d_ref[act], "graph")
 
 
-def test_apply_after_every_slot_reset_leaves_y():
+@pytest.mark.parametrize("policy", [0, 3], ids=["fused", "split"])
+def test_apply_after_every_slot_reset_leaves_y(policy):
     # Every slot reset: the key-major shrink's CTAs all find rank 0 and leave
     # at once.  They must still let the expand start only after the metadata
     # build is complete, so the expand neither reads the previous build's
     # tile lists nor rewrites y rows the previous apply is still storing.
+    # Policy 3 keeps the batch on the split kernels (key-major shrink and the
+    # tensor-core expand); 0 takes the fused decode kernel.
     c = gen.decode_qkv()
+    L.lora_set_kernel_policy(policy)
     run = H.DenseRun(c)
     try:
         run.step()
@@ -251,6 +255,7 @@ def test_apply_after_every_slot_reset_leaves_y():
         assert run.status() == 0
     finally:
         run.close()
+        L.lora_set_kernel_policy(0)
     assert np.array_equal(y1, y2)
     _, d_ref = oracle.dense_delta(c)
     act = active_mask(c.idx, c.L, c.enabled, c.ranks)

@@ -94,6 +94,7 @@ struct EArgs {
     int *status;
     int spin_limit;
     int v_div, v_rows;       // v_div > 0: partials of row r at row sorted[r] / v_div of v_rows
+    const CUtensorMap *kmaps;  // tensor-core expand: B maps of the slices ([slice][rs/8 - 1])
 };
 
 // Dynamic work distribution: the CTAs of a one-wave grid take items from a
@@ -981,9 +982,11 @@ __global__ void __launch_bounds__(kThreads, PW == 8 ? 3 : (KS >= 3 ? 4 : 5))
 // slot's ranks (16 per instruction), accumulated in tensor memory (16 fp32
 // columns per block).  Both operands are K-major without swizzle: 8-row x
 // 16-byte core matrices, the K-adjacent ones LBO apart and the M/N-adjacent
-// ones SBO = 128 bytes apart.  B_j rows are copied in with 16-byte cp.async
-// (chunk kc of row i at kc * 2048 + i * 16 of its block), v is written by the
-// threads that sum the partials (chunk kc of row t at kc * 256 + t * 16).
+// ones SBO = 128 bytes apart.  B_j rows arrive by TMA, one box of 8 ranks x
+// 128 rows per chunk (chunk kc of row i at kc * 2048 + i * 16 of its block;
+// boxes past the slot's rank lie outside the tensor and are zero-filled), v is
+// written by the threads that sum the partials (chunk kc of row t at
+// kc * 256 + t * 16).
 // One thread issues the MMAs; each warp then reads its lane quarter of every
 // block (32 outputs x 16 rows) and adds it to the y rows staged in shared
 // memory, which are stored back with bulk copies as in bgmv_expand_kernel.
@@ -1010,9 +1013,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
         : "r"(taddr)
         : "memory");
 }
-__device__ __forceinline__ void cp_async16_cg(void *dst, const void *src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
 
 // MT: 128-output blocks per item (oc_w / 128).  Shared memory: B blocks
 // [MT][kcb][128][8], y rows [16][ys_stride], v hi and lo [n_slices][kcb][16][8]
@@ -1020,13 +1020,13 @@ __device__ __forceinline__ void cp_async16_cg(void *dst, const void *src) {
 template <int MT>
 __global__ void __launch_bounds__(kThreads) bgmv_expand_tc_kernel(const __grid_constant__ EArgs p) {
     extern __shared__ __align__(128) char smem[];
-    __shared__ __align__(8) uint64_t ybar, mbar;
+    __shared__ __align__(8) uint64_t ybar, mbar, bbar;
     __shared__ int s_rows[2][kTileRows];
     __shared__ int s_next, s_ninfo[3];
     __shared__ int s_item;
     __shared__ uint32_t s_tmem;
-    __shared__ const uint16_t *s_bp[MT];  // this item's B rows of block m (row 0 of the block)
-    __shared__ int s_mj[MT];              // ... and its slice
+    __shared__ int s_by[MT];  // this item's block m: row of its first output in its tensor map
+    __shared__ int s_mj[MT];  // ... and its slice
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int ns = p.n_slices;
     const int n_tiles = p.counters[p.count_idx];
@@ -1042,6 +1042,7 @@ __global__ void __launch_bounds__(kThreads) bgmv_expand_tc_kernel(const __grid_c
     if (tid == 0) {
         mbar_init(&ybar, 1);
         mbar_init(&mbar, 1);
+        mbar_init(&bbar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     char *bs = smem + p.off_b;
@@ -1087,20 +1088,19 @@ __global__ void __launch_bounds__(kThreads) bgmv_expand_tc_kernel(const __grid_c
             if (lane < n)
                 bulk_g2s(ys + lane * p.ys_stride, p.out + (long long)rows[lane] * p.ld_out + ob, rowb, &ybar);
         } else if (warp == 1 && lane < MT) {
-            // each block's slice and B rows (constant parameter indices)
+            // each block's slice and row in the slice's maps (constant
+            // parameter indices)
             const int o0 = ob + lane * kTcM;
-            int jm = 0;
-            const uint16_t *bp = nullptr;
+            int jm = 0, by = 0;
 #pragma unroll
             for (int jj = 0; jj < LORA_MAX_SLICES; ++jj) {
                 if (jj < ns && o0 >= p.out_off[jj] && o0 < p.out_off[jj] + p.out_w[jj]) {
                     jm = jj;
-                    bp = p.B[jj] + (long long)a * p.B_ss[jj] +
-                         (p.B_shared[jj] ? 0ll : (long long)e * p.out_w[jj] * rs) + (long long)(o0 - p.out_off[jj]) * rs;
+                    by = (p.B_shared[jj] ? 0 : e * p.out_w[jj]) + (o0 - p.out_off[jj]);
                 }
             }
             s_mj[lane] = jm;
-            s_bp[lane] = bp;
+            s_by[lane] = by;
         }
         // the v row this thread converts, and its weight factors (loads in
         // flight across the barrier and the copies; multiplied only in the
@@ -1124,19 +1124,19 @@ __global__ void __launch_bounds__(kThreads) bgmv_expand_tc_kernel(const __grid_c
             for (int cc = 0; cc < 4; ++cc)
                 if (cc < nc) pre[cc] = __ldcg(src + cc * cstride);
         }
-        // B blocks: row i of every block is thread i's, its chunks one after
-        // another; chunks past the rank (up to the 16-rank step) are zero
-        for (int m = 0; m < mta; ++m) {
-            const uint16_t *src = s_bp[m] + (long long)tid * rs;
-            char *dst = bs + m * blk_bytes + tid * 16;
-            for (int kc = 0; kc < kcs; ++kc) {
-                if (kc < kcr)
-                    cp_async16_cg(dst + kc * (kTcM * 16), src + kc * 8);
-                else
-                    *(uint4 *)(dst + kc * (kTcM * 16)) = make_uint4(0u, 0u, 0u, 0u);
+        // B blocks: a TMA box of 8 ranks x 128 rows per chunk of the rank,
+        // issued by one thread; the chunk past an odd 8-rank step (up to the
+        // 16-rank step) is zeroed by the threads, one row each
+        if (tid == 32) {
+            mbar_expect_tx(&bbar, (uint32_t)(mta * kcr) * (kTcM * 16));
+            for (int m = 0; m < mta; ++m) {
+                const CUtensorMap *bm = p.kmaps + s_mj[m] * 8 + (rs >> 3) - 1;
+                for (int kc = 0; kc < kcr; ++kc)
+                    tc::tma_load_3d(bs + m * blk_bytes + kc * (kTcM * 16), bm, kc * 8, s_by[m], a, &bbar);
             }
         }
-        asm volatile("cp.async.commit_group;" ::: "memory");
+        if (kcs > kcr)
+            for (int m = 0; m < mta; ++m) *(uint4 *)(bs + m * blk_bytes + kcr * (kTcM * 16) + tid * 16) = make_uint4(0u, 0u, 0u, 0u);
         if (!waited) {
             asm volatile("griddepcontrol.wait;" ::: "memory");  // the shrink's partials are complete
             waited = true;
@@ -1178,8 +1178,7 @@ __global__ void __launch_bounds__(kThreads) bgmv_expand_tc_kernel(const __grid_c
             }
         }
         if (tid == 0) s_next = nxt_t;
-        asm volatile("cp.async.wait_all;" ::: "memory");
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> tensor core reads
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // v (generic writes) -> tensor core reads
         tc::tc_fence_before();
         __syncthreads();
         tc::tc_fence_after();
@@ -1192,6 +1191,8 @@ __global__ void __launch_bounds__(kThreads) bgmv_expand_tc_kernel(const __grid_c
             nkeyn = p.tile_keyn[nt];
         }
         if (tid == 0) {
+            mbar_wait(&bbar, phase, p.spin_limit, p.status);  // the B boxes are in
+            tc::tc_fence_after();
             const uint32_t idesc = tc::idesc_bf16(kTcM, kTileRows);
             const uint32_t b_addr = smem_u32(bs), vh_addr = smem_u32(vh), vl_addr = smem_u32(vl);
             const int ksteps = kcs >> 1;
@@ -1436,7 +1437,7 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     }
     // the tensor-core expand: every slice a whole number of 128-output
     // blocks (a block then lies in one slice) and ranks up to 64
-    bool tc_expand = g_lora_kernel_policy != 8 && R8 <= 64 && oc_w % kTcM == 0;
+    bool tc_expand = g_lora_kernel_policy != 8 && R8 <= 64 && oc_w % kTcM == 0 && pool->d_kmaps != nullptr;
     for (int j = 0; j < ns; ++j) tc_expand = tc_expand && pr.out_w[j] % kTcM == 0 && pr.out_off[j] % kTcM == 0;
     const int kcb = ((R8 + 15) / 16) * 2;
     if (tc_expand) {
@@ -1568,6 +1569,7 @@ lora_status_t lora_split_apply(const lora_pool_t *pool, const LoraProblem &pr, v
     }
     ea.status = pr.status;
     ea.spin_limit = pr.spin_limit;
+    ea.kmaps = pool->d_kmaps ? pool->d_kmaps + (long long)pr.kmap_base * 8 : nullptr;
 
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));

@@ -956,6 +956,7 @@ extern "C" lora_status_t lora_moe_apply(const lora_pool_t *pool, const lora_meta
         bool shared_a = which == LORA_MOE_W13 && E > 1 && meta->top_k > 1;
         for (int j = 0; j < g.n_slices; ++j) shared_a = shared_a && g.A_es[j] == 0;
         pr.tok_dedup = shared_a ? 1 : 0;
+        pr.kmap_base = which == LORA_MOE_W13 ? 0 : n13;  // the pool's tensors: w13 slices, then w2
         if (pol_split(pol) && have_split_region) {
             st = lora_split_apply(pool, pr, cv.data, cv.data_bytes, cv.ctrl + 2, s, &launched);
             if (st != LORA_OK || launched) return st;

@@ -41,6 +41,11 @@ struct lora_pool {
     // compact row length rs = 8, 16, .., 64 ([slice][rs/8 - 1], device
     // memory), 3D over (rank, output row, slot); null when not built
     CUtensorMap *d_bmaps;
+    // pools of max_rank <= 64 (dense and MoE): TMA maps of every tensor's B
+    // for each compact row length ([tensor][rs/8 - 1]), 3D over (rank, row =
+    // expert * out + output, slot), boxes of 8 ranks x 128 rows without
+    // swizzle (one column of 8-row x 16-byte core matrices); null when not built
+    CUtensorMap *d_kmaps;
 };
 
 // ------------------------------------------------------------ device helpers
@@ -126,6 +131,7 @@ struct LoraProblem {
     int shrink_only;                        // split path: launch the shrink alone
     int *nc_out;                            // ... and report its hidden chunk count here
     int tok_dedup;                          // MoE with A of expert dimension 1: shrink once per token
+    int kmap_base;                          // first pool tensor of the problem's slices (d_kmaps index / 8)
 };
 
 // Cluster kernel (cluster.cu): launches and sets *launched when the shape
@@ -155,6 +161,8 @@ bool lora_make_tmap_2d(CUtensorMap *m, const void *base, long long cols, long lo
 // slots}, slot stride slot_elems elements, box {64, 128, 1}, 128-byte swizzle
 // (columns past rs read as zero).
 bool lora_make_tmap_b3d(CUtensorMap *m, const void *base, int rs, int rows, int slots, long long slot_elems);
+// The same view with boxes of 8 ranks x 128 rows and no swizzle.
+bool lora_make_tmap_bk(CUtensorMap *m, const void *base, int rs, long long rows, int slots, long long slot_elems);
 bool lora_make_tmap_a_chunks(CUtensorMap *m, const void *base, long long rows, long long cols, int box_rows,
                              int box_chunks);
 

@@ -108,6 +108,10 @@ extern "C" lora_status_t lora_pool_create(const lora_pool_desc_t *desc, void *st
     const bool maps = !p->is_moe && desc->max_rank <= 64;
     const size_t offMaps = bytes;
     if (maps) bytes = align256(bytes + (size_t)desc->n_slices * 8 * sizeof(CUtensorMap));
+    // K-chunk maps of every tensor's B for the tensor-core split expand
+    const bool kmaps = desc->max_rank <= 64;
+    const size_t offKmaps = bytes;
+    if (kmaps) bytes = align256(bytes + (size_t)p->n_tensors * 8 * sizeof(CUtensorMap));
     if (cudaMalloc(&p->d_base, bytes) != cudaSuccess) {
         free(p);
         return LORA_ERR_NOMEM;
@@ -140,6 +144,20 @@ extern "C" lora_status_t lora_pool_create(const lora_pool_desc_t *desc, void *st
         if (ok && cudaStreamSynchronize((cudaStream_t)stream) == cudaSuccess &&
             cudaMemcpy(base + offMaps, h, (size_t)ns * 8 * sizeof(CUtensorMap), cudaMemcpyHostToDevice) == cudaSuccess)
             p->d_bmaps = (CUtensorMap *)(base + offMaps);
+        free(h);
+    }
+    p->d_kmaps = nullptr;
+    if (kmaps) {
+        const int nt = p->n_tensors;
+        CUtensorMap *h = (CUtensorMap *)calloc((size_t)nt * 8, sizeof(CUtensorMap));
+        bool ok = h != nullptr;
+        for (int i = 0; ok && i < nt; ++i)
+            for (int q = 0; ok && q < 8; ++q)
+                ok = lora_make_tmap_bk(&h[i * 8 + q], p->B[i], 8 * (q + 1), (long long)p->b_experts[i] * p->b_out[i], L,
+                                       p->b_slot_elems[i]);
+        if (ok && cudaStreamSynchronize((cudaStream_t)stream) == cudaSuccess &&
+            cudaMemcpy(base + offKmaps, h, (size_t)nt * 8 * sizeof(CUtensorMap), cudaMemcpyHostToDevice) == cudaSuccess)
+            p->d_kmaps = (CUtensorMap *)(base + offKmaps);
         free(h);
     }
     *out = p;

@@ -428,6 +428,18 @@ bool lora_make_tmap_b3d(CUtensorMap *m, const void *base, int rs, int rows, int 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool lora_make_tmap_bk(CUtensorMap *m, const void *base, int rs, long long rows, int slots, long long slot_elems) {
+    PFN_cuTensorMapEncodeTiled_v12000 f = encode_fn();
+    if (!f || rs % 8 || slot_elems % 8 || rows < kOT) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)rs, (cuuint64_t)rows, (cuuint64_t)slots};
+    cuuint64_t strides[2] = {(cuuint64_t)rs * 2, (cuuint64_t)slot_elems * 2};
+    cuuint32_t box[3] = {8, (cuuint32_t)kOT, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool lora_make_tmap_a_chunks(CUtensorMap *m, const void *base, long long rows, long long cols, int box_rows,
                              int box_chunks) {
     PFN_cuTensorMapEncodeTiled_v12000 f = encode_fn();

@@ -107,6 +107,9 @@ typedef struct lora_pool lora_pool_t;   /* opaque; owns the stacked weights and 
 /* Allocate a zeroed pool on the current device (every slot reset: zero
  * weights, rank 0, disabled).  The pool owns its device memory; it keeps its
  * weights in its own layout (A rows [R][in], B compact [out][ceil8(rank)]).
+ * With max_rank <= 64 it also holds TMA tensor maps of its B tensors for the
+ * tensor-core kernels (built here, with a host synchronisation of `stream`);
+ * kernels that would use a map that could not be built take another path.
  * Errors: LORA_ERR_INVALID_ARG, LORA_ERR_SHAPE, LORA_ERR_NOMEM, LORA_ERR_CUDA. */
 LORA_API lora_status_t lora_pool_create(const lora_pool_desc_t *desc, void *stream, lora_pool_t **out);
 

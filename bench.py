@@ -586,33 +586,56 @@ def run_gpu(args, rank, world, local_rank):
         # refilled only once its previous result has been copied out.
         e_runs = [runs[0], runs[1] if len(runs) > 1 else make_run()]
 
-        def pin(a):
-            return torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
-
+        # the step's inputs (attribute paths on a run) and their host arrays;
+        # the outputs are copied back from the run's tensors
         if moe:
-            h_in = [pin(c.x.view(np.int16)), pin(c.ic2.view(np.int16)), pin(c.idx), pin(c.topk_ids),
-                    pin(c.topk_w.reshape(-1)), pin(c.ic1_0.view(np.int16)), pin(c.ic3_0.view(np.int16))]
-
-            def io(r):
-                return [r.x, r.ic2, r.idx, r.topk, r.topk_w, r.ic1, r.ic3], [r.ic1, r.ic3]
+            in_paths = ["x", "ic2", "idx", "topk", "topk_w", "ic1", "ic3"]
+            h_arrays = [c.x.view(np.int16), c.ic2.view(np.int16), c.idx, c.topk_ids, c.topk_w.reshape(-1),
+                        c.ic1_0.view(np.int16), c.ic3_0.view(np.int16)]
+            out_paths = ["ic1", "ic3"]
         elif lin:
-            h_in = [pin(c.x.view(np.int16)), pin(c.idx)]
-
-            def io(r):
-                return [r.x, r.idx], [r.y]
+            in_paths, h_arrays, out_paths = ["x", "idx"], [c.x.view(np.int16), c.idx], ["y"]
         elif sink:
-            h_in = [pin(c.w13.x.view(np.int16)), pin(c.w13.idx), pin(c.w13.y0.view(np.int16)), pin(c.gammas),
-                    pin(c.w2.y0.view(np.int16))]
-
-            def io(r):
-                return [r.r13.x, r.r13.idx, r.r13.y, r.gammas, r.r2.y], [r.r2.y]
+            in_paths = ["r13.x", "r13.idx", "r13.y", "gammas", "r2.y"]
+            h_arrays = [c.w13.x.view(np.int16), c.w13.idx, c.w13.y0.view(np.int16), c.gammas, c.w2.y0.view(np.int16)]
+            out_paths = ["r2.y"]
         else:
-            h_in = [pin(c.x.view(np.int16)), pin(c.idx), pin(c.y0.view(np.int16))]
+            in_paths, h_arrays, out_paths = ["x", "idx", "y"], [c.x.view(np.int16), c.idx, c.y0.view(np.int16)], ["y"]
 
-            def io(r):
-                return [r.x, r.idx, r.y], [r.y]
-        h_out = [[torch.empty_like(d, device="cpu").pin_memory() for d in io(r)[1]] for r in e_runs]
-        bi = sum(t.numel() * t.element_size() for t in h_in)
+        def attr(r, path):
+            o = r
+            for k in path.split(".")[:-1]:
+                o = getattr(o, k)
+            return o, path.split(".")[-1]
+
+        # Inputs staged as a serving loop would: one pinned host buffer and,
+        # per buffer set, one device buffer of the same layout whose pieces are
+        # the run's input tensors (views), so a step copies its inputs in with
+        # a single copy (each copy costs a few microseconds of its own).
+        offs, size = [], 0
+        for a in h_arrays:
+            offs.append(size)
+            size = (size + np.ascontiguousarray(a).nbytes + 255) // 256 * 256
+        h_pack = torch.empty(size, dtype=torch.uint8).pin_memory()
+        for a, o in zip(h_arrays, offs):
+            b = np.ascontiguousarray(a).view(np.uint8).reshape(-1)
+            h_pack[o:o + b.size].copy_(torch.from_numpy(b))
+        d_packs = []
+        for r in e_runs:
+            buf = torch.empty(size, dtype=torch.uint8, device=dev)
+            for pth, o in zip(in_paths, offs):
+                obj, k = attr(r, pth)
+                t = getattr(obj, k)
+                v = buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+                v.copy_(t)
+                setattr(obj, k, v)
+            d_packs.append(buf)
+
+        def io(r):
+            return [getattr(*attr(r, pth)) for pth in out_paths]
+
+        h_out = [[torch.empty_like(d, device="cpu").pin_memory() for d in io(r)] for r in e_runs]
+        bi = size
         bo = sum(t.numel() * t.element_size() for t in h_out[0])
         s_in = torch.cuda.Stream(device=dev)
         s_out = torch.cuda.Stream(device=dev)
@@ -629,12 +652,11 @@ def run_gpu(args, rank, world, local_rank):
             for i in range(n):
                 b = i % 2
                 r = e_runs[b]
-                d_in, d_out = io(r)
+                d_out = io(r)
                 if i >= 2:
                     s_in.wait_event(ev_out[i - 2])  # set b's last result is out, its calls done
                 with torch.cuda.stream(s_in):
-                    for h, d in zip(h_in, d_in):
-                        d.copy_(h, non_blocking=True)
+                    d_packs[b].copy_(h_pack, non_blocking=True)
                     ev_in[i].record(s_in)
                 stream.wait_event(ev_in[i])
                 with torch.cuda.stream(stream):

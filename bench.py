@@ -580,11 +580,12 @@ def run_gpu(args, rank, world, local_rank):
         # end to end through the public API with host buffers: every step copies
         # its inputs in from pinned host memory, makes the calls and copies its
         # result out.  As a serving loop does, consecutive steps are pipelined
-        # over two sets of device buffers: step i's copies in (one copy
-        # stream), step i-1's calls (the compute stream) and step i-2's copy
-        # out (a second copy stream) run at the same time; a buffer set is
-        # refilled only once its previous result has been copied out.
-        e_runs = [runs[0], runs[1] if len(runs) > 1 else make_run()]
+        # over three sets of device buffers: step i's copy in (one copy
+        # stream), earlier steps' calls (the compute stream) and copies out (a
+        # second copy stream) run at the same time; a buffer set is refilled
+        # only once its previous result has been copied out.
+        NSET = 3  # buffer sets: a step's copy in waits for the copy out of the step NSET back
+        e_runs = [runs[q] if len(runs) > q else make_run() for q in range(NSET)]
 
         # the step's inputs (attribute paths on a run) and their host arrays;
         # the outputs are copied back from the run's tensors
@@ -650,11 +651,11 @@ def run_gpu(args, rank, world, local_rank):
             s_in.wait_event(start)
             s_out.wait_event(start)
             for i in range(n):
-                b = i % 2
+                b = i % NSET
                 r = e_runs[b]
                 d_out = io(r)
-                if i >= 2:
-                    s_in.wait_event(ev_out[i - 2])  # set b's last result is out, its calls done
+                if i >= NSET:
+                    s_in.wait_event(ev_out[i - NSET])  # set b's last result is out, its calls done
                 with torch.cuda.stream(s_in):
                     d_packs[b].copy_(h_pack, non_blocking=True)
                     ev_in[i].record(s_in)
@@ -769,7 +770,7 @@ def run_gpu(args, rank, world, local_rank):
         "clocks": cs.summary(),
         "e2e": {"value": e2e, "unit": "tokens/s", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
                 "steps": e2e_n,
-                "timing": (f"CUDA graphs of {G} steps pipelined over two buffer sets: pinned H2D copies "
+                "timing": (f"CUDA graphs of {G} steps pipelined over {NSET} buffer sets: pinned H2D copies "
                            "(copy stream), metadata + apply (compute stream), D2H copy (second copy stream)")
                           if e2e_graph is not None else "eager pipelined calls"},
         "gpu_launches": m["launches_per_step"] * args.steps,

@@ -1078,6 +1078,22 @@ __global__ void __launch_bounds__(kThreads) bgmv_expand_tc_kernel(const __grid_c
         const int *rows = s_rows[buf];
         int nxt_t = total;
         if (dyn && tid == 0) nxt_t = atomicAdd(p.ticket, 1);  // lands while this item runs
+        // after the first item: this thread's first partial sums (the slice
+        // of the item's first output, ranks 4 lq ..) are requested first, so
+        // their latency overlaps the item's set-up, copies and barrier
+        const int tq = tid >> 3, lq = tid & 7;
+        const int j0 = slice_of(p, ob);
+        const int vrows = p.v_div > 0 ? p.v_rows : p.rows;
+        const long long cstride = (long long)ns * vrows * p.R8 / 4;
+        const int prow = tq < n ? (p.v_div > 0 ? rows[tq] / p.v_div : row0 + tq) : 0;
+        float4 pre[4];
+        const bool pre_ok = waited && tq < n && lq * 4 < rs;
+        if (pre_ok) {
+            const float4 *src = (const float4 *)(p.part + ((long long)j0 * vrows + prow) * p.R8 + lq * 4);
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc)
+                if (cc < nc) pre[cc] = __ldcg(src + cc * cstride);
+        }
         // y rows: bulk copies (they do not depend on the shrink).  The y
         // tile's last generic writes were ordered before the async proxy by
         // the fence ahead of the previous item's stores.
@@ -1102,28 +1118,13 @@ __global__ void __launch_bounds__(kThreads) bgmv_expand_tc_kernel(const __grid_c
             s_mj[lane] = jm;
             s_by[lane] = by;
         }
-        // the v row this thread converts, and its weight factors (loads in
+        // the weight factors of the v row this thread converts (loads in
         // flight across the barrier and the copies; multiplied only in the
         // sum below)
-        const int tq = tid >> 3, lq = tid & 7;
         const float w_sc = tq < n ? __ldg(p.scale + a) : 0.f;
         const float w_rw = (tq < n && p.row_w) ? __ldg(p.row_w + rows[tq]) : 1.f;
         __syncthreads();
-        const int j0 = s_mj[0], j1 = s_mj[mta - 1];
-        const int vrows = p.v_div > 0 ? p.v_rows : p.rows;
-        const long long cstride = (long long)ns * vrows * p.R8 / 4;
-        const int prow = tq < n ? (p.v_div > 0 ? rows[tq] / p.v_div : row0 + tq) : 0;
-        // after the first item: this thread's first partial sums (slice j0,
-        // ranks 4 lq ..) are requested before the B copies, so the two
-        // latencies overlap
-        float4 pre[4];
-        const bool pre_ok = waited && tq < n && lq * 4 < rs;
-        if (pre_ok) {
-            const float4 *src = (const float4 *)(p.part + ((long long)j0 * vrows + prow) * p.R8 + lq * 4);
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc)
-                if (cc < nc) pre[cc] = __ldcg(src + cc * cstride);
-        }
+        const int j1 = s_mj[mta - 1];  // j0 = s_mj[0]
         // B blocks: a TMA box of 8 ranks x 128 rows per chunk of the rank,
         // issued by one thread; the chunk past an odd 8-rank step (up to the
         // 16-rank step) is zeroed by the threads, one row each
